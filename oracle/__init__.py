@@ -1,0 +1,162 @@
+"""Float64 CPU oracle (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package.  It wraps ``mtp_oracle.c`` (plain C,
+double precision, OpenMP over rows) through ctypes and shares nothing with the
+CUDA library.  See ``mtp_oracle.c`` for the definitions it follows and the
+pages' sections they come from.
+
+Every function takes host arrays: logits as float32, float64 or uint16
+bfloat16 bit patterns (widened exactly), and returns NumPy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mtp_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM = 1, 2, 4, 8, 16
+ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (-O2 -fopenmp) if missing or stale."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            lib.oracle_softmax.argtypes = [P, I, I, I, D, P]
+            lib.oracle_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]
+            lib.oracle_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
+            lib.oracle_tv_loss.argtypes = [P, P, I, D, I, I, I, D, I, P, P, P, P, P, P]
+            lib.oracle_num_threads.argtypes = []
+            for f in (lib.oracle_softmax, lib.oracle_verify, lib.oracle_row_stats, lib.oracle_tv_loss,
+                      lib.oracle_num_threads):
+                f.restype = I
+            _lib = lib
+    return _lib
+
+
+def _logits(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return a, 0
+    if a.dtype == np.uint16:
+        return a, 1
+    if a.dtype == np.float64:
+        return a, 2
+    raise TypeError(f"unsupported logit storage {a.dtype}")
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def num_threads() -> int:
+    """Threads the oracle's parallel loops use (OMP_NUM_THREADS respected)."""
+    return _load().oracle_num_threads()
+
+
+def softmax(z, T: float = 1.0) -> np.ndarray:
+    """p = softmax(z / T) along the last axis, float64."""
+    z, dt = _logits(z)
+    V = z.shape[-1]
+    rows = z.size // V
+    p = np.empty(z.shape, dtype=np.float64)
+    _load().oracle_softmax(_ptr(z), dt, rows, V, float(T), _ptr(p))
+    return p
+
+
+def verify(target, draft, draft_ids, temperature, uniforms, want_stats: bool = False) -> dict:
+    """Batched RS verification.  target [B, gamma+1, V], draft [B, gamma, V].
+
+    Returns dict with tokens [B, gamma+1] int32 (-1 padded), accept_len [B],
+    flags [B], acc_margin [B, gamma], cdf_margin [B], and with want_stats
+    alpha, tv [B, gamma], entropy [B, gamma+1].
+    """
+    t, dt = _logits(target)
+    d, dt2 = _logits(draft)
+    assert dt == dt2
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    assert d.shape == (B, gamma, V)
+    ids = np.ascontiguousarray(draft_ids, dtype=np.int32).reshape(B, gamma)
+    temp = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, gamma + 1)
+    out = {
+        "tokens": np.empty((B, gamma + 1), np.int32),
+        "accept_len": np.empty(B, np.int32),
+        "flags": np.empty(B, np.int32),
+        "acc_margin": np.empty((B, gamma), np.float64),
+        "cdf_margin": np.empty(B, np.float64),
+    }
+    if want_stats:
+        out["alpha"] = np.empty((B, gamma), np.float64)
+        out["tv"] = np.empty((B, gamma), np.float64)
+        out["entropy"] = np.empty((B, gamma + 1), np.float64)
+    rc = _load().oracle_verify(
+        _ptr(t), _ptr(d), dt, _ptr(ids), _ptr(temp), _ptr(u), B, gamma, V, int(want_stats),
+        _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out.get("alpha")), _ptr(out.get("tv")),
+        _ptr(out.get("entropy")), _ptr(out["flags"]), _ptr(out["acc_margin"]), _ptr(out["cdf_margin"]))
+    if rc:
+        raise RuntimeError(f"oracle_verify failed ({rc})")
+    return out
+
+
+def row_stats(target, draft, temperature) -> dict:
+    """alpha, tv [B, gamma] and entropy [B, gamma+1], flags [B]."""
+    t, dt = _logits(target)
+    d, _ = _logits(draft)
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    temp = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    out = {"alpha": np.empty((B, gamma)), "tv": np.empty((B, gamma)), "entropy": np.empty((B, g1)),
+           "flags": np.empty(B, np.int32)}
+    rc = _load().oracle_row_stats(_ptr(t), _ptr(d), dt, _ptr(temp), B, gamma, V, _ptr(out["alpha"]),
+                                  _ptr(out["tv"]), _ptr(out["entropy"]), _ptr(out["flags"]))
+    if rc:
+        raise RuntimeError(f"oracle_row_stats failed ({rc})")
+    return out
+
+
+def tv_loss(target, draft, temperature: float = 1.0, grad_scale: float = 1.0, with_grad: bool = True,
+            tie_le: bool = True) -> dict:
+    """End-to-end TV loss forward/backward over [N, gamma, V] inputs.
+
+    Returns loss [N], alpha, S, g [N, gamma], flags [N] and (with_grad)
+    grad [N, gamma, V] float64.
+    """
+    t, dt = _logits(target)
+    d, _ = _logits(draft)
+    N, gamma, V = t.shape
+    out = {"loss": np.empty(N), "alpha": np.empty((N, gamma)), "S": np.empty((N, gamma)),
+           "g": np.empty((N, gamma)), "flags": np.empty(N, np.int32)}
+    if with_grad:
+        out["grad"] = np.empty((N, gamma, V))
+    rc = _load().oracle_tv_loss(_ptr(t), _ptr(d), dt, float(temperature), N, gamma, V, float(grad_scale),
+                                int(tie_le), _ptr(out["loss"]), _ptr(out["alpha"]), _ptr(out["S"]),
+                                _ptr(out["g"]), _ptr(out.get("grad")), _ptr(out["flags"]))
+    if rc:
+        raise RuntimeError(f"oracle_tv_loss failed ({rc})")
+    return out

@@ -1,0 +1,454 @@
+/*
+ * mtp_oracle.c -- plain float64 CPU oracle for MTP rejection-sampling
+ * verification, per-position row statistics and the end-to-end TV loss.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links or calls this
+ * file: only the test suite, the package smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; it is written from the method's definitions, one row at a
+ * time, with no blocking, fusion or reordering beyond what they state.
+ *
+ * Sources (cited by page title and section):
+ *   [BB]  "Breaking Entropy Bounds: Accelerating RL Training via MTP with
+ *         Rejection Sampling" (paperlayer.ai summary of arXiv 2606.12370).
+ *   [BBz] The same paper, Chinese summary (paper.rainbus.top), sections
+ *         "前置知识" (background) and "核心方法" / "技术新颖性" (method).
+ *   [EM]  "EntMTP: Accelerating LLM Inference with Entropy Guided Multi Token
+ *         Prediction", Related Work, "Speculative Decoding".
+ *
+ * Readings of points the pages leave open (each one is listed with its reason
+ * in the design notes of the repository):
+ *   - One temperature T per sequence scales both target and draft logits.
+ *   - Accept test is the strict comparison u*q(y) < p(y), u in [0,1).
+ *   - u[b, 0..gamma-1] are the accept tests; u[b, gamma] is the single final
+ *     draw (residual or bonus).  Uniforms after the stop are not used.
+ *   - The bonus token after gamma accepts is the residual draw with q = 0,
+ *     i.e. a draw from p_gamma.
+ *   - Inverse CDF: ascending vocabulary index, smallest v with C(v) > u*R; if
+ *     rounding leaves no such v, the last v with r_v > 0.  R == 0 at a
+ *     rejection (only reachable through rounding) draws from p_j and sets the
+ *     ZERO_MASS flag.
+ *   - TV-gradient indicator 1[q <= p] as the pages write it (tie_le = 1);
+ *     tie_le = 0 selects the strict 1[q < p].
+ *   - e2e loss l = -sum_{k=1..gamma} prod_{i<=k} alpha_i, unnormalised.
+ *
+ * Logit storage codes: 0 = float32, 1 = bfloat16 (uint16 bit patterns),
+ * 2 = float64.  Every element is widened exactly to double before use.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_F32 0
+#define OR_BF16 1
+#define OR_F64 2
+
+/* Row flag bits (same meanings as the library's documented flags). */
+#define OR_ROW_NONFINITE 1
+#define OR_ROW_BAD_ID 2
+#define OR_ROW_BAD_TEMP 4
+#define OR_ROW_ZERO_MASS 8
+#define OR_ROW_BAD_UNIFORM 16
+#define OR_ERROR_BITS (OR_ROW_NONFINITE | OR_ROW_BAD_ID | OR_ROW_BAD_TEMP | OR_ROW_BAD_UNIFORM)
+
+/* Exact widening of one stored logit to double. */
+static double load_logit(const void *base, int dtype, size_t idx)
+{
+    if (dtype == OR_F64) return ((const double *)base)[idx];
+    if (dtype == OR_F32) return (double)((const float *)base)[idx];
+    uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * p = softmax(z / T) over one row of V logits starting at element `off`.
+ * Temperature-scaled softmax [BB, §7 "Temperature and generation position";
+ * App. G.2 caches temperature-scaled logits].  Max subtraction only guards
+ * exp() against overflow.  Returns 0 on success, OR_ROW_NONFINITE if a logit
+ * is NaN or +inf or every logit is -inf (no probability can be formed).
+ */
+static int softmax_row(const void *z, int dtype, size_t off, int V, double T, double *p)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double x = load_logit(z, dtype, off + (size_t)v);
+        if (isnan(x) || (isinf(x) && x > 0)) return OR_ROW_NONFINITE;
+        x = x / T;
+        p[v] = x;
+        if (x > m) m = x;
+    }
+    if (isinf(m)) return OR_ROW_NONFINITE; /* all -inf */
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) {
+        p[v] = exp(p[v] - m);
+        s += p[v];
+    }
+    for (int v = 0; v < V; ++v) p[v] /= s;
+    return 0;
+}
+
+/* Exported for tests: softmax of `rows` rows of length V at temperature T. */
+int oracle_softmax(const void *z, int dtype, int rows, int V, double T, double *p)
+{
+    int bad = 0;
+    for (int r = 0; r < rows; ++r)
+        bad |= softmax_row(z, dtype, (size_t)r * V, V, T, p + (size_t)r * V);
+    return bad;
+}
+
+/* alpha = sum_v min(p_v, q_v): the RS acceptance probability, equal to the
+ * TV overlap [BB, §3 "Rejection Sampling"; §8 "Total Variation Distance"]. */
+static double overlap(const double *p, const double *q, int V)
+{
+    double a = 0.0;
+    for (int v = 0; v < V; ++v) a += (p[v] < q[v]) ? p[v] : q[v];
+    return a;
+}
+
+/* d_TV(p, q) = 1/2 sum_v |p_v - q_v| [BBz, 前置知识 "Total Variation Distance"].
+ * Computed independently of overlap() so tests can check alpha = 1 - TV. */
+static double tv_distance(const double *p, const double *q, int V)
+{
+    double d = 0.0;
+    for (int v = 0; v < V; ++v) d += fabs(p[v] - q[v]);
+    return 0.5 * d;
+}
+
+/* H(p) = -sum_v p_v log p_v, in nats, terms with p_v = 0 omitted
+ * [BBz, 前置知识 "Entropy"]. */
+static double entropy(const double *p, int V)
+{
+    double h = 0.0;
+    for (int v = 0; v < V; ++v)
+        if (p[v] > 0.0) h -= p[v] * log(p[v]);
+    return h;
+}
+
+/*
+ * Inverse-CDF draw from the unnormalised weights r[0..V-1] with uniform u:
+ * C(v) = sum_{w<=v} r_w, R = C(V-1); returns the smallest v with C(v) > u*R,
+ * or the last v with r_v > 0 if rounding leaves none.  This is the residual
+ * resampling step [EM, "Speculative Decoding": draw from
+ * norm(max(0, p - q))] done as a two-pass CDF inversion [BB, App. G.1]:
+ * pass one sums R, pass two walks the CDF.  *margin receives
+ * min(u*R - C(v-1), C(v) - u*R) / R, the distance of the draw from the
+ * nearest CDF breakpoint (0 when R == 0).
+ */
+static int cdf_draw(const double *r, int V, double u, double *margin)
+{
+    double R = 0.0;
+    for (int v = 0; v < V; ++v) R += r[v];
+    double t = u * R;
+    double c = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double prev = c;
+        c += r[v];
+        if (c > t) {
+            double a = t - prev, b = c - t;
+            *margin = (R > 0.0) ? ((a < b) ? a : b) / R : 0.0;
+            return v;
+        }
+    }
+    int last = -1;
+    for (int v = 0; v < V; ++v)
+        if (r[v] > 0.0) last = v;
+    *margin = 0.0;
+    return last;
+}
+
+/*
+ * One sequence of the verify step.  target: gamma+1 rows, draft: gamma rows,
+ * row-major [., V] starting at the given element offsets.
+ *
+ * Steps [BB, §2 "Acceptance methods"; App. G.1; EM, "Speculative Decoding"]:
+ * for i = 0..gamma-1 compute p_i = softmax(target_i / T), q_i =
+ * softmax(draft_i / T) and accept draft y_i iff u_i * q_i(y_i) < p_i(y_i),
+ * i.e. with probability min(1, p_i(y_i)/q_i(y_i)); stop at the first
+ * rejection j and draw the replacement from norm(max(0, p_j - q_j)).  If all
+ * gamma drafts are accepted, draw the bonus token from p_gamma.
+ *
+ * With want_stats, alpha_i, TV_i (i < gamma) and H_i (i <= gamma) are formed
+ * for every position, including positions after the stop.
+ */
+static void verify_one(const void *target, const void *draft, int dtype, size_t toff, size_t doff,
+                       const int32_t *ids, double T, const double *u, int gamma, int V, int want_stats,
+                       int32_t *tokens, int32_t *accept_len, double *alpha, double *tv, double *ent,
+                       int32_t *flags, double *acc_margin, double *cdf_margin, double *p, double *q,
+                       double *r)
+{
+    int f = 0;
+    for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
+    for (int i = 0; i < gamma; ++i) acc_margin[i] = NAN;
+    *cdf_margin = NAN;
+    if (want_stats) {
+        for (int i = 0; i < gamma; ++i) alpha[i] = tv[i] = NAN;
+        for (int i = 0; i <= gamma; ++i) ent[i] = NAN;
+    }
+    if (!(T > 0.0) || isinf(T)) f |= OR_ROW_BAD_TEMP;
+    for (int i = 0; i < gamma; ++i)
+        if (ids[i] < 0 || ids[i] >= V) f |= OR_ROW_BAD_ID;
+    for (int i = 0; i <= gamma; ++i)
+        if (!(u[i] >= 0.0 && u[i] < 1.0)) f |= OR_ROW_BAD_UNIFORM;
+    if (f) {
+        *accept_len = -1;
+        *flags = f;
+        return;
+    }
+
+    /* Stats pass: every position, independent of the decisions. */
+    if (want_stats) {
+        for (int i = 0; i <= gamma; ++i) {
+            f |= softmax_row(target, dtype, toff + (size_t)i * V, V, T, p);
+            if (f) break;
+            ent[i] = entropy(p, V);
+            if (i < gamma) {
+                f |= softmax_row(draft, dtype, doff + (size_t)i * V, V, T, q);
+                if (f) break;
+                alpha[i] = overlap(p, q, V);
+                tv[i] = tv_distance(p, q, V);
+            }
+        }
+        if (f) {
+            for (int i = 0; i < gamma; ++i) alpha[i] = tv[i] = NAN;
+            for (int i = 0; i <= gamma; ++i) ent[i] = NAN;
+            *accept_len = -1;
+            *flags = f;
+            return;
+        }
+    }
+
+    /* Accept chain: left to right, stop at the first rejection. */
+    int n = 0, rejected = 0;
+    for (int i = 0; i < gamma; ++i) {
+        f |= softmax_row(target, dtype, toff + (size_t)i * V, V, T, p);
+        f |= softmax_row(draft, dtype, doff + (size_t)i * V, V, T, q);
+        if (f) break;
+        double py = p[ids[i]], qy = q[ids[i]];
+        double ratio = (qy > 0.0) ? py / qy : (py > 0.0 ? INFINITY : NAN);
+        acc_margin[i] = isnan(ratio) ? 0.0 : fabs(u[i] - ratio);
+        if (u[i] * qy < py) {
+            tokens[i] = ids[i];
+            ++n;
+            continue;
+        }
+        rejected = 1;
+        break;
+    }
+    if (f) {
+        for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
+        *accept_len = -1;
+        *flags = f;
+        return;
+    }
+
+    /* Final draw: residual at the rejection, or bonus from p_gamma. */
+    if (rejected) {
+        double R = 0.0;
+        for (int v = 0; v < V; ++v) {
+            double d = p[v] - q[v];
+            r[v] = d > 0.0 ? d : 0.0;
+            R += r[v];
+        }
+        if (!(R > 0.0)) {
+            f |= OR_ROW_ZERO_MASS;
+            memcpy(r, p, sizeof(double) * (size_t)V);
+        }
+    } else {
+        f |= softmax_row(target, dtype, toff + (size_t)gamma * V, V, T, p);
+        if (f) {
+            for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
+            *accept_len = -1;
+            *flags = f;
+            return;
+        }
+        memcpy(r, p, sizeof(double) * (size_t)V);
+    }
+    tokens[n] = cdf_draw(r, V, u[gamma], cdf_margin);
+    *accept_len = n;
+    *flags = f;
+}
+
+/*
+ * Batched verify over B sequences (OpenMP over sequences).
+ *   target  [B, gamma+1, V], draft [B, gamma, V] in storage `dtype`
+ *   ids     [B, gamma] int32, temp [B] (double), u [B, gamma+1] (double)
+ * Outputs: tokens [B, gamma+1] (-1 padded), accept_len [B] (-1 if flagged),
+ *   flags [B]; with want_stats alpha, tv [B, gamma] and ent [B, gamma+1]
+ *   (may be NULL otherwise); acc_margin [B, gamma] = |u_i - p_i(y)/q_i(y)|
+ *   for every decision taken (NaN where none), cdf_margin [B].
+ */
+int oracle_verify(const void *target, const void *draft, int dtype, const int32_t *ids, const double *temp,
+                  const double *u, int B, int gamma, int V, int want_stats, int32_t *tokens,
+                  int32_t *accept_len, double *alpha, double *tv, double *ent, int32_t *flags,
+                  double *acc_margin, double *cdf_margin)
+{
+    if (B < 0 || gamma < 1 || V < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)V * 3);
+        if (!buf) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        verify_one(target, draft, dtype, (size_t)b * (gamma + 1) * V, (size_t)b * gamma * V, ids + (size_t)b * gamma,
+                   temp[b], u + (size_t)b * (gamma + 1), gamma, V, want_stats, tokens + (size_t)b * (gamma + 1),
+                   accept_len + b, want_stats ? alpha + (size_t)b * gamma : NULL,
+                   want_stats ? tv + (size_t)b * gamma : NULL, want_stats ? ent + (size_t)b * (gamma + 1) : NULL,
+                   flags + b, acc_margin + (size_t)b * gamma, cdf_margin + b, buf, buf + V, buf + 2 * (size_t)V);
+        free(buf);
+    }
+    return fail ? 2 : 0;
+}
+
+/*
+ * Per-position row statistics (no decisions): alpha_i = sum min(p_i, q_i) and
+ * TV_i for i < gamma, H(p_i) for i <= gamma [BB, §3 "Rejection Sampling";
+ * BBz, 前置知识 "Entropy"].  Flagged sequences get NaN statistics.
+ */
+int oracle_row_stats(const void *target, const void *draft, int dtype, const double *temp, int B, int gamma,
+                     int V, double *alpha, double *tv, double *ent, int32_t *flags)
+{
+    if (B < 0 || gamma < 1 || V < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V * 2);
+        if (!p) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        double *q = p + V;
+        double T = temp[b];
+        int f = (!(T > 0.0) || isinf(T)) ? OR_ROW_BAD_TEMP : 0;
+        size_t toff = (size_t)b * (gamma + 1) * V, doff = (size_t)b * gamma * V;
+        for (int i = 0; i <= gamma && !f; ++i) {
+            f |= softmax_row(target, dtype, toff + (size_t)i * V, V, T, p);
+            if (f) break;
+            ent[(size_t)b * (gamma + 1) + i] = entropy(p, V);
+            if (i < gamma) {
+                f |= softmax_row(draft, dtype, doff + (size_t)i * V, V, T, q);
+                if (f) break;
+                alpha[(size_t)b * gamma + i] = overlap(p, q, V);
+                tv[(size_t)b * gamma + i] = tv_distance(p, q, V);
+            }
+        }
+        if (f) {
+            for (int i = 0; i < gamma; ++i) alpha[(size_t)b * gamma + i] = tv[(size_t)b * gamma + i] = NAN;
+            for (int i = 0; i <= gamma; ++i) ent[(size_t)b * (gamma + 1) + i] = NAN;
+        }
+        flags[b] = f;
+        free(p);
+    }
+    return fail ? 2 : 0;
+}
+
+/*
+ * End-to-end TV loss forward and backward for N token positions, gamma draft
+ * steps each.  target, draft: [N, gamma, V]; p is detached [BB, App. A].
+ *
+ *   alpha_k = sum_v min(p_kv, q_kv)                 [BB, §8]
+ *   S_k     = sum_v 1[q_kv <= p_kv] q_kv            [BB, App. A]
+ *   l_t     = -sum_{m=1..gamma} prod_{i<=m} alpha_i [BB, §4 "End-to-end TV
+ *             loss": expected acceptance length, multiplicative over steps]
+ *   g_k     = dl_t/dalpha_k = -sum_{m>=k} prod_{i<=m, i!=k} alpha_i
+ *   dalpha_k/dz_j = (1/T) q_kj (1[q_kj <= p_kj] - S_k)   [BB, App. A; the
+ *             1/T is the chain rule through q = softmax(z/T)]
+ *   grad[t,k,j] = grad_scale * g_k * dalpha_k/dz_j.
+ *
+ * Outputs: loss [N], alpha [N, gamma], S [N, gamma], g [N, gamma], flags [N],
+ * and grad [N, gamma, V] unless grad is NULL.  Flagged positions get NaN.
+ */
+int oracle_tv_loss(const void *target, const void *draft, int dtype, double T, int N, int gamma, int V,
+                   double grad_scale, int tie_le, double *loss, double *alpha, double *S, double *g,
+                   double *grad, int32_t *flags)
+{
+    if (N < 0 || gamma < 1 || V < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < N; ++t) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V * 2);
+        if (!p) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        double *q = p + V;
+        int f = (!(T > 0.0) || isinf(T)) ? OR_ROW_BAD_TEMP : 0;
+        double *a = alpha + (size_t)t * gamma, *s = S + (size_t)t * gamma, *gk = g + (size_t)t * gamma;
+        for (int k = 0; k < gamma && !f; ++k) {
+            size_t off = ((size_t)t * gamma + k) * V;
+            f |= softmax_row(target, dtype, off, V, T, p);
+            f |= softmax_row(draft, dtype, off, V, T, q);
+            if (f) break;
+            a[k] = overlap(p, q, V);
+            double sk = 0.0;
+            for (int v = 0; v < V; ++v)
+                if (tie_le ? (q[v] <= p[v]) : (q[v] < p[v])) sk += q[v];
+            s[k] = sk;
+        }
+        flags[t] = f;
+        if (f) {
+            loss[t] = NAN;
+            for (int k = 0; k < gamma; ++k) a[k] = s[k] = gk[k] = NAN;
+            if (grad)
+                for (size_t e = 0; e < (size_t)gamma * V; ++e) grad[(size_t)t * gamma * V + e] = NAN;
+            free(p);
+            continue;
+        }
+        /* Loss: sum over the gamma prefix products. */
+        double l = 0.0;
+        for (int m = 0; m < gamma; ++m) {
+            double prod = 1.0;
+            for (int i = 0; i <= m; ++i) prod *= a[i];
+            l -= prod;
+        }
+        loss[t] = l;
+        /* dl/dalpha_k: each product containing alpha_k, with alpha_k removed. */
+        for (int k = 0; k < gamma; ++k) {
+            double d = 0.0;
+            for (int m = k; m < gamma; ++m) {
+                double prod = 1.0;
+                for (int i = 0; i <= m; ++i)
+                    if (i != k) prod *= a[i];
+                d -= prod;
+            }
+            gk[k] = d;
+        }
+        if (grad) {
+            for (int k = 0; k < gamma; ++k) {
+                size_t off = ((size_t)t * gamma + k) * V;
+                softmax_row(target, dtype, off, V, T, p);
+                softmax_row(draft, dtype, off, V, T, q);
+                for (int v = 0; v < V; ++v) {
+                    double ind = (tie_le ? (q[v] <= p[v]) : (q[v] < p[v])) ? 1.0 : 0.0;
+                    grad[off + v] = grad_scale * gk[k] * (1.0 / T) * q[v] * (ind - s[k]);
+                }
+            }
+        }
+        free(p);
+    }
+    return fail ? 2 : 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+    int n = 1;
+#ifdef _OPENMP
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+#endif
+    return n;
+}

@@ -1,0 +1,391 @@
+"""Pins of the float64 oracle against what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: each test checks it against a
+library routine, a closed form, an invariant the pages state, a hand-derived
+fixture, or an exact enumeration of the sampling law.  Page references:
+"Breaking Entropy Bounds: Accelerating RL Training via MTP with Rejection
+Sampling" (summary pages) and "EntMTP", Related Work "Speculative Decoding".
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split("=")
+            vals[k.strip()] = [float(x) for x in v.split()]
+    return vals
+
+
+def _rows(rng, n, V, scale=1.5):
+    return (rng.standard_normal((n, V)) * scale).astype(np.float64)
+
+
+# ---------------------------------------------------------------- softmax --
+
+@pytest.mark.parametrize("T", [0.6, 1.0, 1.7])
+def test_softmax_matches_scipy(T):
+    rng = np.random.default_rng(1)
+    z = _rows(rng, 5, 1000, 3.0)
+    ref = scipy.special.softmax(z / T, axis=-1)
+    np.testing.assert_allclose(oracle.softmax(z, T), ref, rtol=1e-12, atol=1e-300)
+    # log-probabilities against the library's log-sum-exp
+    lse = scipy.special.logsumexp(z / T, axis=-1, keepdims=True)
+    np.testing.assert_allclose(np.log(oracle.softmax(z, T)), z / T - lse, rtol=0, atol=1e-10)
+
+
+def test_bf16_widening_is_exact():
+    import torch
+
+    x = np.random.default_rng(2).standard_normal((2, 64)).astype(np.float32) * 4
+    b = torch.from_numpy(x).to(torch.bfloat16)
+    bits = b.view(torch.int16).numpy().view(np.uint16)
+    ref = b.to(torch.float64).numpy()
+    np.testing.assert_allclose(oracle.softmax(bits, 1.0), scipy.special.softmax(ref, axis=-1), rtol=1e-12)
+
+
+# ------------------------------------------------------------ row stats ----
+
+def test_alpha_equals_one_minus_tv():
+    rng = np.random.default_rng(3)
+    B, gamma, V = 6, 3, 777
+    t = _rows(rng, B * (gamma + 1), V).reshape(B, gamma + 1, V)
+    d = (t[:, :gamma] + rng.standard_normal((B, gamma, V)) * rng.uniform(0.05, 2.0, (B, 1, 1)))
+    s = oracle.row_stats(t, d, np.full(B, 0.9))
+    np.testing.assert_allclose(s["alpha"], 1.0 - s["tv"], rtol=0, atol=1e-12)
+    assert np.all(s["alpha"] > 0) and np.all(s["alpha"] < 1)
+
+
+def test_alpha_special_cases():
+    rng = np.random.default_rng(4)
+    V = 64
+    z = _rows(rng, 2, V).reshape(1, 2, V)
+    s = oracle.row_stats(z, z[:, :1].copy(), [1.3])
+    assert abs(s["alpha"][0, 0] - 1.0) < 1e-14  # p == q
+    # disjoint supports (-inf logits are zero probability)
+    t = np.full((1, 2, V), -np.inf)
+    d = np.full((1, 1, V), -np.inf)
+    t[0, :, : V // 2] = 0.0
+    d[0, 0, V // 2:] = 0.0
+    s = oracle.row_stats(t, d, [1.0])
+    assert s["alpha"][0, 0] == 0.0 and abs(s["tv"][0, 0] - 1.0) < 1e-15
+
+
+def test_entropy_closed_forms():
+    V = 1000
+    uni = np.zeros((1, 2, V))
+    s = oracle.row_stats(uni, uni[:, :1].copy(), [1.0])
+    assert abs(s["entropy"][0, 0] - math.log(V)) < 1e-12
+    onehot = np.full((1, 2, V), -np.inf)
+    onehot[0, :, 17] = 3.0
+    s = oracle.row_stats(onehot, onehot[:, :1].copy(), [0.7])
+    assert s["entropy"][0, 0] == 0.0
+    # library entropy and the target-only bound max p >= exp(-H) (summary App. D.2)
+    rng = np.random.default_rng(5)
+    z = _rows(rng, 4, V, 4.0).reshape(1, 4, V)
+    s = oracle.row_stats(z, z[:, :3].copy(), [1.0])
+    for i in range(4):
+        p = scipy.special.softmax(z[0, i])
+        assert abs(s["entropy"][0, i] - scipy.stats.entropy(p)) < 1e-12
+        assert p.max() >= math.exp(-s["entropy"][0, i])
+
+
+def test_proportional_mismatch_bound():
+    """|q - p| <= delta p  =>  alpha >= 1 - delta/2 (summary App. D.4)."""
+    rng = np.random.default_rng(6)
+    V = 512
+    for delta in (0.05, 0.3, 0.9):
+        p = scipy.special.softmax(rng.standard_normal(V) * 2)
+        # q = p (1 + delta s) with s in {-1, +1} chosen so sum p s = 0 exactly
+        order = rng.permutation(V)
+        half = order[: V // 2]
+        s = np.ones(V)
+        s[half] = -1.0
+        w_plus, w_minus = p[s > 0].sum(), p[s < 0].sum()
+        s[s > 0] *= min(1.0, w_minus / w_plus)
+        s[s < 0] *= min(1.0, w_plus / w_minus)
+        q = p * (1 + delta * s)
+        assert np.all(np.abs(q - p) <= delta * p + 1e-15) and abs(q.sum() - 1) < 1e-12
+        st = oracle.row_stats(np.log(np.stack([p, p]))[None], np.log(q)[None, None], [1.0])
+        assert st["alpha"][0, 0] >= 1 - delta / 2 - 1e-12
+
+
+# ------------------------------------------------------------ accept rule --
+
+def _verify_rows(t_rows, d_rows, ids, us, T=1.0, want_stats=False):
+    """Replicate one set of rows over a batch of (ids, uniforms)."""
+    ids = np.asarray(ids, np.int32)
+    us = np.asarray(us, np.float64)
+    B = ids.shape[0]
+    t = np.broadcast_to(t_rows, (B,) + t_rows.shape).copy()
+    d = np.broadcast_to(d_rows, (B,) + d_rows.shape).copy()
+    return oracle.verify(t, d, ids, np.full(B, T), us, want_stats)
+
+
+def test_equal_rows_accept_everything():
+    rng = np.random.default_rng(7)
+    V, gamma = 300, 3
+    t = _rows(rng, gamma + 1, V)
+    d = t[:gamma].copy()
+    us = [[0.0, 0.5, 0.999999, 0.2], [1 - 2.0 ** -24, 1 - 2.0 ** -24, 1 - 2.0 ** -24, 0.7]]
+    ids = [[1, 2, 3], [299, 0, 150]]
+    out = _verify_rows(t, d, ids, us)
+    assert list(out["accept_len"]) == [3, 3]
+    assert list(out["tokens"][0, :3]) == ids[0] and list(out["tokens"][1, :3]) == ids[1]
+
+
+def test_one_hot_draft_accepts_with_probability_p():
+    """q one-hot at y: accept iff u < p(y) (summary §2; App. D.2)."""
+    rng = np.random.default_rng(8)
+    V = 50
+    t = _rows(rng, 2, V)
+    y = 11
+    d = np.full((1, V), -np.inf)
+    d[0, y] = 0.0
+    py = scipy.special.softmax(t[0])[y]
+    out = _verify_rows(t, d, [[y], [y]], [[py * (1 - 1e-9), 0.5], [py * (1 + 1e-9), 0.5]])
+    assert list(out["accept_len"]) == [1, 0]
+
+
+def test_hand_fixture():
+    g = _golden("hand_v3.txt")
+    p, q = np.array(g["p"]), np.array(g["q"])
+    t_rows = np.log(np.stack([p, p]))
+    d_rows = np.log(q)[None]
+    st = oracle.row_stats(t_rows[None], d_rows[None], [1.0])
+    assert abs(st["alpha"][0, 0] - g["alpha"][0]) < 1e-15
+    assert abs(st["tv"][0, 0] - g["tv"][0]) < 1e-15
+    assert abs(st["entropy"][0, 0] - g["entropy"][0]) < 1e-15
+    r = g["accept_ratio_y1"][0]
+    out = _verify_rows(t_rows, d_rows, [[1], [1], [0], [0]],
+                       [[r - 0.01, 0.5], [r + 0.01, 0.99], [0.999, 0.5], [0.0, 0.5]])
+    assert list(out["accept_len"]) == [1, 0, 1, 1]
+    assert out["tokens"][1, 0] == int(g["residual_token"][0])
+    for u, tok in zip(g["bonus_u"], g["bonus_tokens"]):
+        o = _verify_rows(t_rows, d_rows, [[0]], [[0.1, u]])
+        assert o["tokens"][0, 1] == int(tok)
+    tl = oracle.tv_loss(np.log(p)[None, None], np.log(q)[None, None], 1.0, 1.0)
+    assert abs(tl["S"][0, 0] - g["S"][0]) < 1e-15
+    assert abs(tl["loss"][0] + g["alpha"][0]) < 1e-15
+    np.testing.assert_allclose(tl["grad"][0, 0], g["dloss_dz"], rtol=0, atol=1e-15)
+
+
+def test_cdf_strict_breakpoint():
+    """Smallest v with C(v) > u R: at u R == C(0) exactly the draw is v = 1."""
+    t_rows = np.zeros((2, 2))  # p = (0.5, 0.5) exactly
+    d_rows = np.zeros((1, 2))
+    out = _verify_rows(t_rows, d_rows, [[0]], [[0.3, 0.5]])
+    assert out["accept_len"][0] == 1 and out["tokens"][0, 1] == 1
+
+
+# ----------------------------------------------- exact sampling-law checks --
+
+def _intervals(weights):
+    """u-intervals [a, b) over which the inverse CDF of `weights` is constant
+    (breakpoints C(v)/R); returns (midpoints, lengths)."""
+    w = np.maximum(weights, 0.0)
+    c = np.concatenate([[0.0], np.cumsum(w) / w.sum()])
+    a, b = c[:-1], c[1:]
+    keep = b > a
+    return (a[keep] + b[keep]) / 2, (b - a)[keep]
+
+
+def _accept_regions(p, q, y):
+    thr = min(1.0, p[y] / q[y]) if q[y] > 0 else 1.0
+    regs = []
+    if thr > 0:
+        regs.append(("acc", thr / 2, thr))
+    if thr < 1:
+        regs.append(("rej", (thr + 1) / 2, 1 - thr))
+    return regs
+
+
+@pytest.mark.parametrize("T", [1.0, 0.8])
+def test_enumeration_gamma1_law_is_p(T):
+    """Output-token law equals p exactly (summary §2: RS preserves p; EntMTP
+    "Speculative Decoding"): exhaustive enumeration at V = 8."""
+    rng = np.random.default_rng(9)
+    V = 8
+    zt = _rows(rng, 2, V, 1.2)
+    zd = zt[:1] + rng.standard_normal((1, V)) * 0.8
+    p0, p1 = scipy.special.softmax(zt / T, axis=-1)
+    q0 = scipy.special.softmax(zd[0] / T)
+    cases, weights = [], []
+    for y in range(V):
+        for kind, u0, l0 in _accept_regions(p0, q0, y):
+            w = p1 if kind == "acc" else np.maximum(p0 - q0, 0)
+            for u1, l1 in zip(*_intervals(w)):
+                cases.append((y, u0, u1))
+                weights.append(q0[y] * l0 * l1)
+    ids = [[c[0]] for c in cases]
+    us = [[c[1], c[2]] for c in cases]
+    out = _verify_rows(zt, zd, ids, us, T)
+    weights = np.array(weights)
+    first = np.zeros(V)
+    second = np.zeros(V)
+    np.add.at(first, out["tokens"][:, 0], weights)
+    acc = out["accept_len"] == 1
+    np.add.at(second, out["tokens"][acc, 1], weights[acc])
+    np.testing.assert_allclose(first, p0, rtol=0, atol=1e-12)
+    alpha = np.minimum(p0, q0).sum()
+    np.testing.assert_allclose(weights[acc].sum(), alpha, atol=1e-12)
+    np.testing.assert_allclose(second / alpha, p1, rtol=0, atol=1e-12)
+
+
+def test_enumeration_gamma2_acceptance_product_and_tv_loss():
+    """gamma = 2, fixed rows: P(n >= k) = prod_{i<=k} alpha_i, the second
+    token given n >= 1 has law p_1, and E[n] equals minus the e2e TV loss of
+    the same rows (summary §4: the loss is the expected acceptance length)."""
+    rng = np.random.default_rng(10)
+    V = 8
+    zt = _rows(rng, 3, V, 1.0)
+    zd = zt[:2] + rng.standard_normal((2, V)) * 0.7
+    p = scipy.special.softmax(zt, axis=-1)
+    q = scipy.special.softmax(zd, axis=-1)
+    cases, weights = [], []
+    for y0 in range(V):
+        for k0, u0, l0 in _accept_regions(p[0], q[0], y0):
+            if k0 == "rej":
+                for u2, l2 in zip(*_intervals(np.maximum(p[0] - q[0], 0))):
+                    cases.append(([y0, 0], [u0, 0.5, u2]))
+                    weights.append(q[0][y0] * l0 * l2)
+                continue
+            for y1 in range(V):
+                for k1, u1, l1 in _accept_regions(p[1], q[1], y1):
+                    w = p[2] if k1 == "acc" else np.maximum(p[1] - q[1], 0)
+                    for u2, l2 in zip(*_intervals(w)):
+                        cases.append(([y0, y1], [u0, u1, u2]))
+                        weights.append(q[0][y0] * l0 * q[1][y1] * l1 * l2)
+    out = _verify_rows(zt, zd, [c[0] for c in cases], [c[1] for c in cases])
+    w = np.array(weights)
+    n = out["accept_len"]
+    a = np.minimum(p[:2], q).sum(axis=1)
+    assert abs(w.sum() - 1) < 1e-12
+    assert abs(w[n >= 1].sum() - a[0]) < 1e-12
+    assert abs(w[n >= 2].sum() - a[0] * a[1]) < 1e-12
+    first = np.zeros(V)
+    np.add.at(first, out["tokens"][:, 0], w)
+    np.testing.assert_allclose(first, p[0], atol=1e-12)
+    second = np.zeros(V)
+    m = n >= 1
+    np.add.at(second, out["tokens"][m, 1], w[m])
+    np.testing.assert_allclose(second / a[0], p[1], atol=1e-12)
+    third = np.zeros(V)
+    m = n >= 2
+    np.add.at(third, out["tokens"][m, 2], w[m])
+    np.testing.assert_allclose(third / (a[0] * a[1]), p[2], atol=1e-12)
+    tl = oracle.tv_loss(zt[None, :2], zd[None], 1.0, 1.0, with_grad=False)
+    assert abs(-tl["loss"][0] - (w * n).sum()) < 1e-12
+
+
+# --------------------------------------------------------- TV loss / grad --
+
+def _kink_free_inputs(rng, N, gamma, V, T, min_gap=1e-3):
+    while True:
+        t = rng.standard_normal((N, gamma, V)) * 1.3
+        d = t + rng.standard_normal((N, gamma, V)) * 0.6
+        p = scipy.special.softmax(t / T, axis=-1)
+        q = scipy.special.softmax(d / T, axis=-1)
+        if np.abs(p - q).min() > min_gap:
+            return t, d
+
+
+@pytest.mark.parametrize("T,scale", [(1.0, 1.0), (0.7, 2.5)])
+def test_tv_gradient_finite_differences(T, scale):
+    """Analytic gradient (summary App. A, chained through the product of
+    §4) against central differences of the loss, h = 1e-6."""
+    rng = np.random.default_rng(11)
+    N, gamma, V = 2, 3, 16
+    t, d = _kink_free_inputs(rng, N, gamma, V, T, 2e-4)
+    out = oracle.tv_loss(t, d, T, scale)
+    h = 1e-6
+    fd = np.empty_like(d)
+    for idx in np.ndindex(d.shape):
+        dp = d.copy()
+        dm = d.copy()
+        dp[idx] += h
+        dm[idx] -= h
+        lp = oracle.tv_loss(t, dp, T, 1.0, with_grad=False)["loss"].sum()
+        lm = oracle.tv_loss(t, dm, T, 1.0, with_grad=False)["loss"].sum()
+        fd[idx] = scale * (lp - lm) / (2 * h)
+    np.testing.assert_allclose(out["grad"], fd, rtol=0, atol=1e-7)
+
+
+def test_tv_gradient_structure():
+    """sum_j dalpha/dz_j = 0 and |dalpha/dz_j| <= q_j / T (App. A bound)."""
+    rng = np.random.default_rng(12)
+    N, gamma, V, T = 3, 3, 200, 0.8
+    t = rng.standard_normal((N, gamma, V)) * 2
+    d = t + rng.standard_normal((N, gamma, V)) * 0.5
+    out = oracle.tv_loss(t, d, T, 1.0)
+    q = scipy.special.softmax(d / T, axis=-1)
+    dadz = out["grad"] / out["g"][:, :, None]
+    assert np.abs(dadz.sum(-1)).max() < 1e-15
+    assert np.all(np.abs(dadz) <= q / T + 1e-15)
+    assert np.all((out["S"] >= 0) & (out["S"] <= 1))
+
+
+def test_e2e_loss_special_cases():
+    rng = np.random.default_rng(13)
+    V = 100
+    # gamma = 1: l = -alpha
+    t = rng.standard_normal((4, 1, V))
+    d = t + rng.standard_normal((4, 1, V))
+    out = oracle.tv_loss(t, d, 1.0, 1.0, with_grad=False)
+    np.testing.assert_allclose(out["loss"], -out["alpha"][:, 0], atol=0)
+    # all alpha = 1 (p == q): l = -gamma, gradient zero under either tie rule
+    t = rng.standard_normal((2, 5, V))
+    for tie in (True, False):
+        out = oracle.tv_loss(t, t.copy(), 1.0, 1.0, tie_le=tie)
+        np.testing.assert_allclose(out["loss"], -5.0, atol=1e-12)
+        assert np.abs(out["grad"]).max() < 1e-15
+    # alpha_0 = 0 zeroes every term; g_0 = -(1 + alpha_1 + alpha_1 alpha_2) = -3, later g_k = 0
+    t = np.full((1, 3, V), -np.inf)
+    d = np.full((1, 3, V), -np.inf)
+    t[0, 0, :50] = 0
+    d[0, 0, 50:] = 0
+    t[0, 1:] = 0
+    d[0, 1:] = 0
+    out = oracle.tv_loss(t, d, 1.0, 1.0)
+    assert out["loss"][0] == 0.0 and abs(out["g"][0, 0] + 3.0) < 1e-12 and np.all(out["g"][0, 1:] == 0)
+    assert np.isfinite(out["grad"]).all()
+
+
+# ----------------------------------------------------------------- flags ---
+
+def test_flags_and_defined_outputs():
+    rng = np.random.default_rng(14)
+    B, gamma, V = 6, 2, 40
+    t = rng.standard_normal((B, gamma + 1, V))
+    d = t[:, :gamma] + 0.1
+    ids = np.zeros((B, gamma), np.int32)
+    u = np.full((B, gamma + 1), 0.5)
+    temp = np.ones(B)
+    temp[1] = 0.0
+    ids[2, 1] = V
+    u[3, 0] = 1.0
+    t[4, 0, 7] = np.nan
+    d[5, 0, :] = -np.inf
+    out = oracle.verify(t, d, ids, temp, u)
+    assert out["flags"][0] == 0 and out["accept_len"][0] >= 0
+    assert out["flags"][1] == oracle.ROW_BAD_TEMP
+    assert out["flags"][2] == oracle.ROW_BAD_ID
+    assert out["flags"][3] == oracle.ROW_BAD_UNIFORM
+    assert out["flags"][4] == oracle.ROW_NONFINITE
+    assert out["flags"][5] == oracle.ROW_NONFINITE
+    for b in range(1, B):
+        assert out["accept_len"][b] == -1 and np.all(out["tokens"][b] == -1)
