@@ -1,0 +1,494 @@
+"""Benchmark: verified draft positions per second and logit GB/s (fraction of
+the measured HBM roofline) at V = 151,936 on one GB300.
+
+Step = one call of the hot path over one batch of synthetic input.  The
+headline workload is the verify batch (B = 64 sequences, gamma = 3,
+V = 151,936, bf16 logits, entropy-spanning target rows, draft = target +
+N(0, 0.3), T = 1): one mtp_rs_verify call per step.  The same JSON line also
+reports the other workloads measured in the same run: RL-rollout verify
+(B = 512), deep speculation with per-position alpha and entropy (B = 256,
+gamma = 7, fp32) and the e2e TV-loss forward+backward (N = 16,384).
+
+Timing: inputs resident in HBM; several copies of each input are rotated so
+successive steps never hit L2 (each copy is > L2 or the rotation exceeds 4x
+L2); steps are replayed from a captured CUDA graph and timed with CUDA events
+on the launching stream, synchronised on both sides.  `e2e` measures the same
+metric through the public API with pinned host buffers: host-to-device copy
+of the step's inputs, the call, and the device-to-host copy of its outputs.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
+       [--workloads verify64,rl512,deep256,tvloss]
+Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and logit GB/s (% of HBM roofline) at V=151936"
+UNIT = "positions/s"
+L2_BYTES = 129 * 1024 * 1024
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
+# ncu captures (profiles/), keyed by workload, valid only for the kernel
+# sources they were taken on (hash of csrc/).
+TRAFFIC = {}
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "mtp_speculative_decoding_row_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "cuda" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device=None) -> float:
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except FileNotFoundError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.rows.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = self.rows
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# -------------------------------------------------------------- workloads --
+
+def alg_bytes_verify(accept_len: np.ndarray, gamma: int, V: int, es: int, stats: bool) -> int:
+    """Logit bytes the method must read.  Without statistics the verify
+    stops at the first rejection: (n+1) target rows and min(n+1, gamma)
+    draft rows per sequence; with statistics every row is read."""
+    B = accept_len.shape[0]
+    if stats:
+        return B * (2 * gamma + 1) * V * es
+    n = accept_len.astype(np.int64)
+    return int(((n + 1) + np.minimum(n + 1, gamma)).sum()) * V * es
+
+
+class VerifyWorkload:
+    def __init__(self, name: str, device, copies: int):
+        import torch
+
+        import workloads as W
+        import mtp_speculative_decoding_row_gb300 as mtp
+
+        self.mtp = mtp
+        self.x = x = W.config(name)
+        self.name, self.device = name, device
+        self.B, self.gamma, self.V, self.es = x.B, x.gamma, x.V, x.esize
+        self.stats = x.want_stats
+
+        def up(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+            return torch.from_numpy(a).to(device)
+
+        base = [up(x.target), up(x.draft), up(x.draft_ids), up(x.temperature), up(x.uniforms)]
+        self.inputs = [base] + [[t.clone() for t in base] for _ in range(copies - 1)]
+        self.copies = copies
+        self.outs = [None] * copies
+        self.positions = x.B * x.gamma
+        self.bytes_full = x.B * (2 * x.gamma + 1) * x.V * x.esize
+
+    def call(self, i: int, stream=None):
+        t, d, ids, T, u = self.inputs[i % self.copies]
+        self.outs[i % self.copies] = self.mtp.mtp_rs_verify(t, d, ids, T, u, with_stats=self.stats,
+                                                            out=self.outs[i % self.copies], stream=stream)
+
+    def alg_bytes(self) -> int:
+        n = self.outs[0].accept_len.cpu().numpy()
+        return alg_bytes_verify(n, self.gamma, self.V, self.es, self.stats)
+
+    def describe(self) -> str:
+        x = self.x
+        return {"verify64": "verify batch: B=64 gamma=3 V=151936 bf16 logits, entropy-spanning target (0.5-4 nats), "
+                            "draft = target + N(0,0.3), draft ids ~ q, T=1",
+                "rl512": "RL rollout verify: B=512 gamma=3 V=151936 bf16, peaked Zipf(1.1)+8 rows, 30% N(0,1) rows, "
+                         "delta in {0.1,0.5}, T in {0.6,1.0}",
+                "deep256": "deep speculation + stats: B=256 gamma=7 V=151936 fp32, T in {0.6,0.8,1.0}, delta 0..1, "
+                           "alpha and H for every position"}[x.name]
+
+
+class TVWorkload:
+    def __init__(self, device):
+        import torch
+
+        import workloads as W
+        import mtp_speculative_decoding_row_gb300 as mtp
+
+        self.mtp = mtp
+        self.x = x = W.config("tvloss", device=device)
+        self.N, self.gamma, self.V, self.es = x.N, x.gamma, x.V, 2
+        self.out = None
+        self.copies = 1
+        self.positions = x.N * x.gamma
+        self.bytes_full = x.N * x.gamma * x.V * (2 * 2 + 4)
+
+    def call(self, i: int, stream=None):
+        self.out = self.mtp.mtp_tv_loss_fwd_bwd(self.x.target, self.x.draft, self.x.temperature, self.x.grad_scale,
+                                                out=self.out, stream=stream)
+
+    def alg_bytes(self) -> int:
+        return self.bytes_full
+
+    def describe(self) -> str:
+        return ("e2e TV loss fwd+bwd: N=16384 positions x gamma=3, V=151936, bf16 logits (entropy-spanning target, "
+                "draft = target + N(0,0.5)), fp32 gradient, T=1")
+
+
+def time_graph(wl, steps: int, warmup: int, device) -> dict:
+    """Capture `copies` consecutive calls in a CUDA graph; replay; time K calls."""
+    import torch
+
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    for i in range(max(1, wl.copies)):
+        wl.call(i)  # first calls: plan caches, output allocation
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        stream.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(wl.copies):
+                wl.call(i, stream=torch.cuda.current_stream(device))
+    torch.cuda.synchronize(device)
+    reps, extra = divmod(steps, wl.copies)
+    wreps = max(1, math.ceil(warmup / wl.copies))
+    with torch.cuda.stream(stream):
+        for _ in range(wreps):
+            g.replay()
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        for i in range(extra):
+            wl.call(i, stream=stream)
+        ev1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = ev0.elapsed_time(ev1)
+    return {"ms_total": ms, "ms_per_step": ms / steps, "launches": steps}
+
+
+def time_e2e(wl: VerifyWorkload, steps: int, warmup: int, device) -> dict:
+    """Same metric through the public call with pinned host buffers: per step
+    H2D of the inputs, the call, D2H of tokens and accept lengths."""
+    import torch
+
+    host = [t.cpu().pin_memory() for t in wl.inputs[0]]
+    dev_in = [torch.empty_like(t) for t in wl.inputs[0]]
+    out = None
+    tok_h = torch.empty((wl.B, wl.gamma + 1), dtype=torch.int32).pin_memory()
+    len_h = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        nonlocal out
+        for d, h in zip(dev_in, host):
+            d.copy_(h, non_blocking=True)
+        out = wl.mtp.mtp_rs_verify(*dev_in, with_stats=wl.stats, out=out, stream=stream)
+        tok_h.copy_(out.tokens, non_blocking=True)
+        len_h.copy_(out.accept_len, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(device)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = ev0.elapsed_time(ev1)
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = tok_h.numel() * 4 + len_h.numel() * 4
+    return {"value": wl.positions * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def oracle_verify_rate(name: str, budget_s: float, sample_b: int) -> dict:
+    """Positions/s of the float64 oracle on a bounded sample of the workload."""
+    import oracle
+    import workloads as W
+
+    x = W.config(name)
+    sl = slice(0, min(sample_b, x.B))
+    args = (x.target[sl], x.draft[sl], x.draft_ids[sl], x.temperature[sl], x.uniforms[sl])
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.verify(*args, want_stats=x.want_stats)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    pos = reps * (sl.stop - sl.start) * x.gamma
+    return {"value": pos / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{sl.stop - sl.start} sequences of {name} x {reps} repeats ({el:.1f} s, float64 C, OpenMP)"}
+
+
+# ------------------------------------------------------------------- main --
+
+def run_reference(args, world, rank):
+    """Reference arm: the float64 oracle timed on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    import workloads as W
+
+    x = W.config("verify64")
+    sample = 8
+    sl = slice(0, sample)
+    a = (x.target[sl], x.draft[sl], x.draft_ids[sl], x.temperature[sl], x.uniforms[sl])
+    for _ in range(args.warmup):
+        oracle.verify(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(*a)
+    el = time.perf_counter() - t0
+    val = args.steps * sample * x.gamma / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "verify64 (bounded sample: 8 of 64 sequences per step)", "B": 64, "gamma": 3,
+                   "V": 151936, "input_dtype": "bf16"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{sample} sequences of verify64 per step"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_cuda(args, world, rank, local, pg):
+    import torch
+
+    import mtp_speculative_decoding_row_gb300 as mtp
+    from mtp_speculative_decoding_row_gb300 import build as mtp_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0 or not os.path.exists(mtp_build.LIB):
+        mtp_build.build()
+    barrier(pg, device)
+    mtp.load_library()
+    peaks = load_peaks()
+    peak = peaks["hbm_gbs"]
+    uuid = str(torch.cuda.get_device_properties(device).uuid)
+    gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+
+    names = [w for w in args.workloads.split(",") if w]
+    results = {}
+    head = None
+    for name in names:
+        if name == "tvloss":
+            wl = TVWorkload(device)
+            steps = max(3, min(args.steps, 20)) if name != names[0] else args.steps
+        else:
+            per_copy = VerifyWorkloadBytes(name)
+            copies = max(2, math.ceil(4 * L2_BYTES / per_copy))
+            wl = VerifyWorkload(name, device, min(copies, 8))
+            steps = args.steps
+        sampler = ClockSampler(gpu_id) if name == names[0] else None
+        barrier(pg, device)
+        torch.cuda.synchronize(device)
+        if sampler:
+            sampler.start()
+        t = time_graph(wl, steps, args.warmup, device)
+        clocks = sampler.stop() if sampler else None
+        t_ms = max_over_ranks(pg, t["ms_total"], device)
+        alg = wl.alg_bytes()
+        per_launch_s = t["ms_total"] / 1e3 / t["launches"]
+        achieved = alg / per_launch_s / 1e9
+        r = {
+            "workload": wl.describe(),
+            "positions_per_s": world * wl.positions * steps / (t_ms / 1e3),
+            "ms_per_step": t_ms / steps,
+            "logit_gbps": achieved,
+            "roofline_frac": achieved / peak,
+            "alg_bytes_per_step": alg,
+            "full_bytes_per_step": wl.bytes_full,
+            "steps": steps,
+            "input_copies": wl.copies,
+        }
+        results[name] = r
+        if head is None:
+            head = (name, wl, t, t_ms, steps, clocks, alg, achieved)
+        del wl
+        torch.cuda.empty_cache()
+
+    name, wl0, t, t_ms, steps, clocks, alg, achieved = head
+    # e2e leg on the headline workload
+    e2e = None
+    if name != "tvloss":
+        wl = VerifyWorkload(name, device, 1)
+        e2e = time_e2e(wl, max(3, min(args.steps, 50)), max(3, args.warmup), device)
+        e2e["value"] = max_over_ranks(pg, -e2e["value"], device) * -1 * world
+    h = csrc_hash()
+    traffic = TRAFFIC.get(name)
+    traffic_val = traffic["bytes"] if traffic and traffic.get("csrc") == h else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and name != "tvloss":
+        cpu = oracle_verify_rate(name, args.cpu_seconds, 16)
+
+    if rank == 0:
+        hr = results[name]
+        line = {
+            "metric": METRIC, "value": hr["positions_per_s"], "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": hr["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": hr["workload"], "B": wl0.B if hasattr(wl0, "B") else wl0.N, "gamma": wl0.gamma,
+                       "V": wl0.V, "input_dtype": "bf16" if wl0.es == 2 else "f32",
+                       "l2": f"{hr['input_copies']} rotated input copies of {hr['full_bytes_per_step'] / 1e6:.0f} MB "
+                             f"(> 4x L2 between reuses)",
+                       "timing": "CUDA graph replay, CUDA events on the launching stream",
+                       "parallelism": f"replicas x{world}"},
+            "logit_gbps": hr["logit_gbps"],
+            "logit_gbps_full_rows": hr["full_bytes_per_step"] / (hr["ms_per_step"] / 1e3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic_val,
+                         "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)",
+                         "algorithmic_bytes_per_launch": alg},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": t["launches"],
+            "clocks": clocks,
+            "workloads": results,
+            "kernel_sources": h,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def VerifyWorkloadBytes(name: str) -> int:
+    return {"verify64": 64 * 7 * 151936 * 2, "rl512": 512 * 7 * 151936 * 2, "deep256": 256 * 15 * 151936 * 4}[name]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workloads", default="verify64,rl512,deep256,tvloss")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_cuda(args, world, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

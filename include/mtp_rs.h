@@ -1,0 +1,154 @@
+/*
+ * mtp_rs.h -- C ABI of the GB300 (sm_103a) library for multi-token-prediction
+ * rejection-sampling verification, per-position row statistics and the fused
+ * forward+backward of the end-to-end TV loss.
+ *
+ * Method references (page title, section):
+ *   [BB] "Breaking Entropy Bounds: Accelerating RL Training via MTP with
+ *        Rejection Sampling" -- §2 "Acceptance methods" (accept with
+ *        probability min(1, p(y)/q(y)); RS preserves p), §3 and §8 (acceptance
+ *        equals the overlap sum_v min(p_v, q_v) = 1 - TV), §4 "End-to-end TV
+ *        loss", App. A (TV gradient with S = sum_v 1[q_v <= p_v] q_v),
+ *        App. F (fused TV loss kernel), App. G.1 (stop at the first rejection;
+ *        residual or bonus token by two-pass CDF inversion).
+ *   [EM] "EntMTP: Accelerating LLM Inference with Entropy Guided Multi Token
+ *        Prediction", Related Work, "Speculative Decoding" (left-to-right
+ *        acceptance; replacement from norm(max(0, p - q)); suffix discarded).
+ *
+ * Conventions shared by every entry point
+ *   - Logits are row-major with the vocabulary contiguous: target
+ *     [B, gamma+1, V] (verify, stats) or [N, gamma, V] (TV loss), draft
+ *     [B, gamma, V] or [N, gamma, V].  Storage is float32 or bfloat16; all
+ *     arithmetic is float32.
+ *   - Every pointer is caller-owned DEVICE memory on the current device.  The
+ *     library allocates nothing, keeps no per-call state and never modifies
+ *     its inputs.  Optional outputs may be NULL.
+ *   - Logit base pointers must be 16-byte aligned (MTP_ERR_MISALIGNED
+ *     otherwise); any V >= 1 is accepted, and rows that are not 16-byte
+ *     aligned (V * element size not a multiple of 16) are handled in-kernel.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).  The
+ *     return value covers argument validation and the launch; an error from
+ *     an earlier asynchronous failure surfaces as MTP_ERR_CUDA.
+ *   - Bad data never traps: it sets row-flag bits, and the flagged row gets
+ *     defined outputs (tokens and accept length -1, statistics and loss NaN,
+ *     gradient 0).
+ *   - Temperatures scale both target and draft logits: p = softmax(z_t / T),
+ *     q = softmax(z_d / T).  -inf logits are allowed (probability 0).
+ */
+#ifndef MTP_RS_H
+#define MTP_RS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st *mtp_stream_t;
+
+typedef enum {
+    MTP_OK = 0,
+    MTP_ERR_INVALID_ARG = 1,      /* NULL required pointer, bad size or gamma */
+    MTP_ERR_UNSUPPORTED_DTYPE = 2,
+    MTP_ERR_MISALIGNED = 3,       /* logit base pointer not 16-byte aligned */
+    MTP_ERR_CUDA = 4,             /* CUDA launch / earlier asynchronous error */
+    MTP_ERR_NO_DEVICE = 5         /* no usable cluster launch configuration */
+} mtp_status;
+
+typedef enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 } mtp_dtype;
+
+/* Per-row flag bits written by the device. */
+enum {
+    MTP_ROW_NONFINITE = 1,   /* a read logit is NaN or +inf, or a read row is all -inf */
+    MTP_ROW_BAD_ID = 2,      /* a draft id outside [0, V) */
+    MTP_ROW_BAD_TEMP = 4,    /* temperature <= 0, NaN or inf */
+    MTP_ROW_ZERO_MASS = 8,   /* residual mass rounded to 0 at a rejection; the
+                                token was drawn from p_j instead (outputs valid) */
+    MTP_ROW_BAD_UNIFORM = 16,/* a uniform outside [0, 1) or NaN */
+    MTP_ROW_TIMEOUT = 32     /* an on-chip wait gave up (bounded waits) */
+};
+
+/* Maximum number of draft steps per call. */
+#define MTP_MAX_GAMMA 32
+
+/*
+ * mtp_rs_verify -- batched MTP rejection-sampling verification [BB §2,
+ * App. G.1; EM "Speculative Decoding"].
+ *
+ * For each sequence b: for i = 0..gamma-1, p_i = softmax(target[b,i]/T_b),
+ * q_i = softmax(draft[b,i]/T_b); draft token y_i = draft_ids[b,i] is
+ * accepted iff uniforms[b,i] * q_i(y_i) < p_i(y_i) (probability
+ * min(1, p/q)).  At the first rejection j the replacement is drawn from
+ * norm(max(0, p_j - q_j)) by inverse CDF with uniforms[b,gamma]: the smallest
+ * vocabulary index v with C(v) > u * R (ascending index, C the running sum, R
+ * the total).  If all gamma drafts are accepted, the bonus token is drawn the
+ * same way from p_gamma.  Rows after the stop are not read unless statistics
+ * are requested.
+ *
+ *   target_logits [B, gamma+1, V] dtype     draft_logits [B, gamma, V] dtype
+ *   draft_ids     [B, gamma] int32          temperature  [B] float32 (> 0)
+ *   uniforms      [B, gamma+1] float32 in [0, 1)
+ *   out_tokens    [B, gamma+1] int32: accepted drafts, then the drawn token,
+ *                 then -1 padding.                               (required)
+ *   accept_len    [B] int32: number of accepted drafts n in [0, gamma], -1 if
+ *                 the row is flagged with an error bit.          (required)
+ *   alpha         [B, gamma] float32 or NULL: overlap sum_v min(p_i, q_i)
+ *   entropy       [B, gamma+1] float32 or NULL: H(p_i) in nats
+ *                 (alpha and entropy must both be given or both NULL; when
+ *                 given, every row of the sequence is read.)
+ *   row_flags     [B] int32 or NULL.
+ * Requirements: B >= 0 (B = 0 is a no-op), 1 <= gamma <= MTP_MAX_GAMMA,
+ * V >= 1.
+ */
+int mtp_rs_verify(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                  const int32_t *draft_ids, const float *temperature, const float *uniforms,
+                  int B, int gamma, int V,
+                  int32_t *out_tokens, int32_t *accept_len, float *alpha, float *entropy,
+                  int32_t *row_flags, mtp_stream_t stream);
+
+/*
+ * mtp_row_stats -- per-position overlap and target entropy without
+ * decisions [BB §3, §8: alpha = sum_v min(p_v, q_v) = 1 - TV; entropy
+ * H(p) = -sum_v p_v log p_v in nats].
+ *
+ *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V], temperature [B]
+ *   alpha [B, gamma] float32 (required), entropy [B, gamma+1] float32
+ *   (required), row_flags [B] int32 or NULL.
+ */
+int mtp_row_stats(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                  const float *temperature, int B, int gamma, int V,
+                  float *alpha, float *entropy, int32_t *row_flags, mtp_stream_t stream);
+
+/*
+ * mtp_tv_loss_fwd_bwd -- fused forward and backward of the end-to-end TV
+ * loss [BB §4, App. A, App. F].
+ *
+ * For every token position t and draft step k: p = softmax(target[t,k]/T)
+ * (detached), q = softmax(draft[t,k]/T), alpha_k = sum_v min(p_v, q_v),
+ * S_k = sum_v 1[q_v <= p_v] q_v.  The loss of position t is
+ *     l_t = - sum_{m=1..gamma} prod_{i<=m} alpha_i
+ * and the gradient with respect to the draft logits is
+ *     grad[t,k,j] = grad_scale * (dl_t/dalpha_k) * (1/T) * q_j (1[q_j <= p_j] - S_k).
+ * The pages call the loss "normalised"; a constant normaliser such as 1/gamma
+ * is folded into grad_scale by the caller.
+ *
+ *   target_logits, draft_logits [N, gamma, V] dtype
+ *   loss  [N] float32 (required)            alpha [N, gamma] float32 or NULL
+ *   grad_draft_logits [N, gamma, V] float32 (required; fully overwritten)
+ *   row_flags [N] int32 or NULL.
+ * Requirements: N >= 0, 1 <= gamma <= MTP_MAX_GAMMA, V >= 1, temperature > 0
+ * (otherwise every position is flagged MTP_ROW_BAD_TEMP).
+ */
+int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                        float temperature, int N, int gamma, int V, float grad_scale,
+                        float *loss, float *alpha, float *grad_draft_logits, int32_t *row_flags,
+                        mtp_stream_t stream);
+
+/* Static description of a status code. */
+const char *mtp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MTP_RS_H */

@@ -1,0 +1,209 @@
+"""Python binding of the C-ABI library ``libmtprs.so`` (see ``include/mtp_rs.h``).
+
+Argument marshalling only: each function checks tensor devices, dtypes,
+shapes and contiguity, allocates outputs with PyTorch on the inputs' device,
+and calls the C function of the same name on the current CUDA stream.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+or PyTorch fallback, and importing a missing library raises.
+
+Method references: "Breaking Entropy Bounds: Accelerating RL Training via MTP
+with Rejection Sampling" (§2, §3, §4, §8, App. A, App. F, App. G.1) and
+"EntMTP", Related Work "Speculative Decoding".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+from . import build as _build
+
+__all__ = [
+    "mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_status_string", "MTPError", "load_library",
+    "VerifyResult", "StatsResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID", "ROW_BAD_TEMP",
+    "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
+]
+
+ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM, ROW_TIMEOUT = 1, 2, 4, 8, 16, 32
+ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_TIMEOUT
+MAX_GAMMA = 32
+DTYPE_F32, DTYPE_BF16 = 0, 1
+EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_status_string")
+
+_lib = None
+
+
+class MTPError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {mtp_status_string(status)} (status {status})")
+        self.status = status
+
+
+def load_library(path: Optional[str] = None, build_if_missing: bool = False):
+    """Load libmtprs.so (ctypes) and declare the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        if build_if_missing:
+            _build.build()
+        else:
+            raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                              f"g.build()'` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.mtp_rs_verify.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.mtp_rs_verify.restype = I
+    lib.mtp_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
+    lib.mtp_row_stats.restype = I
+    lib.mtp_tv_loss_fwd_bwd.argtypes = [P, P, I, F, I, I, I, F, P, P, P, P, P]
+    lib.mtp_tv_loss_fwd_bwd.restype = I
+    lib.mtp_status_string.argtypes = [I]
+    lib.mtp_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def mtp_status_string(status: int) -> str:
+    return load_library().mtp_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------ marshalling --
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _check(t, name, device, dtype=None, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device, stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class VerifyResult(NamedTuple):
+    tokens: "object"      # [B, gamma+1] int32, -1 padded
+    accept_len: "object"  # [B] int32 (-1 if flagged)
+    alpha: "object"       # [B, gamma] float32 or None
+    entropy: "object"     # [B, gamma+1] float32 or None
+    row_flags: "object"   # [B] int32
+
+
+class StatsResult(NamedTuple):
+    alpha: "object"
+    entropy: "object"
+    row_flags: "object"
+
+
+class TVLossResult(NamedTuple):
+    loss: "object"        # [N] float32
+    alpha: "object"       # [N, gamma] float32
+    grad: "object"        # [N, gamma, V] float32
+    row_flags: "object"   # [N] int32
+
+
+def mtp_rs_verify(target_logits, draft_logits, draft_ids, temperature, uniforms, *, with_stats: bool = False,
+                  out: Optional[VerifyResult] = None, stream=None) -> VerifyResult:
+    """Batched MTP rejection-sampling verification (see mtp_rs_verify in
+    include/mtp_rs.h).  target_logits [B, gamma+1, V], draft_logits
+    [B, gamma, V] (float32 or bfloat16), draft_ids [B, gamma] int32,
+    temperature [B] float32, uniforms [B, gamma+1] float32."""
+    torch = _torch()
+    dev = target_logits.device
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    _check(target_logits, "target_logits", dev)
+    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
+    _check(draft_ids, "draft_ids", dev, torch.int32, (B, gamma))
+    _check(temperature, "temperature", dev, torch.float32, (B,))
+    _check(uniforms, "uniforms", dev, torch.float32, (B, gamma + 1))
+    if out is None:
+        out = VerifyResult(
+            torch.empty((B, gamma + 1), dtype=torch.int32, device=dev),
+            torch.empty((B,), dtype=torch.int32, device=dev),
+            torch.empty((B, gamma), dtype=torch.float32, device=dev) if with_stats else None,
+            torch.empty((B, gamma + 1), dtype=torch.float32, device=dev) if with_stats else None,
+            torch.empty((B,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_rs_verify(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_ids), _ptr(temperature),
+        _ptr(uniforms), B, gamma, V, _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.alpha), _ptr(out.entropy),
+        _ptr(out.row_flags), _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_rs_verify", rc)
+    return out
+
+
+def mtp_row_stats(target_logits, draft_logits, temperature, *, out: Optional[StatsResult] = None,
+                  stream=None) -> StatsResult:
+    """Per-position alpha = sum min(p, q) [B, gamma] and H(p) [B, gamma+1]."""
+    torch = _torch()
+    dev = target_logits.device
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    _check(target_logits, "target_logits", dev)
+    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
+    _check(temperature, "temperature", dev, torch.float32, (B,))
+    if out is None:
+        out = StatsResult(torch.empty((B, gamma), dtype=torch.float32, device=dev),
+                          torch.empty((B, g1), dtype=torch.float32, device=dev),
+                          torch.empty((B,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_row_stats(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(temperature), B, gamma, V,
+        _ptr(out.alpha), _ptr(out.entropy), _ptr(out.row_flags), _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_row_stats", rc)
+    return out
+
+
+def mtp_tv_loss_fwd_bwd(target_logits, draft_logits, temperature: float = 1.0, grad_scale: float = 1.0, *,
+                        out: Optional[TVLossResult] = None, stream=None) -> TVLossResult:
+    """Fused e2e TV loss forward + backward over [N, gamma, V] logits; returns
+    per-position loss, alpha, the float32 gradient w.r.t. the draft logits and
+    row flags."""
+    torch = _torch()
+    dev = target_logits.device
+    N, gamma, V = target_logits.shape
+    _check(target_logits, "target_logits", dev)
+    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (N, gamma, V))
+    if out is None:
+        out = TVLossResult(torch.empty((N,), dtype=torch.float32, device=dev),
+                           torch.empty((N, gamma), dtype=torch.float32, device=dev),
+                           torch.empty((N, gamma, V), dtype=torch.float32, device=dev),
+                           torch.empty((N,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_tv_loss_fwd_bwd(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), float(temperature), N, gamma, V,
+        float(grad_scale), _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad), _ptr(out.row_flags),
+        _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_tv_loss_fwd_bwd", rc)
+    return out

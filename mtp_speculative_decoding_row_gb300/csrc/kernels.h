@@ -1,0 +1,50 @@
+// kernels.h -- internal interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <stdint.h>
+
+namespace mtp {
+
+constexpr int MAX_GAMMA = 32;
+
+// Kernel modes of the row kernel.
+enum RowMode { MODE_VERIFY = 0, MODE_VERIFY_STATS = 1, MODE_STATS = 2 };
+
+struct VerifyArgs {
+    const void *target;  // [B, gamma+1, V]
+    const void *draft;   // [B, gamma, V]
+    const int32_t *ids;  // [B, gamma]          (verify modes)
+    const float *temp;   // [B]
+    const float *unif;   // [B, gamma+1]        (verify modes)
+    int B, gamma, V;
+    int aligned;            // every row starts on 16 bytes and V is whole vectors
+    uint32_t slice_bytes;   // shared bytes of one row slice
+    int32_t *tokens;        // [B, gamma+1]      (verify modes)
+    int32_t *accept_len;    // [B]               (verify modes)
+    float *alpha;           // [B, gamma]        (stats modes)
+    float *entropy;         // [B, gamma+1]      (stats modes)
+    int32_t *flags;         // [B] or null
+};
+
+struct TVArgs {
+    const void *target;  // [N, gamma, V]
+    const void *draft;   // [N, gamma, V]
+    float temperature, grad_scale;
+    int N, gamma, V;
+    int aligned;
+    int nres;               // draft slices kept on chip (1..gamma)
+    uint32_t slice_bytes;
+    float *loss;            // [N]
+    float *alpha;           // [N, gamma] or null
+    float *grad;            // [N, gamma, V]
+    int32_t *flags;         // [N] or null
+};
+
+// Shared-memory header bytes in front of the slice buffers.
+constexpr uint32_t HDR_BYTES = 4096;
+
+// Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
+const void *row_kernel(int dtype, int mode);
+const void *tv_kernel(int dtype);
+
+}  // namespace mtp

@@ -1,0 +1,153 @@
+"""Parity checks of library outputs against the float64 oracle (test
+infrastructure, used by the test suite and the smoke check).
+
+Rules (tolerances fixed by the method's accuracy bar):
+* token ids and accept lengths must be identical, except in sequences where
+  a decision the oracle took is near its margin: |u_i - p_i(y)/q_i(y)| <
+  1e-5 for an accept test, or a CDF margin below 1e-5 for the final draw.
+  Those sequences are counted and only checked for validity (the accepted
+  prefix equals the draft ids, the drawn token has positive weight).
+* alpha, entropy and the TV loss within 1e-5 relative for float32 logits and
+  2e-3 for bfloat16 logits (plus 1e-6 absolute, since entropy and alpha may
+  be zero), gradients within 1e-4 absolute.
+* flags must match exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MARGIN = 1e-5
+ERROR_BITS = 1 | 2 | 4 | 16 | 32  # every flag except ZERO_MASS (8)
+GRAD_ATOL = 1e-4
+ATOL = 1e-6
+
+
+def rtol_for(dtype: str) -> float:
+    return 1e-5 if dtype == "f32" else 2e-3
+
+
+def _relerr(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.abs(a - b) / np.maximum(np.abs(b), 1e-30)
+
+
+def verify_report(tokens, accept_len, flags, orc: dict, draft_ids, gamma: int, V: int, dtype: str,
+                  alpha=None, entropy=None) -> dict:
+    """Compare one verify call; returns a report dict (see assert_ok)."""
+    B = accept_len.shape[0]
+    rep = {"B": B, "exact": 0, "near_margin": 0, "mismatch": [], "flag_mismatch": [], "stats_bad": []}
+    for b in range(B):
+        if flags[b] != orc["flags"][b]:
+            rep["flag_mismatch"].append((b, int(flags[b]), int(orc["flags"][b])))
+            continue
+        if orc["accept_len"][b] < 0:
+            if accept_len[b] != -1 or np.any(tokens[b] != -1):
+                rep["mismatch"].append((b, "flagged row outputs"))
+            continue
+        n_o = int(orc["accept_len"][b])
+        taken = orc["acc_margin"][b, : min(n_o + 1, gamma)]
+        near = bool(np.any(taken < MARGIN)) or bool(orc["cdf_margin"][b] < MARGIN)
+        same = accept_len[b] == n_o and np.array_equal(tokens[b], orc["tokens"][b])
+        if same:
+            rep["exact"] += 1
+            continue
+        if near:
+            rep["near_margin"] += 1
+            n = int(accept_len[b])
+            ok = 0 <= n <= gamma and np.array_equal(tokens[b, :n], draft_ids[b, :n])
+            ok = ok and 0 <= tokens[b, n] < V and np.all(tokens[b, n + 1:] == -1)
+            if not ok:
+                rep["mismatch"].append((b, "invalid near-margin output"))
+            continue
+        rep["mismatch"].append((b, f"gpu n={int(accept_len[b])} tok={tokens[b].tolist()} "
+                                   f"oracle n={n_o} tok={orc['tokens'][b].tolist()}"))
+    if alpha is not None:
+        rep.update(stats_report(alpha, entropy, orc, dtype, flags))
+    return rep
+
+
+def stats_report(alpha, entropy, orc: dict, dtype: str, flags=None) -> dict:
+    rt = rtol_for(dtype)
+    good = (orc["flags"] & ERROR_BITS) == 0  # rows without error bits
+    ea = np.abs(alpha[good].astype(np.float64) - orc["alpha"][good])
+    eh = np.abs(entropy[good].astype(np.float64) - orc["entropy"][good])
+    bad_a = ea > rt * np.abs(orc["alpha"][good]) + ATOL
+    bad_h = eh > rt * np.abs(orc["entropy"][good]) + ATOL
+    out = {
+        "alpha_max_abs": float(ea.max()) if ea.size else 0.0,
+        "alpha_max_rel": float(_relerr(alpha[good], orc["alpha"][good]).max()) if ea.size else 0.0,
+        "entropy_max_abs": float(eh.max()) if eh.size else 0.0,
+        "entropy_max_rel": float(_relerr(entropy[good], orc["entropy"][good]).max()) if eh.size else 0.0,
+        "stats_bad": [],
+    }
+    if bad_a.any():
+        out["stats_bad"].append(("alpha", int(bad_a.sum())))
+    if bad_h.any():
+        out["stats_bad"].append(("entropy", int(bad_h.sum())))
+    if not np.all(np.isnan(alpha[~good])) or not np.all(np.isnan(entropy[~good])):
+        out["stats_bad"].append(("flagged rows not NaN", 1))
+    if flags is not None and not np.array_equal(flags, orc["flags"]):
+        out["stats_bad"].append(("flags", int((flags != orc["flags"]).sum())))
+    return out
+
+
+def tv_report(loss, alpha, grad, flags, orc: dict, dtype: str, target_f64=None, draft_f64=None,
+              temperature: float = 1.0) -> dict:
+    """Compare TV-loss outputs.  Rows (t, k) whose oracle log-ratio
+    min_v |log q_v - log p_v| is below MARGIN sit on an indicator tie and are
+    only checked for sum_j grad = 0; they are counted as near-margin."""
+    rt = rtol_for(dtype)
+    rep = {"positions": int(loss.shape[0]), "near_margin_rows": 0, "bad": []}
+    if not np.array_equal(flags, orc["flags"]):
+        rep["bad"].append(("flags", int((flags != orc["flags"]).sum())))
+    good = orc["flags"] == 0
+    el = np.abs(loss[good].astype(np.float64) - orc["loss"][good])
+    ea = np.abs(alpha[good].astype(np.float64) - orc["alpha"][good])
+    rep["loss_max_abs"] = float(el.max()) if el.size else 0.0
+    rep["alpha_max_abs"] = float(ea.max()) if ea.size else 0.0
+    if np.any(el > rt * np.abs(orc["loss"][good]) + ATOL):
+        rep["bad"].append(("loss", int((el > rt * np.abs(orc["loss"][good]) + ATOL).sum())))
+    if np.any(ea > rt * np.abs(orc["alpha"][good]) + ATOL):
+        rep["bad"].append(("alpha", int((ea > rt * np.abs(orc["alpha"][good]) + ATOL).sum())))
+    N, gamma = alpha.shape
+    gmax = 0.0
+    for t in range(N):
+        if not good[t]:
+            if np.any(grad[t] != 0):
+                rep["bad"].append(("flagged grad not zero", t))
+            continue
+        for k in range(gamma):
+            d = np.abs(grad[t, k].astype(np.float64) - orc["grad"][t, k])
+            near = False
+            if target_f64 is not None:
+                lp = target_f64[t, k] / temperature
+                lq = draft_f64[t, k] / temperature
+                lp = lp - np.logaddexp.reduce(lp)
+                lq = lq - np.logaddexp.reduce(lq)
+                with np.errstate(invalid="ignore"):
+                    gap = np.abs(lq - lp)
+                near = bool(np.nanmin(gap) < MARGIN)
+            if near and d.max() > GRAD_ATOL:
+                rep["near_margin_rows"] += 1
+                if abs(float(grad[t, k].astype(np.float64).sum())) > 1e-3:
+                    rep["bad"].append(("near-margin row sum", (t, k)))
+                continue
+            gmax = max(gmax, float(d.max()))
+            if d.max() > GRAD_ATOL:
+                rep["bad"].append(("grad", (t, k, float(d.max()))))
+    rep["grad_max_abs"] = gmax
+    return rep
+
+
+def assert_ok(rep: dict, what: str = "") -> None:
+    problems = []
+    for key in ("mismatch", "flag_mismatch", "stats_bad", "bad"):
+        if rep.get(key):
+            problems.append(f"{key}: {rep[key][:8]}")
+    if problems:
+        raise AssertionError(f"{what} parity failed: " + "; ".join(problems) + f" | report {_short(rep)}")
+
+
+def _short(rep):
+    return {k: v for k, v in rep.items() if not isinstance(v, list)}

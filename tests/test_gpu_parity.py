@@ -1,0 +1,231 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 oracle
+on the same seeded inputs.  See oracle/compare.py for the bar."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from oracle import compare
+from tests.gpu_util import env, ensure_library, run_stats, run_tv, run_verify, to_dev, to_host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_library()
+
+
+def _check_verify(x, with_stats=False, what=""):
+    g = run_verify(x, with_stats)
+    o = oracle.verify(x.target, x.draft, x.draft_ids, x.temperature, x.uniforms, want_stats=with_stats)
+    rep = compare.verify_report(g["tokens"], g["accept_len"], g["row_flags"], o, x.draft_ids, x.gamma, x.V, x.dtype,
+                                g["alpha"], g["entropy"])
+    compare.assert_ok(rep, what)
+    return rep, g, o
+
+
+# ------------------------------------------------------------ verify -------
+
+@pytest.mark.parametrize("with_stats", [False, True])
+def test_verify_tiny_config(with_stats):
+    x = W.config("tiny")
+    rep, g, o = _check_verify(x, with_stats, "tiny")
+    assert rep["exact"] + rep["near_margin"] == x.B
+
+
+SWEEP = [
+    # (V, dtype, gamma, T, forced cluster)
+    (1, "f32", 3, 1.0, None),
+    (7, "bf16", 3, 0.6, 4),
+    (8, "bf16", 1, 1.7, None),
+    (100, "f32", 7, 1.0, 16),
+    (1000, "bf16", 3, 0.6, 2),
+    (1024, "f32", 3, 1.7, 8),
+    (4097, "bf16", 7, 1.0, 4),
+    (4097, "f32", 1, 0.6, 16),
+    (40000, "bf16", 3, 1.0, 8),
+    (40003, "f32", 3, 0.8, 16),
+]
+
+
+@pytest.mark.parametrize("V,dtype,gamma,T,C", SWEEP)
+@pytest.mark.parametrize("with_stats", [False, True])
+def test_verify_sweep(V, dtype, gamma, T, C, with_stats):
+    x = W.verify_inputs(f"sweep{V}", 24, gamma, V, dtype, 1000 + V + gamma, family="sigma",
+                        sigmas=np.linspace(0.5, 4.0, 24), delta=np.linspace(0.0, 1.0, 24), temperature=T)
+    with env(MTP_RS_CLUSTER=C):
+        rep, g, o = _check_verify(x, with_stats, f"sweep V={V} {dtype} gamma={gamma} C={C}")
+    assert rep["exact"] >= x.B - 2
+
+
+@pytest.mark.parametrize("name", ["verify64", "rl512", "deep256"])
+def test_verify_full_configs(name):
+    x = W.config(name)
+    rep, g, o = _check_verify(x, x.want_stats, name)
+    assert rep["exact"] + rep["near_margin"] == x.B
+    # both the accept path and the residual path occur at these sizes
+    n = g["accept_len"]
+    assert (n == x.gamma).any() and (n < x.gamma).any()
+    print(name, {k: v for k, v in rep.items() if not isinstance(v, list)})
+
+
+def test_verify_equal_rows_accept_all():
+    """delta = 0 rows give q == p: every draft accepted, alpha = 1."""
+    x = W.verify_inputs("eq", 16, 5, 5000, "bf16", 7, family="sigma", sigmas=3.0, delta=0.0)
+    g = run_verify(x, with_stats=True)
+    assert np.all(g["accept_len"] == 5)
+    np.testing.assert_array_equal(g["tokens"][:, :5], x.draft_ids)
+    np.testing.assert_allclose(g["alpha"], 1.0, atol=2e-6)
+
+
+def test_verify_deterministic():
+    x = W.verify_inputs("det", 32, 3, 30000, "bf16", 8, family="sigma", sigmas=np.linspace(1, 6, 32), delta=0.4)
+    a = run_verify(x, True)
+    b = run_verify(x, True)
+    for k in ("tokens", "accept_len", "alpha", "entropy", "row_flags"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_verify_output_law_chi_square():
+    """Output-token law equals p ("RS preserves the exact target
+    distribution"): one V = 8 row pair replicated 2^20 times with fresh
+    uniforms and draft ids ~ q; chi-square at a fixed seed."""
+    B, V = 1 << 20, 8
+    rng = np.random.Generator(np.random.Philox(4242))
+    zt = rng.standard_normal((2, V)).astype(np.float32) * 1.3
+    zd = (zt[:1] + rng.standard_normal((1, V)).astype(np.float32) * 0.9).astype(np.float32)
+    q = np.exp(zd[0].astype(np.float64) - zd[0].max())
+    q /= q.sum()
+    ids = rng.choice(V, size=(B, 1), p=q).astype(np.int32)
+    u = rng.random((B, 2), dtype=np.float32)
+    t = torch.from_numpy(np.broadcast_to(zt, (B, 2, V)).copy()).cuda()
+    d = torch.from_numpy(np.broadcast_to(zd, (B, 1, V)).copy()).cuda()
+    import mtp_speculative_decoding_row_gb300 as mtp
+    out = mtp.mtp_rs_verify(t, d, torch.from_numpy(ids).cuda(), torch.ones(B, device="cuda"),
+                            torch.from_numpy(u).cuda())
+    first = out.tokens[:, 0].cpu().numpy()
+    p = oracle.softmax(zt[0])
+    counts = np.bincount(first, minlength=V)
+    chi2 = ((counts - B * p) ** 2 / (B * p)).sum()
+    assert chi2 < 24.3, (chi2, counts, B * p)  # 0.999 quantile, 7 dof
+
+
+# ------------------------------------------------------------- stats -------
+
+@pytest.mark.parametrize("V,dtype,gamma,C", [(1024, "f32", 3, None), (4097, "bf16", 5, 8), (151936, "bf16", 3, None),
+                                             (30001, "f32", 2, 16)])
+def test_row_stats(V, dtype, gamma, C):
+    x = W.verify_inputs("stats", 12, gamma, V, dtype, 2000 + V, family="sigma", sigmas=np.linspace(0.3, 9, 12),
+                        delta=np.linspace(0, 1.5, 12), temperature=np.linspace(0.6, 1.4, 12))
+    with env(MTP_RS_CLUSTER=C):
+        g = run_stats(x)
+    o = oracle.row_stats(x.target, x.draft, x.temperature)
+    rep = compare.stats_report(g["alpha"], g["entropy"], o, dtype, g["row_flags"])
+    compare.assert_ok(rep, f"stats V={V}")
+
+
+def test_row_stats_deep_config():
+    x = W.config("deep256")
+    g = run_stats(x)
+    o = oracle.row_stats(x.target, x.draft, x.temperature)
+    rep = compare.stats_report(g["alpha"], g["entropy"], o, x.dtype, g["row_flags"])
+    compare.assert_ok(rep, "deep256 stats")
+    # alpha = 1 - TV against the oracle's independent TV
+    np.testing.assert_allclose(g["alpha"], 1 - o["tv"], rtol=0, atol=1e-5)
+
+
+# ------------------------------------------------------------ flags --------
+
+def test_flags_and_defined_outputs():
+    x = W.verify_inputs("flags", 8, 3, 3000, "f32", 31, family="sigma", sigmas=2.0, delta=0.3)
+    x.temperature[1] = 0.0
+    x.draft_ids[2, 1] = 3000
+    x.uniforms[3, 2] = 1.0
+    x.target[4, 0, 17] = np.nan
+    x.draft[5, 0, :] = -np.inf
+    x.target[6, 0, 5] = np.inf
+    x.uniforms[7, 0] = np.nan
+    for stats in (False, True):
+        g = run_verify(x, stats)
+        o = oracle.verify(x.target, x.draft, x.draft_ids, x.temperature, x.uniforms, want_stats=stats)
+        np.testing.assert_array_equal(g["row_flags"], o["flags"])
+        for b in range(1, 8):
+            assert g["accept_len"][b] == -1 and np.all(g["tokens"][b] == -1)
+        if stats:
+            assert np.all(np.isnan(g["alpha"][1:])) and np.all(np.isnan(g["entropy"][1:]))
+
+
+def test_masked_vocab_is_allowed():
+    """-inf logits are probability 0, not an error."""
+    x = W.verify_inputs("mask", 8, 3, 2048, "bf16", 32, family="sigma", sigmas=2.0, delta=0.3)
+    x.target[:, :, 1000:1500] = W.to_bf16_bits(np.array([-np.inf], np.float32))[0]
+    x.draft[:, :, 1200:1800] = W.to_bf16_bits(np.array([-np.inf], np.float32))[0]
+    for stats in (False, True):
+        rep, g, o = _check_verify(x, stats, "masked")
+        assert np.all(g["row_flags"] == 0)
+
+
+# ------------------------------------------------------------- TV loss -----
+
+TV_SWEEP = [
+    # (N, gamma, V, dtype, T, scale, C, nres cap)
+    (6, 1, 1000, "f32", 1.0, 1.0, None, None),
+    (6, 3, 4097, "bf16", 0.7, 0.5, 4, None),
+    (5, 3, 40000, "bf16", 1.0, 1.0, 16, None),
+    (4, 5, 12000, "f32", 1.3, 2.0, 8, 2),
+    (4, 3, 7, "bf16", 1.0, 1.0, 2, 1),
+    (3, 7, 151936, "bf16", 1.0, 1.0, None, None),
+]
+
+
+@pytest.mark.parametrize("N,gamma,V,dtype,T,scale,C,nres", TV_SWEEP)
+def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres):
+    x = W.tvloss_inputs("tv", N, gamma, V, dtype, 500 + V + gamma, delta=0.5, sigmas=np.linspace(1.0, 8.0, N))
+    with env(MTP_RS_CLUSTER=C, MTP_RS_TV_NRES=nres):
+        out = run_tv(to_dev(x.target), to_dev(x.draft), T, scale)
+    o = oracle.tv_loss(x.target, x.draft, T, scale)
+    tf = W.bf16_bits_to_f32(x.target).astype(np.float64) if dtype == "bf16" else x.target.astype(np.float64)
+    df = W.bf16_bits_to_f32(x.draft).astype(np.float64) if dtype == "bf16" else x.draft.astype(np.float64)
+    rep = compare.tv_report(out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy(),
+                            out.row_flags.cpu().numpy(), o, dtype, tf, df, T)
+    compare.assert_ok(rep, f"tv N={N} V={V}")
+
+
+def test_tv_loss_full_config_sampled():
+    """N = 16,384, gamma = 3, V = 151,936 bf16 on device: sampled positions
+    against the oracle, sum_j grad = 0 on every row, loss in [-gamma, 0]."""
+    x = W.config("tvloss", device="cuda")
+    out = run_tv(x.target, x.draft, x.temperature, x.grad_scale)
+    loss = out.loss.cpu().numpy()
+    assert np.all(out.row_flags.cpu().numpy() == 0)
+    assert np.all(loss <= 0) and np.all(loss >= -x.gamma)
+    rows = out.grad.view(-1, x.V)
+    sums = torch.zeros(rows.shape[0], dtype=torch.float64, device="cuda")
+    for s in range(0, rows.shape[0], 4096):
+        sums[s:s + 4096] = rows[s:s + 4096].double().sum(dim=1)
+    # per-element bar is 1e-4; fp32 normalisers (log2 Z ~ 17) give ~1e-6 relative error in every q
+    assert sums.abs().max().item() < 1e-4
+    idx = np.unique(np.linspace(0, x.N - 1, 24).astype(int))
+    it = torch.from_numpy(idx).cuda()
+    tb, db = to_host_bits(x.target[it]), to_host_bits(x.draft[it])
+    o = oracle.tv_loss(tb, db, x.temperature, x.grad_scale)
+    rep = compare.tv_report(loss[idx], out.alpha[it].cpu().numpy(), out.grad[it].cpu().numpy(),
+                            out.row_flags[it].cpu().numpy(), o, "bf16",
+                            W.bf16_bits_to_f32(tb).astype(np.float64), W.bf16_bits_to_f32(db).astype(np.float64),
+                            x.temperature)
+    compare.assert_ok(rep, "tvloss sampled")
+    print("tvloss sampled", {k: v for k, v in rep.items() if not isinstance(v, list)})
+
+
+def test_tv_loss_bad_temperature_and_nan():
+    x = W.tvloss_inputs("tvbad", 3, 2, 2000, "f32", 9, sigmas=2.0)
+    x.target[1, 1, 3] = np.nan
+    out = run_tv(to_dev(x.target), to_dev(x.draft), 1.0, 1.0)
+    f = out.row_flags.cpu().numpy()
+    assert list(f) == [0, oracle.ROW_NONFINITE, 0]
+    assert np.isnan(out.loss[1].item()) and torch.all(out.grad[1] == 0)
+    out = run_tv(to_dev(x.target), to_dev(x.draft), 0.0, 1.0)
+    assert np.all(out.row_flags.cpu().numpy() == oracle.ROW_BAD_TEMP)
+    assert torch.all(out.grad == 0)
