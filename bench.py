@@ -210,14 +210,14 @@ class VerifyWorkload:
 
 
 class TVWorkload:
-    def __init__(self, device):
+    def __init__(self, device, N=None):
         import torch
 
         import workloads as W
         import mtp_speculative_decoding_row_gb300 as mtp
 
         self.mtp = mtp
-        self.x = x = W.config("tvloss", device=device)
+        self.x = x = W.config("tvloss", device=device, N_override=N)
         self.N, self.gamma, self.V, self.es = x.N, x.gamma, x.V, 2
         self.out = None
         self.copies = 1
@@ -232,7 +232,7 @@ class TVWorkload:
         return self.bytes_full
 
     def describe(self) -> str:
-        return ("e2e TV loss fwd+bwd: N=16384 positions x gamma=3, V=151936, bf16 logits (entropy-spanning target, "
+        return (f"e2e TV loss fwd+bwd: N={self.N} positions x gamma=3, V=151936, bf16 logits (entropy-spanning target, "
                 "draft = target + N(0,0.5)), fp32 gradient, T=1")
 
 
@@ -388,7 +388,7 @@ def run_cuda(args, world, rank, local, pg):
     head = None
     for name in names:
         if name == "tvloss":
-            wl = TVWorkload(device)
+            wl = TVWorkload(device, args.tv_n)
             steps = max(3, min(args.steps, 20)) if name != names[0] else args.steps
         else:
             per_copy = VerifyWorkloadBytes(name)
@@ -478,6 +478,7 @@ def main():
     ap.add_argument("--workloads", default="verify64,rl512,deep256,tvloss")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

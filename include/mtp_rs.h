@@ -145,6 +145,19 @@ int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp
                         float *loss, float *alpha, float *grad_draft_logits, int32_t *row_flags,
                         mtp_stream_t stream);
 
+/*
+ * mtp_query_plan -- the launch plan a call would use on the current device
+ * (diagnostics; launches nothing).  op: 0 = mtp_rs_verify, 1 = mtp_rs_verify
+ * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd.  units = B
+ * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
+ * CTAs per thread-block cluster; the vocabulary is split into C slices),
+ * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
+ * per CTA), resident_drafts (TV loss: draft slices kept on chip, else 0).
+ * Returns the status the call's planning step would return.
+ */
+int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size, int *clusters,
+                   int *smem_bytes, int *resident_drafts);
+
 /* Static description of a status code. */
 const char *mtp_status_string(int status);
 

@@ -19,7 +19,8 @@ from typing import NamedTuple, Optional
 from . import build as _build
 
 __all__ = [
-    "mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_status_string", "MTPError", "load_library",
+    "mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string", "MTPError",
+    "load_library",
     "VerifyResult", "StatsResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID", "ROW_BAD_TEMP",
     "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
 ]
@@ -28,7 +29,8 @@ ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM, ROW_TIM
 ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_TIMEOUT
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_status_string")
+EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string")
+PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3}
 
 _lib = None
 
@@ -61,10 +63,23 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_row_stats.restype = I
     lib.mtp_tv_loss_fwd_bwd.argtypes = [P, P, I, F, I, I, I, F, P, P, P, P, P]
     lib.mtp_tv_loss_fwd_bwd.restype = I
+    lib.mtp_query_plan.argtypes = [I, I, I, I, I, P, P, P, P]
+    lib.mtp_query_plan.restype = I
     lib.mtp_status_string.argtypes = [I]
     lib.mtp_status_string.restype = ctypes.c_char_p
     _lib = lib
     return lib
+
+
+def mtp_query_plan(op: str, dtype: str, units: int, gamma: int, V: int) -> dict:
+    """Launch plan of a call on the current device: cluster size, persistent
+    clusters, shared memory per CTA and (TV loss) resident draft slices."""
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    rc = load_library().mtp_query_plan(PLAN_OPS[op], DTYPE_BF16 if dtype == "bf16" else DTYPE_F32, units, gamma, V,
+                                       *[ctypes.byref(v) for v in vals])
+    if rc:
+        raise MTPError("mtp_query_plan", rc)
+    return dict(zip(("cluster_size", "clusters", "smem_bytes", "resident_drafts"), (v.value for v in vals)))
 
 
 def mtp_status_string(status: int) -> str:

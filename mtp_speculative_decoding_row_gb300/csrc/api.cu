@@ -16,14 +16,14 @@ namespace {
 using namespace mtp;
 
 constexpr uint32_t kMaxSmem = 232448;        // 227 KB per CTA on sm_100-class parts
-constexpr uint32_t kRowBudget = 100 * 1024;  // row kernel: two CTAs per SM
-constexpr uint32_t kTVBudget = 110 * 1024;   // TV kernel: two CTAs per SM
 
 struct Plan {
     int C = 0;
     uint32_t slice_bytes = 0;
     uint32_t smem = 0;
     int nres = 0;
+    int clusters = 0;  // persistent grid: co-resident clusters used
+    int streams = 1;   // row kernel: sequences in flight per CTA
 };
 
 struct CacheEntry {
@@ -67,12 +67,13 @@ cudaError_t prepare_func(int dev, const void *func) {
     return cudaSuccess;
 }
 
-// Whether clusters of C CTAs with `smem` bytes each can be resident.
-bool cluster_fits(int dev, const void *func, int C, uint32_t smem) {
+// Largest number of co-resident clusters of C CTAs with `smem` bytes each
+// (0 when the configuration cannot run).
+int max_clusters(int dev, const void *func, int C, uint32_t smem) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (auto &c : g_cache)
-            if (c.device == dev && c.func == func && c.C == C && c.smem == smem) return c.ok != 0;
+            if (c.device == dev && c.func == func && c.C == C && c.smem == smem) return c.ok;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C);
@@ -87,57 +88,89 @@ bool cluster_fits(int dev, const void *func, int C, uint32_t smem) {
     cfg.numAttrs = 1;
     int n = 0;
     const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, func, &cfg);
-    const int ok = (e == cudaSuccess && n > 0) ? 1 : 0;
-    if (e != cudaSuccess) (void)cudaGetLastError();
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_cache.push_back({dev, func, C, smem, ok});
-    return ok != 0;
-}
-
-// Row kernel: two row slices per CTA.  Smallest cluster under the budget.
-bool plan_row(int dev, const void *func, int V, int es, Plan &p) {
-    const int forced = env_cluster();
-    for (int C = 1; C <= MAX_C; C *= 2) {
-        if (forced && C != forced) continue;
-        const uint32_t sb = slice_buffer_bytes(V, es, C);
-        const uint32_t smem = HDR_BYTES + 2 * sb;
-        if (smem > kMaxSmem) continue;
-        if (!forced && smem > kRowBudget && C < MAX_C) continue;
-        if (!cluster_fits(dev, func, C, smem)) continue;
-        p = {C, sb, smem, 0};
-        return true;
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
     }
-    return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_cache.push_back({dev, func, C, smem, n});
+    return n;
 }
 
-// TV kernel: one target slice, nres draft slices and gamma bit rows.
-bool plan_tv(int dev, const void *func, int V, int es, int gamma, Plan &p) {
+uint32_t smem_optin(int dev) {
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return static_cast<uint32_t>(optin < static_cast<int>(kMaxSmem) ? optin : kMaxSmem);
+}
+
+// Persistent row kernel: `streams` (1 or 2) sequences in flight per CTA, one
+// row pair slice each.  Picks the cluster size (1..16) and stream count that
+// keep the most sequence slices in flight for `units` sequences; the grid is
+// the co-resident cluster count.
+bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
     const int forced = env_cluster();
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int C = 1; C <= MAX_C; C *= 2) {
+    const int forced_ns = env_int("MTP_RS_STREAMS");
+    const uint32_t cap = smem_optin(dev);
+    long best = -1;
+    for (int ns = 1; ns <= 2; ++ns) {
+        if (forced_ns && ns != forced_ns) continue;
+        for (int C = 1; C <= MAX_C; ++C) {
             if (forced && C != forced) continue;
             const uint32_t sb = slice_buffer_bytes(V, es, C);
-            const uint32_t bitb = static_cast<uint32_t>(gamma) * static_cast<uint32_t>(slice_vectors(V, 16 / es, C));
-            const uint32_t fixed = HDR_BYTES + sb + ((bitb + 127u) & ~127u);
-            const uint32_t budget = (pass == 0 && !forced) ? kTVBudget : kMaxSmem;
-            if (fixed + sb > budget) continue;
-            int nres = static_cast<int>((budget - fixed) / sb);
-            if (nres > gamma) nres = gamma;
-            const int cap = env_int("MTP_RS_TV_NRES");
-            if (cap > 0 && nres > cap) nres = cap;
-            if (pass == 0 && !forced && nres < gamma && C < MAX_C) continue;
-            const uint32_t smem = fixed + static_cast<uint32_t>(nres) * sb;
-            if (!cluster_fits(dev, func, C, smem)) continue;
-            p = {C, sb, smem, nres};
-            return true;
+            const uint32_t smem = row_hdr_bytes() + 2 * ns * sb;
+            if (smem > cap) continue;
+            const int nc = max_clusters(dev, func, C, smem);
+            if (nc <= 0) continue;
+            const int used = nc < units ? nc : units;
+            const long inflight = static_cast<long>(nc) * ns < units ? static_cast<long>(nc) * ns : units;
+            const long score = inflight * C * 4 + used;  // slices in flight, then clusters used
+            if (score > best) {
+                best = score;
+                p = {C, sb, smem, 0, used, ns};
+            }
         }
     }
-    return false;
+    return best > 0;
 }
 
-int launch(const void *func, const Plan &p, int units, void *args, mtp_stream_t stream) {
+// Persistent TV kernel: two target slots, nres (>= 2, ideally gamma) draft
+// slots and gamma rows of indicator bits per CTA.
+bool plan_tv(int dev, const void *func, int V, int es, int gamma, int units, Plan &p) {
+    const int forced = env_cluster();
+    const int cap_nres = env_int("MTP_RS_TV_NRES");
+    const uint32_t cap = smem_optin(dev);
+    long best = -1;
+    for (int C = 1; C <= MAX_C; ++C) {
+        if (forced && C != forced) continue;
+        const uint32_t sb = slice_buffer_bytes(V, es, C);
+        const uint32_t bitb = static_cast<uint32_t>(gamma) * static_cast<uint32_t>(slice_vectors(V, 16 / es, C));
+        const uint32_t fixed = tv_hdr_bytes() + 2 * sb + ((bitb + 127u) & ~127u);
+        if (fixed + sb > cap) continue;
+        int nres = static_cast<int>((cap - fixed) / sb);
+        if (nres > gamma) nres = gamma;
+        if (cap_nres > 0 && nres > cap_nres) nres = cap_nres;
+        if (nres < 1) continue;
+        // with every draft resident, prefer the smallest footprint that holds them
+        const uint32_t smem = fixed + static_cast<uint32_t>(nres) * sb;
+        const int nc = max_clusters(dev, func, C, smem);
+        if (nc <= 0) continue;
+        const int used = nc < units ? nc : units;
+        // working CTAs, with a penalty for draft slices re-read in the epilogue
+        const long score = static_cast<long>(used) * C * (nres == gamma ? 2 : 1);
+        if (score > best) {
+            best = score;
+            p = {C, sb, smem, nres, used, 1};
+        }
+    }
+    return best > 0;
+}
+
+int launch(const void *func, const Plan &p, void *args, mtp_stream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(units) * static_cast<unsigned>(p.C));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.clusters) * static_cast<unsigned>(p.C));
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -179,7 +212,7 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
     const int es = esize(dtype);
     Plan p;
-    if (!plan_row(dev, func, V, es, p)) return MTP_ERR_NO_DEVICE;
+    if (!plan_row(dev, func, V, es, B, p)) return MTP_ERR_NO_DEVICE;
     VerifyArgs A;
     A.target = target;
     A.draft = draft;
@@ -191,12 +224,13 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     A.V = V;
     A.aligned = (V % (16 / es) == 0) ? 1 : 0;
     A.slice_bytes = p.slice_bytes;
+    A.streams = p.streams;
     A.tokens = tokens;
     A.accept_len = accept_len;
     A.alpha = alpha;
     A.entropy = entropy;
     A.flags = flags;
-    return launch(func, p, B, &A, stream);
+    return launch(func, p, &A, stream);
 }
 
 }  // namespace
@@ -236,7 +270,7 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
     if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
     const int es = esize(dtype);
     Plan p;
-    if (!plan_tv(dev, func, V, es, gamma, p)) return MTP_ERR_NO_DEVICE;
+    if (!plan_tv(dev, func, V, es, gamma, N, p)) return MTP_ERR_NO_DEVICE;
     TVArgs A;
     A.target = target_logits;
     A.draft = draft_logits;
@@ -252,7 +286,27 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
     A.alpha = alpha;
     A.grad = grad_draft_logits;
     A.flags = row_flags;
-    return launch(func, p, N, &A, stream);
+    return launch(func, p, &A, stream);
+}
+
+extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
+                              int *clusters, int *smem_bytes, int *resident_drafts) {
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (op < 0 || op > 3 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
+    const void *func = op == 3 ? tv_kernel(d) : row_kernel(d, op == 0 ? MODE_VERIFY : op == 1 ? MODE_VERIFY_STATS : MODE_STATS);
+    if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
+    Plan p;
+    const bool ok = op == 3 ? plan_tv(dev, func, V, esize(dtype), gamma, units, p)
+                            : plan_row(dev, func, V, esize(dtype), units, p);
+    if (!ok) return MTP_ERR_NO_DEVICE;
+    if (cluster_size) *cluster_size = p.C;
+    if (clusters) *clusters = p.clusters;
+    if (smem_bytes) *smem_bytes = static_cast<int>(p.smem);
+    if (resident_drafts) *resident_drafts = p.nres;
+    return MTP_OK;
 }
 
 extern "C" const char *mtp_status_string(int status) {

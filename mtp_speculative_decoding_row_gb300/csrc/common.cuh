@@ -13,7 +13,7 @@
 
 namespace mtp {
 
-constexpr int NT = 512;        // threads per CTA
+constexpr int NT = 128;        // threads per CTA (>= 128: parameter prefetch uses tids 0..127)
 constexpr int NW = NT / 32;    // warps per CTA
 constexpr int MAX_C = 16;      // largest cluster
 constexpr float LOG2E = 1.4426950408889634f;
@@ -60,11 +60,25 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// try_wait that suspends the thread in hardware until the phase completes or
+// about `ns` nanoseconds pass (no issue slots are spent while suspended).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for an mbarrier phase with a 2 s limit; false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
         if (globaltimer_ns() - t0 > 2000000000ull) return false;
     }
     return true;
@@ -127,6 +141,25 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
     return v;
 }
 
+// Asynchronous 16-byte store into a peer CTA's shared memory; its bytes are
+// counted on the peer's mbarrier (complete_tx).  Both addresses come from
+// mapa (shared::cluster window).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+        "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+        "r"(rbar)
+        : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (completion by cp_async_wait_all
+// in the issuing thread).
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 2^x on the MUFU unit (flushes subnormal results to zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -139,6 +172,13 @@ __device__ __forceinline__ float max_nan(float a, float b) {
     float r;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
+}
+
+// max.NaN on two packed bf16 pairs.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // ------------------------------------------------------- logit storage ----
@@ -159,6 +199,11 @@ struct Store<float> {
         z[1] = __uint_as_float(r.y);
         z[2] = __uint_as_float(r.z);
         z[3] = __uint_as_float(r.w);
+    }
+    // max of the vector's elements (NaN if any element is NaN)
+    __device__ static __forceinline__ float vmax(const uint4 &r) {
+        return max_nan(max_nan(__uint_as_float(r.x), __uint_as_float(r.y)),
+                       max_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
     }
     __device__ static __forceinline__ float scalar(const unsigned char *smem, int idx) {
         return reinterpret_cast<const float *>(smem)[idx];
@@ -181,6 +226,11 @@ struct Store<bf16_t> {
         z[5] = __uint_as_float(r.z & 0xffff0000u);
         z[6] = __uint_as_float(r.w << 16);
         z[7] = __uint_as_float(r.w & 0xffff0000u);
+    }
+    // max of the vector's elements on packed pairs (exact; NaN if any is NaN)
+    __device__ static __forceinline__ float vmax(const uint4 &r) {
+        const uint32_t m = bmax2_nan(bmax2_nan(r.x, r.y), bmax2_nan(r.z, r.w));
+        return max_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
     }
     __device__ static __forceinline__ float scalar(const unsigned char *smem, int idx) {
         return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(smem)[idx]) << 16);
@@ -273,11 +323,206 @@ struct Soft {
 
 __device__ __forceinline__ Soft soft_empty() { return {-INFINITY, 0.f, 0.f}; }
 
-template <int N, bool ENT>
-__device__ __forceinline__ void soft_add(Soft &a, const float (&z)[N], float k, bool &bad) {
-    float vm = z[0];
+// ---------------------------------------------- packed float pairs (f32x2) --
+
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The two elements of a 32-bit word of the image as floats: bf16 pair
+// (exact widening) or, for float32 storage, the word itself (lo) and the next.
+__device__ __forceinline__ uint64_t bf16pair_f2(uint32_t x) {
+    return f2pack(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+// Exact path: softmax partial of this thread's vectors j = tid, tid + NT, ...
+// < nvec of one row slice, in two passes over shared memory: (1) the exact
+// maximum m (NaN-propagating; a NaN or +inf sets `bad`), (2)
+// s = sum 2^{(z - m) k} and, with ENT, s1 = sum 2^{(z - m) k} (z - m) k.
+template <typename Tin, bool ENT>
+__device__ __forceinline__ Soft thread_soft_exact(const unsigned char *buf, int nvec, float k, bool &bad) {
+    Soft a = soft_empty();
+    float m;
+    if (Store<Tin>::ES == 2) {
+        uint32_t m2 = 0xff80ff80u;  // (-inf, -inf)
+        for (int j = threadIdx.x; j < nvec; j += NT) {
+            const uint4 r = vec_at(buf, j);
+            m2 = bmax2_nan(m2, bmax2_nan(bmax2_nan(r.x, r.y), bmax2_nan(r.z, r.w)));
+        }
+        m = max_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
+    } else {
+        m = -INFINITY;
+        for (int j = threadIdx.x; j < nvec; j += NT) {
+            const uint4 r = vec_at(buf, j);
+            m = max_nan(m, max_nan(max_nan(__uint_as_float(r.x), __uint_as_float(r.y)),
+                                   max_nan(__uint_as_float(r.z), __uint_as_float(r.w))));
+        }
+    }
+    if (!(m < INFINITY)) {  // NaN or +inf in the slice
+        bad = true;
+        return a;
+    }
+    if (m == -INFINITY) return a;  // nothing but -inf (or no elements)
+    a.m = m;
+    const float mk = m * k;
+    const uint64_t K2 = f2pack(k, k), NMK2 = f2pack(-mk, -mk);
+    uint64_t acc = f2pack(0.f, 0.f), acc1 = f2pack(0.f, 0.f);
+    for (int j = threadIdx.x; j < nvec; j += NT) {
+        const uint4 r = vec_at(buf, j);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        if (Store<Tin>::ES == 2) {
 #pragma unroll
-    for (int j = 1; j < N; ++j) vm = max_nan(vm, z[j]);
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t d2 = f2fma(bf16pair_f2(w[q]), K2, NMK2);
+                float d0, d1;
+                f2unpack(d2, d0, d1);
+                if (ENT) {
+                    d0 = fmaxf(d0, -256.f);
+                    d1 = fmaxf(d1, -256.f);
+                }
+                const float e0 = ex2(d0), e1 = ex2(d1);
+                const uint64_t e2 = f2pack(e0, e1);
+                acc = f2add(acc, e2);
+                if (ENT) acc1 = f2fma(e2, f2pack(d0, d1), acc1);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint64_t z2 = f2pack(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1]));
+                const uint64_t d2 = f2fma(z2, K2, NMK2);
+                float d0, d1;
+                f2unpack(d2, d0, d1);
+                if (ENT) {
+                    d0 = fmaxf(d0, -256.f);
+                    d1 = fmaxf(d1, -256.f);
+                }
+                const float e0 = ex2(d0), e1 = ex2(d1);
+                const uint64_t e2 = f2pack(e0, e1);
+                acc = f2add(acc, e2);
+                if (ENT) acc1 = f2fma(e2, f2pack(d0, d1), acc1);
+            }
+        }
+    }
+    float s0, s1v, t0, t1;
+    f2unpack(acc, s0, s1v);
+    a.s = s0 + s1v;
+    if (ENT) {
+        f2unpack(acc1, t0, t1);
+        a.s1 = t0 + t1;
+    }
+    return a;
+}
+
+// Sum of 2^{z k - mk} over the VEC elements of one vector into two
+// accumulators (and, with ENT, of 2^{d} d with d = z k - mk, clamped).
+template <typename Tin, bool ENT>
+__device__ __forceinline__ void vec_expsum(const uint4 &r, float k, float mk, float &s0, float &s1, float &t0,
+                                           float &t1) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float z0, z1;
+        if (Store<Tin>::ES == 2) {
+            z0 = __uint_as_float(w[q] << 16);
+            z1 = __uint_as_float(w[q] & 0xffff0000u);
+        } else {
+            if (q & 1) continue;
+            z0 = __uint_as_float(w[q]);
+            z1 = __uint_as_float(w[q + 1]);
+        }
+        float d0 = fmaf(z0, k, -mk), d1 = fmaf(z1, k, -mk);
+        if (ENT) {
+            d0 = fmaxf(d0, -256.f);
+            d1 = fmaxf(d1, -256.f);
+        }
+        const float e0 = ex2(d0), e1 = ex2(d1);
+        s0 += e0;
+        s1 += e1;
+        if (ENT) {
+            t0 = fmaf(e0, d0, t0);
+            t1 = fmaf(e1, d1, t1);
+        }
+    }
+}
+
+template <typename Tin, bool ENT>
+__device__ __noinline__ Soft thread_soft_exact_call(const unsigned char *buf, int nvec, float k, bool &bad) {
+    return thread_soft_exact<Tin, ENT>(buf, nvec, k, bad);
+}
+
+// Softmax partial of this thread's vectors of one row slice (see
+// thread_soft_exact for the definition).  With ENT (entropy) the exact path
+// always runs: with a reference below the maximum, ln Z and the entropy sum
+// would both be large and cancel.  Otherwise, fast path: one pass with the
+// reference m = max of the thread's first vector instead of the exact
+// maximum; any reference gives the same normaliser after the rescaled merge,
+// and the pass is kept only if its sum stays finite and below 2^64 (no
+// overflow; NaN or +inf make it non-finite).  Otherwise the exact two-pass
+// path runs, which also flags NaN / +inf.
+template <typename Tin, bool ENT>
+__device__ __forceinline__ Soft thread_soft(const unsigned char *buf, int nvec, float k, bool &bad) {
+    if (ENT) return thread_soft_exact<Tin, ENT>(buf, nvec, k, bad);
+    const int j0 = threadIdx.x;
+    if (j0 >= nvec) return soft_empty();
+    const uint4 first = vec_at(buf, j0);
+    float mref;
+    if (Store<Tin>::ES == 2) {
+        uint32_t m2;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(first.x), "r"(first.y));
+        uint32_t m3;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(m3) : "r"(first.z), "r"(first.w));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(m2), "r"(m3));
+        mref = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
+    } else {
+        mref = fmaxf(fmaxf(__uint_as_float(first.x), __uint_as_float(first.y)),
+                     fmaxf(__uint_as_float(first.z), __uint_as_float(first.w)));
+    }
+    if (mref > -INFINITY && mref < INFINITY) {
+        const float mk = mref * k;
+        float s0 = 0.f, s1 = 0.f, t0 = 0.f, t1 = 0.f;
+        int j = j0;
+        for (; j + 3 * NT < nvec; j += 4 * NT) {
+            const uint4 r0 = vec_at(buf, j), r1 = vec_at(buf, j + NT), r2 = vec_at(buf, j + 2 * NT),
+                        r3 = vec_at(buf, j + 3 * NT);
+            vec_expsum<Tin, ENT>(r0, k, mk, s0, s1, t0, t1);
+            vec_expsum<Tin, ENT>(r1, k, mk, s0, s1, t0, t1);
+            vec_expsum<Tin, ENT>(r2, k, mk, s0, s1, t0, t1);
+            vec_expsum<Tin, ENT>(r3, k, mk, s0, s1, t0, t1);
+        }
+        for (; j < nvec; j += NT) vec_expsum<Tin, ENT>(vec_at(buf, j), k, mk, s0, s1, t0, t1);
+        const float s = s0 + s1;
+        if (s < 1.8e19f) {  // finite, no NaN, far from overflow after merging
+            Soft a;
+            a.m = mref;
+            a.s = s;
+            a.s1 = ENT ? (t0 + t1) : 0.f;
+            return a;
+        }
+    }
+    return thread_soft_exact_call<Tin, ENT>(buf, nvec, k, bad);
+}
+
+// Add one vector of logits z (its max vm, NaN if any element is NaN).
+template <int N, bool ENT>
+__device__ __forceinline__ void soft_add(Soft &a, const float (&z)[N], float vm, float k, bool &bad) {
     if (!(vm < INFINITY)) {  // NaN or +inf
         bad = true;
         return;
@@ -304,44 +549,29 @@ __device__ __forceinline__ void soft_add(Soft &a, const float (&z)[N], float k, 
     }
 }
 
-// Symmetric merge: merge(a, b) and merge(b, a) are bitwise equal.
+// Lane `lane` of warp 0 merges the per-thread partials lane, lane+32, ...
+// (NT/32 of them) stored as m[], s[], s1[] columns in shared memory.
 template <bool ENT>
-__device__ __forceinline__ Soft soft_merge(const Soft &a, const Soft &b, float k) {
-    Soft r;
-    r.m = fmaxf(a.m, b.m);
-    if (r.m == -INFINITY) return soft_empty();
-    float sa = 0.f, sb = 0.f, ta = 0.f, tb = 0.f;
-    if (a.s != 0.f) {
-        const float dl = (r.m - a.m) * k;
-        const float sc = ex2(-dl);
-        sa = a.s * sc;
-        if (ENT) ta = sc * (a.s1 - dl * a.s);
-    }
-    if (b.s != 0.f) {
-        const float dl = (r.m - b.m) * k;
-        const float sc = ex2(-dl);
-        sb = b.s * sc;
-        if (ENT) tb = sc * (b.s1 - dl * b.s);
-    }
-    r.s = sa + sb;
-    r.s1 = ENT ? (ta + tb) : 0.f;
-    return r;
-}
-
-template <bool ENT>
-__device__ __forceinline__ Soft soft_shfl_xor(const Soft &a, int mask) {
-    Soft o;
-    o.m = __shfl_xor_sync(FULL, a.m, mask);
-    o.s = __shfl_xor_sync(FULL, a.s, mask);
-    o.s1 = ENT ? __shfl_xor_sync(FULL, a.s1, mask) : 0.f;
-    return o;
-}
-
-template <bool ENT>
-__device__ __forceinline__ Soft soft_warp_allreduce(Soft a, float k) {
+__device__ __forceinline__ Soft soft_lane_merge(const float *m, const float *s, const float *s1, int lane, float k) {
+    float M = m[lane];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = soft_merge<ENT>(a, soft_shfl_xor<ENT>(a, o), k);
-    return a;
+    for (int q = 1; q < NW; ++q) M = fmaxf(M, m[lane + 32 * q]);
+    Soft r;
+    r.m = M;
+    r.s = 0.f;
+    r.s1 = 0.f;
+    if (M == -INFINITY) return r;
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+        const float sq = s[lane + 32 * q];
+        if (sq != 0.f) {
+            const float dl = (M - m[lane + 32 * q]) * k;
+            const float sc = ex2(-dl);
+            r.s += sq * sc;
+            if (ENT) r.s1 += sc * (s1[lane + 32 * q] - dl * sq);
+        }
+    }
+    return r;
 }
 
 // Symmetric butterfly sum (every lane ends with the same bits).
@@ -351,10 +581,77 @@ __device__ __forceinline__ float warp_allsum(float v) {
     return v;
 }
 
+__device__ __forceinline__ float warp_allmax(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+
+// Warp reduction of softmax partials: exact max over the lanes, one rescale
+// per lane, then butterfly sums.  Every lane ends with the same bits.
+template <bool ENT>
+__device__ __forceinline__ Soft soft_warp_allreduce(const Soft &a, float k) {
+    Soft r;
+    r.m = warp_allmax(a.m);
+    float s = 0.f, s1 = 0.f;
+    if (r.m != -INFINITY && a.s != 0.f) {
+        const float dl = (r.m - a.m) * k;
+        const float sc = ex2(-dl);
+        s = a.s * sc;
+        if (ENT) s1 = sc * (a.s1 - dl * a.s);
+    }
+    r.s = warp_allsum(s);
+    r.s1 = ENT ? warp_allsum(s1) : 0.f;
+    return r;
+}
+
 __device__ __forceinline__ int warp_allor(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(FULL, v, o);
     return v;
+}
+
+// ------------------------------------------------------ cluster exchange --
+//
+// All-gather of one record (XW words) per CTA.  Warp 0 of every CTA pushes
+// its record into slot `round % XR` of every peer with st.async; each CTA
+// arms its own mbarrier for C records and waits (bounded).  A round is sent
+// only after the previous round of the same CTA completed and every warp
+// passed a __syncthreads, so a slot is never overwritten while it is read.
+constexpr int XR = 2;   // ring of exchange slots (one round outstanding at a time)
+constexpr int XW = 8;   // words per record
+
+struct Xchg {
+    float rec[XR][MAX_C][XW];
+    unsigned long long bar[XR];
+};
+
+__device__ __forceinline__ void xchg_init(Xchg &x) {
+    for (int s = 0; s < XR; ++s) mbar_init(smem_addr(&x.bar[s]), 1);
+}
+
+// Every thread calls; warp 0 holds the record `v` (same value in all its
+// lanes).  Returns the slot to read (records 0..C-1); `ok` is false when the
+// wait gave up.
+template <int W>
+__device__ __forceinline__ int xchg_round(Xchg &x, int &round, const float (&v)[W], int C, int rank, bool &ok) {
+    static_assert(W % 4 == 0 && W <= XW, "record width");
+    const int slot = round % XR;
+    const uint32_t par = static_cast<uint32_t>(round / XR) & 1u;
+    const uint32_t bar = smem_addr(&x.bar[slot]);
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        if (lane < C) {
+            const uint32_t raddr = map_rank(smem_addr(&x.rec[slot][rank][0]), lane);
+            const uint32_t rbar = map_rank(bar, lane);
+#pragma unroll
+            for (int q = 0; q < W / 4; ++q) st_async_v4(raddr + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], rbar);
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(C * W * 4));
+    }
+    ok = __syncthreads_and(mbar_wait_bounded(bar, par) ? 1 : 0) != 0;  // same verdict in every thread
+    ++round;
+    return slot;
 }
 
 // Inclusive prefix sum across the warp (Hillis-Steele).

@@ -19,6 +19,7 @@ struct VerifyArgs {
     int B, gamma, V;
     int aligned;            // every row starts on 16 bytes and V is whole vectors
     uint32_t slice_bytes;   // shared bytes of one row slice
+    int streams;            // sequences in flight per CTA (1 or 2)
     int32_t *tokens;        // [B, gamma+1]      (verify modes)
     int32_t *accept_len;    // [B]               (verify modes)
     float *alpha;           // [B, gamma]        (stats modes)
@@ -40,8 +41,9 @@ struct TVArgs {
     int32_t *flags;         // [N] or null
 };
 
-// Shared-memory header bytes in front of the slice buffers.
-constexpr uint32_t HDR_BYTES = 4096;
+// Shared-memory header bytes in front of the slice buffers of each kernel.
+uint32_t row_hdr_bytes();
+uint32_t tv_hdr_bytes();
 
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);

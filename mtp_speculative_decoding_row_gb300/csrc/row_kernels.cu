@@ -1,21 +1,24 @@
 // row_kernels.cu -- batched MTP rejection-sampling verification and
 // per-position row statistics on sm_103a.
 //
-// One thread-block cluster of C CTAs per sequence.  For each position the
-// cluster bulk-loads the target row (and the draft row) slice by slice into
-// shared memory, forms the temperature-scaled softmax normalisers with an
-// online max/sum pass, combines the CTA partials through DSMEM, and then
-// (method: "Breaking Entropy Bounds: Accelerating RL Training via MTP with
-// Rejection Sampling", §2 "Acceptance methods" and App. G.1; "EntMTP",
-// Related Work "Speculative Decoding"):
-//   - accepts draft y_i iff u_i q_i(y_i) < p_i(y_i), tested as
+// Persistent thread-block clusters of C CTAs.  Cluster c owns sequences
+// c, c + NC, c + 2 NC, ... and keeps two of them ("streams") in flight: while
+// one stream's unit (the target row, plus the draft row, of one position) is
+// being reduced and decided, the other stream's next unit is arriving by bulk
+// copy.  Each CTA holds its vocabulary slice of the unit in shared memory,
+// forms the temperature-scaled softmax normalisers in one online pass, and
+// the cluster all-gathers the CTA partials with DSMEM pushes (st.async onto
+// the peers' mbarriers).  Then (method: "Breaking Entropy Bounds:
+// Accelerating RL Training via MTP with Rejection Sampling", §2 "Acceptance
+// methods" and App. G.1; "EntMTP", Related Work "Speculative Decoding"):
+//   - draft y_i is accepted iff u_i q_i(y_i) < p_i(y_i), tested as
 //     log2 u_i + log2 q_i(y_i) < log2 p_i(y_i);
-//   - at the first rejection draws the replacement from norm(max(0, p - q))
-//     by a two-pass inverse CDF over the slices still held on chip;
-//   - after gamma accepts draws the bonus token from p_gamma the same way;
-//   - optionally forms alpha_i = sum_v min(p_i, q_i) (§3, §8) and
-//     H(p_i) = -sum_v p log p for every position.
-// Rows after the stop are never loaded unless statistics are requested.
+//   - at the first rejection the replacement is drawn from
+//     norm(max(0, p - q)) by a two-pass inverse CDF over the slices still
+//     held on chip; after gamma accepts the bonus token is drawn from p_gamma;
+//   - optionally alpha_i = sum_v min(p_i, q_i) (§3, §8) and
+//     H(p_i) = -sum_v p log p are formed for every position.
+// Without statistics no row after the stop is ever loaded.
 #include <cstddef>
 
 #include "common.cuh"
@@ -23,140 +26,110 @@
 
 namespace mtp {
 
-struct alignas(16) Rec {
-    float tm, ts, ts1, dm, ds, zty, zdy, x0;
-    int hasy, bad, tok, pad0;
-    float x1, pad1, pad2, pad3;
+struct StreamSt {
+    int active;   // stream holds a sequence
+    int b;        // sequence
+    int i;        // position of the unit in flight
+    int n;        // accepted drafts
+    int stopped;  // decision chain finished
+    int flags;    // row flags
+    int drawn;    // residual / bonus token
+    int armed;    // a bulk copy is in flight on the stream's barrier
+    uint32_t ph;  // parity of the stream's load barrier
+    int writer;   // cluster rank that writes the sequence's outputs
+    int pad[2];
 };
-static_assert(sizeof(Rec) == 64, "record layout");
 
 struct RowShared {
-    Rec rec[2];               // cluster exchange slots (alternating)
-    float wred[NW][8];        // per-warp partials
-    float comb[8];            // cluster-combined values (broadcast)
-    int combi[4];
-    float segtot[NW];         // per-warp CDF segment totals
-    float ctatot[MAX_C];      // per-CTA residual totals (rank order)
+    Xchg x;
+    float tpart[6][NT];     // per-thread partials (columns)
+    float segtot[NW];       // per-warp CDF segment totals
+    int sampi[4];
     float sampf[4];
-    int sampi[8];
-    int tok[MAX_GAMMA + 1];   // accepted draft ids
-    float alpha[MAX_GAMMA];
-    float ent[MAX_GAMMA + 1];
-    unsigned long long bar[2];
+    StreamSt st[2];
+    int tok[2][MAX_GAMMA + 1];
+    float alpha[2][MAX_GAMMA];
+    float ent[2][MAX_GAMMA + 1];
+    // per-stream sequence parameters, prefetched when the stream takes a sequence
+    float T[2];
+    int ids[2][MAX_GAMMA];
+    float u[2][MAX_GAMMA + 1];
+    unsigned long long lbar[2];  // load barriers, one per stream
 };
-static_assert(sizeof(RowShared) <= HDR_BYTES, "shared header too large");
+constexpr uint32_t HDR_BYTES = (sizeof(RowShared) + 127u) & ~127u;
+uint32_t row_hdr_bytes() { return HDR_BYTES; }
 
-// ------------------------------------------------------------ combines -----
+constexpr int ERR_BITS = F_NONFINITE | F_BAD_ID | F_BAD_TEMP | F_BAD_UNIFORM | F_TIMEOUT;
 
-// Block + cluster combine of the target/draft softmax partials and of the
-// logits at the draft id (held by exactly one CTA).  Results in all threads.
+// ------------------------------------------------------------ reductions ---
+
+// Per-thread softmax partials -> CTA partial in every lane of warp 0: every
+// thread stores its partials (column layout), warp 0 merges NT/32 of them per
+// lane and finishes with one butterfly.
 template <bool ENT>
-__device__ __forceinline__ void combine_soft(RowShared &sh, Soft at, Soft ad, int bad, float zty, float zdy,
-                                             int hasy, float k, int &slot, int C, Soft &Ct, Soft &Cd, int &cbad,
-                                             float &Zty, float &Zdy) {
+__device__ __forceinline__ void block_soft(float (*tp)[NT], Soft &at, Soft &ad, int &bad, float k) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    at = soft_warp_allreduce<ENT>(at, k);
-    ad = soft_warp_allreduce<false>(ad, k);
-    bad = warp_allor(bad);
-    if (lane == 0) {
-        float *w = sh.wred[warp];
-        w[0] = at.m;
-        w[1] = at.s;
-        w[2] = at.s1;
-        w[3] = ad.m;
-        w[4] = ad.s;
-        w[5] = __int_as_float(bad);
-    }
+    tp[0][tid] = at.m;
+    tp[1][tid] = at.s;
+    tp[2][tid] = at.s1;
+    tp[3][tid] = ad.m;
+    tp[4][tid] = ad.s;
+    tp[5][tid] = __int_as_float(bad);
     __syncthreads();
     if (warp == 0) {
-        Soft a = soft_empty(), d = soft_empty();
+        const Soft a = soft_lane_merge<ENT>(tp[0], tp[1], tp[2], lane, k);
+        const Soft d = soft_lane_merge<false>(tp[3], tp[4], tp[4], lane, k);
         int bb = 0;
-        if (lane < NW) {
-            const float *w = sh.wred[lane];
-            a = {w[0], w[1], w[2]};
-            d = {w[3], w[4], 0.f};
-            bb = __float_as_int(w[5]);
-        }
-        a = soft_warp_allreduce<ENT>(a, k);
-        d = soft_warp_allreduce<false>(d, k);
-        bb = warp_allor(bb);
-        if (lane == 0) {
-            Rec &r = sh.rec[slot];
-            r.tm = a.m;
-            r.ts = a.s;
-            r.ts1 = a.s1;
-            r.dm = d.m;
-            r.ds = d.s;
-            r.zty = zty;
-            r.zdy = zdy;
-            r.hasy = hasy;
-            r.bad = bb;
-        }
+#pragma unroll
+        for (int q = 0; q < NW; ++q) bb |= __float_as_int(tp[5][lane + 32 * q]);
+        at = soft_warp_allreduce<ENT>(a, k);
+        ad = soft_warp_allreduce<false>(d, k);
+        bad = warp_allor(bb);
     }
-    cluster_sync();
-    if (warp == 0) {
-        Soft a = soft_empty(), d = soft_empty();
-        int bb = 0, hy = 0;
-        float zt = 0.f, zd = 0.f;
-        if (lane < C) {
-            const uint32_t base = map_rank(smem_addr(&sh.rec[slot]), lane);
-            a.m = ld_cluster_f32(base + offsetof(Rec, tm));
-            a.s = ld_cluster_f32(base + offsetof(Rec, ts));
-            a.s1 = ld_cluster_f32(base + offsetof(Rec, ts1));
-            d.m = ld_cluster_f32(base + offsetof(Rec, dm));
-            d.s = ld_cluster_f32(base + offsetof(Rec, ds));
-            zt = ld_cluster_f32(base + offsetof(Rec, zty));
-            zd = ld_cluster_f32(base + offsetof(Rec, zdy));
-            hy = ld_cluster_s32(base + offsetof(Rec, hasy));
-            bb = ld_cluster_s32(base + offsetof(Rec, bad));
-        }
-        a = soft_warp_allreduce<ENT>(a, k);
-        d = soft_warp_allreduce<false>(d, k);
-        bb = warp_allor(bb);
-        const unsigned hm = __ballot_sync(FULL, hy != 0);
-        const int src = hm ? (__ffs(hm) - 1) : 0;
-        zt = __shfl_sync(FULL, zt, src);
-        zd = __shfl_sync(FULL, zd, src);
-        if (lane == 0) {
-            sh.comb[0] = a.m;
-            sh.comb[1] = a.s;
-            sh.comb[2] = a.s1;
-            sh.comb[3] = d.m;
-            sh.comb[4] = d.s;
-            sh.comb[5] = zt;
-            sh.comb[6] = zd;
-            sh.combi[0] = bb;
-        }
-    }
-    __syncthreads();
-    Ct = {sh.comb[0], sh.comb[1], sh.comb[2]};
-    Cd = {sh.comb[3], sh.comb[4], 0.f};
-    Zty = sh.comb[5];
-    Zdy = sh.comb[6];
-    cbad = sh.combi[0];
-    slot ^= 1;
 }
 
-// Block + cluster sum of one value; result in all threads.
-__device__ __forceinline__ float cluster_sum(RowShared &sh, float v, int &slot, int C) {
+// Per-thread sum -> CTA sum in every lane of warp 0.
+__device__ __forceinline__ float block_sum(float (*tp)[NT], float v) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    v = warp_allsum(v);
-    if (lane == 0) sh.wred[warp][0] = v;
+    tp[0][tid] = v;
     __syncthreads();
+    float r = 0.f;
     if (warp == 0) {
-        float x = (lane < NW) ? sh.wred[lane][0] : 0.f;
-        x = warp_allsum(x);
-        if (lane == 0) sh.rec[slot].x0 = x;
+#pragma unroll
+        for (int q = 0; q < NW; ++q) r += tp[0][lane + 32 * q];
+        r = warp_allsum(r);
     }
-    cluster_sync();
-    if (warp == 0) {
-        float x = (lane < C) ? ld_cluster_f32(map_rank(smem_addr(&sh.rec[slot].x0), lane)) : 0.f;
-        x = warp_allsum(x);
-        if (lane == 0) sh.comb[7] = x;
+    return r;
+}
+
+// Combine the C softmax records of an exchange slot (every warp, every lane).
+template <bool ENT>
+__device__ __forceinline__ void gather_soft(const Xchg &x, int slot, int C, float k, Soft &Ct, Soft &Cd, int &bits,
+                                            float &zty, float &zdy) {
+    const int lane = threadIdx.x & 31;
+    Soft a = soft_empty(), d = soft_empty();
+    int bb = 0;
+    float zt = 0.f, zd = 0.f;
+    if (lane < C) {
+        const float *r = x.rec[slot][lane];
+        a = {r[0], r[1], r[2]};
+        d = {r[3], r[4], 0.f};
+        zt = r[5];
+        zd = r[6];
+        bb = __float_as_int(r[7]);
     }
-    __syncthreads();
-    slot ^= 1;
-    return sh.comb[7];
+    Ct = soft_warp_allreduce<ENT>(a, k);
+    Cd = soft_warp_allreduce<false>(d, k);
+    const unsigned hm = __ballot_sync(FULL, (bb & 0x100) != 0);
+    const int src = hm ? (__ffs(hm) - 1) : 0;
+    zty = __shfl_sync(FULL, zt, src);
+    zdy = __shfl_sync(FULL, zd, src);
+    bits = warp_allor(bb & 0xff);
+}
+
+__device__ __forceinline__ float gather_sum(const Xchg &x, int slot, int C) {
+    const int lane = threadIdx.x & 31;
+    return warp_allsum(lane < C ? x.rec[slot][lane][0] : 0.f);
 }
 
 // ------------------------------------------------------------- sampling ----
@@ -188,104 +161,93 @@ __device__ __forceinline__ float vec_sum(const float (&w)[VEC]) {
     return s;
 }
 
-// Two-pass inverse CDF over the whole row held by the cluster: pass one
-// forms the per-warp, per-CTA and total masses; the draw is the smallest
-// vocabulary index whose running sum exceeds u * R (ascending index order:
-// CTA rank, warp segment, 32-vector round, lane, element).  If rounding
-// leaves no such index, the last index with positive weight in the selected
-// unit is taken.  Returns the token in every thread, or -2 when R == 0.
+struct SampleOut {
+    int status;  // 0 drawn, -2 the weights sum to zero, -3 an exchange gave up
+    int writer;  // rank of the CTA that found the token (same in every CTA)
+    int token;   // the token, valid in the writer CTA
+};
+
+// Two-pass inverse CDF over the row held by the cluster.  Pass one forms the
+// per-warp segment totals, the CTA total and (exchange) every CTA's total;
+// the draw is the smallest vocabulary index whose running sum exceeds u * R,
+// in ascending index order (CTA rank, warp segment, 32-vector round, lane,
+// element).  If rounding leaves no such index in the selected unit, the last
+// index of that unit with positive weight is taken.  Only the selected CTA
+// walks its segment; it keeps the token and writes the sequence's outputs.
 template <typename Tin, int WMODE>
-__device__ int cluster_sample(RowShared &sh, const unsigned char *tb, const unsigned char *db, const Slice &s,
-                              float k, float ct, float cd, float u, int &slot, int C, int rank) {
+__device__ __noinline__ SampleOut cluster_sample(RowShared &sh, int &round, const unsigned char *tb,
+                                                 const unsigned char *db, const Slice &s, float k, float ct, float cd,
+                                                 float u, int C, int rank) {
     constexpr int VEC = Store<Tin>::VEC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nvw = (s.nvec + NW - 1) / NW;
     const int a0 = min(s.nvec, warp * nvw), a1 = min(s.nvec, a0 + nvw);
+    SampleOut out = {0, 0, -1};
 
-    // pass one: segment totals
-    float run = 0.f;
-    for (int base = a0; base < a1; base += 32) {
-        const int j = base + lane;
-        float vs = 0.f;
-        if (j < a1) {
-            float w[VEC];
-            vec_weights<Tin, WMODE>(tb, db, j, k, ct, cd, w);
-            vs = vec_sum<VEC>(w);
-        }
-        const float inc = warp_incl_scan(vs);
-        run += __shfl_sync(FULL, inc, 31);
+    // pass one: per-thread sums, one reduction per warp segment
+    float part = 0.f;
+    for (int j = a0 + lane; j < a1; j += 32) {
+        float w[VEC];
+        vec_weights<Tin, WMODE>(tb, db, j, k, ct, cd, w);
+        part += vec_sum<VEC>(w);
     }
-    if (lane == 0) sh.segtot[warp] = run;
+    part = warp_allsum(part);
+    if (lane == 0) sh.segtot[warp] = part;
     __syncthreads();
-    if (tid == 0) {
-        float tot = 0.f;
+    float tot = 0.f;
+    if (warp == 0)
         for (int w = 0; w < NW; ++w) tot += sh.segtot[w];
-        sh.rec[slot].x0 = tot;
+    float rec[4] = {tot, 0.f, 0.f, 0.f};
+    bool ok;
+    const int slot = xchg_round<4>(sh.x, round, rec, C, rank, ok);
+    if (!ok) {
+        out.status = -3;
+        return out;
     }
-    cluster_sync();
-    if (warp == 0) {
-        if (lane < C) sh.ctatot[lane] = ld_cluster_f32(map_rank(smem_addr(&sh.rec[slot].x0), lane));
-        __syncwarp();
-        if (lane == 0) {
-            float R = 0.f;
-            for (int r = 0; r < C; ++r) R += sh.ctatot[r];
-            int rs = -1, last = 0;
-            float rem = u * R;
-            if (R > 0.f) {
-                for (int r = 0; r < C; ++r) {
-                    const float vr = sh.ctatot[r];
-                    if (vr > rem) {
-                        rs = r;
-                        break;
-                    }
-                    rem -= vr;
-                }
-                if (rs < 0) {
-                    last = 1;
-                    for (int r = 0; r < C; ++r)
-                        if (sh.ctatot[r] > 0.f) rs = r;
-                }
+    // every thread: rank-ordered scan of the CTA totals
+    float R = 0.f;
+    for (int r = 0; r < C; ++r) R += sh.x.rec[slot][r][0];
+    int rs = -1, last = 0;
+    float rem = u * R;
+    if (R > 0.f) {
+        for (int r = 0; r < C; ++r) {
+            const float vr = sh.x.rec[slot][r][0];
+            if (vr > rem) {
+                rs = r;
+                break;
             }
-            sh.sampi[0] = rs;
-            sh.sampi[1] = last;
-            sh.sampf[0] = rem;
+            rem -= vr;
+        }
+        if (rs < 0) {
+            last = 1;
+            for (int r = 0; r < C; ++r)
+                if (sh.x.rec[slot][r][0] > 0.f) rs = r;
         }
     }
-    __syncthreads();
-    slot ^= 1;
-    const int rs = sh.sampi[0];
-    if (rs < 0) return -2;
-
-    int found = -1;
+    if (rs < 0) {
+        out.status = -2;
+        return out;
+    }
+    out.writer = rs;
     if (rank == rs) {
-        if (tid == 0) {
-            int lm = sh.sampi[1];
-            float rem = sh.sampf[0];
-            int ws = -1;
-            if (!lm) {
-                for (int w = 0; w < NW; ++w) {
-                    const float t = sh.segtot[w];
-                    if (t > rem) {
-                        ws = w;
-                        break;
-                    }
-                    rem -= t;
+        // warp segment (same scan in every thread of this CTA)
+        int lm = last, ws = -1;
+        if (!lm) {
+            for (int w = 0; w < NW; ++w) {
+                const float t = sh.segtot[w];
+                if (t > rem) {
+                    ws = w;
+                    break;
                 }
+                rem -= t;
             }
-            if (ws < 0) {
-                lm = 1;
-                for (int w = 0; w < NW; ++w)
-                    if (sh.segtot[w] > 0.f) ws = w;
-            }
-            sh.sampi[2] = ws;
-            sh.sampi[3] = lm;
-            sh.sampf[1] = rem;
         }
-        __syncthreads();
-        const int ws = sh.sampi[2];
+        if (ws < 0) {
+            lm = 1;
+            for (int w = 0; w < NW; ++w)
+                if (sh.segtot[w] > 0.f) ws = w;
+        }
         if (warp == ws) {
-            int lm = sh.sampi[3];
-            float rem = sh.sampf[1];
             const int b0 = min(s.nvec, ws * nvw), b1 = min(s.nvec, b0 + nvw);
             int tok = -1;
             if (!lm) {
@@ -301,13 +263,13 @@ __device__ int cluster_sample(RowShared &sh, const unsigned char *tb, const unsi
                         for (int e = 0; e < VEC; ++e) w[e] = 0.f;
                     }
                     const float inc = warp_incl_scan(vs);
-                    const float tot = __shfl_sync(FULL, inc, 31);
-                    if (tot > rem) {
+                    const float t = __shfl_sync(FULL, inc, 31);
+                    if (t > rem) {
                         const unsigned bal = __ballot_sync(FULL, inc > rem);
                         const int L = __ffs(bal) - 1;
                         float exc = __shfl_up_sync(FULL, inc, 1);
                         if (lane == 0) exc = 0.f;
-                        int t = -1;
+                        int tk = -1;
                         if (lane == L) {
                             float r2 = rem - exc;
                             int ef = -1;
@@ -325,12 +287,12 @@ __device__ int cluster_sample(RowShared &sh, const unsigned char *tb, const unsi
                                 for (int e = 0; e < VEC; ++e)
                                     if (w[e] > 0.f) ef = e;
                             }
-                            t = s.lo + j * VEC + ef;
+                            tk = s.lo + j * VEC + ef;
                         }
-                        tok = __shfl_sync(FULL, t, L);
+                        tok = __shfl_sync(FULL, tk, L);
                         break;
                     }
-                    rem -= tot;
+                    rem -= t;
                 }
                 if (tok < 0) lm = 1;
             }
@@ -350,206 +312,301 @@ __device__ int cluster_sample(RowShared &sh, const unsigned char *tb, const unsi
                 for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(FULL, best, o));
                 tok = best;
             }
-            if (lane == 0) sh.sampi[4] = tok;
+            if (lane == 0) sh.sampi[0] = tok;
         }
-        __syncthreads();
-        found = sh.sampi[4];
+        __syncthreads();  // CTA-uniform branch
+        out.token = sh.sampi[0];
     }
-    // publish the token to every CTA
-    if (tid == 0) sh.rec[slot].tok = (rank == rs) ? found : -1;
-    cluster_sync();
-    if (warp == 0) {
-        int t = (lane < C) ? ld_cluster_s32(map_rank(smem_addr(&sh.rec[slot].tok), lane)) : -1;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t = max(t, __shfl_xor_sync(FULL, t, o));
-        if (lane == 0) sh.sampi[5] = t;
+    return out;
+}
+
+// ----------------------------------------------------------- unit loads ----
+
+template <typename Tin>
+__device__ __forceinline__ const unsigned char *row_ptr(const void *base, size_t row, int V) {
+    return reinterpret_cast<const unsigned char *>(base) + row * static_cast<size_t>(V) * Store<Tin>::ES;
+}
+
+// Start the loads of unit (b, i) of stream `st` (aligned rows: one bulk copy
+// per row slice on the stream's barrier; otherwise loads happen at use).
+template <typename Tin>
+__device__ __forceinline__ void issue_unit(const VerifyArgs &A, StreamSt &st, const Slice &s, unsigned char *tb,
+                                           unsigned char *db, uint32_t bar) {
+    st.armed = 0;
+    if (!A.aligned || s.nvec == 0) return;
+    const int g = A.gamma;
+    const uint32_t bytes = static_cast<uint32_t>(s.nvec) * 16u;
+    const bool has_d = st.i < g;
+    if (threadIdx.x == 0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, has_d ? 2 * bytes : bytes);
+        const size_t lo = static_cast<size_t>(s.lo) * Store<Tin>::ES;
+        bulk_g2s(smem_addr(tb), row_ptr<Tin>(A.target, static_cast<size_t>(st.b) * (g + 1) + st.i, A.V) + lo, bytes,
+                 bar);
+        if (has_d)
+            bulk_g2s(smem_addr(db), row_ptr<Tin>(A.draft, static_cast<size_t>(st.b) * g + st.i, A.V) + lo, bytes, bar);
     }
-    __syncthreads();
-    slot ^= 1;
-    return sh.sampi[5];
+    st.armed = 1;
+}
+
+// Argument checks of stream si's sequence, from its prefetched parameters
+// (the same in every CTA of the cluster).
+__device__ __forceinline__ int validate_seq(const RowShared &sh, int si, int g, int V, bool decide) {
+    const float T = sh.T[si];
+    int f = 0;
+    if (!(T > 0.f) || !(T < INFINITY)) f |= F_BAD_TEMP;
+    if (decide) {
+        for (int i = 0; i < g; ++i) {
+            const int y = sh.ids[si][i];
+            if (y < 0 || y >= V) f |= F_BAD_ID;
+        }
+        for (int i = 0; i <= g; ++i) {
+            const float u = sh.u[si][i];
+            if (!(u >= 0.f && u < 1.f)) f |= F_BAD_UNIFORM;
+        }
+    }
+    return f;
+}
+
+// Stream si takes sequence b: state reset and asynchronous copies of the
+// sequence's temperature, draft ids and uniforms into shared memory (waited
+// for by the issuing threads at the start of the stream's next step).
+__device__ __forceinline__ StreamSt start_seq(const VerifyArgs &A, RowShared &sh, int si, int b, bool decide,
+                                              uint32_t ph) {
+    StreamSt st = {};
+    st.ph = ph;
+    if (b >= A.B) return st;
+    st.active = 1;
+    st.b = b;
+    st.drawn = -1;
+    const int g = A.gamma, tid = threadIdx.x;
+    if (decide && tid <= g) cp_async4(&sh.u[si][tid], A.unif + static_cast<size_t>(b) * (g + 1) + tid);
+    if (decide && tid >= 64 && tid < 64 + g) cp_async4(&sh.ids[si][tid - 64], A.ids + static_cast<size_t>(b) * g + (tid - 64));
+    if (tid == NT - 1) cp_async4(&sh.T[si], A.temp + b);
+    return st;
 }
 
 // ---------------------------------------------------------------- kernel ---
 
 template <typename Tin, int MODE>
-__global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
+__global__ void __launch_bounds__(NT, 4) row_kernel_impl(const VerifyArgs A) {
     using S = Store<Tin>;
-    constexpr int VEC = S::VEC, ES = S::ES;
+    constexpr int VEC = S::VEC;
     constexpr bool STATS = (MODE != MODE_VERIFY);
     constexpr bool DECIDE = (MODE != MODE_STATS);
     extern __shared__ __align__(128) unsigned char smem[];
     RowShared &sh = *reinterpret_cast<RowShared *>(smem);
-    unsigned char *tb = smem + HDR_BYTES;
-    unsigned char *db = tb + A.slice_bytes;
 
     const int tid = threadIdx.x;
     const int C = static_cast<int>(cluster_size());
     const int rank = static_cast<int>(cluster_rank());
-    const int b = static_cast<int>(cluster_id_x());
-    const int g = A.gamma, V = A.V;
-    const uint32_t bar_t = smem_addr(&sh.bar[0]), bar_d = smem_addr(&sh.bar[1]);
+    const int cid = static_cast<int>(cluster_id_x());
+    const int NC = static_cast<int>(gridDim.x) / C;
+    const int g = A.gamma;
+    const Slice s = make_slice<Tin>(A.V, C, rank);
+
+    // stream si: target slice at tbuf(si), draft slice right after it
+    auto tbuf = [&](int si) { return smem + HDR_BYTES + static_cast<size_t>(si) * 2 * A.slice_bytes; };
+
     if (tid == 0) {
-        mbar_init(bar_t, 1);
-        mbar_init(bar_d, 1);
+        xchg_init(sh.x);
+        mbar_init(smem_addr(&sh.lbar[0]), 1);
+        mbar_init(smem_addr(&sh.lbar[1]), 1);
         fence_mbar_init();
     }
-
-    // Argument checks that are the same in every CTA of the cluster.
-    const float T = A.temp[b];
-    int flags = 0;
-    if (!(T > 0.f) || !(T < INFINITY)) flags |= F_BAD_TEMP;
-    if (DECIDE) {
-        for (int i = 0; i < g; ++i) {
-            const int y = A.ids[static_cast<size_t>(b) * g + i];
-            if (y < 0 || y >= V) flags |= F_BAD_ID;
-        }
-        for (int i = 0; i <= g; ++i) {
-            const float u = A.unif[static_cast<size_t>(b) * (g + 1) + i];
-            if (!(u >= 0.f && u < 1.f)) flags |= F_BAD_UNIFORM;
-        }
-    }
+    const int NS = A.streams;  // sequences in flight per CTA
+    int next_seq = cid + NS * NC;
+    StreamSt st0 = start_seq(A, sh, 0, cid, DECIDE, 0);
+    StreamSt st1 = NS > 1 ? start_seq(A, sh, 1, cid + NC, DECIDE, 0) : StreamSt{};
     __syncthreads();
-    cluster_sync();  // every CTA has started: DSMEM is safe from here on
+    cluster_sync();  // peers' barriers are initialised before any push
+    if (st0.active) issue_unit<Tin>(A, st0, s, tbuf(0), tbuf(0) + A.slice_bytes, smem_addr(&sh.lbar[0]));
+    if (st1.active) issue_unit<Tin>(A, st1, s, tbuf(1), tbuf(1) + A.slice_bytes, smem_addr(&sh.lbar[1]));
+    if (tid == 0) {
+        sh.st[0] = st0;
+        sh.st[1] = st1;
+    }
+    int round = 0;
+    bool dead = false;  // an exchange gave up: finish without further work
+    __syncthreads();
 
-    const float k = LOG2E / T;
-    const Slice s = make_slice<Tin>(V, C, rank);
-    int slot = 0, n = 0, drawn = -1;
-    uint32_t ph_t = 0, ph_d = 0;
-    bool stopped = false, pend_t = false, pend_d = false;
+    for (;;) {
+        bool any = false;
+        for (int si = 0; si < NS; ++si) {
+            cp_async_wait_all();  // sequence parameters issued by this thread
+            StreamSt st = sh.st[si];
+            __syncthreads();  // state and parameters visible; everyone has read the state
+            if (!st.active) continue;
+            any = true;
+            unsigned char *tb = tbuf(si), *db = tb + A.slice_bytes;
+            const uint32_t lbar = smem_addr(&sh.lbar[si]);
+            const int b = st.b, i = st.i;
+            bool finish = false;
+            if (i == 0) st.flags |= validate_seq(sh, si, g, A.V, DECIDE);
 
-    if (!flags) {
-        for (int i = 0; i <= g; ++i) {
-            if (!STATS && stopped) break;
-            const bool has_d = i < g;
-            const unsigned char *trow = reinterpret_cast<const unsigned char *>(A.target) +
-                                        (static_cast<size_t>(b) * (g + 1) + i) * static_cast<size_t>(V) * ES;
-            const unsigned char *drow = reinterpret_cast<const unsigned char *>(A.draft) +
-                                        (static_cast<size_t>(b) * g + i) * static_cast<size_t>(V) * ES;
-            fence_proxy_async();
-            const bool arm_t = load_slice<Tin>(s, trow, tb, bar_t, A.aligned != 0);
-            const bool arm_d = has_d && load_slice<Tin>(s, drow, db, bar_d, A.aligned != 0);
-            int tmo = 0;
-            if (arm_t) {
-                if (!mbar_wait_bounded(bar_t, ph_t)) {
-                    tmo = 1;
-                    pend_t = true;
+            if ((st.flags & ERR_BITS) || dead) {
+                finish = true;
+                if (dead) st.flags |= F_TIMEOUT;
+                if (st.armed) {  // drain the copy before the buffers change hands
+                    mbar_wait_bounded(lbar, st.ph);
+                    st.ph ^= 1u;
+                    st.armed = 0;
                 }
-                ph_t ^= 1;
-            }
-            if (arm_d) {
-                if (!mbar_wait_bounded(bar_d, ph_d)) {
-                    tmo = 1;
-                    pend_d = true;
+            } else {
+                const float T = sh.T[si];
+                const float k = LOG2E / T;
+                const bool has_d = i < g;
+                int tmo = 0;
+                if (st.armed) {
+                    if (!mbar_wait_bounded(lbar, st.ph)) tmo = 1;
+                    st.ph ^= 1u;
+                    st.armed = 0;
+                } else if (!A.aligned) {
+                    load_slice<Tin>(s, row_ptr<Tin>(A.target, static_cast<size_t>(b) * (g + 1) + i, A.V), tb, 0, false);
+                    if (has_d) load_slice<Tin>(s, row_ptr<Tin>(A.draft, static_cast<size_t>(b) * g + i, A.V), db, 0, false);
                 }
-                ph_d ^= 1;
-            }
-            __syncthreads();
+                __syncthreads();
 
-            // pass A: online max / normaliser (and entropy sum) per row
-            Soft at = soft_empty(), ad = soft_empty();
-            bool nonfin = false;
-            for (int j = tid; j < s.nvec; j += NT) {
-                float zt[VEC];
-                S::unpack(vec_at(tb, j), zt);
-                soft_add<VEC, STATS>(at, zt, k, nonfin);
-                if (has_d) {
-                    float zd[VEC];
-                    S::unpack(vec_at(db, j), zd);
-                    soft_add<VEC, false>(ad, zd, k, nonfin);
-                }
-            }
-            const bool want_y = DECIDE && has_d && !stopped;
-            const int y = want_y ? A.ids[static_cast<size_t>(b) * g + i] : -1;
-            float zty = 0.f, zdy = 0.f;
-            int hasy = 0;
-            if (tid == 0 && want_y && y >= s.lo && y < s.hi) {
-                zty = S::scalar(tb, y - s.lo);
-                zdy = S::scalar(db, y - s.lo);
-                hasy = 1;
-            }
-            Soft Ct, Cd;
-            int cbad;
-            float Zty, Zdy;
-            combine_soft<STATS>(sh, at, ad, (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0), zty, zdy, hasy,
-                                k, slot, C, Ct, Cd, cbad, Zty, Zdy);
-            int rf = cbad;
-            if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY)) rf |= F_NONFINITE;
-            if (has_d && (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY))) rf |= F_NONFINITE;
-            if (rf) {
-                flags |= rf;
-                break;
-            }
-            const float ct = fmaf(Ct.m, k, log2f(Ct.s));
-            const float cd = has_d ? fmaf(Cd.m, k, log2f(Cd.s)) : 0.f;
-
-            if (STATS) {
-                if (tid == 0) sh.ent[i] = logf(Ct.s) - LN2 * (Ct.s1 / Ct.s);
-                if (has_d) {
-                    float acc = 0.f;
-                    for (int j = tid; j < s.nvec; j += NT) {
-                        float zt[VEC], zd[VEC];
-                        S::unpack(vec_at(tb, j), zt);
-                        S::unpack(vec_at(db, j), zd);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            acc += ex2(fminf(fmaf(zt[e], k, -ct), fmaf(zd[e], k, -cd)));
+                // pass A: online max / normaliser (and entropy sum) per row
+                bool nonfin = false;
+                Soft at = thread_soft<Tin, STATS>(tb, s.nvec, k, nonfin);
+                Soft ad = has_d ? thread_soft<Tin, false>(db, s.nvec, k, nonfin) : soft_empty();
+                const bool want_y = DECIDE && has_d && !st.stopped;
+                const int y = want_y ? sh.ids[si][i] : -1;
+                int bad = (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0);
+                block_soft<STATS>(sh.tpart, at, ad, bad, k);
+                float rec[8];
+                {
+                    float zty = 0.f, zdy = 0.f;
+                    int hasy = 0;
+                    if (want_y && y >= s.lo && y < s.hi) {
+                        zty = S::scalar(tb, y - s.lo);
+                        zdy = S::scalar(db, y - s.lo);
+                        hasy = 0x100;
                     }
-                    const float a = cluster_sum(sh, acc, slot, C);
-                    if (tid == 0) sh.alpha[i] = a;
+                    rec[0] = at.m;
+                    rec[1] = at.s;
+                    rec[2] = at.s1;
+                    rec[3] = ad.m;
+                    rec[4] = ad.s;
+                    rec[5] = zty;
+                    rec[6] = zdy;
+                    rec[7] = __int_as_float(bad | hasy);
                 }
-            }
-
-            if (DECIDE && !stopped) {
-                const float uf = A.unif[static_cast<size_t>(b) * (g + 1) + g];
-                if (has_d) {
-                    const float lp = fmaf(Zty, k, -ct), lq = fmaf(Zdy, k, -cd);
-                    const float u = A.unif[static_cast<size_t>(b) * (g + 1) + i];
-                    if (log2f(u) + lq < lp) {
-                        if (tid == 0) sh.tok[n] = y;
-                        ++n;
-                    } else {
-                        stopped = true;
-                        int t = cluster_sample<Tin, 0>(sh, tb, db, s, k, ct, cd, uf, slot, C, rank);
-                        if (t == -2) {
-                            flags |= F_ZERO_MASS;
-                            t = cluster_sample<Tin, 1>(sh, tb, db, s, k, ct, cd, uf, slot, C, rank);
-                        }
-                        drawn = t;
-                    }
+                bool ok;
+                int slot = xchg_round<8>(sh.x, round, rec, C, rank, ok);
+                Soft Ct, Cd;
+                int cbits;
+                float Zty, Zdy;
+                gather_soft<STATS>(sh.x, slot, C, k, Ct, Cd, cbits, Zty, Zdy);
+                int rf = cbits | (ok ? 0 : F_TIMEOUT);
+                if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY)) rf |= F_NONFINITE;
+                if (has_d && (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY))) rf |= F_NONFINITE;
+                if (!ok) dead = true;
+                if (rf) {
+                    st.flags |= rf;
+                    finish = true;
                 } else {
-                    stopped = true;
-                    drawn = cluster_sample<Tin, 1>(sh, tb, db, s, k, ct, cd, uf, slot, C, rank);
-                }
-                if (stopped && drawn < 0) {
-                    flags |= F_NONFINITE;
-                    break;
+                    const float ct = fmaf(Ct.m, k, log2f(Ct.s));
+                    const float cd = has_d ? fmaf(Cd.m, k, log2f(Cd.s)) : 0.f;
+                    if (STATS) {
+                        if (tid == 0) sh.ent[si][i] = logf(Ct.s) - LN2 * (Ct.s1 / Ct.s);
+                        if (has_d) {
+                            float acc = 0.f;
+                            for (int j = tid; j < s.nvec; j += NT) {
+                                float zt[VEC], zd[VEC];
+                                S::unpack(vec_at(tb, j), zt);
+                                S::unpack(vec_at(db, j), zd);
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e)
+                                    acc += ex2(fminf(fmaf(zt[e], k, -ct), fmaf(zd[e], k, -cd)));
+                            }
+                            float r4[4] = {block_sum(sh.tpart, acc), 0.f, 0.f, 0.f};
+                            const int sl2 = xchg_round<4>(sh.x, round, r4, C, rank, ok);
+                            const float a = gather_sum(sh.x, sl2, C);
+                            if (tid == 0) sh.alpha[si][i] = a;
+                            if (!ok) {
+                                dead = true;
+                                st.flags |= F_TIMEOUT;
+                                finish = true;
+                            }
+                        }
+                    }
+                    if (DECIDE && !st.stopped && !finish) {
+                        const float uf = sh.u[si][g];
+                        SampleOut so = {0, 0, -1};
+                        if (has_d) {
+                            const float lp = fmaf(Zty, k, -ct), lq = fmaf(Zdy, k, -cd);
+                            const float u = sh.u[si][i];
+                            if (log2f(u) + lq < lp) {
+                                if (tid == 0) sh.tok[si][st.n] = y;
+                                ++st.n;
+                            } else {
+                                st.stopped = 1;
+                                so = cluster_sample<Tin, 0>(sh, round, tb, db, s, k, ct, cd, uf, C, rank);
+                                if (so.status == -2) {
+                                    st.flags |= F_ZERO_MASS;
+                                    so = cluster_sample<Tin, 1>(sh, round, tb, db, s, k, ct, cd, uf, C, rank);
+                                }
+                            }
+                        } else {
+                            st.stopped = 1;
+                            so = cluster_sample<Tin, 1>(sh, round, tb, db, s, k, ct, cd, uf, C, rank);
+                        }
+                        if (st.stopped) {
+                            st.drawn = so.token;  // meaningful in the writer CTA
+                            st.writer = so.writer;
+                            if (so.status == -3) {
+                                dead = true;
+                                st.flags |= F_TIMEOUT;
+                            } else if (so.status < 0) {
+                                st.flags |= F_NONFINITE;
+                            }
+                        }
+                    }
+                    if (st.flags & ERR_BITS) finish = true;
+                    if (!(i < g && (STATS || !st.stopped))) finish = true;
                 }
             }
-            __syncthreads();  // every read of the slices is done before they are reloaded
-        }
-    }
 
-    // A copy that outlived its wait must land before this CTA may exit.
-    if (pend_t) mbar_wait_bounded(bar_t, ph_t ^ 1);
-    if (pend_d) mbar_wait_bounded(bar_d, ph_d ^ 1);
-
-    if (rank == 0 && tid == 0) {
-        const bool err = (flags & (F_NONFINITE | F_BAD_ID | F_BAD_TEMP | F_BAD_UNIFORM | F_TIMEOUT)) != 0;
-        if (DECIDE) {
-            for (int j = 0; j <= g; ++j) {
-                int v = -1;
-                if (!err) v = (j < n) ? sh.tok[j] : (j == n ? drawn : -1);
-                A.tokens[static_cast<size_t>(b) * (g + 1) + j] = v;
+            __syncthreads();  // every read of this stream's slices and shared outputs is done
+            if (finish) {
+                if (rank == st.writer && tid == 0) {
+                    const int f = st.flags;
+                    const bool err = (f & ERR_BITS) != 0;
+                    if (DECIDE) {
+                        for (int j = 0; j <= g; ++j) {
+                            int v = -1;
+                            if (!err) v = (j < st.n) ? sh.tok[si][j] : (j == st.n ? st.drawn : -1);
+                            A.tokens[static_cast<size_t>(b) * (g + 1) + j] = v;
+                        }
+                        A.accept_len[b] = err ? -1 : st.n;
+                    }
+                    if (STATS && A.alpha) {
+                        for (int j = 0; j < g; ++j) A.alpha[static_cast<size_t>(b) * g + j] = err ? NAN : sh.alpha[si][j];
+                        for (int j = 0; j <= g; ++j)
+                            A.entropy[static_cast<size_t>(b) * (g + 1) + j] = err ? NAN : sh.ent[si][j];
+                    }
+                    if (A.flags) A.flags[b] = f;
+                }
+                st = start_seq(A, sh, si, next_seq, DECIDE, st.ph);
+                next_seq += NC;
+            } else {
+                st.i = i + 1;
             }
-            A.accept_len[b] = err ? -1 : n;
+            if (st.active && !dead) issue_unit<Tin>(A, st, s, tb, db, lbar);
+            if (tid == 0) sh.st[si] = st;
         }
-        if (STATS && A.alpha) {
-            for (int i = 0; i < g; ++i) A.alpha[static_cast<size_t>(b) * g + i] = err ? NAN : sh.alpha[i];
-            for (int i = 0; i <= g; ++i) A.entropy[static_cast<size_t>(b) * (g + 1) + i] = err ? NAN : sh.ent[i];
-        }
-        if (A.flags) A.flags[b] = flags;
+        __syncthreads();
+        if (!any) break;
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+
+    // Copies that outlived a bounded wait must land before the CTA exits.
+    for (int si = 0; si < NS; ++si) {
+        const StreamSt st = sh.st[si];
+        if (st.armed) mbar_wait_bounded(smem_addr(&sh.lbar[si]), st.ph);
+    }
+    cluster_sync();  // no CTA leaves while a peer may still push into it
 }
 
 const void *row_kernel(int dtype, int mode) {

@@ -2,9 +2,11 @@
 // sm_103a ("Breaking Entropy Bounds: Accelerating RL Training via MTP with
 // Rejection Sampling", §4 "End-to-end TV loss", App. A, App. F).
 //
-// One thread-block cluster per token position t.  For each draft step k the
-// cluster bulk-loads the target and draft row slices into shared memory,
-// forms both softmax normalisers (online max/sum, DSMEM combine), then in one
+// Persistent thread-block clusters; cluster c handles token positions
+// c, c + NC, ...  For each draft step k of a position the cluster bulk-loads
+// the target and draft row slices into shared memory (the next step's pair is
+// already in flight while this one is reduced), forms both softmax
+// normalisers (online max/sum, cluster all-gather by DSMEM push), then in one
 // pass over the on-chip slices accumulates
 //     alpha_k = sum_v min(p_v, q_v),   S_k = sum_v 1[q_v <= p_v] q_v
 // and records the indicator bits.  The draft slices stay on chip.  After the
@@ -13,10 +15,10 @@
 //     dl_t/dalpha_k = -P_{k-1} W_k,  W_k = 1 + alpha_{k+1} W_{k+1}, W_gamma = 1
 // (no division), and the epilogue streams
 //     grad[t,k,j] = grad_scale (dl_t/dalpha_k) (1/T) q_j (1[q_j <= p_j] - S_k)
-// from the resident draft slices and bits.  Each logit is read from HBM once
-// and each gradient entry written once; the softmax is never materialised.
-// When gamma draft slices do not fit on chip, the oldest are re-read from
-// global memory in the epilogue.
+// from the resident draft slices and bits with 16-byte streaming stores.
+// Each logit is read from HBM once and each gradient entry written once; the
+// softmax is never materialised.  When fewer than gamma draft slices fit on
+// chip, the older ones are re-read in the epilogue.
 #include <cstddef>
 
 #include "common.cuh"
@@ -24,132 +26,61 @@
 
 namespace mtp {
 
-struct alignas(16) TRec {
-    float tm, ts, dm, ds, x0, x1;
-    int bad, pad;
-};
-
 struct TVShared {
-    TRec rec[2];
-    float wred[NW][8];
-    float comb[8];
-    int combi[4];
+    Xchg x;
+    float wpart[2][NW][8];
     float cd[MAX_GAMMA];
     float Sk[MAX_GAMMA];
     float ak[MAX_GAMMA];
     float gk[MAX_GAMMA];
     float loss;
-    unsigned long long bar[2];
+    unsigned long long tbar[2];          // target slots
+    unsigned long long dbar[MAX_GAMMA];  // draft slots
 };
-static_assert(sizeof(TVShared) <= HDR_BYTES, "shared header too large");
+constexpr uint32_t HDR_BYTES = (sizeof(TVShared) + 127u) & ~127u;
+uint32_t tv_hdr_bytes() { return HDR_BYTES; }
 
-// Block + cluster combine of target/draft normalisers.  Results in all threads.
-__device__ __forceinline__ void tv_combine_soft(TVShared &sh, Soft at, Soft ad, int bad, float k, int &slot, int C,
-                                                Soft &Ct, Soft &Cd, int &cbad) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Per-thread partials of two rows -> CTA partial in every lane of warp 0.
+__device__ __forceinline__ void block_soft2(float (*wp)[8], Soft &at, Soft &ad, int &bad, float k) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     at = soft_warp_allreduce<false>(at, k);
     ad = soft_warp_allreduce<false>(ad, k);
     bad = warp_allor(bad);
     if (lane == 0) {
-        float *w = sh.wred[warp];
-        w[0] = at.m;
-        w[1] = at.s;
-        w[2] = ad.m;
-        w[3] = ad.s;
-        w[4] = __int_as_float(bad);
+        wp[warp][0] = at.m;
+        wp[warp][1] = at.s;
+        wp[warp][2] = ad.m;
+        wp[warp][3] = ad.s;
+        wp[warp][4] = __int_as_float(bad);
     }
     __syncthreads();
     if (warp == 0) {
         Soft a = soft_empty(), d = soft_empty();
         int bb = 0;
         if (lane < NW) {
-            const float *w = sh.wred[lane];
-            a = {w[0], w[1], 0.f};
-            d = {w[2], w[3], 0.f};
-            bb = __float_as_int(w[4]);
+            a = {wp[lane][0], wp[lane][1], 0.f};
+            d = {wp[lane][2], wp[lane][3], 0.f};
+            bb = __float_as_int(wp[lane][4]);
         }
-        a = soft_warp_allreduce<false>(a, k);
-        d = soft_warp_allreduce<false>(d, k);
-        bb = warp_allor(bb);
-        if (lane == 0) {
-            TRec &r = sh.rec[slot];
-            r.tm = a.m;
-            r.ts = a.s;
-            r.dm = d.m;
-            r.ds = d.s;
-            r.bad = bb;
-        }
+        at = soft_warp_allreduce<false>(a, k);
+        ad = soft_warp_allreduce<false>(d, k);
+        bad = warp_allor(bb);
     }
-    cluster_sync();
-    if (warp == 0) {
-        Soft a = soft_empty(), d = soft_empty();
-        int bb = 0;
-        if (lane < C) {
-            const uint32_t base = map_rank(smem_addr(&sh.rec[slot]), lane);
-            a.m = ld_cluster_f32(base + offsetof(TRec, tm));
-            a.s = ld_cluster_f32(base + offsetof(TRec, ts));
-            d.m = ld_cluster_f32(base + offsetof(TRec, dm));
-            d.s = ld_cluster_f32(base + offsetof(TRec, ds));
-            bb = ld_cluster_s32(base + offsetof(TRec, bad));
-        }
-        a = soft_warp_allreduce<false>(a, k);
-        d = soft_warp_allreduce<false>(d, k);
-        bb = warp_allor(bb);
-        if (lane == 0) {
-            sh.comb[0] = a.m;
-            sh.comb[1] = a.s;
-            sh.comb[2] = d.m;
-            sh.comb[3] = d.s;
-            sh.combi[0] = bb;
-        }
-    }
-    __syncthreads();
-    Ct = {sh.comb[0], sh.comb[1], 0.f};
-    Cd = {sh.comb[2], sh.comb[3], 0.f};
-    cbad = sh.combi[0];
-    slot ^= 1;
 }
 
-// Block + cluster sums of two values; results in all threads.
-__device__ __forceinline__ void tv_cluster_sum2(TVShared &sh, float v0, float v1, int &slot, int C, float &r0,
-                                                float &r1) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ void block_sum2(float (*wp)[8], float &v0, float &v1) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v0 = warp_allsum(v0);
     v1 = warp_allsum(v1);
     if (lane == 0) {
-        sh.wred[warp][0] = v0;
-        sh.wred[warp][1] = v1;
+        wp[warp][0] = v0;
+        wp[warp][1] = v1;
     }
     __syncthreads();
     if (warp == 0) {
-        float x0 = (lane < NW) ? sh.wred[lane][0] : 0.f;
-        float x1 = (lane < NW) ? sh.wred[lane][1] : 0.f;
-        x0 = warp_allsum(x0);
-        x1 = warp_allsum(x1);
-        if (lane == 0) {
-            sh.rec[slot].x0 = x0;
-            sh.rec[slot].x1 = x1;
-        }
+        v0 = warp_allsum(lane < NW ? wp[lane][0] : 0.f);
+        v1 = warp_allsum(lane < NW ? wp[lane][1] : 0.f);
     }
-    cluster_sync();
-    if (warp == 0) {
-        float x0 = 0.f, x1 = 0.f;
-        if (lane < C) {
-            const uint32_t base = map_rank(smem_addr(&sh.rec[slot]), lane);
-            x0 = ld_cluster_f32(base + offsetof(TRec, x0));
-            x1 = ld_cluster_f32(base + offsetof(TRec, x1));
-        }
-        x0 = warp_allsum(x0);
-        x1 = warp_allsum(x1);
-        if (lane == 0) {
-            sh.comb[4] = x0;
-            sh.comb[5] = x1;
-        }
-    }
-    __syncthreads();
-    r0 = sh.comb[4];
-    r1 = sh.comb[5];
-    slot ^= 1;
 }
 
 // Store VEC gradient values for image vector j of row `out` (elements
@@ -169,186 +100,310 @@ __device__ __forceinline__ void store_grad(float *out, int v0, int V, bool align
 }
 
 template <typename Tin>
-__global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
+__device__ __forceinline__ const unsigned char *tv_row(const void *base, int t, int k, int g, int V) {
+    return reinterpret_cast<const unsigned char *>(base) +
+           ((static_cast<size_t>(t) * g + k) * static_cast<size_t>(V)) * Store<Tin>::ES;
+}
+
+// One row slice by bulk copy on `bar` (thread 0); aligned rows only.
+template <typename Tin>
+__device__ __forceinline__ void issue_row(const Slice &s, const unsigned char *row, unsigned char *buf, uint32_t bar) {
+    if (threadIdx.x == 0 && s.nvec > 0) {
+        const uint32_t bytes = static_cast<uint32_t>(s.nvec) * 16u;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(smem_addr(buf), row + static_cast<size_t>(s.lo) * Store<Tin>::ES, bytes, bar);
+    }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
     using S = Store<Tin>;
-    constexpr int VEC = S::VEC, ES = S::ES;
+    constexpr int VEC = S::VEC;
     extern __shared__ __align__(128) unsigned char smem[];
     TVShared &sh = *reinterpret_cast<TVShared *>(smem);
     const int g = A.gamma, V = A.V, nres = A.nres;
-    unsigned char *tb = smem + HDR_BYTES;
-    unsigned char *dres = tb + A.slice_bytes;
+    const bool aligned = A.aligned != 0;
+    unsigned char *tslot[2];
+    tslot[0] = smem + HDR_BYTES;
+    tslot[1] = tslot[0] + A.slice_bytes;
+    unsigned char *dres = tslot[1] + A.slice_bytes;
     unsigned char *bits = dres + static_cast<size_t>(nres) * A.slice_bytes;
 
     const int tid = threadIdx.x;
     const int C = static_cast<int>(cluster_size());
     const int rank = static_cast<int>(cluster_rank());
-    const int t = static_cast<int>(cluster_id_x());
-    const uint32_t bar_t = smem_addr(&sh.bar[0]), bar_d = smem_addr(&sh.bar[1]);
+    const int cid = static_cast<int>(cluster_id_x());
+    const int NC = static_cast<int>(gridDim.x) / C;
+    const Slice s = make_slice<Tin>(V, C, rank);
+    const int nvc = slice_vectors(V, VEC, C);  // bit bytes per step
+    const bool pipe = (nres == g);             // every draft slice stays on chip
+
     if (tid == 0) {
-        mbar_init(bar_t, 1);
-        mbar_init(bar_d, 1);
+        xchg_init(sh.x);
+        mbar_init(smem_addr(&sh.tbar[0]), 1);
+        mbar_init(smem_addr(&sh.tbar[1]), 1);
+        for (int d = 0; d < nres; ++d) mbar_init(smem_addr(&sh.dbar[d]), 1);
         fence_mbar_init();
     }
     const float T = A.temperature;
-    int flags = (!(T > 0.f) || !(T < INFINITY)) ? F_BAD_TEMP : 0;
+    const bool bad_temp = !(T > 0.f) || !(T < INFINITY);
+    const float k = LOG2E / T;
     __syncthreads();
     cluster_sync();
 
-    const float k = LOG2E / T;
-    const Slice s = make_slice<Tin>(V, C, rank);
-    const int nvc = slice_vectors(V, VEC, C);  // bit bytes per step
-    int slot = 0;
-    uint32_t ph_t = 0, ph_d = 0;
-    bool pend_t = false, pend_d = false;
+    // Barrier parities (uniform): target slots and draft slots.
+    uint32_t tph = 0;        // bit s: parity of target slot s
+    uint32_t dph = 0;        // bit d: parity of draft slot d
+    uint32_t tarm = 0, darm = 0;  // armed bits
+    int round = 0, wset = 0;
+    bool dead = false;
+    int pc = 0;  // pairs consumed by this CTA (target slot = pc & 1)
 
-    for (int kk = 0; kk < g && !flags; ++kk) {
-        const size_t row = (static_cast<size_t>(t) * g + kk) * static_cast<size_t>(V);
-        const unsigned char *trow = reinterpret_cast<const unsigned char *>(A.target) + row * ES;
-        const unsigned char *drow = reinterpret_cast<const unsigned char *>(A.draft) + row * ES;
-        unsigned char *db = dres + static_cast<size_t>(kk % nres) * A.slice_bytes;
-        fence_proxy_async();
-        const bool arm_t = load_slice<Tin>(s, trow, tb, bar_t, A.aligned != 0);
-        const bool arm_d = load_slice<Tin>(s, drow, db, bar_d, A.aligned != 0);
-        int tmo = 0;
-        if (arm_t) {
-            if (!mbar_wait_bounded(bar_t, ph_t)) {
-                tmo = 1;
-                pend_t = true;
-            }
-            ph_t ^= 1;
+    auto wait_t = [&](int sl) -> bool {
+        bool ok = true;
+        if (tarm & (1u << sl)) {
+            ok = mbar_wait_bounded(smem_addr(&sh.tbar[sl]), (tph >> sl) & 1u);
+            tph ^= 1u << sl;
+            tarm &= ~(1u << sl);
         }
-        if (arm_d) {
-            if (!mbar_wait_bounded(bar_d, ph_d)) {
-                tmo = 1;
-                pend_d = true;
-            }
-            ph_d ^= 1;
+        return ok;
+    };
+    auto wait_d = [&](int sl) -> bool {
+        bool ok = true;
+        if (darm & (1u << sl)) {
+            ok = mbar_wait_bounded(smem_addr(&sh.dbar[sl]), (dph >> sl) & 1u);
+            dph ^= 1u << sl;
+            darm &= ~(1u << sl);
         }
-        __syncthreads();
+        return ok;
+    };
+    auto load_t = [&](int t, int kk, int sl) {
+        if (aligned && s.nvec > 0) {
+            issue_row<Tin>(s, tv_row<Tin>(A.target, t, kk, g, V), tslot[sl], smem_addr(&sh.tbar[sl]));
+            tarm |= 1u << sl;
+        }
+    };
+    auto load_d = [&](int t, int kk, int sl) {
+        if (aligned && s.nvec > 0) {
+            issue_row<Tin>(s, tv_row<Tin>(A.draft, t, kk, g, V), dres + static_cast<size_t>(sl) * A.slice_bytes,
+                           smem_addr(&sh.dbar[sl]));
+            darm |= 1u << sl;
+        }
+    };
 
-        Soft at = soft_empty(), ad = soft_empty();
-        bool nonfin = false;
-        for (int j = tid; j < s.nvec; j += NT) {
-            float zt[VEC], zd[VEC];
-            S::unpack(vec_at(tb, j), zt);
-            S::unpack(vec_at(db, j), zd);
-            soft_add<VEC, false>(at, zt, k, nonfin);
-            soft_add<VEC, false>(ad, zd, k, nonfin);
-        }
-        Soft Ct, Cd;
-        int cbad;
-        tv_combine_soft(sh, at, ad, (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0), k, slot, C, Ct, Cd, cbad);
-        int rf = cbad;
-        if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY)) rf |= F_NONFINITE;
-        if (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY)) rf |= F_NONFINITE;
-        if (rf) {
-            flags |= rf;
-            break;
-        }
-        const float ct = fmaf(Ct.m, k, log2f(Ct.s));
-        const float cd = fmaf(Cd.m, k, log2f(Cd.s));
-
-        // overlap, S and indicator bits in one pass over the on-chip slices
-        float acc_a = 0.f, acc_s = 0.f;
-        unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
-        for (int j = tid; j < s.nvec; j += NT) {
-            float zt[VEC], zd[VEC];
-            S::unpack(vec_at(tb, j), zt);
-            S::unpack(vec_at(db, j), zd);
-            unsigned m = 0;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float lp = fmaf(zt[e], k, -ct), lq = fmaf(zd[e], k, -cd);
-                const float x = ex2(fminf(lp, lq));
-                acc_a += x;
-                if (lq <= lp) {
-                    acc_s += x;
-                    m |= 1u << e;
-                }
-            }
-            bk[j] = static_cast<unsigned char>(m);
-        }
-        float a, sk;
-        tv_cluster_sum2(sh, acc_a, acc_s, slot, C, a, sk);
-        if (tid == 0) {
-            sh.ak[kk] = a;
-            sh.Sk[kk] = sk;
-            sh.cd[kk] = cd;
-        }
-        __syncthreads();
+    int t = cid;
+    bool d_issued = false;  // the draft slice of the next pair is already requested
+    if (!bad_temp && t < A.N) {
+        load_t(t, 0, 0);
+        load_d(t, 0, 0);
+        d_issued = true;
     }
 
-    if (!flags) {
-        if (tid == 0) {
-            // chain of the e2e loss: prefix products forward, W backward
-            float P[MAX_GAMMA];
-            float prod = 1.f, loss = 0.f;
-            for (int kk = 0; kk < g; ++kk) {
-                prod *= sh.ak[kk];
-                P[kk] = prod;
-                loss -= prod;
-            }
-            float W = 1.f;
-            for (int kk = g - 1; kk >= 0; --kk) {
-                const float Pprev = kk ? P[kk - 1] : 1.f;
-                sh.gk[kk] = -Pprev * W;
-                W = fmaf(sh.ak[kk], W, 1.f);
-            }
-            sh.loss = loss;
-        }
-        __syncthreads();
-        const bool out_aligned = A.aligned != 0;
+    for (; t < A.N; t += NC) {
+        const int tn = t + NC;  // next position of this cluster
+        int flags = bad_temp ? F_BAD_TEMP : 0;
         for (int kk = 0; kk < g; ++kk) {
-            const size_t row = (static_cast<size_t>(t) * g + kk) * static_cast<size_t>(V);
-            const unsigned char *db;
-            if (kk >= g - nres) {
-                db = dres + static_cast<size_t>(kk % nres) * A.slice_bytes;
-            } else {  // re-read a draft slice that did not stay on chip
-                fence_proxy_async();
-                const unsigned char *drow = reinterpret_cast<const unsigned char *>(A.draft) + row * ES;
-                if (load_slice<Tin>(s, drow, tb, bar_t, A.aligned != 0)) {
-                    if (!mbar_wait_bounded(bar_t, ph_t)) pend_t = true;
-                    ph_t ^= 1;
+            const int ts = pc & 1;
+            const int ds = kk % nres;
+            unsigned char *tb = tslot[ts];
+            unsigned char *db = dres + static_cast<size_t>(ds) * A.slice_bytes;
+            int tmo = 0;
+            if (!bad_temp && !dead && !d_issued) load_d(t, kk, ds);
+            if (!bad_temp) {
+                if (!wait_t(ts)) tmo = 1;
+                if (!wait_d(ds)) tmo = 1;
+                if (!aligned) {
+                    load_slice<Tin>(s, tv_row<Tin>(A.target, t, kk, g, V), tb, 0, false);
+                    load_slice<Tin>(s, tv_row<Tin>(A.draft, t, kk, g, V), db, 0, false);
                 }
-                __syncthreads();
-                db = tb;
-            }
-            const float coef = A.grad_scale * sh.gk[kk] / T;
-            const float cd = sh.cd[kk], sk = sh.Sk[kk];
-            const float on = coef * (1.f - sk), off = -coef * sk;
-            const unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
-            float *out = A.grad + row;
-            for (int j = tid; j < s.nvec; j += NT) {
-                float zd[VEC], gr[VEC];
-                S::unpack(vec_at(db, j), zd);
-                const unsigned m = bk[j];
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float q = ex2(fmaf(zd[e], k, -cd));
-                    gr[e] = q * (((m >> e) & 1u) ? on : off);
-                }
-                store_grad<VEC>(out, s.lo + j * VEC, V, out_aligned, gr);
             }
             __syncthreads();
+            // prefetch the next pair: (t, kk+1), or the next position's first target
+            if (!bad_temp && !dead) {
+                d_issued = false;
+                if (kk + 1 < g) {
+                    load_t(t, kk + 1, ts ^ 1);
+                    if (nres > 1) {
+                        load_d(t, kk + 1, (kk + 1) % nres);
+                        d_issued = true;
+                    }
+                } else if (tn < A.N) {
+                    load_t(tn, 0, ts ^ 1);
+                }
+            }
+            ++pc;
+            if (flags || dead) continue;
+
+            bool nonfin = false;
+            Soft at = thread_soft<Tin, false>(tb, s.nvec, k, nonfin);
+            Soft ad = thread_soft<Tin, false>(db, s.nvec, k, nonfin);
+            int bad = (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0);
+            block_soft2(sh.wpart[wset], at, ad, bad, k);
+            wset ^= 1;
+            float rec[8] = {at.m, at.s, ad.m, ad.s, __int_as_float(bad), 0.f, 0.f, 0.f};
+            bool ok;
+            int slot = xchg_round<8>(sh.x, round, rec, C, rank, ok);
+            Soft Ct = soft_empty(), Cd = soft_empty();
+            int cb = 0;
+            {
+                const int lane = tid & 31;
+                Soft a = soft_empty(), d = soft_empty();
+                if (lane < C) {
+                    const float *r = sh.x.rec[slot][lane];
+                    a = {r[0], r[1], 0.f};
+                    d = {r[2], r[3], 0.f};
+                    cb = __float_as_int(r[4]);
+                }
+                Ct = soft_warp_allreduce<false>(a, k);
+                Cd = soft_warp_allreduce<false>(d, k);
+                cb = warp_allor(cb);
+            }
+            if (!ok) {
+                dead = true;
+                cb |= F_TIMEOUT;
+            }
+            if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY)) cb |= F_NONFINITE;
+            if (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY)) cb |= F_NONFINITE;
+            if (cb) {
+                flags |= cb;
+                continue;
+            }
+            const float ct = fmaf(Ct.m, k, log2f(Ct.s));
+            const float cd = fmaf(Cd.m, k, log2f(Cd.s));
+
+            // overlap, S and indicator bits in one pass over the on-chip slices
+            float acc_a = 0.f, acc_s = 0.f;
+            unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
+            for (int j = tid; j < s.nvec; j += NT) {
+                float zt[VEC], zd[VEC];
+                S::unpack(vec_at(tb, j), zt);
+                S::unpack(vec_at(db, j), zd);
+                unsigned m = 0;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float lp = fmaf(zt[e], k, -ct), lq = fmaf(zd[e], k, -cd);
+                    const float x = ex2(fminf(lp, lq));
+                    acc_a += x;
+                    if (lq <= lp) {
+                        acc_s += x;
+                        m |= 1u << e;
+                    }
+                }
+                bk[j] = static_cast<unsigned char>(m);
+            }
+            block_sum2(sh.wpart[wset], acc_a, acc_s);
+            wset ^= 1;
+            float rec2[4] = {acc_a, acc_s, 0.f, 0.f};
+            slot = xchg_round<4>(sh.x, round, rec2, C, rank, ok);
+            float a = 0.f, sk = 0.f;
+            {
+                const int lane = tid & 31;
+                a = warp_allsum(lane < C ? sh.x.rec[slot][lane][0] : 0.f);
+                sk = warp_allsum(lane < C ? sh.x.rec[slot][lane][1] : 0.f);
+            }
+            if (!ok) {
+                dead = true;
+                flags |= F_TIMEOUT;
+                continue;
+            }
+            if (tid == 0) {
+                sh.ak[kk] = a;
+                sh.Sk[kk] = sk;
+                sh.cd[kk] = cd;
+            }
         }
-    } else {
-        // flagged position: defined zero gradient
-        for (int kk = 0; kk < g; ++kk) {
-            float *out = A.grad + (static_cast<size_t>(t) * g + kk) * static_cast<size_t>(V);
-            for (int v = s.lo + tid; v < s.hi; v += NT) out[v] = 0.f;
+        if (dead) flags |= F_TIMEOUT;
+        __syncthreads();
+
+        float *gbase = A.grad + static_cast<size_t>(t) * g * static_cast<size_t>(V);
+        if (!flags) {
+            if (tid == 0) {
+                // chain of the e2e loss: prefix products forward, W backward
+                float P[MAX_GAMMA];
+                float prod = 1.f, loss = 0.f;
+                for (int kk = 0; kk < g; ++kk) {
+                    prod *= sh.ak[kk];
+                    P[kk] = prod;
+                    loss -= prod;
+                }
+                float W = 1.f;
+                for (int kk = g - 1; kk >= 0; --kk) {
+                    const float Pprev = kk ? P[kk - 1] : 1.f;
+                    sh.gk[kk] = -Pprev * W;
+                    W = fmaf(sh.ak[kk], W, 1.f);
+                }
+                sh.loss = loss;
+            }
+            __syncthreads();
+            for (int kk = 0; kk < g; ++kk) {
+                const unsigned char *db;
+                if (kk >= g - nres) {
+                    db = dres + static_cast<size_t>(kk % nres) * A.slice_bytes;
+                } else {  // re-read a draft slice that did not stay on chip
+                    const int sl = (pc - 1) & 1;  // the last pair's target slot is free
+                    const unsigned char *drow = tv_row<Tin>(A.draft, t, kk, g, V);
+                    if (aligned) {
+                        if (s.nvec > 0) {
+                            issue_row<Tin>(s, drow, tslot[sl], smem_addr(&sh.tbar[sl]));
+                            tarm |= 1u << sl;
+                        }
+                        wait_t(sl);
+                    } else {
+                        load_slice<Tin>(s, drow, tslot[sl], 0, false);
+                    }
+                    __syncthreads();
+                    db = tslot[sl];
+                }
+                const float coef = A.grad_scale * sh.gk[kk] / T;
+                const float cd = sh.cd[kk], sk = sh.Sk[kk];
+                const float on = coef * (1.f - sk), off = -coef * sk;
+                const unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
+                float *out = gbase + static_cast<size_t>(kk) * V;
+                for (int j = tid; j < s.nvec; j += NT) {
+                    float zd[VEC], gr[VEC];
+                    S::unpack(vec_at(db, j), zd);
+                    const unsigned m = bk[j];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float q = ex2(fmaf(zd[e], k, -cd));
+                        gr[e] = q * (((m >> e) & 1u) ? on : off);
+                    }
+                    store_grad<VEC>(out, s.lo + j * VEC, V, aligned, gr);
+                }
+                __syncthreads();
+                if (pipe && kk == 0 && tn < A.N && !dead) {
+                    load_d(tn, 0, 0);
+                    d_issued = true;
+                }
+            }
+        } else {
+            for (int kk = 0; kk < g; ++kk) {
+                float *out = gbase + static_cast<size_t>(kk) * V;
+                for (int v = s.lo + tid; v < s.hi; v += NT) out[v] = 0.f;
+            }
+            if (pipe && tn < A.N && !dead && !bad_temp) {
+                load_d(tn, 0, 0);
+                d_issued = true;
+            }
         }
+        if (!pipe && tn < A.N && !dead && !bad_temp) {
+            load_d(tn, 0, 0);
+            d_issued = true;
+        }
+
+        if (rank == 0 && tid == 0) {
+            A.loss[t] = flags ? NAN : sh.loss;
+            if (A.alpha)
+                for (int kk = 0; kk < g; ++kk) A.alpha[static_cast<size_t>(t) * g + kk] = flags ? NAN : sh.ak[kk];
+            if (A.flags) A.flags[t] = flags;
+        }
+        __syncthreads();
     }
 
-    if (pend_t) mbar_wait_bounded(bar_t, ph_t ^ 1);
-    if (pend_d) mbar_wait_bounded(bar_d, ph_d ^ 1);
-
-    if (rank == 0 && tid == 0) {
-        const bool err = flags != 0;
-        A.loss[t] = err ? NAN : sh.loss;
-        if (A.alpha)
-            for (int kk = 0; kk < g; ++kk) A.alpha[static_cast<size_t>(t) * g + kk] = err ? NAN : sh.ak[kk];
-        if (A.flags) A.flags[t] = flags;
-    }
+    // Copies that outlived a bounded wait must land before the CTA exits.
+    for (int sl = 0; sl < 2; ++sl) wait_t(sl);
+    for (int d = 0; d < nres; ++d) wait_d(d);
     cluster_sync();
 }
 
