@@ -46,7 +46,10 @@ L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
 # ncu captures (profiles/), keyed by workload, valid only for the kernel
 # sources they were taken on (hash of csrc/).
-TRAFFIC = {}
+TRAFFIC = {
+    # row_kernel_impl<bf16_t,0>, B=64 gamma=3 V=151936: 124,055,552 read + 3,932,928 written
+    "verify64": {"bytes": 127988480, "csrc": "5ae2997d51598d49"},
+}
 
 
 def csrc_hash() -> str:
@@ -219,6 +222,7 @@ class TVWorkload:
         self.mtp = mtp
         self.x = x = W.config("tvloss", device=device, N_override=N)
         self.N, self.gamma, self.V, self.es = x.N, x.gamma, x.V, 2
+        self.stats = False
         self.out = None
         self.copies = 1
         self.positions = x.N * x.gamma
@@ -406,8 +410,11 @@ def run_cuda(args, world, rank, local, pg):
         alg = wl.alg_bytes()
         per_launch_s = t["ms_total"] / 1e3 / t["launches"]
         achieved = alg / per_launch_s / 1e9
+        plan = mtp.mtp_query_plan("tv_loss" if name == "tvloss" else ("verify_stats" if wl.stats else "verify"),
+                                  "bf16" if wl.es == 2 else "f32", wl.N if name == "tvloss" else wl.B, wl.gamma, wl.V)
         r = {
             "workload": wl.describe(),
+            "launch_plan": plan,
             "positions_per_s": world * wl.positions * steps / (t_ms / 1e3),
             "ms_per_step": t_ms / steps,
             "logit_gbps": achieved,

@@ -24,6 +24,7 @@ struct Plan {
     int nres = 0;
     int clusters = 0;  // persistent grid: co-resident clusters used
     int streams = 1;   // row kernel: sequences in flight per CTA
+    int threads = 0;   // threads per CTA
 };
 
 struct CacheEntry {
@@ -69,7 +70,7 @@ cudaError_t prepare_func(int dev, const void *func) {
 
 // Largest number of co-resident clusters of C CTAs with `smem` bytes each
 // (0 when the configuration cannot run).
-int max_clusters(int dev, const void *func, int C, uint32_t smem) {
+int max_clusters(int dev, const void *func, int C, uint32_t smem, int threads) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (auto &c : g_cache)
@@ -77,7 +78,7 @@ int max_clusters(int dev, const void *func, int C, uint32_t smem) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C);
-    cfg.blockDim = dim3(NT);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -122,14 +123,14 @@ bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
             const uint32_t sb = slice_buffer_bytes(V, es, C);
             const uint32_t smem = row_hdr_bytes() + 2 * ns * sb;
             if (smem > cap) continue;
-            const int nc = max_clusters(dev, func, C, smem);
+            const int nc = max_clusters(dev, func, C, smem, row_threads());
             if (nc <= 0) continue;
             const int used = nc < units ? nc : units;
             const long inflight = static_cast<long>(nc) * ns < units ? static_cast<long>(nc) * ns : units;
             const long score = inflight * C * 4 + used;  // slices in flight, then clusters used
             if (score > best) {
                 best = score;
-                p = {C, sb, smem, 0, used, ns};
+                p = {C, sb, smem, 0, used, ns, row_threads()};
             }
         }
     }
@@ -155,14 +156,14 @@ bool plan_tv(int dev, const void *func, int V, int es, int gamma, int units, Pla
         if (nres < 1) continue;
         // with every draft resident, prefer the smallest footprint that holds them
         const uint32_t smem = fixed + static_cast<uint32_t>(nres) * sb;
-        const int nc = max_clusters(dev, func, C, smem);
+        const int nc = max_clusters(dev, func, C, smem, tv_threads());
         if (nc <= 0) continue;
         const int used = nc < units ? nc : units;
         // working CTAs, with a penalty for draft slices re-read in the epilogue
         const long score = static_cast<long>(used) * C * (nres == gamma ? 2 : 1);
         if (score > best) {
             best = score;
-            p = {C, sb, smem, nres, used, 1};
+            p = {C, sb, smem, nres, used, 1, tv_threads()};
         }
     }
     return best > 0;
@@ -171,7 +172,7 @@ bool plan_tv(int dev, const void *func, int V, int es, int gamma, int units, Pla
 int launch(const void *func, const Plan &p, void *args, mtp_stream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.clusters) * static_cast<unsigned>(p.C));
-    cfg.blockDim = dim3(NT);
+    cfg.blockDim = dim3(p.threads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];

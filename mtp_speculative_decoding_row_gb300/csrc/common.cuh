@@ -13,8 +13,6 @@
 
 namespace mtp {
 
-constexpr int NT = 128;        // threads per CTA (>= 128: parameter prefetch uses tids 0..127)
-constexpr int NW = NT / 32;    // warps per CTA
 constexpr int MAX_C = 16;      // largest cluster
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -282,7 +280,7 @@ __device__ __forceinline__ Slice make_slice(int V, int C, int r) {
 // `bar` and issues one bulk copy; returns true (same value in all threads).
 // Otherwise every thread copies elements and pads; the caller publishes the
 // plain stores with __syncthreads().
-template <typename Tin>
+template <typename Tin, int NTH>
 __device__ __forceinline__ bool load_slice(const Slice &s, const void *row, unsigned char *buf, uint32_t bar,
                                            bool row_aligned) {
     constexpr int ES = Store<Tin>::ES, VEC = Store<Tin>::VEC;
@@ -297,7 +295,7 @@ __device__ __forceinline__ bool load_slice(const Slice &s, const void *row, unsi
         return true;
     }
     const int n = s.hi - s.lo;
-    for (int e = threadIdx.x; e < s.nvec * VEC; e += NT) {
+    for (int e = threadIdx.x; e < s.nvec * VEC; e += NTH) {
         if (ES == 4) {
             reinterpret_cast<float *>(buf)[e] = (e < n) ? reinterpret_cast<const float *>(g)[e] : -INFINITY;
         } else {
@@ -357,7 +355,7 @@ __device__ __forceinline__ uint64_t bf16pair_f2(uint32_t x) {
 // < nvec of one row slice, in two passes over shared memory: (1) the exact
 // maximum m (NaN-propagating; a NaN or +inf sets `bad`), (2)
 // s = sum 2^{(z - m) k} and, with ENT, s1 = sum 2^{(z - m) k} (z - m) k.
-template <typename Tin, bool ENT>
+template <typename Tin, bool ENT, int NT>
 __device__ __forceinline__ Soft thread_soft_exact(const unsigned char *buf, int nvec, float k, bool &bad) {
     Soft a = soft_empty();
     float m;
@@ -463,9 +461,9 @@ __device__ __forceinline__ void vec_expsum(const uint4 &r, float k, float mk, fl
     }
 }
 
-template <typename Tin, bool ENT>
+template <typename Tin, bool ENT, int NT>
 __device__ __noinline__ Soft thread_soft_exact_call(const unsigned char *buf, int nvec, float k, bool &bad) {
-    return thread_soft_exact<Tin, ENT>(buf, nvec, k, bad);
+    return thread_soft_exact<Tin, ENT, NT>(buf, nvec, k, bad);
 }
 
 // Softmax partial of this thread's vectors of one row slice (see
@@ -477,9 +475,9 @@ __device__ __noinline__ Soft thread_soft_exact_call(const unsigned char *buf, in
 // and the pass is kept only if its sum stays finite and below 2^64 (no
 // overflow; NaN or +inf make it non-finite).  Otherwise the exact two-pass
 // path runs, which also flags NaN / +inf.
-template <typename Tin, bool ENT>
+template <typename Tin, bool ENT, int NT>
 __device__ __forceinline__ Soft thread_soft(const unsigned char *buf, int nvec, float k, bool &bad) {
-    if (ENT) return thread_soft_exact<Tin, ENT>(buf, nvec, k, bad);
+    if (ENT) return thread_soft_exact<Tin, ENT, NT>(buf, nvec, k, bad);
     const int j0 = threadIdx.x;
     if (j0 >= nvec) return soft_empty();
     const uint4 first = vec_at(buf, j0);
@@ -517,7 +515,7 @@ __device__ __forceinline__ Soft thread_soft(const unsigned char *buf, int nvec, 
             return a;
         }
     }
-    return thread_soft_exact_call<Tin, ENT>(buf, nvec, k, bad);
+    return thread_soft_exact_call<Tin, ENT, NT>(buf, nvec, k, bad);
 }
 
 // Add one vector of logits z (its max vm, NaN if any element is NaN).
@@ -551,7 +549,7 @@ __device__ __forceinline__ void soft_add(Soft &a, const float (&z)[N], float vm,
 
 // Lane `lane` of warp 0 merges the per-thread partials lane, lane+32, ...
 // (NT/32 of them) stored as m[], s[], s1[] columns in shared memory.
-template <bool ENT>
+template <bool ENT, int NW>
 __device__ __forceinline__ Soft soft_lane_merge(const float *m, const float *s, const float *s1, int lane, float k) {
     float M = m[lane];
 #pragma unroll

@@ -44,6 +44,9 @@ struct TVArgs {
 // Shared-memory header bytes in front of the slice buffers of each kernel.
 uint32_t row_hdr_bytes();
 uint32_t tv_hdr_bytes();
+// Threads per CTA of each kernel.
+int row_threads();
+int tv_threads();
 
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);

@@ -26,6 +26,9 @@
 
 namespace mtp {
 
+constexpr int NT = 128;      // threads per CTA
+constexpr int NW = NT / 32;  // warps per CTA
+
 struct StreamSt {
     int active;   // stream holds a sequence
     int b;        // sequence
@@ -58,6 +61,7 @@ struct RowShared {
 };
 constexpr uint32_t HDR_BYTES = (sizeof(RowShared) + 127u) & ~127u;
 uint32_t row_hdr_bytes() { return HDR_BYTES; }
+int row_threads() { return NT; }
 
 constexpr int ERR_BITS = F_NONFINITE | F_BAD_ID | F_BAD_TEMP | F_BAD_UNIFORM | F_TIMEOUT;
 
@@ -77,8 +81,8 @@ __device__ __forceinline__ void block_soft(float (*tp)[NT], Soft &at, Soft &ad, 
     tp[5][tid] = __int_as_float(bad);
     __syncthreads();
     if (warp == 0) {
-        const Soft a = soft_lane_merge<ENT>(tp[0], tp[1], tp[2], lane, k);
-        const Soft d = soft_lane_merge<false>(tp[3], tp[4], tp[4], lane, k);
+        const Soft a = soft_lane_merge<ENT, NW>(tp[0], tp[1], tp[2], lane, k);
+        const Soft d = soft_lane_merge<false, NW>(tp[3], tp[4], tp[4], lane, k);
         int bb = 0;
 #pragma unroll
         for (int q = 0; q < NW; ++q) bb |= __float_as_int(tp[5][lane + 32 * q]);
@@ -462,15 +466,15 @@ __global__ void __launch_bounds__(NT, 4) row_kernel_impl(const VerifyArgs A) {
                     st.ph ^= 1u;
                     st.armed = 0;
                 } else if (!A.aligned) {
-                    load_slice<Tin>(s, row_ptr<Tin>(A.target, static_cast<size_t>(b) * (g + 1) + i, A.V), tb, 0, false);
-                    if (has_d) load_slice<Tin>(s, row_ptr<Tin>(A.draft, static_cast<size_t>(b) * g + i, A.V), db, 0, false);
+                    load_slice<Tin, NT>(s, row_ptr<Tin>(A.target, static_cast<size_t>(b) * (g + 1) + i, A.V), tb, 0, false);
+                    if (has_d) load_slice<Tin, NT>(s, row_ptr<Tin>(A.draft, static_cast<size_t>(b) * g + i, A.V), db, 0, false);
                 }
                 __syncthreads();
 
                 // pass A: online max / normaliser (and entropy sum) per row
                 bool nonfin = false;
-                Soft at = thread_soft<Tin, STATS>(tb, s.nvec, k, nonfin);
-                Soft ad = has_d ? thread_soft<Tin, false>(db, s.nvec, k, nonfin) : soft_empty();
+                Soft at = thread_soft<Tin, STATS, NT>(tb, s.nvec, k, nonfin);
+                Soft ad = has_d ? thread_soft<Tin, false, NT>(db, s.nvec, k, nonfin) : soft_empty();
                 const bool want_y = DECIDE && has_d && !st.stopped;
                 const int y = want_y ? sh.ids[si][i] : -1;
                 int bad = (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0);

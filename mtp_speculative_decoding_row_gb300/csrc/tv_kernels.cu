@@ -26,9 +26,12 @@
 
 namespace mtp {
 
+constexpr int NT = 256;      // threads per CTA
+constexpr int NW = NT / 32;  // warps per CTA
+
 struct TVShared {
     Xchg x;
-    float wpart[2][NW][8];
+    float tpart[5][NT];  // per-thread partials (columns)
     float cd[MAX_GAMMA];
     float Sk[MAX_GAMMA];
     float ak[MAX_GAMMA];
@@ -39,47 +42,45 @@ struct TVShared {
 };
 constexpr uint32_t HDR_BYTES = (sizeof(TVShared) + 127u) & ~127u;
 uint32_t tv_hdr_bytes() { return HDR_BYTES; }
+int tv_threads() { return NT; }
 
-// Per-thread partials of two rows -> CTA partial in every lane of warp 0.
-__device__ __forceinline__ void block_soft2(float (*wp)[8], Soft &at, Soft &ad, int &bad, float k) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    at = soft_warp_allreduce<false>(at, k);
-    ad = soft_warp_allreduce<false>(ad, k);
-    bad = warp_allor(bad);
-    if (lane == 0) {
-        wp[warp][0] = at.m;
-        wp[warp][1] = at.s;
-        wp[warp][2] = ad.m;
-        wp[warp][3] = ad.s;
-        wp[warp][4] = __int_as_float(bad);
-    }
+// Per-thread partials of two rows -> CTA partial in every lane of warp 0
+// (column layout in shared memory; warp 0 merges NT/32 per lane, then one
+// butterfly).
+__device__ __forceinline__ void block_soft2(float (*tp)[NT], Soft &at, Soft &ad, int &bad, float k) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    tp[0][tid] = at.m;
+    tp[1][tid] = at.s;
+    tp[2][tid] = ad.m;
+    tp[3][tid] = ad.s;
+    tp[4][tid] = __int_as_float(bad);
     __syncthreads();
     if (warp == 0) {
-        Soft a = soft_empty(), d = soft_empty();
+        const Soft a = soft_lane_merge<false, NW>(tp[0], tp[1], tp[1], lane, k);
+        const Soft d = soft_lane_merge<false, NW>(tp[2], tp[3], tp[3], lane, k);
         int bb = 0;
-        if (lane < NW) {
-            a = {wp[lane][0], wp[lane][1], 0.f};
-            d = {wp[lane][2], wp[lane][3], 0.f};
-            bb = __float_as_int(wp[lane][4]);
-        }
+#pragma unroll
+        for (int q = 0; q < NW; ++q) bb |= __float_as_int(tp[4][lane + 32 * q]);
         at = soft_warp_allreduce<false>(a, k);
         ad = soft_warp_allreduce<false>(d, k);
         bad = warp_allor(bb);
     }
 }
 
-__device__ __forceinline__ void block_sum2(float (*wp)[8], float &v0, float &v1) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v0 = warp_allsum(v0);
-    v1 = warp_allsum(v1);
-    if (lane == 0) {
-        wp[warp][0] = v0;
-        wp[warp][1] = v1;
-    }
+__device__ __forceinline__ void block_sum2(float (*tp)[NT], float &v0, float &v1) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    tp[0][tid] = v0;
+    tp[1][tid] = v1;
     __syncthreads();
     if (warp == 0) {
-        v0 = warp_allsum(lane < NW ? wp[lane][0] : 0.f);
-        v1 = warp_allsum(lane < NW ? wp[lane][1] : 0.f);
+        float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+            r0 += tp[0][lane + 32 * q];
+            r1 += tp[1][lane + 32 * q];
+        }
+        v0 = warp_allsum(r0);
+        v1 = warp_allsum(r1);
     }
 }
 
@@ -117,7 +118,7 @@ __device__ __forceinline__ void issue_row(const Slice &s, const unsigned char *r
 }
 
 template <typename Tin>
-__global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
+__global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
     using S = Store<Tin>;
     constexpr int VEC = S::VEC;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
     uint32_t tph = 0;        // bit s: parity of target slot s
     uint32_t dph = 0;        // bit d: parity of draft slot d
     uint32_t tarm = 0, darm = 0;  // armed bits
-    int round = 0, wset = 0;
+    int round = 0;
     bool dead = false;
     int pc = 0;  // pairs consumed by this CTA (target slot = pc & 1)
 
@@ -203,6 +204,10 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
     for (; t < A.N; t += NC) {
         const int tn = t + NC;  // next position of this cluster
         int flags = bad_temp ? F_BAD_TEMP : 0;
+        // (alpha, S) partials of the previous step travel with the next
+        // step's normaliser record: gamma + 1 exchange rounds per position.
+        float pa = 0.f, ps = 0.f;  // CTA partials of the previous step (warp 0)
+        bool have_prev = false;
         for (int kk = 0; kk < g; ++kk) {
             const int ts = pc & 1;
             const int ds = kk % nres;
@@ -214,8 +219,8 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
                 if (!wait_t(ts)) tmo = 1;
                 if (!wait_d(ds)) tmo = 1;
                 if (!aligned) {
-                    load_slice<Tin>(s, tv_row<Tin>(A.target, t, kk, g, V), tb, 0, false);
-                    load_slice<Tin>(s, tv_row<Tin>(A.draft, t, kk, g, V), db, 0, false);
+                    load_slice<Tin, NT>(s, tv_row<Tin>(A.target, t, kk, g, V), tb, 0, false);
+                    load_slice<Tin, NT>(s, tv_row<Tin>(A.draft, t, kk, g, V), db, 0, false);
                 }
             }
             __syncthreads();
@@ -236,16 +241,16 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
             if (flags || dead) continue;
 
             bool nonfin = false;
-            Soft at = thread_soft<Tin, false>(tb, s.nvec, k, nonfin);
-            Soft ad = thread_soft<Tin, false>(db, s.nvec, k, nonfin);
+            Soft at = thread_soft<Tin, false, NT>(tb, s.nvec, k, nonfin);
+            Soft ad = thread_soft<Tin, false, NT>(db, s.nvec, k, nonfin);
             int bad = (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0);
-            block_soft2(sh.wpart[wset], at, ad, bad, k);
-            wset ^= 1;
-            float rec[8] = {at.m, at.s, ad.m, ad.s, __int_as_float(bad), 0.f, 0.f, 0.f};
+            block_soft2(sh.tpart, at, ad, bad, k);
+            float rec[8] = {at.m, at.s, ad.m, ad.s, __int_as_float(bad), pa, ps, 0.f};
             bool ok;
-            int slot = xchg_round<8>(sh.x, round, rec, C, rank, ok);
+            const int slot = xchg_round<8>(sh.x, round, rec, C, rank, ok);
             Soft Ct = soft_empty(), Cd = soft_empty();
             int cb = 0;
+            float sa = 0.f, ss = 0.f;
             {
                 const int lane = tid & 31;
                 Soft a = soft_empty(), d = soft_empty();
@@ -254,10 +259,18 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
                     a = {r[0], r[1], 0.f};
                     d = {r[2], r[3], 0.f};
                     cb = __float_as_int(r[4]);
+                    sa = r[5];
+                    ss = r[6];
                 }
                 Ct = soft_warp_allreduce<false>(a, k);
                 Cd = soft_warp_allreduce<false>(d, k);
                 cb = warp_allor(cb);
+                sa = warp_allsum(sa);
+                ss = warp_allsum(ss);
+            }
+            if (have_prev && tid == 0) {
+                sh.ak[kk - 1] = sa;
+                sh.Sk[kk - 1] = ss;
             }
             if (!ok) {
                 dead = true;
@@ -267,10 +280,12 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
             if (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY)) cb |= F_NONFINITE;
             if (cb) {
                 flags |= cb;
+                have_prev = false;
                 continue;
             }
             const float ct = fmaf(Ct.m, k, log2f(Ct.s));
             const float cd = fmaf(Cd.m, k, log2f(Cd.s));
+            if (tid == 0) sh.cd[kk] = cd;
 
             // overlap, S and indicator bits in one pass over the on-chip slices
             float acc_a = 0.f, acc_s = 0.f;
@@ -292,26 +307,23 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
                 }
                 bk[j] = static_cast<unsigned char>(m);
             }
-            block_sum2(sh.wpart[wset], acc_a, acc_s);
-            wset ^= 1;
-            float rec2[4] = {acc_a, acc_s, 0.f, 0.f};
-            slot = xchg_round<4>(sh.x, round, rec2, C, rank, ok);
-            float a = 0.f, sk = 0.f;
-            {
-                const int lane = tid & 31;
-                a = warp_allsum(lane < C ? sh.x.rec[slot][lane][0] : 0.f);
-                sk = warp_allsum(lane < C ? sh.x.rec[slot][lane][1] : 0.f);
-            }
-            if (!ok) {
-                dead = true;
-                flags |= F_TIMEOUT;
-                continue;
-            }
+            block_sum2(sh.tpart, acc_a, acc_s);
+            pa = acc_a;
+            ps = acc_s;
+            have_prev = true;
+        }
+        if (!flags && !dead && have_prev) {  // last step's (alpha, S)
+            float rec[8] = {0.f, 0.f, 0.f, 0.f, 0.f, pa, ps, 0.f};
+            bool ok;
+            const int slot = xchg_round<8>(sh.x, round, rec, C, rank, ok);
+            const int lane = tid & 31;
+            const float sa = warp_allsum(lane < C ? sh.x.rec[slot][lane][5] : 0.f);
+            const float ss = warp_allsum(lane < C ? sh.x.rec[slot][lane][6] : 0.f);
             if (tid == 0) {
-                sh.ak[kk] = a;
-                sh.Sk[kk] = sk;
-                sh.cd[kk] = cd;
+                sh.ak[g - 1] = sa;
+                sh.Sk[g - 1] = ss;
             }
+            if (!ok) dead = true;
         }
         if (dead) flags |= F_TIMEOUT;
         __syncthreads();
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
                         }
                         wait_t(sl);
                     } else {
-                        load_slice<Tin>(s, drow, tslot[sl], 0, false);
+                        load_slice<Tin, NT>(s, drow, tslot[sl], 0, false);
                     }
                     __syncthreads();
                     db = tslot[sl];
@@ -360,16 +372,31 @@ __global__ void __launch_bounds__(NT, 4) tv_kernel_impl(const TVArgs A) {
                 const float on = coef * (1.f - sk), off = -coef * sk;
                 const unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
                 float *out = gbase + static_cast<size_t>(kk) * V;
-                for (int j = tid; j < s.nvec; j += NT) {
-                    float zd[VEC], gr[VEC];
-                    S::unpack(vec_at(db, j), zd);
-                    const unsigned m = bk[j];
+                // four consecutive outputs per thread: every warp store is
+                // 512 contiguous bytes
+                const int nquad = s.nvec * VEC / 4;
+                for (int h = tid; h < nquad; h += NT) {
+                    float zd[4], gr[4];
+                    if (S::ES == 2) {
+                        const uint2 r = reinterpret_cast<const uint2 *>(db)[h];
+                        zd[0] = __uint_as_float(r.x << 16);
+                        zd[1] = __uint_as_float(r.x & 0xffff0000u);
+                        zd[2] = __uint_as_float(r.y << 16);
+                        zd[3] = __uint_as_float(r.y & 0xffff0000u);
+                    } else {
+                        const uint4 r = reinterpret_cast<const uint4 *>(db)[h];
+                        zd[0] = __uint_as_float(r.x);
+                        zd[1] = __uint_as_float(r.y);
+                        zd[2] = __uint_as_float(r.z);
+                        zd[3] = __uint_as_float(r.w);
+                    }
+                    const unsigned m = static_cast<unsigned>(bk[(4 * h) / VEC]) >> ((4 * h) % VEC);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
+                    for (int e = 0; e < 4; ++e) {
                         const float q = ex2(fmaf(zd[e], k, -cd));
                         gr[e] = q * (((m >> e) & 1u) ? on : off);
                     }
-                    store_grad<VEC>(out, s.lo + j * VEC, V, aligned, gr);
+                    store_grad<4>(out, s.lo + 4 * h, V, aligned, gr);
                 }
                 __syncthreads();
                 if (pipe && kk == 0 && tn < A.N && !dead) {
