@@ -83,8 +83,10 @@ enum {
  * norm(max(0, p_j - q_j)) by inverse CDF with uniforms[b,gamma]: the smallest
  * vocabulary index v with C(v) > u * R (ascending index, C the running sum, R
  * the total).  If all gamma drafts are accepted, the bonus token is drawn the
- * same way from p_gamma.  Rows after the stop are not read unless statistics
- * are requested.
+ * same way from p_gamma.  Rows after the stop are not used unless statistics
+ * are requested (without statistics the streaming kernel may prefetch a
+ * bounded part of the next position's rows before a decision is known; it
+ * never reads beyond the caller's arrays).
  *
  *   target_logits [B, gamma+1, V] dtype     draft_logits [B, gamma, V] dtype
  *   draft_ids     [B, gamma] int32          temperature  [B] float32 (> 0)
@@ -148,11 +150,14 @@ int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp
 /*
  * mtp_query_plan -- the launch plan a call would use on the current device
  * (diagnostics; launches nothing).  op: 0 = mtp_rs_verify, 1 = mtp_rs_verify
- * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd.  units = B
+ * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd, 4 =
+ * mtp_rs_verify forced onto the cluster-resident kernel.  units = B
  * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
- * CTAs per thread-block cluster; the vocabulary is split into C slices),
+ * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
- * per CTA), resident_drafts (TV loss: draft slices kept on chip, else 0).
+ * per CTA), resident_drafts (TV loss: draft slices kept on chip; op 0: chunk
+ * slots per warp of the streaming kernel, 0 when the call would use the
+ * cluster-resident kernel; else 0).
  * Returns the status the call's planning step would return.
  */
 int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size, int *clusters,

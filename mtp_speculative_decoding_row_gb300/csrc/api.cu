@@ -25,6 +25,9 @@ struct Plan {
     int clusters = 0;  // persistent grid: co-resident clusters used
     int streams = 1;   // row kernel: sequences in flight per CTA
     int threads = 0;   // threads per CTA
+    int ring = 0;      // streaming kernel: chunk slots per warp
+    int depth = 0;     // streaming kernel: look-ahead positions
+    int seg_vectors = 0;
 };
 
 struct CacheEntry {
@@ -125,7 +128,9 @@ bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
             if (smem > cap) continue;
             const int nc = max_clusters(dev, func, C, smem, row_threads());
             if (nc <= 0) continue;
-            const int used = nc < units ? nc : units;
+            int used = nc < units ? nc : units;
+            const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
+            if (cap_nc > 0 && used > cap_nc) used = cap_nc;
             const long inflight = static_cast<long>(nc) * ns < units ? static_cast<long>(nc) * ns : units;
             const long score = inflight * C * 4 + used;  // slices in flight, then clusters used
             if (score > best) {
@@ -135,6 +140,62 @@ bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
         }
     }
     return best > 0;
+}
+
+// Streaming verify kernel: clusters of C CTAs x NT/32 warps, one vocabulary
+// segment per warp, one sequence per cluster at a time.  Picks the cluster
+// size with the smallest estimated makespan, ceil(units / clusters) waves of
+// (1 / C + a fixed latency share) sequence-times, among sizes whose segments
+// hold at least 64 vectors (or C = 1) and at most the chunk-list limit; ties
+// go to more busy CTAs.
+bool stream_usable(int V, int es, int gamma) {
+    const char *e = std::getenv("MTP_RS_VERIFY_KERNEL");
+    if (e && e[0] == 'r') return false;  // "resident"
+    return gamma <= stream_max_gamma() && V % (16 / es) == 0;
+}
+
+bool plan_stream(int dev, const void *func, int V, int es, int gamma, int units, Plan &p) {
+    const int forced = env_cluster();
+    int R = env_int("MTP_RS_RING");
+    if (R < 2 || R > stream_max_ring()) R = 3;
+    int depth = gamma;  // stream every position without waiting for decisions
+    const char *de = std::getenv("MTP_RS_DEPTH");
+    if (de) depth = std::atoi(de);
+    if (depth < 0) depth = 0;
+    if (depth > gamma) depth = gamma;
+    const uint32_t cap = smem_optin(dev);
+    const int nw = stream_threads() / 32;
+    const int nv = V / (16 / es);
+    double best = 1e30;
+    long best_busy = -1;
+    bool found = false;
+    for (int C = 1; C <= MAX_C; ++C) {
+        if (forced && C != forced) continue;
+        const int S = C * nw;
+        if (S > stream_max_segments()) continue;
+        const int nvs = (nv + S - 1) / S;
+        if ((nvs + stream_chunk_vectors() - 1) / stream_chunk_vectors() > stream_max_chunks()) continue;
+        if (!forced && C > 1 && nvs < 64) continue;
+        const uint32_t smem = stream_hdr_bytes() + stream_rec_bytes(gamma, S) +
+                              static_cast<uint32_t>(nw * R) * stream_slot_bytes();
+        if (smem > cap) continue;
+        const int nc = max_clusters(dev, func, C, smem, stream_threads());
+        if (nc <= 0) continue;
+        int used = nc < units ? nc : units;
+        const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
+        if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+        // per wave: the sequence's share of the row (1 / C) plus a fixed
+        // latency term (exchanges, decision, sampling)
+        const double est = static_cast<double>((units + used - 1) / used) * (1.0 / C + 0.03);
+        const long busy = static_cast<long>(used) * C;
+        if (est < best - 1e-12 || (est < best + 1e-12 && busy > best_busy)) {
+            best = est;
+            best_busy = busy;
+            p = {C, 0, smem, 0, used, 1, stream_threads(), R, depth, nvs};
+            found = true;
+        }
+    }
+    return found;
 }
 
 // Persistent TV kernel: two target slots, nres (>= 2, ideally gamma) draft
@@ -209,11 +270,19 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     if (!aligned16(target) || !aligned16(draft)) return MTP_ERR_MISALIGNED;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
-    const void *func = row_kernel(dtype == MTP_DTYPE_F32 ? 0 : 1, mode);
-    if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
     const int es = esize(dtype);
+    const void *func = nullptr;
     Plan p;
-    if (!plan_row(dev, func, V, es, B, p)) return MTP_ERR_NO_DEVICE;
+    if (mode == MODE_VERIFY && stream_usable(V, es, gamma)) {
+        const void *sf = stream_kernel(dtype == MTP_DTYPE_F32 ? 0 : 1);
+        if (prepare_func(dev, sf) != cudaSuccess) return MTP_ERR_CUDA;
+        if (plan_stream(dev, sf, V, es, gamma, B, p)) func = sf;
+    }
+    if (!func) {
+        func = row_kernel(dtype == MTP_DTYPE_F32 ? 0 : 1, mode);
+        if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
+        if (!plan_row(dev, func, V, es, B, p)) return MTP_ERR_NO_DEVICE;
+    }
     VerifyArgs A;
     A.target = target;
     A.draft = draft;
@@ -226,6 +295,9 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     A.aligned = (V % (16 / es) == 0) ? 1 : 0;
     A.slice_bytes = p.slice_bytes;
     A.streams = p.streams;
+    A.ring = p.ring;
+    A.depth = p.depth;
+    A.seg_vectors = p.seg_vectors;
     A.tokens = tokens;
     A.accept_len = accept_len;
     A.alpha = alpha;
@@ -293,16 +365,26 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
                               int *clusters, int *smem_bytes, int *resident_drafts) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
-    if (op < 0 || op > 3 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (op < 0 || op > 4 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
-    const void *func = op == 3 ? tv_kernel(d) : row_kernel(d, op == 0 ? MODE_VERIFY : op == 1 ? MODE_VERIFY_STATS : MODE_STATS);
-    if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
+    const int es = esize(dtype);
     Plan p;
-    const bool ok = op == 3 ? plan_tv(dev, func, V, esize(dtype), gamma, units, p)
-                            : plan_row(dev, func, V, esize(dtype), units, p);
+    bool ok = false, streamed = false;
+    if (op == 0 && stream_usable(V, es, gamma)) {
+        const void *sf = stream_kernel(d);
+        if (prepare_func(dev, sf) != cudaSuccess) return MTP_ERR_CUDA;
+        ok = streamed = plan_stream(dev, sf, V, es, gamma, units, p);
+    }
+    if (!ok) {
+        const int mode = (op == 0 || op == 4) ? MODE_VERIFY : op == 1 ? MODE_VERIFY_STATS : MODE_STATS;
+        const void *func = op == 3 ? tv_kernel(d) : row_kernel(d, mode);
+        if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
+        ok = op == 3 ? plan_tv(dev, func, V, es, gamma, units, p) : plan_row(dev, func, V, es, units, p);
+    }
     if (!ok) return MTP_ERR_NO_DEVICE;
+    if (streamed) p.nres = p.ring;
     if (cluster_size) *cluster_size = p.C;
     if (clusters) *clusters = p.clusters;
     if (smem_bytes) *smem_bytes = static_cast<int>(p.smem);

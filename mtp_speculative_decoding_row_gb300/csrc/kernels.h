@@ -20,6 +20,9 @@ struct VerifyArgs {
     int aligned;            // every row starts on 16 bytes and V is whole vectors
     uint32_t slice_bytes;   // shared bytes of one row slice
     int streams;            // sequences in flight per CTA (1 or 2)
+    int ring;               // streaming kernel: chunk slots per warp
+    int depth;              // streaming kernel: positions streamed ahead of the last decision
+    int seg_vectors;        // streaming kernel: 16-byte vectors per warp segment
     int32_t *tokens;        // [B, gamma+1]      (verify modes)
     int32_t *accept_len;    // [B]               (verify modes)
     float *alpha;           // [B, gamma]        (stats modes)
@@ -48,8 +51,20 @@ uint32_t tv_hdr_bytes();
 int row_threads();
 int tv_threads();
 
+// Streaming verify kernel geometry.
+uint32_t stream_hdr_bytes();
+uint32_t stream_rec_bytes(int gamma, int S);
+int stream_max_gamma();
+int stream_threads();
+uint32_t stream_slot_bytes();
+int stream_chunk_vectors();
+int stream_max_chunks();
+int stream_max_segments();
+int stream_max_ring();
+
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);
+const void *stream_kernel(int dtype);
 const void *tv_kernel(int dtype);
 
 }  // namespace mtp

@@ -1,0 +1,1023 @@
+// stream_kernels.cu -- batched MTP rejection-sampling verification (no
+// statistics) as a streaming kernel on sm_103a.
+//
+// Method ("Breaking Entropy Bounds: Accelerating RL Training via MTP with
+// Rejection Sampling", §2 "Acceptance methods" and App. G.1; "EntMTP",
+// Related Work "Speculative Decoding"): with p_i = softmax(z_t[i] / T) and
+// q_i = softmax(z_d[i] / T), draft y_i is accepted iff u_i q_i(y_i) <
+// p_i(y_i); checking stops at the first rejection j, whose replacement is
+// drawn from norm(max(0, p_j - q_j)) by inverse CDF with u_gamma; after
+// gamma accepts the bonus token is drawn from p_gamma the same way.
+//
+// Layout of the work.  A persistent cluster of C CTAs x NW warps verifies
+// one sequence at a time (sequences cid, cid + NC, ...).  The vocabulary is
+// cut into S = C * NW contiguous segments of whole 16-byte vectors, one per
+// warp, and every warp works on its own segment only:
+//   - it streams its segment of each needed row through a private ring of
+//     R chunk slots (CV vectors of the target row + CV of the draft row per
+//     slot), filled by cp.async.bulk on one mbarrier per slot; lane 0 is the
+//     producer, the whole warp the consumer, and there is no CTA-wide barrier
+//     on the streaming path;
+//   - per position it folds each chunk into per-lane online softmax partials
+//     (exact running maximum, so no overflow path), reduces them across the
+//     warp and pushes a 16-byte record (plus the logits at the draft token,
+//     from the warp whose segment holds it) to every CTA of the cluster with
+//     st.async onto that position's exchange mbarrier;
+//   - it runs up to `depth` positions ahead of the last decided one, so the
+//     all-gather of one position overlaps the streaming of the next; every
+//     warp gathers the S records of a position and takes the accept decision
+//     itself (same records, same reduction order: the same verdict
+//     everywhere).  A rejection drops the look-ahead.
+// Sampling: after a rejection every warp re-streams its segment of rows j
+// (now mostly in L2) to form per-chunk residual sums, the segment totals are
+// all-gathered, and the warp owning the selected segment walks its chunk sums
+// and then the elements of one chunk (fetched again from global memory).
+// For the bonus token the per-chunk (max, sum) records taken while streaming
+// row gamma give the chunk weights directly, so row gamma is read only once.
+//
+// Exchange slots: each sequence uses gamma + 2 rounds (one per position and
+// one for the residual totals) in one of two banks, alternating by sequence.
+// Every warp pushes into every round of its sequence (a zero record where a
+// position was not needed), so every slot completes one phase per use; warp
+// 0 waits for all of them and re-arms the bank before it pushes anything for
+// the next sequence, and a bank is reused two sequences later, after every
+// warp has read it.
+#include <cstddef>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtp {
+namespace {
+
+constexpr int NT = 128;          // threads per CTA
+constexpr int NW = NT / 32;      // warps (segments) per CTA
+constexpr int CV = 128;          // vectors per row per chunk (2 KB)
+constexpr int QV = CV / 32;      // vectors per lane per chunk
+static_assert(QV == 4, "chunk layout: four vectors per lane per row");
+constexpr int MAXCH = 64;        // chunks per segment
+constexpr int MAXS = 64;         // segments per cluster (C * NW)
+constexpr int MAXG = 8;          // largest gamma
+constexpr int QMAX = MAXG + 2;   // exchange rounds per sequence
+constexpr int MAXR = 8;          // ring slots per warp
+constexpr uint32_t SLOT_BYTES = 2u * CV * 16u;
+
+enum { K_NORM = 0, K_RES = 1 };
+
+struct WarpShared {
+    unsigned long long full[MAXR];  // ring slot barriers
+    float cm[MAXCH];                // per-chunk maxima (bonus records)
+    float cs[MAXCH];                // per-chunk sums
+};
+
+// Fixed header; the exchange records ([2][gamma + 2][S + 1] float4) follow
+// it, then the warps' rings.
+struct StreamShared {
+    unsigned long long xbar[2][QMAX];
+    WarpShared w[NW];
+};
+constexpr uint32_t HDR_BYTES = (sizeof(StreamShared) + 127u) & ~127u;
+
+__host__ __device__ constexpr uint32_t rec_bytes(int gamma, int S) {
+    return ((2u * static_cast<uint32_t>(gamma + 2) * static_cast<uint32_t>(S + 1) * 16u) + 127u) & ~127u;
+}
+
+constexpr int ERR_BITS = F_NONFINITE | F_BAD_ID | F_BAD_TEMP | F_BAD_UNIFORM | F_TIMEOUT;
+
+template <typename Tin>
+struct NegInf;
+template <>
+struct NegInf<float> {
+    static constexpr uint32_t w = 0xff800000u;
+};
+template <>
+struct NegInf<bf16_t> {
+    static constexpr uint32_t w = 0xff80ff80u;
+};
+
+// Per-warp state (warp-uniform).
+struct Ctx {
+    // geometry
+    int C, rank, warp, lane, sg, S, NC, cid, R, depth, g, Q;
+    int seg_lo;   // first vector of the segment
+    int seg_n;    // vectors in the segment
+    int nch;      // chunks in the segment
+    unsigned char *ring;
+    WarpShared *ws;
+    float4 *rec;  // exchange records
+    // producer cursor: next chunk to issue
+    uint32_t pcount, pslot;
+    int p_ord, p_i, p_kind, p_c;
+    bool p_done;
+    const unsigned char *p_t, *p_d;  // segment start of the unit's rows (p_d null: target only)
+    // consumer
+    uint32_t ccount, cslot, cphase;
+    int c_ord, c_conf;  // consumer's sequence (order in the cluster list) and highest needed position
+    bool dead;
+    int bank;           // exchange bank of the current sequence
+    uint32_t bpar;      // bit b: phase parity of bank b's current use
+};
+
+__device__ __forceinline__ int seq_of(const Ctx &c, int ord) { return c.cid + ord * c.NC; }
+
+// What the sampling helpers need of a warp's segment (passed by value).
+struct Seg {
+    WarpShared *ws;
+    int seg_lo, seg_n, nch;
+};
+
+__device__ __forceinline__ Seg seg_of(const Ctx &c) { return {c.ws, c.seg_lo, c.seg_n, c.nch}; }
+
+// Point the producer at the first row of the sequence after `ord`.
+__device__ __forceinline__ void redirect_next(Ctx &c, int ord, int B) {
+    c.p_ord = ord + 1;
+    c.p_i = 0;
+    c.p_kind = K_NORM;
+    c.p_c = 0;
+    c.p_done = c.dead || c.nch == 0 || seq_of(c, ord + 1) >= B;
+}
+
+template <typename Tin>
+__device__ __forceinline__ const unsigned char *row_base(const VerifyArgs &A, bool target, int b, int i) {
+    const size_t row = target ? static_cast<size_t>(b) * (A.gamma + 1) + i : static_cast<size_t>(b) * A.gamma + i;
+    return reinterpret_cast<const unsigned char *>(target ? A.target : A.draft) +
+           row * static_cast<size_t>(A.V) * Store<Tin>::ES;
+}
+
+__device__ __forceinline__ int chunk_count(const Ctx &c, int ch) { return min(CV, c.seg_n - ch * CV); }
+__device__ __forceinline__ int chunk_count(const Seg &c, int ch) { return min(CV, c.seg_n - ch * CV); }
+
+// ------------------------------------------------------------ producer ----
+
+// Enter the producer's next unit: apply the look-ahead rule (positions up
+// to c_conf + depth of the consumer's sequence; a later sequence only once
+// the current one's path is fixed) and set the unit's row pointers.  False
+// when the producer has to wait or has no work left.
+template <typename Tin>
+__device__ __forceinline__ bool enter_unit(const VerifyArgs &A, Ctx &c) {
+    const int g = c.g;
+    if (c.p_kind == K_NORM) {
+        if (c.p_i > g) {  // end of the sequence's rows
+            if (c.p_ord == c.c_ord && c.c_conf < g) return false;
+            c.p_ord += 1;
+            c.p_i = 0;
+            if (seq_of(c, c.p_ord) >= A.B) {
+                c.p_done = true;
+                return false;
+            }
+        }
+        const int lim = (c.p_ord == c.c_ord) ? c.c_conf + c.depth : c.depth;
+        if (c.p_i > lim) return false;
+    }
+    const int b = seq_of(c, c.p_ord);
+    const size_t off = static_cast<size_t>(c.seg_lo) * 16u;
+    c.p_t = row_base<Tin>(A, true, b, c.p_i) + off;
+    c.p_d = c.p_i < g ? row_base<Tin>(A, false, b, c.p_i) + off : nullptr;
+    return true;
+}
+
+// Issue chunk copies while ring slots are free and the next chunk is needed
+// or inside the look-ahead.
+template <typename Tin>
+__device__ __forceinline__ void produce(const VerifyArgs &A, Ctx &c) {
+    if (c.p_done || c.dead) return;
+    while (c.pcount - c.ccount < static_cast<uint32_t>(c.R)) {
+        if (c.p_c == 0 && !enter_unit<Tin>(A, c)) break;
+        const int cnt = chunk_count(c, c.p_c);
+        if (c.lane == 0) {
+            // No proxy fence: every generic read of this slot has completed
+            // (its value was consumed) before the consumer released it.
+            const uint32_t bar = smem_addr(&c.ws->full[c.pslot]);
+            const uint32_t dst = smem_addr(c.ring + c.pslot * SLOT_BYTES);
+            const uint32_t bytes = static_cast<uint32_t>(cnt) * 16u;
+            const size_t off = static_cast<size_t>(c.p_c) * (CV * 16);
+            mbar_arrive_expect_tx_relaxed(bar, c.p_d ? 2u * bytes : bytes);
+            bulk_g2s(dst, c.p_t + off, bytes, bar);
+            if (c.p_d) bulk_g2s(dst + CV * 16, c.p_d + off, bytes, bar);
+        }
+        ++c.pcount;
+        if (++c.pslot == static_cast<uint32_t>(c.R)) c.pslot = 0;
+        if (++c.p_c == c.nch) {
+            c.p_c = 0;
+            if (c.p_kind == K_NORM) {
+                c.p_i += 1;  // p_i == g + 1 marks the end of the rows
+            } else {
+                c.p_kind = K_NORM;
+                c.p_i = c.g + 1;  // residual pass done: the sequence's path is fixed
+            }
+        }
+    }
+}
+
+// Wait for the next ring slot; false (and dead) on timeout.
+__device__ __forceinline__ bool slot_wait(Ctx &c) {
+    if (!mbar_wait_spin(smem_addr(&c.ws->full[c.cslot]), c.cphase)) {
+        c.dead = true;
+        return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void consumed(Ctx &c) {
+    ++c.ccount;
+    if (++c.cslot == static_cast<uint32_t>(c.R)) {
+        c.cslot = 0;
+        c.cphase ^= 1u;
+    }
+}
+
+// Drop every issued chunk that has not been consumed (waits for each copy).
+__device__ __forceinline__ void drain(Ctx &c) {
+    while (c.ccount != c.pcount) {
+        if (!mbar_wait_spin(smem_addr(&c.ws->full[c.cslot]), c.cphase)) c.dead = true;
+        consumed(c);
+    }
+}
+
+// ------------------------------------------------------------ exchange ----
+
+__device__ __forceinline__ float4 *rec_at(const Ctx &c, int bank, int i, int r) {
+    return c.rec + (static_cast<size_t>(bank * c.Q + i) * (c.S + 1) + r);
+}
+
+// Bytes every CTA receives in round i of a sequence: S records, plus the
+// draft-token logits for a position with a draft.
+__device__ __forceinline__ uint32_t round_bytes(const Ctx &c, int i) {
+    return static_cast<uint32_t>(c.S + (i < c.g ? 1 : 0)) * 16u;
+}
+
+// Push this warp's record for round i of the current bank into every CTA of
+// the cluster; `ylog` adds the draft-token record (warp holding y only).
+__device__ __forceinline__ void xpush(StreamShared &sh, const Ctx &c, int i, float4 v, bool ylog, float4 yv) {
+    if (c.lane < c.C) {
+        const uint32_t rbar = map_rank(smem_addr(&sh.xbar[c.bank][i]), c.lane);
+        const uint32_t ra = map_rank(smem_addr(rec_at(c, c.bank, i, c.sg)), c.lane);
+        st_async_v4(ra, v.x, v.y, v.z, v.w, rbar);
+        if (ylog) {
+            const uint32_t ya = map_rank(smem_addr(rec_at(c, c.bank, i, c.S)), c.lane);
+            st_async_v4(ya, yv.x, yv.y, yv.z, yv.w, rbar);
+        }
+    }
+}
+
+// Blocking (bounded) wait for round i of the current bank.
+__device__ __forceinline__ bool xwait(StreamShared &sh, Ctx &c, int i) {
+    if (!mbar_wait_spin(smem_addr(&sh.xbar[c.bank][i]), (c.bpar >> c.bank) & 1u)) c.dead = true;
+    return !c.dead;
+}
+
+// Non-blocking test of round i of the current bank.
+__device__ __forceinline__ bool xtest(StreamShared &sh, const Ctx &c, int i) {
+    return mbar_test_wait(smem_addr(&sh.xbar[c.bank][i]), (c.bpar >> c.bank) & 1u);
+}
+
+// ------------------------------------------------------------ sampling ----
+
+// Inverse CDF over the S segment totals held two per lane (segments 2l and
+// 2l + 1 in lane l, zero beyond S): the first segment whose running sum
+// exceeds u * R, in ascending order; if rounding leaves none, the last
+// segment with positive weight (and `last` is set so the walk below takes
+// the last positive element).  Returns -1 if R == 0.
+__device__ __forceinline__ int pick_segment(float t0, float t1, float u, float &rem, int &last) {
+    const int lane = threadIdx.x & 31;
+    const float tl = t0 + t1;
+    const float inc = warp_incl_scan(tl);
+    const float R = __shfl_sync(FULL, inc, 31);
+    last = 0;
+    rem = 0.f;
+    if (!(R > 0.f)) return -1;
+    const float x = u * R;
+    const unsigned bal = __ballot_sync(FULL, inc > x);
+    if (bal) {
+        const int L = __ffs(bal) - 1;
+        const float excl = __shfl_sync(FULL, inc - tl, L);
+        const float a0 = __shfl_sync(FULL, t0, L);
+        const float r = x - excl;
+        if (a0 > r) {
+            rem = r;
+            return 2 * L;
+        }
+        rem = r - a0;
+        return 2 * L + 1;
+    }
+    last = 1;
+    const unsigned pos = __ballot_sync(FULL, tl > 0.f);
+    const int L = 31 - __clz(pos);
+    const float a1 = __shfl_sync(FULL, t1, L);
+    (void)lane;
+    return a1 > 0.f ? 2 * L + 1 : 2 * L;
+}
+
+// Weights of one vector: residual max(0, p - q) (RES) or p relative to the
+// row maximum (otherwise).  p = 2^{z_t k - ct}, q = 2^{z_d k - cd}.
+template <typename Tin, bool RES>
+__device__ __forceinline__ void vweights(const uint4 &rt, const uint4 &rd, float k, float ct, float cd,
+                                         float (&w)[Store<Tin>::VEC]) {
+    constexpr int VEC = Store<Tin>::VEC;
+    float zt[VEC];
+    Store<Tin>::unpack(rt, zt);
+    if (RES) {
+        float zd[VEC];
+        Store<Tin>::unpack(rd, zd);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) w[e] = fmaxf(ex2(fmaf(zt[e], k, -ct)) - ex2(fmaf(zd[e], k, -cd)), 0.f);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) w[e] = ex2(fmaf(zt[e], k, -ct));
+    }
+}
+
+// Walk inside the owning warp: chunk sums (cs[c] * 2^{(cm[c] - ref) k} when
+// `scaled`), then the elements of the selected chunk fetched from global
+// memory, in ascending index order (chunk, 32-vector round, lane, element).
+// `rem` is the remaining mass inside this segment.  Falls back to the last
+// positive weight of the selected unit when rounding leaves no index.
+template <typename Tin, bool RES>
+__device__ __noinline__ int walk_segment(const Seg c, const unsigned char *trow, const unsigned char *drow,
+                                         bool scaled, float ref, float k, float ct, float cd, float rem,
+                                         int last) {
+    constexpr int VEC = Store<Tin>::VEC;
+    const int lane = threadIdx.x & 31;
+    // chunk selection
+    int ch = -1;
+    if (!last) {
+        for (int base = 0; base < c.nch && ch < 0; base += 32) {
+            const int q = base + lane;
+            float w = 0.f;
+            if (q < c.nch) w = scaled ? c.ws->cs[q] * ex2((c.ws->cm[q] - ref) * k) : c.ws->cs[q];
+            if (scaled && !(w == w)) w = 0.f;
+            const float inc = warp_incl_scan(w);
+            const float tot = __shfl_sync(FULL, inc, 31);
+            if (tot > rem) {
+                const unsigned bal = __ballot_sync(FULL, inc > rem);
+                const int L = __ffs(bal) - 1;
+                rem -= __shfl_sync(FULL, inc - w, L);
+                ch = base + L;
+            } else {
+                rem -= tot;
+            }
+        }
+    }
+    if (ch < 0) {
+        last = 1;
+        for (int base = 0; base < c.nch; base += 32) {
+            const int q = base + lane;
+            float w = 0.f;
+            if (q < c.nch) w = scaled ? c.ws->cs[q] * ex2((c.ws->cm[q] - ref) * k) : c.ws->cs[q];
+            const unsigned pos = __ballot_sync(FULL, w > 0.f);
+            if (pos) ch = base + 31 - __clz(pos);
+        }
+        if (ch < 0) return -1;
+    }
+    // element walk inside chunk ch
+    const int cnt = chunk_count(c, ch);
+    const size_t v0 = static_cast<size_t>(c.seg_lo) + static_cast<size_t>(ch) * CV;
+    const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + v0;
+    const uint4 *gd = RES ? reinterpret_cast<const uint4 *>(drow) + v0 : gt;
+    float w[QV][VEC];
+#pragma unroll
+    for (int r = 0; r < QV; ++r) {
+        const int j = r * 32 + lane;
+        if (j < cnt) {
+            const uint4 rt = __ldg(gt + j);
+            const uint4 rd = RES ? __ldg(gd + j) : rt;
+            vweights<Tin, RES>(rt, rd, k, ct, cd, w[r]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) w[r][e] = 0.f;
+        }
+    }
+    if (!last) {
+#pragma unroll
+        for (int r = 0; r < QV; ++r) {
+            float vs = w[r][0];
+#pragma unroll
+            for (int e = 1; e < VEC; ++e) vs += w[r][e];
+            const float inc = warp_incl_scan(vs);
+            const float tot = __shfl_sync(FULL, inc, 31);
+            if (tot > rem) {
+                const unsigned bal = __ballot_sync(FULL, inc > rem);
+                const int L = __ffs(bal) - 1;
+                const float excl = __shfl_sync(FULL, inc - vs, L);
+                int tk = -1;
+                if (lane == L) {
+                    float r2 = rem - excl;
+                    int ef = -1;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        if (ef < 0) {
+                            if (w[r][e] > r2) ef = e;
+                            else r2 -= w[r][e];
+                        }
+                    }
+                    if (ef < 0) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (w[r][e] > 0.f) ef = e;
+                    }
+                    tk = static_cast<int>((v0 + r * 32 + L) * VEC) + ef;
+                }
+                return __shfl_sync(FULL, tk, L);
+            }
+            rem -= tot;
+        }
+    }
+    // last positive element of the chunk
+    int best = -1;
+#pragma unroll
+    for (int r = 0; r < QV; ++r)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            if (w[r][e] > 0.f) best = max(best, static_cast<int>((v0 + r * 32 + lane) * VEC) + e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(FULL, best, o));
+    return best;
+}
+
+// Per-chunk sums of p (relative to `ref`) of this warp's segment of `trow`,
+// read straight from global memory (used when the residual mass rounds to 0).
+template <typename Tin>
+__device__ __noinline__ void direct_chunk_sums(const Seg c, const unsigned char *trow, float k, float ref) {
+    constexpr int VEC = Store<Tin>::VEC;
+    const int lane = threadIdx.x & 31;
+    for (int ch = 0; ch < c.nch; ++ch) {
+        const int cnt = chunk_count(c, ch);
+        const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + c.seg_lo + static_cast<size_t>(ch) * CV;
+        float s = 0.f;
+        for (int j = lane; j < cnt; j += 32) {
+            float w[VEC];
+            vweights<Tin, false>(__ldg(gt + j), __ldg(gt + j), k, ref * k, 0.f, w);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) s += w[e];
+        }
+        s = warp_allsum(s);
+        if (lane == 0) {
+            c.ws->cs[ch] = s;
+            c.ws->cm[ch] = ref;
+        }
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------ chunk math --
+
+// This lane's vectors q * 32 + lane (q < QV) of one chunk row, -inf beyond
+// the chunk's `cnt` vectors unless FULL.
+template <typename Tin, bool FULL>
+__device__ __forceinline__ void load_chunk(const unsigned char *buf, int cnt, int lane, uint4 (&r)[QV]) {
+    const uint4 NEG = make_uint4(NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w);
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        const int j = q * 32 + lane;
+        r[q] = (FULL || j < cnt) ? vec_at(buf, j) : NEG;
+    }
+}
+
+// Element e (0 <= e < VEC) of a 16-byte vector of logits, as float.
+template <typename Tin>
+__device__ __forceinline__ float vec_elem(const uint4 &v, int e) {
+    if (Store<Tin>::ES == 4) {
+        const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+        return __uint_as_float(w);
+    }
+    const int wi = e >> 1;
+    const uint32_t w = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// Maximum over the chunk row's elements held by this lane (NaN if any is).
+template <typename Tin>
+__device__ __forceinline__ float chunk_max(const uint4 (&r)[QV]);
+template <>
+__device__ __forceinline__ float chunk_max<bf16_t>(const uint4 (&r)[QV]) {
+    uint32_t a = bmax2_nan(r[0].x, r[0].y), b = bmax2_nan(r[0].z, r[0].w);
+#pragma unroll
+    for (int q = 1; q < QV; ++q) {
+        a = bmax2_nan(a, bmax2_nan(r[q].x, r[q].y));
+        b = bmax2_nan(b, bmax2_nan(r[q].z, r[q].w));
+    }
+    a = bmax2_nan(a, b);
+    return max_nan(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float chunk_max<float>(const uint4 (&r)[QV]) {
+    float a = max_nan(__uint_as_float(r[0].x), __uint_as_float(r[0].y));
+    float b = max_nan(__uint_as_float(r[0].z), __uint_as_float(r[0].w));
+#pragma unroll
+    for (int q = 1; q < QV; ++q) {
+        a = max_nan(a, max_nan(__uint_as_float(r[q].x), __uint_as_float(r[q].y)));
+        b = max_nan(b, max_nan(__uint_as_float(r[q].z), __uint_as_float(r[q].w)));
+    }
+    return max_nan(a, b);
+}
+
+// Fold one chunk row (its lane maximum cmx from chunk_max) into the lane's
+// running softmax partial without branches: exact running maximum m (a NaN
+// or +inf sets `bad`, the values that follow are then meaningless),
+// s = sum 2^{z k - m k}.  Returns the chunk's own sum relative to the
+// updated m.
+template <typename Tin>
+__device__ __forceinline__ float fold_regs(const uint4 (&r)[QV], float cmx, float k, float &m, float &s, int &bad) {
+    using St = Store<Tin>;
+    bad |= !(cmx < INFINITY);
+    const float nm = fmaxf(m, cmx);
+    const float mr = nm > -INFINITY ? nm : 0.f;  // all -inf so far: any finite reference
+    s *= ex2((m - mr) * k);
+    m = nm;
+    const float mk = mr * k;
+    // element pairs on the packed f32x2 pipe: one FMA and one add per pair
+    const uint64_t K2 = f2pack(k, k), NMK2 = f2pack(-mk, -mk);
+    uint64_t acc0 = f2pack(0.f, 0.f), acc1 = f2pack(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        const uint32_t w[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+#pragma unroll
+        for (int h = 0; h < 4; h += 2) {
+            uint64_t z0, z1;
+            if (St::ES == 2) {
+                z0 = bf16pair_f2(w[h]);
+                z1 = bf16pair_f2(w[h + 1]);
+            } else {
+                z0 = f2pack(__uint_as_float(w[h]), __uint_as_float(w[h + 1]));
+                z1 = 0;
+            }
+            float d0, d1;
+            f2unpack(f2fma(z0, K2, NMK2), d0, d1);
+            acc0 = f2add(acc0, f2pack(ex2(d0), ex2(d1)));
+            if (St::ES == 2) {
+                f2unpack(f2fma(z1, K2, NMK2), d0, d1);
+                acc1 = f2add(acc1, f2pack(ex2(d0), ex2(d1)));
+            }
+        }
+    }
+    float a0, a1, b0, b1;
+    f2unpack(acc0, a0, a1);
+    f2unpack(acc1, b0, b1);
+    const float cs = (a0 + a1) + (b0 + b1);
+    s += cs;
+    return cs;
+}
+
+// This lane's residual mass sum max(0, p - q) over one chunk (registers;
+// -inf padding contributes 0).
+template <typename Tin>
+__device__ __forceinline__ float res_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], float k, float ct,
+                                          float cd) {
+    constexpr int VEC = Store<Tin>::VEC;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        float w[VEC];
+        vweights<Tin, true>(rt[q], rd[q], k, ct, cd, w);
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2) {
+            ps0 += w[e];
+            ps1 += w[e + 1];
+        }
+    }
+    return ps0 + ps1;
+}
+
+// ----------------------------------------------------------------- kernel --
+
+// One position's round, gathered: log2 normalisers (log2 p = z k - ct),
+// target maximum, the logits at the draft token, flags, and this lane's two
+// target segment records (segments 2 lane and 2 lane + 1).
+struct Norm {
+    float ct, cd, Mt, Zty, Zdy;
+    int rf;
+    float m0, s0, m1, s1;
+};
+
+__device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool has_d) {
+    Norm r;
+    r.m0 = r.m1 = -INFINITY;
+    r.s0 = r.s1 = 0.f;
+    float dm = -INFINITY, ds = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int q = 2 * c.lane + h;
+        if (q < c.S) {
+            const float4 v = *rec_at(c, c.bank, i, q);
+            if (h == 0) {
+                r.m0 = v.x;
+                r.s0 = v.y;
+            } else {
+                r.m1 = v.x;
+                r.s1 = v.y;
+            }
+            if (v.w != 0.f) {  // draft partial of this lane (NaN propagates)
+                if (v.z > dm) {
+                    ds = (ds != 0.f ? ds * ex2((dm - v.z) * k) : 0.f) + v.w;
+                    dm = v.z;
+                } else {
+                    ds += v.w * ex2((v.z - dm) * k);
+                }
+            }
+        }
+    }
+    Soft lt;
+    lt.m = fmaxf(r.m0, r.m1);
+    lt.s = 0.f;
+    lt.s1 = 0.f;
+    if (lt.m > -INFINITY) {
+        if (r.s0 != 0.f) lt.s += r.s0 * ex2((r.m0 - lt.m) * k);
+        if (r.s1 != 0.f) lt.s += r.s1 * ex2((r.m1 - lt.m) * k);
+    } else if (r.s0 != 0.f || r.s1 != 0.f) {
+        lt.s = NAN;  // a flagged segment with no finite maximum
+    }
+    const Soft Ct = soft_warp_allreduce<false>(lt, k);
+    r.rf = 0;
+    if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY)) r.rf |= F_NONFINITE;
+    r.Mt = Ct.m;
+    r.ct = fmaf(Ct.m, k, log2f(Ct.s));
+    r.cd = 0.f;
+    r.Zty = r.Zdy = 0.f;
+    if (has_d) {
+        Soft ld;
+        ld.m = dm;
+        ld.s = ds;
+        ld.s1 = 0.f;
+        const Soft Cd = soft_warp_allreduce<false>(ld, k);
+        if (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY)) r.rf |= F_NONFINITE;
+        r.cd = fmaf(Cd.m, k, log2f(Cd.s));
+        const float4 y = *rec_at(c, c.bank, i, c.S);
+        r.Zty = y.x;
+        r.Zdy = y.y;
+    }
+    return r;
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) {
+    using St = Store<Tin>;
+    constexpr int VEC = St::VEC;
+    extern __shared__ __align__(128) unsigned char smem[];
+    StreamShared &sh = *reinterpret_cast<StreamShared *>(smem);
+
+    Ctx c;
+    c.C = static_cast<int>(cluster_size());
+    c.rank = static_cast<int>(cluster_rank());
+    c.cid = static_cast<int>(cluster_id_x());
+    c.NC = static_cast<int>(gridDim.x) / c.C;
+    c.warp = threadIdx.x >> 5;
+    c.lane = threadIdx.x & 31;
+    c.S = c.C * NW;
+    c.sg = c.rank * NW + c.warp;
+    c.R = A.ring;
+    c.depth = A.depth;
+    c.g = A.gamma;
+    c.Q = A.gamma + 2;
+    const int g = c.g;
+    const int nv = A.V / VEC;  // aligned rows only
+    const int nvs = A.seg_vectors;
+    c.seg_lo = min(nv, c.sg * nvs);
+    c.seg_n = min(nv, c.seg_lo + nvs) - c.seg_lo;
+    c.nch = (c.seg_n + CV - 1) / CV;
+    c.ws = &sh.w[c.warp];
+    c.rec = reinterpret_cast<float4 *>(smem + HDR_BYTES);
+    c.ring = smem + HDR_BYTES + rec_bytes(g, c.S) + static_cast<size_t>(c.warp) * c.R * SLOT_BYTES;
+    c.pcount = c.ccount = 0;
+    c.pslot = c.cslot = c.cphase = 0;
+    c.p_ord = 0;
+    c.p_i = 0;
+    c.p_kind = K_NORM;
+    c.p_c = 0;
+    c.p_done = (c.nch == 0) || (c.cid >= A.B);
+    c.p_t = c.p_d = nullptr;
+    c.c_ord = 0;
+    c.c_conf = 0;
+    c.dead = false;
+    c.bank = 0;
+    c.bpar = 0;
+
+    if (c.lane == 0)
+        for (int s = 0; s < c.R; ++s) mbar_init(smem_addr(&c.ws->full[s]), 1);
+    if (threadIdx.x == 0) {
+        for (int bk = 0; bk < 2; ++bk)
+            for (int i = 0; i < c.Q; ++i) mbar_init(smem_addr(&sh.xbar[bk][i]), 1);
+        fence_mbar_init();
+        for (int bk = 0; bk < 2; ++bk)
+            for (int i = 0; i < c.Q; ++i) mbar_arrive_expect_tx(smem_addr(&sh.xbar[bk][i]), round_bytes(c, i));
+    }
+    fence_mbar_init();
+    __syncthreads();
+    cluster_sync();  // every barrier of the cluster is initialised and armed before any push
+
+    // sequence parameters, prefetched one sequence ahead (lane l: u_l, y_l)
+    auto load_params = [&](int b, float &u, int &y, float &T) {
+        u = 2.f;
+        y = 0;
+        T = 1.f;
+        if (b < A.B) {
+            if (c.lane <= g) u = __ldg(A.unif + static_cast<size_t>(b) * (g + 1) + c.lane);
+            if (c.lane < g) y = __ldg(A.ids + static_cast<size_t>(b) * g + c.lane);
+            T = __ldg(A.temp + b);
+        }
+    };
+    float nu, nT;
+    int ny;
+    load_params(c.cid, nu, ny, nT);
+    produce<Tin>(A, c);
+
+    const float4 ZERO4 = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int ord = 0;; ++ord) {
+        const int b = seq_of(c, ord);
+        if (b >= A.B) break;
+        const float my_u = nu, T = nT;
+        const int my_y = ny;
+        load_params(seq_of(c, ord + 1), nu, ny, nT);
+        c.c_ord = ord;
+        c.c_conf = 0;
+
+        int flags = 0;
+        if (c.dead) flags |= F_TIMEOUT;
+        if (!(T > 0.f) || !(T < INFINITY)) flags |= F_BAD_TEMP;
+        {
+            const bool bad_y = (c.lane < g) && (my_y < 0 || my_y >= A.V);
+            const bool bad_u = (c.lane <= g) && !(my_u >= 0.f && my_u < 1.f);
+            if (__any_sync(FULL, bad_y)) flags |= F_BAD_ID;
+            if (__any_sync(FULL, bad_u)) flags |= F_BAD_UNIFORM;
+        }
+        const float k = LOG2E / T;
+        int n = 0;          // accepted drafts
+        int tok = -1;       // drawn token (owner warp)
+        int owner = 0;      // segment whose warp writes the outputs
+        // lanes l < gamma: does this warp's segment hold draft token y_l?
+        const int yv_l = my_y / VEC - c.seg_lo;
+        const bool own_l = (c.lane < g) && yv_l >= 0 && yv_l < c.seg_n;
+        const unsigned own_mask = __ballot_sync(FULL, own_l);
+
+        if (flags) {
+            drain(c);
+            redirect_next(c, ord, A.B);
+        } else {
+            int dec = 0;      // next position to decide
+            int pushed = -1;  // last position whose record this warp pushed
+            int rej = -1;     // rejected position
+            bool fin = false; // decisions over (rejection or error)
+            auto decide = [&](int i) {
+                const Norm r = gather_norm(c, i, k, true);
+                if (r.rf) {
+                    flags |= r.rf;
+                    fin = true;
+                    return;
+                }
+                const float ui = __shfl_sync(FULL, my_u, i);
+                if (log2f(ui) + fmaf(r.Zdy, k, -r.cd) < fmaf(r.Zty, k, -r.ct)) {
+                    ++n;
+                    ++dec;
+                    c.c_conf = dec;
+                } else {
+                    rej = i;
+                    fin = true;
+                }
+            };
+            for (int p = 0; p <= g && !fin && !c.dead; ++p) {
+                while (!fin && p > c.c_conf + c.depth) {
+                    if (!xwait(sh, c, dec)) break;
+                    decide(dec);
+                }
+                if (fin || c.dead) break;
+                const bool has_d = p < g;
+                const int y = __shfl_sync(FULL, my_y, has_d ? p : 0);
+                const bool owns_y = has_d && ((own_mask >> p) & 1u);
+                const int yv = y / VEC - c.seg_lo;
+                // ---- stream the segment of rows (t_p, d_p)
+                float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
+                float zty = 0.f, zdy = 0.f;
+                int bad = 0;
+                for (int ch = 0; ch < c.nch; ++ch) {
+                    // a decision may already be out: stop streaming a position
+                    // that will not be used
+                    if (dec < p && xtest(sh, c, dec)) {
+                        decide(dec);
+                        if (fin) break;
+                    }
+                    produce<Tin>(A, c);
+                    if (c.pcount == c.ccount) c.dead = true;  // nothing issued: never wait on it
+                    if (c.dead || !slot_wait(c)) break;
+                    const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
+                    const unsigned char *db = tb + CV * 16;
+                    const int cnt = chunk_count(c, ch);
+                    uint4 rt[QV], rd[QV];
+                    if (cnt == CV) {
+                        load_chunk<Tin, true>(tb, cnt, c.lane, rt);
+                        if (has_d) load_chunk<Tin, true>(db, cnt, c.lane, rd);
+                    } else {
+                        load_chunk<Tin, false>(tb, cnt, c.lane, rt);
+                        if (has_d) load_chunk<Tin, false>(db, cnt, c.lane, rd);
+                    }
+                    // the maxima consume every loaded register: the slot's
+                    // reads are complete before it is handed back
+                    const float cmt = chunk_max<Tin>(rt);
+                    const float cmd = has_d ? chunk_max<Tin>(rd) : 0.f;
+                    __syncwarp();
+                    consumed(c);  // the slot refills while this chunk is reduced
+                    produce<Tin>(A, c);
+                    if (owns_y && yv >= ch * CV && yv < ch * CV + cnt) {
+                        const int jv = yv - ch * CV, q = jv >> 5, e = y % VEC;
+                        const uint4 vt = q == 0 ? rt[0] : q == 1 ? rt[1] : q == 2 ? rt[2] : rt[3];
+                        const uint4 vd = q == 0 ? rd[0] : q == 1 ? rd[1] : q == 2 ? rd[2] : rd[3];
+                        zty = __shfl_sync(FULL, vec_elem<Tin>(vt, e), jv & 31);
+                        zdy = __shfl_sync(FULL, vec_elem<Tin>(vd, e), jv & 31);
+                    }
+                    const float csum = fold_regs<Tin>(rt, cmt, k, mt, st, bad);
+                    if (has_d) fold_regs<Tin>(rd, cmd, k, md, sd, bad);
+                    if (!has_d) {  // per-chunk record of row gamma for the bonus draw
+                        Soft a;
+                        a.m = mt;
+                        a.s = csum;
+                        a.s1 = 0.f;
+                        const Soft r = soft_warp_allreduce<false>(a, k);
+                        if (c.lane == 0) {
+                            c.ws->cm[ch] = r.m;
+                            c.ws->cs[ch] = r.s;
+                        }
+                    }
+                }
+                if (c.dead || fin) break;  // fin: position p abandoned, its round gets a zero record
+                // ---- warp record -> every CTA of the cluster
+                Soft a;
+                a.m = mt;
+                a.s = st;
+                a.s1 = 0.f;
+                const Soft wt = soft_warp_allreduce<false>(a, k);
+                a.m = md;
+                a.s = sd;
+                const Soft wd = soft_warp_allreduce<false>(a, k);
+                const bool wbad = warp_allor(bad) != 0;
+                xpush(sh, c, p, make_float4(wt.m, wbad ? NAN : wt.s, wd.m, wbad ? NAN : wd.s), owns_y,
+                      make_float4(zty, zdy, 0.f, 0.f));
+                pushed = p;
+                produce<Tin>(A, c);
+                // decisions whose rounds are already complete
+                while (!fin && dec < g && dec <= p && xtest(sh, c, dec)) decide(dec);
+            }
+            while (!fin && !c.dead && dec < g) {
+                if (!xwait(sh, c, dec)) break;
+                decide(dec);
+            }
+            // zero records for the rounds this warp did not fill
+            if (!c.dead)
+                for (int p = pushed + 1; p <= g; ++p) xpush(sh, c, p, ZERO4, p < g && ((own_mask >> p) & 1u), ZERO4);
+            if (c.dead) {
+                flags |= F_TIMEOUT;
+            } else if (flags & ERR_BITS) {
+                xpush(sh, c, g + 1, ZERO4, false, ZERO4);
+            } else if (rej >= 0) {
+                // ---- rejection at rej: residual pass over rows (t_rej, d_rej)
+                drain(c);
+                c.p_ord = ord;
+                c.p_i = rej;
+                c.p_kind = K_RES;
+                c.p_c = 0;
+                c.p_done = (c.nch == 0);
+                c.c_conf = g;  // the path is fixed: the producer may move on after the pass
+                const Norm r = gather_norm(c, rej, k, true);
+                float Rw = 0.f;
+                for (int ch = 0; ch < c.nch; ++ch) {
+                    produce<Tin>(A, c);
+                    if (c.pcount == c.ccount) c.dead = true;
+                    if (c.dead || !slot_wait(c)) break;
+                    const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
+                    const unsigned char *db = tb + CV * 16;
+                    const int cnt = chunk_count(c, ch);
+                    uint4 rt[QV], rd[QV];
+                    if (cnt == CV) {
+                        load_chunk<Tin, true>(tb, cnt, c.lane, rt);
+                        load_chunk<Tin, true>(db, cnt, c.lane, rd);
+                    } else {
+                        load_chunk<Tin, false>(tb, cnt, c.lane, rt);
+                        load_chunk<Tin, false>(db, cnt, c.lane, rd);
+                    }
+                    const float ps = warp_allsum(res_regs<Tin>(rt, rd, k, r.ct, r.cd));
+                    __syncwarp();
+                    consumed(c);
+                    produce<Tin>(A, c);
+                    if (c.lane == 0) c.ws->cs[ch] = ps;
+                    Rw += ps;
+                }
+                if (!c.dead) {
+                    xpush(sh, c, g + 1, make_float4(Rw, 0.f, 0.f, 0.f), false, ZERO4);
+                    xwait(sh, c, g + 1);
+                }
+                if (c.dead) {
+                    flags |= F_TIMEOUT;
+                } else {
+                    const int q0 = 2 * c.lane, q1 = 2 * c.lane + 1;
+                    const float t0 = q0 < c.S ? rec_at(c, c.bank, g + 1, q0)->x : 0.f;
+                    const float t1 = q1 < c.S ? rec_at(c, c.bank, g + 1, q1)->x : 0.f;
+                    const float uf = __shfl_sync(FULL, my_u, g);
+                    float rem;
+                    int last;
+                    const int sel = pick_segment(t0, t1, uf, rem, last);
+                    if (sel >= 0) {
+                        owner = sel;
+                        if (sel == c.sg)
+                            tok = walk_segment<Tin, true>(seg_of(c), row_base<Tin>(A, true, b, rej),
+                                                          row_base<Tin>(A, false, b, rej), false, 0.f, k, r.ct, r.cd,
+                                                          rem, last);
+                    } else {
+                        // residual mass rounded to zero: draw from p_rej
+                        flags |= F_ZERO_MASS;
+                        const float a0 = (r.s0 != 0.f) ? r.s0 * ex2((r.m0 - r.Mt) * k) : 0.f;
+                        const float a1 = (r.s1 != 0.f) ? r.s1 * ex2((r.m1 - r.Mt) * k) : 0.f;
+                        const int sp = pick_segment(a0, a1, uf, rem, last);
+                        if (sp < 0) {
+                            flags |= F_NONFINITE;
+                        } else {
+                            owner = sp;
+                            if (sp == c.sg) {
+                                direct_chunk_sums<Tin>(seg_of(c), row_base<Tin>(A, true, b, rej), k, r.Mt);
+                                tok = walk_segment<Tin, false>(seg_of(c), row_base<Tin>(A, true, b, rej), nullptr,
+                                                               true, r.Mt, k, r.Mt * k, 0.f, rem, last);
+                            }
+                        }
+                    }
+                }
+            } else {
+                // ---- bonus: all gamma drafts accepted, draw from p_gamma
+                xpush(sh, c, g + 1, ZERO4, false, ZERO4);
+                if (xwait(sh, c, g)) {
+                    const Norm r = gather_norm(c, g, k, false);
+                    if (r.rf) {
+                        flags |= r.rf;
+                    } else {
+                        const float a0 = (r.s0 != 0.f) ? r.s0 * ex2((r.m0 - r.Mt) * k) : 0.f;
+                        const float a1 = (r.s1 != 0.f) ? r.s1 * ex2((r.m1 - r.Mt) * k) : 0.f;
+                        const float uf = __shfl_sync(FULL, my_u, g);
+                        float rem;
+                        int last;
+                        const int sp = pick_segment(a0, a1, uf, rem, last);
+                        if (sp < 0) {
+                            flags |= F_NONFINITE;
+                        } else {
+                            owner = sp;
+                            if (sp == c.sg)
+                                tok = walk_segment<Tin, false>(seg_of(c), row_base<Tin>(A, true, b, g), nullptr, true,
+                                                               r.Mt, k, r.Mt * k, 0.f, rem, last);
+                        }
+                    }
+                } else {
+                    flags |= F_TIMEOUT;
+                }
+            }
+            if (flags & ERR_BITS) {
+                // drop the look-ahead; the next sequence starts from its first row
+                drain(c);
+                redirect_next(c, ord, A.B);
+            }
+            // warp 0 closes the bank: every round of this sequence complete, re-armed
+            if (c.warp == 0 && !c.dead) {
+                for (int i = 0; i < c.Q; ++i) {
+                    if (!xwait(sh, c, i)) break;
+                    if (c.lane == 0) mbar_arrive_expect_tx(smem_addr(&sh.xbar[c.bank][i]), round_bytes(c, i));
+                }
+                __syncwarp();
+            }
+            c.bpar ^= 1u << c.bank;
+            c.bank ^= 1;
+        }
+        if (flags & ERR_BITS) owner = 0;
+        if (tok < 0 && !(flags & ERR_BITS) && c.sg == owner) flags |= F_NONFINITE;
+        // ---- outputs, written by the owning warp
+        if (c.sg == owner || (c.dead && c.sg == 0)) {
+            const bool err = (flags & ERR_BITS) != 0;
+            if (c.lane <= g) {
+                int v = -1;
+                if (!err) v = (c.lane < n) ? my_y : (c.lane == n ? tok : -1);
+                A.tokens[static_cast<size_t>(b) * (g + 1) + c.lane] = v;
+            }
+            if (c.lane == 0) {
+                A.accept_len[b] = err ? -1 : n;
+                if (A.flags) A.flags[b] = flags;
+            }
+        }
+        produce<Tin>(A, c);
+    }
+
+    drain(c);
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while a peer may still push into it
+}
+
+}  // namespace
+
+uint32_t stream_hdr_bytes() { return HDR_BYTES; }
+uint32_t stream_rec_bytes(int gamma, int S) { return rec_bytes(gamma, S); }
+int stream_threads() { return NT; }
+uint32_t stream_slot_bytes() { return SLOT_BYTES; }
+int stream_chunk_vectors() { return CV; }
+int stream_max_chunks() { return MAXCH; }
+int stream_max_segments() { return MAXS; }
+int stream_max_ring() { return MAXR; }
+int stream_max_gamma() { return MAXG; }
+
+const void *stream_kernel(int dtype) {
+    if (dtype == 0) return reinterpret_cast<const void *>(&stream_kernel_impl<float>);
+    return reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t>);
+}
+
+}  // namespace mtp

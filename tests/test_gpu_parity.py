@@ -60,10 +60,74 @@ def test_verify_sweep(V, dtype, gamma, T, C, with_stats):
     assert rep["exact"] >= x.B - 2
 
 
-@pytest.mark.parametrize("name", ["verify64", "rl512", "deep256"])
-def test_verify_full_configs(name):
+@pytest.mark.parametrize("V,dtype,gamma,T,C", [s for s in SWEEP if s[0] % (4 if s[1] == "f32" else 8) == 0])
+def test_verify_sweep_resident_kernel(V, dtype, gamma, T, C):
+    """Aligned rows without statistics normally take the streaming kernel;
+    the cluster-resident kernel must agree as well."""
+    x = W.verify_inputs(f"sweep{V}", 24, gamma, V, dtype, 1000 + V + gamma, family="sigma",
+                        sigmas=np.linspace(0.5, 4.0, 24), delta=np.linspace(0.0, 1.0, 24), temperature=T)
+    with env(MTP_RS_CLUSTER=C, MTP_RS_VERIFY_KERNEL="resident"):
+        rep, g, o = _check_verify(x, False, f"resident V={V} {dtype} gamma={gamma} C={C}")
+    assert rep["exact"] >= x.B - 2
+
+
+@pytest.mark.parametrize("ring,depth,C,clusters", [(2, 0, 4, None), (2, 1, 8, 3), (3, 5, None, None), (8, 5, 2, 5),
+                                                   (4, 0, 16, 2), (3, 2, 1, 7), (2, 3, 4, 1)])
+def test_verify_stream_ring_variants(ring, depth, C, clusters):
+    """Ring slots, look-ahead depth, cluster size and several sequences per
+    cluster (capped grid) on rows with many rejections."""
+    B = 40
+    x = W.verify_inputs("ring", B, 5, 40000, "bf16", 77, family="sigma", sigmas=np.linspace(0.5, 6.0, B),
+                        delta=np.linspace(0.0, 2.0, B), temperature=np.linspace(0.6, 1.3, B))
+    with env(MTP_RS_RING=ring, MTP_RS_DEPTH=depth, MTP_RS_CLUSTER=C, MTP_RS_MAX_CLUSTERS=clusters):
+        rep, g, o = _check_verify(x, False, f"ring={ring} depth={depth} C={C} clusters={clusters}")
+    n = g["accept_len"]
+    assert (n == x.gamma).any() and (n < x.gamma).any() and (n == 0).any()
+
+
+def test_verify_stream_bad_rows_between_good_ones():
+    """Flagged sequences in the middle of a cluster's list: the look-ahead
+    into them is dropped and the following sequences stay exact."""
+    B = 64
+    x = W.verify_inputs("mix", B, 3, 8192, "f32", 78, family="sigma", sigmas=np.linspace(1.0, 5.0, B),
+                        delta=np.linspace(0.1, 1.5, B))
+    x.temperature[5::9] = -1.0
+    x.draft_ids[7::11, 1] = -4
+    x.uniforms[3::13, 3] = 1.5
+    x.target[10::17, 1, 100] = np.inf
+    with env(MTP_RS_CLUSTER=2, MTP_RS_MAX_CLUSTERS=5):
+        rep, g, o = _check_verify(x, False, "bad rows mixed")
+    np.testing.assert_array_equal(g["row_flags"], o["flags"])
+    assert (o["flags"] != 0).sum() >= 10
+
+
+@pytest.mark.parametrize("gamma", [8, 9, 31, 32])
+def test_verify_long_draft(gamma):
+    """gamma = 8 is the streaming kernel's limit; longer drafts take the
+    cluster-resident kernel."""
+    x = W.verify_inputs("long", 6, gamma, 2048, "bf16", 79, family="sigma", sigmas=1.0, delta=0.0)
+    j = min(20, gamma - 2)
+    x.draft[2, j] = x.draft[2, j] ^ np.uint16(0x0040)  # a perturbed row late in one sequence
+    rep, g, o = _check_verify(x, False, f"gamma={gamma}")
+    assert rep["exact"] + rep["near_margin"] == x.B
+
+
+def test_verify_plan_kernels():
+    import mtp_speculative_decoding_row_gb300 as mtp
+    p = mtp.mtp_query_plan("verify", "bf16", 64, 3, 151936)
+    assert p["resident_drafts"] > 0  # streaming kernel: ring slots per warp
+    q = mtp.mtp_query_plan("verify_resident", "bf16", 64, 3, 151936)
+    assert q["resident_drafts"] == 0
+    with env(MTP_RS_VERIFY_KERNEL="resident"):
+        assert mtp.mtp_query_plan("verify", "bf16", 64, 3, 151936)["resident_drafts"] == 0
+
+
+@pytest.mark.parametrize("name,kernel", [("verify64", None), ("rl512", None), ("deep256", None),
+                                         ("verify64", "resident"), ("rl512", "resident")])
+def test_verify_full_configs(name, kernel):
     x = W.config(name)
-    rep, g, o = _check_verify(x, x.want_stats, name)
+    with env(MTP_RS_VERIFY_KERNEL=kernel):
+        rep, g, o = _check_verify(x, x.want_stats, name)
     assert rep["exact"] + rep["near_margin"] == x.B
     # both the accept path and the residual path occur at these sizes
     n = g["accept_len"]
