@@ -27,6 +27,8 @@ struct Plan {
     int threads = 0;   // threads per CTA
     int ring = 0;      // streaming kernel: chunk slots per warp
     int depth = 0;     // streaming kernel: look-ahead positions
+    int cv = 0;        // streaming kernel: vectors of each row per chunk
+    const void *func = nullptr;
     int seg_vectors = 0;
 };
 
@@ -154,10 +156,20 @@ bool stream_usable(int V, int es, int gamma) {
     return gamma <= stream_max_gamma() && V % (16 / es) == 0;
 }
 
-bool plan_stream(int dev, const void *func, int V, int es, int gamma, int units, Plan &p) {
+// Chunk size for a warp segment of nvs vectors: 3 KB chunks when the
+// segment holds at least eight of them (fewer copies and less per-chunk
+// control for the same bytes), else 2 KB chunks (less waste in the ragged
+// last chunk of short segments).
+int stream_chunk_for(int nvs) {
+    const int forced = env_int("MTP_RS_CHUNK");
+    if (forced == 128 || forced == 192) return forced;
+    return nvs >= 8 * 192 ? 192 : 128;
+}
+
+bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) {
     const int forced = env_cluster();
     int R = env_int("MTP_RS_RING");
-    if (R < 2 || R > stream_max_ring()) R = 3;
+    if (R < 2 || R > stream_max_ring()) R = 2;
     int depth = gamma;  // stream every position without waiting for decisions
     const char *de = std::getenv("MTP_RS_DEPTH");
     if (de) depth = std::atoi(de);
@@ -174,11 +186,14 @@ bool plan_stream(int dev, const void *func, int V, int es, int gamma, int units,
         const int S = C * nw;
         if (S > stream_max_segments()) continue;
         const int nvs = (nv + S - 1) / S;
-        if ((nvs + stream_chunk_vectors() - 1) / stream_chunk_vectors() > stream_max_chunks()) continue;
+        const int cv = stream_chunk_for(nvs);
+        if ((nvs + cv - 1) / cv > stream_max_chunks()) continue;
         if (!forced && C > 1 && nvs < 64) continue;
         const uint32_t smem = stream_hdr_bytes() + stream_rec_bytes(gamma, S) +
-                              static_cast<uint32_t>(nw * R) * stream_slot_bytes();
+                              static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
         if (smem > cap) continue;
+        const void *func = stream_kernel(dtype, cv);
+        if (prepare_func(dev, func) != cudaSuccess) return false;
         const int nc = max_clusters(dev, func, C, smem, stream_threads());
         if (nc <= 0) continue;
         int used = nc < units ? nc : units;
@@ -191,7 +206,16 @@ bool plan_stream(int dev, const void *func, int V, int es, int gamma, int units,
         if (est < best - 1e-12 || (est < best + 1e-12 && busy > best_busy)) {
             best = est;
             best_busy = busy;
-            p = {C, 0, smem, 0, used, 1, stream_threads(), R, depth, nvs};
+            p = Plan{};
+            p.C = C;
+            p.smem = smem;
+            p.clusters = used;
+            p.threads = stream_threads();
+            p.ring = R;
+            p.depth = depth;
+            p.seg_vectors = nvs;
+            p.cv = cv;
+            p.func = func;
             found = true;
         }
     }
@@ -274,9 +298,7 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     const void *func = nullptr;
     Plan p;
     if (mode == MODE_VERIFY && stream_usable(V, es, gamma)) {
-        const void *sf = stream_kernel(dtype == MTP_DTYPE_F32 ? 0 : 1);
-        if (prepare_func(dev, sf) != cudaSuccess) return MTP_ERR_CUDA;
-        if (plan_stream(dev, sf, V, es, gamma, B, p)) func = sf;
+        if (plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, gamma, B, p)) func = p.func;
     }
     if (!func) {
         func = row_kernel(dtype == MTP_DTYPE_F32 ? 0 : 1, mode);
@@ -372,11 +394,7 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     const int es = esize(dtype);
     Plan p;
     bool ok = false, streamed = false;
-    if (op == 0 && stream_usable(V, es, gamma)) {
-        const void *sf = stream_kernel(d);
-        if (prepare_func(dev, sf) != cudaSuccess) return MTP_ERR_CUDA;
-        ok = streamed = plan_stream(dev, sf, V, es, gamma, units, p);
-    }
+    if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
     if (!ok) {
         const int mode = (op == 0 || op == 4) ? MODE_VERIFY : op == 1 ? MODE_VERIFY_STATS : MODE_STATS;
         const void *func = op == 3 ? tv_kernel(d) : row_kernel(d, mode);

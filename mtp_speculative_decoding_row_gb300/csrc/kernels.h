@@ -56,15 +56,14 @@ uint32_t stream_hdr_bytes();
 uint32_t stream_rec_bytes(int gamma, int S);
 int stream_max_gamma();
 int stream_threads();
-uint32_t stream_slot_bytes();
-int stream_chunk_vectors();
+uint32_t stream_slot_bytes(int cv);
 int stream_max_chunks();
 int stream_max_segments();
 int stream_max_ring();
 
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);
-const void *stream_kernel(int dtype);
+const void *stream_kernel(int dtype, int cv);  // cv: 128 or 192 vectors per chunk
 const void *tv_kernel(int dtype);
 
 }  // namespace mtp

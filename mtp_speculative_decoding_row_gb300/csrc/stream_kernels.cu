@@ -52,15 +52,13 @@ namespace {
 
 constexpr int NT = 128;          // threads per CTA
 constexpr int NW = NT / 32;      // warps (segments) per CTA
-constexpr int CV = 128;          // vectors per row per chunk (2 KB)
-constexpr int QV = CV / 32;      // vectors per lane per chunk
-static_assert(QV == 4, "chunk layout: four vectors per lane per row");
+// Chunk geometry is a template parameter of the kernel: CV vectors of each
+// row per ring slot (128 = 2 KB or 192 = 3 KB), CV / 32 per lane.
 constexpr int MAXCH = 64;        // chunks per segment
 constexpr int MAXS = 64;         // segments per cluster (C * NW)
 constexpr int MAXG = 8;          // largest gamma
 constexpr int QMAX = MAXG + 2;   // exchange rounds per sequence
 constexpr int MAXR = 8;          // ring slots per warp
-constexpr uint32_t SLOT_BYTES = 2u * CV * 16u;
 
 enum { K_NORM = 0, K_RES = 1 };
 
@@ -99,6 +97,7 @@ struct NegInf<bf16_t> {
 struct Ctx {
     // geometry
     int C, rank, warp, lane, sg, S, NC, cid, R, depth, g, Q;
+    int cv;       // vectors of each row per chunk
     int seg_lo;   // first vector of the segment
     int seg_n;    // vectors in the segment
     int nch;      // chunks in the segment
@@ -123,10 +122,10 @@ __device__ __forceinline__ int seq_of(const Ctx &c, int ord) { return c.cid + or
 // What the sampling helpers need of a warp's segment (passed by value).
 struct Seg {
     WarpShared *ws;
-    int seg_lo, seg_n, nch;
+    int seg_lo, seg_n, nch, cv;
 };
 
-__device__ __forceinline__ Seg seg_of(const Ctx &c) { return {c.ws, c.seg_lo, c.seg_n, c.nch}; }
+__device__ __forceinline__ Seg seg_of(const Ctx &c) { return {c.ws, c.seg_lo, c.seg_n, c.nch, c.cv}; }
 
 // Point the producer at the first row of the sequence after `ord`.
 __device__ __forceinline__ void redirect_next(Ctx &c, int ord, int B) {
@@ -144,8 +143,8 @@ __device__ __forceinline__ const unsigned char *row_base(const VerifyArgs &A, bo
            row * static_cast<size_t>(A.V) * Store<Tin>::ES;
 }
 
-__device__ __forceinline__ int chunk_count(const Ctx &c, int ch) { return min(CV, c.seg_n - ch * CV); }
-__device__ __forceinline__ int chunk_count(const Seg &c, int ch) { return min(CV, c.seg_n - ch * CV); }
+__device__ __forceinline__ int chunk_count(const Ctx &c, int ch) { return min(c.cv, c.seg_n - ch * c.cv); }
+__device__ __forceinline__ int chunk_count(const Seg &c, int ch) { return min(c.cv, c.seg_n - ch * c.cv); }
 
 // ------------------------------------------------------------ producer ----
 
@@ -188,12 +187,12 @@ __device__ __forceinline__ void produce(const VerifyArgs &A, Ctx &c) {
             // No proxy fence: every generic read of this slot has completed
             // (its value was consumed) before the consumer released it.
             const uint32_t bar = smem_addr(&c.ws->full[c.pslot]);
-            const uint32_t dst = smem_addr(c.ring + c.pslot * SLOT_BYTES);
+            const uint32_t dst = smem_addr(c.ring + c.pslot * (2u * c.cv * 16u));
             const uint32_t bytes = static_cast<uint32_t>(cnt) * 16u;
-            const size_t off = static_cast<size_t>(c.p_c) * (CV * 16);
+            const size_t off = static_cast<size_t>(c.p_c) * (c.cv * 16);
             mbar_arrive_expect_tx_relaxed(bar, c.p_d ? 2u * bytes : bytes);
             bulk_g2s(dst, c.p_t + off, bytes, bar);
-            if (c.p_d) bulk_g2s(dst + CV * 16, c.p_d + off, bytes, bar);
+            if (c.p_d) bulk_g2s(dst + c.cv * 16, c.p_d + off, bytes, bar);
         }
         ++c.pcount;
         if (++c.pslot == static_cast<uint32_t>(c.R)) c.pslot = 0;
@@ -332,7 +331,7 @@ __device__ __forceinline__ void vweights(const uint4 &rt, const uint4 &rd, float
 // memory, in ascending index order (chunk, 32-vector round, lane, element).
 // `rem` is the remaining mass inside this segment.  Falls back to the last
 // positive weight of the selected unit when rounding leaves no index.
-template <typename Tin, bool RES>
+template <typename Tin, bool RES, int QV>
 __device__ __noinline__ int walk_segment(const Seg c, const unsigned char *trow, const unsigned char *drow,
                                          bool scaled, float ref, float k, float ct, float cd, float rem,
                                          int last) {
@@ -371,7 +370,7 @@ __device__ __noinline__ int walk_segment(const Seg c, const unsigned char *trow,
     }
     // element walk inside chunk ch
     const int cnt = chunk_count(c, ch);
-    const size_t v0 = static_cast<size_t>(c.seg_lo) + static_cast<size_t>(ch) * CV;
+    const size_t v0 = static_cast<size_t>(c.seg_lo) + static_cast<size_t>(ch) * c.cv;
     const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + v0;
     const uint4 *gd = RES ? reinterpret_cast<const uint4 *>(drow) + v0 : gt;
     float w[QV][VEC];
@@ -442,7 +441,7 @@ __device__ __noinline__ void direct_chunk_sums(const Seg c, const unsigned char 
     const int lane = threadIdx.x & 31;
     for (int ch = 0; ch < c.nch; ++ch) {
         const int cnt = chunk_count(c, ch);
-        const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + c.seg_lo + static_cast<size_t>(ch) * CV;
+        const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + c.seg_lo + static_cast<size_t>(ch) * c.cv;
         float s = 0.f;
         for (int j = lane; j < cnt; j += 32) {
             float w[VEC];
@@ -463,7 +462,7 @@ __device__ __noinline__ void direct_chunk_sums(const Seg c, const unsigned char 
 
 // This lane's vectors q * 32 + lane (q < QV) of one chunk row, -inf beyond
 // the chunk's `cnt` vectors unless FULL.
-template <typename Tin, bool FULL>
+template <typename Tin, bool FULL, int QV>
 __device__ __forceinline__ void load_chunk(const unsigned char *buf, int cnt, int lane, uint4 (&r)[QV]) {
     const uint4 NEG = make_uint4(NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w);
 #pragma unroll
@@ -486,29 +485,27 @@ __device__ __forceinline__ float vec_elem(const uint4 &v, int e) {
 }
 
 // Maximum over the chunk row's elements held by this lane (NaN if any is).
-template <typename Tin>
-__device__ __forceinline__ float chunk_max(const uint4 (&r)[QV]);
-template <>
-__device__ __forceinline__ float chunk_max<bf16_t>(const uint4 (&r)[QV]) {
-    uint32_t a = bmax2_nan(r[0].x, r[0].y), b = bmax2_nan(r[0].z, r[0].w);
+template <typename Tin, int QV>
+__device__ __forceinline__ float chunk_max(const uint4 (&r)[QV]) {
+    if constexpr (Store<Tin>::ES == 2) {
+        uint32_t a = bmax2_nan(r[0].x, r[0].y), b = bmax2_nan(r[0].z, r[0].w);
 #pragma unroll
-    for (int q = 1; q < QV; ++q) {
-        a = bmax2_nan(a, bmax2_nan(r[q].x, r[q].y));
-        b = bmax2_nan(b, bmax2_nan(r[q].z, r[q].w));
-    }
-    a = bmax2_nan(a, b);
-    return max_nan(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
-}
-template <>
-__device__ __forceinline__ float chunk_max<float>(const uint4 (&r)[QV]) {
-    float a = max_nan(__uint_as_float(r[0].x), __uint_as_float(r[0].y));
-    float b = max_nan(__uint_as_float(r[0].z), __uint_as_float(r[0].w));
+        for (int q = 1; q < QV; ++q) {
+            a = bmax2_nan(a, bmax2_nan(r[q].x, r[q].y));
+            b = bmax2_nan(b, bmax2_nan(r[q].z, r[q].w));
+        }
+        a = bmax2_nan(a, b);
+        return max_nan(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+    } else {
+        float a = max_nan(__uint_as_float(r[0].x), __uint_as_float(r[0].y));
+        float b = max_nan(__uint_as_float(r[0].z), __uint_as_float(r[0].w));
 #pragma unroll
-    for (int q = 1; q < QV; ++q) {
-        a = max_nan(a, max_nan(__uint_as_float(r[q].x), __uint_as_float(r[q].y)));
-        b = max_nan(b, max_nan(__uint_as_float(r[q].z), __uint_as_float(r[q].w)));
+        for (int q = 1; q < QV; ++q) {
+            a = max_nan(a, max_nan(__uint_as_float(r[q].x), __uint_as_float(r[q].y)));
+            b = max_nan(b, max_nan(__uint_as_float(r[q].z), __uint_as_float(r[q].w)));
+        }
+        return max_nan(a, b);
     }
-    return max_nan(a, b);
 }
 
 // Fold one chunk row (its lane maximum cmx from chunk_max) into the lane's
@@ -516,7 +513,7 @@ __device__ __forceinline__ float chunk_max<float>(const uint4 (&r)[QV]) {
 // or +inf sets `bad`, the values that follow are then meaningless),
 // s = sum 2^{z k - m k}.  Returns the chunk's own sum relative to the
 // updated m.
-template <typename Tin>
+template <typename Tin, int QV>
 __device__ __forceinline__ float fold_regs(const uint4 (&r)[QV], float cmx, float k, float &m, float &s, int &bad) {
     using St = Store<Tin>;
     bad |= !(cmx < INFINITY);
@@ -560,7 +557,7 @@ __device__ __forceinline__ float fold_regs(const uint4 (&r)[QV], float cmx, floa
 
 // This lane's residual mass sum max(0, p - q) over one chunk (registers;
 // -inf padding contributes 0).
-template <typename Tin>
+template <typename Tin, int QV>
 __device__ __forceinline__ float res_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], float k, float ct,
                                           float cd) {
     constexpr int VEC = Store<Tin>::VEC;
@@ -648,10 +645,13 @@ __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool h
     return r;
 }
 
-template <typename Tin>
+template <typename Tin, int CV>
 __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) {
     using St = Store<Tin>;
     constexpr int VEC = St::VEC;
+    constexpr int QV = CV / 32;
+    static_assert(CV % 32 == 0, "chunk layout: whole vectors per lane");
+    constexpr uint32_t SLOT_BYTES = 2u * CV * 16u;
     extern __shared__ __align__(128) unsigned char smem[];
     StreamShared &sh = *reinterpret_cast<StreamShared *>(smem);
 
@@ -673,6 +673,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
     const int nvs = A.seg_vectors;
     c.seg_lo = min(nv, c.sg * nvs);
     c.seg_n = min(nv, c.seg_lo + nvs) - c.seg_lo;
+    c.cv = CV;
     c.nch = (c.seg_n + CV - 1) / CV;
     c.ws = &sh.w[c.warp];
     c.rec = reinterpret_cast<float4 *>(smem + HDR_BYTES);
@@ -803,28 +804,34 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     const int cnt = chunk_count(c, ch);
                     uint4 rt[QV], rd[QV];
                     if (cnt == CV) {
-                        load_chunk<Tin, true>(tb, cnt, c.lane, rt);
-                        if (has_d) load_chunk<Tin, true>(db, cnt, c.lane, rd);
+                        load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
+                        if (has_d) load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
                     } else {
-                        load_chunk<Tin, false>(tb, cnt, c.lane, rt);
-                        if (has_d) load_chunk<Tin, false>(db, cnt, c.lane, rd);
+                        load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
+                        if (has_d) load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
                     }
                     // the maxima consume every loaded register: the slot's
                     // reads are complete before it is handed back
-                    const float cmt = chunk_max<Tin>(rt);
-                    const float cmd = has_d ? chunk_max<Tin>(rd) : 0.f;
+                    const float cmt = chunk_max<Tin, QV>(rt);
+                    const float cmd = has_d ? chunk_max<Tin, QV>(rd) : 0.f;
                     __syncwarp();
                     consumed(c);  // the slot refills while this chunk is reduced
                     produce<Tin>(A, c);
                     if (owns_y && yv >= ch * CV && yv < ch * CV + cnt) {
                         const int jv = yv - ch * CV, q = jv >> 5, e = y % VEC;
-                        const uint4 vt = q == 0 ? rt[0] : q == 1 ? rt[1] : q == 2 ? rt[2] : rt[3];
-                        const uint4 vd = q == 0 ? rd[0] : q == 1 ? rd[1] : q == 2 ? rd[2] : rd[3];
+                        uint4 vt = rt[0], vd = rd[0];
+#pragma unroll
+                        for (int qq = 1; qq < QV; ++qq) {
+                            if (q == qq) {
+                                vt = rt[qq];
+                                vd = rd[qq];
+                            }
+                        }
                         zty = __shfl_sync(FULL, vec_elem<Tin>(vt, e), jv & 31);
                         zdy = __shfl_sync(FULL, vec_elem<Tin>(vd, e), jv & 31);
                     }
-                    const float csum = fold_regs<Tin>(rt, cmt, k, mt, st, bad);
-                    if (has_d) fold_regs<Tin>(rd, cmd, k, md, sd, bad);
+                    const float csum = fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
+                    if (has_d) fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
                     if (!has_d) {  // per-chunk record of row gamma for the bonus draw
                         Soft a;
                         a.m = mt;
@@ -886,13 +893,13 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     const int cnt = chunk_count(c, ch);
                     uint4 rt[QV], rd[QV];
                     if (cnt == CV) {
-                        load_chunk<Tin, true>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, true>(db, cnt, c.lane, rd);
+                        load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
+                        load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
                     } else {
-                        load_chunk<Tin, false>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, false>(db, cnt, c.lane, rd);
+                        load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
+                        load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
                     }
-                    const float ps = warp_allsum(res_regs<Tin>(rt, rd, k, r.ct, r.cd));
+                    const float ps = warp_allsum(res_regs<Tin, QV>(rt, rd, k, r.ct, r.cd));
                     __syncwarp();
                     consumed(c);
                     produce<Tin>(A, c);
@@ -916,7 +923,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     if (sel >= 0) {
                         owner = sel;
                         if (sel == c.sg)
-                            tok = walk_segment<Tin, true>(seg_of(c), row_base<Tin>(A, true, b, rej),
+                            tok = walk_segment<Tin, true, QV>(seg_of(c), row_base<Tin>(A, true, b, rej),
                                                           row_base<Tin>(A, false, b, rej), false, 0.f, k, r.ct, r.cd,
                                                           rem, last);
                     } else {
@@ -931,7 +938,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             owner = sp;
                             if (sp == c.sg) {
                                 direct_chunk_sums<Tin>(seg_of(c), row_base<Tin>(A, true, b, rej), k, r.Mt);
-                                tok = walk_segment<Tin, false>(seg_of(c), row_base<Tin>(A, true, b, rej), nullptr,
+                                tok = walk_segment<Tin, false, QV>(seg_of(c), row_base<Tin>(A, true, b, rej), nullptr,
                                                                true, r.Mt, k, r.Mt * k, 0.f, rem, last);
                             }
                         }
@@ -956,7 +963,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         } else {
                             owner = sp;
                             if (sp == c.sg)
-                                tok = walk_segment<Tin, false>(seg_of(c), row_base<Tin>(A, true, b, g), nullptr, true,
+                                tok = walk_segment<Tin, false, QV>(seg_of(c), row_base<Tin>(A, true, b, g), nullptr, true,
                                                                r.Mt, k, r.Mt * k, 0.f, rem, last);
                         }
                     }
@@ -1008,16 +1015,18 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
 uint32_t stream_hdr_bytes() { return HDR_BYTES; }
 uint32_t stream_rec_bytes(int gamma, int S) { return rec_bytes(gamma, S); }
 int stream_threads() { return NT; }
-uint32_t stream_slot_bytes() { return SLOT_BYTES; }
-int stream_chunk_vectors() { return CV; }
+uint32_t stream_slot_bytes(int cv) { return 2u * static_cast<uint32_t>(cv) * 16u; }
 int stream_max_chunks() { return MAXCH; }
 int stream_max_segments() { return MAXS; }
 int stream_max_ring() { return MAXR; }
 int stream_max_gamma() { return MAXG; }
 
-const void *stream_kernel(int dtype) {
-    if (dtype == 0) return reinterpret_cast<const void *>(&stream_kernel_impl<float>);
-    return reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t>);
+const void *stream_kernel(int dtype, int cv) {
+    if (dtype == 0)
+        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192>)
+                         : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128>);
+    return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192>)
+                     : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128>);
 }
 
 }  // namespace mtp

@@ -71,16 +71,19 @@ def test_verify_sweep_resident_kernel(V, dtype, gamma, T, C):
     assert rep["exact"] >= x.B - 2
 
 
-@pytest.mark.parametrize("ring,depth,C,clusters", [(2, 0, 4, None), (2, 1, 8, 3), (3, 5, None, None), (8, 5, 2, 5),
-                                                   (4, 0, 16, 2), (3, 2, 1, 7), (2, 3, 4, 1)])
-def test_verify_stream_ring_variants(ring, depth, C, clusters):
-    """Ring slots, look-ahead depth, cluster size and several sequences per
-    cluster (capped grid) on rows with many rejections."""
+@pytest.mark.parametrize("ring,depth,C,clusters,chunk", [(2, 0, 4, None, None), (2, 1, 8, 3, None),
+                                                         (3, 5, None, None, None), (8, 5, 2, 5, 128),
+                                                         (4, 0, 16, 2, None), (3, 2, 1, 7, 192), (2, 3, 4, 1, 192),
+                                                         (2, 5, 1, 3, 192), (2, 5, 2, None, 128)])
+def test_verify_stream_ring_variants(ring, depth, C, clusters, chunk):
+    """Ring slots, look-ahead depth, cluster size, chunk size and several
+    sequences per cluster (capped grid) on rows with many rejections."""
     B = 40
     x = W.verify_inputs("ring", B, 5, 40000, "bf16", 77, family="sigma", sigmas=np.linspace(0.5, 6.0, B),
                         delta=np.linspace(0.0, 2.0, B), temperature=np.linspace(0.6, 1.3, B))
-    with env(MTP_RS_RING=ring, MTP_RS_DEPTH=depth, MTP_RS_CLUSTER=C, MTP_RS_MAX_CLUSTERS=clusters):
-        rep, g, o = _check_verify(x, False, f"ring={ring} depth={depth} C={C} clusters={clusters}")
+    with env(MTP_RS_RING=ring, MTP_RS_DEPTH=depth, MTP_RS_CLUSTER=C, MTP_RS_MAX_CLUSTERS=clusters,
+             MTP_RS_CHUNK=chunk):
+        rep, g, o = _check_verify(x, False, f"ring={ring} depth={depth} C={C} clusters={clusters} chunk={chunk}")
     n = g["accept_len"]
     assert (n == x.gamma).any() and (n < x.gamma).any() and (n == 0).any()
 
