@@ -151,13 +151,14 @@ int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp
  * mtp_query_plan -- the launch plan a call would use on the current device
  * (diagnostics; launches nothing).  op: 0 = mtp_rs_verify, 1 = mtp_rs_verify
  * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd, 4 =
- * mtp_rs_verify forced onto the cluster-resident kernel.  units = B
+ * mtp_rs_verify forced onto the cluster-resident kernel, 5 =
+ * mtp_tv_loss_fwd_bwd forced onto the cluster-resident kernel.  units = B
  * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
  * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
- * per CTA), resident_drafts (TV loss: draft slices kept on chip; op 0: chunk
- * slots per warp of the streaming kernel, 0 when the call would use the
- * cluster-resident kernel; else 0).
+ * per CTA), resident_drafts (cluster-resident TV kernel: draft slices kept on
+ * chip; op 0: chunk slots per warp of the streaming kernel, 0 when the call
+ * would use the cluster-resident kernel; else 0).
  * Returns the status the call's planning step would return.
  */
 int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size, int *clusters,

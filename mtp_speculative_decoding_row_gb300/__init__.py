@@ -30,7 +30,8 @@ ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_T
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string")
-PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4}
+PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
+            "tv_loss_resident": 5}
 
 _lib = None
 
@@ -73,9 +74,10 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
 
 def mtp_query_plan(op: str, dtype: str, units: int, gamma: int, V: int) -> dict:
     """Launch plan of a call on the current device: cluster size, persistent
-    clusters, shared memory per CTA and ``resident_drafts`` (TV loss: draft
-    slices kept on chip; "verify": ring slots per warp of the streaming
-    kernel, 0 when the call would use the cluster-resident kernel)."""
+    clusters, shared memory per CTA and ``resident_drafts`` (cluster-resident
+    TV kernel: draft slices kept on chip, 0 for the streaming TV kernel;
+    "verify": ring slots per warp of the streaming kernel, 0 when the call
+    would use the cluster-resident kernel)."""
     vals = [ctypes.c_int(0) for _ in range(4)]
     rc = load_library().mtp_query_plan(PLAN_OPS[op], DTYPE_BF16 if dtype == "bf16" else DTYPE_F32, units, gamma, V,
                                        *[ctypes.byref(v) for v in vals])

@@ -222,6 +222,68 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
     return found;
 }
 
+// Streaming TV kernel: clusters of C CTAs x NT/32 warps, one vocabulary
+// segment per warp, one position per cluster at a time.  Among cluster sizes
+// (powers of two) whose shared memory fits, the one with the most warps in
+// flight wins; within 5 % the larger cluster (shorter per-position chain).  Measured on
+// GB300, concurrency matters more than keeping every re-read row in L2, so
+// the positions in flight are capped only when MTP_RS_TV_L2MB sets an L2
+// budget for the 2 gamma rows a position re-reads.
+bool tvs_usable(int V, int es, int gamma) {
+    const char *e = std::getenv("MTP_RS_TV_KERNEL");
+    if (e && e[0] == 'r') return false;  // "resident"
+    return gamma <= tvs_max_gamma() && V % (16 / es) == 0;
+}
+
+bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) {
+    const int forced = env_cluster();
+    int R = env_int("MTP_RS_RING");
+    if (R < 2 || R > stream_max_ring()) R = 2;
+    const int l2mb = env_int("MTP_RS_TV_L2MB");
+    const double pos_bytes = 2.0 * gamma * static_cast<double>(V) * es;
+    int cap_l2 = l2mb > 0 ? static_cast<int>((static_cast<double>(l2mb) * 1048576.0) / pos_bytes) : 1 << 30;
+    if (cap_l2 < 1) cap_l2 = 1;
+    const uint32_t cap = smem_optin(dev);
+    const int nw = tvs_threads() / 32;
+    const int nv = V / (16 / es);
+    long best = -1;
+    bool found = false;
+    for (int C = 1; C <= MAX_C; C *= 2) {
+        if (forced && C != forced) continue;
+        const int S = C * nw;
+        if (S > tvs_max_segments()) continue;
+        const int nvs = (nv + S - 1) / S;
+        const int cv = stream_chunk_for(nvs);
+        const uint32_t smem = tvs_hdr_bytes() + tvs_rec_bytes(gamma, S) + tvs_bits_bytes(gamma, nvs) +
+                              static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
+        if (smem > cap) continue;
+        const void *func = tvs_kernel(dtype, cv);
+        if (prepare_func(dev, func) != cudaSuccess) return false;
+        const int nc = max_clusters(dev, func, C, smem, tvs_threads());
+        if (nc <= 0) continue;
+        int used = nc < units ? nc : units;
+        if (used > cap_l2) used = cap_l2;
+        const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
+        if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+        const long warps = static_cast<long>(used) * C * nw;
+        // the most warps in flight; within 5 % the larger cluster
+        if (!found || warps * 20 > best * 21 || (warps * 21 >= best * 20 && C > p.C)) {
+            if (warps > best) best = warps;
+            p = Plan{};
+            p.C = C;
+            p.smem = smem;
+            p.clusters = used;
+            p.threads = tvs_threads();
+            p.ring = R;
+            p.seg_vectors = nvs;
+            p.cv = cv;
+            p.func = func;
+            found = true;
+        }
+    }
+    return found;
+}
+
 // Persistent TV kernel: two target slots, nres (>= 2, ideally gamma) draft
 // slots and gamma rows of indicator bits per CTA.
 bool plan_tv(int dev, const void *func, int V, int es, int gamma, int units, Plan &p) {
@@ -361,11 +423,16 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
         return MTP_ERR_MISALIGNED;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
-    const void *func = tv_kernel(dtype == MTP_DTYPE_F32 ? 0 : 1);
-    if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
     const int es = esize(dtype);
+    const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
+    const void *func = nullptr;
     Plan p;
-    if (!plan_tv(dev, func, V, es, gamma, N, p)) return MTP_ERR_NO_DEVICE;
+    if (tvs_usable(V, es, gamma) && plan_tvs(dev, d, V, es, gamma, N, p)) func = p.func;
+    if (!func) {
+        func = tv_kernel(d);
+        if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
+        if (!plan_tv(dev, func, V, es, gamma, N, p)) return MTP_ERR_NO_DEVICE;
+    }
     TVArgs A;
     A.target = target_logits;
     A.draft = draft_logits;
@@ -377,6 +444,8 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
     A.aligned = (V % (16 / es) == 0) ? 1 : 0;
     A.nres = p.nres;
     A.slice_bytes = p.slice_bytes;
+    A.ring = p.ring;
+    A.seg_vectors = p.seg_vectors;
     A.loss = loss;
     A.alpha = alpha;
     A.grad = grad_draft_logits;
@@ -387,7 +456,7 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
                               int *clusters, int *smem_bytes, int *resident_drafts) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
-    if (op < 0 || op > 4 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (op < 0 || op > 5 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
@@ -395,14 +464,16 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     Plan p;
     bool ok = false, streamed = false;
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
+    if (op == 3 && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
     if (!ok) {
         const int mode = (op == 0 || op == 4) ? MODE_VERIFY : op == 1 ? MODE_VERIFY_STATS : MODE_STATS;
-        const void *func = op == 3 ? tv_kernel(d) : row_kernel(d, mode);
+        const bool tv = op == 3 || op == 5;
+        const void *func = tv ? tv_kernel(d) : row_kernel(d, mode);
         if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
-        ok = op == 3 ? plan_tv(dev, func, V, es, gamma, units, p) : plan_row(dev, func, V, es, units, p);
+        ok = tv ? plan_tv(dev, func, V, es, gamma, units, p) : plan_row(dev, func, V, es, units, p);
     }
     if (!ok) return MTP_ERR_NO_DEVICE;
-    if (streamed) p.nres = p.ring;
+    if (streamed) p.nres = (op == 0) ? p.ring : 0;
     if (cluster_size) *cluster_size = p.C;
     if (clusters) *clusters = p.clusters;
     if (smem_bytes) *smem_bytes = static_cast<int>(p.smem);

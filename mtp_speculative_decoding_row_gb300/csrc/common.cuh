@@ -79,30 +79,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// try_wait that suspends the thread in hardware until the phase completes or
-// about `ns` nanoseconds pass (no issue slots are spent while suspended).
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for an mbarrier phase with a 2 s limit; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
-        if (globaltimer_ns() - t0 > 2000000000ull) return false;
-    }
-    return true;
-}
-
 // Wait for an mbarrier phase with plain try_wait (the hardware suspends the
 // thread inside each try_wait for a while, so polling costs few issue
 // slots); the clock is read every 32 polls and the wait gives up after 2 s.
@@ -115,6 +91,11 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity) {
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > 2000000000ull) return false;
     }
+}
+
+// Wait for an mbarrier phase with a 2 s limit; false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    return mbar_wait_spin(bar, parity);
 }
 
 // Bulk copy global -> own shared memory; completion counted on `bar`.
@@ -496,6 +477,28 @@ __device__ __forceinline__ void vec_expsum(const uint4 &r, float k, float mk, fl
     }
 }
 
+// Sum of 2^{z k - mk} over one vector on the packed f32x2 pipe, into two
+// pair accumulators (K2 = (k, k), NMK2 = (-mk, -mk)).
+template <typename Tin>
+__device__ __forceinline__ void vec_expsum2(const uint4 &r, uint64_t K2, uint64_t NMK2, uint64_t &acc0,
+                                            uint64_t &acc1) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    float d0, d1;
+    if (Store<Tin>::ES == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            f2unpack(f2fma(bf16pair_f2(w[q]), K2, NMK2), d0, d1);
+            if (q & 1) acc1 = f2add(acc1, f2pack(ex2(d0), ex2(d1)));
+            else acc0 = f2add(acc0, f2pack(ex2(d0), ex2(d1)));
+        }
+    } else {
+        f2unpack(f2fma(f2pack(__uint_as_float(w[0]), __uint_as_float(w[1])), K2, NMK2), d0, d1);
+        acc0 = f2add(acc0, f2pack(ex2(d0), ex2(d1)));
+        f2unpack(f2fma(f2pack(__uint_as_float(w[2]), __uint_as_float(w[3])), K2, NMK2), d0, d1);
+        acc1 = f2add(acc1, f2pack(ex2(d0), ex2(d1)));
+    }
+}
+
 template <typename Tin, bool ENT, int NT>
 __device__ __noinline__ Soft thread_soft_exact_call(const unsigned char *buf, int nvec, float k, bool &bad) {
     return thread_soft_exact<Tin, ENT, NT>(buf, nvec, k, bad);
@@ -530,23 +533,27 @@ __device__ __forceinline__ Soft thread_soft(const unsigned char *buf, int nvec, 
     }
     if (mref > -INFINITY && mref < INFINITY) {
         const float mk = mref * k;
-        float s0 = 0.f, s1 = 0.f, t0 = 0.f, t1 = 0.f;
+        const uint64_t K2 = f2pack(k, k), NMK2 = f2pack(-mk, -mk);
+        uint64_t acc0 = f2pack(0.f, 0.f), acc1 = f2pack(0.f, 0.f);
         int j = j0;
         for (; j + 3 * NT < nvec; j += 4 * NT) {
             const uint4 r0 = vec_at(buf, j), r1 = vec_at(buf, j + NT), r2 = vec_at(buf, j + 2 * NT),
                         r3 = vec_at(buf, j + 3 * NT);
-            vec_expsum<Tin, ENT>(r0, k, mk, s0, s1, t0, t1);
-            vec_expsum<Tin, ENT>(r1, k, mk, s0, s1, t0, t1);
-            vec_expsum<Tin, ENT>(r2, k, mk, s0, s1, t0, t1);
-            vec_expsum<Tin, ENT>(r3, k, mk, s0, s1, t0, t1);
+            vec_expsum2<Tin>(r0, K2, NMK2, acc0, acc1);
+            vec_expsum2<Tin>(r1, K2, NMK2, acc0, acc1);
+            vec_expsum2<Tin>(r2, K2, NMK2, acc0, acc1);
+            vec_expsum2<Tin>(r3, K2, NMK2, acc0, acc1);
         }
-        for (; j < nvec; j += NT) vec_expsum<Tin, ENT>(vec_at(buf, j), k, mk, s0, s1, t0, t1);
-        const float s = s0 + s1;
+        for (; j < nvec; j += NT) vec_expsum2<Tin>(vec_at(buf, j), K2, NMK2, acc0, acc1);
+        float a0, a1, b0, b1;
+        f2unpack(acc0, a0, a1);
+        f2unpack(acc1, b0, b1);
+        const float s = (a0 + a1) + (b0 + b1);
         if (s < 1.8e19f) {  // finite, no NaN, far from overflow after merging
             Soft a;
             a.m = mref;
             a.s = s;
-            a.s1 = ENT ? (t0 + t1) : 0.f;
+            a.s1 = 0.f;
             return a;
         }
     }

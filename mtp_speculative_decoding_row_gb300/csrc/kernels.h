@@ -38,6 +38,8 @@ struct TVArgs {
     int aligned;
     int nres;               // draft slices kept on chip (1..gamma)
     uint32_t slice_bytes;
+    int ring;               // streaming kernel: chunk slots per warp
+    int seg_vectors;        // streaming kernel: 16-byte vectors per warp segment
     float *loss;            // [N]
     float *alpha;           // [N, gamma] or null
     float *grad;            // [N, gamma, V]
@@ -65,5 +67,14 @@ int stream_max_ring();
 const void *row_kernel(int dtype, int mode);
 const void *stream_kernel(int dtype, int cv);  // cv: 128 or 192 vectors per chunk
 const void *tv_kernel(int dtype);
+const void *tvs_kernel(int dtype, int cv);  // streaming TV kernel, cv: 128 or 192
+
+// Streaming TV kernel geometry.
+uint32_t tvs_hdr_bytes();
+uint32_t tvs_rec_bytes(int gamma, int S);
+uint32_t tvs_bits_bytes(int gamma, int nvs);
+int tvs_threads();
+int tvs_max_gamma();
+int tvs_max_segments();
 
 }  // namespace mtp

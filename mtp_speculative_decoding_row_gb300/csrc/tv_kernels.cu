@@ -117,6 +117,86 @@ __device__ __forceinline__ void issue_row(const Slice &s, const unsigned char *r
     }
 }
 
+// One pass over a CTA's target and draft slices with the final normalisers
+// (log2 p = z_t k - ct, log2 q = z_d k - cd): this thread's share of
+// alpha = sum_v min(p_v, q_v) and S = sum_v 1[q_v <= p_v] q_v (min(p, q) is
+// 2^{min(log2 p, log2 q)}, and equals q where q <= p), plus one indicator
+// byte per vector (bit e: q <= p for element e).
+template <typename Tin, int NTH>
+__device__ __forceinline__ void overlap_pass(const unsigned char *tb, const unsigned char *db, unsigned char *bk,
+                                             int nvec, float k, float ct, float cd, float &acc_a, float &acc_s) {
+    const uint64_t K2 = f2pack(k, k), NCT = f2pack(-ct, -ct), NCD = f2pack(-cd, -cd);
+    uint64_t aa = f2pack(0.f, 0.f), as = f2pack(0.f, 0.f);
+    for (int j = threadIdx.x; j < nvec; j += NTH) {
+        const uint4 rt = vec_at(tb, j), rd = vec_at(db, j);
+        const uint32_t wt[4] = {rt.x, rt.y, rt.z, rt.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
+        unsigned m = 0;
+#pragma unroll
+        for (int q = 0; q < (Store<Tin>::ES == 2 ? 4 : 2); ++q) {
+            uint64_t zt2, zd2;
+            if (Store<Tin>::ES == 2) {
+                zt2 = bf16pair_f2(wt[q]);
+                zd2 = bf16pair_f2(wd[q]);
+            } else {
+                zt2 = f2pack(__uint_as_float(wt[2 * q]), __uint_as_float(wt[2 * q + 1]));
+                zd2 = f2pack(__uint_as_float(wd[2 * q]), __uint_as_float(wd[2 * q + 1]));
+            }
+            float lp0, lp1, lq0, lq1;
+            f2unpack(f2fma(zt2, K2, NCT), lp0, lp1);
+            f2unpack(f2fma(zd2, K2, NCD), lq0, lq1);
+            const float x0 = ex2(fminf(lp0, lq0)), x1 = ex2(fminf(lp1, lq1));
+            const bool b0 = lq0 <= lp0, b1 = lq1 <= lp1;
+            aa = f2add(aa, f2pack(x0, x1));
+            as = f2add(as, f2pack(b0 ? x0 : 0.f, b1 ? x1 : 0.f));
+            m |= (b0 ? 1u : 0u) << (2 * q);
+            m |= (b1 ? 1u : 0u) << (2 * q + 1);
+        }
+        bk[j] = static_cast<unsigned char>(m);
+    }
+    float a0, a1, s0, s1;
+    f2unpack(aa, a0, a1);
+    f2unpack(as, s0, s1);
+    acc_a = a0 + a1;
+    acc_s = s0 + s1;
+}
+
+// Gradient of one draft row slice (aligned rows): out[j] =
+// q_j * (bit_j ? on : off) with q_j = 2^{z_j k - cd}; each thread writes four
+// consecutive outputs per iteration, so every warp store covers 512
+// contiguous bytes (streaming stores: the gradient is not re-read).
+template <typename Tin, int NTH>
+__device__ __forceinline__ void grad_pass(const unsigned char *db, const unsigned char *bk, int nvec, float k,
+                                          float cd, float on, float off, float *out) {
+    constexpr int VEC = Store<Tin>::VEC;
+    const uint64_t K2 = f2pack(k, k), NCD = f2pack(-cd, -cd);
+    const int nquad = nvec * VEC / 4;
+    float4 *o4 = reinterpret_cast<float4 *>(out);
+    for (int h = threadIdx.x; h < nquad; h += NTH) {
+        uint64_t z01, z23;
+        unsigned m;
+        if (Store<Tin>::ES == 2) {
+            const uint2 r = reinterpret_cast<const uint2 *>(db)[h];
+            z01 = bf16pair_f2(r.x);
+            z23 = bf16pair_f2(r.y);
+            m = static_cast<unsigned>(bk[h >> 1]) >> ((h & 1) * 4);
+        } else {
+            const uint4 r = reinterpret_cast<const uint4 *>(db)[h];
+            z01 = f2pack(__uint_as_float(r.x), __uint_as_float(r.y));
+            z23 = f2pack(__uint_as_float(r.z), __uint_as_float(r.w));
+            m = bk[h];
+        }
+        float d0, d1, d2, d3;
+        f2unpack(f2fma(z01, K2, NCD), d0, d1);
+        f2unpack(f2fma(z23, K2, NCD), d2, d3);
+        float4 g;
+        g.x = ex2(d0) * ((m & 1u) ? on : off);
+        g.y = ex2(d1) * ((m & 2u) ? on : off);
+        g.z = ex2(d2) * ((m & 4u) ? on : off);
+        g.w = ex2(d3) * ((m & 8u) ? on : off);
+        __stcs(o4 + h, g);
+    }
+}
+
 template <typename Tin>
 __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
     using S = Store<Tin>;
@@ -288,25 +368,9 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
             if (tid == 0) sh.cd[kk] = cd;
 
             // overlap, S and indicator bits in one pass over the on-chip slices
-            float acc_a = 0.f, acc_s = 0.f;
             unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
-            for (int j = tid; j < s.nvec; j += NT) {
-                float zt[VEC], zd[VEC];
-                S::unpack(vec_at(tb, j), zt);
-                S::unpack(vec_at(db, j), zd);
-                unsigned m = 0;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float lp = fmaf(zt[e], k, -ct), lq = fmaf(zd[e], k, -cd);
-                    const float x = ex2(fminf(lp, lq));
-                    acc_a += x;
-                    if (lq <= lp) {
-                        acc_s += x;
-                        m |= 1u << e;
-                    }
-                }
-                bk[j] = static_cast<unsigned char>(m);
-            }
+            float acc_a, acc_s;
+            overlap_pass<Tin, NT>(tb, db, bk, s.nvec, k, ct, cd, acc_a, acc_s);
             block_sum2(sh.tpart, acc_a, acc_s);
             pa = acc_a;
             ps = acc_s;
@@ -372,31 +436,34 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
                 const float on = coef * (1.f - sk), off = -coef * sk;
                 const unsigned char *bk = bits + static_cast<size_t>(kk) * nvc;
                 float *out = gbase + static_cast<size_t>(kk) * V;
-                // four consecutive outputs per thread: every warp store is
-                // 512 contiguous bytes
-                const int nquad = s.nvec * VEC / 4;
-                for (int h = tid; h < nquad; h += NT) {
-                    float zd[4], gr[4];
-                    if (S::ES == 2) {
-                        const uint2 r = reinterpret_cast<const uint2 *>(db)[h];
-                        zd[0] = __uint_as_float(r.x << 16);
-                        zd[1] = __uint_as_float(r.x & 0xffff0000u);
-                        zd[2] = __uint_as_float(r.y << 16);
-                        zd[3] = __uint_as_float(r.y & 0xffff0000u);
-                    } else {
-                        const uint4 r = reinterpret_cast<const uint4 *>(db)[h];
-                        zd[0] = __uint_as_float(r.x);
-                        zd[1] = __uint_as_float(r.y);
-                        zd[2] = __uint_as_float(r.z);
-                        zd[3] = __uint_as_float(r.w);
-                    }
-                    const unsigned m = static_cast<unsigned>(bk[(4 * h) / VEC]) >> ((4 * h) % VEC);
+                if (aligned) {
+                    grad_pass<Tin, NT>(db, bk, s.nvec, k, cd, on, off, out + s.lo);
+                } else {
+                    // four consecutive outputs per thread, masked at the row end
+                    const int nquad = s.nvec * VEC / 4;
+                    for (int h = tid; h < nquad; h += NT) {
+                        float zd[4], gr[4];
+                        if (S::ES == 2) {
+                            const uint2 r = reinterpret_cast<const uint2 *>(db)[h];
+                            zd[0] = __uint_as_float(r.x << 16);
+                            zd[1] = __uint_as_float(r.x & 0xffff0000u);
+                            zd[2] = __uint_as_float(r.y << 16);
+                            zd[3] = __uint_as_float(r.y & 0xffff0000u);
+                        } else {
+                            const uint4 r = reinterpret_cast<const uint4 *>(db)[h];
+                            zd[0] = __uint_as_float(r.x);
+                            zd[1] = __uint_as_float(r.y);
+                            zd[2] = __uint_as_float(r.z);
+                            zd[3] = __uint_as_float(r.w);
+                        }
+                        const unsigned m = static_cast<unsigned>(bk[(4 * h) / VEC]) >> ((4 * h) % VEC);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float q = ex2(fmaf(zd[e], k, -cd));
-                        gr[e] = q * (((m >> e) & 1u) ? on : off);
+                        for (int e = 0; e < 4; ++e) {
+                            const float q = ex2(fmaf(zd[e], k, -cd));
+                            gr[e] = q * (((m >> e) & 1u) ? on : off);
+                        }
+                        store_grad<4>(out, s.lo + 4 * h, V, false, gr);
                     }
-                    store_grad<4>(out, s.lo + 4 * h, V, aligned, gr);
                 }
                 __syncthreads();
                 if (pipe && kk == 0 && tn < A.N && !dead) {

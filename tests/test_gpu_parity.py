@@ -260,6 +260,37 @@ def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres):
     compare.assert_ok(rep, f"tv N={N} V={V}")
 
 
+@pytest.mark.parametrize("N,gamma,V,dtype,C,clusters,ring,kernel", [
+    (9, 3, 40000, "bf16", 16, 2, None, None),     # several positions per cluster: both exchange banks
+    (7, 2, 20000, "f32", 4, 3, 3, None),
+    (5, 4, 65536, "bf16", 8, 1, 2, None),
+    (6, 3, 40000, "bf16", None, None, None, "resident"),
+    (4, 5, 12000, "f32", 8, None, None, "resident"),
+    (3, 8, 30000, "bf16", None, 2, None, None),   # gamma = 8, the streaming limit
+    (3, 9, 30000, "bf16", None, None, None, None),  # gamma = 9 takes the resident kernel
+])
+def test_tv_loss_kernels(N, gamma, V, dtype, C, clusters, ring, kernel):
+    """Streaming and cluster-resident TV kernels, several positions per
+    cluster, ring depths and the gamma limit."""
+    x = W.tvloss_inputs("tvk", N, gamma, V, dtype, 600 + V + gamma, delta=0.5, sigmas=np.linspace(0.7, 9.0, N))
+    with env(MTP_RS_CLUSTER=C, MTP_RS_MAX_CLUSTERS=clusters, MTP_RS_RING=ring, MTP_RS_TV_KERNEL=kernel):
+        out = run_tv(to_dev(x.target), to_dev(x.draft), 0.8, 1.5)
+    o = oracle.tv_loss(x.target, x.draft, 0.8, 1.5)
+    tf = W.bf16_bits_to_f32(x.target).astype(np.float64) if dtype == "bf16" else x.target.astype(np.float64)
+    df = W.bf16_bits_to_f32(x.draft).astype(np.float64) if dtype == "bf16" else x.draft.astype(np.float64)
+    rep = compare.tv_report(out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy(),
+                            out.row_flags.cpu().numpy(), o, dtype, tf, df, 0.8)
+    compare.assert_ok(rep, f"tv kernels N={N} gamma={gamma} V={V} C={C} kernel={kernel}")
+
+
+def test_tv_plan_kernels():
+    import mtp_speculative_decoding_row_gb300 as mtp
+    p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
+    q = mtp.mtp_query_plan("tv_loss_resident", "bf16", 16384, 3, 151936)
+    assert p["resident_drafts"] == 0 and q["resident_drafts"] >= 1
+    assert p["clusters"] * p["cluster_size"] > q["clusters"] * q["cluster_size"]
+
+
 def test_tv_loss_full_config_sampled():
     """N = 16,384, gamma = 3, V = 151,936 bf16 on device: sampled positions
     against the oracle, sum_j grad = 0 on every row, loss in [-gamma, 0]."""
@@ -286,13 +317,18 @@ def test_tv_loss_full_config_sampled():
     print("tvloss sampled", {k: v for k, v in rep.items() if not isinstance(v, list)})
 
 
-def test_tv_loss_bad_temperature_and_nan():
+@pytest.mark.parametrize("kernel", [None, "resident"])
+def test_tv_loss_bad_temperature_and_nan(kernel):
     x = W.tvloss_inputs("tvbad", 3, 2, 2000, "f32", 9, sigmas=2.0)
     x.target[1, 1, 3] = np.nan
-    out = run_tv(to_dev(x.target), to_dev(x.draft), 1.0, 1.0)
+    with env(MTP_RS_TV_KERNEL=kernel, MTP_RS_MAX_CLUSTERS=1 if kernel is None else None):
+        out = run_tv(to_dev(x.target), to_dev(x.draft), 1.0, 1.0)
     f = out.row_flags.cpu().numpy()
     assert list(f) == [0, oracle.ROW_NONFINITE, 0]
+    o = oracle.tv_loss(x.target, x.draft, 1.0, 1.0)
+    np.testing.assert_allclose(out.loss.cpu().numpy()[[0, 2]], o["loss"][[0, 2]], rtol=1e-5)
     assert np.isnan(out.loss[1].item()) and torch.all(out.grad[1] == 0)
-    out = run_tv(to_dev(x.target), to_dev(x.draft), 0.0, 1.0)
+    with env(MTP_RS_TV_KERNEL=kernel):
+        out = run_tv(to_dev(x.target), to_dev(x.draft), 0.0, 1.0)
     assert np.all(out.row_flags.cpu().numpy() == oracle.ROW_BAD_TEMP)
     assert torch.all(out.grad == 0)
