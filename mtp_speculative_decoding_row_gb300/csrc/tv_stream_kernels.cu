@@ -18,11 +18,11 @@
 // ahead through it:
 //   pass N(k), k < gamma: target and draft rows from HBM; online softmax
 //     partials, one 16-byte record per warp to every CTA (DSMEM push);
-//   pass O(k): the same rows again (now in L2) with the final normalisers:
-//     alpha and S partials and one indicator byte per vector kept in shared
-//     memory; one record per warp;
-//   pass G(k): the draft row again (L2) and the indicator bytes: the
-//     gradient, written with streaming stores.
+//   pass O(k), one step behind N: the same rows again (now in L2) with the
+//     final normalisers: alpha and S partials and one indicator byte per
+//     vector kept in shared memory; one record per warp;
+//   pass G(k), after every O, latest step first: the draft row again and
+//     the indicator bytes: the gradient, written with streaming stores.
 // Every warp gathers the records itself and evaluates the chain (same
 // records, same order: the same values everywhere).  The number of
 // positions in flight is capped so that the rows being re-read stay in L2.
@@ -92,15 +92,35 @@ __device__ __forceinline__ const unsigned char *tv_row_ptr(const void *base, int
 
 __device__ __forceinline__ int tchunk(const TC &c, int ch) { return min(c.cv, c.seg_n - ch * c.cv); }
 
-// Issue chunk copies while ring slots are free: the schedule of a position
-// is N(0..g-1), O(0..g-1), G(0..g-1), then the next position.
+// Pass u (0 <= u < 3 g) of a position: N(0), then N(k) and O(k - 1) in
+// turn, then O(g - 1), then G(g-1), ..., G(0).
+__device__ __forceinline__ void unit_of(int u, int g, int &kind, int &k) {
+    if (u == 0) {
+        kind = P_NORM;
+        k = 0;
+    } else if (u < 2 * g - 1) {
+        const int j = (u + 1) >> 1;
+        kind = (u & 1) ? P_NORM : P_OVL;
+        k = (u & 1) ? j : j - 1;
+    } else if (u == 2 * g - 1) {
+        kind = P_OVL;
+        k = g - 1;
+    } else {
+        kind = P_GRAD;
+        k = 3 * g - 1 - u;  // latest step first: its draft row is the most recently read
+    }
+}
+
+// Issue chunk copies while ring slots are free, in the order of unit_of,
+// then the next position.
 template <typename Tin>
 __device__ __forceinline__ void tproduce(const TVArgs &A, TC &c) {
     if (c.p_done || c.dead) return;
     while (c.pcount - c.ccount < static_cast<uint32_t>(c.R)) {
         if (c.p_c == 0) {
             const int t = c.cid + c.p_ord * c.NC;
-            const int kind = c.p_u / c.g, k = c.p_u - kind * c.g;
+            int kind, k;
+            unit_of(c.p_u, c.g, kind, k);
             const size_t off = static_cast<size_t>(c.seg_lo) * 16u;
             c.p_t = kind == P_GRAD ? nullptr : tv_row_ptr<Tin>(A.target, t, k, c.g, A.V) + off;
             c.p_d = tv_row_ptr<Tin>(A.draft, t, k, c.g, A.V) + off;
@@ -345,106 +365,111 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
             flags = bad_temp ? F_BAD_TEMP : F_TIMEOUT;
             for (int kk = 0; kk < g; ++kk) zero_segment<Tin>(c, grow + static_cast<size_t>(kk) * A.V);
         } else {
-            // ---- N(k): softmax partials of both rows, one record per warp
-            for (int kk = 0; kk < g; ++kk) {
-                float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
-                int bad = 0;
-                for (int ch = 0; ch < c.nch; ++ch) {
-                    tproduce<Tin>(A, c);
-                    if (!twait_slot(c)) break;
-                    const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
-                    const unsigned char *db = tb + CV * 16;
-                    const int cnt = tchunk(c, ch);
-                    uint4 rt[QV], rd[QV];
-                    if (cnt == CV) {
-                        load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
-                    } else {
-                        load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
+            // ---- N(k) and O(k), the overlap pass one step behind the
+            // normaliser pass: N(0), N(1), O(0), N(2), O(1), ..., O(g-1).
+            // O(k) re-reads rows k right after N(k+1), while they are in L2,
+            // and the all-gather of N(k) overlaps the streaming of N(k+1).
+            for (int u = 0; u < 2 * g && !c.dead; ++u) {
+                int kind, kk;
+                unit_of(u, g, kind, kk);
+                if (kind == P_NORM) {
+                    float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
+                    int bad = 0;
+                    for (int ch = 0; ch < c.nch; ++ch) {
+                        tproduce<Tin>(A, c);
+                        if (!twait_slot(c)) break;
+                        const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
+                        const unsigned char *db = tb + CV * 16;
+                        const int cnt = tchunk(c, ch);
+                        uint4 rt[QV], rd[QV];
+                        if (cnt == CV) {
+                            load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
+                            load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
+                        } else {
+                            load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
+                            load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
+                        }
+                        // the maxima consume every loaded register: the slot's
+                        // reads are complete before it is handed back
+                        const float cmt = chunk_max<Tin, QV>(rt), cmd = chunk_max<Tin, QV>(rd);
+                        __syncwarp();
+                        tconsumed(c);
+                        tproduce<Tin>(A, c);
+                        fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
+                        fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
                     }
-                    // the maxima consume every loaded register: the slot's
-                    // reads are complete before it is handed back
-                    const float cmt = chunk_max<Tin, QV>(rt), cmd = chunk_max<Tin, QV>(rd);
-                    __syncwarp();
-                    tconsumed(c);
-                    tproduce<Tin>(A, c);
-                    fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
-                    fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
-                }
-                if (c.dead) break;
-                Soft a;
-                a.m = mt;
-                a.s = st;
-                a.s1 = 0.f;
-                const Soft wt = soft_warp_allreduce<false>(a, k);
-                a.m = md;
-                a.s = sd;
-                const Soft wd = soft_warp_allreduce<false>(a, k);
-                const bool wbad = warp_allor(bad) != 0;
-                tpush(sh, c, kk, make_float4(wt.m, wbad ? NAN : wt.s, wd.m, wbad ? NAN : wd.s));
-            }
-            // ---- O(k): overlap and S with the final normalisers
-            for (int kk = 0; kk < g && !c.dead; ++kk) {
-                if (!twait_round(sh, c, kk)) break;
-                // gather: lane l holds segments 2l and 2l + 1
-                Soft lt = soft_empty(), ld = soft_empty();
+                    if (c.dead) continue;
+                    Soft a;
+                    a.m = mt;
+                    a.s = st;
+                    a.s1 = 0.f;
+                    const Soft wt = soft_warp_allreduce<false>(a, k);
+                    a.m = md;
+                    a.s = sd;
+                    const Soft wd = soft_warp_allreduce<false>(a, k);
+                    const bool wbad = warp_allor(bad) != 0;
+                    tpush(sh, c, kk, make_float4(wt.m, wbad ? NAN : wt.s, wd.m, wbad ? NAN : wd.s));
+                } else {
+                    if (!twait_round(sh, c, kk)) continue;
+                    // gather: lane l holds segments 2l and 2l + 1
+                    Soft lt = soft_empty(), ld = soft_empty();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int q = 2 * c.lane + h;
-                    if (q < c.S) {
-                        const float4 v = *trec(c, kk, q);
-                        Soft r;
-                        r.m = v.x;
-                        r.s = v.y;
-                        r.s1 = 0.f;
-                        lt = soft_pair_merge(lt, r, k);
-                        r.m = v.z;
-                        r.s = v.w;
-                        ld = soft_pair_merge(ld, r, k);
+                    for (int h = 0; h < 2; ++h) {
+                        const int q = 2 * c.lane + h;
+                        if (q < c.S) {
+                            const float4 v = *trec(c, kk, q);
+                            Soft r;
+                            r.m = v.x;
+                            r.s = v.y;
+                            r.s1 = 0.f;
+                            lt = soft_pair_merge(lt, r, k);
+                            r.m = v.z;
+                            r.s = v.w;
+                            ld = soft_pair_merge(ld, r, k);
+                        }
                     }
-                }
-                const Soft Ct = soft_warp_allreduce<false>(lt, k), Cd = soft_warp_allreduce<false>(ld, k);
-                if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY) || !(Cd.m > -INFINITY) ||
-                    !(Cd.s > 0.f) || !(Cd.s < INFINITY))
-                    flags |= F_NONFINITE;
-                const float ct = fmaf(Ct.m, k, log2f(Ct.s)), cd = fmaf(Cd.m, k, log2f(Cd.s));
-                if (c.lane == 0) {
-                    c.ws->ct[kk] = ct;
-                    c.ws->cd[kk] = cd;
-                }
-                float acc_a = 0.f, acc_s = 0.f;
-                unsigned char *bk = c.bits + static_cast<size_t>(kk) * nvs;
-                for (int ch = 0; ch < c.nch; ++ch) {
-                    tproduce<Tin>(A, c);
-                    if (!twait_slot(c)) break;
-                    const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
-                    const unsigned char *db = tb + CV * 16;
-                    const int cnt = tchunk(c, ch);
-                    uint4 rt[QV], rd[QV];
-                    if (cnt == CV) {
-                        load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
-                    } else {
-                        load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
+                    const Soft Ct = soft_warp_allreduce<false>(lt, k), Cd = soft_warp_allreduce<false>(ld, k);
+                    if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY) || !(Cd.m > -INFINITY) ||
+                        !(Cd.s > 0.f) || !(Cd.s < INFINITY))
+                        flags |= F_NONFINITE;
+                    const float ct = fmaf(Ct.m, k, log2f(Ct.s)), cd = fmaf(Cd.m, k, log2f(Cd.s));
+                    if (c.lane == 0) {
+                        c.ws->ct[kk] = ct;
+                        c.ws->cd[kk] = cd;
                     }
-                    // hand the slot back once every loaded register is consumed
-                    const uint32_t x = consume_regs<QV>(rt) ^ consume_regs<QV>(rd);
-                    asm volatile("" ::"r"(x));
-                    __syncwarp();
-                    tconsumed(c);
-                    tproduce<Tin>(A, c);
-                    uint32_t m[QV];
-                    ovl_regs<Tin, QV>(rt, rd, k, ct, cd, acc_a, acc_s, m);
+                    float acc_a = 0.f, acc_s = 0.f;
+                    unsigned char *bk = c.bits + static_cast<size_t>(kk) * nvs;
+                    for (int ch = 0; ch < c.nch; ++ch) {
+                        tproduce<Tin>(A, c);
+                        if (!twait_slot(c)) break;
+                        const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
+                        const unsigned char *db = tb + CV * 16;
+                        const int cnt = tchunk(c, ch);
+                        uint4 rt[QV], rd[QV];
+                        if (cnt == CV) {
+                            load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
+                            load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
+                        } else {
+                            load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
+                            load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
+                        }
+                        // hand the slot back once every loaded register is consumed
+                        const uint32_t x = consume_regs<QV>(rt) ^ consume_regs<QV>(rd);
+                        asm volatile("" ::"r"(x));
+                        __syncwarp();
+                        tconsumed(c);
+                        tproduce<Tin>(A, c);
+                        uint32_t m[QV];
+                        ovl_regs<Tin, QV>(rt, rd, k, ct, cd, acc_a, acc_s, m);
 #pragma unroll
-                    for (int q = 0; q < QV; ++q) {
-                        const int j = q * 32 + c.lane;
-                        if (j < cnt) bk[ch * CV + j] = static_cast<unsigned char>(m[q]);
+                        for (int q = 0; q < QV; ++q) {
+                            const int j = q * 32 + c.lane;
+                            if (j < cnt) bk[ch * CV + j] = static_cast<unsigned char>(m[q]);
+                        }
                     }
+                    if (c.dead) break;
+                    tpush(sh, c, g + kk, make_float4(warp_allsum(acc_a), warp_allsum(acc_s), 0.f, 0.f));
                 }
-                if (c.dead) break;
-                tpush(sh, c, g + kk, make_float4(warp_allsum(acc_a), warp_allsum(acc_s), 0.f, 0.f));
             }
             // ---- the chain: every warp from the gathered records
             if (!c.dead) {
@@ -501,8 +526,8 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
             }
             if (c.dead) flags |= F_TIMEOUT;
             __syncwarp();
-            // ---- G(k): the gradient
-            for (int kk = 0; kk < g; ++kk) {
+            // ---- G(k): the gradient, latest step first (the order of unit_of)
+            for (int kk = g - 1; kk >= 0; --kk) {
                 float *orow = grow + static_cast<size_t>(kk) * A.V;
                 const float cd = c.ws->cd[kk], on = c.ws->on[kk], off = c.ws->off[kk];
                 const unsigned char *bk = c.bits + static_cast<size_t>(kk) * nvs;
