@@ -50,6 +50,8 @@ def _load():
             lib.oracle_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]
             lib.oracle_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
             lib.oracle_tv_loss.argtypes = [P, P, I, D, I, I, I, D, I, P, P, P, P, P, P]
+            lib.oracle_to_verify.argtypes = [P, P, I, P, P, I, I, I, P, P, P, P, P, P]
+            lib.oracle_diagnostics.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P, P, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_softmax, lib.oracle_verify, lib.oracle_row_stats, lib.oracle_tv_loss,
                       lib.oracle_num_threads):
@@ -121,6 +123,60 @@ def verify(target, draft, draft_ids, temperature, uniforms, want_stats: bool = F
         _ptr(out.get("entropy")), _ptr(out["flags"]), _ptr(out["acc_margin"]), _ptr(out["cdf_margin"]))
     if rc:
         raise RuntimeError(f"oracle_verify failed ({rc})")
+    return out
+
+
+def to_verify(target, draft, temperature, uniforms) -> dict:
+    """Batched target-only verification: draft token = arg max of the draft
+    logits, accepted iff u < p(y); replacement from p without y; T = 0 is
+    greedy.  Returns tokens [B, gamma+1], accept_len [B], yhat [B, gamma]
+    (-1 past the chain), flags [B], acc_margin [B, gamma] = |u - p(y)|,
+    cdf_margin [B]."""
+    t, dt = _logits(target)
+    d, dt2 = _logits(draft)
+    assert dt == dt2
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    assert d.shape == (B, gamma, V)
+    temp = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, gamma + 1)
+    out = {
+        "tokens": np.empty((B, gamma + 1), np.int32),
+        "accept_len": np.empty(B, np.int32),
+        "yhat": np.empty((B, gamma), np.int32),
+        "flags": np.empty(B, np.int32),
+        "acc_margin": np.empty((B, gamma), np.float64),
+        "cdf_margin": np.empty(B, np.float64),
+    }
+    rc = _load().oracle_to_verify(_ptr(t), _ptr(d), dt, _ptr(temp), _ptr(u), B, gamma, V, _ptr(out["tokens"]),
+                                  _ptr(out["accept_len"]), _ptr(out["yhat"]), _ptr(out["flags"]),
+                                  _ptr(out["acc_margin"]), _ptr(out["cdf_margin"]))
+    if rc:
+        raise RuntimeError(f"oracle_to_verify failed ({rc})")
+    return out
+
+
+def diagnostics(target, draft, temperature) -> dict:
+    """Per-position acceptance diagnostics: alpha, tv, ent_q, kl (q || p),
+    yhat, p_yhat, rs_better, boundary_margin [B, gamma]; ent_p [B, gamma+1];
+    flags [B]."""
+    t, dt = _logits(target)
+    d, dt2 = _logits(draft)
+    assert dt == dt2
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    temp = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    out = {k: np.empty((B, gamma), np.float64) for k in ("alpha", "tv", "ent_q", "kl", "p_yhat", "boundary_margin")}
+    out["yhat"] = np.empty((B, gamma), np.int32)
+    out["rs_better"] = np.empty((B, gamma), np.int32)
+    out["ent_p"] = np.empty((B, gamma + 1), np.float64)
+    out["flags"] = np.empty(B, np.int32)
+    rc = _load().oracle_diagnostics(_ptr(t), _ptr(d), dt, _ptr(temp), B, gamma, V, _ptr(out["alpha"]), _ptr(out["tv"]),
+                                    _ptr(out["ent_q"]), _ptr(out["kl"]), _ptr(out["yhat"]), _ptr(out["p_yhat"]),
+                                    _ptr(out["rs_better"]), _ptr(out["boundary_margin"]), _ptr(out["ent_p"]),
+                                    _ptr(out["flags"]))
+    if rc:
+        raise RuntimeError(f"oracle_diagnostics failed ({rc})")
     return out
 
 

@@ -31,6 +31,14 @@
  *   - TV-gradient indicator 1[q <= p] as the pages write it (tie_le = 1);
  *     tie_le = 0 selects the strict 1[q < p].
  *   - e2e loss l = -sum_{k=1..gamma} prod_{i<=k} alpha_i, unnormalised.
+ *   - T == 0 is greedy decoding: p and q are one-hot at the row's arg max
+ *     (ties to the smallest index), so a draft is accepted iff it is the
+ *     target's arg max and the replacement / bonus token is the arg max.
+ *     Statistics need T > 0.  T < 0, NaN or inf is a bad temperature.
+ *   - Target-only acceptance: the draft token is the arg max of the draft
+ *     logits (ties to the smallest index), accepted iff u < p(y); at the
+ *     first rejection the replacement is drawn from p with y removed, i.e.
+ *     the residual of rejection sampling with a one-hot draft.
  *
  * Logit storage codes: 0 = float32, 1 = bfloat16 (uint16 bit patterns),
  * 2 = float64.  Every element is widened exactly to double before use.
@@ -131,6 +139,42 @@ static double entropy(const double *p, int V)
 }
 
 /*
+ * Index of the largest logit of one row (smallest index among equals);
+ * -1 if a logit is NaN or +inf or every logit is -inf.  Greedy decoding and
+ * target-only draft selection take the arg max [BB, App. D.2 "Target-Only
+ * Sampling": the draft token is arg max_y q(y), and arg max of the softmax
+ * is the arg max of the logits].
+ */
+static int argmax_row(const void *z, int dtype, size_t off, int V)
+{
+    int best = -1;
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double x = load_logit(z, dtype, off + (size_t)v);
+        if (isnan(x) || (isinf(x) && x > 0)) return -1;
+        if (x > m) {
+            m = x;
+            best = v;
+        }
+    }
+    return best;
+}
+
+/* D_KL(q || p) = sum_{q_v > 0} q_v log(q_v / p_v), in nats; +inf where some
+ * q_v > 0 has p_v = 0 [BB, §9 "Distributional effects of TV loss"]. */
+static double kl_qp(const double *q, const double *p, int V)
+{
+    double d = 0.0;
+    for (int v = 0; v < V; ++v) {
+        if (q[v] > 0.0) {
+            if (!(p[v] > 0.0)) return INFINITY;
+            d += q[v] * log(q[v] / p[v]);
+        }
+    }
+    return d;
+}
+
+/*
  * Inverse-CDF draw from the unnormalised weights r[0..V-1] with uniform u:
  * C(v) = sum_{w<=v} r_w, R = C(V-1); returns the smallest v with C(v) > u*R,
  * or the last v with r_v > 0 if rounding leaves none.  This is the residual
@@ -190,7 +234,7 @@ static void verify_one(const void *target, const void *draft, int dtype, size_t 
         for (int i = 0; i < gamma; ++i) alpha[i] = tv[i] = NAN;
         for (int i = 0; i <= gamma; ++i) ent[i] = NAN;
     }
-    if (!(T > 0.0) || isinf(T)) f |= OR_ROW_BAD_TEMP;
+    if (!(T >= 0.0) || isinf(T) || (T == 0.0 && want_stats)) f |= OR_ROW_BAD_TEMP;
     for (int i = 0; i < gamma; ++i)
         if (ids[i] < 0 || ids[i] >= V) f |= OR_ROW_BAD_ID;
     for (int i = 0; i <= gamma; ++i)
@@ -198,6 +242,33 @@ static void verify_one(const void *target, const void *draft, int dtype, size_t 
     if (f) {
         *accept_len = -1;
         *flags = f;
+        return;
+    }
+
+    /* Greedy (T == 0): accept while the draft is the target's arg max, then
+     * emit the target's arg max.  No probability is formed. */
+    if (T == 0.0) {
+        int n = 0;
+        for (int i = 0; i <= gamma; ++i) {
+            int a = argmax_row(target, dtype, toff + (size_t)i * V, V);
+            if (a < 0) {
+                for (int j = 0; j <= gamma; ++j) tokens[j] = -1;
+                *accept_len = -1;
+                *flags = OR_ROW_NONFINITE;
+                return;
+            }
+            if (i < gamma) acc_margin[i] = INFINITY;
+            if (i < gamma && ids[i] == a) {
+                tokens[i] = a;
+                ++n;
+                continue;
+            }
+            tokens[i] = a;
+            break;
+        }
+        *cdf_margin = INFINITY;
+        *accept_len = n;
+        *flags = 0;
         return;
     }
 
@@ -304,6 +375,195 @@ int oracle_verify(const void *target, const void *draft, int dtype, const int32_
                    want_stats ? tv + (size_t)b * gamma : NULL, want_stats ? ent + (size_t)b * (gamma + 1) : NULL,
                    flags + b, acc_margin + (size_t)b * gamma, cdf_margin + b, buf, buf + V, buf + 2 * (size_t)V);
         free(buf);
+    }
+    return fail ? 2 : 0;
+}
+
+/*
+ * One sequence of target-only verification [BB, §2 "Acceptance methods":
+ * the draft token is selected greedily and accepted with probability p(y);
+ * App. D.2]: for i = 0..gamma-1, y_i = arg max of draft row i, p_i =
+ * softmax(target_i / T); accept iff u_i < p_i(y_i); at the first rejection j
+ * draw the replacement from p_j with y_j removed (the residual of rejection
+ * sampling with a one-hot draft, so the output law stays p); after gamma
+ * accepts draw the bonus from p_gamma.  With T == 0: accept iff y_i is the
+ * target's arg max, and emit the target's arg max.  yhat[i] receives y_i
+ * for every position the chain reached (-1 elsewhere).
+ */
+static void to_verify_one(const void *target, const void *draft, int dtype, size_t toff, size_t doff, double T,
+                          const double *u, int gamma, int V, int32_t *tokens, int32_t *accept_len, int32_t *yhat,
+                          int32_t *flags, double *acc_margin, double *cdf_margin, double *p, double *r)
+{
+    for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
+    for (int i = 0; i < gamma; ++i) {
+        acc_margin[i] = NAN;
+        yhat[i] = -1;
+    }
+    *cdf_margin = NAN;
+    int f = 0;
+    if (!(T >= 0.0) || isinf(T)) f |= OR_ROW_BAD_TEMP;
+    for (int i = 0; i <= gamma; ++i)
+        if (!(u[i] >= 0.0 && u[i] < 1.0)) f |= OR_ROW_BAD_UNIFORM;
+    if (f) {
+        *accept_len = -1;
+        *flags = f;
+        return;
+    }
+    int n = 0, rejected = 0, yj = -1;
+    for (int i = 0; i < gamma; ++i) {
+        int y = argmax_row(draft, dtype, doff + (size_t)i * V, V);
+        if (y < 0) {
+            f |= OR_ROW_NONFINITE;
+            break;
+        }
+        yhat[i] = y;
+        if (T == 0.0) {
+            int a = argmax_row(target, dtype, toff + (size_t)i * V, V);
+            if (a < 0) {
+                f |= OR_ROW_NONFINITE;
+                break;
+            }
+            acc_margin[i] = INFINITY;
+            if (y == a) {
+                tokens[i] = y;
+                ++n;
+                continue;
+            }
+            tokens[i] = a;
+            *cdf_margin = INFINITY;
+            *accept_len = n;
+            *flags = 0;
+            return;
+        }
+        f |= softmax_row(target, dtype, toff + (size_t)i * V, V, T, p);
+        if (f) break;
+        acc_margin[i] = fabs(u[i] - p[y]);
+        if (u[i] < p[y]) {
+            tokens[i] = y;
+            ++n;
+            continue;
+        }
+        rejected = 1;
+        yj = y;
+        break;
+    }
+    if (!f && !rejected) {
+        if (T == 0.0) {
+            int a = argmax_row(target, dtype, toff + (size_t)gamma * V, V);
+            if (a < 0) {
+                f |= OR_ROW_NONFINITE;
+            } else {
+                tokens[gamma] = a;
+                *cdf_margin = INFINITY;
+                *accept_len = n;
+                *flags = 0;
+                return;
+            }
+        } else {
+            f |= softmax_row(target, dtype, toff + (size_t)gamma * V, V, T, p);
+        }
+    }
+    if (f) {
+        for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
+        *accept_len = -1;
+        *flags = f;
+        return;
+    }
+    memcpy(r, p, sizeof(double) * (size_t)V);
+    if (rejected) r[yj] = 0.0;
+    tokens[n] = cdf_draw(r, V, u[gamma], cdf_margin);
+    *accept_len = n;
+    *flags = 0;
+}
+
+/*
+ * Batched target-only verification (OpenMP over sequences).
+ *   target [B, gamma+1, V], draft [B, gamma, V], temp [B], u [B, gamma+1]
+ * Outputs: tokens [B, gamma+1], accept_len [B], yhat [B, gamma], flags [B],
+ *   acc_margin [B, gamma] = |u_i - p_i(y_i)|, cdf_margin [B].
+ */
+int oracle_to_verify(const void *target, const void *draft, int dtype, const double *temp, const double *u, int B,
+                     int gamma, int V, int32_t *tokens, int32_t *accept_len, int32_t *yhat, int32_t *flags,
+                     double *acc_margin, double *cdf_margin)
+{
+    if (B < 0 || gamma < 1 || V < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)V * 2);
+        if (!buf) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        to_verify_one(target, draft, dtype, (size_t)b * (gamma + 1) * V, (size_t)b * gamma * V, temp[b],
+                      u + (size_t)b * (gamma + 1), gamma, V, tokens + (size_t)b * (gamma + 1), accept_len + b,
+                      yhat + (size_t)b * gamma, flags + b, acc_margin + (size_t)b * gamma, cdf_margin + b, buf,
+                      buf + V);
+        free(buf);
+    }
+    return fail ? 2 : 0;
+}
+
+/*
+ * Per-position acceptance diagnostics, every position (no decisions).  For
+ * draft position i < gamma with p = softmax(target_i / T), q =
+ * softmax(draft_i / T): alpha_i = sum min(p, q), tv_i = d_TV(p, q), ent_q_i =
+ * H(q), kl_i = D_KL(q || p), yhat_i = arg max of the draft logits, p_yhat_i
+ * = p(yhat_i), and rs_better_i = [d_TV(p, q) < 1 - p(yhat_i)], the boundary
+ * below which rejection sampling accepts more than target-only sampling
+ * [BB, App. E "Rejection Sampling Decision Boundary Derivation"; §8
+ * "Robustness of acceptance methods"].  ent_p_i = H(p_i) for i <= gamma.
+ * boundary_margin_i = |d_TV - (1 - p(yhat))| for the parity rule.
+ */
+int oracle_diagnostics(const void *target, const void *draft, int dtype, const double *temp, int B, int gamma, int V,
+                       double *alpha, double *tv, double *ent_q, double *kl, int32_t *yhat, double *p_yhat,
+                       int32_t *rs_better, double *boundary_margin, double *ent_p, int32_t *flags)
+{
+    if (B < 0 || gamma < 1 || V < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V * 2);
+        if (!p) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        double *q = p + V;
+        double T = temp[b];
+        int f = (!(T > 0.0) || isinf(T)) ? OR_ROW_BAD_TEMP : 0;
+        size_t toff = (size_t)b * (gamma + 1) * V, doff = (size_t)b * gamma * V;
+        for (int i = 0; i <= gamma && !f; ++i) {
+            f |= softmax_row(target, dtype, toff + (size_t)i * V, V, T, p);
+            if (f) break;
+            ent_p[(size_t)b * (gamma + 1) + i] = entropy(p, V);
+            if (i < gamma) {
+                size_t o = (size_t)b * gamma + i;
+                f |= softmax_row(draft, dtype, doff + (size_t)i * V, V, T, q);
+                if (f) break;
+                int y = argmax_row(draft, dtype, doff + (size_t)i * V, V);
+                alpha[o] = overlap(p, q, V);
+                tv[o] = tv_distance(p, q, V);
+                ent_q[o] = entropy(q, V);
+                kl[o] = kl_qp(q, p, V);
+                yhat[o] = y;
+                p_yhat[o] = p[y];
+                rs_better[o] = tv[o] < 1.0 - p[y];
+                boundary_margin[o] = fabs(tv[o] - (1.0 - p[y]));
+            }
+        }
+        if (f) {
+            for (int i = 0; i < gamma; ++i) {
+                size_t o = (size_t)b * gamma + i;
+                alpha[o] = tv[o] = ent_q[o] = kl[o] = p_yhat[o] = boundary_margin[o] = NAN;
+                yhat[o] = -1;
+                rs_better[o] = -1;
+            }
+            for (int i = 0; i <= gamma; ++i) ent_p[(size_t)b * (gamma + 1) + i] = NAN;
+        }
+        flags[b] = f;
+        free(p);
     }
     return fail ? 2 : 0;
 }

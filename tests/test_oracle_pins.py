@@ -375,7 +375,7 @@ def test_flags_and_defined_outputs():
     ids = np.zeros((B, gamma), np.int32)
     u = np.full((B, gamma + 1), 0.5)
     temp = np.ones(B)
-    temp[1] = 0.0
+    temp[1] = -1.0  # T = 0 is greedy decoding, a negative temperature is invalid
     ids[2, 1] = V
     u[3, 0] = 1.0
     t[4, 0, 7] = np.nan
@@ -389,3 +389,171 @@ def test_flags_and_defined_outputs():
     assert out["flags"][5] == oracle.ROW_NONFINITE
     for b in range(1, B):
         assert out["accept_len"][b] == -1 and np.all(out["tokens"][b] == -1)
+
+
+# ------------------------------------------------ greedy and target-only --
+
+def _greedy_reference(t, ids):
+    """Greedy decoding written out with numpy arg max (first index among
+    equals): accept while the draft is the target's arg max, then emit it."""
+    toks = []
+    for i in range(ids.shape[0] + 1):
+        a = int(np.argmax(t[i]))
+        if i < ids.shape[0] and ids[i] == a:
+            toks.append(a)
+            continue
+        toks.append(a)
+        break
+    n = len(toks) - 1
+    return toks + [-1] * (ids.shape[0] + 1 - len(toks)), n
+
+
+def test_greedy_verify_is_the_argmax_prefix():
+    """T = 0 is greedy decoding: p and q one-hot at their arg max, so rejection
+    sampling accepts a draft iff it is the target's arg max (summary App. D.2,
+    App. G: target-only selects by arg max)."""
+    rng = np.random.default_rng(21)
+    B, gamma, V = 40, 4, 60
+    t = rng.standard_normal((B, gamma + 1, V))
+    t[5, 2, 7] = t[5, 2].max() + 1.0
+    t[5, 2, 3] = t[5, 2, 7]  # a tie: the smaller index wins
+    ids = np.where(rng.random((B, gamma)) < 0.7, t[:, :gamma].argmax(-1), rng.integers(0, V, (B, gamma))).astype(np.int32)
+    d = rng.standard_normal((B, gamma, V))
+    u = rng.random((B, gamma + 1))
+    out = oracle.verify(t, d, ids, np.zeros(B), u)
+    to = oracle.to_verify(t, np.where(np.arange(V)[None, None] == ids[..., None], 5.0, 0.0), np.zeros(B), u)
+    for b in range(B):
+        toks, n = _greedy_reference(t[b], ids[b])
+        assert list(out["tokens"][b]) == toks and out["accept_len"][b] == n, b
+        assert list(to["tokens"][b]) == toks and to["accept_len"][b] == n, b
+    assert np.all(out["flags"] == 0)
+    # statistics need T > 0
+    assert np.all(oracle.verify(t[:2], d[:2], ids[:2], np.zeros(2), u[:2], want_stats=True)["flags"] == oracle.ROW_BAD_TEMP)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_target_only_law_is_p_enumeration(T):
+    """Target-only sampling (summary §2, App. D.2): the draft is arg max q,
+    accepted with probability p(yhat); the replacement at a rejection is drawn
+    from p without yhat.  Exhaustive enumeration at V = 8: the first-token law
+    is p exactly and the acceptance probability is p(yhat)."""
+    rng = np.random.default_rng(22)
+    V = 8
+    zt = _rows(rng, 2, V, 1.3)
+    zd = zt[:1] + rng.standard_normal((1, V)) * 0.9
+    p0, p1 = scipy.special.softmax(zt / T, axis=-1)
+    yhat = int(np.argmax(zd[0]))
+    py = p0[yhat]
+    resid = p0.copy()
+    resid[yhat] = 0.0
+    cases, weights, kinds = [], [], []
+    for kind, u0, l0 in [("acc", py / 2, py), ("rej", (py + 1) / 2, 1 - py)]:
+        w = p1 if kind == "acc" else resid
+        for u1, l1 in zip(*_intervals(w)):
+            cases.append([u0, u1])
+            weights.append(l0 * l1)
+            kinds.append(kind)
+    B = len(cases)
+    out = oracle.to_verify(np.broadcast_to(zt, (B, 2, V)).copy(), np.broadcast_to(zd, (B, 1, V)).copy(),
+                           np.full(B, T), np.array(cases))
+    weights = np.array(weights)
+    assert np.all(out["yhat"][:, 0] == yhat)
+    first = np.zeros(V)
+    np.add.at(first, out["tokens"][:, 0], weights)
+    np.testing.assert_allclose(first, p0, rtol=0, atol=1e-12)
+    acc = out["accept_len"] == 1
+    np.testing.assert_allclose(weights[acc].sum(), py, atol=1e-12)
+    second = np.zeros(V)
+    np.add.at(second, out["tokens"][acc, 1], weights[acc])
+    np.testing.assert_allclose(second / py, p1, rtol=0, atol=1e-12)
+
+
+def test_target_only_acceptance_product():
+    """gamma = 2: P(n >= 1) = p_0(yhat_0) and P(n >= 2) = p_0(yhat_0) p_1(yhat_1)."""
+    rng = np.random.default_rng(23)
+    V = 8
+    zt = _rows(rng, 3, V, 1.0)
+    zd = zt[:2] + rng.standard_normal((2, V)) * 0.7
+    p = scipy.special.softmax(zt, axis=-1)
+    y = zd.argmax(-1)
+    a0, a1 = p[0, y[0]], p[1, y[1]]
+    cases, weights = [], []
+    for u0, l0 in [(a0 / 2, a0), ((a0 + 1) / 2, 1 - a0)]:
+        for u1, l1 in [(a1 / 2, a1), ((a1 + 1) / 2, 1 - a1)]:
+            cases.append([u0, u1, 0.5])
+            weights.append(l0 * l1)
+    B = len(cases)
+    out = oracle.to_verify(np.broadcast_to(zt, (B, 3, V)).copy(), np.broadcast_to(zd, (B, 2, V)).copy(),
+                           np.ones(B), np.array(cases))
+    n = out["accept_len"]
+    w = np.array(weights)
+    np.testing.assert_allclose(w[n >= 1].sum(), a0, atol=1e-12)
+    np.testing.assert_allclose(w[n >= 2].sum(), a0 * a1, atol=1e-12)
+
+
+def test_diagnostics_against_library_routines():
+    """alpha = 1 - TV; H(q) and D_KL(q || p) as scipy.stats.entropy computes
+    them; yhat = arg max q; p(yhat); rs_better = [TV < 1 - p(yhat)]
+    (summary App. E)."""
+    rng = np.random.default_rng(24)
+    B, gamma, V = 6, 3, 400
+    t = rng.standard_normal((B, gamma + 1, V)) * np.linspace(0.5, 4, B)[:, None, None]
+    d = t[:, :gamma] + rng.standard_normal((B, gamma, V)) * 0.6
+    T = np.linspace(0.6, 1.4, B)
+    o = oracle.diagnostics(t, d, T)
+    assert np.all(o["flags"] == 0)
+    for b in range(B):
+        for i in range(gamma):
+            p = scipy.special.softmax(t[b, i] / T[b])
+            q = scipy.special.softmax(d[b, i] / T[b])
+            assert o["yhat"][b, i] == int(np.argmax(q))
+            np.testing.assert_allclose(o["ent_q"][b, i], scipy.stats.entropy(q), rtol=1e-12)
+            np.testing.assert_allclose(o["kl"][b, i], scipy.stats.entropy(q, p), rtol=1e-10)
+            np.testing.assert_allclose(o["p_yhat"][b, i], p[np.argmax(q)], rtol=1e-12)
+            tv = 0.5 * np.abs(p - q).sum()
+            np.testing.assert_allclose(o["alpha"][b, i], 1 - tv, atol=1e-12)
+            assert o["rs_better"][b, i] == int(tv < 1 - p[np.argmax(q)])
+        for i in range(gamma + 1):
+            np.testing.assert_allclose(o["ent_p"][b, i], scipy.stats.entropy(scipy.special.softmax(t[b, i] / T[b])),
+                                       rtol=1e-12)
+    # D_KL(q || q) = 0, and an unsupported q mass makes it infinite
+    same = oracle.diagnostics(t[:1], t[:1, :gamma], [1.0])
+    np.testing.assert_allclose(same["kl"], 0.0, atol=1e-12)
+    masked = t[:1].copy()
+    masked[0, 0, 0] = -np.inf
+    assert np.isinf(oracle.diagnostics(masked, t[:1, :gamma], [1.0])["kl"][0, 0])
+
+
+def test_decision_boundary_matches_enumerated_acceptance():
+    """Summary App. E: rejection sampling accepts the first draft more often
+    than target-only sampling iff d_TV(p, q) < 1 - p(yhat).  The acceptance
+    probabilities are enumerated from the two verify oracles (y ~ q with the
+    accept threshold of each draft, and the target-only threshold)."""
+    rng = np.random.default_rng(25)
+    V = 8
+    seen = set()
+    for trial in range(40):
+        zt = _rows(rng, 2, V, rng.uniform(0.3, 3.0))
+        zd = zt[:1] + rng.standard_normal((1, V)) * rng.uniform(0.05, 2.5)
+        p0 = scipy.special.softmax(zt[0])
+        q0 = scipy.special.softmax(zd[0])
+        # RS: y ~ q, accept region of u per y
+        ids, us, w = [], [], []
+        for y in range(V):
+            for kind, u0, l0 in _accept_regions(p0, q0, y):
+                ids.append([y])
+                us.append([u0, 0.5])
+                w.append(q0[y] * l0)
+        rs = _verify_rows(zt, zd, ids, us)
+        p_rs = np.array(w)[rs["accept_len"] == 1].sum()
+        # TO: one draft (arg max q), two u-regions
+        py = p0[np.argmax(zd[0])]
+        to = oracle.to_verify(np.broadcast_to(zt, (2, 2, V)).copy(), np.broadcast_to(zd, (2, 1, V)).copy(),
+                              np.ones(2), np.array([[py / 2, 0.5], [(py + 1) / 2, 0.5]]))
+        p_to = np.array([py, 1 - py])[to["accept_len"] == 1].sum()
+        dg = oracle.diagnostics(zt[None], zd[None], [1.0])
+        if dg["boundary_margin"][0, 0] < 1e-9:
+            continue
+        assert dg["rs_better"][0, 0] == int(p_rs > p_to), trial
+        seen.add(int(p_rs > p_to))
+    assert seen == {0, 1}
