@@ -470,10 +470,18 @@ static void to_verify_one(const void *target, const void *draft, int dtype, size
         return;
     }
     memcpy(r, p, sizeof(double) * (size_t)V);
-    if (rejected) r[yj] = 0.0;
+    if (rejected) {
+        r[yj] = 0.0;
+        double R = 0.0;
+        for (int v = 0; v < V; ++v) R += r[v];
+        if (!(R > 0.0)) { /* p(y) rounds to 1: draw from p, as for rejection sampling */
+            f |= OR_ROW_ZERO_MASS;
+            memcpy(r, p, sizeof(double) * (size_t)V);
+        }
+    }
     tokens[n] = cdf_draw(r, V, u[gamma], cdf_margin);
     *accept_len = n;
-    *flags = 0;
+    *flags = f;
 }
 
 /*
