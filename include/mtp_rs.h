@@ -62,7 +62,7 @@ typedef enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 } mtp_dtype;
 enum {
     MTP_ROW_NONFINITE = 1,   /* a read logit is NaN or +inf, or a read row is all -inf */
     MTP_ROW_BAD_ID = 2,      /* a draft id outside [0, V) */
-    MTP_ROW_BAD_TEMP = 4,    /* temperature <= 0, NaN or inf */
+    MTP_ROW_BAD_TEMP = 4,    /* temperature < 0, NaN or inf (0 is greedy where supported) */
     MTP_ROW_ZERO_MASS = 8,   /* residual mass rounded to 0 at a rejection; the
                                 token was drawn from p_j instead (outputs valid) */
     MTP_ROW_BAD_UNIFORM = 16,/* a uniform outside [0, 1) or NaN */
@@ -88,8 +88,14 @@ enum {
  * bounded part of the next position's rows before a decision is known; it
  * never reads beyond the caller's arrays).
  *
+ * T_b == 0 is greedy decoding: p and q are one-hot at the row's arg max
+ * (ties to the smallest index), so y_i is accepted iff it is the target's
+ * arg max, and the next token is the target's arg max; statistics need
+ * T_b > 0 (a greedy sequence with alpha/entropy requested is flagged
+ * MTP_ROW_BAD_TEMP).
+ *
  *   target_logits [B, gamma+1, V] dtype     draft_logits [B, gamma, V] dtype
- *   draft_ids     [B, gamma] int32          temperature  [B] float32 (> 0)
+ *   draft_ids     [B, gamma] int32          temperature  [B] float32 (>= 0)
  *   uniforms      [B, gamma+1] float32 in [0, 1)
  *   out_tokens    [B, gamma+1] int32: accepted drafts, then the drawn token,
  *                 then -1 padding.                               (required)
@@ -108,6 +114,34 @@ int mtp_rs_verify(const void *target_logits, const void *draft_logits, mtp_dtype
                   int B, int gamma, int V,
                   int32_t *out_tokens, int32_t *accept_len, float *alpha, float *entropy,
                   int32_t *row_flags, mtp_stream_t stream);
+
+/*
+ * mtp_to_verify -- batched target-only verification [BB §2 "Acceptance
+ * methods", App. D.2 "Target-Only Sampling"].
+ *
+ * For each sequence b: the draft token of position i is y_i = arg max of
+ * draft[b,i] (ties to the smallest index; no draft probability is formed),
+ * accepted iff uniforms[b,i] < p_i(y_i) with p_i = softmax(target[b,i]/T_b).
+ * At the first rejection j the replacement is drawn by inverse CDF with
+ * uniforms[b,gamma] from p_j with y_j removed -- the residual of rejection
+ * sampling with a one-hot draft, so the output law stays p.  After gamma
+ * accepts the bonus token is drawn from p_gamma.  T_b == 0 is greedy: accept
+ * while y_i is the target's arg max, then emit the target's arg max.
+ *
+ *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V], dtype as above
+ *   temperature [B] (>= 0), uniforms [B, gamma+1] in [0, 1)
+ *   out_tokens [B, gamma+1], accept_len [B]              (required)
+ *   draft_tokens [B, gamma] int32 or NULL: y_i for every position whose
+ *                decision was taken, -1 elsewhere
+ *   row_flags [B] or NULL
+ * Requirements: rows of whole 16-byte vectors (V a multiple of 8 for bf16,
+ * 4 for float32; MTP_ERR_MISALIGNED otherwise) and gamma <= 8
+ * (MTP_ERR_INVALID_ARG otherwise).
+ */
+int mtp_to_verify(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                  const float *temperature, const float *uniforms, int B, int gamma, int V,
+                  int32_t *out_tokens, int32_t *accept_len, int32_t *draft_tokens, int32_t *row_flags,
+                  mtp_stream_t stream);
 
 /*
  * mtp_row_stats -- per-position overlap and target entropy without

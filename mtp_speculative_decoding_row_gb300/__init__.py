@@ -29,7 +29,8 @@ ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM, ROW_TIM
 ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_TIMEOUT
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string")
+EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan",
+                    "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
             "tv_loss_resident": 5}
 
@@ -60,6 +61,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.mtp_rs_verify.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, P]
     lib.mtp_rs_verify.restype = I
+    lib.mtp_to_verify.argtypes = [P, P, I, P, P, I, I, I, P, P, P, P, P]
+    lib.mtp_to_verify.restype = I
     lib.mtp_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
     lib.mtp_row_stats.restype = I
     lib.mtp_tv_loss_fwd_bwd.argtypes = [P, P, I, F, I, I, I, F, P, P, P, P, P]
@@ -138,6 +141,13 @@ class VerifyResult(NamedTuple):
     row_flags: "object"   # [B] int32
 
 
+class TOVerifyResult(NamedTuple):
+    tokens: "object"        # [B, gamma+1] int32, -1 padded
+    accept_len: "object"    # [B] int32 (-1 if flagged)
+    draft_tokens: "object"  # [B, gamma] int32: arg max draft token of each decided position, -1 elsewhere
+    row_flags: "object"     # [B] int32
+
+
 class StatsResult(NamedTuple):
     alpha: "object"
     entropy: "object"
@@ -179,6 +189,35 @@ def mtp_rs_verify(target_logits, draft_logits, draft_ids, temperature, uniforms,
         _ptr(out.row_flags), _stream(dev, stream))
     if rc:
         raise MTPError("mtp_rs_verify", rc)
+    return out
+
+
+def mtp_to_verify(target_logits, draft_logits, temperature, uniforms, *, out: Optional["TOVerifyResult"] = None,
+                  stream=None) -> "TOVerifyResult":
+    """Batched target-only verification (see mtp_to_verify in
+    include/mtp_rs.h): the draft token of each position is the arg max of its
+    draft logits, accepted iff u < p(y).  Returns tokens [B, gamma+1],
+    accept_len [B], draft_tokens [B, gamma] and row_flags [B]."""
+    torch = _torch()
+    dev = target_logits.device
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    _check(target_logits, "target_logits", dev)
+    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
+    _check(temperature, "temperature", dev, torch.float32, (B,))
+    _check(uniforms, "uniforms", dev, torch.float32, (B, gamma + 1))
+    if out is None:
+        out = TOVerifyResult(
+            torch.empty((B, gamma + 1), dtype=torch.int32, device=dev),
+            torch.empty((B,), dtype=torch.int32, device=dev),
+            torch.empty((B, gamma), dtype=torch.int32, device=dev),
+            torch.empty((B,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_to_verify(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(temperature), _ptr(uniforms), B,
+        gamma, V, _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.draft_tokens), _ptr(out.row_flags),
+        _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_to_verify", rc)
     return out
 
 

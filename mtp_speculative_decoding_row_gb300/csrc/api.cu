@@ -166,7 +166,7 @@ int stream_chunk_for(int nvs) {
     return nvs >= 8 * 192 ? 192 : 128;
 }
 
-bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) {
+bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, int mode = 0) {
     const int forced = env_cluster();
     int R = env_int("MTP_RS_RING");
     if (R < 2 || R > stream_max_ring()) R = 2;
@@ -186,13 +186,13 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
         const int S = C * nw;
         if (S > stream_max_segments()) continue;
         const int nvs = (nv + S - 1) / S;
-        const int cv = stream_chunk_for(nvs);
+        const int cv = mode == 1 ? 128 : stream_chunk_for(nvs);
         if ((nvs + cv - 1) / cv > stream_max_chunks()) continue;
         if (!forced && C > 1 && nvs < 64) continue;
         const uint32_t smem = stream_hdr_bytes() + stream_rec_bytes(gamma, S) +
                               static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
         if (smem > cap) continue;
-        const void *func = stream_kernel(dtype, cv);
+        const void *func = stream_kernel(dtype, cv, mode);
         if (prepare_func(dev, func) != cudaSuccess) return false;
         const int nc = max_clusters(dev, func, C, smem, stream_threads());
         if (nc <= 0) continue;
@@ -387,6 +387,7 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     A.alpha = alpha;
     A.entropy = entropy;
     A.flags = flags;
+    A.yhat = nullptr;
     return launch(func, p, &A, stream);
 }
 
@@ -401,6 +402,46 @@ extern "C" int mtp_rs_verify(const void *target_logits, const void *draft_logits
     const int mode = alpha ? MODE_VERIFY_STATS : MODE_VERIFY;
     return row_call(mode, target_logits, draft_logits, dtype, draft_ids, temperature, uniforms, B, gamma, V,
                     out_tokens, accept_len, alpha, entropy, row_flags, stream);
+}
+
+extern "C" int mtp_to_verify(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                             const float *temperature, const float *uniforms, int B, int gamma, int V,
+                             int32_t *out_tokens, int32_t *accept_len, int32_t *draft_tokens, int32_t *row_flags,
+                             mtp_stream_t stream) {
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (B == 0) return MTP_OK;
+    if (!target_logits || !draft_logits || !temperature || !uniforms || !out_tokens || !accept_len)
+        return MTP_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return MTP_ERR_MISALIGNED;
+    const int es = esize(dtype);
+    // the streaming kernel serves target-only verification: whole 16-byte
+    // vectors per row and gamma up to its limit
+    if (V % (16 / es) != 0) return MTP_ERR_MISALIGNED;
+    if (gamma > stream_max_gamma()) return MTP_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    Plan p;
+    if (!plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, gamma, B, p, 1)) return MTP_ERR_NO_DEVICE;
+    VerifyArgs A = {};
+    A.target = target_logits;
+    A.draft = draft_logits;
+    A.ids = nullptr;
+    A.temp = temperature;
+    A.unif = uniforms;
+    A.B = B;
+    A.gamma = gamma;
+    A.V = V;
+    A.aligned = 1;
+    A.streams = 1;
+    A.ring = p.ring;
+    A.depth = p.depth;
+    A.seg_vectors = p.seg_vectors;
+    A.tokens = out_tokens;
+    A.accept_len = accept_len;
+    A.flags = row_flags;
+    A.yhat = draft_tokens;
+    return launch(p.func, p, &A, stream);
 }
 
 extern "C" int mtp_row_stats(const void *target_logits, const void *draft_logits, mtp_dtype dtype,

@@ -28,6 +28,7 @@ struct VerifyArgs {
     float *alpha;           // [B, gamma]        (stats modes)
     float *entropy;         // [B, gamma+1]      (stats modes)
     int32_t *flags;         // [B] or null
+    int32_t *yhat;          // [B, gamma] or null (target-only: the arg max draft tokens)
 };
 
 struct TVArgs {
@@ -65,7 +66,8 @@ int stream_max_ring();
 
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);
-const void *stream_kernel(int dtype, int cv);  // cv: 128 or 192 vectors per chunk
+// cv: 128 or 192 vectors per chunk; mode 0 = rejection sampling, 1 = target-only
+const void *stream_kernel(int dtype, int cv, int mode);
 const void *tv_kernel(int dtype);
 const void *tvs_kernel(int dtype, int cv);  // streaming TV kernel, cv: 128 or 192
 

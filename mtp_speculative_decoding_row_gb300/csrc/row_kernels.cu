@@ -92,6 +92,47 @@ __device__ __forceinline__ void block_soft(float (*tp)[NT], Soft &at, Soft &ad, 
     }
 }
 
+// Arg max across the warp: the largest value, ties to the smallest index
+// (index -1: none).  Same result in every lane.
+__device__ __forceinline__ void warp_argmax(float &v, int &i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(FULL, v, o);
+        const int oi = __shfl_xor_sync(FULL, i, o);
+        if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+// Per-thread arg max (and flag bits) -> CTA arg max in every lane of warp 0.
+__device__ __forceinline__ void block_argmax(float (*tp)[NT], float &v, int &i, int &bad) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    tp[0][tid] = v;
+    tp[1][tid] = __int_as_float(i);
+    tp[2][tid] = __int_as_float(bad);
+    __syncthreads();
+    if (warp == 0) {
+        float bv = -INFINITY;
+        int bi = -1, bb = 0;
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+            const float ov = tp[0][lane + 32 * q];
+            const int oi = __float_as_int(tp[1][lane + 32 * q]);
+            if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+            bb |= __float_as_int(tp[2][lane + 32 * q]);
+        }
+        warp_argmax(bv, bi);
+        v = bv;
+        i = bi;
+        bad = warp_allor(bb);
+    }
+}
+
 // Per-thread sum -> CTA sum in every lane of warp 0.
 __device__ __forceinline__ float block_sum(float (*tp)[NT], float v) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -355,10 +396,10 @@ __device__ __forceinline__ void issue_unit(const VerifyArgs &A, StreamSt &st, co
 
 // Argument checks of stream si's sequence, from its prefetched parameters
 // (the same in every CTA of the cluster).
-__device__ __forceinline__ int validate_seq(const RowShared &sh, int si, int g, int V, bool decide) {
+__device__ __forceinline__ int validate_seq(const RowShared &sh, int si, int g, int V, bool decide, bool greedy_ok) {
     const float T = sh.T[si];
     int f = 0;
-    if (!(T > 0.f) || !(T < INFINITY)) f |= F_BAD_TEMP;
+    if (!(greedy_ok ? T >= 0.f : T > 0.f) || !(T < INFINITY)) f |= F_BAD_TEMP;
     if (decide) {
         for (int i = 0; i < g; ++i) {
             const int y = sh.ids[si][i];
@@ -446,7 +487,7 @@ __global__ void __launch_bounds__(NT, 4) row_kernel_impl(const VerifyArgs A) {
             const uint32_t lbar = smem_addr(&sh.lbar[si]);
             const int b = st.b, i = st.i;
             bool finish = false;
-            if (i == 0) st.flags |= validate_seq(sh, si, g, A.V, DECIDE);
+            if (i == 0) st.flags |= validate_seq(sh, si, g, A.V, DECIDE, MODE == MODE_VERIFY);
 
             if ((st.flags & ERR_BITS) || dead) {
                 finish = true;
@@ -456,6 +497,69 @@ __global__ void __launch_bounds__(NT, 4) row_kernel_impl(const VerifyArgs A) {
                     st.ph ^= 1u;
                     st.armed = 0;
                 }
+            } else if (MODE == MODE_VERIFY && sh.T[si] == 0.f) {
+                // ---- greedy (T = 0): the target's arg max decides
+                int tmo = 0;
+                if (st.armed) {
+                    if (!mbar_wait_bounded(lbar, st.ph)) tmo = 1;
+                    st.ph ^= 1u;
+                    st.armed = 0;
+                } else if (!A.aligned) {
+                    load_slice<Tin, NT>(s, row_ptr<Tin>(A.target, static_cast<size_t>(b) * (g + 1) + i, A.V), tb, 0, false);
+                }
+                __syncthreads();
+                float bv = -INFINITY;
+                int bi = -1, bad = tmo ? F_TIMEOUT : 0;
+                for (int j = tid; j < s.nvec; j += NT) {
+                    float z[VEC];
+                    S::unpack(vec_at(tb, j), z);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const int v = s.lo + j * VEC + e;
+                        if (v >= s.hi) break;
+                        if (!(z[e] < INFINITY) || z[e] != z[e]) bad |= F_NONFINITE;
+                        else if (z[e] > bv) {
+                            bv = z[e];
+                            bi = v;
+                        }
+                    }
+                }
+                block_argmax(sh.tpart, bv, bi, bad);
+                float rec[4] = {bv, __int_as_float(bi), __int_as_float(bad), 0.f};
+                bool ok;
+                const int slot = xchg_round<4>(sh.x, round, rec, C, rank, ok);
+                float gv = -INFINITY;
+                int gi = -1, gb = ok ? 0 : F_TIMEOUT;
+                {
+                    const int lane = tid & 31;
+                    float v = -INFINITY;
+                    int ix = -1, bb = 0;
+                    if (lane < C) {
+                        v = sh.x.rec[slot][lane][0];
+                        ix = __float_as_int(sh.x.rec[slot][lane][1]);
+                        bb = __float_as_int(sh.x.rec[slot][lane][2]);
+                    }
+                    warp_argmax(v, ix);
+                    gv = v;
+                    gi = ix;
+                    gb |= warp_allor(bb);
+                }
+                (void)gv;
+                if (!ok) dead = true;
+                if (gi < 0) gb |= F_NONFINITE;
+                if (gb) {
+                    st.flags |= gb;
+                    finish = true;
+                } else if (i < g && sh.ids[si][i] == gi) {
+                    if (tid == 0) sh.tok[si][st.n] = gi;
+                    ++st.n;
+                } else {
+                    st.stopped = 1;
+                    st.drawn = gi;
+                    st.writer = 0;
+                    finish = true;
+                }
+                if (!(i < g)) finish = true;
             } else {
                 const float T = sh.T[si];
                 const float k = LOG2E / T;

@@ -69,17 +69,21 @@ struct WarpShared {
     float cs[MAXCH];                // per-chunk sums
 };
 
-// Fixed header; the exchange records ([2][gamma + 2][S + 1] float4) follow
-// it, then the warps' rings.
+// Fixed header; the exchange records follow it, then the warps' rings.
 struct StreamShared {
     unsigned long long xbar[2][QMAX];
     WarpShared w[NW];
 };
 constexpr uint32_t HDR_BYTES = (sizeof(StreamShared) + 127u) & ~127u;
 
+// Exchange records: two float4 per warp per round (a main and an auxiliary
+// record, [2][gamma + 2][2 S] float4), so every round carries the same bytes
+// whatever the sequence's mode.
 __host__ __device__ constexpr uint32_t rec_bytes(int gamma, int S) {
-    return ((2u * static_cast<uint32_t>(gamma + 2) * static_cast<uint32_t>(S + 1) * 16u) + 127u) & ~127u;
+    return ((2u * static_cast<uint32_t>(gamma + 2) * static_cast<uint32_t>(2 * S) * 16u) + 127u) & ~127u;
 }
+
+enum { M_RS = 0, M_TO = 1 };  // rejection sampling / target-only acceptance
 
 constexpr int ERR_BITS = F_NONFINITE | F_BAD_ID | F_BAD_TEMP | F_BAD_UNIFORM | F_TIMEOUT;
 
@@ -142,7 +146,7 @@ __device__ __forceinline__ int chunk_count(const Seg &c, int ch) { return min(c.
 // to c_conf + depth of the consumer's sequence; a later sequence only once
 // the current one's path is fixed) and set the unit's row pointers.  False
 // when the producer has to wait or has no work left.
-template <typename Tin>
+template <typename Tin, int MODE>
 __device__ __forceinline__ bool enter_unit(const VerifyArgs &A, Ctx &c) {
     const int g = c.g;
     if (c.p_kind == K_NORM) {
@@ -161,17 +165,19 @@ __device__ __forceinline__ bool enter_unit(const VerifyArgs &A, Ctx &c) {
     const int b = seq_of(c, c.p_ord);
     const size_t off = static_cast<size_t>(c.seg_lo) * 16u;
     c.p_t = row_base<Tin>(A, true, b, c.p_i) + off;
-    c.p_d = c.p_i < g ? row_base<Tin>(A, false, b, c.p_i) + off : nullptr;
+    // target-only residual passes need the target row alone
+    const bool want_d = c.p_i < g && !(MODE == M_TO && c.p_kind == K_RES);
+    c.p_d = want_d ? row_base<Tin>(A, false, b, c.p_i) + off : nullptr;
     return true;
 }
 
 // Issue chunk copies while ring slots are free and the next chunk is needed
 // or inside the look-ahead.
-template <typename Tin>
+template <typename Tin, int MODE>
 __device__ __forceinline__ void produce(const VerifyArgs &A, Ctx &c) {
     if (c.p_done || c.dead) return;
     while (c.pcount - c.ccount < static_cast<uint32_t>(c.R)) {
-        if (c.p_c == 0 && !enter_unit<Tin>(A, c)) break;
+        if (c.p_c == 0 && !enter_unit<Tin, MODE>(A, c)) break;
         const int cnt = chunk_count(c, c.p_c);
         if (c.lane == 0) {
             // No proxy fence: every generic read of this slot has completed
@@ -225,27 +231,24 @@ __device__ __forceinline__ void drain(Ctx &c) {
 
 // ------------------------------------------------------------ exchange ----
 
+// Record r of round i in `bank`: main records at r = segment, auxiliary
+// records at r = S + segment.
 __device__ __forceinline__ float4 *rec_at(const Ctx &c, int bank, int i, int r) {
-    return c.rec + (static_cast<size_t>(bank * c.Q + i) * (c.S + 1) + r);
+    return c.rec + (static_cast<size_t>(bank * c.Q + i) * (2 * c.S) + r);
 }
 
-// Bytes every CTA receives in round i of a sequence: S records, plus the
-// draft-token logits for a position with a draft.
-__device__ __forceinline__ uint32_t round_bytes(const Ctx &c, int i) {
-    return static_cast<uint32_t>(c.S + (i < c.g ? 1 : 0)) * 16u;
-}
+// Bytes every CTA receives in one round: two records per warp.
+__device__ __forceinline__ uint32_t round_bytes(const Ctx &c) { return static_cast<uint32_t>(2 * c.S) * 16u; }
 
-// Push this warp's record for round i of the current bank into every CTA of
-// the cluster; `ylog` adds the draft-token record (warp holding y only).
-__device__ __forceinline__ void xpush(StreamShared &sh, const Ctx &c, int i, float4 v, bool ylog, float4 yv) {
+// Push this warp's main and auxiliary records for round i of the current
+// bank into every CTA of the cluster.
+__device__ __forceinline__ void xpush(StreamShared &sh, const Ctx &c, int i, float4 v, float4 aux) {
     if (c.lane < c.C) {
         const uint32_t rbar = map_rank(smem_addr(&sh.xbar[c.bank][i]), c.lane);
         const uint32_t ra = map_rank(smem_addr(rec_at(c, c.bank, i, c.sg)), c.lane);
+        const uint32_t xa = map_rank(smem_addr(rec_at(c, c.bank, i, c.S + c.sg)), c.lane);
         st_async_v4(ra, v.x, v.y, v.z, v.w, rbar);
-        if (ylog) {
-            const uint32_t ya = map_rank(smem_addr(rec_at(c, c.bank, i, c.S)), c.lane);
-            st_async_v4(ya, yv.x, yv.y, yv.z, yv.w, rbar);
-        }
+        st_async_v4(xa, aux.x, aux.y, aux.z, aux.w, rbar);
     }
 }
 
@@ -323,8 +326,8 @@ __device__ __forceinline__ void vweights(const uint4 &rt, const uint4 &rd, float
 // positive weight of the selected unit when rounding leaves no index.
 template <typename Tin, bool RES, int QV>
 __device__ __noinline__ int walk_segment(const Seg c, const unsigned char *trow, const unsigned char *drow,
-                                         bool scaled, float ref, float k, float ct, float cd, float rem,
-                                         int last) {
+                                         bool scaled, float ref, float k, float ct, float cd, float rem, int last,
+                                         int excl) {
     constexpr int VEC = Store<Tin>::VEC;
     const int lane = threadIdx.x & 31;
     // chunk selection
@@ -371,6 +374,7 @@ __device__ __noinline__ int walk_segment(const Seg c, const unsigned char *trow,
             const uint4 rt = __ldg(gt + j);
             const uint4 rd = RES ? __ldg(gd + j) : rt;
             vweights<Tin, RES>(rt, rd, k, ct, cd, w[r]);
+            if (excl >= 0 && static_cast<size_t>(excl / VEC) == v0 + j) w[r][excl % VEC] = 0.f;
         } else {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) w[r][e] = 0.f;
@@ -473,24 +477,58 @@ __device__ __forceinline__ float res_regs(const uint4 (&rt)[QV], const uint4 (&r
 // ----------------------------------------------------------------- kernel --
 
 // One position's round, gathered: log2 normalisers (log2 p = z k - ct),
-// target maximum, the logits at the draft token, flags, and this lane's two
-// target segment records (segments 2 lane and 2 lane + 1).
+// target maximum, flags, and this lane's two target segment records
+// (segments 2 lane and 2 lane + 1).  Rejection sampling: the logits at the
+// draft token (Zty, Zdy).  Target-only: the draft arg max yhat and the target
+// logit at it (Zty).
 struct Norm {
     float ct, cd, Mt, Zty, Zdy;
+    int yhat;
     int rf;
     float m0, s0, m1, s1;
 };
 
+// Arg max across the warp: the largest value, ties to the smallest index
+// (index -1: no element); `x` travels with the winner.  Same result in every
+// lane.
+__device__ __forceinline__ void argmax_allreduce(float &v, int &i, float &x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(FULL, v, o), ox = __shfl_xor_sync(FULL, x, o);
+        const int oi = __shfl_xor_sync(FULL, i, o);
+        if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
+            v = ov;
+            i = oi;
+            x = ox;
+        }
+    }
+}
+
+__device__ __forceinline__ void argmax_merge(float &v, int &i, float &x, float ov, int oi, float ox) {
+    if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
+        v = ov;
+        i = oi;
+        x = ox;
+    }
+}
+
+template <int MODE>
 __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool has_d) {
     Norm r;
     r.m0 = r.m1 = -INFINITY;
     r.s0 = r.s1 = 0.f;
+    r.yhat = -1;
     float dm = -INFINITY, ds = 0.f;
+    float zt_l = 0.f, zd_l = 0.f;
+    int hy = 0;
+    float av = -INFINITY, ax = 0.f;  // target-only: draft arg max and target logit there
+    int ai = -1;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int q = 2 * c.lane + h;
         if (q < c.S) {
             const float4 v = *rec_at(c, c.bank, i, q);
+            const float4 x = *rec_at(c, c.bank, i, c.S + q);
             if (h == 0) {
                 r.m0 = v.x;
                 r.s0 = v.y;
@@ -498,13 +536,22 @@ __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool h
                 r.m1 = v.x;
                 r.s1 = v.y;
             }
-            if (v.w != 0.f) {  // draft partial of this lane (NaN propagates)
-                if (v.z > dm) {
-                    ds = (ds != 0.f ? ds * ex2((dm - v.z) * k) : 0.f) + v.w;
-                    dm = v.z;
-                } else {
-                    ds += v.w * ex2((v.z - dm) * k);
+            if (MODE == M_RS) {
+                if (v.w != 0.f) {  // draft partial of this lane (NaN propagates)
+                    if (v.z > dm) {
+                        ds = (ds != 0.f ? ds * ex2((dm - v.z) * k) : 0.f) + v.w;
+                        dm = v.z;
+                    } else {
+                        ds += v.w * ex2((v.z - dm) * k);
+                    }
                 }
+                if (x.z != 0.f) {
+                    hy = 1;
+                    zt_l = x.x;
+                    zd_l = x.y;
+                }
+            } else {
+                argmax_merge(av, ai, ax, v.z, __float_as_int(x.x), v.w);
             }
         }
     }
@@ -526,21 +573,117 @@ __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool h
     r.cd = 0.f;
     r.Zty = r.Zdy = 0.f;
     if (has_d) {
-        Soft ld;
-        ld.m = dm;
-        ld.s = ds;
-        ld.s1 = 0.f;
-        const Soft Cd = soft_warp_allreduce<false>(ld, k);
-        if (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY)) r.rf |= F_NONFINITE;
-        r.cd = fmaf(Cd.m, k, log2f(Cd.s));
-        const float4 y = *rec_at(c, c.bank, i, c.S);
-        r.Zty = y.x;
-        r.Zdy = y.y;
+        if (MODE == M_RS) {
+            Soft ld;
+            ld.m = dm;
+            ld.s = ds;
+            ld.s1 = 0.f;
+            const Soft Cd = soft_warp_allreduce<false>(ld, k);
+            if (!(Cd.m > -INFINITY) || !(Cd.s > 0.f) || !(Cd.s < INFINITY)) r.rf |= F_NONFINITE;
+            r.cd = fmaf(Cd.m, k, log2f(Cd.s));
+            const unsigned hm = __ballot_sync(FULL, hy != 0);
+            const int src = hm ? (__ffs(hm) - 1) : 0;
+            r.Zty = __shfl_sync(FULL, zt_l, src);
+            r.Zdy = __shfl_sync(FULL, zd_l, src);
+        } else {
+            argmax_allreduce(av, ai, ax);
+            if (ai < 0) r.rf |= F_NONFINITE;  // an all -inf draft row
+            r.yhat = ai;
+            r.Zty = ax;
+        }
     }
     return r;
 }
 
-template <typename Tin, int CV>
+// Greedy round (T = 0): target arg max and, target-only, the draft arg max.
+struct Greedy {
+    int tidx, didx, bad;
+};
+
+__device__ __forceinline__ Greedy gather_greedy(const Ctx &c, int i) {
+    float tv = -INFINITY, dv = -INFINITY, dummy = 0.f;
+    int ti = -1, di = -1, bad = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int q = 2 * c.lane + h;
+        if (q < c.S) {
+            const float4 v = *rec_at(c, c.bank, i, q);
+            const float4 x = *rec_at(c, c.bank, i, c.S + q);
+            argmax_merge(tv, ti, dummy, v.x, __float_as_int(v.y), 0.f);
+            argmax_merge(dv, di, dummy, v.z, __float_as_int(v.w), 0.f);
+            bad |= x.x != 0.f;
+        }
+    }
+    argmax_allreduce(tv, ti, dummy);
+    argmax_allreduce(dv, di, dummy);
+    Greedy r;
+    r.tidx = ti;
+    r.didx = di;
+    r.bad = __any_sync(FULL, bad) ? 1 : 0;
+    return r;
+}
+
+// Running arg max of one chunk row held by this lane (first index among
+// equals in ascending vocabulary order; cmx: the lane's chunk maximum from
+// chunk_max).  vbase: vocabulary index of this lane's first vector in the
+// chunk (vector q sits 32 q vectors further).  With `other`, x receives the
+// other row's logit at the new arg max.
+template <typename Tin, int QV, bool OTHER>
+__device__ __forceinline__ void argmax_regs(const uint4 (&r)[QV], const uint4 (&o)[QV], float cmx, int vbase,
+                                            float &m, int &idx, float &x) {
+    constexpr int VEC = Store<Tin>::VEC;
+    if (!(cmx > m) || !(cmx < INFINITY)) return;  // no improvement (or a NaN / +inf row, flagged elsewhere)
+    bool found = false;
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            if (!found && vec_elem<Tin>(r[q], e) == cmx) {
+                found = true;
+                idx = (vbase + q * 32) * VEC + e;
+                if (OTHER) x = vec_elem<Tin>(o[q], e);
+            }
+        }
+    }
+    m = cmx;
+}
+
+// Element e of a 16-byte logit vector set to -inf (probability 0).
+template <typename Tin>
+__device__ __forceinline__ void vec_set_neginf(uint4 &v, int e) {
+    if (Store<Tin>::ES == 4) {
+        const uint32_t w = 0xff800000u;
+        if (e == 0) v.x = w;
+        else if (e == 1) v.y = w;
+        else if (e == 2) v.z = w;
+        else v.w = w;
+    } else {
+        const int wi = e >> 1;
+        const uint32_t mask = (e & 1) ? 0xffff0000u : 0x0000ffffu, val = (e & 1) ? 0xff800000u : 0x0000ff80u;
+        uint32_t *p = wi == 0 ? &v.x : wi == 1 ? &v.y : wi == 2 ? &v.z : &v.w;
+        *p = (*p & ~mask) | val;
+    }
+}
+
+// This lane's sum of p = 2^{z k - ct} over one chunk of the target row.
+template <typename Tin, int QV>
+__device__ __forceinline__ float psum_regs(const uint4 (&rt)[QV], float k, float ct) {
+    constexpr int VEC = Store<Tin>::VEC;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        float w[VEC];
+        vweights<Tin, false>(rt[q], rt[q], k, ct, 0.f, w);
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2) {
+            s0 += w[e];
+            s1 += w[e + 1];
+        }
+    }
+    return s0 + s1;
+}
+
+template <typename Tin, int CV, int MODE>
 __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) {
     using St = Store<Tin>;
     constexpr int VEC = St::VEC;
@@ -594,7 +737,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
             for (int i = 0; i < c.Q; ++i) mbar_init(smem_addr(&sh.xbar[bk][i]), 1);
         fence_mbar_init();
         for (int bk = 0; bk < 2; ++bk)
-            for (int i = 0; i < c.Q; ++i) mbar_arrive_expect_tx(smem_addr(&sh.xbar[bk][i]), round_bytes(c, i));
+            for (int i = 0; i < c.Q; ++i) mbar_arrive_expect_tx(smem_addr(&sh.xbar[bk][i]), round_bytes(c));
     }
     fence_mbar_init();
     __syncthreads();
@@ -607,14 +750,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
         T = 1.f;
         if (b < A.B) {
             if (c.lane <= g) u = __ldg(A.unif + static_cast<size_t>(b) * (g + 1) + c.lane);
-            if (c.lane < g) y = __ldg(A.ids + static_cast<size_t>(b) * g + c.lane);
+            if (MODE == M_RS && c.lane < g) y = __ldg(A.ids + static_cast<size_t>(b) * g + c.lane);
             T = __ldg(A.temp + b);
         }
     };
     float nu, nT;
     int ny;
     load_params(c.cid, nu, ny, nT);
-    produce<Tin>(A, c);
+    produce<Tin, MODE>(A, c);
 
     const float4 ZERO4 = make_float4(0.f, 0.f, 0.f, 0.f);
 
@@ -622,27 +765,30 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
         const int b = seq_of(c, ord);
         if (b >= A.B) break;
         const float my_u = nu, T = nT;
-        const int my_y = ny;
+        int my_y = ny;  // lane l: draft token of position l (target-only: filled at its decision)
         load_params(seq_of(c, ord + 1), nu, ny, nT);
         c.c_ord = ord;
         c.c_conf = 0;
 
         int flags = 0;
         if (c.dead) flags |= F_TIMEOUT;
-        if (!(T > 0.f) || !(T < INFINITY)) flags |= F_BAD_TEMP;
+        if (!(T >= 0.f) || !(T < INFINITY)) flags |= F_BAD_TEMP;
+        const bool greedy = (T == 0.f);
+        if (MODE == M_TO) my_y = -1;
         {
-            const bool bad_y = (c.lane < g) && (my_y < 0 || my_y >= A.V);
+            const bool bad_y = MODE == M_RS && (c.lane < g) && (my_y < 0 || my_y >= A.V);
             const bool bad_u = (c.lane <= g) && !(my_u >= 0.f && my_u < 1.f);
             if (__any_sync(FULL, bad_y)) flags |= F_BAD_ID;
             if (__any_sync(FULL, bad_u)) flags |= F_BAD_UNIFORM;
         }
-        const float k = LOG2E / T;
+        const float k = greedy ? 0.f : LOG2E / T;
         int n = 0;          // accepted drafts
-        int tok = -1;       // drawn token (owner warp)
+        int tok = -1;       // drawn token (owner warp; every warp when greedy)
         int owner = 0;      // segment whose warp writes the outputs
+        int reached = 0;    // positions whose decision was taken
         // lanes l < gamma: does this warp's segment hold draft token y_l?
         const int yv_l = my_y / VEC - c.seg_lo;
-        const bool own_l = (c.lane < g) && yv_l >= 0 && yv_l < c.seg_n;
+        const bool own_l = MODE == M_RS && (c.lane < g) && yv_l >= 0 && yv_l < c.seg_n;
         const unsigned own_mask = __ballot_sync(FULL, own_l);
 
         if (flags) {
@@ -652,21 +798,50 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
             int dec = 0;      // next position to decide
             int pushed = -1;  // last position whose record this warp pushed
             int rej = -1;     // rejected position
-            bool fin = false; // decisions over (rejection or error)
+            int rej_y = -1;   // target-only: the draft token rejected there
+            bool fin = false; // decisions over (rejection, error or greedy stop)
             auto decide = [&](int i) {
-                const Norm r = gather_norm(c, i, k, true);
+                ++reached;
+                if (greedy) {
+                    const Greedy r = gather_greedy(c, i);
+                    if (r.bad || r.tidx < 0 || (MODE == M_TO && r.didx < 0)) {
+                        flags |= F_NONFINITE;
+                        fin = true;
+                        return;
+                    }
+                    const int y = MODE == M_RS ? __shfl_sync(FULL, my_y, i) : r.didx;
+                    if (MODE == M_TO && c.lane == i) my_y = y;
+                    if (y == r.tidx) {
+                        ++n;
+                        ++dec;
+                        c.c_conf = dec;
+                    } else {
+                        tok = r.tidx;
+                        fin = true;
+                    }
+                    return;
+                }
+                const Norm r = gather_norm<MODE>(c, i, k, true);
                 if (r.rf) {
                     flags |= r.rf;
                     fin = true;
                     return;
                 }
                 const float ui = __shfl_sync(FULL, my_u, i);
-                if (log2f(ui) + fmaf(r.Zdy, k, -r.cd) < fmaf(r.Zty, k, -r.ct)) {
+                bool acc;
+                if (MODE == M_RS) {
+                    acc = log2f(ui) + fmaf(r.Zdy, k, -r.cd) < fmaf(r.Zty, k, -r.ct);
+                } else {
+                    if (c.lane == i) my_y = r.yhat;
+                    acc = log2f(ui) < fmaf(r.Zty, k, -r.ct);
+                }
+                if (acc) {
                     ++n;
                     ++dec;
                     c.c_conf = dec;
                 } else {
                     rej = i;
+                    rej_y = r.yhat;
                     fin = true;
                 }
             };
@@ -677,12 +852,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 }
                 if (fin || c.dead) break;
                 const bool has_d = p < g;
-                const int y = __shfl_sync(FULL, my_y, has_d ? p : 0);
-                const bool owns_y = has_d && ((own_mask >> p) & 1u);
+                const bool use_d = has_d && !(greedy && MODE == M_RS);  // a greedy RS draft row is never read
+                const int y = MODE == M_RS ? __shfl_sync(FULL, my_y, has_d ? p : 0) : 0;
+                const bool owns_y = MODE == M_RS && has_d && !greedy && ((own_mask >> p) & 1u);
                 const int yv = y / VEC - c.seg_lo;
                 // ---- stream the segment of rows (t_p, d_p)
                 float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
-                float zty = 0.f, zdy = 0.f;
+                float zty = 0.f, zdy = 0.f;  // RS: logits at y; TO: zty = target logit at the draft arg max
+                int tix = -1, dix = -1;      // running arg max indices (greedy target, greedy / TO draft)
                 int bad = 0;
                 for (int ch = 0; ch < c.nch; ++ch) {
                     // a decision may already be out: stop streaming a position
@@ -691,7 +868,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         decide(dec);
                         if (fin) break;
                     }
-                    produce<Tin>(A, c);
+                    produce<Tin, MODE>(A, c);
                     if (c.pcount == c.ccount) c.dead = true;  // nothing issued: never wait on it
                     if (c.dead || !slot_wait(c)) break;
                     const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
@@ -700,18 +877,26 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     uint4 rt[QV], rd[QV];
                     if (cnt == CV) {
                         load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
-                        if (has_d) load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
+                        if (use_d) load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
                     } else {
                         load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
-                        if (has_d) load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
+                        if (use_d) load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
                     }
                     // the maxima consume every loaded register: the slot's
                     // reads are complete before it is handed back
                     const float cmt = chunk_max<Tin, QV>(rt);
-                    const float cmd = has_d ? chunk_max<Tin, QV>(rd) : 0.f;
+                    const float cmd = use_d ? chunk_max<Tin, QV>(rd) : 0.f;
                     __syncwarp();
                     consumed(c);  // the slot refills while this chunk is reduced
-                    produce<Tin>(A, c);
+                    produce<Tin, MODE>(A, c);
+                    const int vbase = c.seg_lo + ch * CV + c.lane;
+                    if (greedy) {
+                        bad |= !(cmt < INFINITY) || (use_d && !(cmd < INFINITY));
+                        float dummy = 0.f;
+                        argmax_regs<Tin, QV, false>(rt, rt, cmt, vbase, mt, tix, dummy);
+                        if (use_d) argmax_regs<Tin, QV, false>(rd, rd, cmd, vbase, md, dix, dummy);
+                        continue;
+                    }
                     if (owns_y && yv >= ch * CV && yv < ch * CV + cnt) {
                         const int jv = yv - ch * CV, q = jv >> 5, e = y % VEC;
                         uint4 vt = rt[0], vd = rd[0];
@@ -726,7 +911,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         zdy = __shfl_sync(FULL, vec_elem<Tin>(vd, e), jv & 31);
                     }
                     const float csum = fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
-                    if (has_d) fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
+                    if (has_d) {
+                        if (MODE == M_RS) {
+                            fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
+                        } else {
+                            bad |= !(cmd < INFINITY);
+                            argmax_regs<Tin, QV, true>(rd, rt, cmd, vbase, md, dix, zty);
+                        }
+                    }
                     if (!has_d) {  // per-chunk record of row gamma for the bonus draw
                         Soft a;
                         a.m = mt;
@@ -740,20 +932,34 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     }
                 }
                 if (c.dead || fin) break;  // fin: position p abandoned, its round gets a zero record
-                // ---- warp record -> every CTA of the cluster
-                Soft a;
-                a.m = mt;
-                a.s = st;
-                a.s1 = 0.f;
-                const Soft wt = soft_warp_allreduce<false>(a, k);
-                a.m = md;
-                a.s = sd;
-                const Soft wd = soft_warp_allreduce<false>(a, k);
+                // ---- warp records -> every CTA of the cluster
                 const bool wbad = warp_allor(bad) != 0;
-                xpush(sh, c, p, make_float4(wt.m, wbad ? NAN : wt.s, wd.m, wbad ? NAN : wd.s), owns_y,
-                      make_float4(zty, zdy, 0.f, 0.f));
+                if (greedy) {
+                    float dummy = 0.f;
+                    argmax_allreduce(mt, tix, dummy);
+                    argmax_allreduce(md, dix, dummy);
+                    xpush(sh, c, p, make_float4(mt, __int_as_float(tix), md, __int_as_float(dix)),
+                          make_float4(wbad ? 1.f : 0.f, 0.f, 0.f, 0.f));
+                } else {
+                    Soft a;
+                    a.m = mt;
+                    a.s = st;
+                    a.s1 = 0.f;
+                    const Soft wt = soft_warp_allreduce<false>(a, k);
+                    if (MODE == M_RS) {
+                        a.m = md;
+                        a.s = sd;
+                        const Soft wd = soft_warp_allreduce<false>(a, k);
+                        xpush(sh, c, p, make_float4(wt.m, wbad ? NAN : wt.s, wd.m, wbad ? NAN : wd.s),
+                              make_float4(zty, zdy, owns_y ? 1.f : 0.f, 0.f));
+                    } else {
+                        argmax_allreduce(md, dix, zty);
+                        xpush(sh, c, p, make_float4(wt.m, wbad ? NAN : wt.s, md, zty),
+                              make_float4(__int_as_float(dix), 0.f, 0.f, 0.f));
+                    }
+                }
                 pushed = p;
-                produce<Tin>(A, c);
+                produce<Tin, MODE>(A, c);
                 // decisions whose rounds are already complete
                 while (!fin && dec < g && dec <= p && xtest(sh, c, dec)) decide(dec);
             }
@@ -763,13 +969,25 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
             }
             // zero records for the rounds this warp did not fill
             if (!c.dead)
-                for (int p = pushed + 1; p <= g; ++p) xpush(sh, c, p, ZERO4, p < g && ((own_mask >> p) & 1u), ZERO4);
+                for (int p = pushed + 1; p <= g; ++p) xpush(sh, c, p, ZERO4, ZERO4);
             if (c.dead) {
                 flags |= F_TIMEOUT;
-            } else if (flags & ERR_BITS) {
-                xpush(sh, c, g + 1, ZERO4, false, ZERO4);
+            } else if ((flags & ERR_BITS) || (greedy && fin)) {
+                xpush(sh, c, g + 1, ZERO4, ZERO4);
+            } else if (greedy) {
+                // ---- greedy bonus: the arg max of row gamma
+                xpush(sh, c, g + 1, ZERO4, ZERO4);
+                if (xwait(sh, c, g)) {
+                    ++reached;
+                    const Greedy r = gather_greedy(c, g);
+                    if (r.bad || r.tidx < 0) flags |= F_NONFINITE;
+                    else tok = r.tidx;
+                } else {
+                    flags |= F_TIMEOUT;
+                }
             } else if (rej >= 0) {
-                // ---- rejection at rej: residual pass over rows (t_rej, d_rej)
+                // ---- rejection at rej: residual pass over rows (t_rej, d_rej);
+                // target-only: over t_rej with the rejected token excluded
                 drain(c);
                 c.p_ord = ord;
                 c.p_i = rej;
@@ -777,10 +995,11 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 c.p_c = 0;
                 c.p_done = (c.nch == 0);
                 c.c_conf = g;  // the path is fixed: the producer may move on after the pass
-                const Norm r = gather_norm(c, rej, k, true);
+                const Norm r = gather_norm<MODE>(c, rej, k, true);
+                const int ex_v = MODE == M_TO ? rej_y / VEC - c.seg_lo : -1;  // excluded vector in the segment
                 float Rw = 0.f;
                 for (int ch = 0; ch < c.nch; ++ch) {
-                    produce<Tin>(A, c);
+                    produce<Tin, MODE>(A, c);
                     if (c.pcount == c.ccount) c.dead = true;
                     if (c.dead || !slot_wait(c)) break;
                     const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
@@ -789,20 +1008,31 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     uint4 rt[QV], rd[QV];
                     if (cnt == CV) {
                         load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
+                        if (MODE == M_RS) load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
                     } else {
                         load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
-                        load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
+                        if (MODE == M_RS) load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
                     }
-                    const float ps = warp_allsum(res_regs<Tin, QV>(rt, rd, k, r.ct, r.cd));
+                    float ps;
+                    if (MODE == M_RS) {
+                        ps = warp_allsum(res_regs<Tin, QV>(rt, rd, k, r.ct, r.cd));
+                    } else {
+                        if (ex_v >= ch * CV && ex_v < ch * CV + cnt && ((ex_v - ch * CV) & 31) == c.lane) {
+                            const int q = (ex_v - ch * CV) >> 5;
+#pragma unroll
+                            for (int qq = 0; qq < QV; ++qq)
+                                if (qq == q) vec_set_neginf<Tin>(rt[qq], rej_y % VEC);
+                        }
+                        ps = warp_allsum(psum_regs<Tin, QV>(rt, k, r.ct));
+                    }
                     __syncwarp();
                     consumed(c);
-                    produce<Tin>(A, c);
+                    produce<Tin, MODE>(A, c);
                     if (c.lane == 0) c.ws->cs[ch] = ps;
                     Rw += ps;
                 }
                 if (!c.dead) {
-                    xpush(sh, c, g + 1, make_float4(Rw, 0.f, 0.f, 0.f), false, ZERO4);
+                    xpush(sh, c, g + 1, make_float4(Rw, 0.f, 0.f, 0.f), ZERO4);
                     xwait(sh, c, g + 1);
                 }
                 if (c.dead) {
@@ -817,10 +1047,15 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     const int sel = pick_segment(t0, t1, uf, rem, last);
                     if (sel >= 0) {
                         owner = sel;
-                        if (sel == c.sg)
-                            tok = walk_segment<Tin, true, QV>(seg_of(c), row_base<Tin>(A, true, b, rej),
-                                                          row_base<Tin>(A, false, b, rej), false, 0.f, k, r.ct, r.cd,
-                                                          rem, last);
+                        if (sel == c.sg) {
+                            if (MODE == M_RS)
+                                tok = walk_segment<Tin, true, QV>(seg_of(c), row_base<Tin>(A, true, b, rej),
+                                                                  row_base<Tin>(A, false, b, rej), false, 0.f, k, r.ct,
+                                                                  r.cd, rem, last, -1);
+                            else
+                                tok = walk_segment<Tin, false, QV>(seg_of(c), row_base<Tin>(A, true, b, rej), nullptr,
+                                                                   false, 0.f, k, r.ct, 0.f, rem, last, rej_y);
+                        }
                     } else {
                         // residual mass rounded to zero: draw from p_rej
                         flags |= F_ZERO_MASS;
@@ -834,16 +1069,16 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             if (sp == c.sg) {
                                 direct_chunk_sums<Tin>(seg_of(c), row_base<Tin>(A, true, b, rej), k, r.Mt);
                                 tok = walk_segment<Tin, false, QV>(seg_of(c), row_base<Tin>(A, true, b, rej), nullptr,
-                                                               true, r.Mt, k, r.Mt * k, 0.f, rem, last);
+                                                                   true, r.Mt, k, r.Mt * k, 0.f, rem, last, -1);
                             }
                         }
                     }
                 }
             } else {
                 // ---- bonus: all gamma drafts accepted, draw from p_gamma
-                xpush(sh, c, g + 1, ZERO4, false, ZERO4);
+                xpush(sh, c, g + 1, ZERO4, ZERO4);
                 if (xwait(sh, c, g)) {
-                    const Norm r = gather_norm(c, g, k, false);
+                    const Norm r = gather_norm<MODE>(c, g, k, false);
                     if (r.rf) {
                         flags |= r.rf;
                     } else {
@@ -858,16 +1093,17 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         } else {
                             owner = sp;
                             if (sp == c.sg)
-                                tok = walk_segment<Tin, false, QV>(seg_of(c), row_base<Tin>(A, true, b, g), nullptr, true,
-                                                               r.Mt, k, r.Mt * k, 0.f, rem, last);
+                                tok = walk_segment<Tin, false, QV>(seg_of(c), row_base<Tin>(A, true, b, g), nullptr,
+                                                                   true, r.Mt, k, r.Mt * k, 0.f, rem, last, -1);
                         }
                     }
                 } else {
                     flags |= F_TIMEOUT;
                 }
             }
-            if (flags & ERR_BITS) {
-                // drop the look-ahead; the next sequence starts from its first row
+            if ((flags & ERR_BITS) || (greedy && fin)) {
+                // drop the look-ahead (rows past an error or a greedy stop);
+                // the next sequence starts from its first row
                 drain(c);
                 redirect_next(c, ord, A.B);
             }
@@ -875,14 +1111,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
             if (c.warp == 0 && !c.dead) {
                 for (int i = 0; i < c.Q; ++i) {
                     if (!xwait(sh, c, i)) break;
-                    if (c.lane == 0) mbar_arrive_expect_tx(smem_addr(&sh.xbar[c.bank][i]), round_bytes(c, i));
+                    if (c.lane == 0) mbar_arrive_expect_tx(smem_addr(&sh.xbar[c.bank][i]), round_bytes(c));
                 }
                 __syncwarp();
             }
             c.bpar ^= 1u << c.bank;
             c.bank ^= 1;
         }
-        if (flags & ERR_BITS) owner = 0;
+        if ((flags & ERR_BITS) || greedy) owner = 0;
         if (tok < 0 && !(flags & ERR_BITS) && c.sg == owner) flags |= F_NONFINITE;
         // ---- outputs, written by the owning warp
         if (c.sg == owner || (c.dead && c.sg == 0)) {
@@ -892,12 +1128,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 if (!err) v = (c.lane < n) ? my_y : (c.lane == n ? tok : -1);
                 A.tokens[static_cast<size_t>(b) * (g + 1) + c.lane] = v;
             }
+            if (MODE == M_TO && A.yhat && c.lane < g)
+                A.yhat[static_cast<size_t>(b) * g + c.lane] = (!err && c.lane < reached) ? my_y : -1;
             if (c.lane == 0) {
                 A.accept_len[b] = err ? -1 : n;
                 if (A.flags) A.flags[b] = flags;
             }
         }
-        produce<Tin>(A, c);
+        produce<Tin, MODE>(A, c);
     }
 
     drain(c);
@@ -916,12 +1154,15 @@ int stream_max_segments() { return MAXS; }
 int stream_max_ring() { return MAXR; }
 int stream_max_gamma() { return MAXG; }
 
-const void *stream_kernel(int dtype, int cv) {
+const void *stream_kernel(int dtype, int cv, int mode) {
+    if (mode == 1)  // target-only: 2 KB chunks (the arg max keeps two rows of registers live)
+        return dtype == 0 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_TO>)
+                          : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_TO>);
     if (dtype == 0)
-        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192>)
-                         : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128>);
-    return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192>)
-                     : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128>);
+        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_RS>)
+                         : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_RS>);
+    return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_RS>)
+                     : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_RS>);
 }
 
 }  // namespace mtp

@@ -179,6 +179,79 @@ def test_verify_output_law_chi_square():
     assert chi2 < 24.3, (chi2, counts, B * p)  # 0.999 quantile, 7 dof
 
 
+# --------------------------------------------- greedy and target-only ------
+
+def _check_to_verify(x, what=""):
+    import mtp_speculative_decoding_row_gb300 as mtp
+    out = mtp.mtp_to_verify(to_dev(x.target), to_dev(x.draft), to_dev(x.temperature), to_dev(x.uniforms))
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out._asdict().items()}
+    o = oracle.to_verify(x.target, x.draft, x.temperature, x.uniforms)
+    rep = compare.verify_report(g["tokens"], g["accept_len"], g["row_flags"], o, o["yhat"], x.gamma, x.V, x.dtype)
+    compare.assert_ok(rep, what)
+    exact = (g["accept_len"] == o["accept_len"]) & np.all(g["tokens"] == o["tokens"], axis=1)
+    np.testing.assert_array_equal(g["draft_tokens"][exact], o["yhat"][exact])
+    return rep, g, o
+
+
+TO_SWEEP = [
+    # (V, dtype, gamma, C, clusters)
+    (1024, "f32", 3, None, None),
+    (4096, "bf16", 5, 4, None),
+    (40000, "bf16", 3, 8, None),
+    (40000, "f32", 8, 16, None),
+    (40000, "f32", 8, 4, 2),
+    (151936, "bf16", 3, None, None),
+]
+
+
+@pytest.mark.parametrize("V,dtype,gamma,C,clusters", TO_SWEEP)
+def test_to_verify(V, dtype, gamma, C, clusters):
+    """Target-only verification: arg max drafts, u < p(y), residual p without
+    y; a quarter of the rows greedy (T = 0), mixed with sampled rows on the
+    same cluster."""
+    B = 32
+    x = W.verify_inputs(f"to{V}", B, gamma, V, dtype, 3000 + V + gamma, family="sigma",
+                        sigmas=np.linspace(0.5, 6.0, B), delta=np.linspace(0.0, 1.5, B),
+                        temperature=np.where(np.arange(B) % 4 == 3, 0.0, np.linspace(0.6, 1.3, B)))
+    with env(MTP_RS_CLUSTER=C, MTP_RS_MAX_CLUSTERS=clusters):
+        rep, g, o = _check_to_verify(x, f"to V={V} {dtype} gamma={gamma} C={C} clusters={clusters}")
+    n = g["accept_len"]
+    assert (n > 0).any() and (n < gamma).any()
+
+
+def test_to_verify_full_config():
+    x = W.config("verify64")
+    rep, g, o = _check_to_verify(x, "to verify64")
+    assert rep["exact"] + rep["near_margin"] == x.B
+
+
+@pytest.mark.parametrize("V,dtype,gamma,kernel,clusters", [(30000, "bf16", 3, None, None),
+                                                           (4096, "f32", 5, "resident", None),
+                                                           (4097, "bf16", 3, None, None),
+                                                           (2048, "bf16", 12, None, None),
+                                                           (40000, "f32", 8, None, 2),
+                                                           (30000, "bf16", 5, "resident", 3)])
+def test_greedy_rs_verify(V, dtype, gamma, kernel, clusters):
+    """T = 0 rows of mtp_rs_verify are greedy: accept while the draft is the
+    target's arg max (streaming kernel, cluster-resident kernel, unaligned
+    rows, gamma > 8, and greedy stops followed by more sequences on the same
+    cluster, whose look-ahead rows must be dropped)."""
+    B = 24
+    x = W.verify_inputs(f"greedy{V}", B, gamma, V, dtype, 3100 + V, family="sigma", sigmas=np.linspace(1, 5, B),
+                        delta=np.linspace(0.0, 0.8, B), temperature=np.where(np.arange(B) % 2 == 0, 0.0, 1.0))
+    # half of the greedy rows draft the target's arg max at every position
+    tgt = W.bf16_bits_to_f32(x.target) if dtype == "bf16" else x.target
+    am = tgt[:, :gamma].argmax(-1).astype(np.int32)
+    x.draft_ids[::4] = am[::4]
+    with env(MTP_RS_VERIFY_KERNEL=kernel, MTP_RS_MAX_CLUSTERS=clusters):
+        rep, g, o = _check_verify(x, False, f"greedy V={V} gamma={gamma} kernel={kernel} clusters={clusters}")
+    greedy = x.temperature == 0
+    assert np.all(g["accept_len"][::4] == gamma)
+    assert rep["exact"] == B
+    np.testing.assert_array_equal(g["tokens"][greedy], o["tokens"][greedy])
+
+
 # ------------------------------------------------------------- stats -------
 
 @pytest.mark.parametrize("V,dtype,gamma,C", [(1024, "f32", 3, None), (4097, "bf16", 5, 8), (151936, "bf16", 3, None),
@@ -207,7 +280,7 @@ def test_row_stats_deep_config():
 
 def test_flags_and_defined_outputs():
     x = W.verify_inputs("flags", 8, 3, 3000, "f32", 31, family="sigma", sigmas=2.0, delta=0.3)
-    x.temperature[1] = 0.0
+    x.temperature[1] = -1.0  # 0 is greedy decoding; a negative temperature is invalid
     x.draft_ids[2, 1] = 3000
     x.uniforms[3, 2] = 1.0
     x.target[4, 0, 17] = np.nan

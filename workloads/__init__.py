@@ -184,12 +184,16 @@ def verify_inputs(
         zt = _widen(target[b, :gamma], dtype)
         nz = philox(200 + c, b).standard_normal((gamma, V), dtype=np.float32)
         draft[b] = _round(zt + np.float32(delta[b]) * nz, dtype)
-        # Draft-stage sample y ~ softmax(draft / T) by Gumbel-max (float64).
-        dz = _widen(draft[b], dtype).astype(np.float64) / float(temp[b])
+        # Draft-stage sample y ~ softmax(draft / T) by Gumbel-max (float64);
+        # at T = 0 (greedy) the draft's arg max.
         u = philox(300 + c, b).random((gamma, V))
-        with np.errstate(divide="ignore"):
-            gum = -np.log(-np.log(u))
-        ids[b] = np.argmax(dz + gum, axis=1).astype(np.int32)
+        if temp[b] > 0:
+            dz = _widen(draft[b], dtype).astype(np.float64) / float(temp[b])
+            with np.errstate(divide="ignore"):
+                gum = -np.log(-np.log(u))
+            ids[b] = np.argmax(dz + gum, axis=1).astype(np.int32)
+        else:
+            ids[b] = np.argmax(_widen(draft[b], dtype), axis=1).astype(np.int32)
 
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(one, range(B)))
