@@ -17,7 +17,7 @@ metric through the public API with pinned host buffers: host-to-device copy
 of the step's inputs, the call, and the device-to-host copy of its outputs.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
-       [--workloads verify64,rl512,deep256,tvloss]
+       [--workloads verify64,rl512,deep256,stats256,diag256,tvloss]
 Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -168,6 +168,10 @@ def alg_bytes_verify(accept_len: np.ndarray, gamma: int, V: int, es: int, stats:
     return int(((n + 1) + np.minimum(n + 1, gamma)).sum()) * V * es
 
 
+# Row-statistics workloads on the deep-speculation inputs: (input config, call).
+STATS_WORKLOADS = {"stats256": ("deep256", "stats"), "diag256": ("deep256", "diag")}
+
+
 class VerifyWorkload:
     def __init__(self, name: str, device, copies: int):
         import torch
@@ -176,10 +180,11 @@ class VerifyWorkload:
         import mtp_speculative_decoding_row_gb300 as mtp
 
         self.mtp = mtp
-        self.x = x = W.config(name)
+        base_name, self.kind = STATS_WORKLOADS.get(name, (name, "verify"))
+        self.x = x = W.config(base_name)
         self.name, self.device = name, device
         self.B, self.gamma, self.V, self.es = x.B, x.gamma, x.V, x.esize
-        self.stats = x.want_stats
+        self.stats = x.want_stats or self.kind != "verify"
 
         def up(a):
             if a.dtype == np.uint16:
@@ -195,12 +200,24 @@ class VerifyWorkload:
 
     def call(self, i: int, stream=None):
         t, d, ids, T, u = self.inputs[i % self.copies]
-        self.outs[i % self.copies] = self.mtp.mtp_rs_verify(t, d, ids, T, u, with_stats=self.stats,
-                                                            out=self.outs[i % self.copies], stream=stream)
+        o = self.outs[i % self.copies]
+        if self.kind == "stats":
+            o = self.mtp.mtp_row_stats(t, d, T, out=o, stream=stream)
+        elif self.kind == "diag":
+            o = self.mtp.mtp_rs_diagnostics(t, d, T, out=o, stream=stream)
+        else:
+            o = self.mtp.mtp_rs_verify(t, d, ids, T, u, with_stats=self.stats, out=o, stream=stream)
+        self.outs[i % self.copies] = o
 
     def alg_bytes(self) -> int:
+        if self.kind != "verify":
+            return self.bytes_full
         n = self.outs[0].accept_len.cpu().numpy()
         return alg_bytes_verify(n, self.gamma, self.V, self.es, self.stats)
+
+    def plan_op(self) -> str:
+        return {"stats": "row_stats", "diag": "diagnostics"}.get(self.kind,
+                                                                  "verify_stats" if self.stats else "verify")
 
     def describe(self) -> str:
         x = self.x
@@ -209,7 +226,11 @@ class VerifyWorkload:
                 "rl512": "RL rollout verify: B=512 gamma=3 V=151936 bf16, peaked Zipf(1.1)+8 rows, 30% N(0,1) rows, "
                          "delta in {0.1,0.5}, T in {0.6,1.0}",
                 "deep256": "deep speculation + stats: B=256 gamma=7 V=151936 fp32, T in {0.6,0.8,1.0}, delta 0..1, "
-                           "alpha and H for every position"}[x.name]
+                           "alpha and H for every position",
+                "stats256": "row statistics (alpha, H(p)) without decisions on the deep256 inputs: B=256 gamma=7 "
+                            "V=151936 fp32",
+                "diag256": "acceptance diagnostics (alpha, H(p), H(q), KL(q||p), arg max draft, p(yhat), "
+                           "rs_better) on the deep256 inputs: B=256 gamma=7 V=151936 fp32"}[self.name]
 
 
 class TVWorkload:
@@ -410,7 +431,7 @@ def run_cuda(args, world, rank, local, pg):
         alg = wl.alg_bytes()
         per_launch_s = t["ms_total"] / 1e3 / t["launches"]
         achieved = alg / per_launch_s / 1e9
-        plan = mtp.mtp_query_plan("tv_loss" if name == "tvloss" else ("verify_stats" if wl.stats else "verify"),
+        plan = mtp.mtp_query_plan("tv_loss" if name == "tvloss" else wl.plan_op(),
                                   "bf16" if wl.es == 2 else "f32", wl.N if name == "tvloss" else wl.B, wl.gamma, wl.V)
         r = {
             "workload": wl.describe(),
@@ -473,7 +494,8 @@ def run_cuda(args, world, rank, local, pg):
 
 
 def VerifyWorkloadBytes(name: str) -> int:
-    return {"verify64": 64 * 7 * 151936 * 2, "rl512": 512 * 7 * 151936 * 2, "deep256": 256 * 15 * 151936 * 4}[name]
+    return {"verify64": 64 * 7 * 151936 * 2, "rl512": 512 * 7 * 151936 * 2, "deep256": 256 * 15 * 151936 * 4,
+            "stats256": 256 * 15 * 151936 * 4, "diag256": 256 * 15 * 151936 * 4}[name]
 
 
 def main():
@@ -482,7 +504,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workloads", default="verify64,rl512,deep256,tvloss")
+    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,tvloss")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")

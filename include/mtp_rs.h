@@ -151,10 +151,47 @@ int mtp_to_verify(const void *target_logits, const void *draft_logits, mtp_dtype
  *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V], temperature [B]
  *   alpha [B, gamma] float32 (required), entropy [B, gamma+1] float32
  *   (required), row_flags [B] int32 or NULL.
+ * Runs on the cluster-resident kernel; with MTP_RS_STATS_KERNEL=stream (and
+ * aligned rows, gamma <= 8) on the streaming kernel of mtp_rs_diagnostics.
  */
 int mtp_row_stats(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
                   const float *temperature, int B, int gamma, int V,
                   float *alpha, float *entropy, int32_t *row_flags, mtp_stream_t stream);
+
+/*
+ * mtp_rs_diagnostics -- per-position acceptance diagnostics without
+ * decisions [BB §2 "Acceptance methods", §8 "Robustness of acceptance
+ * methods", App. E "Rejection Sampling Decision Boundary Derivation"].
+ *
+ * For sequence b and draft position i < gamma, with p = softmax(target[b,i]
+ * / T_b) and q = softmax(draft[b,i] / T_b):
+ *   alpha[b,i]     = sum_v min(p_v, q_v) = 1 - d_TV(p, q)
+ *   ent_q[b,i]     = H(q) in nats
+ *   kl[b,i]        = D_KL(q || p) = sum_v q_v ln(q_v / p_v) in nats (rounding
+ *                    below 0 is clamped to 0; +inf where some p_v = 0 < q_v)
+ *   yhat[b,i]      = arg max_v draft[b,i,v], ties to the smallest index
+ *                    (the token target-only acceptance proposes)
+ *   p_yhat[b,i]    = p(yhat), the target-only acceptance probability
+ *   rs_better[b,i] = 1 if d_TV(p, q) < 1 - p(yhat), else 0: rejection
+ *                    sampling then accepts more often than target-only
+ *                    acceptance (evaluated as p(yhat) < alpha)
+ * and for i <= gamma ent_p[b,i] = H(p_i) in nats.
+ *
+ *   target_logits [B, gamma+1, V] dtype, draft_logits [B, gamma, V] dtype,
+ *   temperature [B] float32 (T_b > 0; otherwise, T = 0 included, the row is
+ *   flagged MTP_ROW_BAD_TEMP: these statistics need T > 0).
+ *   Outputs, each float32 / int32 in the layout above or NULL (not written):
+ *   alpha, ent_p, ent_q, kl, yhat, p_yhat, rs_better; row_flags [B].
+ *   A flagged row gets NaN in its float outputs and -1 in yhat and
+ *   rs_better.
+ * Requirements: 1 <= gamma <= 8 (else MTP_ERR_INVALID_ARG); 16-byte aligned
+ * logit bases and V a multiple of 16 / esize (else MTP_ERR_MISALIGNED).
+ * Every row is read twice: once from HBM, once more shortly after (L2).
+ */
+int mtp_rs_diagnostics(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                       const float *temperature, int B, int gamma, int V, float *alpha, float *ent_p,
+                       float *ent_q, float *kl, int32_t *yhat, float *p_yhat, int32_t *rs_better,
+                       int32_t *row_flags, mtp_stream_t stream);
 
 /*
  * mtp_tv_loss_fwd_bwd -- fused forward and backward of the end-to-end TV
@@ -186,7 +223,9 @@ int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp
  * (diagnostics; launches nothing).  op: 0 = mtp_rs_verify, 1 = mtp_rs_verify
  * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd, 4 =
  * mtp_rs_verify forced onto the cluster-resident kernel, 5 =
- * mtp_tv_loss_fwd_bwd forced onto the cluster-resident kernel.  units = B
+ * mtp_tv_loss_fwd_bwd forced onto the cluster-resident kernel, 6 =
+ * mtp_rs_diagnostics, 7 = mtp_row_stats forced onto the cluster-resident
+ * kernel.  units = B
  * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
  * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory

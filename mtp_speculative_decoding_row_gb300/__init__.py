@@ -19,9 +19,9 @@ from typing import NamedTuple, Optional
 from . import build as _build
 
 __all__ = [
-    "mtp_rs_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string", "MTPError",
-    "load_library",
-    "VerifyResult", "StatsResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID", "ROW_BAD_TEMP",
+    "mtp_rs_verify", "mtp_to_verify", "mtp_row_stats", "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd",
+    "mtp_query_plan", "mtp_status_string", "MTPError", "load_library",
+    "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID", "ROW_BAD_TEMP",
     "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
 ]
 
@@ -29,10 +29,10 @@ ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM, ROW_TIM
 ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_TIMEOUT
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_row_stats", "mtp_tv_loss_fwd_bwd", "mtp_query_plan",
-                    "mtp_status_string")
+EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_row_stats", "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd",
+                    "mtp_query_plan", "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
-            "tv_loss_resident": 5}
+            "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7}
 
 _lib = None
 
@@ -65,6 +65,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_to_verify.restype = I
     lib.mtp_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
     lib.mtp_row_stats.restype = I
+    lib.mtp_rs_diagnostics.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P, P]
+    lib.mtp_rs_diagnostics.restype = I
     lib.mtp_tv_loss_fwd_bwd.argtypes = [P, P, I, F, I, I, I, F, P, P, P, P, P]
     lib.mtp_tv_loss_fwd_bwd.restype = I
     lib.mtp_query_plan.argtypes = [I, I, I, I, I, P, P, P, P]
@@ -154,6 +156,17 @@ class StatsResult(NamedTuple):
     row_flags: "object"
 
 
+class DiagResult(NamedTuple):
+    alpha: "object"      # [B, gamma] float32: sum min(p, q) = 1 - d_TV
+    ent_p: "object"      # [B, gamma+1] float32: H(p) in nats
+    ent_q: "object"      # [B, gamma] float32: H(q) in nats
+    kl: "object"         # [B, gamma] float32: D_KL(q || p) in nats
+    yhat: "object"       # [B, gamma] int32: arg max of the draft logits
+    p_yhat: "object"     # [B, gamma] float32: p(yhat)
+    rs_better: "object"  # [B, gamma] int32: 1 if d_TV < 1 - p(yhat)
+    row_flags: "object"  # [B] int32
+
+
 class TVLossResult(NamedTuple):
     loss: "object"        # [N] float32
     alpha: "object"       # [N, gamma] float32
@@ -240,6 +253,32 @@ def mtp_row_stats(target_logits, draft_logits, temperature, *, out: Optional[Sta
         _ptr(out.alpha), _ptr(out.entropy), _ptr(out.row_flags), _stream(dev, stream))
     if rc:
         raise MTPError("mtp_row_stats", rc)
+    return out
+
+
+def mtp_rs_diagnostics(target_logits, draft_logits, temperature, *, out: Optional[DiagResult] = None,
+                       stream=None) -> DiagResult:
+    """Per-position acceptance diagnostics (no decisions): alpha, H(p), H(q),
+    D_KL(q || p), the arg max draft token, its target probability and the
+    rejection-sampling-better test d_TV < 1 - p(yhat)."""
+    torch = _torch()
+    dev = target_logits.device
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    _check(target_logits, "target_logits", dev)
+    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
+    _check(temperature, "temperature", dev, torch.float32, (B,))
+    if out is None:
+        f = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)  # noqa: E731
+        i = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)  # noqa: E731
+        out = DiagResult(f(B, gamma), f(B, g1), f(B, gamma), f(B, gamma), i(B, gamma), f(B, gamma), i(B, gamma),
+                         i(B))
+    rc = load_library().mtp_rs_diagnostics(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(temperature), B, gamma, V,
+        _ptr(out.alpha), _ptr(out.ent_p), _ptr(out.ent_q), _ptr(out.kl), _ptr(out.yhat), _ptr(out.p_yhat),
+        _ptr(out.rs_better), _ptr(out.row_flags), _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_rs_diagnostics", rc)
     return out
 
 

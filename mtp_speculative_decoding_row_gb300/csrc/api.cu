@@ -391,6 +391,101 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
     return launch(func, p, &A, stream);
 }
 
+// Streaming row-pair statistics kernel (diagnostics; row statistics on
+// request): clusters of C CTAs x NT/32 warps, one vocabulary segment per
+// warp, one sequence per cluster at a time.  Same rule as the streaming TV
+// kernel: the most warps in flight, within 5 % the larger cluster;
+// MTP_RS_PAIR_L2MB caps the sequences in flight by the bytes of the row
+// pairs they re-read.  Measured on GB300 at B = 256, gamma = 7, V = 151,936
+// fp32, the cluster-resident kernel (one load per row, the second pass from
+// shared memory) computes the row statistics faster than this kernel, whose
+// second pass re-reads rows that L2 no longer holds; mtp_row_stats therefore
+// uses it only when MTP_RS_STATS_KERNEL=stream.
+bool pairs_usable(int V, int es, int gamma) {
+    return gamma <= pair_max_gamma() && V % (16 / es) == 0;
+}
+
+bool stats_streamed() {
+    const char *e = std::getenv("MTP_RS_STATS_KERNEL");
+    return e && e[0] == 's';  // "stream"
+}
+
+bool plan_pairs(int dev, int dtype, int V, int es, int gamma, int units, int mode, Plan &p) {
+    const int forced = env_cluster();
+    int R = env_int("MTP_RS_RING");
+    if (R < 2 || R > pair_max_ring()) R = 2;
+    const int l2mb = env_int("MTP_RS_PAIR_L2MB");
+    const double seq_bytes = 2.0 * static_cast<double>(V) * es;  // the row pair a sequence re-reads next
+    int cap_l2 = l2mb > 0 ? static_cast<int>((static_cast<double>(l2mb) * 1048576.0) / seq_bytes) : 1 << 30;
+    if (cap_l2 < 1) cap_l2 = 1;
+    const uint32_t cap = smem_optin(dev);
+    const int nw = pair_threads() / 32;
+    const int nv = V / (16 / es);
+    long best = -1;
+    bool found = false;
+    for (int C = 1; C <= MAX_C; C *= 2) {
+        if (forced && C != forced) continue;
+        const int S = C * nw;
+        if (S > pair_max_segments()) continue;
+        const int nvs = (nv + S - 1) / S;
+        const int cv = mode == PAIR_DIAG ? 128 : stream_chunk_for(nvs);
+        const uint32_t smem = pair_hdr_bytes() + pair_rec_bytes(gamma, S, mode) +
+                              static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
+        if (smem > cap) continue;
+        const void *func = pair_kernel(dtype, cv, mode);
+        if (prepare_func(dev, func) != cudaSuccess) return false;
+        const int nc = max_clusters(dev, func, C, smem, pair_threads());
+        if (nc <= 0) continue;
+        int used = nc < units ? nc : units;
+        if (used > cap_l2) used = cap_l2;
+        const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
+        if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+        const long warps = static_cast<long>(used) * C * nw;
+        if (!found || warps * 20 > best * 21 || (warps * 21 >= best * 20 && C > p.C)) {
+            if (warps > best) best = warps;
+            p = Plan{};
+            p.C = C;
+            p.smem = smem;
+            p.clusters = used;
+            p.threads = pair_threads();
+            p.ring = R;
+            p.seg_vectors = nvs;
+            p.cv = cv;
+            p.func = func;
+            found = true;
+        }
+    }
+    return found;
+}
+
+int pair_call(int mode, const void *target, const void *draft, mtp_dtype dtype, const float *temp, int B,
+              int gamma, int V, float *alpha, float *ent_p, float *ent_q, float *kl, int32_t *yhat, float *p_yhat,
+              int32_t *rs_better, int32_t *flags, mtp_stream_t stream) {
+    int dev;
+    if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    const int es = esize(dtype);
+    Plan p;
+    if (!plan_pairs(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, gamma, B, mode, p)) return MTP_ERR_NO_DEVICE;
+    PairArgs A = {};
+    A.target = target;
+    A.draft = draft;
+    A.temp = temp;
+    A.B = B;
+    A.gamma = gamma;
+    A.V = V;
+    A.ring = p.ring;
+    A.seg_vectors = p.seg_vectors;
+    A.alpha = alpha;
+    A.ent_p = ent_p;
+    A.ent_q = ent_q;
+    A.kl = kl;
+    A.yhat = yhat;
+    A.p_yhat = p_yhat;
+    A.rs_better = rs_better;
+    A.flags = flags;
+    return launch(p.func, p, &A, stream);
+}
+
 }  // namespace
 
 extern "C" int mtp_rs_verify(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
@@ -448,8 +543,27 @@ extern "C" int mtp_row_stats(const void *target_logits, const void *draft_logits
                              const float *temperature, int B, int gamma, int V, float *alpha, float *entropy,
                              int32_t *row_flags, mtp_stream_t stream) {
     if (B > 0 && (!alpha || !entropy)) return MTP_ERR_INVALID_ARG;
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (B > 0 && gamma >= 1 && V >= 1 && target_logits && draft_logits && temperature && aligned16(target_logits) &&
+        aligned16(draft_logits) && stats_streamed() && pairs_usable(V, esize(dtype), gamma))
+        return pair_call(PAIR_STATS, target_logits, draft_logits, dtype, temperature, B, gamma, V, alpha, entropy,
+                         nullptr, nullptr, nullptr, nullptr, nullptr, row_flags, stream);
     return row_call(MODE_STATS, target_logits, draft_logits, dtype, nullptr, temperature, nullptr, B, gamma, V,
                     nullptr, nullptr, alpha, entropy, row_flags, stream);
+}
+
+extern "C" int mtp_rs_diagnostics(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                                  const float *temperature, int B, int gamma, int V, float *alpha, float *ent_p,
+                                  float *ent_q, float *kl, int32_t *yhat, float *p_yhat, int32_t *rs_better,
+                                  int32_t *row_flags, mtp_stream_t stream) {
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || gamma < 1 || gamma > pair_max_gamma() || V < 1) return MTP_ERR_INVALID_ARG;
+    if (B == 0) return MTP_OK;
+    if (!target_logits || !draft_logits || !temperature) return MTP_ERR_INVALID_ARG;
+    const int es = esize(dtype);
+    if (!aligned16(target_logits) || !aligned16(draft_logits) || V % (16 / es) != 0) return MTP_ERR_MISALIGNED;
+    return pair_call(PAIR_DIAG, target_logits, draft_logits, dtype, temperature, B, gamma, V, alpha, ent_p, ent_q,
+                     kl, yhat, p_yhat, rs_better, row_flags, stream);
 }
 
 extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
@@ -497,7 +611,7 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
                               int *clusters, int *smem_bytes, int *resident_drafts) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
-    if (op < 0 || op > 5 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (op < 0 || op > 7 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
@@ -506,6 +620,12 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     bool ok = false, streamed = false;
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
     if (op == 3 && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
+    if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
+    if (op == 6) {
+        if (gamma > pair_max_gamma() || V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
+        ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_DIAG, p);
+        if (!ok) return MTP_ERR_NO_DEVICE;
+    }
     if (!ok) {
         const int mode = (op == 0 || op == 4) ? MODE_VERIFY : op == 1 ? MODE_VERIFY_STATS : MODE_STATS;
         const bool tv = op == 3 || op == 5;

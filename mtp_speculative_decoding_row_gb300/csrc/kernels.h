@@ -47,6 +47,26 @@ struct TVArgs {
     int32_t *flags;         // [N] or null
 };
 
+// Modes of the streaming row-pair statistics kernel.
+enum PairMode { PAIR_STATS = 0, PAIR_DIAG = 1 };
+
+struct PairArgs {
+    const void *target;  // [B, gamma+1, V]
+    const void *draft;   // [B, gamma, V]
+    const float *temp;   // [B]
+    int B, gamma, V;
+    int ring;            // chunk slots per warp
+    int seg_vectors;     // 16-byte vectors per warp segment
+    float *alpha;        // [B, gamma] or null
+    float *ent_p;        // [B, gamma+1] or null
+    float *ent_q;        // [B, gamma] or null   (diagnostics)
+    float *kl;           // [B, gamma] or null   (diagnostics)
+    int32_t *yhat;       // [B, gamma] or null   (diagnostics)
+    float *p_yhat;       // [B, gamma] or null   (diagnostics)
+    int32_t *rs_better;  // [B, gamma] or null   (diagnostics)
+    int32_t *flags;      // [B] or null
+};
+
 // Shared-memory header bytes in front of the slice buffers of each kernel.
 uint32_t row_hdr_bytes();
 uint32_t tv_hdr_bytes();
@@ -70,6 +90,14 @@ const void *row_kernel(int dtype, int mode);
 const void *stream_kernel(int dtype, int cv, int mode);
 const void *tv_kernel(int dtype);
 const void *tvs_kernel(int dtype, int cv);  // streaming TV kernel, cv: 128 or 192
+// Streaming row-pair statistics kernel (mode: PairMode), cv: 128 or 192.
+const void *pair_kernel(int dtype, int cv, int mode);
+uint32_t pair_hdr_bytes();
+uint32_t pair_rec_bytes(int gamma, int S, int mode);
+int pair_threads();
+int pair_max_gamma();
+int pair_max_segments();
+int pair_max_ring();
 
 // Streaming TV kernel geometry.
 uint32_t tvs_hdr_bytes();

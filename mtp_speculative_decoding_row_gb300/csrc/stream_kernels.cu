@@ -623,31 +623,6 @@ __device__ __forceinline__ Greedy gather_greedy(const Ctx &c, int i) {
     return r;
 }
 
-// Running arg max of one chunk row held by this lane (first index among
-// equals in ascending vocabulary order; cmx: the lane's chunk maximum from
-// chunk_max).  vbase: vocabulary index of this lane's first vector in the
-// chunk (vector q sits 32 q vectors further).  With `other`, x receives the
-// other row's logit at the new arg max.
-template <typename Tin, int QV, bool OTHER>
-__device__ __forceinline__ void argmax_regs(const uint4 (&r)[QV], const uint4 (&o)[QV], float cmx, int vbase,
-                                            float &m, int &idx, float &x) {
-    constexpr int VEC = Store<Tin>::VEC;
-    if (!(cmx > m) || !(cmx < INFINITY)) return;  // no improvement (or a NaN / +inf row, flagged elsewhere)
-    bool found = false;
-#pragma unroll
-    for (int q = 0; q < QV; ++q) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            if (!found && vec_elem<Tin>(r[q], e) == cmx) {
-                found = true;
-                idx = (vbase + q * 32) * VEC + e;
-                if (OTHER) x = vec_elem<Tin>(o[q], e);
-            }
-        }
-    }
-    m = cmx;
-}
-
 // Element e of a 16-byte logit vector set to -inf (probability 0).
 template <typename Tin>
 __device__ __forceinline__ void vec_set_neginf(uint4 &v, int e) {

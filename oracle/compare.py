@@ -92,6 +92,54 @@ def stats_report(alpha, entropy, orc: dict, dtype: str, flags=None) -> dict:
     return out
 
 
+def diag_report(g: dict, orc: dict, dtype: str, logit_scale=None) -> dict:
+    """Compare acceptance diagnostics.  Floats within the dtype's relative
+    tolerance; the KL divergence is a difference of log-normalisers and
+    weighted logit means, so its absolute tolerance also grows with the
+    position's logit magnitude |z| / T (logit_scale [B, gamma]); yhat exact;
+    rs_better exact except where the oracle's |d_TV - (1 - p(yhat))| is
+    below MARGIN (counted as near-margin)."""
+    rt = rtol_for(dtype)
+    rep = {"B": int(orc["flags"].shape[0]), "near_margin": 0, "bad": []}
+    if not np.array_equal(g["row_flags"], orc["flags"]):
+        rep["bad"].append(("flags", int((g["row_flags"] != orc["flags"]).sum())))
+    good = (orc["flags"] & ERROR_BITS) == 0
+    for key in ("alpha", "ent_p", "ent_q", "p_yhat"):
+        a = g[key][good].astype(np.float64)
+        o = orc[key][good]
+        e = np.abs(a - o)
+        rep[key + "_max_abs"] = float(e.max()) if e.size else 0.0
+        if np.any(~(e <= rt * np.abs(o) + ATOL)):
+            rep["bad"].append((key, int((~(e <= rt * np.abs(o) + ATOL)).sum())))
+    a = g["kl"][good].astype(np.float64)
+    o = orc["kl"][good]
+    fin = np.isfinite(o)
+    if not np.array_equal(np.isfinite(a), fin) or np.any(a[~fin] != o[~fin]):
+        rep["bad"].append(("kl infinities", int((np.isfinite(a) != fin).sum())))
+    sc = np.zeros_like(o) if logit_scale is None else np.asarray(logit_scale, np.float64)[good]
+    tol = rt * np.abs(o) + ATOL + 4e-7 * (1.0 + sc)
+    e = np.where(fin, np.abs(np.where(fin, a, 0.0) - np.where(fin, o, 0.0)), 0.0)
+    rep["kl_max_abs"] = float(e[fin].max()) if fin.any() else 0.0
+    if np.any(~(e[fin] <= tol[fin])):
+        rep["bad"].append(("kl", int((~(e[fin] <= tol[fin])).sum())))
+    if not np.array_equal(g["yhat"][good], orc["yhat"][good]):
+        rep["bad"].append(("yhat", int((g["yhat"][good] != orc["yhat"][good]).sum())))
+    near = orc["boundary_margin"][good] < MARGIN
+    rep["near_margin"] = int(near.sum())
+    diff = (g["rs_better"][good] != orc["rs_better"][good]) & ~near
+    if diff.any():
+        rep["bad"].append(("rs_better", int(diff.sum())))
+    bad_rows = ~good
+    if bad_rows.any():
+        for key in ("alpha", "ent_p", "ent_q", "kl", "p_yhat"):
+            if not np.all(np.isnan(g[key][bad_rows])):
+                rep["bad"].append((key + " of flagged rows not NaN", 1))
+        for key in ("yhat", "rs_better"):
+            if not np.all(g[key][bad_rows] == -1):
+                rep["bad"].append((key + " of flagged rows not -1", 1))
+    return rep
+
+
 def tv_report(loss, alpha, grad, flags, orc: dict, dtype: str, target_f64=None, draft_f64=None,
               temperature: float = 1.0) -> dict:
     """Compare TV-loss outputs.  Rows (t, k) whose oracle log-ratio

@@ -254,12 +254,21 @@ def test_greedy_rs_verify(V, dtype, gamma, kernel, clusters):
 
 # ------------------------------------------------------------- stats -------
 
-@pytest.mark.parametrize("V,dtype,gamma,C", [(1024, "f32", 3, None), (4097, "bf16", 5, 8), (151936, "bf16", 3, None),
-                                             (30001, "f32", 2, 16)])
-def test_row_stats(V, dtype, gamma, C):
+@pytest.mark.parametrize("V,dtype,gamma,C,kernel", [(1024, "f32", 3, None, None), (4097, "bf16", 5, 8, None),
+                                                    (151936, "bf16", 3, None, None), (30001, "f32", 2, 16, None),
+                                                    (40000, "bf16", 10, None, None),
+                                                    (1024, "f32", 3, None, "stream"), (40000, "f32", 7, 4, "stream"),
+                                                    (40000, "bf16", 8, 16, "stream"), (64, "f32", 3, 16, "stream"),
+                                                    (151936, "bf16", 3, None, "stream"),
+                                                    (4097, "bf16", 5, 8, "stream")])
+def test_row_stats(V, dtype, gamma, C, kernel):
+    """Row statistics on the cluster-resident kernel (the default) and on the
+    streaming row-pair kernel when asked for (aligned rows, gamma <= 8, else
+    the resident kernel; V = 64 over 64 segments leaves most warps without
+    vocabulary)."""
     x = W.verify_inputs("stats", 12, gamma, V, dtype, 2000 + V, family="sigma", sigmas=np.linspace(0.3, 9, 12),
                         delta=np.linspace(0, 1.5, 12), temperature=np.linspace(0.6, 1.4, 12))
-    with env(MTP_RS_CLUSTER=C):
+    with env(MTP_RS_CLUSTER=C, MTP_RS_STATS_KERNEL=kernel):
         g = run_stats(x)
     o = oracle.row_stats(x.target, x.draft, x.temperature)
     rep = compare.stats_report(g["alpha"], g["entropy"], o, dtype, g["row_flags"])
@@ -274,6 +283,91 @@ def test_row_stats_deep_config():
     compare.assert_ok(rep, "deep256 stats")
     # alpha = 1 - TV against the oracle's independent TV
     np.testing.assert_allclose(g["alpha"], 1 - o["tv"], rtol=0, atol=1e-5)
+
+
+# ------------------------------------------------------- diagnostics -------
+
+def _logit_scale(x):
+    t = W.bf16_bits_to_f32(x.target) if x.dtype == "bf16" else x.target
+    d = W.bf16_bits_to_f32(x.draft) if x.dtype == "bf16" else x.draft
+    T = np.where(x.temperature > 0, x.temperature, 1.0)[:, None]
+    with np.errstate(invalid="ignore"):
+        mt = np.nanmax(np.where(np.isfinite(t), np.abs(t), 0.0), axis=-1)[:, :x.gamma]
+        md = np.nanmax(np.where(np.isfinite(d), np.abs(d), 0.0), axis=-1)
+    return np.maximum(mt, md) / T
+
+
+def _check_diag(x, what=""):
+    import mtp_speculative_decoding_row_gb300 as mtp
+    out = mtp.mtp_rs_diagnostics(to_dev(x.target), to_dev(x.draft), to_dev(x.temperature))
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out._asdict().items()}
+    o = oracle.diagnostics(x.target, x.draft, x.temperature)
+    rep = compare.diag_report(g, o, x.dtype, _logit_scale(x))
+    if rep["bad"]:
+        raise AssertionError(f"{what} diagnostics parity failed: {rep}")
+    return rep, g, o
+
+
+DIAG_SWEEP = [
+    # (V, dtype, gamma, C)
+    (1024, "f32", 3, None),
+    (4096, "bf16", 5, 4),
+    (40000, "f32", 8, 16),
+    (40000, "bf16", 7, 2),
+    (30000, "f32", 2, 1),
+    (64, "f32", 3, 16),
+    (151936, "bf16", 3, None),
+]
+
+
+@pytest.mark.parametrize("V,dtype,gamma,C", DIAG_SWEEP)
+def test_diagnostics(V, dtype, gamma, C):
+    """alpha, H(p), H(q), KL(q || p), arg max draft, p(yhat) and the
+    rejection-sampling-better test against the oracle; delta = 0 rows have
+    q == p (alpha = 1, KL = 0); T = 0 and T < 0 rows are flagged."""
+    B = 24
+    T = np.linspace(0.5, 1.5, B).astype(np.float32)
+    T[5] = 0.0
+    T[11] = -1.0
+    x = W.verify_inputs(f"diag{V}", B, gamma, V, dtype, 4000 + V + gamma, family="sigma",
+                        sigmas=np.linspace(0.3, 8.0, B), delta=np.linspace(0.0, 1.5, B), temperature=T)
+    with env(MTP_RS_CLUSTER=C):
+        rep, g, o = _check_diag(x, f"V={V} {dtype} gamma={gamma} C={C}")
+    good = o["flags"] == 0
+    assert good.sum() == B - 2
+    np.testing.assert_array_equal(g["row_flags"][[5, 11]], [4, 4])
+    # both outcomes of the boundary test occur
+    assert (o["rs_better"][good] == 1).any() and (o["rs_better"][good] == 0).any()
+    # q == p: alpha 1 and KL 0
+    np.testing.assert_allclose(g["alpha"][0], 1.0, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(g["kl"][0], 0.0, rtol=0, atol=2e-6)
+
+
+def test_diagnostics_masked_and_bad_logits():
+    """-inf logits (masked vocabulary): p = 0 < q gives KL = inf, both -inf
+    adds nothing; a NaN logit flags the row."""
+    B, gamma, V = 6, 3, 8192
+    x = W.verify_inputs("diagmask", B, gamma, V, "f32", 4100, family="sigma", sigmas=np.linspace(1, 4, B),
+                        delta=0.4)
+    x.target[0, 1, 100:300] = -np.inf          # p = 0 where q > 0: KL infinite
+    x.target[1, :, 7000:] = -np.inf            # both masked: finite statistics
+    x.draft[1, :, 7000:] = -np.inf
+    x.target[2, 3, 5] = np.nan                 # H(p_gamma) row: flagged
+    x.draft[3, 0, 17] = np.nan
+    x.draft[4, 2, :] = -np.inf                 # all -inf draft row: flagged
+    rep, g, o = _check_diag(x, "masked")
+    assert np.isinf(o["kl"][0, 1]) and np.isinf(g["kl"][0, 1])
+    assert np.all(np.isfinite(g["kl"][1]))
+    np.testing.assert_array_equal(o["flags"][[2, 3, 4]], [1, 1, 1])
+
+
+def test_diagnostics_full_config():
+    """The deep256 workload (B = 256, gamma = 7, V = 151936, f32)."""
+    x = W.config("deep256")
+    rep, g, o = _check_diag(x, "deep256")
+    # positions within 1e-5 of the boundary (an oracle-only count) stay rare
+    assert rep["near_margin"] <= 0.05 * x.B * x.gamma
 
 
 # ------------------------------------------------------------ flags --------
