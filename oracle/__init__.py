@@ -52,6 +52,10 @@ def _load():
             lib.oracle_tv_loss.argtypes = [P, P, I, D, I, I, I, D, I, P, P, P, P, P, P]
             lib.oracle_to_verify.argtypes = [P, P, I, P, P, I, I, I, P, P, P, P, P, P]
             lib.oracle_diagnostics.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P, P, P]
+            U32 = ctypes.c_uint32
+            lib.oracle_philox4x32_10.argtypes = [P, P, P]
+            lib.oracle_gumbel_noise.argtypes = [U32, U32, U32, U32, I, I, I, P]
+            lib.oracle_gumbel_verify.argtypes = [P, P, I, P, P, P, U32, U32, U32, I, I, I, P, P, P, P, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_softmax, lib.oracle_verify, lib.oracle_row_stats, lib.oracle_tv_loss,
                       lib.oracle_num_threads):
@@ -153,6 +157,59 @@ def to_verify(target, draft, temperature, uniforms) -> dict:
                                   _ptr(out["acc_margin"]), _ptr(out["cdf_margin"]))
     if rc:
         raise RuntimeError(f"oracle_to_verify failed ({rc})")
+    return out
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox4x32-10 of one 4-word counter under a 2-word key (uint32)."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32).reshape(4)
+    k = np.ascontiguousarray(key, dtype=np.uint32).reshape(2)
+    out = np.empty(4, np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def _seed_words(seed: int):
+    seed = int(seed) & ((1 << 64) - 1)
+    return seed & 0xFFFFFFFF, seed >> 32
+
+
+def gumbel_noise(seed: int, offset: int, b: int, i: int, v0: int, n: int) -> np.ndarray:
+    """Standard Gumbel noise G_v, v = v0 .. v0+n-1, of row i of sequence b."""
+    lo, hi = _seed_words(seed)
+    out = np.empty(n, np.float64)
+    _load().oracle_gumbel_noise(lo, hi, int(offset) & 0xFFFFFFFF, int(b), int(i), int(v0), int(n), _ptr(out))
+    return out
+
+
+def gumbel_verify(target, draft, draft_ids, temperature, uniforms, seed: int, offset: int = 0) -> dict:
+    """Batched verify whose final token (residual or bonus) is a Gumbel-max
+    draw with Philox noise keyed by (seed, offset, sequence, row).  Returns
+    tokens [B, gamma+1], accept_len [B], flags [B], acc_margin [B, gamma],
+    gumbel_margin [B] (best minus second best key of the final draw)."""
+    t, dt = _logits(target)
+    d, dt2 = _logits(draft)
+    assert dt == dt2
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    assert d.shape == (B, gamma, V)
+    ids = np.ascontiguousarray(draft_ids, dtype=np.int32).reshape(B, gamma)
+    temp = np.ascontiguousarray(temperature, dtype=np.float64).reshape(B)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, gamma + 1)
+    lo, hi = _seed_words(seed)
+    out = {
+        "tokens": np.empty((B, gamma + 1), np.int32),
+        "accept_len": np.empty(B, np.int32),
+        "flags": np.empty(B, np.int32),
+        "acc_margin": np.empty((B, gamma), np.float64),
+        "gumbel_margin": np.empty(B, np.float64),
+    }
+    rc = _load().oracle_gumbel_verify(_ptr(t), _ptr(d), dt, _ptr(ids), _ptr(temp), _ptr(u), lo, hi,
+                                      int(offset) & 0xFFFFFFFF, B, gamma, V, _ptr(out["tokens"]),
+                                      _ptr(out["accept_len"]), _ptr(out["flags"]), _ptr(out["acc_margin"]),
+                                      _ptr(out["gumbel_margin"]))
+    if rc:
+        raise RuntimeError(f"oracle_gumbel_verify failed ({rc})")
     return out
 
 

@@ -39,6 +39,16 @@
  *     logits (ties to the smallest index), accepted iff u < p(y); at the
  *     first rejection the replacement is drawn from p with y removed, i.e.
  *     the residual of rejection sampling with a one-hot draft.
+ *   - Gumbel-max final draw ([BB] App. G.2): the acceptance chain is the
+ *     same; the residual (or bonus) token is arg max_v [ln w_v + G_v] over
+ *     the v with w_v > 0, G_v = -ln(-ln U_v) standard Gumbel noise.  U_v
+ *     comes from the counter-based generator Philox4x32-10 (Salmon, Moraes,
+ *     Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011)
+ *     with key (seed_lo, seed_hi) and counter (v / 4, i, b, offset), word
+ *     v mod 4, where b is the sequence and i the row drawn from (the
+ *     rejected position, or gamma for the bonus): U_v = (floor(x / 2^8) +
+ *     1/2) / 2^24, exact in single precision and strictly inside (0, 1).
+ *     u[b, gamma] is not used.
  *
  * Logit storage codes: 0 = float32, 1 = bfloat16 (uint16 bit patterns),
  * 2 = float64.  Every element is widened exactly to double before use.
@@ -220,11 +230,104 @@ static int cdf_draw(const double *r, int V, double u, double *margin)
  * With want_stats, alpha_i, TV_i (i < gamma) and H_i (i <= gamma) are formed
  * for every position, including positions after the stop.
  */
+/*
+ * Philox4x32-10 [Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011]: ten rounds of the Philox S-box on a 4 x 32-bit
+ * counter.  A round multiplies counter words 0 and 2 by the two round
+ * multipliers (full 64-bit products), and forms the new counter (hi(M1 c2)
+ * ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key is bumped
+ * by the two Weyl constants between rounds.
+ */
+static void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)M0 * c0, p1 = (uint64_t)M1 * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+int oracle_philox4x32_10(const uint32_t *ctr, const uint32_t *key, uint32_t *out)
+{
+    philox4x32_10(ctr, key, out);
+    return 0;
+}
+
+/* Key and counter words of one Gumbel stream (one sequence). */
+struct gumbel_ctx {
+    uint32_t seed_lo, seed_hi, offset, b;
+};
+
+/* U_v in (0, 1) for vocabulary index v of row i (see the header). */
+static double gumbel_uniform(const struct gumbel_ctx *g, int i, int v)
+{
+    const uint32_t ctr[4] = {(uint32_t)v >> 2, (uint32_t)i, g->b, g->offset};
+    const uint32_t key[2] = {g->seed_lo, g->seed_hi};
+    uint32_t x[4];
+    philox4x32_10(ctr, key, x);
+    return ((double)(x[v & 3] >> 8) + 0.5) / 16777216.0;
+}
+
+/* Standard Gumbel noise G = -ln(-ln U). */
+static double gumbel_noise(const struct gumbel_ctx *g, int i, int v)
+{
+    return -log(-log(gumbel_uniform(g, i, v)));
+}
+
+int oracle_gumbel_noise(uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, uint32_t b, int i, int v0, int n,
+                        double *out)
+{
+    const struct gumbel_ctx g = {seed_lo, seed_hi, offset, b};
+    for (int j = 0; j < n; ++j) out[j] = gumbel_noise(&g, i, v0 + j);
+    return 0;
+}
+
+/*
+ * Gumbel-max draw from the unnormalised weights w[0..V-1] of row i [BB, App.
+ * G.2]: arg max over w_v > 0 of ln w_v + G_v (-1 if every weight is 0).
+ * *margin receives the gap between the best and the second best key (+inf
+ * with a single candidate): the decision is exact unless rounding of the
+ * keys exceeds it.
+ */
+static int gumbel_draw(const double *w, int V, const struct gumbel_ctx *g, int i, double *margin)
+{
+    double best = -INFINITY, second = -INFINITY;
+    int arg = -1;
+    for (int v = 0; v < V; ++v) {
+        if (!(w[v] > 0.0)) continue;
+        const double key = log(w[v]) + gumbel_noise(g, i, v);
+        if (arg < 0 || key > best) {
+            second = best;
+            best = key;
+            arg = v;
+        } else if (key > second) {
+            second = key;
+        }
+    }
+    *margin = arg < 0 ? 0.0 : best - second;
+    return arg;
+}
+
 static void verify_one(const void *target, const void *draft, int dtype, size_t toff, size_t doff,
                        const int32_t *ids, double T, const double *u, int gamma, int V, int want_stats,
                        int32_t *tokens, int32_t *accept_len, double *alpha, double *tv, double *ent,
                        int32_t *flags, double *acc_margin, double *cdf_margin, double *p, double *q,
-                       double *r)
+                       double *r, const struct gumbel_ctx *gumbel)
 {
     int f = 0;
     for (int i = 0; i <= gamma; ++i) tokens[i] = -1;
@@ -237,7 +340,7 @@ static void verify_one(const void *target, const void *draft, int dtype, size_t 
     if (!(T >= 0.0) || isinf(T) || (T == 0.0 && want_stats)) f |= OR_ROW_BAD_TEMP;
     for (int i = 0; i < gamma; ++i)
         if (ids[i] < 0 || ids[i] >= V) f |= OR_ROW_BAD_ID;
-    for (int i = 0; i <= gamma; ++i)
+    for (int i = 0; i < gamma + (gumbel ? 0 : 1); ++i)  /* the Gumbel draw uses no u[gamma] */
         if (!(u[i] >= 0.0 && u[i] < 1.0)) f |= OR_ROW_BAD_UNIFORM;
     if (f) {
         *accept_len = -1;
@@ -340,7 +443,7 @@ static void verify_one(const void *target, const void *draft, int dtype, size_t 
         }
         memcpy(r, p, sizeof(double) * (size_t)V);
     }
-    tokens[n] = cdf_draw(r, V, u[gamma], cdf_margin);
+    tokens[n] = gumbel ? gumbel_draw(r, V, gumbel, n, cdf_margin) : cdf_draw(r, V, u[gamma], cdf_margin);
     *accept_len = n;
     *flags = f;
 }
@@ -373,7 +476,40 @@ int oracle_verify(const void *target, const void *draft, int dtype, const int32_
                    temp[b], u + (size_t)b * (gamma + 1), gamma, V, want_stats, tokens + (size_t)b * (gamma + 1),
                    accept_len + b, want_stats ? alpha + (size_t)b * gamma : NULL,
                    want_stats ? tv + (size_t)b * gamma : NULL, want_stats ? ent + (size_t)b * (gamma + 1) : NULL,
-                   flags + b, acc_margin + (size_t)b * gamma, cdf_margin + b, buf, buf + V, buf + 2 * (size_t)V);
+                   flags + b, acc_margin + (size_t)b * gamma, cdf_margin + b, buf, buf + V, buf + 2 * (size_t)V,
+                   NULL);
+        free(buf);
+    }
+    return fail ? 2 : 0;
+}
+
+/*
+ * Batched verify with the Gumbel-max final draw [BB, App. G.2]: the
+ * acceptance chain of oracle_verify, then the residual (or bonus) token by
+ * gumbel_draw with the stream (seed, offset, b).  u [B, gamma+1]: only
+ * u[b, 0..gamma-1] are used.  gumbel_margin [B] receives the gap between the
+ * best and second best key of the final draw (+inf for greedy rows).
+ */
+int oracle_gumbel_verify(const void *target, const void *draft, int dtype, const int32_t *ids, const double *temp,
+                         const double *u, uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, int B, int gamma,
+                         int V, int32_t *tokens, int32_t *accept_len, int32_t *flags, double *acc_margin,
+                         double *gumbel_margin)
+{
+    if (B < 0 || gamma < 1 || V < 1) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)V * 3);
+        if (!buf) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        const struct gumbel_ctx g = {seed_lo, seed_hi, offset, (uint32_t)b};
+        verify_one(target, draft, dtype, (size_t)b * (gamma + 1) * V, (size_t)b * gamma * V, ids + (size_t)b * gamma,
+                   temp[b], u + (size_t)b * (gamma + 1), gamma, V, 0, tokens + (size_t)b * (gamma + 1),
+                   accept_len + b, NULL, NULL, NULL, flags + b, acc_margin + (size_t)b * gamma, gumbel_margin + b,
+                   buf, buf + V, buf + 2 * (size_t)V, &g);
         free(buf);
     }
     return fail ? 2 : 0;

@@ -557,3 +557,112 @@ def test_decision_boundary_matches_enumerated_acceptance():
         assert dg["rs_better"][0, 0] == int(p_rs > p_to), trial
         seen.add(int(p_rs > p_to))
     assert seen == {0, 1}
+
+
+# ------------------------------------------------ Gumbel-max final draw ----
+
+def _kat(name):
+    rows = []
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(w, 16) for w in line.split()])
+    return rows
+
+
+def test_philox_known_answers():
+    """The oracle's Philox4x32-10 reproduces the generator's published
+    known-answer vectors (tests/golden/philox4x32_10_kat.txt)."""
+    rows = _kat("philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for r in rows:
+        out = oracle.philox4x32_10(r[0:4], r[4:6])
+        assert [int(x) for x in out] == r[6:10]
+
+
+def test_gumbel_noise_is_standard_gumbel():
+    """G_v = -ln(-ln U_v) from the Philox stream is standard Gumbel: a
+    Kolmogorov-Smirnov test against the library Gumbel law, the mean (Euler's
+    constant) and the variance (pi^2 / 6); distinct rows, sequences, offsets
+    and seeds give distinct streams."""
+    g = np.concatenate([oracle.gumbel_noise(7, 0, b, i, 0, 4000) for b in range(5) for i in range(5)])
+    assert scipy.stats.kstest(g, scipy.stats.gumbel_r.cdf).pvalue > 1e-3
+    assert abs(g.mean() - np.euler_gamma) < 0.02
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.05
+    a = oracle.gumbel_noise(7, 0, 0, 0, 0, 64)
+    for other in (oracle.gumbel_noise(7, 0, 1, 0, 0, 64), oracle.gumbel_noise(7, 0, 0, 1, 0, 64),
+                  oracle.gumbel_noise(7, 1, 0, 0, 0, 64), oracle.gumbel_noise(8, 0, 0, 0, 0, 64),
+                  oracle.gumbel_noise(7 + (1 << 32), 0, 0, 0, 0, 64)):
+        assert not np.any(a == other)
+    # word v mod 4 of counter v / 4: v = 0..3 share one counter
+    np.testing.assert_array_equal(oracle.gumbel_noise(7, 0, 0, 0, 2, 6), a[2:8])
+
+
+def _chi2_ok(counts, probs, q=0.999):
+    keep = probs > 0
+    assert counts[~keep].sum() == 0
+    n = counts.sum()
+    e = n * probs[keep]
+    chi2 = ((counts[keep] - e) ** 2 / e).sum()
+    return chi2 < scipy.stats.chi2.ppf(q, keep.sum() - 1), chi2
+
+
+def test_gumbel_final_draw_law():
+    """The Gumbel-max final draw (summary App. G.2) samples the residual
+    norm(max(0, p - q)) at a certain rejection and p_gamma after gamma
+    accepts: chi-square over 30,000 independent streams (one per sequence)
+    at V = 8, with every accept decision the same."""
+    V, B = 8, 30000
+    rng = np.random.default_rng(31)
+    zt = rng.standard_normal((2, V)) * 1.2
+    zd = rng.standard_normal(V) * 1.2
+    p0, p1 = scipy.special.softmax(zt, axis=1)
+    q0 = scipy.special.softmax(zd)
+    # rejection at position 0: the draft token where q is largest relative to p, u close to 1
+    y = int(np.argmax(q0 / p0))
+    t = np.broadcast_to(zt, (B, 2, V)).copy()
+    d = np.broadcast_to(zd, (B, 1, V)).copy()
+    ids = np.full((B, 1), y, np.int32)
+    u = np.tile([[0.9999, 0.5]], (B, 1))
+    out = oracle.gumbel_verify(t, d, ids, np.ones(B), u, seed=1234, offset=3)
+    assert np.all(out["accept_len"] == 0) and np.all(out["flags"] == 0)
+    r = np.maximum(p0 - q0, 0)
+    ok, chi2 = _chi2_ok(np.bincount(out["tokens"][:, 0], minlength=V), r / r.sum())
+    assert ok, chi2
+    # all accepted (q == p): the bonus token follows p_1
+    d2 = np.broadcast_to(zt[0], (B, 1, V)).copy()
+    out = oracle.gumbel_verify(t, d2, ids, np.ones(B), u, seed=99)
+    assert np.all(out["accept_len"] == 1)
+    ok, chi2 = _chi2_ok(np.bincount(out["tokens"][:, 1], minlength=V), p1)
+    assert ok, chi2
+
+
+def test_gumbel_verify_acceptance_is_the_rejection_sampling_chain():
+    """Only the final draw changes: accept lengths, accepted tokens and flags
+    equal those of the inverse-CDF verify, greedy rows (T = 0) entirely;
+    u[b, gamma] is not examined."""
+    rng = np.random.default_rng(32)
+    B, gamma, V = 64, 4, 200
+    t = rng.standard_normal((B, gamma + 1, V)) * 2
+    d = t[:, :gamma] + rng.standard_normal((B, gamma, V)) * 0.7
+    ids = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    T = np.where(np.arange(B) % 5 == 0, 0.0, rng.uniform(0.6, 1.4, B))
+    u = rng.random((B, gamma + 1))
+    a = oracle.verify(t, d, ids, T, u)
+    u2 = u.copy()
+    u2[:, gamma] = 7.0  # not a valid uniform, and not used by the Gumbel draw
+    g = oracle.gumbel_verify(t, d, ids, T, u2, seed=5)
+    np.testing.assert_array_equal(a["accept_len"], g["accept_len"])
+    np.testing.assert_array_equal(a["flags"], g["flags"])
+    for b in range(B):
+        n = a["accept_len"][b]
+        np.testing.assert_array_equal(a["tokens"][b, :n], g["tokens"][b, :n])
+        if T[b] == 0:
+            np.testing.assert_array_equal(a["tokens"][b], g["tokens"][b])
+    assert (a["accept_len"] < gamma).any() and (a["accept_len"] == gamma).any()
+    # the draw depends on the stream: another seed changes some final tokens
+    g2 = oracle.gumbel_verify(t, d, ids, T, u2, seed=6)
+    fin = np.array([g["tokens"][b, g["accept_len"][b]] for b in range(B)])
+    fin2 = np.array([g2["tokens"][b, g2["accept_len"][b]] for b in range(B)])
+    assert (fin != fin2).any()
