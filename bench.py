@@ -17,7 +17,7 @@ metric through the public API with pinned host buffers: host-to-device copy
 of the step's inputs, the call, and the device-to-host copy of its outputs.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
-       [--workloads verify64,rl512,deep256,stats256,diag256,tvloss]
+       [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss]
 Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -168,8 +168,10 @@ def alg_bytes_verify(accept_len: np.ndarray, gamma: int, V: int, es: int, stats:
     return int(((n + 1) + np.minimum(n + 1, gamma)).sum()) * V * es
 
 
-# Row-statistics workloads on the deep-speculation inputs: (input config, call).
-STATS_WORKLOADS = {"stats256": ("deep256", "stats"), "diag256": ("deep256", "diag")}
+# Workloads that run another call on the inputs of a named configuration:
+# (input config, call).
+STATS_WORKLOADS = {"stats256": ("deep256", "stats"), "diag256": ("deep256", "diag"),
+                   "to64": ("verify64", "to"), "gumbel64": ("verify64", "gumbel")}
 
 
 class VerifyWorkload:
@@ -184,7 +186,7 @@ class VerifyWorkload:
         self.x = x = W.config(base_name)
         self.name, self.device = name, device
         self.B, self.gamma, self.V, self.es = x.B, x.gamma, x.V, x.esize
-        self.stats = x.want_stats or self.kind != "verify"
+        self.stats = x.want_stats or self.kind in ("stats", "diag")
 
         def up(a):
             if a.dtype == np.uint16:
@@ -205,19 +207,23 @@ class VerifyWorkload:
             o = self.mtp.mtp_row_stats(t, d, T, out=o, stream=stream)
         elif self.kind == "diag":
             o = self.mtp.mtp_rs_diagnostics(t, d, T, out=o, stream=stream)
+        elif self.kind == "to":
+            o = self.mtp.mtp_to_verify(t, d, T, u, out=o, stream=stream)
+        elif self.kind == "gumbel":
+            o = self.mtp.mtp_gumbel_verify(t, d, ids, T, u, 1234, i % self.copies, out=o, stream=stream)
         else:
             o = self.mtp.mtp_rs_verify(t, d, ids, T, u, with_stats=self.stats, out=o, stream=stream)
         self.outs[i % self.copies] = o
 
     def alg_bytes(self) -> int:
-        if self.kind != "verify":
+        if self.kind in ("stats", "diag"):
             return self.bytes_full
         n = self.outs[0].accept_len.cpu().numpy()
         return alg_bytes_verify(n, self.gamma, self.V, self.es, self.stats)
 
     def plan_op(self) -> str:
-        return {"stats": "row_stats", "diag": "diagnostics"}.get(self.kind,
-                                                                  "verify_stats" if self.stats else "verify")
+        return {"stats": "row_stats", "diag": "diagnostics", "to": "to_verify", "gumbel": "gumbel_verify"}.get(
+            self.kind, "verify_stats" if self.stats else "verify")
 
     def describe(self) -> str:
         x = self.x
@@ -230,7 +236,10 @@ class VerifyWorkload:
                 "stats256": "row statistics (alpha, H(p)) without decisions on the deep256 inputs: B=256 gamma=7 "
                             "V=151936 fp32",
                 "diag256": "acceptance diagnostics (alpha, H(p), H(q), KL(q||p), arg max draft, p(yhat), "
-                           "rs_better) on the deep256 inputs: B=256 gamma=7 V=151936 fp32"}[self.name]
+                           "rs_better) on the deep256 inputs: B=256 gamma=7 V=151936 fp32",
+                "to64": "target-only verification (arg max drafts, accept iff u < p(yhat)) on the verify64 inputs",
+                "gumbel64": "rejection sampling with the Gumbel-max final draw (in-kernel Philox noise) on the "
+                            "verify64 inputs"}[self.name]
 
 
 class TVWorkload:
@@ -495,7 +504,8 @@ def run_cuda(args, world, rank, local, pg):
 
 def VerifyWorkloadBytes(name: str) -> int:
     return {"verify64": 64 * 7 * 151936 * 2, "rl512": 512 * 7 * 151936 * 2, "deep256": 256 * 15 * 151936 * 4,
-            "stats256": 256 * 15 * 151936 * 4, "diag256": 256 * 15 * 151936 * 4}[name]
+            "stats256": 256 * 15 * 151936 * 4, "diag256": 256 * 15 * 151936 * 4, "to64": 64 * 7 * 151936 * 2,
+            "gumbel64": 64 * 7 * 151936 * 2}[name]
 
 
 def main():
@@ -504,7 +514,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,tvloss")
+    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")

@@ -144,6 +144,35 @@ int mtp_to_verify(const void *target_logits, const void *draft_logits, mtp_dtype
                   mtp_stream_t stream);
 
 /*
+ * mtp_gumbel_verify -- mtp_rs_verify with the Gumbel-max final draw [BB App.
+ * G.2 "Gumbel-Max Trick (vLLM)"]: the acceptance chain is the same (u_i
+ * q_i(y_i) < p_i(y_i), stop at the first rejection, T = 0 greedy); the
+ * replacement at a rejection j is arg max_v [ln r_v + G_v] over r =
+ * max(0, p_j - q_j) (the p_j keys if every r_v rounds to 0, flagged
+ * MTP_ROW_ZERO_MASS), and the bonus after gamma accepts is arg max_v [ln
+ * p_gamma(v) + G_v].  G_v = -ln(-ln U_v) is standard Gumbel noise drawn in
+ * the kernel from Philox4x32-10 (Salmon et al., "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011): key = seed (low 32 bits first), counter =
+ * (v / 4, row, b, offset) with row the position drawn from (j, or gamma for
+ * the bonus) and b the sequence, word v mod 4, U_v = (floor(x / 2^8) + 1/2)
+ * / 2^24.  The same (seed, offset) gives the same tokens; callers advance
+ * offset (or the seed) between calls for fresh noise.
+ *
+ *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V] dtype
+ *   draft_ids [B, gamma] int32, temperature [B] float32 (0 = greedy)
+ *   uniforms [B, gamma+1] float32: u[b, 0..gamma-1] are the accept tests,
+ *     u[b, gamma] is not read
+ *   out_tokens [B, gamma+1], accept_len [B], row_flags [B] or NULL: as for
+ *   mtp_rs_verify.
+ * Requirements: 1 <= gamma <= 8 (else MTP_ERR_INVALID_ARG); 16-byte aligned
+ * logit bases and V a multiple of 16 / esize (else MTP_ERR_MISALIGNED).
+ */
+int mtp_gumbel_verify(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                      const int32_t *draft_ids, const float *temperature, const float *uniforms, uint64_t seed,
+                      uint32_t offset, int B, int gamma, int V, int32_t *out_tokens, int32_t *accept_len,
+                      int32_t *row_flags, mtp_stream_t stream);
+
+/*
  * mtp_row_stats -- per-position overlap and target entropy without
  * decisions [BB §3, §8: alpha = sum_v min(p_v, q_v) = 1 - TV; entropy
  * H(p) = -sum_v p_v log p_v in nats].
@@ -225,12 +254,12 @@ int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp
  * mtp_rs_verify forced onto the cluster-resident kernel, 5 =
  * mtp_tv_loss_fwd_bwd forced onto the cluster-resident kernel, 6 =
  * mtp_rs_diagnostics, 7 = mtp_row_stats forced onto the cluster-resident
- * kernel.  units = B
+ * kernel, 8 = mtp_to_verify, 9 = mtp_gumbel_verify.  units = B
  * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
  * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
  * per CTA), resident_drafts (cluster-resident TV kernel: draft slices kept on
- * chip; op 0: chunk slots per warp of the streaming kernel, 0 when the call
+ * chip; ops 0, 8, 9: chunk slots per warp of the streaming kernel, 0 when the call
  * would use the cluster-resident kernel; else 0).
  * Returns the status the call's planning step would return.
  */

@@ -19,20 +19,21 @@ from typing import NamedTuple, Optional
 from . import build as _build
 
 __all__ = [
-    "mtp_rs_verify", "mtp_to_verify", "mtp_row_stats", "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd",
+    "mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_row_stats", "mtp_rs_diagnostics",
+    "mtp_tv_loss_fwd_bwd",
     "mtp_query_plan", "mtp_status_string", "MTPError", "load_library",
-    "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID", "ROW_BAD_TEMP",
-    "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
+    "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID",
+    "ROW_BAD_TEMP", "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
 ]
 
 ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM, ROW_TIMEOUT = 1, 2, 4, 8, 16, 32
 ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_TIMEOUT
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_row_stats", "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd",
-                    "mtp_query_plan", "mtp_status_string")
+EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_row_stats", "mtp_rs_diagnostics",
+                    "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
-            "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7}
+            "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9}
 
 _lib = None
 
@@ -65,6 +66,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_to_verify.restype = I
     lib.mtp_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
     lib.mtp_row_stats.restype = I
+    lib.mtp_gumbel_verify.argtypes = [P, P, I, P, P, P, ctypes.c_uint64, ctypes.c_uint32, I, I, I, P, P, P, P]
+    lib.mtp_gumbel_verify.restype = I
     lib.mtp_rs_diagnostics.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P, P]
     lib.mtp_rs_diagnostics.restype = I
     lib.mtp_tv_loss_fwd_bwd.argtypes = [P, P, I, F, I, I, I, F, P, P, P, P, P]
@@ -231,6 +234,34 @@ def mtp_to_verify(target_logits, draft_logits, temperature, uniforms, *, out: Op
         _stream(dev, stream))
     if rc:
         raise MTPError("mtp_to_verify", rc)
+    return out
+
+
+def mtp_gumbel_verify(target_logits, draft_logits, draft_ids, temperature, uniforms, seed: int, offset: int = 0, *,
+                      out: Optional[VerifyResult] = None, stream=None) -> VerifyResult:
+    """Rejection-sampling verification whose final token (residual or bonus)
+    is a Gumbel-max draw with in-kernel Philox noise keyed by (seed, offset,
+    sequence, row); u[:, gamma] is not read.  Returns tokens, accept_len and
+    row_flags (alpha and entropy None)."""
+    torch = _torch()
+    dev = target_logits.device
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    _check(target_logits, "target_logits", dev)
+    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
+    _check(draft_ids, "draft_ids", dev, torch.int32, (B, gamma))
+    _check(temperature, "temperature", dev, torch.float32, (B,))
+    _check(uniforms, "uniforms", dev, torch.float32, (B, g1))
+    if out is None:
+        out = VerifyResult(torch.empty((B, g1), dtype=torch.int32, device=dev),
+                           torch.empty((B,), dtype=torch.int32, device=dev), None, None,
+                           torch.empty((B,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_gumbel_verify(
+        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(draft_ids), _ptr(temperature),
+        _ptr(uniforms), int(seed) & ((1 << 64) - 1), int(offset) & 0xFFFFFFFF, B, gamma, V, _ptr(out.tokens),
+        _ptr(out.accept_len), _ptr(out.row_flags), _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_gumbel_verify", rc)
     return out
 
 

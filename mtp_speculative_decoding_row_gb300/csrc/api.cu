@@ -539,6 +539,49 @@ extern "C" int mtp_to_verify(const void *target_logits, const void *draft_logits
     return launch(p.func, p, &A, stream);
 }
 
+extern "C" int mtp_gumbel_verify(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                                 const int32_t *draft_ids, const float *temperature, const float *uniforms,
+                                 uint64_t seed, uint32_t offset, int B, int gamma, int V, int32_t *out_tokens,
+                                 int32_t *accept_len, int32_t *row_flags, mtp_stream_t stream) {
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (B < 0 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (B == 0) return MTP_OK;
+    if (!target_logits || !draft_logits || !draft_ids || !temperature || !uniforms || !out_tokens || !accept_len)
+        return MTP_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return MTP_ERR_MISALIGNED;
+    const int es = esize(dtype);
+    // the streaming kernel serves the Gumbel-max variant: whole 16-byte
+    // vectors per row and gamma up to its limit
+    if (V % (16 / es) != 0) return MTP_ERR_MISALIGNED;
+    if (gamma > stream_max_gamma()) return MTP_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    Plan p;
+    if (!plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, gamma, B, p, 2)) return MTP_ERR_NO_DEVICE;
+    VerifyArgs A = {};
+    A.target = target_logits;
+    A.draft = draft_logits;
+    A.ids = draft_ids;
+    A.temp = temperature;
+    A.unif = uniforms;
+    A.B = B;
+    A.gamma = gamma;
+    A.V = V;
+    A.aligned = 1;
+    A.streams = 1;
+    A.ring = p.ring;
+    A.depth = p.depth;
+    A.seg_vectors = p.seg_vectors;
+    A.tokens = out_tokens;
+    A.accept_len = accept_len;
+    A.flags = row_flags;
+    A.yhat = nullptr;
+    A.seed_lo = static_cast<uint32_t>(seed);
+    A.seed_hi = static_cast<uint32_t>(seed >> 32);
+    A.offset = offset;
+    return launch(p.func, p, &A, stream);
+}
+
 extern "C" int mtp_row_stats(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
                              const float *temperature, int B, int gamma, int V, float *alpha, float *entropy,
                              int32_t *row_flags, mtp_stream_t stream) {
@@ -611,7 +654,7 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
                               int *clusters, int *smem_bytes, int *resident_drafts) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
-    if (op < 0 || op > 7 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (op < 0 || op > 9 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
@@ -621,6 +664,11 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
     if (op == 3 && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
     if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
+    if (op == 8 || op == 9) {  // target-only verify, Gumbel-max verify: streaming kernel only
+        if (gamma > stream_max_gamma() || V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
+        ok = streamed = plan_stream(dev, d, V, es, gamma, units, p, op == 8 ? 1 : 2);
+        if (!ok) return MTP_ERR_NO_DEVICE;
+    }
     if (op == 6) {
         if (gamma > pair_max_gamma() || V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
         ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_DIAG, p);
@@ -634,7 +682,7 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
         ok = tv ? plan_tv(dev, func, V, es, gamma, units, p) : plan_row(dev, func, V, es, units, p);
     }
     if (!ok) return MTP_ERR_NO_DEVICE;
-    if (streamed) p.nres = (op == 0) ? p.ring : 0;
+    if (streamed) p.nres = (op == 0 || op == 8 || op == 9) ? p.ring : 0;
     if (cluster_size) *cluster_size = p.C;
     if (clusters) *clusters = p.clusters;
     if (smem_bytes) *smem_bytes = static_cast<int>(p.smem);

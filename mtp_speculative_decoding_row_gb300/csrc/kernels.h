@@ -29,6 +29,7 @@ struct VerifyArgs {
     float *entropy;         // [B, gamma+1]      (stats modes)
     int32_t *flags;         // [B] or null
     int32_t *yhat;          // [B, gamma] or null (target-only: the arg max draft tokens)
+    uint32_t seed_lo, seed_hi, offset;  // Gumbel-max final draw: noise stream key and counter word
 };
 
 struct TVArgs {
@@ -86,7 +87,8 @@ int stream_max_ring();
 
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);
-// cv: 128 or 192 vectors per chunk; mode 0 = rejection sampling, 1 = target-only
+// cv: 128 or 192 vectors per chunk; mode 0 = rejection sampling, 1 = target-only,
+// 2 = rejection sampling with the Gumbel-max final draw
 const void *stream_kernel(int dtype, int cv, int mode);
 const void *tv_kernel(int dtype);
 const void *tvs_kernel(int dtype, int cv);  // streaming TV kernel, cv: 128 or 192

@@ -46,6 +46,7 @@
 
 #include "chunk_math.cuh"
 #include "common.cuh"
+#include "philox.cuh"
 #include "kernels.h"
 
 namespace mtp {
@@ -83,7 +84,9 @@ __host__ __device__ constexpr uint32_t rec_bytes(int gamma, int S) {
     return ((2u * static_cast<uint32_t>(gamma + 2) * static_cast<uint32_t>(2 * S) * 16u) + 127u) & ~127u;
 }
 
-enum { M_RS = 0, M_TO = 1 };  // rejection sampling / target-only acceptance
+// rejection sampling with an inverse-CDF final draw / target-only acceptance /
+// rejection sampling with a Gumbel-max final draw
+enum { M_RS = 0, M_TO = 1, M_GB = 2 };
 
 constexpr int ERR_BITS = F_NONFINITE | F_BAD_ID | F_BAD_TEMP | F_BAD_UNIFORM | F_TIMEOUT;
 
@@ -536,7 +539,7 @@ __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool h
                 r.m1 = v.x;
                 r.s1 = v.y;
             }
-            if (MODE == M_RS) {
+            if (MODE != M_TO) {
                 if (v.w != 0.f) {  // draft partial of this lane (NaN propagates)
                     if (v.z > dm) {
                         ds = (ds != 0.f ? ds * ex2((dm - v.z) * k) : 0.f) + v.w;
@@ -573,7 +576,7 @@ __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool h
     r.cd = 0.f;
     r.Zty = r.Zdy = 0.f;
     if (has_d) {
-        if (MODE == M_RS) {
+        if (MODE != M_TO) {
             Soft ld;
             ld.m = dm;
             ld.s = ds;
@@ -658,6 +661,110 @@ __device__ __forceinline__ float psum_regs(const uint4 (&rt)[QV], float k, float
     return s0 + s1;
 }
 
+// Bounds of the Gumbel term g = -log2(-log2 U) (log2 units) over the
+// generator's U in [2^-25, 1 - 2^-25]: g <= 24.47 and g >= -log2(25) =
+// -4.64, widened for the approximate logarithms.
+constexpr float GUMBEL2_MAX = 25.5f;
+constexpr float GUMBEL2_MIN = -6.f;
+
+// Gumbel-max keys of one chunk (registers; vbase: vector index of the lane's
+// first vector) into the lane's running arg maxes, first index among equals:
+// p keys z_v k + g_v into (kp, ip) and, with RESID, residual keys
+// log2(p_v - q_v) + g_v over the v with p_v > q_v into (kr, ir) (p =
+// 2^{z_t k - ct}, q = 2^{z_d k - cd}; g_v the noise of index v in row j of
+// sequence b).  A group of four indices (one generator call) is skipped when
+// none of them can raise either running maximum even with the largest noise
+// (for the residual, log2(p - q) <= log2 p = z k - ct).  kp starts at a
+// lower bound of the row's best p key, so skipped indices never hold a draw.
+template <typename Tin, int QV, bool RESID>
+__device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], int cnt, int lane, float k,
+                                            float ct, float cd, int vbase, uint32_t seed_lo, uint32_t seed_hi, int j,
+                                            uint32_t b, uint32_t offset, float &kr, int &ir, float &kp, int &ip) {
+    constexpr int VEC = Store<Tin>::VEC;
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        if (q * 32 + lane >= cnt) break;
+        const int vv = vbase + q * 32;  // vector index in the row
+        float zt[VEC], zd[VEC];
+        Store<Tin>::unpack(rt[q], zt);
+        if (RESID) Store<Tin>::unpack(rd[q], zd);
+#pragma unroll
+        for (int h = 0; h < VEC / 4; ++h) {
+            float zk[4];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                zk[e4] = zt[h * 4 + e4] * k;
+                mx = fmaxf(mx, zk[e4]);
+            }
+            const bool want_p = mx + GUMBEL2_MAX >= kp;
+            const bool want_r = RESID && mx - ct + GUMBEL2_MAX >= kr;
+            if (!want_p && !want_r) continue;  // no index of the group can win either draw
+            const uint4 x = philox4x32_10(
+                make_uint4(static_cast<uint32_t>(vv * (VEC / 4) + h), static_cast<uint32_t>(j), b, offset), seed_lo,
+                seed_hi);
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const int e = h * 4 + e4;
+                const float gv = gumbel2(xs[e4]);
+                const float key_p = zk[e4] + gv;
+                if (key_p > kp) {
+                    kp = key_p;
+                    ip = vv * VEC + e;
+                }
+                if (RESID && want_r) {
+                    const float w = ex2(zk[e4] - ct) - ex2(fmaf(zd[e], k, -cd));
+                    if (w > 0.f) {
+                        const float key_r = __log2f(w) + gv;
+                        if (key_r > kr) {
+                            kr = key_r;
+                            ir = vv * VEC + e;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// The Gumbel-max pass of one warp over its segment [seg_lo, seg_lo + seg_n)
+// of row j (target row trow, draft row drow), read directly from global
+// memory (the rows were streamed moments ago and mostly sit in L2): the
+// warp's best residual and p keys with their indices {key_r, idx_r, key_p,
+// idx_p} (index -1: no candidate; the p keys start at the bound lb).  Out of
+// line and by value: it runs once per sequence, and neither its generator
+// state nor the warp's streaming state should crowd the other's registers.
+template <typename Tin, bool RESID>
+__device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsigned char *drow, int seg_lo,
+                                           int seg_n, int j, uint32_t b, float k, float ct, float cd, float lb,
+                                           uint32_t seed_lo, uint32_t seed_hi, uint32_t offset) {
+    constexpr int QV = 4;
+    const int lane = threadIdx.x & 31;
+    const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + seg_lo;
+    const uint4 *gd = reinterpret_cast<const uint4 *>(drow) + seg_lo;
+    float kr = -INFINITY, kp = lb;
+    int ir = -1, ip = -1;
+    for (int base = 0; base < seg_n; base += QV * 32) {
+        const int cnt = min(QV * 32, seg_n - base);
+        uint4 rt[QV], rd[QV];
+#pragma unroll
+        for (int q = 0; q < QV; ++q) {
+            const int jv = base + q * 32 + lane;
+            if (jv < cnt + base) {
+                rt[q] = __ldg(gt + jv);
+                if (RESID) rd[q] = __ldg(gd + jv);
+            }
+        }
+        gumbel_regs<Tin, QV, RESID>(rt, rd, cnt, lane, k, ct, cd, seg_lo + base + lane, seed_lo, seed_hi, j, b,
+                                    offset, kr, ir, kp, ip);
+    }
+    float d0 = 0.f;
+    argmax_allreduce(kr, ir, d0);
+    argmax_allreduce(kp, ip, d0);
+    return make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
+}
+
 template <typename Tin, int CV, int MODE>
 __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) {
     using St = Store<Tin>;
@@ -725,7 +832,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
         T = 1.f;
         if (b < A.B) {
             if (c.lane <= g) u = __ldg(A.unif + static_cast<size_t>(b) * (g + 1) + c.lane);
-            if (MODE == M_RS && c.lane < g) y = __ldg(A.ids + static_cast<size_t>(b) * g + c.lane);
+            if (MODE != M_TO && c.lane < g) y = __ldg(A.ids + static_cast<size_t>(b) * g + c.lane);
             T = __ldg(A.temp + b);
         }
     };
@@ -751,8 +858,9 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
         const bool greedy = (T == 0.f);
         if (MODE == M_TO) my_y = -1;
         {
-            const bool bad_y = MODE == M_RS && (c.lane < g) && (my_y < 0 || my_y >= A.V);
-            const bool bad_u = (c.lane <= g) && !(my_u >= 0.f && my_u < 1.f);
+            const bool bad_y = MODE != M_TO && (c.lane < g) && (my_y < 0 || my_y >= A.V);
+            // the Gumbel-max final draw uses no uniform u_gamma
+            const bool bad_u = (c.lane < g || (MODE != M_GB && c.lane == g)) && !(my_u >= 0.f && my_u < 1.f);
             if (__any_sync(FULL, bad_y)) flags |= F_BAD_ID;
             if (__any_sync(FULL, bad_u)) flags |= F_BAD_UNIFORM;
         }
@@ -763,7 +871,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
         int reached = 0;    // positions whose decision was taken
         // lanes l < gamma: does this warp's segment hold draft token y_l?
         const int yv_l = my_y / VEC - c.seg_lo;
-        const bool own_l = MODE == M_RS && (c.lane < g) && yv_l >= 0 && yv_l < c.seg_n;
+        const bool own_l = MODE != M_TO && (c.lane < g) && yv_l >= 0 && yv_l < c.seg_n;
         const unsigned own_mask = __ballot_sync(FULL, own_l);
 
         if (flags) {
@@ -784,7 +892,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         fin = true;
                         return;
                     }
-                    const int y = MODE == M_RS ? __shfl_sync(FULL, my_y, i) : r.didx;
+                    const int y = MODE != M_TO ? __shfl_sync(FULL, my_y, i) : r.didx;
                     if (MODE == M_TO && c.lane == i) my_y = y;
                     if (y == r.tidx) {
                         ++n;
@@ -804,7 +912,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 }
                 const float ui = __shfl_sync(FULL, my_u, i);
                 bool acc;
-                if (MODE == M_RS) {
+                if (MODE != M_TO) {
                     acc = log2f(ui) + fmaf(r.Zdy, k, -r.cd) < fmaf(r.Zty, k, -r.ct);
                 } else {
                     if (c.lane == i) my_y = r.yhat;
@@ -827,9 +935,9 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 }
                 if (fin || c.dead) break;
                 const bool has_d = p < g;
-                const bool use_d = has_d && !(greedy && MODE == M_RS);  // a greedy RS draft row is never read
-                const int y = MODE == M_RS ? __shfl_sync(FULL, my_y, has_d ? p : 0) : 0;
-                const bool owns_y = MODE == M_RS && has_d && !greedy && ((own_mask >> p) & 1u);
+                const bool use_d = has_d && !(greedy && MODE != M_TO);  // a greedy RS draft row is never read
+                const int y = MODE != M_TO ? __shfl_sync(FULL, my_y, has_d ? p : 0) : 0;
+                const bool owns_y = MODE != M_TO && has_d && !greedy && ((own_mask >> p) & 1u);
                 const int yv = y / VEC - c.seg_lo;
                 // ---- stream the segment of rows (t_p, d_p)
                 float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
@@ -887,14 +995,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     }
                     const float csum = fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
                     if (has_d) {
-                        if (MODE == M_RS) {
+                        if (MODE != M_TO) {
                             fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
                         } else {
                             bad |= !(cmd < INFINITY);
                             argmax_regs<Tin, QV, true>(rd, rt, cmd, vbase, md, dix, zty);
                         }
                     }
-                    if (!has_d) {  // per-chunk record of row gamma for the bonus draw
+                    if (!has_d && MODE != M_GB) {  // per-chunk record of row gamma for the bonus draw
                         Soft a;
                         a.m = mt;
                         a.s = csum;
@@ -921,7 +1029,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     a.s = st;
                     a.s1 = 0.f;
                     const Soft wt = soft_warp_allreduce<false>(a, k);
-                    if (MODE == M_RS) {
+                    if (MODE != M_TO) {
                         a.m = md;
                         a.s = sd;
                         const Soft wd = soft_warp_allreduce<false>(a, k);
@@ -960,6 +1068,72 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 } else {
                     flags |= F_TIMEOUT;
                 }
+            } else if (MODE == M_GB) {
+                // ---- Gumbel-max final draw: one pass over row j (the rejected
+                // position: residual weights, with the p keys as the zero-mass
+                // fallback; after gamma accepts: row gamma, p keys), one round
+                const bool resid = rej >= 0;
+                const int j = resid ? rej : g;
+                bool ok = true;
+                Norm r{};
+                if (!resid) {
+                    ok = xwait(sh, c, g);  // row gamma's normaliser flags
+                    if (ok) {
+                        ++reached;
+                        r = gather_norm<MODE>(c, g, k, false);
+                        flags |= r.rf;
+                    }
+                } else {
+                    r = gather_norm<MODE>(c, j, k, true);
+                }
+                if (!ok) flags |= F_TIMEOUT;
+                // one pass: residual keys (at a rejection) and p keys; the p
+                // draw is the bonus, or the residual's fallback when every
+                // residual weight rounded to zero (ZERO_MASS)
+                float4 best = make_float4(-INFINITY, __int_as_float(-1), -INFINITY, __int_as_float(-1));
+                if (!(flags & ERR_BITS)) {
+                    if (resid) {
+                        // drop the look-ahead rows past the rejection; the
+                        // producer moves on to the next sequence's first row
+                        drain(c);
+                        redirect_next(c, ord, A.B);
+                    }
+                    c.c_conf = g;  // the path is fixed: the producer may move on to the next sequence
+                    produce<Tin, MODE>(A, c);
+                    const float lb = fmaf(r.Mt, k, GUMBEL2_MIN);  // the best p key is at least max z k + min g
+                    const uint32_t bb = static_cast<uint32_t>(b);
+                    const unsigned char *tr = row_base<Tin>(A, true, b, j);
+                    best = resid ? gumbel_pass<Tin, true>(tr, row_base<Tin>(A, false, b, j), c.seg_lo, c.seg_n, j, bb,
+                                                          k, r.ct, r.cd, lb, A.seed_lo, A.seed_hi, A.offset)
+                                 : gumbel_pass<Tin, false>(tr, tr, c.seg_lo, c.seg_n, j, bb, k, r.ct, r.cd, lb,
+                                                           A.seed_lo, A.seed_hi, A.offset);
+                }
+                // every warp fills round gamma + 1 (no candidate when the row is flagged)
+                if (!c.dead) {
+                    xpush(sh, c, g + 1, best, ZERO4);
+                    xwait(sh, c, g + 1);
+                }
+                if (c.dead) {
+                    flags |= F_TIMEOUT;
+                } else if (!(flags & ERR_BITS)) {
+                    float vr = -INFINITY, vp = -INFINITY, d0 = 0.f;
+                    int jr = -1, jp = -1;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int q = 2 * c.lane + h;
+                        if (q < c.S) {
+                            const float4 v = *rec_at(c, c.bank, g + 1, q);
+                            argmax_merge(vr, jr, d0, v.x, __float_as_int(v.y), 0.f);
+                            argmax_merge(vp, jp, d0, v.z, __float_as_int(v.w), 0.f);
+                        }
+                    }
+                    argmax_allreduce(vr, jr, d0);
+                    argmax_allreduce(vp, jp, d0);
+                    if (resid && jr < 0) flags |= F_ZERO_MASS;  // every residual weight rounded to zero
+                    tok = (resid && jr >= 0) ? jr : jp;
+                    if (tok < 0) flags |= F_NONFINITE;
+                }
+                owner = 0;
             } else if (rej >= 0) {
                 // ---- rejection at rej: residual pass over rows (t_rej, d_rej);
                 // target-only: over t_rej with the rejected token excluded
@@ -1133,6 +1307,13 @@ const void *stream_kernel(int dtype, int cv, int mode) {
     if (mode == 1)  // target-only: 2 KB chunks (the arg max keeps two rows of registers live)
         return dtype == 0 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_TO>)
                           : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_TO>);
+    if (mode == 2) {  // Gumbel-max final draw
+        if (dtype == 0)
+            return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_GB>)
+                             : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_GB>);
+        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_GB>)
+                         : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_GB>);
+    }
     if (dtype == 0)
         return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_RS>)
                          : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_RS>);

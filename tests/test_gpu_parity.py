@@ -285,6 +285,64 @@ def test_row_stats_deep_config():
     np.testing.assert_allclose(g["alpha"], 1 - o["tv"], rtol=0, atol=1e-5)
 
 
+# ------------------------------------------------- Gumbel-max final draw ---
+
+def _check_gumbel(x, seed, offset, what=""):
+    import mtp_speculative_decoding_row_gb300 as mtp
+    out = mtp.mtp_gumbel_verify(to_dev(x.target), to_dev(x.draft), to_dev(x.draft_ids), to_dev(x.temperature),
+                                to_dev(x.uniforms), seed, offset)
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out._asdict().items() if v is not None}
+    o = oracle.gumbel_verify(x.target, x.draft, x.draft_ids, x.temperature, x.uniforms, seed, offset)
+    rep = compare.verify_report(g["tokens"], g["accept_len"], g["row_flags"], compare.gumbel_margins(o), x.draft_ids,
+                                x.gamma, x.V, x.dtype)
+    compare.assert_ok(rep, what)
+    return rep, g, o
+
+
+GB_SWEEP = [
+    # (V, dtype, gamma, C)
+    (1024, "f32", 3, None),
+    (4096, "bf16", 5, 4),
+    (40000, "f32", 8, 16),
+    (40000, "bf16", 3, 2),
+    (30000, "f32", 4, 1),
+    (151936, "bf16", 3, None),
+]
+
+
+@pytest.mark.parametrize("V,dtype,gamma,C", GB_SWEEP)
+def test_gumbel_verify(V, dtype, gamma, C):
+    """Rejection sampling with the Gumbel-max final draw (Philox noise in the
+    kernel) against the oracle: residual and bonus draws, greedy rows
+    (T = 0), a bad draft id; u[:, gamma] is not read."""
+    B = 32
+    x = W.verify_inputs(f"gb{V}", B, gamma, V, dtype, 5000 + V + gamma, family="sigma",
+                        sigmas=np.linspace(0.5, 6.0, B), delta=np.linspace(0.0, 1.2, B),
+                        temperature=np.where(np.arange(B) % 8 == 7, 0.0, np.linspace(0.6, 1.3, B)))
+    x.uniforms[:, gamma] = 3.0  # not a valid uniform: must be ignored
+    x.draft_ids[9, 0] = V + 5
+    seed, offset = (1 << 40) + 12345, 7
+    with env(MTP_RS_CLUSTER=C):
+        rep, g, o = _check_gumbel(x, seed, offset, f"gumbel V={V} {dtype} gamma={gamma} C={C}")
+        assert g["row_flags"][9] == 2 and (g["row_flags"][np.arange(B) != 9] & 31 == 0).all()
+        n = g["accept_len"]
+        assert (n == gamma).any() and (n < gamma).any()
+        # same stream: same tokens; another offset: other final tokens
+        _, g2, _ = _check_gumbel(x, seed, offset, "repeat")
+        np.testing.assert_array_equal(g["tokens"], g2["tokens"])
+        _, g3, _ = _check_gumbel(x, seed, offset + 1, "offset + 1")
+    sampled = (x.temperature > 0) & (g["row_flags"] == 0)
+    fin = lambda t, a: t[np.arange(B), np.maximum(a, 0)]  # noqa: E731
+    assert (fin(g["tokens"], n)[sampled] != fin(g3["tokens"], g3["accept_len"])[sampled]).any()
+
+
+def test_gumbel_verify_full_config():
+    x = W.config("verify64")
+    rep, g, o = _check_gumbel(x, 2024, 0, "gumbel verify64")
+    assert rep["exact"] + rep["near_margin"] == x.B and rep["near_margin"] <= 2
+
+
 # ------------------------------------------------------- diagnostics -------
 
 def _logit_scale(x):
