@@ -50,6 +50,7 @@ def _load():
             lib.oracle_verify.argtypes = [P, P, I, P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]
             lib.oracle_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
             lib.oracle_tv_loss.argtypes = [P, P, I, D, I, I, I, D, I, P, P, P, P, P, P]
+            lib.oracle_tv_loss_ex.argtypes = [P, P, I, D, I, I, I, D, I, I, I, D, P, P, P, P, P, P]
             lib.oracle_to_verify.argtypes = [P, P, I, P, P, I, I, I, P, P, P, P, P, P]
             lib.oracle_diagnostics.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P, P, P]
             U32 = ctypes.c_uint32
@@ -254,22 +255,31 @@ def row_stats(target, draft, temperature) -> dict:
 
 
 def tv_loss(target, draft, temperature: float = 1.0, grad_scale: float = 1.0, with_grad: bool = True,
-            tie_le: bool = True) -> dict:
-    """End-to-end TV loss forward/backward over [N, gamma, V] inputs.
+            tie_le: bool = True, shared_target: bool = False, clamp_tau=None) -> dict:
+    """TV loss forward/backward over draft [N, gamma, V] and target [N, gamma,
+    V] (or, shared_target, [N + gamma - 1, V] with pair (t, k) on row t + k).
+    Loss: the e2e loss, or with clamp_tau = tau_max the per-step clamped loss
+    sum_k clamp(1 - alpha_k, 0, tau_max).
 
-    Returns loss [N], alpha, S, g [N, gamma], flags [N] and (with_grad)
-    grad [N, gamma, V] float64.
+    Returns loss [N], alpha, S, g [N, gamma] (g = dl/dalpha), flags [N] and
+    (with_grad) grad [N, gamma, V] float64.
     """
     t, dt = _logits(target)
     d, _ = _logits(draft)
-    N, gamma, V = t.shape
+    N, gamma, V = d.shape
+    if shared_target:
+        assert t.ndim == 2 and t.shape[0] >= N + gamma - 1 and t.shape[1] == V
+    else:
+        assert t.shape == d.shape
     out = {"loss": np.empty(N), "alpha": np.empty((N, gamma)), "S": np.empty((N, gamma)),
            "g": np.empty((N, gamma)), "flags": np.empty(N, np.int32)}
     if with_grad:
         out["grad"] = np.empty((N, gamma, V))
-    rc = _load().oracle_tv_loss(_ptr(t), _ptr(d), dt, float(temperature), N, gamma, V, float(grad_scale),
-                                int(tie_le), _ptr(out["loss"]), _ptr(out["alpha"]), _ptr(out["S"]),
-                                _ptr(out["g"]), _ptr(out.get("grad")), _ptr(out["flags"]))
+    kind, tau = (0, 0.0) if clamp_tau is None else (1, float(clamp_tau))
+    rc = _load().oracle_tv_loss_ex(_ptr(t), _ptr(d), dt, float(temperature), N, gamma, V, float(grad_scale),
+                                   int(tie_le), int(bool(shared_target)), kind, tau, _ptr(out["loss"]),
+                                   _ptr(out["alpha"]), _ptr(out["S"]), _ptr(out["g"]), _ptr(out.get("grad")),
+                                   _ptr(out["flags"]))
     if rc:
-        raise RuntimeError(f"oracle_tv_loss failed ({rc})")
+        raise RuntimeError(f"oracle_tv_loss_ex failed ({rc})")
     return out

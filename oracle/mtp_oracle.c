@@ -49,6 +49,12 @@
  *     rejected position, or gamma for the bonus): U_v = (floor(x / 2^8) +
  *     1/2) / 2^24, exact in single precision and strictly inside (0, 1).
  *     u[b, gamma] is not used.
+ *   - Shared target rows (the MTP layout): with target [N + gamma - 1, V],
+ *     pair (t, k) uses target row t + k, the target model's distribution at
+ *     the token that draft step k of position t predicts.
+ *   - App. F clamped loss: per position the sum over steps of clamp(1 -
+ *     alpha_k, 0, tau_max); its derivative in alpha_k is -1 strictly inside
+ *     (0, tau_max) and 0 elsewhere (the subgradient 0 at the two kinks).
  *
  * Logit storage codes: 0 = float32, 1 = bfloat16 (uint16 bit patterns),
  * 2 = float64.  Every element is widened exactly to double before use.
@@ -771,11 +777,36 @@ int oracle_row_stats(const void *target, const void *draft, int dtype, const dou
  * Outputs: loss [N], alpha [N, gamma], S [N, gamma], g [N, gamma], flags [N],
  * and grad [N, gamma, V] unless grad is NULL.  Flagged positions get NaN.
  */
+/*
+ * The TV-loss variants of [BB] App. F and of the MTP layout, as options of
+ * the same computation:
+ *   shared_target = 1: target is [N + gamma - 1, V], one row per token
+ *     position, and pair (t, k) uses target row t + k (the target model's
+ *     distribution at the token that draft step k of position t predicts);
+ *     shared_target = 0: target is [N, gamma, V] like the draft.
+ *   loss_kind = 1: the per-step clamped loss of App. F summed over the
+ *     steps, l_t = sum_k clamp(1 - alpha_k, 0, tau_max), whose derivative
+ *     dl_t/dalpha_k is -1 where 0 < 1 - alpha_k < tau_max and 0 elsewhere
+ *     (the subgradient 0 at the kinks); loss_kind = 0: the e2e loss above.
+ */
+int oracle_tv_loss_ex(const void *target, const void *draft, int dtype, double T, int N, int gamma, int V,
+                      double grad_scale, int tie_le, int shared_target, int loss_kind, double tau_max,
+                      double *loss, double *alpha, double *S, double *g, double *grad, int32_t *flags);
+
 int oracle_tv_loss(const void *target, const void *draft, int dtype, double T, int N, int gamma, int V,
                    double grad_scale, int tie_le, double *loss, double *alpha, double *S, double *g,
                    double *grad, int32_t *flags)
 {
+    return oracle_tv_loss_ex(target, draft, dtype, T, N, gamma, V, grad_scale, tie_le, 0, 0, 0.0, loss, alpha, S,
+                             g, grad, flags);
+}
+
+int oracle_tv_loss_ex(const void *target, const void *draft, int dtype, double T, int N, int gamma, int V,
+                      double grad_scale, int tie_le, int shared_target, int loss_kind, double tau_max,
+                      double *loss, double *alpha, double *S, double *g, double *grad, int32_t *flags)
+{
     if (N < 0 || gamma < 1 || V < 1) return 1;
+    if (loss_kind == 1 && !(tau_max >= 0.0)) return 1;
     int fail = 0;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < N; ++t) {
@@ -790,7 +821,8 @@ int oracle_tv_loss(const void *target, const void *draft, int dtype, double T, i
         double *a = alpha + (size_t)t * gamma, *s = S + (size_t)t * gamma, *gk = g + (size_t)t * gamma;
         for (int k = 0; k < gamma && !f; ++k) {
             size_t off = ((size_t)t * gamma + k) * V;
-            f |= softmax_row(target, dtype, off, V, T, p);
+            size_t toff = shared_target ? (size_t)(t + k) * V : off;
+            f |= softmax_row(target, dtype, toff, V, T, p);
             f |= softmax_row(draft, dtype, off, V, T, q);
             if (f) break;
             a[k] = overlap(p, q, V);
@@ -808,29 +840,40 @@ int oracle_tv_loss(const void *target, const void *draft, int dtype, double T, i
             free(p);
             continue;
         }
-        /* Loss: sum over the gamma prefix products. */
         double l = 0.0;
-        for (int m = 0; m < gamma; ++m) {
-            double prod = 1.0;
-            for (int i = 0; i <= m; ++i) prod *= a[i];
-            l -= prod;
-        }
-        loss[t] = l;
-        /* dl/dalpha_k: each product containing alpha_k, with alpha_k removed. */
-        for (int k = 0; k < gamma; ++k) {
-            double d = 0.0;
-            for (int m = k; m < gamma; ++m) {
-                double prod = 1.0;
-                for (int i = 0; i <= m; ++i)
-                    if (i != k) prod *= a[i];
-                d -= prod;
+        if (loss_kind == 1) {
+            /* Clamped per-step loss and its (sub)gradient. */
+            for (int k = 0; k < gamma; ++k) {
+                const double d = 1.0 - a[k];
+                l += d < 0.0 ? 0.0 : (d > tau_max ? tau_max : d);
+                gk[k] = (d > 0.0 && d < tau_max) ? -1.0 : 0.0;
             }
-            gk[k] = d;
+            loss[t] = l;
+        } else {
+            /* Loss: sum over the gamma prefix products. */
+            for (int m = 0; m < gamma; ++m) {
+                double prod = 1.0;
+                for (int i = 0; i <= m; ++i) prod *= a[i];
+                l -= prod;
+            }
+            loss[t] = l;
+            /* dl/dalpha_k: each product containing alpha_k, with alpha_k removed. */
+            for (int k = 0; k < gamma; ++k) {
+                double d = 0.0;
+                for (int m = k; m < gamma; ++m) {
+                    double prod = 1.0;
+                    for (int i = 0; i <= m; ++i)
+                        if (i != k) prod *= a[i];
+                    d -= prod;
+                }
+                gk[k] = d;
+            }
         }
         if (grad) {
             for (int k = 0; k < gamma; ++k) {
                 size_t off = ((size_t)t * gamma + k) * V;
-                softmax_row(target, dtype, off, V, T, p);
+                size_t toff = shared_target ? (size_t)(t + k) * V : off;
+                softmax_row(target, dtype, toff, V, T, p);
                 softmax_row(draft, dtype, off, V, T, q);
                 for (int v = 0; v < V; ++v) {
                     double ind = (tie_le ? (q[v] <= p[v]) : (q[v] < p[v])) ? 1.0 : 0.0;

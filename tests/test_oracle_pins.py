@@ -666,3 +666,79 @@ def test_gumbel_verify_acceptance_is_the_rejection_sampling_chain():
     fin = np.array([g["tokens"][b, g["accept_len"][b]] for b in range(B)])
     fin2 = np.array([g2["tokens"][b, g2["accept_len"][b]] for b in range(B)])
     assert (fin != fin2).any()
+
+
+# -------------------------------------------- TV-loss layout and variants --
+
+def test_shared_target_layout_is_the_row_gather():
+    """Shared target rows [N + gamma - 1, V]: pair (t, k) uses row t + k, the
+    target distribution at the token draft step k of position t predicts.
+    Equal to the per-position loss on the explicitly gathered target."""
+    rng = np.random.default_rng(41)
+    N, gamma, V = 7, 3, 50
+    ts = rng.standard_normal((N + gamma - 1, V)) * 2
+    d = rng.standard_normal((N, gamma, V)) * 2
+    gathered = np.stack([np.stack([ts[t + k] for k in range(gamma)]) for t in range(N)])
+    a = oracle.tv_loss(gathered, d, 0.9, 1.5)
+    b = oracle.tv_loss(ts, d, 0.9, 1.5, shared_target=True)
+    for key in ("loss", "alpha", "S", "g", "grad"):
+        np.testing.assert_array_equal(a[key], b[key])
+    c = oracle.tv_loss(ts, d, 0.9, 1.5, shared_target=True, clamp_tau=0.4)
+    e = oracle.tv_loss(gathered, d, 0.9, 1.5, clamp_tau=0.4)
+    for key in ("loss", "alpha", "grad"):
+        np.testing.assert_array_equal(c[key], e[key])
+
+
+def test_clamped_step_loss_closed_forms():
+    """App. F per-step loss clamp(1 - alpha, 0, tau_max): with tau_max >= 1 it
+    is the summed total variation 1/2 sum |p - q| (a library softmax), with
+    tau_max = 0 it vanishes with a zero gradient, and a step whose 1 - alpha
+    exceeds tau_max contributes tau_max and no gradient."""
+    rng = np.random.default_rng(42)
+    N, gamma, V, T = 5, 3, 80, 1.1
+    t = rng.standard_normal((N, gamma, V)) * 2
+    d = t + rng.standard_normal((N, gamma, V)) * 0.8
+    p = scipy.special.softmax(t / T, axis=-1)
+    q = scipy.special.softmax(d / T, axis=-1)
+    tv = 0.5 * np.abs(p - q).sum(-1)
+    out = oracle.tv_loss(t, d, T, 1.0, clamp_tau=1.0)
+    np.testing.assert_allclose(out["loss"], tv.sum(-1), rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(out["g"], -1.0)
+    z = oracle.tv_loss(t, d, T, 1.0, clamp_tau=0.0)
+    assert np.all(z["loss"] == 0) and np.all(z["grad"] == 0)
+    tau = float(np.median(tv))
+    c = oracle.tv_loss(t, d, T, 1.0, clamp_tau=tau)
+    np.testing.assert_allclose(c["loss"], np.minimum(tv, tau).sum(-1), rtol=1e-12, atol=1e-14)
+    over = tv > tau
+    assert over.any() and (~over).any()
+    assert np.all(c["grad"][over] == 0)
+    # inside the clamp: the gradient of -alpha, i.e. that of the e2e loss at gamma = 1
+    one = oracle.tv_loss(t[:, :1], d[:, :1], T, 1.0)
+    inside = ~over[:, 0]
+    np.testing.assert_allclose(c["grad"][inside, 0], one["grad"][inside, 0], rtol=0, atol=1e-15)
+
+
+def test_clamped_step_loss_finite_differences():
+    """Gradient of sum_k clamp(1 - alpha_k, 0, tau_max) against central
+    differences, with tau_max between the steps' 1 - alpha so that both the
+    clamped and the open side occur and no step sits on a kink."""
+    rng = np.random.default_rng(43)
+    N, gamma, V, T = 2, 3, 12, 0.9
+    t, d = _kink_free_inputs(rng, N, gamma, V, T, 2e-4)
+    a = oracle.tv_loss(t, d, T, 1.0)["alpha"]
+    steps = np.sort((1 - a).ravel())
+    tau = 0.5 * (steps[2] + steps[3])
+    assert np.min(np.abs((1 - a) - tau)) > 1e-3
+    out = oracle.tv_loss(t, d, T, 2.0, clamp_tau=tau)
+    h = 1e-6
+    fd = np.empty_like(d)
+    for idx in np.ndindex(d.shape):
+        dp = d.copy()
+        dm = d.copy()
+        dp[idx] += h
+        dm[idx] -= h
+        lp = oracle.tv_loss(t, dp, T, 1.0, with_grad=False, clamp_tau=tau)["loss"].sum()
+        lm = oracle.tv_loss(t, dm, T, 1.0, with_grad=False, clamp_tau=tau)["loss"].sum()
+        fd[idx] = 2.0 * (lp - lm) / (2 * h)
+    np.testing.assert_allclose(out["grad"], fd, rtol=0, atol=1e-7)
+    assert (out["g"] == 0).any() and (out["g"] == -1).any()
