@@ -17,7 +17,7 @@ metric through the public API with pinned host buffers: host-to-device copy
 of the step's inputs, the call, and the device-to-host copy of its outputs.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
-       [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss]
+       [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss,tvshared]
 Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -243,29 +243,38 @@ class VerifyWorkload:
 
 
 class TVWorkload:
-    def __init__(self, device, N=None):
-        import torch
-
+    def __init__(self, device, N=None, shared=False):
         import workloads as W
         import mtp_speculative_decoding_row_gb300 as mtp
 
         self.mtp = mtp
-        self.x = x = W.config("tvloss", device=device, N_override=N)
+        self.shared = shared
+        if shared:
+            N = N or 16384
+            self.x = x = W.tvloss_shared_inputs_device("tvshared", N, 3, W.V_QWEN, W.CONFIG_NAMES.index("tvloss"),
+                                                       device)
+        else:
+            self.x = x = W.config("tvloss", device=device, N_override=N)
         self.N, self.gamma, self.V, self.es = x.N, x.gamma, x.V, 2
         self.stats = False
         self.out = None
         self.copies = 1
         self.positions = x.N * x.gamma
-        self.bytes_full = x.N * x.gamma * x.V * (2 * 2 + 4)
+        # draft read (2 B) and gradient written (4 B) per (t, k, v); target rows read once
+        tgt = (x.N + x.gamma - 1) * x.V * 2 if shared else x.N * x.gamma * x.V * 2
+        self.bytes_full = x.N * x.gamma * x.V * (2 + 4) + tgt
 
     def call(self, i: int, stream=None):
         self.out = self.mtp.mtp_tv_loss_fwd_bwd(self.x.target, self.x.draft, self.x.temperature, self.x.grad_scale,
-                                                out=self.out, stream=stream)
+                                                shared_target=self.shared, out=self.out, stream=stream)
 
     def alg_bytes(self) -> int:
         return self.bytes_full
 
     def describe(self) -> str:
+        if self.shared:
+            return (f"e2e TV loss fwd+bwd, shared target rows [N+gamma-1, V] (pair (t,k) on row t+k): N={self.N} "
+                    "positions x gamma=3, V=151936, bf16 logits, draft = target row + N(0,0.5), fp32 gradient, T=1")
         return (f"e2e TV loss fwd+bwd: N={self.N} positions x gamma=3, V=151936, bf16 logits (entropy-spanning target, "
                 "draft = target + N(0,0.5)), fp32 gradient, T=1")
 
@@ -421,8 +430,8 @@ def run_cuda(args, world, rank, local, pg):
     results = {}
     head = None
     for name in names:
-        if name == "tvloss":
-            wl = TVWorkload(device, args.tv_n)
+        if name in ("tvloss", "tvshared"):
+            wl = TVWorkload(device, args.tv_n, shared=name == "tvshared")
             steps = max(3, min(args.steps, 20)) if name != names[0] else args.steps
         else:
             per_copy = VerifyWorkloadBytes(name)
@@ -440,8 +449,9 @@ def run_cuda(args, world, rank, local, pg):
         alg = wl.alg_bytes()
         per_launch_s = t["ms_total"] / 1e3 / t["launches"]
         achieved = alg / per_launch_s / 1e9
-        plan = mtp.mtp_query_plan("tv_loss" if name == "tvloss" else wl.plan_op(),
-                                  "bf16" if wl.es == 2 else "f32", wl.N if name == "tvloss" else wl.B, wl.gamma, wl.V)
+        tv = name in ("tvloss", "tvshared")
+        plan = mtp.mtp_query_plan("tv_loss" if tv else wl.plan_op(), "bf16" if wl.es == 2 else "f32",
+                                  wl.N if tv else wl.B, wl.gamma, wl.V)
         r = {
             "workload": wl.describe(),
             "launch_plan": plan,
@@ -463,7 +473,7 @@ def run_cuda(args, world, rank, local, pg):
     name, wl0, t, t_ms, steps, clocks, alg, achieved = head
     # e2e leg on the headline workload
     e2e = None
-    if name != "tvloss":
+    if name not in ("tvloss", "tvshared"):
         wl = VerifyWorkload(name, device, 1)
         e2e = time_e2e(wl, max(3, min(args.steps, 50)), max(3, args.warmup), device)
         e2e["value"] = max_over_ranks(pg, -e2e["value"], device) * -1 * world
@@ -471,7 +481,7 @@ def run_cuda(args, world, rank, local, pg):
     traffic = TRAFFIC.get(name)
     traffic_val = traffic["bytes"] if traffic and traffic.get("csrc") == h else None
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and name != "tvloss":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and name not in ("tvloss", "tvshared"):
         cpu = oracle_verify_rate(name, args.cpu_seconds, 16)
 
     if rank == 0:
@@ -514,7 +524,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss")
+    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss,tvshared")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")

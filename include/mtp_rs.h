@@ -248,6 +248,25 @@ int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp
                         mtp_stream_t stream);
 
 /*
+ * mtp_tv_loss_ex -- mtp_tv_loss_fwd_bwd with the layout and loss variants of
+ * [BB] App. F:
+ *   target_layout 0: target_logits [N, gamma, V] like the draft;
+ *   target_layout 1: shared target rows [N + gamma - 1, V]: pair (t, k)
+ *     reads row t + k, the target model's distribution at the token draft
+ *     step k of position t predicts (consecutive positions share rows);
+ *   loss_kind 0: the e2e loss of mtp_tv_loss_fwd_bwd;
+ *   loss_kind 1: l_t = sum_k clamp(1 - alpha_k, 0, tau_max), the per-step
+ *     clamped loss, with dl_t/dalpha_k = -1 strictly inside the clamp and 0
+ *     elsewhere (the subgradient 0 at the kinks); tau_max >= 0.
+ * Other arguments, outputs and flags as for mtp_tv_loss_fwd_bwd.  Returns
+ * MTP_ERR_INVALID_ARG for another layout or loss kind, or tau_max < 0 or NaN
+ * with loss_kind 1.
+ */
+int mtp_tv_loss_ex(const void *target_logits, const void *draft_logits, mtp_dtype dtype, float temperature,
+                   int N, int gamma, int V, float grad_scale, int target_layout, int loss_kind, float tau_max,
+                   float *loss, float *alpha, float *grad_draft_logits, int32_t *row_flags, mtp_stream_t stream);
+
+/*
  * mtp_query_plan -- the launch plan a call would use on the current device
  * (diagnostics; launches nothing).  op: 0 = mtp_rs_verify, 1 = mtp_rs_verify
  * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd, 4 =

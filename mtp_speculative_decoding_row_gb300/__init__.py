@@ -31,7 +31,7 @@ ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_T
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_row_stats", "mtp_rs_diagnostics",
-                    "mtp_tv_loss_fwd_bwd", "mtp_query_plan", "mtp_status_string")
+                    "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_query_plan", "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
             "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9}
 
@@ -66,6 +66,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_to_verify.restype = I
     lib.mtp_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
     lib.mtp_row_stats.restype = I
+    lib.mtp_tv_loss_ex.argtypes = [P, P, I, F, I, I, I, F, I, I, F, P, P, P, P, P]
+    lib.mtp_tv_loss_ex.restype = I
     lib.mtp_gumbel_verify.argtypes = [P, P, I, P, P, P, ctypes.c_uint64, ctypes.c_uint32, I, I, I, P, P, P, P]
     lib.mtp_gumbel_verify.restype = I
     lib.mtp_rs_diagnostics.argtypes = [P, P, I, P, I, I, I, P, P, P, P, P, P, P, P, P]
@@ -314,24 +316,43 @@ def mtp_rs_diagnostics(target_logits, draft_logits, temperature, *, out: Optiona
 
 
 def mtp_tv_loss_fwd_bwd(target_logits, draft_logits, temperature: float = 1.0, grad_scale: float = 1.0, *,
+                        shared_target: bool = False, clamp_tau: Optional[float] = None,
                         out: Optional[TVLossResult] = None, stream=None) -> TVLossResult:
-    """Fused e2e TV loss forward + backward over [N, gamma, V] logits; returns
-    per-position loss, alpha, the float32 gradient w.r.t. the draft logits and
-    row flags."""
+    """Fused TV loss forward + backward over draft logits [N, gamma, V];
+    returns per-position loss, alpha, the float32 gradient w.r.t. the draft
+    logits and row flags.  Target logits are [N, gamma, V], or with
+    shared_target [N + gamma - 1, V] (pair (t, k) on row t + k).  The loss is
+    the e2e loss, or with clamp_tau = tau_max the per-step clamped loss
+    sum_k clamp(1 - alpha_k, 0, tau_max)."""
     torch = _torch()
-    dev = target_logits.device
-    N, gamma, V = target_logits.shape
-    _check(target_logits, "target_logits", dev)
-    _check(draft_logits, "draft_logits", dev, target_logits.dtype, (N, gamma, V))
+    dev = draft_logits.device
+    N, gamma, V = draft_logits.shape
+    _check(draft_logits, "draft_logits", dev)
+    if shared_target:
+        if target_logits.dim() != 2 or target_logits.shape[0] < N + gamma - 1 or target_logits.shape[1] != V:
+            raise ValueError(f"shared target_logits must be [>= N + gamma - 1, V], got {tuple(target_logits.shape)}")
+        _check(target_logits, "target_logits", dev, draft_logits.dtype)
+    else:
+        _check(target_logits, "target_logits", dev, draft_logits.dtype, (N, gamma, V))
     if out is None:
         out = TVLossResult(torch.empty((N,), dtype=torch.float32, device=dev),
                            torch.empty((N, gamma), dtype=torch.float32, device=dev),
                            torch.empty((N, gamma, V), dtype=torch.float32, device=dev),
                            torch.empty((N,), dtype=torch.int32, device=dev))
-    rc = load_library().mtp_tv_loss_fwd_bwd(
-        _ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), float(temperature), N, gamma, V,
-        float(grad_scale), _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad), _ptr(out.row_flags),
-        _stream(dev, stream))
+    lib = load_library()
+    if not shared_target and clamp_tau is None:
+        rc = lib.mtp_tv_loss_fwd_bwd(
+            _ptr(target_logits), _ptr(draft_logits), _dtype_code(draft_logits), float(temperature), N, gamma, V,
+            float(grad_scale), _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad), _ptr(out.row_flags),
+            _stream(dev, stream))
+        name = "mtp_tv_loss_fwd_bwd"
+    else:
+        rc = lib.mtp_tv_loss_ex(
+            _ptr(target_logits), _ptr(draft_logits), _dtype_code(draft_logits), float(temperature), N, gamma, V,
+            float(grad_scale), int(bool(shared_target)), 0 if clamp_tau is None else 1,
+            0.0 if clamp_tau is None else float(clamp_tau), _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad),
+            _ptr(out.row_flags), _stream(dev, stream))
+        name = "mtp_tv_loss_ex"
     if rc:
-        raise MTPError("mtp_tv_loss_fwd_bwd", rc)
+        raise MTPError(name, rc)
     return out

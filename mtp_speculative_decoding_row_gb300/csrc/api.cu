@@ -609,12 +609,14 @@ extern "C" int mtp_rs_diagnostics(const void *target_logits, const void *draft_l
                      kl, yhat, p_yhat, rs_better, row_flags, stream);
 }
 
-extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
-                                   float temperature, int N, int gamma, int V, float grad_scale, float *loss,
-                                   float *alpha, float *grad_draft_logits, int32_t *row_flags,
-                                   mtp_stream_t stream) {
+extern "C" int mtp_tv_loss_ex(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                              float temperature, int N, int gamma, int V, float grad_scale, int target_layout,
+                              int loss_kind, float tau_max, float *loss, float *alpha, float *grad_draft_logits,
+                              int32_t *row_flags, mtp_stream_t stream) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
     if (N < 0 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if ((target_layout != 0 && target_layout != 1) || (loss_kind != 0 && loss_kind != 1)) return MTP_ERR_INVALID_ARG;
+    if (loss_kind == 1 && !(tau_max >= 0.f)) return MTP_ERR_INVALID_ARG;
     if (N == 0) return MTP_OK;
     if (!target_logits || !draft_logits || !loss || !grad_draft_logits) return MTP_ERR_INVALID_ARG;
     if (!aligned16(target_logits) || !aligned16(draft_logits) || !aligned16(grad_draft_logits))
@@ -648,7 +650,18 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
     A.alpha = alpha;
     A.grad = grad_draft_logits;
     A.flags = row_flags;
+    A.shared_target = target_layout;
+    A.loss_kind = loss_kind;
+    A.tau_max = loss_kind == 1 ? tau_max : 0.f;
     return launch(func, p, &A, stream);
+}
+
+extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
+                                   float temperature, int N, int gamma, int V, float grad_scale, float *loss,
+                                   float *alpha, float *grad_draft_logits, int32_t *row_flags,
+                                   mtp_stream_t stream) {
+    return mtp_tv_loss_ex(target_logits, draft_logits, dtype, temperature, N, gamma, V, grad_scale, 0, 0, 0.f, loss,
+                          alpha, grad_draft_logits, row_flags, stream);
 }
 
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,

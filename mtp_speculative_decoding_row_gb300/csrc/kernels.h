@@ -46,6 +46,9 @@ struct TVArgs {
     float *alpha;           // [N, gamma] or null
     float *grad;            // [N, gamma, V]
     int32_t *flags;         // [N] or null
+    int shared_target;      // 1: target is [N + gamma - 1, V], pair (t, k) on row t + k
+    int loss_kind;          // 0: e2e loss; 1: sum_k clamp(1 - alpha_k, 0, tau_max)
+    float tau_max;
 };
 
 // Modes of the streaming row-pair statistics kernel.

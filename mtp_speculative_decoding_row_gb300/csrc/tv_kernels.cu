@@ -106,6 +106,16 @@ __device__ __forceinline__ const unsigned char *tv_row(const void *base, int t, 
            ((static_cast<size_t>(t) * g + k) * static_cast<size_t>(V)) * Store<Tin>::ES;
 }
 
+// Target row of pair (t, k): [N, gamma, V], or shared rows [N + gamma - 1, V]
+// where pair (t, k) reads row t + k.
+template <typename Tin>
+__device__ __forceinline__ const unsigned char *tv_trow(const TVArgs &A, int t, int k) {
+    if (A.shared_target)
+        return reinterpret_cast<const unsigned char *>(A.target) +
+               (static_cast<size_t>(t + k) * static_cast<size_t>(A.V)) * Store<Tin>::ES;
+    return tv_row<Tin>(A.target, t, k, A.gamma, A.V);
+}
+
 // One row slice by bulk copy on `bar` (thread 0); aligned rows only.
 template <typename Tin>
 __device__ __forceinline__ void issue_row(const Slice &s, const unsigned char *row, unsigned char *buf, uint32_t bar) {
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
     };
     auto load_t = [&](int t, int kk, int sl) {
         if (aligned && s.nvec > 0) {
-            issue_row<Tin>(s, tv_row<Tin>(A.target, t, kk, g, V), tslot[sl], smem_addr(&sh.tbar[sl]));
+            issue_row<Tin>(s, tv_trow<Tin>(A, t, kk), tslot[sl], smem_addr(&sh.tbar[sl]));
             tarm |= 1u << sl;
         }
     };
@@ -299,7 +309,7 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
                 if (!wait_t(ts)) tmo = 1;
                 if (!wait_d(ds)) tmo = 1;
                 if (!aligned) {
-                    load_slice<Tin, NT>(s, tv_row<Tin>(A.target, t, kk, g, V), tb, 0, false);
+                    load_slice<Tin, NT>(s, tv_trow<Tin>(A, t, kk), tb, 0, false);
                     load_slice<Tin, NT>(s, tv_row<Tin>(A.draft, t, kk, g, V), db, 0, false);
                 }
             }
@@ -395,19 +405,30 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
         float *gbase = A.grad + static_cast<size_t>(t) * g * static_cast<size_t>(V);
         if (!flags) {
             if (tid == 0) {
-                // chain of the e2e loss: prefix products forward, W backward
-                float P[MAX_GAMMA];
-                float prod = 1.f, loss = 0.f;
-                for (int kk = 0; kk < g; ++kk) {
-                    prod *= sh.ak[kk];
-                    P[kk] = prod;
-                    loss -= prod;
-                }
-                float W = 1.f;
-                for (int kk = g - 1; kk >= 0; --kk) {
-                    const float Pprev = kk ? P[kk - 1] : 1.f;
-                    sh.gk[kk] = -Pprev * W;
-                    W = fmaf(sh.ak[kk], W, 1.f);
+                float loss = 0.f;
+                if (A.loss_kind == 1) {
+                    // App. F per-step loss clamp(1 - alpha_k, 0, tau_max): slope -1
+                    // strictly inside the clamp, 0 elsewhere
+                    for (int kk = 0; kk < g; ++kk) {
+                        const float d = 1.f - sh.ak[kk];
+                        loss += fminf(fmaxf(d, 0.f), A.tau_max);
+                        sh.gk[kk] = (d > 0.f && d < A.tau_max) ? -1.f : 0.f;
+                    }
+                } else {
+                    // chain of the e2e loss: prefix products forward, W backward
+                    float P[MAX_GAMMA];
+                    float prod = 1.f;
+                    for (int kk = 0; kk < g; ++kk) {
+                        prod *= sh.ak[kk];
+                        P[kk] = prod;
+                        loss -= prod;
+                    }
+                    float W = 1.f;
+                    for (int kk = g - 1; kk >= 0; --kk) {
+                        const float Pprev = kk ? P[kk - 1] : 1.f;
+                        sh.gk[kk] = -Pprev * W;
+                        W = fmaf(sh.ak[kk], W, 1.f);
+                    }
                 }
                 sh.loss = loss;
             }

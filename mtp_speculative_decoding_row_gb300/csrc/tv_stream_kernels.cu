@@ -122,7 +122,10 @@ __device__ __forceinline__ void tproduce(const TVArgs &A, TC &c) {
             int kind, k;
             unit_of(c.p_u, c.g, kind, k);
             const size_t off = static_cast<size_t>(c.seg_lo) * 16u;
-            c.p_t = kind == P_GRAD ? nullptr : tv_row_ptr<Tin>(A.target, t, k, c.g, A.V) + off;
+            c.p_t = kind == P_GRAD ? nullptr
+                                   : (A.shared_target ? tv_row_ptr<Tin>(A.target, t + k, 0, 1, A.V)
+                                                      : tv_row_ptr<Tin>(A.target, t, k, c.g, A.V)) +
+                                         off;
             c.p_d = tv_row_ptr<Tin>(A.draft, t, k, c.g, A.V) + off;
         }
         const int cnt = tchunk(c, c.p_c);
@@ -497,12 +500,14 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                 if (!c.dead && !flags) {
                     float P[MAXG];
                     float prod = 1.f, ls = 0.f;
+                    const bool clamped = A.loss_kind == 1;
 #pragma unroll
                     for (int kk = 0; kk < MAXG; ++kk) {
                         if (kk < g) {
                             prod *= av[kk];
                             P[kk] = prod;
-                            ls -= prod;
+                            // e2e: -sum of the prefix products; clamped: sum of clamp(1 - alpha, 0, tau_max)
+                            ls += clamped ? fminf(fmaxf(1.f - av[kk], 0.f), A.tau_max) : -prod;
                         }
                     }
                     float W = 1.f;
@@ -510,7 +515,9 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                     for (int kk = MAXG - 1; kk >= 0; --kk) {
                         if (kk < g) {
                             const float Pprev = kk ? P[kk - 1] : 1.f;
-                            const float coef = A.grad_scale * (-Pprev * W) / T;
+                            const float d = 1.f - av[kk];
+                            const float dl = clamped ? ((d > 0.f && d < A.tau_max) ? -1.f : 0.f) : -Pprev * W;
+                            const float coef = A.grad_scale * dl / T;
                             if (c.lane == 0) {
                                 c.ws->on[kk] = coef * (1.f - sv[kk]);
                                 c.ws->off[kk] = -coef * sv[kk];

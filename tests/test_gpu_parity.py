@@ -508,6 +508,53 @@ def test_tv_loss_kernels(N, gamma, V, dtype, C, clusters, ring, kernel):
     compare.assert_ok(rep, f"tv kernels N={N} gamma={gamma} V={V} C={C} kernel={kernel}")
 
 
+TV_VARIANTS = [
+    # (N, gamma, V, dtype, shared, clamp_tau, C, kernel)
+    (7, 3, 4096, "f32", True, None, None, None),
+    (9, 3, 40000, "bf16", True, None, 16, None),
+    (6, 5, 12000, "bf16", True, 0.5, 4, None),
+    (6, 3, 30000, "f32", False, 0.3, None, None),
+    (5, 2, 20000, "bf16", False, 1.0, 8, None),
+    (5, 3, 4097, "bf16", True, 0.4, None, None),      # unaligned rows: the resident kernel
+    (6, 3, 20000, "f32", True, 0.3, 4, "resident"),
+    (4, 9, 8192, "bf16", True, None, None, None),     # gamma = 9: the resident kernel
+]
+
+
+@pytest.mark.parametrize("N,gamma,V,dtype,shared,tau,C,kernel", TV_VARIANTS)
+def test_tv_loss_variants(N, gamma, V, dtype, shared, tau, C, kernel):
+    """Shared target rows [N + gamma - 1, V] (pair (t, k) on row t + k) and
+    the App. F clamped per-step loss, on both TV kernels."""
+    if shared:
+        x = W.tvloss_shared_inputs("tvs", N, gamma, V, dtype, 700 + V + gamma, delta=0.5,
+                                   sigmas=np.linspace(0.7, 8.0, N + gamma - 1))
+    else:
+        x = W.tvloss_inputs("tvc", N, gamma, V, dtype, 700 + V + gamma, delta=0.5, sigmas=np.linspace(0.7, 8.0, N))
+    import mtp_speculative_decoding_row_gb300 as mtp
+    if tau is not None and tau < 1.0:
+        # tau_max at the median step of the oracle's 1 - alpha: both sides of the clamp occur
+        steps = np.sort(1 - oracle.tv_loss(x.target, x.draft, 0.9, 1.0, with_grad=False,
+                                           shared_target=shared)["alpha"].ravel())
+        mid = len(steps) // 2
+        tau = float(0.5 * (steps[mid - 1] + steps[mid]))
+    with env(MTP_RS_CLUSTER=C, MTP_RS_TV_KERNEL=kernel):
+        out = mtp.mtp_tv_loss_fwd_bwd(to_dev(x.target), to_dev(x.draft), 0.9, 1.25, shared_target=shared,
+                                      clamp_tau=tau)
+        torch.cuda.synchronize()
+    o = oracle.tv_loss(x.target, x.draft, 0.9, 1.25, shared_target=shared, clamp_tau=tau)
+    tf = W.bf16_bits_to_f32(x.target).astype(np.float64) if dtype == "bf16" else x.target.astype(np.float64)
+    df = W.bf16_bits_to_f32(x.draft).astype(np.float64) if dtype == "bf16" else x.draft.astype(np.float64)
+    if shared:
+        tf = np.stack([tf[t:t + gamma] for t in range(N)])
+    rep = compare.tv_report(out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy(),
+                            out.row_flags.cpu().numpy(), o, dtype, tf, df, 0.9)
+    compare.assert_ok(rep, f"tv variant N={N} gamma={gamma} V={V} shared={shared} tau={tau} kernel={kernel}")
+    if tau is not None:
+        steps = 1 - o["alpha"]
+        assert ((steps > tau).any() and (steps < tau).any()) or tau >= 1.0
+        assert np.min(np.abs(steps - tau)) > 1e-6  # no step on the kink
+
+
 def test_tv_plan_kernels():
     import mtp_speculative_decoding_row_gb300 as mtp
     p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)

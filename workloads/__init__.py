@@ -277,6 +277,62 @@ def tvloss_inputs_device(name: str, N: int, gamma: int, V: int, c: int, device, 
                         {"sigma": sig, "delta": delta, "backend": "torch-cuda"})
 
 
+def tvloss_shared_inputs(name: str, N: int, gamma: int, V: int, dtype: str, c: int, *, delta: float = 0.5,
+                         temperature: float = 1.0, grad_scale: float = 1.0, sigmas=None) -> TVLossInputs:
+    """Host TV-loss inputs in the shared-target layout: target rows r = 0 ..
+    N + gamma - 2, sigma_r * N(0, 1) (entropy-spanning unless ``sigmas``
+    gives one value per row), and draft[t, k] = rounded target row t + k +
+    delta * N(0, 1).  ``target`` is [N + gamma - 1, V]."""
+    R = N + gamma - 1
+    sig = entropy_span_sigmas(R) if sigmas is None else np.broadcast_to(np.asarray(sigmas, np.float64), (R,))
+    esz = np.uint16 if dtype == "bf16" else np.float32
+    target = np.empty((R, V), dtype=esz)
+    draft = np.empty((N, gamma, V), dtype=esz)
+    for r in range(R):
+        target[r] = _round(philox(100 + c, r).standard_normal(V, dtype=np.float32) * np.float32(sig[r]), dtype)
+
+    def one(t: int) -> None:
+        nz = philox(200 + c, t).standard_normal((gamma, V), dtype=np.float32)
+        draft[t] = _round(_widen(target[t:t + gamma], dtype) + np.float32(delta) * nz, dtype)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(N)))
+    return TVLossInputs(name, N, gamma, V, dtype, target, draft, float(temperature), float(grad_scale),
+                        {"sigma": np.asarray(sig), "delta": delta, "backend": "numpy", "layout": "shared"})
+
+
+def tvloss_shared_inputs_device(name: str, N: int, gamma: int, V: int, c: int, device, *, delta: float = 0.5,
+                                temperature: float = 1.0, grad_scale: float = 1.0,
+                                chunk: int = 512) -> TVLossInputs:
+    """Device-resident bf16 inputs of :func:`tvloss_shared_inputs` for sizes
+    too large for the host (torch's seeded CUDA Philox per chunk)."""
+    import torch
+
+    R = N + gamma - 1
+    sig = entropy_span_sigmas(R)
+    target = torch.empty((R, V), dtype=torch.bfloat16, device=device)
+    draft = torch.empty((N, gamma, V), dtype=torch.bfloat16, device=device)
+    sig_t = torch.tensor(sig, dtype=torch.float32, device=device)
+    g = torch.Generator(device=device)
+    for s in range(0, R, chunk):
+        e = min(R, s + chunk)
+        g.manual_seed((100 + c) * 1_000_003 + s)
+        z = torch.randn((e - s, V), generator=g, device=device, dtype=torch.float32)
+        target[s:e] = (z * sig_t[s:e, None]).to(torch.bfloat16)
+        del z
+    for s in range(0, N, chunk):
+        e = min(N, s + chunk)
+        g.manual_seed((200 + c) * 1_000_003 + s)
+        z = torch.randn((e - s, gamma, V), generator=g, device=device, dtype=torch.float32)
+        z.mul_(delta)
+        for k in range(gamma):
+            z[:, k].add_(target[s + k:e + k].float())
+        draft[s:e] = z.to(torch.bfloat16)
+        del z
+    return TVLossInputs(name, N, gamma, V, "bf16", target, draft, float(temperature), float(grad_scale),
+                        {"sigma": sig, "delta": delta, "backend": "torch-cuda", "layout": "shared"})
+
+
 # The five workloads: (index c, description).
 CONFIG_NAMES = ["tiny", "verify64", "rl512", "deep256", "tvloss"]
 
