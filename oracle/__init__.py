@@ -57,6 +57,7 @@ def _load():
             lib.oracle_philox4x32_10.argtypes = [P, P, P]
             lib.oracle_gumbel_noise.argtypes = [U32, U32, U32, U32, I, I, I, P]
             lib.oracle_gumbel_verify.argtypes = [P, P, I, P, P, P, U32, U32, U32, I, I, I, P, P, P, P, P]
+            lib.oracle_draft_sample.argtypes = [P, I, P, P, I, U32, U32, U32, I, I, P, P, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_softmax, lib.oracle_verify, lib.oracle_row_stats, lib.oracle_tv_loss,
                       lib.oracle_num_threads):
@@ -211,6 +212,26 @@ def gumbel_verify(target, draft, draft_ids, temperature, uniforms, seed: int, of
                                       _ptr(out["gumbel_margin"]))
     if rc:
         raise RuntimeError(f"oracle_gumbel_verify failed ({rc})")
+    return out
+
+
+def draft_sample(logits, temperature, uniforms=None, method: str = "multinomial", seed: int = 0,
+                 offset: int = 0) -> dict:
+    """Draw one token per row of logits [R, V] from softmax(z / T): the
+    inverse-CDF draw with uniforms [R] ("multinomial") or the Gumbel-max draw
+    with Philox noise ("gumbel", counter (v / 4, 0, r, offset)); T = 0 is
+    greedy.  Returns ids [R], flags [R], margin [R]."""
+    z, dt = _logits(logits)
+    R, V = z.shape
+    temp = np.ascontiguousarray(temperature, dtype=np.float64).reshape(R)
+    m = {"multinomial": 0, "gumbel": 1}[method]
+    u = np.zeros(R) if uniforms is None else np.ascontiguousarray(uniforms, dtype=np.float64).reshape(R)
+    lo, hi = _seed_words(seed)
+    out = {"ids": np.empty(R, np.int32), "flags": np.empty(R, np.int32), "margin": np.empty(R, np.float64)}
+    rc = _load().oracle_draft_sample(_ptr(z), dt, _ptr(temp), _ptr(u), m, lo, hi, int(offset) & 0xFFFFFFFF, R, V,
+                                     _ptr(out["ids"]), _ptr(out["flags"]), _ptr(out["margin"]))
+    if rc:
+        raise RuntimeError(f"oracle_draft_sample failed ({rc})")
     return out
 
 

@@ -886,6 +886,62 @@ int oracle_tv_loss_ex(const void *target, const void *draft, int dtype, double T
     return fail ? 2 : 0;
 }
 
+/*
+ * Draft sampling, the step before verification [BB, App. G "Rejection
+ * Sampling Inference Implementation": production rejection sampling draws the
+ * draft tokens from q; G.1 multinomial (SGLang), G.2 Gumbel-max (vLLM)]:
+ * for row r of logits [R, V], q = softmax(z_r / T_r) and
+ *   method 0: the inverse-CDF draw with u[r] (cdf_draw: the smallest v with
+ *             C(v) > u R);
+ *   method 1: the Gumbel-max draw arg max_v [ln q_v + G_v] with the noise of
+ *             row 0 of sequence r (counter (v / 4, 0, r, offset)), i.e. the
+ *             bonus draw of a one-row sequence; u is not used.
+ * T_r == 0 is greedy (arg max, ties to the smallest index).  margin[r] is the
+ * draw's distance to a decision boundary: the CDF margin, the gap between
+ * the two best Gumbel keys, or +inf for greedy rows.
+ */
+int oracle_draft_sample(const void *logits, int dtype, const double *temp, const double *u, int method,
+                        uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, int R, int V, int32_t *ids,
+                        int32_t *flags, double *margin)
+{
+    if (R < 0 || V < 1 || (method != 0 && method != 1)) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!q) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        const double T = temp[r];
+        int f = 0;
+        ids[r] = -1;
+        margin[r] = NAN;
+        if (!(T >= 0.0) || isinf(T)) f |= OR_ROW_BAD_TEMP;
+        if (method == 0 && T != 0.0 && !(u[r] >= 0.0 && u[r] < 1.0)) f |= OR_ROW_BAD_UNIFORM;
+        if (!f && T == 0.0) {
+            ids[r] = argmax_row(logits, dtype, (size_t)r * V, V);
+            margin[r] = INFINITY;
+            if (ids[r] < 0) f |= OR_ROW_NONFINITE;
+        } else if (!f) {
+            f |= softmax_row(logits, dtype, (size_t)r * V, V, T, q);
+            if (!f) {
+                if (method == 0) {
+                    ids[r] = cdf_draw(q, V, u[r], &margin[r]);
+                } else {
+                    const struct gumbel_ctx g = {seed_lo, seed_hi, offset, (uint32_t)r};
+                    ids[r] = gumbel_draw(q, V, &g, 0, &margin[r]);
+                }
+            }
+        }
+        if (f) ids[r] = -1;
+        flags[r] = f;
+        free(q);
+    }
+    return fail ? 2 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -742,3 +742,53 @@ def test_clamped_step_loss_finite_differences():
         fd[idx] = 2.0 * (lp - lm) / (2 * h)
     np.testing.assert_allclose(out["grad"], fd, rtol=0, atol=1e-7)
     assert (out["g"] == 0).any() and (out["g"] == -1).any()
+
+
+# ---------------------------------------------------------- draft sampling --
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_draft_sample_multinomial_law_enumeration(T):
+    """Multinomial draft sampling (summary App. G.1, the draft stage draws
+    from q): the inverse-CDF draw is piecewise constant in u with
+    breakpoints C(v) / R; evaluating at every interval midpoint, weighted by
+    the interval length, gives softmax(z / T) (a library routine) to 1e-12."""
+    rng = np.random.default_rng(51)
+    V = 8
+    z = rng.standard_normal(V) * 1.5
+    q = scipy.special.softmax(z / T)
+    edges = np.concatenate([[0.0], np.cumsum(q)])
+    edges[-1] = 1.0
+    mids = 0.5 * (edges[:-1] + edges[1:])
+    out = oracle.draft_sample(np.tile(z, (V, 1)), np.full(V, T), mids)
+    law = np.zeros(V)
+    for i, tok in enumerate(out["ids"]):
+        law[tok] += edges[i + 1] - edges[i]
+    np.testing.assert_allclose(law, q, rtol=0, atol=1e-12)
+    assert np.all(out["flags"] == 0)
+
+
+def test_draft_sample_hand_fixture_and_greedy():
+    """The V = 3 bonus-draw fixture (C = (0.5, 0.8, 1.0)) applies to the draft
+    draw; T = 0 is the arg max with ties to the smaller index; bad
+    temperature and uniform are flagged."""
+    z = np.log(np.array([[0.5, 0.3, 0.2]] * 3))
+    out = oracle.draft_sample(z, np.ones(3), np.array([0.3, 0.79, 0.81]))
+    assert list(out["ids"]) == [0, 1, 2]
+    zz = np.array([[1.0, 3.0, 3.0, -1.0], [0.0, 0.0, 0.0, 0.0]])
+    g = oracle.draft_sample(zz, np.zeros(2), np.array([7.0, 7.0]))
+    assert list(g["ids"]) == [1, 0] and np.all(g["flags"] == 0)
+    bad = oracle.draft_sample(zz, np.array([-1.0, 1.0]), np.array([0.5, 1.0]))
+    assert list(bad["flags"]) == [oracle.ROW_BAD_TEMP, oracle.ROW_BAD_UNIFORM] and list(bad["ids"]) == [-1, -1]
+
+
+def test_draft_sample_gumbel_law():
+    """Gumbel-max draft sampling (summary App. G.2, vLLM): chi-square of
+    30,000 rows with independent streams against softmax(z / T)."""
+    V, R, T = 8, 30000, 0.8
+    z = np.random.default_rng(52).standard_normal(V) * 1.3
+    out = oracle.draft_sample(np.tile(z, (R, 1)), np.full(R, T), method="gumbel", seed=77, offset=5)
+    ok, chi2 = _chi2_ok(np.bincount(out["ids"], minlength=V), scipy.special.softmax(z / T))
+    assert ok, chi2
+    # the draw is the arg max of ln q + G over the row's own noise stream
+    g = oracle.gumbel_noise(77, 5, 3, 0, 0, V)
+    assert out["ids"][3] == int(np.argmax(np.log(scipy.special.softmax(z / T)) + g))
