@@ -19,21 +19,23 @@ from typing import NamedTuple, Optional
 from . import build as _build
 
 __all__ = [
-    "mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_row_stats", "mtp_rs_diagnostics",
-    "mtp_tv_loss_fwd_bwd",
+    "mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_draft_sample", "mtp_row_stats",
+    "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex",
     "mtp_query_plan", "mtp_status_string", "MTPError", "load_library",
-    "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "ROW_NONFINITE", "ROW_BAD_ID",
-    "ROW_BAD_TEMP", "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
+    "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "SampleResult", "ROW_NONFINITE",
+    "ROW_BAD_ID", "ROW_BAD_TEMP", "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
 ]
 
 ROW_NONFINITE, ROW_BAD_ID, ROW_BAD_TEMP, ROW_ZERO_MASS, ROW_BAD_UNIFORM, ROW_TIMEOUT = 1, 2, 4, 8, 16, 32
 ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_TIMEOUT
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_row_stats", "mtp_rs_diagnostics",
-                    "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_query_plan", "mtp_status_string")
+EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_draft_sample", "mtp_row_stats",
+                    "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_query_plan",
+                    "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
-            "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9}
+            "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9,
+            "draft_sample": 10}
 
 _lib = None
 
@@ -66,6 +68,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_to_verify.restype = I
     lib.mtp_row_stats.argtypes = [P, P, I, P, I, I, I, P, P, P, P]
     lib.mtp_row_stats.restype = I
+    lib.mtp_draft_sample.argtypes = [P, I, P, P, I, ctypes.c_uint64, ctypes.c_uint32, I, I, P, P, P]
+    lib.mtp_draft_sample.restype = I
     lib.mtp_tv_loss_ex.argtypes = [P, P, I, F, I, I, I, F, I, I, F, P, P, P, P, P]
     lib.mtp_tv_loss_ex.restype = I
     lib.mtp_gumbel_verify.argtypes = [P, P, I, P, P, P, ctypes.c_uint64, ctypes.c_uint32, I, I, I, P, P, P, P]
@@ -264,6 +268,43 @@ def mtp_gumbel_verify(target_logits, draft_logits, draft_ids, temperature, unifo
         _ptr(out.accept_len), _ptr(out.row_flags), _stream(dev, stream))
     if rc:
         raise MTPError("mtp_gumbel_verify", rc)
+    return out
+
+
+class SampleResult(NamedTuple):
+    ids: "object"        # [R] int32 (-1 for a flagged row)
+    row_flags: "object"  # [R] int32
+
+
+def mtp_draft_sample(draft_logits, temperature, uniforms=None, *, method: str = "multinomial", seed: int = 0,
+                     offset: int = 0, out: Optional[SampleResult] = None, stream=None) -> SampleResult:
+    """One draft token per row of logits [..., V] (flattened to [R, V]) from
+    softmax(z / T): inverse CDF with uniforms [R] ("multinomial") or the
+    Gumbel-max draw with in-kernel Philox noise ("gumbel"); T = 0 is greedy."""
+    torch = _torch()
+    dev = draft_logits.device
+    V = draft_logits.shape[-1]
+    R = draft_logits.numel() // V if V else 0
+    _check(draft_logits, "draft_logits", dev)
+    _check(temperature, "temperature", dev, torch.float32)
+    if temperature.numel() != R:
+        raise ValueError(f"temperature must have {R} entries")
+    m = {"multinomial": 0, "gumbel": 1}[method]
+    if m == 0:
+        if uniforms is None:
+            raise ValueError("the multinomial draw needs uniforms")
+        _check(uniforms, "uniforms", dev, torch.float32)
+        if uniforms.numel() != R:
+            raise ValueError(f"uniforms must have {R} entries")
+    if out is None:
+        out = SampleResult(torch.empty((R,), dtype=torch.int32, device=dev),
+                           torch.empty((R,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_draft_sample(
+        _ptr(draft_logits), _dtype_code(draft_logits), _ptr(temperature), _ptr(uniforms) if m == 0 else None, m,
+        int(seed) & ((1 << 64) - 1), int(offset) & 0xFFFFFFFF, R, V, _ptr(out.ids), _ptr(out.row_flags),
+        _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_draft_sample", rc)
     return out
 
 

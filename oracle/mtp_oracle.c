@@ -919,7 +919,9 @@ int oracle_draft_sample(const void *logits, int dtype, const double *temp, const
         ids[r] = -1;
         margin[r] = NAN;
         if (!(T >= 0.0) || isinf(T)) f |= OR_ROW_BAD_TEMP;
-        if (method == 0 && T != 0.0 && !(u[r] >= 0.0 && u[r] < 1.0)) f |= OR_ROW_BAD_UNIFORM;
+        /* the uniform is checked on every row, greedy ones included, like the
+         * final uniform of verification */
+        if (method == 0 && !(u[r] >= 0.0 && u[r] < 1.0)) f |= OR_ROW_BAD_UNIFORM;
         if (!f && T == 0.0) {
             ids[r] = argmax_row(logits, dtype, (size_t)r * V, V);
             margin[r] = INFINITY;

@@ -775,8 +775,10 @@ def test_draft_sample_hand_fixture_and_greedy():
     out = oracle.draft_sample(z, np.ones(3), np.array([0.3, 0.79, 0.81]))
     assert list(out["ids"]) == [0, 1, 2]
     zz = np.array([[1.0, 3.0, 3.0, -1.0], [0.0, 0.0, 0.0, 0.0]])
-    g = oracle.draft_sample(zz, np.zeros(2), np.array([7.0, 7.0]))
+    g = oracle.draft_sample(zz, np.zeros(2), np.array([0.5, 0.5]))
     assert list(g["ids"]) == [1, 0] and np.all(g["flags"] == 0)
+    # greedy rows draw nothing, but their uniform is still checked (as in verification)
+    assert list(oracle.draft_sample(zz, np.zeros(2), np.array([7.0, 0.5]))["flags"]) == [oracle.ROW_BAD_UNIFORM, 0]
     bad = oracle.draft_sample(zz, np.array([-1.0, 1.0]), np.array([0.5, 1.0]))
     assert list(bad["flags"]) == [oracle.ROW_BAD_TEMP, oracle.ROW_BAD_UNIFORM] and list(bad["ids"]) == [-1, -1]
 
