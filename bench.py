@@ -17,7 +17,8 @@ metric through the public API with pinned host buffers: host-to-device copy
 of the step's inputs, the call, and the device-to-host copy of its outputs.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
-       [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss,tvshared]
+       [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,sample192,gsample192,tvloss,
+                    tvshared]
 Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -171,7 +172,8 @@ def alg_bytes_verify(accept_len: np.ndarray, gamma: int, V: int, es: int, stats:
 # Workloads that run another call on the inputs of a named configuration:
 # (input config, call).
 STATS_WORKLOADS = {"stats256": ("deep256", "stats"), "diag256": ("deep256", "diag"),
-                   "to64": ("verify64", "to"), "gumbel64": ("verify64", "gumbel")}
+                   "to64": ("verify64", "to"), "gumbel64": ("verify64", "gumbel"),
+                   "sample192": ("verify64", "sample"), "gsample192": ("verify64", "gsample")}
 
 
 class VerifyWorkload:
@@ -187,6 +189,7 @@ class VerifyWorkload:
         self.name, self.device = name, device
         self.B, self.gamma, self.V, self.es = x.B, x.gamma, x.V, x.esize
         self.stats = x.want_stats or self.kind in ("stats", "diag")
+        self.sample_args = None
 
         def up(a):
             if a.dtype == np.uint16:
@@ -211,6 +214,16 @@ class VerifyWorkload:
             o = self.mtp.mtp_to_verify(t, d, T, u, out=o, stream=stream)
         elif self.kind == "gumbel":
             o = self.mtp.mtp_gumbel_verify(t, d, ids, T, u, 1234, i % self.copies, out=o, stream=stream)
+        elif self.kind in ("sample", "gsample"):
+            if self.sample_args is None:
+                self.sample_args = [None] * self.copies
+            if self.sample_args[i % self.copies] is None:
+                # per row: the sequence's temperature and one uniform per draft step
+                self.sample_args[i % self.copies] = (T.repeat_interleave(self.gamma).contiguous(),
+                                                     u[:, :self.gamma].reshape(-1).contiguous())
+            Tr, ur = self.sample_args[i % self.copies]
+            o = self.mtp.mtp_draft_sample(d, Tr, ur, method="multinomial" if self.kind == "sample" else "gumbel",
+                                          seed=4321, offset=i % self.copies, out=o, stream=stream)
         else:
             o = self.mtp.mtp_rs_verify(t, d, ids, T, u, with_stats=self.stats, out=o, stream=stream)
         self.outs[i % self.copies] = o
@@ -218,11 +231,14 @@ class VerifyWorkload:
     def alg_bytes(self) -> int:
         if self.kind in ("stats", "diag"):
             return self.bytes_full
+        if self.kind in ("sample", "gsample"):
+            return self.B * self.gamma * self.V * self.es  # every draft row once
         n = self.outs[0].accept_len.cpu().numpy()
         return alg_bytes_verify(n, self.gamma, self.V, self.es, self.stats)
 
     def plan_op(self) -> str:
-        return {"stats": "row_stats", "diag": "diagnostics", "to": "to_verify", "gumbel": "gumbel_verify"}.get(
+        return {"stats": "row_stats", "diag": "diagnostics", "to": "to_verify", "gumbel": "gumbel_verify",
+                "sample": "draft_sample", "gsample": "draft_sample"}.get(
             self.kind, "verify_stats" if self.stats else "verify")
 
     def describe(self) -> str:
@@ -239,7 +255,10 @@ class VerifyWorkload:
                            "rs_better) on the deep256 inputs: B=256 gamma=7 V=151936 fp32",
                 "to64": "target-only verification (arg max drafts, accept iff u < p(yhat)) on the verify64 inputs",
                 "gumbel64": "rejection sampling with the Gumbel-max final draw (in-kernel Philox noise) on the "
-                            "verify64 inputs"}[self.name]
+                            "verify64 inputs",
+                "sample192": "draft sampling by inverse CDF: the 192 draft rows (64 x 3) of verify64, V=151936 bf16",
+                "gsample192": "draft sampling by Gumbel-max (in-kernel Philox noise): the 192 draft rows of verify64"
+                }[self.name]
 
 
 class TVWorkload:
@@ -515,7 +534,7 @@ def run_cuda(args, world, rank, local, pg):
 def VerifyWorkloadBytes(name: str) -> int:
     return {"verify64": 64 * 7 * 151936 * 2, "rl512": 512 * 7 * 151936 * 2, "deep256": 256 * 15 * 151936 * 4,
             "stats256": 256 * 15 * 151936 * 4, "diag256": 256 * 15 * 151936 * 4, "to64": 64 * 7 * 151936 * 2,
-            "gumbel64": 64 * 7 * 151936 * 2}[name]
+            "gumbel64": 64 * 7 * 151936 * 2, "sample192": 192 * 151936 * 2, "gsample192": 192 * 151936 * 2}[name]
 
 
 def main():
@@ -524,7 +543,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,tvloss,tvshared")
+    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,sample192,"
+                                           "gsample192,tvloss,tvshared")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")

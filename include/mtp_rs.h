@@ -173,6 +173,29 @@ int mtp_gumbel_verify(const void *target_logits, const void *draft_logits, mtp_d
                       int32_t *row_flags, mtp_stream_t stream);
 
 /*
+ * mtp_draft_sample -- the draft stage of production rejection sampling [BB
+ * App. G: draft tokens are drawn from q, G.1 multinomial (SGLang), G.2
+ * Gumbel-max (vLLM)]: one token per row of draft_logits [R, V] (R = B x gamma
+ * rows for a batch of MTP steps, any row order) from q_r = softmax(z_r / T_r).
+ *   method 0: inverse CDF with uniforms [R] in [0, 1): the smallest v with
+ *             sum_{w <= v} q_w > u_r (ascending index; if rounding leaves
+ *             none, the last v with q_v > 0);
+ *   method 1: Gumbel-max arg max_v [ln q_v + G_v], the noise of
+ *             mtp_gumbel_verify with counter (v / 4, 0, r, offset) under key
+ *             seed; uniforms is not read (may be NULL).
+ *   T_r = 0: greedy arg max (ties to the smallest index).
+ *   out_ids [R] int32 (-1 for a flagged row), row_flags [R] or NULL
+ *   (BAD_TEMP, BAD_UNIFORM, NONFINITE).
+ * Requirements: 16-byte aligned base and V a multiple of 16 / esize (else
+ * MTP_ERR_MISALIGNED).  Each row is read once from HBM plus, for the draw, a
+ * second time shortly after (inverse CDF: one chunk of the row; Gumbel-max:
+ * the row, mostly from L2).
+ */
+int mtp_draft_sample(const void *draft_logits, mtp_dtype dtype, const float *temperature, const float *uniforms,
+                     int method, uint64_t seed, uint32_t offset, int R, int V, int32_t *out_ids,
+                     int32_t *row_flags, mtp_stream_t stream);
+
+/*
  * mtp_row_stats -- per-position overlap and target entropy without
  * decisions [BB §3, §8: alpha = sum_v min(p_v, q_v) = 1 - TV; entropy
  * H(p) = -sum_v p_v log p_v in nats].
@@ -273,12 +296,13 @@ int mtp_tv_loss_ex(const void *target_logits, const void *draft_logits, mtp_dtyp
  * mtp_rs_verify forced onto the cluster-resident kernel, 5 =
  * mtp_tv_loss_fwd_bwd forced onto the cluster-resident kernel, 6 =
  * mtp_rs_diagnostics, 7 = mtp_row_stats forced onto the cluster-resident
- * kernel, 8 = mtp_to_verify, 9 = mtp_gumbel_verify.  units = B
+ * kernel, 8 = mtp_to_verify, 9 = mtp_gumbel_verify, 10 = mtp_draft_sample
+ * (units = rows).  units = B
  * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
  * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
  * per CTA), resident_drafts (cluster-resident TV kernel: draft slices kept on
- * chip; ops 0, 8, 9: chunk slots per warp of the streaming kernel, 0 when the call
+ * chip; ops 0, 8, 9, 10: chunk slots per warp of the streaming kernel, 0 when the call
  * would use the cluster-resident kernel; else 0).
  * Returns the status the call's planning step would return.
  */

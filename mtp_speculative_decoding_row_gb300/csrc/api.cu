@@ -582,6 +582,47 @@ extern "C" int mtp_gumbel_verify(const void *target_logits, const void *draft_lo
     return launch(p.func, p, &A, stream);
 }
 
+extern "C" int mtp_draft_sample(const void *draft_logits, mtp_dtype dtype, const float *temperature,
+                                const float *uniforms, int method, uint64_t seed, uint32_t offset, int R, int V,
+                                int32_t *out_ids, int32_t *row_flags, mtp_stream_t stream) {
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (R < 0 || V < 1 || (method != 0 && method != 1)) return MTP_ERR_INVALID_ARG;
+    if (R == 0) return MTP_OK;
+    if (!draft_logits || !temperature || !out_ids || (method == 0 && !uniforms)) return MTP_ERR_INVALID_ARG;
+    if (!aligned16(draft_logits)) return MTP_ERR_MISALIGNED;
+    const int es = esize(dtype);
+    if (V % (16 / es) != 0) return MTP_ERR_MISALIGNED;
+    int dev;
+    if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    // each row is a one-row sequence of the streaming verify kernel: no draft
+    // step, and its final draw (the bonus) samples the row
+    const int mode = method == 0 ? 0 : 2;
+    Plan p;
+    if (!plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, 0, R, p, mode)) return MTP_ERR_NO_DEVICE;
+    VerifyArgs A = {};
+    A.target = draft_logits;
+    A.draft = draft_logits;
+    A.ids = nullptr;
+    A.temp = temperature;
+    A.unif = method == 0 ? uniforms : nullptr;
+    A.B = R;
+    A.gamma = 0;
+    A.V = V;
+    A.aligned = 1;
+    A.streams = 1;
+    A.ring = p.ring;
+    A.depth = 0;
+    A.seg_vectors = p.seg_vectors;
+    A.tokens = out_ids;
+    A.accept_len = nullptr;
+    A.flags = row_flags;
+    A.yhat = nullptr;
+    A.seed_lo = static_cast<uint32_t>(seed);
+    A.seed_hi = static_cast<uint32_t>(seed >> 32);
+    A.offset = offset;
+    return launch(p.func, p, &A, stream);
+}
+
 extern "C" int mtp_row_stats(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
                              const float *temperature, int B, int gamma, int V, float *alpha, float *entropy,
                              int32_t *row_flags, mtp_stream_t stream) {
@@ -667,7 +708,7 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
                               int *clusters, int *smem_bytes, int *resident_drafts) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
-    if (op < 0 || op > 9 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (op < 0 || op > 10 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
@@ -677,6 +718,11 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
     if (op == 3 && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
     if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
+    if (op == 10) {  // draft sampling (inverse CDF): one-row sequences of the streaming kernel
+        if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
+        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, 0);
+        if (!ok) return MTP_ERR_NO_DEVICE;
+    }
     if (op == 8 || op == 9) {  // target-only verify, Gumbel-max verify: streaming kernel only
         if (gamma > stream_max_gamma() || V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
         ok = streamed = plan_stream(dev, d, V, es, gamma, units, p, op == 8 ? 1 : 2);
@@ -695,7 +741,7 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
         ok = tv ? plan_tv(dev, func, V, es, gamma, units, p) : plan_row(dev, func, V, es, units, p);
     }
     if (!ok) return MTP_ERR_NO_DEVICE;
-    if (streamed) p.nres = (op == 0 || op == 8 || op == 9) ? p.ring : 0;
+    if (streamed) p.nres = (op == 0 || op >= 8) ? p.ring : 0;
     if (cluster_size) *cluster_size = p.C;
     if (clusters) *clusters = p.clusters;
     if (smem_bytes) *smem_bytes = static_cast<int>(p.smem);

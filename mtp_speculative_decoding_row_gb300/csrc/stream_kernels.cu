@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
         y = 0;
         T = 1.f;
         if (b < A.B) {
-            if (c.lane <= g) u = __ldg(A.unif + static_cast<size_t>(b) * (g + 1) + c.lane);
+            if (A.unif && c.lane <= g) u = __ldg(A.unif + static_cast<size_t>(b) * (g + 1) + c.lane);
             if (MODE != M_TO && c.lane < g) y = __ldg(A.ids + static_cast<size_t>(b) * g + c.lane);
             T = __ldg(A.temp + b);
         }
@@ -1280,7 +1280,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
             if (MODE == M_TO && A.yhat && c.lane < g)
                 A.yhat[static_cast<size_t>(b) * g + c.lane] = (!err && c.lane < reached) ? my_y : -1;
             if (c.lane == 0) {
-                A.accept_len[b] = err ? -1 : n;
+                if (A.accept_len) A.accept_len[b] = err ? -1 : n;
                 if (A.flags) A.flags[b] = flags;
             }
         }

@@ -343,6 +343,71 @@ def test_gumbel_verify_full_config():
     assert rep["exact"] + rep["near_margin"] == x.B and rep["near_margin"] <= 2
 
 
+# ------------------------------------------------------- draft sampling ----
+
+def _draft_rows(V, dtype, gamma, seed, B=16):
+    x = W.verify_inputs(f"ds{V}", B, gamma, V, dtype, seed, family="sigma", sigmas=np.linspace(0.4, 7.0, B),
+                        delta=0.4, temperature=np.linspace(0.6, 1.3, B))
+    z = x.draft.reshape(B * gamma, V)
+    T = np.repeat(x.temperature, gamma).astype(np.float32)
+    T[5::11] = 0.0  # greedy rows
+    u = x.uniforms[:, :gamma].reshape(-1).copy()
+    return z, T, u
+
+
+def _check_draft(z, T, u, method, seed, offset, dtype, what):
+    import mtp_speculative_decoding_row_gb300 as mtp
+    out = mtp.mtp_draft_sample(to_dev(z), to_dev(T), to_dev(u), method=method, seed=seed, offset=offset)
+    torch.cuda.synchronize()
+    ids, flags = out.ids.cpu().numpy(), out.row_flags.cpu().numpy()
+    o = oracle.draft_sample(z, T, u, method=method, seed=seed, offset=offset)
+    np.testing.assert_array_equal(flags, o["flags"], err_msg=what)
+    lim = compare.GUMBEL_MARGIN if method == "gumbel" else compare.MARGIN
+    near = o["margin"] < lim
+    bad = (ids != o["ids"]) & ~near
+    assert not bad.any(), (what, np.nonzero(bad)[0][:8], ids[bad][:8], o["ids"][bad][:8])
+    # a draw within rounding of a CDF breakpoint may take the neighbouring
+    # index (flat rows at large V put many draws there); a near-tie of two
+    # Gumbel keys may take the other key's index
+    moved = (ids != o["ids"]) & near
+    assert np.all((ids[moved] >= 0) & (ids[moved] < z.shape[1])), what
+    if method == "multinomial":
+        assert np.all(np.abs(ids[moved] - o["ids"][moved]) == 1), (what, ids[moved], o["ids"][moved])
+    return ids, o
+
+
+@pytest.mark.parametrize("method", ["multinomial", "gumbel"])
+@pytest.mark.parametrize("V,dtype,C", [(1024, "f32", None), (4096, "bf16", 4), (40000, "f32", 16),
+                                       (30000, "bf16", 1), (151936, "bf16", None)])
+def test_draft_sample(V, dtype, C, method):
+    """One draft token per row from softmax(z / T): inverse CDF with the
+    caller's uniforms, or Gumbel-max with in-kernel Philox noise; T = 0
+    rows are greedy."""
+    z, T, u = _draft_rows(V, dtype, 3, 6000 + V)
+    with env(MTP_RS_CLUSTER=C):
+        ids, o = _check_draft(z, T, u, method, 99, 4, dtype, f"draft sample V={V} {dtype} C={C} {method}")
+    assert len(np.unique(ids)) > len(ids) // 4  # rows differ: the draws are not all one token
+
+
+def test_draft_sample_bad_rows_and_full_size():
+    """Bad temperature / uniform / NaN rows in between good ones, and the
+    verify64 draft rows (192 rows of V = 151,936 bf16) against the oracle."""
+    z, T, u = _draft_rows(8192, "f32", 2, 6100, B=20)
+    T[3] = -1.0
+    u[7] = 1.5
+    z[11, 17] = np.nan
+    for method in ("multinomial", "gumbel"):
+        ids, o = _check_draft(z, T, u, method, 5, 0, "f32", f"bad rows {method}")
+        assert ids[3] == -1 and ids[11] == -1
+        assert (ids[7] == -1) == (method == "multinomial")
+    x = W.config("verify64")
+    z = x.draft.reshape(-1, x.V)
+    T = np.repeat(x.temperature, x.gamma).astype(np.float32)
+    u = x.uniforms[:, :x.gamma].reshape(-1).copy()
+    for method in ("multinomial", "gumbel"):
+        _check_draft(z, T, u, method, 2026, 1, "bf16", f"verify64 rows {method}")
+
+
 # ------------------------------------------------------- diagnostics -------
 
 def _logit_scale(x):
