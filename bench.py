@@ -177,7 +177,7 @@ STATS_WORKLOADS = {"stats256": ("deep256", "stats"), "diag256": ("deep256", "dia
 
 
 class VerifyWorkload:
-    def __init__(self, name: str, device, copies: int):
+    def __init__(self, name: str, device, copies: int, deep_b=None):
         import torch
 
         import workloads as W
@@ -186,6 +186,9 @@ class VerifyWorkload:
         self.mtp = mtp
         base_name, self.kind = STATS_WORKLOADS.get(name, (name, "verify"))
         self.x = x = W.config(base_name)
+        if deep_b and base_name == "deep256" and deep_b < x.B:
+            x = W.subset(x, deep_b)  # the first deep_b sequences (profiling cases)
+            self.x = x
         self.name, self.device = name, device
         self.B, self.gamma, self.V, self.es = x.B, x.gamma, x.V, x.esize
         self.stats = x.want_stats or self.kind in ("stats", "diag")
@@ -455,7 +458,7 @@ def run_cuda(args, world, rank, local, pg):
         else:
             per_copy = VerifyWorkloadBytes(name)
             copies = max(2, math.ceil(4 * L2_BYTES / per_copy))
-            wl = VerifyWorkload(name, device, min(copies, 8))
+            wl = VerifyWorkload(name, device, min(copies, 8), args.deep_b)
             steps = args.steps
         sampler = ClockSampler(gpu_id) if name == names[0] else None
         barrier(pg, device)
@@ -548,6 +551,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")
+    ap.add_argument("--deep-b", type=int, default=None,
+                    help="sequences of the deep256-based workloads (default 256; smaller for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

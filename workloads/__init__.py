@@ -333,6 +333,12 @@ def tvloss_shared_inputs_device(name: str, N: int, gamma: int, V: int, c: int, d
                         {"sigma": sig, "delta": delta, "backend": "torch-cuda", "layout": "shared"})
 
 
+def subset(x: VerifyInputs, B: int) -> VerifyInputs:
+    """The first B sequences of a verify workload (same rows and parameters)."""
+    return VerifyInputs(x.name, B, x.gamma, x.V, x.dtype, x.target[:B], x.draft[:B], x.draft_ids[:B],
+                        x.temperature[:B], x.uniforms[:B], x.want_stats, dict(x.meta))
+
+
 # The five workloads: (index c, description).
 CONFIG_NAMES = ["tiny", "verify64", "rl512", "deep256", "tvloss"]
 
