@@ -57,6 +57,7 @@ def _load():
             lib.oracle_philox4x32_10.argtypes = [P, P, P]
             lib.oracle_gumbel_noise.argtypes = [U32, U32, U32, U32, I, I, I, P]
             lib.oracle_gumbel_verify.argtypes = [P, P, I, P, P, P, U32, U32, U32, I, I, I, P, P, P, P, P]
+            lib.oracle_tv_loss_topk.argtypes = [P, P, P, I, D, I, I, I, I, D, I, I, D, P, P, P, P, P, P]
             lib.oracle_draft_sample.argtypes = [P, I, P, P, I, U32, U32, U32, I, I, P, P, P]
             lib.oracle_num_threads.argtypes = []
             for f in (lib.oracle_softmax, lib.oracle_verify, lib.oracle_row_stats, lib.oracle_tv_loss,
@@ -212,6 +213,32 @@ def gumbel_verify(target, draft, draft_ids, temperature, uniforms, seed: int, of
                                       _ptr(out["gumbel_margin"]))
     if rc:
         raise RuntimeError(f"oracle_gumbel_verify failed ({rc})")
+    return out
+
+
+def tv_loss_topk(values, idx, draft, temperature: float = 1.0, grad_scale: float = 1.0, with_grad: bool = True,
+                 tie_le: bool = True, clamp_tau=None) -> dict:
+    """TV loss against top-K target distributions: values [N, gamma, K]
+    (target logits, same storage as draft) at indices idx [N, gamma, K] of
+    the vocabulary, renormalised over the K entries; draft [N, gamma, V].
+    Returns loss [N], alpha, S, g [N, gamma], flags [N] and grad."""
+    v, dt = _logits(values)
+    d, dt2 = _logits(draft)
+    assert dt == dt2
+    N, gamma, V = d.shape
+    K = v.shape[-1]
+    assert v.shape == (N, gamma, K)
+    ix = np.ascontiguousarray(idx, dtype=np.int32).reshape(N, gamma, K)
+    out = {"loss": np.empty(N), "alpha": np.empty((N, gamma)), "S": np.empty((N, gamma)),
+           "g": np.empty((N, gamma)), "flags": np.empty(N, np.int32)}
+    if with_grad:
+        out["grad"] = np.empty((N, gamma, V))
+    kind, tau = (0, 0.0) if clamp_tau is None else (1, float(clamp_tau))
+    rc = _load().oracle_tv_loss_topk(_ptr(v), _ptr(ix), _ptr(d), dt, float(temperature), N, gamma, K, V,
+                                     float(grad_scale), int(tie_le), kind, tau, _ptr(out["loss"]), _ptr(out["alpha"]),
+                                     _ptr(out["S"]), _ptr(out["g"]), _ptr(out.get("grad")), _ptr(out["flags"]))
+    if rc:
+        raise RuntimeError(f"oracle_tv_loss_topk failed ({rc})")
     return out
 
 

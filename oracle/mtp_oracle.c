@@ -52,6 +52,9 @@
  *   - Shared target rows (the MTP layout): with target [N + gamma - 1, V],
  *     pair (t, k) uses target row t + k, the target model's distribution at
  *     the token that draft step k of position t predicts.
+ *   - Top-K target (App. F): the target of a pair is given as its K largest
+ *     logits and their indices; the target distribution is their softmax,
+ *     renormalised over the K entries; the draft keeps its full softmax.
  *   - App. F clamped loss: per position the sum over steps of clamp(1 -
  *     alpha_k, 0, tau_max); its derivative in alpha_k is -1 strictly inside
  *     (0, tau_max) and 0 elsewhere (the subgradient 0 at the two kinks).
@@ -939,6 +942,107 @@ int oracle_draft_sample(const void *logits, int dtype, const double *temp, const
         }
         if (f) ids[r] = -1;
         flags[r] = f;
+        free(q);
+    }
+    return fail ? 2 : 0;
+}
+
+/*
+ * Top-K TV loss [BB, App. F: "an optional top-K path reduces memory from
+ * O(|V|) to O(K)"]: the detached target of pair (t, k) is cached as its K
+ * largest logits (values [N, gamma, K] in storage `dtype`) and their
+ * vocabulary indices (idx [N, gamma, K], distinct, in [0, V)).  The target
+ * distribution is the softmax over those K entries at temperature T,
+ * renormalised (p~ = 0 elsewhere); q = softmax(z_d / T) over the full row.
+ * alpha~_k = sum_e min(p~_e, q_{idx_e}), S~_k = sum over entries with
+ * q_{idx_e} <= p~_e of q_{idx_e}; the loss (e2e, or the clamped per-step
+ * loss) and the gradient are those of oracle_tv_loss_ex with p~ in place of
+ * p: grad_j = scale g_k (1/T) q_j (1[j is an entry with q_j <= p~_j] - S~_k).
+ * An index outside [0, V) sets BAD_ID; a NaN / +inf value or draft logit, or
+ * an all -inf row, sets NONFINITE.
+ */
+int oracle_tv_loss_topk(const void *values, const int32_t *idx, const void *draft, int dtype, double T, int N,
+                        int gamma, int K, int V, double grad_scale, int tie_le, int loss_kind, double tau_max,
+                        double *loss, double *alpha, double *S, double *g, double *grad, int32_t *flags)
+{
+    if (N < 0 || gamma < 1 || V < 1 || K < 1) return 1;
+    if (loss_kind == 1 && !(tau_max >= 0.0)) return 1;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < N; ++t) {
+        double *q = (double *)malloc(sizeof(double) * ((size_t)V + (size_t)K));
+        if (!q) {
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        double *pk = q + V;
+        int f = (!(T > 0.0) || isinf(T)) ? OR_ROW_BAD_TEMP : 0;
+        double *a = alpha + (size_t)t * gamma, *s = S + (size_t)t * gamma, *gk = g + (size_t)t * gamma;
+        for (int k = 0; k < gamma && !f; ++k) {
+            const size_t base = ((size_t)t * gamma + k) * K;
+            for (int e = 0; e < K; ++e)
+                if (idx[base + e] < 0 || idx[base + e] >= V) f |= OR_ROW_BAD_ID;
+            if (f) break;
+            f |= softmax_row(values, dtype, base, K, T, pk);
+            f |= softmax_row(draft, dtype, ((size_t)t * gamma + k) * V, V, T, q);
+            if (f) break;
+            double ak = 0.0, sk = 0.0;
+            for (int e = 0; e < K; ++e) {
+                const double qv = q[idx[base + e]];
+                ak += qv < pk[e] ? qv : pk[e];
+                if (tie_le ? (qv <= pk[e]) : (qv < pk[e])) sk += qv;
+            }
+            a[k] = ak;
+            s[k] = sk;
+        }
+        flags[t] = f;
+        if (f) {
+            loss[t] = NAN;
+            for (int k = 0; k < gamma; ++k) a[k] = s[k] = gk[k] = NAN;
+            if (grad)
+                for (size_t e = 0; e < (size_t)gamma * V; ++e) grad[(size_t)t * gamma * V + e] = NAN;
+            free(q);
+            continue;
+        }
+        double l = 0.0;
+        if (loss_kind == 1) {
+            for (int k = 0; k < gamma; ++k) {
+                const double d = 1.0 - a[k];
+                l += d < 0.0 ? 0.0 : (d > tau_max ? tau_max : d);
+                gk[k] = (d > 0.0 && d < tau_max) ? -1.0 : 0.0;
+            }
+        } else {
+            for (int m = 0; m < gamma; ++m) {
+                double prod = 1.0;
+                for (int i = 0; i <= m; ++i) prod *= a[i];
+                l -= prod;
+            }
+            for (int k = 0; k < gamma; ++k) {
+                double d = 0.0;
+                for (int m = k; m < gamma; ++m) {
+                    double prod = 1.0;
+                    for (int i = 0; i <= m; ++i)
+                        if (i != k) prod *= a[i];
+                    d -= prod;
+                }
+                gk[k] = d;
+            }
+        }
+        loss[t] = l;
+        if (grad) {
+            for (int k = 0; k < gamma; ++k) {
+                const size_t off = ((size_t)t * gamma + k) * V, base = ((size_t)t * gamma + k) * K;
+                softmax_row(values, dtype, base, K, T, pk);
+                softmax_row(draft, dtype, off, V, T, q);
+                for (int v = 0; v < V; ++v) grad[off + v] = grad_scale * gk[k] * (1.0 / T) * q[v] * (0.0 - s[k]);
+                for (int e = 0; e < K; ++e) {
+                    const int v = idx[base + e];
+                    const double ind = (tie_le ? (q[v] <= pk[e]) : (q[v] < pk[e])) ? 1.0 : 0.0;
+                    grad[off + v] = grad_scale * gk[k] * (1.0 / T) * q[v] * (ind - s[k]);
+                }
+            }
+        }
         free(q);
     }
     return fail ? 2 : 0;

@@ -794,3 +794,73 @@ def test_draft_sample_gumbel_law():
     # the draw is the arg max of ln q + G over the row's own noise stream
     g = oracle.gumbel_noise(77, 5, 3, 0, 0, V)
     assert out["ids"][3] == int(np.argmax(np.log(scipy.special.softmax(z / T)) + g))
+
+
+# ----------------------------------------------------------- top-K TV path --
+
+def _topk(t, K):
+    idx = np.argsort(-t, axis=-1, kind="stable")[..., :K].astype(np.int32)
+    return np.take_along_axis(t, idx, axis=-1), idx
+
+
+def test_topk_with_every_entry_is_the_full_loss():
+    """K = V (a shuffled full list): the top-K loss, alpha, S and gradient
+    equal the full TV loss (App. F top-K path, K = |V|)."""
+    rng = np.random.default_rng(61)
+    N, gamma, V = 3, 3, 40
+    t = rng.standard_normal((N, gamma, V)) * 2
+    d = t + rng.standard_normal((N, gamma, V)) * 0.6
+    perm = np.stack([np.stack([rng.permutation(V) for _ in range(gamma)]) for _ in range(N)]).astype(np.int32)
+    vals = np.take_along_axis(t, perm, axis=-1)
+    a = oracle.tv_loss(t, d, 0.8, 1.5)
+    b = oracle.tv_loss_topk(vals, perm, d, 0.8, 1.5)
+    for key in ("loss", "alpha", "S", "g", "grad"):
+        np.testing.assert_allclose(b[key], a[key], rtol=1e-12, atol=1e-14)
+
+
+def test_topk_is_the_loss_against_the_truncated_target():
+    """The top-K target is the softmax renormalised over its K entries: the
+    same as the full loss with every other target logit at -inf (p = 0), a
+    different code path of the oracle; also for the clamped loss."""
+    rng = np.random.default_rng(62)
+    N, gamma, V, K = 4, 3, 64, 9
+    t = rng.standard_normal((N, gamma, V)) * 2.5
+    d = t + rng.standard_normal((N, gamma, V)) * 0.7
+    vals, idx = _topk(t, K)
+    masked = np.full_like(t, -np.inf)
+    np.put_along_axis(masked, idx, vals, axis=-1)
+    for tau in (None, 0.5):
+        a = oracle.tv_loss(masked, d, 1.1, 2.0, clamp_tau=tau)
+        b = oracle.tv_loss_topk(vals, idx, d, 1.1, 2.0, clamp_tau=tau)
+        for key in ("loss", "alpha", "S", "g", "grad"):
+            np.testing.assert_allclose(b[key], a[key], rtol=1e-12, atol=1e-14)
+    # alpha~ <= 1 and it shrinks with K (less target mass overlaps q)
+    a_small = oracle.tv_loss_topk(*_topk(t, 2), d, 1.1, with_grad=False)["alpha"]
+    assert np.all(a_small <= 1) and np.mean(a_small) < np.mean(oracle.tv_loss_topk(vals, idx, d, 1.1)["alpha"])
+
+
+def test_topk_gradient_finite_differences():
+    """Gradient w.r.t. the draft logits against central differences."""
+    rng = np.random.default_rng(63)
+    N, gamma, V, K, T = 2, 3, 14, 5, 0.9
+    while True:
+        t = rng.standard_normal((N, gamma, V)) * 1.5
+        d = t + rng.standard_normal((N, gamma, V)) * 0.6
+        vals, idx = _topk(t, K)
+        pk = scipy.special.softmax(vals / T, axis=-1)
+        q = scipy.special.softmax(d / T, axis=-1)
+        if np.abs(np.take_along_axis(q, idx, axis=-1) - pk).min() > 2e-4:
+            break
+    out = oracle.tv_loss_topk(vals, idx, d, T, 1.5)
+    h = 1e-6
+    fd = np.empty_like(d)
+    for ix in np.ndindex(d.shape):
+        dp = d.copy()
+        dm = d.copy()
+        dp[ix] += h
+        dm[ix] -= h
+        lp = oracle.tv_loss_topk(vals, idx, dp, T, 1.0, with_grad=False)["loss"].sum()
+        lm = oracle.tv_loss_topk(vals, idx, dm, T, 1.0, with_grad=False)["loss"].sum()
+        fd[ix] = 1.5 * (lp - lm) / (2 * h)
+    np.testing.assert_allclose(out["grad"], fd, rtol=0, atol=1e-7)
+    assert oracle.tv_loss_topk(vals, np.where(idx == idx[0, 0, 0], V, idx), d, T)["flags"][0] == oracle.ROW_BAD_ID
