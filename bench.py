@@ -18,7 +18,7 @@ of the step's inputs, the call, and the device-to-host copy of its outputs.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
        [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,sample192,gsample192,tvloss,
-                    tvshared]
+                    tvshared,tvtopk]
 Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -169,6 +169,8 @@ def alg_bytes_verify(accept_len: np.ndarray, gamma: int, V: int, es: int, stats:
     return int(((n + 1) + np.minimum(n + 1, gamma)).sum()) * V * es
 
 
+TV_WORKLOADS = ("tvloss", "tvshared", "tvtopk")
+
 # Host input sets drawn so far, by configuration name.
 _INPUTS = {}
 
@@ -270,12 +272,17 @@ class VerifyWorkload:
 
 
 class TVWorkload:
-    def __init__(self, device, N=None, shared=False):
+    TOPK = 64  # cached target entries per pair in the top-K workload
+
+    def __init__(self, device, N=None, shared=False, topk=False):
+        import torch
+
         import workloads as W
         import mtp_speculative_decoding_row_gb300 as mtp
 
         self.mtp = mtp
         self.shared = shared
+        self.topk = topk
         if shared:
             N = N or 16384
             self.x = x = W.tvloss_shared_inputs_device("tvshared", N, 3, W.V_QWEN, W.CONFIG_NAMES.index("tvloss"),
@@ -287,11 +294,24 @@ class TVWorkload:
         self.out = None
         self.copies = 1
         self.positions = x.N * x.gamma
+        if topk:
+            # the target cached as its K largest logits per pair (input preparation, not timed)
+            vals, idx = torch.topk(x.target, self.TOPK, dim=-1)
+            self.tk_vals, self.tk_idx = vals.contiguous(), idx.to(torch.int32).contiguous()
+            x.target = None
+            torch.cuda.empty_cache()
         # draft read (2 B) and gradient written (4 B) per (t, k, v); target rows read once
-        tgt = (x.N + x.gamma - 1) * x.V * 2 if shared else x.N * x.gamma * x.V * 2
+        if topk:
+            tgt = x.N * x.gamma * self.TOPK * (2 + 4)
+        else:
+            tgt = (x.N + x.gamma - 1) * x.V * 2 if shared else x.N * x.gamma * x.V * 2
         self.bytes_full = x.N * x.gamma * x.V * (2 + 4) + tgt
 
     def call(self, i: int, stream=None):
+        if self.topk:
+            self.out = self.mtp.mtp_tv_loss_topk(self.tk_vals, self.tk_idx, self.x.draft, self.x.temperature,
+                                                 self.x.grad_scale, out=self.out, stream=stream)
+            return
         self.out = self.mtp.mtp_tv_loss_fwd_bwd(self.x.target, self.x.draft, self.x.temperature, self.x.grad_scale,
                                                 shared_target=self.shared, out=self.out, stream=stream)
 
@@ -299,6 +319,9 @@ class TVWorkload:
         return self.bytes_full
 
     def describe(self) -> str:
+        if self.topk:
+            return (f"e2e TV loss fwd+bwd against top-K targets (K={self.TOPK} cached target logits per pair, "
+                    f"renormalised): N={self.N} positions x gamma=3, V=151936, bf16, fp32 gradient, T=1")
         if self.shared:
             return (f"e2e TV loss fwd+bwd, shared target rows [N+gamma-1, V] (pair (t,k) on row t+k): N={self.N} "
                     "positions x gamma=3, V=151936, bf16 logits, draft = target row + N(0,0.5), fp32 gradient, T=1")
@@ -477,8 +500,8 @@ def run_cuda(args, world, rank, local, pg):
     results = {}
     head = None
     for name in names:
-        if name in ("tvloss", "tvshared"):
-            wl = TVWorkload(device, args.tv_n, shared=name == "tvshared")
+        if name in TV_WORKLOADS:
+            wl = TVWorkload(device, args.tv_n, shared=name == "tvshared", topk=name == "tvtopk")
             steps = max(3, min(args.steps, 20)) if name != names[0] else args.steps
         else:
             per_copy = VerifyWorkloadBytes(name)
@@ -496,7 +519,7 @@ def run_cuda(args, world, rank, local, pg):
         alg = wl.alg_bytes()
         per_launch_s = t["ms_total"] / 1e3 / t["launches"]
         achieved = alg / per_launch_s / 1e9
-        tv = name in ("tvloss", "tvshared")
+        tv = name in TV_WORKLOADS
         plan = mtp.mtp_query_plan("tv_loss" if tv else wl.plan_op(), "bf16" if wl.es == 2 else "f32",
                                   wl.N if tv else wl.B, wl.gamma, wl.V)
         r = {
@@ -520,7 +543,7 @@ def run_cuda(args, world, rank, local, pg):
     name, wl0, t, t_ms, steps, clocks, alg, achieved = head
     # e2e leg on the headline workload
     e2e = None
-    if name not in ("tvloss", "tvshared"):
+    if name not in TV_WORKLOADS:
         wl = VerifyWorkload(name, device, 1)
         e2e = time_e2e(wl, max(3, min(args.steps, 50)), max(3, args.warmup), device)
         e2e["value"] = max_over_ranks(pg, -e2e["value"], device) * -1 * world
@@ -528,7 +551,7 @@ def run_cuda(args, world, rank, local, pg):
     traffic = TRAFFIC.get(name)
     traffic_val = traffic["bytes"] if traffic and traffic.get("csrc") == h else None
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and name not in ("tvloss", "tvshared"):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and name not in TV_WORKLOADS:
         cpu = oracle_verify_rate(name, args.cpu_seconds, 16)
 
     if rank == 0:
@@ -572,7 +595,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,sample192,"
-                                           "gsample192,tvloss,tvshared")
+                                           "gsample192,tvloss,tvshared,tvtopk")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")

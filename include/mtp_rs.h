@@ -290,6 +290,30 @@ int mtp_tv_loss_ex(const void *target_logits, const void *draft_logits, mtp_dtyp
                    float *loss, float *alpha, float *grad_draft_logits, int32_t *row_flags, mtp_stream_t stream);
 
 /*
+ * mtp_tv_loss_topk -- the top-K path of the fused TV loss [BB App. F: "an
+ * optional top-K path reduces memory from O(|V|) to O(K)"]: the detached
+ * target of pair (t, k) is given as its K cached logits target_values
+ * [N, gamma, K] (dtype) at vocabulary indices target_idx [N, gamma, K]
+ * (int32, distinct, in [0, V)).  The target distribution is the softmax of
+ * those K logits at temperature T, renormalised over the K entries (zero
+ * elsewhere); q = softmax(draft[t,k] / T) over the full row.  Then
+ *   alpha~_k = sum_e min(p~_e, q_{idx_e}),  S~_k = sum_{e: q <= p~} q_{idx_e},
+ * the loss is the e2e loss (loss_kind 0) or sum_k clamp(1 - alpha~_k, 0,
+ * tau_max) (loss_kind 1), and the gradient with respect to the draft logits
+ * is that of mtp_tv_loss_fwd_bwd with p~ in place of p.  Outputs and flags
+ * as for mtp_tv_loss_fwd_bwd; an index outside [0, V) flags MTP_ROW_BAD_ID.
+ * Requirements: 1 <= K <= V and gamma <= 8 (else MTP_ERR_INVALID_ARG);
+ * 16-byte aligned draft and gradient bases and V a multiple of 16 / esize
+ * (else MTP_ERR_MISALIGNED).  Bytes per pair: the draft row read once
+ * (plus a re-read from L2), the gradient row written once, 6 K bytes (bf16)
+ * of target entries.
+ */
+int mtp_tv_loss_topk(const void *target_values, const int32_t *target_idx, const void *draft_logits,
+                     mtp_dtype dtype, float temperature, int N, int gamma, int K, int V, float grad_scale,
+                     int loss_kind, float tau_max, float *loss, float *alpha, float *grad_draft_logits,
+                     int32_t *row_flags, mtp_stream_t stream);
+
+/*
  * mtp_query_plan -- the launch plan a call would use on the current device
  * (diagnostics; launches nothing).  op: 0 = mtp_rs_verify, 1 = mtp_rs_verify
  * with statistics, 2 = mtp_row_stats, 3 = mtp_tv_loss_fwd_bwd, 4 =

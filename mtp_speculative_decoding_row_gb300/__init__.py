@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_draft_sample", "mtp_row_stats",
-    "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex",
+    "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_tv_loss_topk",
     "mtp_query_plan", "mtp_status_string", "MTPError", "load_library",
     "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "SampleResult", "ROW_NONFINITE",
     "ROW_BAD_ID", "ROW_BAD_TEMP", "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
@@ -31,8 +31,8 @@ ERROR_BITS = ROW_NONFINITE | ROW_BAD_ID | ROW_BAD_TEMP | ROW_BAD_UNIFORM | ROW_T
 MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_draft_sample", "mtp_row_stats",
-                    "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_query_plan",
-                    "mtp_status_string")
+                    "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_tv_loss_topk",
+                    "mtp_query_plan", "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
             "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9,
             "draft_sample": 10}
@@ -70,6 +70,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_row_stats.restype = I
     lib.mtp_draft_sample.argtypes = [P, I, P, P, I, ctypes.c_uint64, ctypes.c_uint32, I, I, P, P, P]
     lib.mtp_draft_sample.restype = I
+    lib.mtp_tv_loss_topk.argtypes = [P, P, P, I, F, I, I, I, I, F, I, F, P, P, P, P, P]
+    lib.mtp_tv_loss_topk.restype = I
     lib.mtp_tv_loss_ex.argtypes = [P, P, I, F, I, I, I, F, I, I, F, P, P, P, P, P]
     lib.mtp_tv_loss_ex.restype = I
     lib.mtp_gumbel_verify.argtypes = [P, P, I, P, P, P, ctypes.c_uint64, ctypes.c_uint32, I, I, I, P, P, P, P]
@@ -353,6 +355,33 @@ def mtp_rs_diagnostics(target_logits, draft_logits, temperature, *, out: Optiona
         _ptr(out.rs_better), _ptr(out.row_flags), _stream(dev, stream))
     if rc:
         raise MTPError("mtp_rs_diagnostics", rc)
+    return out
+
+
+def mtp_tv_loss_topk(target_values, target_idx, draft_logits, temperature: float = 1.0, grad_scale: float = 1.0, *,
+                     clamp_tau: Optional[float] = None, out: Optional[TVLossResult] = None,
+                     stream=None) -> TVLossResult:
+    """Fused TV loss forward + backward against top-K targets: values and
+    int32 indices [N, gamma, K] of the target's K cached logits (softmax
+    renormalised over them), draft logits [N, gamma, V]."""
+    torch = _torch()
+    dev = draft_logits.device
+    N, gamma, V = draft_logits.shape
+    K = target_values.shape[-1]
+    _check(draft_logits, "draft_logits", dev)
+    _check(target_values, "target_values", dev, draft_logits.dtype, (N, gamma, K))
+    _check(target_idx, "target_idx", dev, torch.int32, (N, gamma, K))
+    if out is None:
+        out = TVLossResult(torch.empty((N,), dtype=torch.float32, device=dev),
+                           torch.empty((N, gamma), dtype=torch.float32, device=dev),
+                           torch.empty((N, gamma, V), dtype=torch.float32, device=dev),
+                           torch.empty((N,), dtype=torch.int32, device=dev))
+    rc = load_library().mtp_tv_loss_topk(
+        _ptr(target_values), _ptr(target_idx), _ptr(draft_logits), _dtype_code(draft_logits), float(temperature), N,
+        gamma, K, V, float(grad_scale), 0 if clamp_tau is None else 1, 0.0 if clamp_tau is None else float(clamp_tau),
+        _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad), _ptr(out.row_flags), _stream(dev, stream))
+    if rc:
+        raise MTPError("mtp_tv_loss_topk", rc)
     return out
 
 

@@ -235,7 +235,7 @@ bool tvs_usable(int V, int es, int gamma) {
     return gamma <= tvs_max_gamma() && V % (16 / es) == 0;
 }
 
-bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) {
+bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, bool topk = false) {
     const int forced = env_cluster();
     int R = env_int("MTP_RS_RING");
     if (R < 2 || R > stream_max_ring()) R = 2;
@@ -257,7 +257,7 @@ bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) 
         const uint32_t smem = tvs_hdr_bytes() + tvs_rec_bytes(gamma, S) + tvs_bits_bytes(gamma, nvs) +
                               static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
         if (smem > cap) continue;
-        const void *func = tvs_kernel(dtype, cv);
+        const void *func = tvs_kernel(dtype, cv, topk);
         if (prepare_func(dev, func) != cudaSuccess) return false;
         const int nc = max_clusters(dev, func, C, smem, tvs_threads());
         if (nc <= 0) continue;
@@ -694,7 +694,50 @@ extern "C" int mtp_tv_loss_ex(const void *target_logits, const void *draft_logit
     A.shared_target = target_layout;
     A.loss_kind = loss_kind;
     A.tau_max = loss_kind == 1 ? tau_max : 0.f;
+    A.topk_idx = nullptr;
+    A.K = 0;
     return launch(func, p, &A, stream);
+}
+
+extern "C" int mtp_tv_loss_topk(const void *target_values, const int32_t *target_idx, const void *draft_logits,
+                                mtp_dtype dtype, float temperature, int N, int gamma, int K, int V, float grad_scale,
+                                int loss_kind, float tau_max, float *loss, float *alpha, float *grad_draft_logits,
+                                int32_t *row_flags, mtp_stream_t stream) {
+    if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (N < 0 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1 || K < 1 || K > V) return MTP_ERR_INVALID_ARG;
+    if (loss_kind != 0 && loss_kind != 1) return MTP_ERR_INVALID_ARG;
+    if (loss_kind == 1 && !(tau_max >= 0.f)) return MTP_ERR_INVALID_ARG;
+    if (N == 0) return MTP_OK;
+    if (!target_values || !target_idx || !draft_logits || !loss || !grad_draft_logits) return MTP_ERR_INVALID_ARG;
+    const int es = esize(dtype);
+    if (!aligned16(draft_logits) || !aligned16(grad_draft_logits) || V % (16 / es) != 0) return MTP_ERR_MISALIGNED;
+    // the streaming TV kernel serves the top-K target: gamma up to its limit
+    if (gamma > tvs_max_gamma()) return MTP_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    Plan p;
+    if (!plan_tvs(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, gamma, N, p, true)) return MTP_ERR_NO_DEVICE;
+    TVArgs A = {};
+    A.target = target_values;
+    A.draft = draft_logits;
+    A.temperature = temperature;
+    A.grad_scale = grad_scale;
+    A.N = N;
+    A.gamma = gamma;
+    A.V = V;
+    A.aligned = 1;
+    A.ring = p.ring;
+    A.seg_vectors = p.seg_vectors;
+    A.loss = loss;
+    A.alpha = alpha;
+    A.grad = grad_draft_logits;
+    A.flags = row_flags;
+    A.shared_target = 0;
+    A.loss_kind = loss_kind;
+    A.tau_max = loss_kind == 1 ? tau_max : 0.f;
+    A.topk_idx = target_idx;
+    A.K = K;
+    return launch(p.func, p, &A, stream);
 }
 
 extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_logits, mtp_dtype dtype,

@@ -49,6 +49,8 @@ struct TVArgs {
     int shared_target;      // 1: target is [N + gamma - 1, V], pair (t, k) on row t + k
     int loss_kind;          // 0: e2e loss; 1: sum_k clamp(1 - alpha_k, 0, tau_max)
     float tau_max;
+    const int32_t *topk_idx;  // top-K mode: [N, gamma, K] vocabulary indices (target = [N, gamma, K] values)
+    int K;
 };
 
 // Modes of the streaming row-pair statistics kernel.
@@ -94,7 +96,8 @@ const void *row_kernel(int dtype, int mode);
 // 2 = rejection sampling with the Gumbel-max final draw
 const void *stream_kernel(int dtype, int cv, int mode);
 const void *tv_kernel(int dtype);
-const void *tvs_kernel(int dtype, int cv);  // streaming TV kernel, cv: 128 or 192
+// streaming TV kernel, cv: 128 or 192; topk: the target is K cached entries per pair
+const void *tvs_kernel(int dtype, int cv, bool topk = false);
 // Streaming row-pair statistics kernel (mode: PairMode), cv: 128 or 192.
 const void *pair_kernel(int dtype, int cv, int mode);
 uint32_t pair_hdr_bytes();

@@ -113,7 +113,7 @@ __device__ __forceinline__ void unit_of(int u, int g, int &kind, int &k) {
 
 // Issue chunk copies while ring slots are free, in the order of unit_of,
 // then the next position.
-template <typename Tin>
+template <typename Tin, bool TOPK>
 __device__ __forceinline__ void tproduce(const TVArgs &A, TC &c) {
     if (c.p_done || c.dead) return;
     while (c.pcount - c.ccount < static_cast<uint32_t>(c.R)) {
@@ -121,11 +121,22 @@ __device__ __forceinline__ void tproduce(const TVArgs &A, TC &c) {
             const int t = c.cid + c.p_ord * c.NC;
             int kind, k;
             unit_of(c.p_u, c.g, kind, k);
+            if (TOPK && kind == P_OVL) {  // top-K overlap passes stream no row
+                if (++c.p_u == 3 * c.g) {
+                    c.p_u = 0;
+                    ++c.p_ord;
+                    if (c.cid + c.p_ord * c.NC >= A.N) {
+                        c.p_done = true;
+                        return;
+                    }
+                }
+                continue;
+            }
             const size_t off = static_cast<size_t>(c.seg_lo) * 16u;
-            c.p_t = kind == P_GRAD ? nullptr
-                                   : (A.shared_target ? tv_row_ptr<Tin>(A.target, t + k, 0, 1, A.V)
-                                                      : tv_row_ptr<Tin>(A.target, t, k, c.g, A.V)) +
-                                         off;
+            c.p_t = (kind == P_GRAD || TOPK) ? nullptr
+                                             : (A.shared_target ? tv_row_ptr<Tin>(A.target, t + k, 0, 1, A.V)
+                                                                : tv_row_ptr<Tin>(A.target, t, k, c.g, A.V)) +
+                                                   off;
             c.p_d = tv_row_ptr<Tin>(A.draft, t, k, c.g, A.V) + off;
         }
         const int cnt = tchunk(c, c.p_c);
@@ -298,7 +309,7 @@ __device__ __forceinline__ void zero_segment(const TC &c, float *row) {
     for (int i = c.lane; i < n4; i += 32) __stcs(o + i, make_float4(0.f, 0.f, 0.f, 0.f));
 }
 
-template <typename Tin, int CV>
+template <typename Tin, int CV, bool TOPK>
 __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
     using St = Store<Tin>;
     constexpr int VEC = St::VEC;
@@ -357,7 +368,7 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
     fence_mbar_init();
     __syncthreads();
     cluster_sync();  // every barrier of the cluster is initialised and armed before any push
-    tproduce<Tin>(A, c);
+    tproduce<Tin, TOPK>(A, c);
 
     for (int t = c.cid; t < A.N; t += c.NC) {
         float *grow = A.grad + static_cast<size_t>(t) * g * static_cast<size_t>(A.V);
@@ -379,26 +390,26 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                     float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
                     int bad = 0;
                     for (int ch = 0; ch < c.nch; ++ch) {
-                        tproduce<Tin>(A, c);
+                        tproduce<Tin, TOPK>(A, c);
                         if (!twait_slot(c)) break;
                         const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
                         const unsigned char *db = tb + CV * 16;
                         const int cnt = tchunk(c, ch);
                         uint4 rt[QV], rd[QV];
                         if (cnt == CV) {
-                            load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
+                            if (!TOPK) load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
                             load_chunk<Tin, true, QV>(db, cnt, c.lane, rd);
                         } else {
-                            load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
+                            if (!TOPK) load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
                             load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
                         }
                         // the maxima consume every loaded register: the slot's
                         // reads are complete before it is handed back
-                        const float cmt = chunk_max<Tin, QV>(rt), cmd = chunk_max<Tin, QV>(rd);
+                        const float cmt = TOPK ? -INFINITY : chunk_max<Tin, QV>(rt), cmd = chunk_max<Tin, QV>(rd);
                         __syncwarp();
                         tconsumed(c);
-                        tproduce<Tin>(A, c);
-                        fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
+                        tproduce<Tin, TOPK>(A, c);
+                        if (!TOPK) fold_regs<Tin, QV>(rt, cmt, k, mt, st, bad);
                         fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
                     }
                     if (c.dead) continue;
@@ -412,6 +423,70 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                     const Soft wd = soft_warp_allreduce<false>(a, k);
                     const bool wbad = warp_allor(bad) != 0;
                     tpush(sh, c, kk, make_float4(wt.m, wbad ? NAN : wt.s, wd.m, wbad ? NAN : wd.s));
+                } else if (TOPK) {
+                    // ---- O(k), top-K target: no row streams.  The draft
+                    // normaliser from the round, the target normaliser over
+                    // the K cached entries (every warp alike), then the
+                    // entries that fall in this warp's segment
+                    if (!twait_round(sh, c, kk)) continue;
+                    Soft ld = soft_empty();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int q = 2 * c.lane + h;
+                        if (q < c.S) {
+                            const float4 v = *trec(c, kk, q);
+                            Soft r;
+                            r.m = v.z;
+                            r.s = v.w;
+                            r.s1 = 0.f;
+                            ld = soft_pair_merge(ld, r, k);
+                        }
+                    }
+                    const Soft Cd = soft_warp_allreduce<false>(ld, k);
+                    const size_t kb = (static_cast<size_t>(t) * g + kk) * static_cast<size_t>(A.K);
+                    const Tin *vals = reinterpret_cast<const Tin *>(A.target) + kb;
+                    const int32_t *ids = A.topk_idx + kb;
+                    float tm = -INFINITY;
+                    int tbad = 0;
+                    for (int e = c.lane; e < A.K; e += 32) {
+                        const float z = St::scalar_g(vals, e);
+                        const int v = __ldg(ids + e);
+                        tbad |= !(z < INFINITY) ? F_NONFINITE : 0;
+                        tbad |= (v < 0 || v >= A.V) ? F_BAD_ID : 0;
+                        tm = fmaxf(tm, z);
+                    }
+                    tm = warp_allmax(tm);
+                    tbad = warp_allor(tbad);
+                    float ts = 0.f;
+                    if (tm > -INFINITY)
+                        for (int e = c.lane; e < A.K; e += 32)
+                            ts += ex2((St::scalar_g(vals, e) - tm) * k);
+                    ts = warp_allsum(ts);
+                    if (!(tm > -INFINITY) || !(ts > 0.f) || !(ts < INFINITY) || !(Cd.m > -INFINITY) || !(Cd.s > 0.f) ||
+                        !(Cd.s < INFINITY))
+                        tbad |= F_NONFINITE;
+                    if (tbad & F_BAD_ID) tbad = F_BAD_ID;  // the first error of the pair, as the oracle reports it
+                    flags |= tbad;
+                    const float ct = fmaf(tm, k, log2f(ts)), cd = fmaf(Cd.m, k, log2f(Cd.s));
+                    if (c.lane == 0) {
+                        c.ws->ct[kk] = ct;
+                        c.ws->cd[kk] = cd;
+                    }
+                    float acc_a = 0.f, acc_s = 0.f;
+                    if (!tbad) {
+                        const unsigned char *drow = tv_row_ptr<Tin>(A.draft, t, kk, g, A.V);
+                        const int v_lo = c.seg_lo * VEC, v_hi = (c.seg_lo + c.seg_n) * VEC;
+                        for (int e = c.lane; e < A.K; e += 32) {
+                            const int v = __ldg(ids + e);
+                            if (v < v_lo || v >= v_hi) continue;
+                            const float lp = fmaf(St::scalar_g(vals, e), k, -ct);
+                            const float lq = fmaf(St::scalar_g(drow, v), k, -cd);
+                            const float x = ex2(fminf(lp, lq));
+                            acc_a += x;
+                            if (lq <= lp) acc_s += x;
+                        }
+                    }
+                    tpush(sh, c, g + kk, make_float4(warp_allsum(acc_a), warp_allsum(acc_s), 0.f, 0.f));
                 } else {
                     if (!twait_round(sh, c, kk)) continue;
                     // gather: lane l holds segments 2l and 2l + 1
@@ -443,7 +518,7 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                     float acc_a = 0.f, acc_s = 0.f;
                     unsigned char *bk = c.bits + static_cast<size_t>(kk) * nvs;
                     for (int ch = 0; ch < c.nch; ++ch) {
-                        tproduce<Tin>(A, c);
+                        tproduce<Tin, TOPK>(A, c);
                         if (!twait_slot(c)) break;
                         const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
                         const unsigned char *db = tb + CV * 16;
@@ -461,7 +536,7 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                         asm volatile("" ::"r"(x));
                         __syncwarp();
                         tconsumed(c);
-                        tproduce<Tin>(A, c);
+                        tproduce<Tin, TOPK>(A, c);
                         uint32_t m[QV];
                         ovl_regs<Tin, QV>(rt, rd, k, ct, cd, acc_a, acc_s, m);
 #pragma unroll
@@ -539,7 +614,7 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                 const float cd = c.ws->cd[kk], on = c.ws->on[kk], off = c.ws->off[kk];
                 const unsigned char *bk = c.bits + static_cast<size_t>(kk) * nvs;
                 for (int ch = 0; ch < c.nch; ++ch) {
-                    tproduce<Tin>(A, c);
+                    tproduce<Tin, TOPK>(A, c);
                     if (!twait_slot(c)) break;
                     const unsigned char *db = c.ring + c.cslot * SLOT_BYTES + CV * 16;
                     const int cnt = tchunk(c, ch);
@@ -549,7 +624,7 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                     asm volatile("" ::"r"(x));
                     __syncwarp();
                     tconsumed(c);
-                    tproduce<Tin>(A, c);
+                    tproduce<Tin, TOPK>(A, c);
 #pragma unroll
                     for (int q = 0; q < QV; ++q) {
                         const int j = q * 32 + c.lane;
@@ -559,12 +634,30 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                                 __stcs(reinterpret_cast<float4 *>(out), make_float4(0.f, 0.f, 0.f, 0.f));
                                 if (VEC == 8) __stcs(reinterpret_cast<float4 *>(out) + 1, make_float4(0.f, 0.f, 0.f, 0.f));
                             } else {
-                                grad_vec<Tin>(rd[q], bk[ch * CV + j], k, cd, on, off, out);
+                                grad_vec<Tin>(rd[q], TOPK ? 0u : bk[ch * CV + j], k, cd, on, off, out);
                             }
                         }
                     }
                 }
                 if (c.dead) break;
+                if (TOPK && !flags) {
+                    // the cached entries of this segment: 1[q <= p~] where it holds
+                    __syncwarp();  // the segment's streamed values are visible to every lane
+                    const size_t kb = (static_cast<size_t>(t) * g + kk) * static_cast<size_t>(A.K);
+                    const unsigned char *vals =
+                        reinterpret_cast<const unsigned char *>(A.target) + kb * St::ES;
+                    const int32_t *ids = A.topk_idx + kb;
+                    const unsigned char *drow = tv_row_ptr<Tin>(A.draft, t, kk, g, A.V);
+                    const float ct = c.ws->ct[kk];
+                    const int v_lo = c.seg_lo * VEC, v_hi = (c.seg_lo + c.seg_n) * VEC;
+                    for (int e = c.lane; e < A.K; e += 32) {
+                        const int v = __ldg(ids + e);
+                        if (v < v_lo || v >= v_hi) continue;
+                        const float lp = fmaf(St::scalar_g(vals, e), k, -ct);
+                        const float lq = fmaf(St::scalar_g(drow, v), k, -cd);
+                        orow[v] = ex2(lq) * (lq <= lp ? on : off);
+                    }
+                }
             }
             if (c.dead) {
                 flags |= F_TIMEOUT;
@@ -605,12 +698,19 @@ int tvs_threads() { return NT; }
 int tvs_max_gamma() { return MAXG; }
 int tvs_max_segments() { return MAXS; }
 
-const void *tvs_kernel(int dtype, int cv) {
+const void *tvs_kernel(int dtype, int cv, bool topk) {
+    if (topk) {
+        if (dtype == 0)
+            return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<float, 192, true>)
+                             : reinterpret_cast<const void *>(&tvs_kernel_impl<float, 128, true>);
+        return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 192, true>)
+                         : reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 128, true>);
+    }
     if (dtype == 0)
-        return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<float, 192>)
-                         : reinterpret_cast<const void *>(&tvs_kernel_impl<float, 128>);
-    return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 192>)
-                     : reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 128>);
+        return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<float, 192, false>)
+                         : reinterpret_cast<const void *>(&tvs_kernel_impl<float, 128, false>);
+    return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 192, false>)
+                     : reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 128, false>);
 }
 
 }  // namespace mtp

@@ -620,6 +620,55 @@ def test_tv_loss_variants(N, gamma, V, dtype, shared, tau, C, kernel):
         assert np.min(np.abs(steps - tau)) > 1e-6  # no step on the kink
 
 
+def _topk_of(x, K):
+    """Top-K entries (values in storage dtype, int32 indices) of each target row."""
+    tf = W.bf16_bits_to_f32(x.target) if x.dtype == "bf16" else x.target
+    idx = np.argsort(-tf, axis=-1, kind="stable")[..., :K].astype(np.int32)
+    return np.ascontiguousarray(np.take_along_axis(x.target, idx, axis=-1)), np.ascontiguousarray(idx)
+
+
+@pytest.mark.parametrize("N,gamma,V,dtype,K,tau,C", [
+    (5, 3, 4096, "f32", 16, None, None),
+    (6, 3, 40000, "bf16", 64, None, 16),
+    (4, 5, 12000, "bf16", 1, None, 4),
+    (3, 8, 30000, "f32", 1000, 0.6, None),
+    (4, 3, 151936, "bf16", 64, None, None),
+])
+def test_tv_loss_topk(N, gamma, V, dtype, K, tau, C):
+    """Top-K target path (K cached target logits per pair, renormalised):
+    loss, alpha and the full-row gradient against the oracle."""
+    x = W.tvloss_inputs("tvk", N, gamma, V, dtype, 800 + V + K, delta=0.4, sigmas=np.linspace(0.8, 7.0, N))
+    vals, idx = _topk_of(x, K)
+    import mtp_speculative_decoding_row_gb300 as mtp
+    with env(MTP_RS_CLUSTER=C):
+        out = mtp.mtp_tv_loss_topk(to_dev(vals), to_dev(idx), to_dev(x.draft), 0.9, 1.25, clamp_tau=tau)
+        torch.cuda.synchronize()
+    o = oracle.tv_loss_topk(vals, idx, x.draft, 0.9, 1.25, clamp_tau=tau)
+    tf = W.bf16_bits_to_f32(x.target).astype(np.float64) if dtype == "bf16" else x.target.astype(np.float64)
+    df = W.bf16_bits_to_f32(x.draft).astype(np.float64) if dtype == "bf16" else x.draft.astype(np.float64)
+    masked = np.full_like(tf, -np.inf)
+    np.put_along_axis(masked, idx.astype(np.int64), np.take_along_axis(tf, idx.astype(np.int64), axis=-1), axis=-1)
+    rep = compare.tv_report(out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy(),
+                            out.row_flags.cpu().numpy(), o, dtype, masked, df, 0.9)
+    compare.assert_ok(rep, f"tv topk N={N} gamma={gamma} V={V} K={K}")
+
+
+def test_tv_loss_topk_bad_index_and_nan():
+    x = W.tvloss_inputs("tvkb", 5, 3, 8192, "f32", 880, delta=0.4, sigmas=np.linspace(1, 4, 5))
+    vals, idx = _topk_of(x, 8)
+    idx[1, 2, 3] = 8192
+    vals[3, 0, 0] = np.nan
+    x.draft[4, 1, 77] = np.inf
+    import mtp_speculative_decoding_row_gb300 as mtp
+    out = mtp.mtp_tv_loss_topk(to_dev(vals), to_dev(idx), to_dev(x.draft), 1.0, 1.0)
+    torch.cuda.synchronize()
+    o = oracle.tv_loss_topk(vals, idx, x.draft, 1.0, 1.0)
+    np.testing.assert_array_equal(out.row_flags.cpu().numpy(), o["flags"])
+    np.testing.assert_array_equal(o["flags"], [0, 2, 0, 1, 1])
+    g = out.grad.cpu().numpy()
+    assert np.all(g[[1, 3, 4]] == 0) and np.all(np.isnan(out.loss.cpu().numpy()[[1, 3, 4]]))
+
+
 def test_tv_plan_kernels():
     import mtp_speculative_decoding_row_gb300 as mtp
     p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
