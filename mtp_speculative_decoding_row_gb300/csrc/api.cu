@@ -159,10 +159,15 @@ bool stream_usable(int V, int es, int gamma) {
 // Chunk size for a warp segment of nvs vectors: 3 KB chunks when the
 // segment holds at least eight of them (fewer copies and less per-chunk
 // control for the same bytes), else 2 KB chunks (less waste in the ragged
-// last chunk of short segments).
-int stream_chunk_for(int nvs) {
+// last chunk of short segments).  The rejection-sampling verify kernel
+// (mode 0) takes 2.5 KB chunks: measured on GB300 they beat both at the
+// B = 64 and B = 512 verify batches (fewer chunks than 2 KB, four CTAs per
+// SM still fit, unlike 3 KB).
+int stream_chunk_for(int nvs, int mode = -1) {
     const int forced = env_int("MTP_RS_CHUNK");
     if (forced == 128 || forced == 192) return forced;
+    if (forced == 160 && mode == 0) return forced;
+    if (mode == 0) return 160;
     return nvs >= 8 * 192 ? 192 : 128;
 }
 
@@ -186,7 +191,7 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
         const int S = C * nw;
         if (S > stream_max_segments()) continue;
         const int nvs = (nv + S - 1) / S;
-        const int cv = mode == 1 ? 128 : stream_chunk_for(nvs);
+        const int cv = mode == 1 ? 128 : stream_chunk_for(nvs, mode);
         if ((nvs + cv - 1) / cv > stream_max_chunks()) continue;
         if (!forced && C > 1 && nvs < 64) continue;
         const uint32_t smem = stream_hdr_bytes() + stream_rec_bytes(gamma, S) +

@@ -1315,10 +1315,12 @@ const void *stream_kernel(int dtype, int cv, int mode) {
                          : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_GB>);
     }
     if (dtype == 0)
-        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_RS>)
-                         : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_RS>);
-    return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_RS>)
-                     : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_RS>);
+        return cv == 192   ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_RS>)
+               : cv == 160 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 160, M_RS>)
+                           : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_RS>);
+    return cv == 192   ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_RS>)
+           : cv == 160 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 160, M_RS>)
+                       : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_RS>);
 }
 
 }  // namespace mtp
