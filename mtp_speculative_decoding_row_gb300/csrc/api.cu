@@ -160,14 +160,15 @@ bool stream_usable(int V, int es, int gamma) {
 // segment holds at least eight of them (fewer copies and less per-chunk
 // control for the same bytes), else 2 KB chunks (less waste in the ragged
 // last chunk of short segments).  The rejection-sampling verify kernel
-// (mode 0) takes 2.5 KB chunks: measured on GB300 they beat both at the
-// B = 64 and B = 512 verify batches (fewer chunks than 2 KB, four CTAs per
+// (mode 0) and the streaming TV kernel (mode 3) take 2.5 KB chunks:
+// measured on GB300 they beat both at the B = 64 and B = 512 verify batches
+// and at the N = 16,384 TV batches (fewer chunks than 2 KB, four CTAs per
 // SM still fit, unlike 3 KB).
 int stream_chunk_for(int nvs, int mode = -1) {
     const int forced = env_int("MTP_RS_CHUNK");
     if (forced == 128 || forced == 192) return forced;
-    if (forced == 160 && mode == 0) return forced;
-    if (mode == 0) return 160;
+    if (forced == 160 && (mode == 0 || mode == 3)) return forced;
+    if (mode == 0 || mode == 3) return 160;
     return nvs >= 8 * 192 ? 192 : 128;
 }
 
@@ -258,7 +259,7 @@ bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, 
         const int S = C * nw;
         if (S > tvs_max_segments()) continue;
         const int nvs = (nv + S - 1) / S;
-        const int cv = stream_chunk_for(nvs);
+        const int cv = stream_chunk_for(nvs, 3);
         const uint32_t smem = tvs_hdr_bytes() + tvs_rec_bytes(gamma, S) + tvs_bits_bytes(gamma, nvs) +
                               static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
         if (smem > cap) continue;

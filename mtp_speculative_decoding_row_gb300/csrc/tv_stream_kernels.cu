@@ -699,18 +699,21 @@ int tvs_max_gamma() { return MAXG; }
 int tvs_max_segments() { return MAXS; }
 
 const void *tvs_kernel(int dtype, int cv, bool topk) {
+#define MTP_TVS_PICK(T, K)                                                                        \
+    return cv == 192   ? reinterpret_cast<const void *>(&tvs_kernel_impl<T, 192, K>)              \
+           : cv == 160 ? reinterpret_cast<const void *>(&tvs_kernel_impl<T, 160, K>)              \
+                       : reinterpret_cast<const void *>(&tvs_kernel_impl<T, 128, K>);
     if (topk) {
-        if (dtype == 0)
-            return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<float, 192, true>)
-                             : reinterpret_cast<const void *>(&tvs_kernel_impl<float, 128, true>);
-        return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 192, true>)
-                         : reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 128, true>);
+        if (dtype == 0) {
+            MTP_TVS_PICK(float, true)
+        }
+        MTP_TVS_PICK(bf16_t, true)
     }
-    if (dtype == 0)
-        return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<float, 192, false>)
-                         : reinterpret_cast<const void *>(&tvs_kernel_impl<float, 128, false>);
-    return cv == 192 ? reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 192, false>)
-                     : reinterpret_cast<const void *>(&tvs_kernel_impl<bf16_t, 128, false>);
+    if (dtype == 0) {
+        MTP_TVS_PICK(float, false)
+    }
+    MTP_TVS_PICK(bf16_t, false)
+#undef MTP_TVS_PICK
 }
 
 }  // namespace mtp
