@@ -160,15 +160,16 @@ bool stream_usable(int V, int es, int gamma) {
 // segment holds at least eight of them (fewer copies and less per-chunk
 // control for the same bytes), else 2 KB chunks (less waste in the ragged
 // last chunk of short segments).  The rejection-sampling verify kernel
-// (mode 0) and the streaming TV kernel (mode 3) take 2.5 KB chunks:
-// measured on GB300 they beat both at the B = 64 and B = 512 verify batches
-// and at the N = 16,384 TV batches (fewer chunks than 2 KB, four CTAs per
-// SM still fit, unlike 3 KB).
+// (mode 0), the streaming TV kernel (mode 3) and the row-pair kernel (mode
+// 4) take 2.5 KB chunks: measured on GB300 they beat both at the B = 64 and
+// B = 512 verify batches, the N = 16,384 TV batches and the B = 256
+// diagnostics (fewer chunks than 2 KB, four CTAs per SM still fit, unlike
+// 3 KB).
 int stream_chunk_for(int nvs, int mode = -1) {
     const int forced = env_int("MTP_RS_CHUNK");
     if (forced == 128 || forced == 192) return forced;
-    if (forced == 160 && (mode == 0 || mode == 3)) return forced;
-    if (mode == 0 || mode == 3) return 160;
+    if (forced == 160 && (mode == 0 || mode == 3 || mode == 4)) return forced;
+    if (mode == 0 || mode == 3 || mode == 4) return 160;
     return nvs >= 8 * 192 ? 192 : 128;
 }
 
@@ -434,7 +435,8 @@ bool plan_pairs(int dev, int dtype, int V, int es, int gamma, int units, int mod
         const int S = C * nw;
         if (S > pair_max_segments()) continue;
         const int nvs = (nv + S - 1) / S;
-        const int cv = mode == PAIR_DIAG ? 128 : stream_chunk_for(nvs);
+        int cv = stream_chunk_for(nvs, 4);
+        if (mode == PAIR_DIAG && cv == 192) cv = 128;  // the 3 KB diagnostics variant spills
         const uint32_t smem = pair_hdr_bytes() + pair_rec_bytes(gamma, S, mode) +
                               static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
         if (smem > cap) continue;

@@ -673,11 +673,14 @@ int pair_max_segments() { return MAXS; }
 int pair_max_ring() { return MAXR; }
 
 const void *pair_kernel(int dtype, int cv, int mode) {
-// the diagnostics run on 128-vector chunks only (the 192 variant spills)
+// the diagnostics run on 128- or 160-vector chunks (the 192 variant spills)
 #define MTP_PAIR_PICK(T)                                                                              \
-    if (mode == PAIR_DIAG) return reinterpret_cast<const void *>(&pair_kernel_impl<T, 128, PAIR_DIAG>); \
-    return cv == 192 ? reinterpret_cast<const void *>(&pair_kernel_impl<T, 192, PAIR_STATS>)          \
-                     : reinterpret_cast<const void *>(&pair_kernel_impl<T, 128, PAIR_STATS>);
+    if (mode == PAIR_DIAG)                                                                            \
+        return cv == 160 ? reinterpret_cast<const void *>(&pair_kernel_impl<T, 160, PAIR_DIAG>)       \
+                         : reinterpret_cast<const void *>(&pair_kernel_impl<T, 128, PAIR_DIAG>);      \
+    return cv == 192   ? reinterpret_cast<const void *>(&pair_kernel_impl<T, 192, PAIR_STATS>)        \
+           : cv == 160 ? reinterpret_cast<const void *>(&pair_kernel_impl<T, 160, PAIR_STATS>)        \
+                       : reinterpret_cast<const void *>(&pair_kernel_impl<T, 128, PAIR_STATS>);
     if (dtype == 0) {
         MTP_PAIR_PICK(float)
     }
