@@ -48,8 +48,8 @@ L2_BYTES = 129 * 1024 * 1024
 # ncu captures (profiles/), keyed by workload, valid only for the kernel
 # sources they were taken on (hash of csrc/).
 TRAFFIC = {
-    # stream_kernel_impl<bf16_t,128>, B=64 gamma=3 V=151936: 128,917,760 read + 4,064,512 written
-    "verify64": {"bytes": 132982272, "csrc": "941a2b3f9790e64c"},
+    # stream_kernel_impl<bf16_t,160,0>, B=64 gamma=3 V=151936: 131,991,296 read + 3,891,456 written
+    "verify64": {"bytes": 135882752, "csrc": "f252cb83d3ff440a"},
 }
 
 
