@@ -1,6 +1,7 @@
 // chunk_math.cuh -- per-lane arithmetic on chunks of logit rows held in
 // registers, shared by the streaming kernels: loading a chunk from its ring
-// slot, the chunk maximum and the branch-free online softmax fold.
+// slot, the chunk maximum, the branch-free online softmax fold and the
+// running and warp-wide arg max.
 //
 // A chunk row is CV = 32 * QV 16-byte vectors; lane l holds vectors
 // q * 32 + l (q < QV).
@@ -140,6 +141,30 @@ __device__ __forceinline__ void argmax_regs(const uint4 (&r)[QV], const uint4 (&
         }
     }
     m = cmx;
+}
+
+// Arg max across the warp: the largest value, ties to the smallest index
+// (index -1: no element); `x` travels with the winner.  Same result in every
+// lane.
+__device__ __forceinline__ void argmax_allreduce(float &v, int &i, float &x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(FULL, v, o), ox = __shfl_xor_sync(FULL, x, o);
+        const int oi = __shfl_xor_sync(FULL, i, o);
+        if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
+            v = ov;
+            i = oi;
+            x = ox;
+        }
+    }
+}
+
+__device__ __forceinline__ void argmax_merge(float &v, int &i, float &x, float ov, int oi, float ox) {
+    if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
+        v = ov;
+        i = oi;
+        x = ox;
+    }
 }
 
 }  // namespace mtp

@@ -92,13 +92,13 @@ int stream_max_ring();
 
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);
-// cv: 128 or 192 vectors per chunk; mode 0 = rejection sampling, 1 = target-only,
+// cv: 128, 160 or 192 vectors per chunk; mode 0 = rejection sampling, 1 = target-only,
 // 2 = rejection sampling with the Gumbel-max final draw
 const void *stream_kernel(int dtype, int cv, int mode);
 const void *tv_kernel(int dtype);
-// streaming TV kernel, cv: 128 or 192; topk: the target is K cached entries per pair
+// streaming TV kernel, cv: 128, 160 or 192; topk: the target is K cached entries per pair
 const void *tvs_kernel(int dtype, int cv, bool topk = false);
-// Streaming row-pair statistics kernel (mode: PairMode), cv: 128 or 192.
+// Streaming row-pair statistics kernel (mode: PairMode), cv: 128, 160 or 192.
 const void *pair_kernel(int dtype, int cv, int mode);
 uint32_t pair_hdr_bytes();
 uint32_t pair_rec_bytes(int gamma, int S, int mode);

@@ -491,30 +491,6 @@ struct Norm {
     float m0, s0, m1, s1;
 };
 
-// Arg max across the warp: the largest value, ties to the smallest index
-// (index -1: no element); `x` travels with the winner.  Same result in every
-// lane.
-__device__ __forceinline__ void argmax_allreduce(float &v, int &i, float &x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(FULL, v, o), ox = __shfl_xor_sync(FULL, x, o);
-        const int oi = __shfl_xor_sync(FULL, i, o);
-        if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
-            v = ov;
-            i = oi;
-            x = ox;
-        }
-    }
-}
-
-__device__ __forceinline__ void argmax_merge(float &v, int &i, float &x, float ov, int oi, float ox) {
-    if (oi >= 0 && (i < 0 || ov > v || (ov == v && oi < i))) {
-        v = ov;
-        i = oi;
-        x = ox;
-    }
-}
-
 template <int MODE>
 __device__ __forceinline__ Norm gather_norm(const Ctx &c, int i, float k, bool has_d) {
     Norm r;
