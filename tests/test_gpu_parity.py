@@ -408,6 +408,25 @@ def test_draft_sample_bad_rows_and_full_size():
         _check_draft(z, T, u, method, 2026, 1, "bf16", f"verify64 rows {method}")
 
 
+def test_draft_sample_gumbel_extreme_noise():
+    """Noise at the top of the uniform's range.  With seed 4696 (offset 0),
+    row 0, index 376 draws U = 1 - 2^-25, the largest Gumbel noise the
+    generator gives (G = 17.33; the row's second largest is 8.64).  Single
+    precision cannot hold that U; the noise must still come out right, not
+    infinite: with a low logit at index 376 another index wins, with a
+    moderately low one index 376 still wins."""
+    seed, v_star = 4696, 376
+    G = oracle.gumbel_noise(seed, 0, 0, 0, 0, 2048)
+    assert int(np.argmax(G)) == v_star and G[v_star] == -np.log(-np.log1p(-2.0 ** -25))
+    for z_star, wins in ((-12.0, False), (-8.5, True)):
+        z = np.zeros((1, 2048), np.float32)
+        z[0, v_star] = z_star
+        T = np.ones(1, np.float32)
+        u = np.full(1, 0.5, np.float32)
+        ids, o = _check_draft(z, T, u, "gumbel", seed, 0, "f32", f"extreme noise z*={z_star}")
+        assert (ids[0] == v_star) == wins, (ids, o["ids"])
+
+
 # ------------------------------------------------------- diagnostics -------
 
 def _logit_scale(x):
