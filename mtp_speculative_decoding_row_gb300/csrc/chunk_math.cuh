@@ -118,29 +118,49 @@ __device__ __forceinline__ float fold_regs(const uint4 (&r)[QV], float cmx, floa
     return cs;
 }
 
-// Running arg max of one chunk row held by this lane (first index among
-// equals in ascending vocabulary order; cmx: the lane's chunk maximum from
-// chunk_max).  vbase: vocabulary index of this lane's first vector in the
-// chunk (vector q sits 32 q vectors further).  With `other`, x receives the
-// other row's logit at the new arg max.
+// Running arg max of one chunk row kept warp-uniform: the warp maximum of
+// the lanes' chunk maxima (cmx from chunk_max; a NaN or +inf lane takes no
+// part, it is flagged elsewhere) replaces (m, idx, x) only when it exceeds
+// m, so an equal value in a later chunk keeps the earlier index.  Then only
+// the lanes holding the new maximum look for it, each finds its first
+// element equal to it, and the smallest such index wins (first index among
+// equals in ascending vocabulary order).  A per-lane running arg max would
+// scan a chunk whenever any lane's own maximum rises, which early in a row is
+// almost every chunk; the warp maximum rises far less often.  vbase:
+// vocabulary index of this lane's first vector in the chunk.  With OTHER, x
+// receives the other row's logit at the new arg max.
 template <typename Tin, int QV, bool OTHER>
-__device__ __forceinline__ void argmax_regs(const uint4 (&r)[QV], const uint4 (&o)[QV], float cmx, int vbase,
+__device__ __forceinline__ void argmax_warp(const uint4 (&r)[QV], const uint4 (&o)[QV], float cmx, int vbase,
                                             float &m, int &idx, float &x) {
     constexpr int VEC = Store<Tin>::VEC;
-    if (!(cmx > m) || !(cmx < INFINITY)) return;  // no improvement (or a NaN / +inf row, flagged elsewhere)
-    bool found = false;
+    const float c = (cmx < INFINITY) ? cmx : -INFINITY;  // NaN and +inf: no part
+    float wm = c;
 #pragma unroll
-    for (int q = 0; q < QV; ++q) {
+    for (int o2 = 16; o2 > 0; o2 >>= 1) wm = fmaxf(wm, __shfl_xor_sync(FULL, wm, o2));
+    if (!(wm > m)) return;  // warp-uniform
+    int li = 0x7fffffff;
+    float lx = 0.f;
+    if (c == wm) {
+        bool found = false;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            if (!found && vec_elem<Tin>(r[q], e) == cmx) {
-                found = true;
-                idx = (vbase + q * 32) * VEC + e;
-                if (OTHER) x = vec_elem<Tin>(o[q], e);
+        for (int q = 0; q < QV; ++q) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                if (!found && vec_elem<Tin>(r[q], e) == wm) {
+                    found = true;
+                    li = (vbase + q * 32) * VEC + e;
+                    if (OTHER) lx = vec_elem<Tin>(o[q], e);
+                }
             }
         }
     }
-    m = cmx;
+    int mi = li;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) mi = min(mi, __shfl_xor_sync(FULL, mi, o2));
+    const int src = __ffs(__ballot_sync(FULL, li == mi)) - 1;
+    if (OTHER) x = __shfl_sync(FULL, lx, src);
+    idx = mi;
+    m = wm;
 }
 
 // Arg max across the warp: the largest value, ties to the smallest index

@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(NT, MODE == PAIR_DIAG ? 3 : 4) pair_kernel_imp
                         if (has_d) {
                             if (DIAG) {
                                 fold_diag<Tin, QV>(rd, rt, cmd, k, md, sd, s1d, xd, bad);
-                                argmax_regs<Tin, QV, true>(rd, rt, cmd, c.seg_lo + ch * CV + c.lane, av, ai, ax);
+                                argmax_warp<Tin, QV, true>(rd, rt, cmd, c.seg_lo + ch * CV + c.lane, av, ai, ax);
                             } else {
                                 fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
                             }

@@ -952,8 +952,8 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     if (greedy) {
                         bad |= !(cmt < INFINITY) || (use_d && !(cmd < INFINITY));
                         float dummy = 0.f;
-                        argmax_regs<Tin, QV, false>(rt, rt, cmt, vbase, mt, tix, dummy);
-                        if (use_d) argmax_regs<Tin, QV, false>(rd, rd, cmd, vbase, md, dix, dummy);
+                        argmax_warp<Tin, QV, false>(rt, rt, cmt, vbase, mt, tix, dummy);
+                        if (use_d) argmax_warp<Tin, QV, false>(rd, rd, cmd, vbase, md, dix, dummy);
                         continue;
                     }
                     if (owns_y && yv >= ch * CV && yv < ch * CV + cnt) {
@@ -975,7 +975,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             fold_regs<Tin, QV>(rd, cmd, k, md, sd, bad);
                         } else {
                             bad |= !(cmd < INFINITY);
-                            argmax_regs<Tin, QV, true>(rd, rt, cmd, vbase, md, dix, zty);
+                            argmax_warp<Tin, QV, true>(rd, rt, cmd, vbase, md, dix, zty);
                         }
                     }
                     if (!has_d && MODE != M_GB) {  // per-chunk record of row gamma for the bonus draw
