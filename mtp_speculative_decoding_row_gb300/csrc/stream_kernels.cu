@@ -55,7 +55,7 @@ namespace {
 constexpr int NT = 128;          // threads per CTA
 constexpr int NW = NT / 32;      // warps (segments) per CTA
 // Chunk geometry is a template parameter of the kernel: CV vectors of each
-// row per ring slot (128 = 2 KB or 192 = 3 KB), CV / 32 per lane.
+// row per ring slot (128, 160 or 192: 2, 2.5 or 3 KB), CV / 32 per lane.
 constexpr int MAXCH = 64;        // chunks per segment
 constexpr int MAXS = 64;         // segments per cluster (C * NW)
 constexpr int MAXG = 8;          // largest gamma

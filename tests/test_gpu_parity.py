@@ -343,6 +343,60 @@ def test_gumbel_verify_full_config():
     assert rep["exact"] + rep["near_margin"] == x.B and rep["near_margin"] <= 2
 
 
+def test_streaming_modes_f32_full_vocab():
+    """float32 rows at V = 151,936 through the three verify modes of the
+    streaming kernel (rejection sampling, target-only, Gumbel-max), with a
+    spread of entropies and temperatures."""
+    B = 12
+    x = W.verify_inputs("f32full", B, 3, W.V_QWEN, "f32", 4242, family="sigma", sigmas=np.linspace(0.5, 6.0, B),
+                        delta=0.5, temperature=np.linspace(0.6, 1.4, B))
+    assert compare_plan_streams("verify", x) and compare_plan_streams("to_verify", x)
+    rep, g, o = _check_verify(x, False, "f32 full vocab")
+    assert rep["exact"] + rep["near_margin"] == B
+    rep, g, o = _check_to_verify(x, "f32 full vocab, target-only")
+    assert rep["exact"] + rep["near_margin"] == B
+    rep, g, o = _check_gumbel(x, 77, 3, "f32 full vocab, Gumbel-max")
+    assert rep["exact"] + rep["near_margin"] == B
+
+
+def compare_plan_streams(op, x):
+    """True when the call would take the streaming kernel (ring slots > 0)."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    return mtp.mtp_query_plan(op, x.dtype, x.B, x.gamma, x.V)["resident_drafts"] > 0
+
+
+def test_verify_in_cuda_graph():
+    """mtp_rs_verify captured once in a CUDA graph on a side stream and
+    replayed on two input sets copied into the captured buffers: the same
+    results as the oracle for each set (no per-call host state is baked into
+    the launch)."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    xs = [W.verify_inputs(f"graph{i}", 16, 3, 40000, "bf16", 5150 + i, family="sigma",
+                          sigmas=np.linspace(1.0, 5.0, 16), delta=0.4) for i in range(2)]
+    bufs = [to_dev(a) for a in (xs[0].target, xs[0].draft, xs[0].draft_ids, xs[0].temperature, xs[0].uniforms)]
+    out = mtp.mtp_rs_verify(*bufs)  # plan caches and outputs before capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            mtp.mtp_rs_verify(*bufs, out=out, stream=s)
+    torch.cuda.synchronize()
+    for x in reversed(xs):
+        for dst, src in zip(bufs, (x.target, x.draft, x.draft_ids, x.temperature, x.uniforms)):
+            dst.copy_(to_dev(src))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        g = {k: (v.cpu().numpy() if v is not None else None) for k, v in out._asdict().items()}
+        o = oracle.verify(x.target, x.draft, x.draft_ids, x.temperature, x.uniforms, want_stats=False)
+        rep = compare.verify_report(g["tokens"], g["accept_len"], g["row_flags"], o, x.draft_ids, x.gamma, x.V,
+                                    x.dtype)
+        compare.assert_ok(rep, "graph replay")
+        assert rep["exact"] + rep["near_margin"] == x.B
+
+
 # ------------------------------------------------------- draft sampling ----
 
 def _draft_rows(V, dtype, gamma, seed, B=16):
