@@ -648,14 +648,24 @@ constexpr float GUMBEL2_MIN = -6.f;
 // p keys z_v k + g_v into (kp, ip) and, with RESID, residual keys
 // log2(p_v - q_v) + g_v over the v with p_v > q_v into (kr, ir) (p =
 // 2^{z_t k - ct}, q = 2^{z_d k - cd}; g_v the noise of index v in row j of
-// sequence b).  A group of four indices (one generator call) is skipped when
-// none of them can raise either running maximum even with the largest noise
-// (for the residual, log2(p - q) <= log2 p = z k - ct).  kp starts at a
-// lower bound of the row's best p key, so skipped indices never hold a draw.
+// sequence b).  Two exact filters keep the work to the indices that can
+// still win; bp and br are bounds that a winning key must reach (the
+// warp's best keys so far; kp and kr themselves at the least):
+//   - a group of four indices (one generator call) is skipped when none of
+//     them can reach a bound even with the largest noise (for the residual,
+//     log2(p - q) <= log2 p = z k - ct);
+//   - without RESID (the p keys alone), an index's noise is formed only if
+//     its raw word can give enough noise: g >= bp - z k needs L = -log2 U <=
+//     2^{z k - bp}, and L >= W / ln 2 with W = 1 - U, so W <= ln 2 2^{mx - bp}
+//     (mx: the group's largest z k) is necessary; W is read off the word
+//     exactly, and the bound is widened for the approximate exponential.
+// kp starts at a lower bound of the row's best p key, so skipped indices
+// never hold a draw.
 template <typename Tin, int QV, bool RESID>
 __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], int cnt, int lane, float k,
                                             float ct, float cd, int vbase, uint32_t seed_lo, uint32_t seed_hi, int j,
-                                            uint32_t b, uint32_t offset, float &kr, int &ir, float &kp, int &ip) {
+                                            uint32_t b, uint32_t offset, float bp, float br, float &kr, int &ir,
+                                            float &kp, int &ip) {
     constexpr int VEC = Store<Tin>::VEC;
 #pragma unroll
     for (int q = 0; q < QV; ++q) {
@@ -673,15 +683,25 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
                 zk[e4] = zt[h * 4 + e4] * k;
                 mx = fmaxf(mx, zk[e4]);
             }
-            const bool want_p = mx + GUMBEL2_MAX >= kp;
-            const bool want_r = RESID && mx - ct + GUMBEL2_MAX >= kr;
+            const float bpv = fmaxf(kp, bp), brv = fmaxf(kr, br);
+            const bool want_p = mx + GUMBEL2_MAX >= bpv;
+            const bool want_r = RESID && mx - ct + GUMBEL2_MAX >= brv;
             if (!want_p && !want_r) continue;  // no index of the group can win either draw
             const uint4 x = philox4x32_10(
                 make_uint4(static_cast<uint32_t>(vv * (VEC / 4) + h), static_cast<uint32_t>(j), b, offset), seed_lo,
                 seed_hi);
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+            // largest W = 1 - U (in units of 2^-24) that can still reach the p
+            // bound (the bonus draw; a residual pass keeps every index of the
+            // group: its bound rises late, and the filter would only cost)
+            const float wlim =
+                RESID ? INFINITY : fmaf(ex2(fminf(mx - bpv, 30.f)), 0.69314724f * 16777216.f * 1.000002f, 2.f);
 #pragma unroll
             for (int e4 = 0; e4 < 4; ++e4) {
+                if (!RESID) {
+                    const float w24 = __uint2float_rn((1u << 24) - 1u - (xs[e4] >> 8)) + 0.5f;  // W 2^24
+                    if (!(w24 <= wlim)) continue;  // too little noise to reach the bound
+                }
                 const int e = h * 4 + e4;
                 const float gv = gumbel2(xs[e4]);
                 const float key_p = zk[e4] + gv;
@@ -719,7 +739,7 @@ __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsi
     const int lane = threadIdx.x & 31;
     const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + seg_lo;
     const uint4 *gd = reinterpret_cast<const uint4 *>(drow) + seg_lo;
-    float kr = -INFINITY, kp = lb;
+    float kr = -INFINITY, kp = lb, bp = lb, br = -INFINITY;
     int ir = -1, ip = -1;
     for (int base = 0; base < seg_n; base += QV * 32) {
         const int cnt = min(QV * 32, seg_n - base);
@@ -733,7 +753,9 @@ __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsi
             }
         }
         gumbel_regs<Tin, QV, RESID>(rt, rd, cnt, lane, k, ct, cd, seg_lo + base + lane, seed_lo, seed_hi, j, b,
-                                    offset, kr, ir, kp, ip);
+                                    offset, bp, br, kr, ir, kp, ip);
+        // the warp's best p key so far bounds every lane's filters
+        if (!RESID) bp = warp_allmax(kp);
     }
     float d0 = 0.f;
     argmax_allreduce(kr, ir, d0);
