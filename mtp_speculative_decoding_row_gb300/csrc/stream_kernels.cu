@@ -735,27 +735,37 @@ template <typename Tin, bool RESID>
 __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsigned char *drow, int seg_lo,
                                            int seg_n, int j, uint32_t b, float k, float ct, float cd, float lb,
                                            uint32_t seed_lo, uint32_t seed_hi, uint32_t offset) {
-    constexpr int QV = 4;
+    constexpr int QV = 2;  // vectors per lane per tile
     const int lane = threadIdx.x & 31;
     const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + seg_lo;
     const uint4 *gd = reinterpret_cast<const uint4 *>(drow) + seg_lo;
     float kr = -INFINITY, kp = lb, bp = lb, br = -INFINITY;
     int ir = -1, ip = -1;
-    for (int base = 0; base < seg_n; base += QV * 32) {
-        const int cnt = min(QV * 32, seg_n - base);
-        uint4 rt[QV], rd[QV];
+    // The pass is bound by load latency, not arithmetic: the next tile's
+    // loads are in flight while a tile is keyed.
+    uint4 rt[QV], rd[QV], nt[QV], nd[QV];
+    auto load_tile = [&](int base, uint4 (&t)[QV], uint4 (&d)[QV]) {
 #pragma unroll
         for (int q = 0; q < QV; ++q) {
             const int jv = base + q * 32 + lane;
-            if (jv < cnt + base) {
-                rt[q] = __ldg(gt + jv);
-                if (RESID) rd[q] = __ldg(gd + jv);
+            if (jv < seg_n) {
+                t[q] = __ldg(gt + jv);
+                if (RESID) d[q] = __ldg(gd + jv);
             }
         }
-        gumbel_regs<Tin, QV, RESID>(rt, rd, cnt, lane, k, ct, cd, seg_lo + base + lane, seed_lo, seed_hi, j, b,
-                                    offset, bp, br, kr, ir, kp, ip);
+    };
+    load_tile(0, rt, rd);
+    for (int base = 0; base < seg_n; base += QV * 32) {
+        if (base + QV * 32 < seg_n) load_tile(base + QV * 32, nt, nd);
+        gumbel_regs<Tin, QV, RESID>(rt, rd, min(QV * 32, seg_n - base), lane, k, ct, cd, seg_lo + base + lane,
+                                    seed_lo, seed_hi, j, b, offset, bp, br, kr, ir, kp, ip);
         // the warp's best p key so far bounds every lane's filters
         if (!RESID) bp = warp_allmax(kp);
+#pragma unroll
+        for (int q = 0; q < QV; ++q) {
+            rt[q] = nt[q];
+            if (RESID) rd[q] = nd[q];
+        }
     }
     float d0 = 0.f;
     argmax_allreduce(kr, ir, d0);
