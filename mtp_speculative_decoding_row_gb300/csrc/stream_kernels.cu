@@ -773,6 +773,28 @@ __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsi
     return make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
 }
 
+// Gumbel-max keys of one chunk of row j held in a ring slot (target half tb,
+// draft half db; cnt vectors; chunk_v0: the chunk's first vector in the row)
+// into the lane's running arg maxes, passed and returned by value as {kr,
+// ir, kp, ip}; bp and br are the warp's best keys so far.  Out of line: it
+// runs once per chunk of the final draw, and neither its generator state
+// nor the warp's streaming state should crowd the other's registers.
+template <typename Tin, int CV, bool RESID>
+__device__ __noinline__ float4 gumbel_slot(const unsigned char *tb, const unsigned char *db, int cnt, int chunk_v0,
+                                           float k, float ct, float cd, int j, uint32_t b, uint32_t seed_lo,
+                                           uint32_t seed_hi, uint32_t offset, float bp, float br, float kr, int ir,
+                                           float kp, int ip) {
+    const int lane = threadIdx.x & 31;
+    for (int q = 0; q < CV / 32 && q * 32 + lane < cnt; ++q) {
+        const uint4 vt[1] = {vec_at(tb, q * 32 + lane)};
+        uint4 vd[1] = {vt[0]};
+        if (RESID) vd[0] = vec_at(db, q * 32 + lane);
+        gumbel_regs<Tin, 1, RESID>(vt, vd, 32, lane, k, ct, cd, chunk_v0 + q * 32 + lane, seed_lo, seed_hi, j, b,
+                                   offset, bp, br, kr, ir, kp, ip);
+    }
+    return make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
+}
+
 template <typename Tin, int CV, int MODE>
 __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) {
     using St = Store<Tin>;
@@ -1100,21 +1122,57 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 // residual weight rounded to zero (ZERO_MASS)
                 float4 best = make_float4(-INFINITY, __int_as_float(-1), -INFINITY, __int_as_float(-1));
                 if (!(flags & ERR_BITS)) {
+                    const uint32_t bb = static_cast<uint32_t>(b);
+                    float kr = -INFINITY, kp = fmaf(r.Mt, k, GUMBEL2_MIN);  // the best p key is at least max z k + min g
+                    int ir = -1, ip = -1;
                     if (resid) {
-                        // drop the look-ahead rows past the rejection; the
-                        // producer moves on to the next sequence's first row
+                        // drop the look-ahead rows past the rejection (the producer
+                        // moves on to the next sequence's first row) and read row j
+                        // directly, mostly from L2
                         drain(c);
                         redirect_next(c, ord, A.B);
+                        c.c_conf = g;  // the path is fixed
+                        produce<Tin, MODE>(A, c);
+                        const float4 kk = gumbel_pass<Tin, true>(row_base<Tin>(A, true, b, j), row_base<Tin>(A, false, b, j),
+                                                                 c.seg_lo, c.seg_n, j, bb, k, r.ct, r.cd, kp, A.seed_lo,
+                                                                 A.seed_hi, A.offset);
+                        kr = kk.x;
+                        ir = __float_as_int(kk.y);
+                        kp = kk.z;
+                        ip = __float_as_int(kk.w);
+                    } else {
+                        // the bonus: row gamma streams through the ring once more
+                        // (mostly from L2) as a residual unit of the target row
+                        // alone, after which the producer moves on to the next
+                        // sequence's first row
+                        drain(c);
+                        c.p_ord = ord;
+                        c.p_i = j;
+                        c.p_kind = K_RES;
+                        c.p_c = 0;
+                        c.p_done = (c.nch == 0);
+                        c.c_conf = g;  // the path is fixed
+                        float bp = kp;
+                        for (int ch = 0; ch < c.nch; ++ch) {
+                            produce<Tin, MODE>(A, c);
+                            if (c.pcount == c.ccount) c.dead = true;
+                            if (c.dead || !slot_wait(c)) break;
+                            const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
+                            const float4 kk = gumbel_slot<Tin, CV, false>(tb, tb, chunk_count(c, ch), c.seg_lo + ch * CV,
+                                                                          k, r.ct, r.cd, j, bb, A.seed_lo, A.seed_hi,
+                                                                          A.offset, bp, -INFINITY, kr, ir, kp, ip);
+                            kp = kk.z;
+                            ip = __float_as_int(kk.w);
+                            __syncwarp();
+                            consumed(c);
+                            produce<Tin, MODE>(A, c);
+                            bp = warp_allmax(kp);  // the warp's best p key so far bounds every lane's filters
+                        }
                     }
-                    c.c_conf = g;  // the path is fixed: the producer may move on to the next sequence
-                    produce<Tin, MODE>(A, c);
-                    const float lb = fmaf(r.Mt, k, GUMBEL2_MIN);  // the best p key is at least max z k + min g
-                    const uint32_t bb = static_cast<uint32_t>(b);
-                    const unsigned char *tr = row_base<Tin>(A, true, b, j);
-                    best = resid ? gumbel_pass<Tin, true>(tr, row_base<Tin>(A, false, b, j), c.seg_lo, c.seg_n, j, bb,
-                                                          k, r.ct, r.cd, lb, A.seed_lo, A.seed_hi, A.offset)
-                                 : gumbel_pass<Tin, false>(tr, tr, c.seg_lo, c.seg_n, j, bb, k, r.ct, r.cd, lb,
-                                                           A.seed_lo, A.seed_hi, A.offset);
+                    float d0 = 0.f;
+                    argmax_allreduce(kr, ir, d0);
+                    argmax_allreduce(kp, ip, d0);
+                    best = make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
                 }
                 // every warp fills round gamma + 1 (no candidate when the row is flagged)
                 if (!c.dead) {
