@@ -773,26 +773,25 @@ __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsi
     return make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
 }
 
-// Gumbel-max keys of one chunk of row j held in a ring slot (target half tb,
-// draft half db; cnt vectors; chunk_v0: the chunk's first vector in the row)
-// into the lane's running arg maxes, passed and returned by value as {kr,
-// ir, kp, ip}; bp and br are the warp's best keys so far.  Out of line: it
-// runs once per chunk of the final draw, and neither its generator state
-// nor the warp's streaming state should crowd the other's registers.
-template <typename Tin, int CV, bool RESID>
-__device__ __noinline__ float4 gumbel_slot(const unsigned char *tb, const unsigned char *db, int cnt, int chunk_v0,
-                                           float k, float ct, float cd, int j, uint32_t b, uint32_t seed_lo,
-                                           uint32_t seed_hi, uint32_t offset, float bp, float br, float kr, int ir,
-                                           float kp, int ip) {
+// Gumbel-max p keys of one chunk of row j held in a ring slot (target
+// vectors at tb; cnt vectors; chunk_v0: the chunk's first vector in the row)
+// into the lane's running arg max, passed and returned by value as {kp,
+// ip}; bp is the warp's best p key so far.  Out of line: it runs once per
+// chunk of the bonus draw, and neither its generator state nor the warp's
+// streaming state should crowd the other's registers.
+template <typename Tin, int CV>
+__device__ __noinline__ float2 gumbel_slot(const unsigned char *tb, int cnt, int chunk_v0, float k, int j, uint32_t b,
+                                           uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, float bp, float kp,
+                                           int ip) {
     const int lane = threadIdx.x & 31;
+    float kr = -INFINITY;
+    int ir = -1;
     for (int q = 0; q < CV / 32 && q * 32 + lane < cnt; ++q) {
-        const uint4 vt[1] = {vec_at(tb, q * 32 + lane)};
-        uint4 vd[1] = {vt[0]};
-        if (RESID) vd[0] = vec_at(db, q * 32 + lane);
-        gumbel_regs<Tin, 1, RESID>(vt, vd, 32, lane, k, ct, cd, chunk_v0 + q * 32 + lane, seed_lo, seed_hi, j, b,
-                                   offset, bp, br, kr, ir, kp, ip);
+        const uint4 v[1] = {vec_at(tb, q * 32 + lane)};
+        gumbel_regs<Tin, 1, false>(v, v, 32, lane, k, 0.f, 0.f, chunk_v0 + q * 32 + lane, seed_lo, seed_hi, j, b,
+                                   offset, bp, -INFINITY, kr, ir, kp, ip);
     }
-    return make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
+    return make_float2(kp, __int_as_float(ip));
 }
 
 template <typename Tin, int CV, int MODE>
@@ -1158,11 +1157,10 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             if (c.pcount == c.ccount) c.dead = true;
                             if (c.dead || !slot_wait(c)) break;
                             const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
-                            const float4 kk = gumbel_slot<Tin, CV, false>(tb, tb, chunk_count(c, ch), c.seg_lo + ch * CV,
-                                                                          k, r.ct, r.cd, j, bb, A.seed_lo, A.seed_hi,
-                                                                          A.offset, bp, -INFINITY, kr, ir, kp, ip);
-                            kp = kk.z;
-                            ip = __float_as_int(kk.w);
+                            const float2 kk = gumbel_slot<Tin, CV>(tb, chunk_count(c, ch), c.seg_lo + ch * CV, k, j, bb,
+                                                                   A.seed_lo, A.seed_hi, A.offset, bp, kp, ip);
+                            kp = kk.x;
+                            ip = __float_as_int(kk.y);
                             __syncwarp();
                             consumed(c);
                             produce<Tin, MODE>(A, c);
