@@ -173,7 +173,8 @@ int stream_chunk_for(int nvs, int mode = -1) {
     return nvs >= 8 * 192 ? 192 : 128;
 }
 
-bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, int mode = 0) {
+bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, int mode = 0,
+                 bool dbl = false) {
     const int forced = env_cluster();
     int R = env_int("MTP_RS_RING");
     if (R < 2 || R > stream_max_ring()) R = 2;
@@ -199,7 +200,7 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
         const uint32_t smem = stream_hdr_bytes() + stream_rec_bytes(gamma, S) +
                               static_cast<uint32_t>(nw * R) * stream_slot_bytes(cv);
         if (smem > cap) continue;
-        const void *func = stream_kernel(dtype, cv, mode);
+        const void *func = stream_kernel(dtype, cv, mode, dbl && gamma == 0);
         if (prepare_func(dev, func) != cudaSuccess) return false;
         const int nc = max_clusters(dev, func, C, smem, stream_threads());
         if (nc <= 0) continue;
@@ -606,7 +607,7 @@ extern "C" int mtp_draft_sample(const void *draft_logits, mtp_dtype dtype, const
     // step, and its final draw (the bonus) samples the row
     const int mode = method == 0 ? 0 : 2;
     Plan p;
-    if (!plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, 0, R, p, mode)) return MTP_ERR_NO_DEVICE;
+    if (!plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, 0, R, p, mode, true)) return MTP_ERR_NO_DEVICE;
     VerifyArgs A = {};
     A.target = draft_logits;
     A.draft = draft_logits;
@@ -771,7 +772,7 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
     if (op == 10) {  // draft sampling (inverse CDF): one-row sequences of the streaming kernel
         if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
-        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, 0);
+        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, 0, true);
         if (!ok) return MTP_ERR_NO_DEVICE;
     }
     if (op == 8 || op == 9) {  // target-only verify, Gumbel-max verify: streaming kernel only

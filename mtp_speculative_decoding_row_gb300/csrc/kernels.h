@@ -93,8 +93,10 @@ int stream_max_ring();
 // Kernel entry points (host-side function pointers for cudaLaunchKernelEx).
 const void *row_kernel(int dtype, int mode);
 // cv: 128, 160 or 192 vectors per chunk; mode 0 = rejection sampling, 1 = target-only,
-// 2 = rejection sampling with the Gumbel-max final draw
-const void *stream_kernel(int dtype, int cv, int mode);
+// 2 = rejection sampling with the Gumbel-max final draw; dbl: every sequence is a
+// single target row (draft sampling), two chunks of it per ring slot (mode 0 at
+// cv 160; other shapes ignore it)
+const void *stream_kernel(int dtype, int cv, int mode, bool dbl = false);
 const void *tv_kernel(int dtype);
 // streaming TV kernel, cv: 128, 160 or 192; topk: the target is K cached entries per pair
 const void *tvs_kernel(int dtype, int cv, bool topk = false);

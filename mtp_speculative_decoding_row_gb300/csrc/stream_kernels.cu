@@ -175,27 +175,34 @@ __device__ __forceinline__ bool enter_unit(const VerifyArgs &A, Ctx &c) {
 }
 
 // Issue chunk copies while ring slots are free and the next chunk is needed
-// or inside the look-ahead.
-template <typename Tin, int MODE>
+// or inside the look-ahead.  With DBL (one-row sequences: draft sampling), a
+// target-only row of the main pass fills both halves of a slot with two
+// consecutive chunks, so each slot carries a full slot's bytes.
+template <typename Tin, int MODE, bool DBL>
 __device__ __forceinline__ void produce(const VerifyArgs &A, Ctx &c) {
     if (c.p_done || c.dead) return;
     while (c.pcount - c.ccount < static_cast<uint32_t>(c.R)) {
         if (c.p_c == 0 && !enter_unit<Tin, MODE>(A, c)) break;
         const int cnt = chunk_count(c, c.p_c);
+        const bool dbl = DBL && !c.p_d && c.p_kind == K_NORM;
+        const int cnt2 = (dbl && c.p_c + 1 < c.nch) ? chunk_count(c, c.p_c + 1) : 0;
         if (c.lane == 0) {
             // No proxy fence: every generic read of this slot has completed
             // (its value was consumed) before the consumer released it.
             const uint32_t bar = smem_addr(&c.ws->full[c.pslot]);
             const uint32_t dst = smem_addr(c.ring + c.pslot * (2u * c.cv * 16u));
             const uint32_t bytes = static_cast<uint32_t>(cnt) * 16u;
+            const uint32_t bytes2 = c.p_d ? bytes : static_cast<uint32_t>(cnt2) * 16u;
             const size_t off = static_cast<size_t>(c.p_c) * (c.cv * 16);
-            mbar_arrive_expect_tx_relaxed(bar, c.p_d ? 2u * bytes : bytes);
+            mbar_arrive_expect_tx_relaxed(bar, bytes + bytes2);
             bulk_g2s(dst, c.p_t + off, bytes, bar);
             if (c.p_d) bulk_g2s(dst + c.cv * 16, c.p_d + off, bytes, bar);
+            else if (bytes2) bulk_g2s(dst + c.cv * 16, c.p_t + off + c.cv * 16, bytes2, bar);
         }
         ++c.pcount;
         if (++c.pslot == static_cast<uint32_t>(c.R)) c.pslot = 0;
-        if (++c.p_c == c.nch) {
+        c.p_c += dbl ? 2 : 1;
+        if (c.p_c >= c.nch) {
             c.p_c = 0;
             if (c.p_kind == K_NORM) {
                 c.p_i += 1;  // p_i == g + 1 marks the end of the rows
@@ -794,7 +801,7 @@ __device__ __noinline__ float2 gumbel_slot(const unsigned char *tb, int cnt, int
     return make_float2(kp, __int_as_float(ip));
 }
 
-template <typename Tin, int CV, int MODE>
+template <typename Tin, int CV, int MODE, bool DBL>
 __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) {
     using St = Store<Tin>;
     constexpr int VEC = St::VEC;
@@ -868,7 +875,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
     float nu, nT;
     int ny;
     load_params(c.cid, nu, ny, nT);
-    produce<Tin, MODE>(A, c);
+    produce<Tin, MODE, DBL>(A, c);
 
     const float4 ZERO4 = make_float4(0.f, 0.f, 0.f, 0.f);
 
@@ -973,19 +980,35 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 float zty = 0.f, zdy = 0.f;  // RS: logits at y; TO: zty = target logit at the draft arg max
                 int tix = -1, dix = -1;      // running arg max indices (greedy target, greedy / TO draft)
                 int bad = 0;
-                for (int ch = 0; ch < c.nch; ++ch) {
+                // a target-only row takes two chunks per slot under DBL
+                const bool dbl = DBL && !has_d;
+                // per-chunk record of row gamma for the bonus draw
+                auto record = [&](int chi, float csum) {
+                    Soft a;
+                    a.m = mt;
+                    a.s = csum;
+                    a.s1 = 0.f;
+                    const Soft r = soft_warp_allreduce<false>(a, k);
+                    if (c.lane == 0) {
+                        c.ws->cm[chi] = r.m;
+                        c.ws->cs[chi] = r.s;
+                    }
+                };
+                for (int ch = 0; ch < c.nch; ch += dbl ? 2 : 1) {
                     // a decision may already be out: stop streaming a position
                     // that will not be used
                     if (dec < p && xtest(sh, c, dec)) {
                         decide(dec);
                         if (fin) break;
                     }
-                    produce<Tin, MODE>(A, c);
+                    produce<Tin, MODE, DBL>(A, c);
                     if (c.pcount == c.ccount) c.dead = true;  // nothing issued: never wait on it
                     if (c.dead || !slot_wait(c)) break;
                     const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
                     const unsigned char *db = tb + CV * 16;
                     const int cnt = chunk_count(c, ch);
+                    const int cnt2 = (dbl && ch + 1 < c.nch) ? chunk_count(c, ch + 1) : 0;
+                    const bool two = cnt2 > 0;  // rd holds chunk ch + 1 of the target row
                     uint4 rt[QV], rd[QV];
                     if (cnt == CV) {
                         load_chunk<Tin, true, QV>(tb, cnt, c.lane, rt);
@@ -994,19 +1017,24 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         load_chunk<Tin, false, QV>(tb, cnt, c.lane, rt);
                         if (use_d) load_chunk<Tin, false, QV>(db, cnt, c.lane, rd);
                     }
+                    if (two) {
+                        if (cnt2 == CV) load_chunk<Tin, true, QV>(db, cnt2, c.lane, rd);
+                        else load_chunk<Tin, false, QV>(db, cnt2, c.lane, rd);
+                    }
                     // the maxima consume every loaded register: the slot's
                     // reads are complete before it is handed back
                     const float cmt = chunk_max<Tin, QV>(rt);
-                    const float cmd = use_d ? chunk_max<Tin, QV>(rd) : 0.f;
+                    const float cmd = (use_d || two) ? chunk_max<Tin, QV>(rd) : 0.f;
                     __syncwarp();
                     consumed(c);  // the slot refills while this chunk is reduced
-                    produce<Tin, MODE>(A, c);
+                    produce<Tin, MODE, DBL>(A, c);
                     const int vbase = c.seg_lo + ch * CV + c.lane;
                     if (greedy) {
-                        bad |= !(cmt < INFINITY) || (use_d && !(cmd < INFINITY));
+                        bad |= !(cmt < INFINITY) || ((use_d || two) && !(cmd < INFINITY));
                         float dummy = 0.f;
                         argmax_warp<Tin, QV, false>(rt, rt, cmt, vbase, mt, tix, dummy);
                         if (use_d) argmax_warp<Tin, QV, false>(rd, rd, cmd, vbase, md, dix, dummy);
+                        else if (two) argmax_warp<Tin, QV, false>(rd, rd, cmd, vbase + CV, mt, tix, dummy);
                         continue;
                     }
                     if (owns_y && yv >= ch * CV && yv < ch * CV + cnt) {
@@ -1031,16 +1059,10 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             argmax_warp<Tin, QV, true>(rd, rt, cmd, vbase, md, dix, zty);
                         }
                     }
-                    if (!has_d && MODE != M_GB) {  // per-chunk record of row gamma for the bonus draw
-                        Soft a;
-                        a.m = mt;
-                        a.s = csum;
-                        a.s1 = 0.f;
-                        const Soft r = soft_warp_allreduce<false>(a, k);
-                        if (c.lane == 0) {
-                            c.ws->cm[ch] = r.m;
-                            c.ws->cs[ch] = r.s;
-                        }
+                    if (!has_d && MODE != M_GB) record(ch, csum);
+                    if (two) {  // DBL: never the Gumbel-max mode
+                        const float csum2 = fold_regs<Tin, QV>(rd, cmd, k, mt, st, bad);
+                        record(ch + 1, csum2);
                     }
                 }
                 if (c.dead || fin) break;  // fin: position p abandoned, its round gets a zero record
@@ -1071,7 +1093,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     }
                 }
                 pushed = p;
-                produce<Tin, MODE>(A, c);
+                produce<Tin, MODE, DBL>(A, c);
                 // decisions whose rounds are already complete
                 while (!fin && dec < g && dec <= p && xtest(sh, c, dec)) decide(dec);
             }
@@ -1131,7 +1153,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         drain(c);
                         redirect_next(c, ord, A.B);
                         c.c_conf = g;  // the path is fixed
-                        produce<Tin, MODE>(A, c);
+                        produce<Tin, MODE, DBL>(A, c);
                         const float4 kk = gumbel_pass<Tin, true>(row_base<Tin>(A, true, b, j), row_base<Tin>(A, false, b, j),
                                                                  c.seg_lo, c.seg_n, j, bb, k, r.ct, r.cd, kp, A.seed_lo,
                                                                  A.seed_hi, A.offset);
@@ -1153,7 +1175,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         c.c_conf = g;  // the path is fixed
                         float bp = kp;
                         for (int ch = 0; ch < c.nch; ++ch) {
-                            produce<Tin, MODE>(A, c);
+                            produce<Tin, MODE, DBL>(A, c);
                             if (c.pcount == c.ccount) c.dead = true;
                             if (c.dead || !slot_wait(c)) break;
                             const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
@@ -1163,7 +1185,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             ip = __float_as_int(kk.y);
                             __syncwarp();
                             consumed(c);
-                            produce<Tin, MODE>(A, c);
+                            produce<Tin, MODE, DBL>(A, c);
                             bp = warp_allmax(kp);  // the warp's best p key so far bounds every lane's filters
                         }
                     }
@@ -1212,7 +1234,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 const int ex_v = MODE == M_TO ? rej_y / VEC - c.seg_lo : -1;  // excluded vector in the segment
                 float Rw = 0.f;
                 for (int ch = 0; ch < c.nch; ++ch) {
-                    produce<Tin, MODE>(A, c);
+                    produce<Tin, MODE, DBL>(A, c);
                     if (c.pcount == c.ccount) c.dead = true;
                     if (c.dead || !slot_wait(c)) break;
                     const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
@@ -1240,7 +1262,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                     }
                     __syncwarp();
                     consumed(c);
-                    produce<Tin, MODE>(A, c);
+                    produce<Tin, MODE, DBL>(A, c);
                     if (c.lane == 0) c.ws->cs[ch] = ps;
                     Rw += ps;
                 }
@@ -1348,7 +1370,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 if (A.flags) A.flags[b] = flags;
             }
         }
-        produce<Tin, MODE>(A, c);
+        produce<Tin, MODE, DBL>(A, c);
     }
 
     drain(c);
@@ -1367,24 +1389,27 @@ int stream_max_segments() { return MAXS; }
 int stream_max_ring() { return MAXR; }
 int stream_max_gamma() { return MAXG; }
 
-const void *stream_kernel(int dtype, int cv, int mode) {
+const void *stream_kernel(int dtype, int cv, int mode, bool dbl) {
+    if (dbl && mode == 0 && cv == 160)  // one-row sequences, inverse-CDF draw
+        return dtype == 0 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 160, M_RS, true>)
+                          : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 160, M_RS, true>);
     if (mode == 1)  // target-only: 2 KB chunks (the arg max keeps two rows of registers live)
-        return dtype == 0 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_TO>)
-                          : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_TO>);
+        return dtype == 0 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_TO, false>)
+                          : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_TO, false>);
     if (mode == 2) {  // Gumbel-max final draw
         if (dtype == 0)
-            return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_GB>)
-                             : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_GB>);
-        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_GB>)
-                         : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_GB>);
+            return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_GB, false>)
+                             : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_GB, false>);
+        return cv == 192 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_GB, false>)
+                         : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_GB, false>);
     }
     if (dtype == 0)
-        return cv == 192   ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_RS>)
-               : cv == 160 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 160, M_RS>)
-                           : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_RS>);
-    return cv == 192   ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_RS>)
-           : cv == 160 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 160, M_RS>)
-                       : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_RS>);
+        return cv == 192   ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 192, M_RS, false>)
+               : cv == 160 ? reinterpret_cast<const void *>(&stream_kernel_impl<float, 160, M_RS, false>)
+                           : reinterpret_cast<const void *>(&stream_kernel_impl<float, 128, M_RS, false>);
+    return cv == 192   ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 192, M_RS, false>)
+           : cv == 160 ? reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 160, M_RS, false>)
+                       : reinterpret_cast<const void *>(&stream_kernel_impl<bf16_t, 128, M_RS, false>);
 }
 
 }  // namespace mtp

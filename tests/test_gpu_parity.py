@@ -462,6 +462,47 @@ def test_draft_sample_bad_rows_and_full_size():
         _check_draft(z, T, u, method, 2026, 1, "bf16", f"verify64 rows {method}")
 
 
+@pytest.mark.parametrize("C", [None, 8])
+def test_draft_sample_nonfinite_rows(C):
+    """NaN and +inf anywhere in a row (first and last index, a middle
+    segment), rows that are all -inf, and -inf entries in valid rows, with
+    good rows after each bad one: flags and draws against the oracle, the
+    greedy rows included."""
+    V = 40000
+    z, T, u = _draft_rows(V, "f32", 2, 6200, B=14)
+    n = z.shape[0]
+    z[1, 0] = np.nan
+    z[4, V - 1] = np.inf
+    z[8, V // 2 + 3] = np.nan
+    z[10, :] = -np.inf
+    z[13, 5000:9000] = -np.inf
+    z[16, 123] = np.inf
+    z[16, 124] = -np.inf
+    z[19, ::7] = -np.inf
+    z[22, 37] = np.nan
+    T[22] = 0.0
+    z[n - 1, V - 2] = np.nan
+    with env(MTP_RS_CLUSTER=C):
+        for method in ("multinomial", "gumbel"):
+            ids, o = _check_draft(z, T, u, method, 17, 3, "f32", f"nonfinite rows {method} C={C}")
+            for r in (1, 4, 8, 10, 16, 22, n - 1):
+                assert ids[r] == -1, (method, r, ids[r])
+            for r in (13, 19):
+                assert ids[r] >= 0 and np.isfinite(z[r, ids[r]]), (method, r, ids[r])
+
+
+@pytest.mark.parametrize("C", [None, 2])
+def test_draft_sample_gumbel_cold(C):
+    """Low temperatures (T = 0.01 to 0.05) scale the keys up to |z k| ~ 10^4
+    and make the per-chunk key bounds of the one-pass draw tight: draws
+    against the oracle."""
+    z, T, u = _draft_rows(65536, "f32", 1, 6300, B=12)
+    T[:] = np.linspace(0.01, 0.05, T.size).astype(np.float32)
+    with env(MTP_RS_CLUSTER=C):
+        ids, o = _check_draft(z, T, u, "gumbel", 31, 0, "f32", f"cold rows C={C}")
+    assert np.all(ids >= 0)
+
+
 def test_draft_sample_gumbel_extreme_noise():
     """Noise at the top of the uniform's range.  With seed 4696 (offset 0),
     row 0, index 376 draws U = 1 - 2^-25, the largest Gumbel noise the
