@@ -49,7 +49,7 @@ L2_BYTES = 129 * 1024 * 1024
 # sources they were taken on (hash of csrc/).
 TRAFFIC = {
     # stream_kernel_impl<bf16_t,160,0>, B=64 gamma=3 V=151936: 132,281,600 read + 3,959,296 written
-    "verify64": {"bytes": 136240896, "csrc": "1de983f9bb5f5b46"},
+    "verify64": {"bytes": 135787264, "csrc": "b6d790cdd4c32916"},
 }
 
 
