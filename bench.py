@@ -49,7 +49,7 @@ L2_BYTES = 129 * 1024 * 1024
 # sources they were taken on (hash of csrc/).
 TRAFFIC = {
     # stream_kernel_impl<bf16_t,160,0>, B=64 gamma=3 V=151936: 132,281,600 read + 3,959,296 written
-    "verify64": {"bytes": 135787264, "csrc": "b6d790cdd4c32916"},
+    "verify64": {"bytes": 135653376, "csrc": "c6a530b9c1f3a6cb"},
 }
 
 
@@ -248,7 +248,7 @@ class VerifyWorkload:
 
     def plan_op(self) -> str:
         return {"stats": "row_stats", "diag": "diagnostics", "to": "to_verify", "gumbel": "gumbel_verify",
-                "sample": "draft_sample", "gsample": "draft_sample"}.get(
+                "sample": "draft_sample", "gsample": "draft_sample_gumbel"}.get(
             self.kind, "verify_stats" if self.stats else "verify")
 
     def describe(self) -> str:
@@ -520,8 +520,9 @@ def run_cuda(args, world, rank, local, pg):
         per_launch_s = t["ms_total"] / 1e3 / t["launches"]
         achieved = alg / per_launch_s / 1e9
         tv = name in TV_WORKLOADS
-        plan = mtp.mtp_query_plan("tv_loss" if tv else wl.plan_op(), "bf16" if wl.es == 2 else "f32",
-                                  wl.N if tv else wl.B, wl.gamma, wl.V)
+        units = wl.N if tv else (wl.B * wl.gamma if wl.kind in ("sample", "gsample") else wl.B)  # draft sampling: rows
+        plan = mtp.mtp_query_plan("tv_loss" if tv else wl.plan_op(), "bf16" if wl.es == 2 else "f32", units,
+                                  wl.gamma, wl.V)
         r = {
             "workload": wl.describe(),
             "launch_plan": plan,

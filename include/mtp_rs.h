@@ -320,13 +320,14 @@ int mtp_tv_loss_topk(const void *target_values, const int32_t *target_idx, const
  * mtp_rs_verify forced onto the cluster-resident kernel, 5 =
  * mtp_tv_loss_fwd_bwd forced onto the cluster-resident kernel, 6 =
  * mtp_rs_diagnostics, 7 = mtp_row_stats forced onto the cluster-resident
- * kernel, 8 = mtp_to_verify, 9 = mtp_gumbel_verify, 10 = mtp_draft_sample
- * (units = rows).  units = B
+ * kernel, 8 = mtp_to_verify, 9 = mtp_gumbel_verify, 10 = mtp_draft_sample by
+ * inverse CDF, 11 = mtp_draft_sample by Gumbel-max (10 and 11: units = rows;
+ * gamma is not used but must be valid).  Otherwise units = B
  * (sequences) or N (positions).  Outputs (any may be NULL): cluster_size (C,
  * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
  * per CTA), resident_drafts (cluster-resident TV kernel: draft slices kept on
- * chip; ops 0, 8, 9, 10: chunk slots per warp of the streaming kernel, 0 when the call
+ * chip; ops 0, 8-11: chunk slots per warp of the streaming kernel, 0 when the call
  * would use the cluster-resident kernel; else 0).
  * Returns the status the call's planning step would return.
  */

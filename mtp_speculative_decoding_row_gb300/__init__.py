@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_
                     "mtp_query_plan", "mtp_status_string")
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
             "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9,
-            "draft_sample": 10}
+            "draft_sample": 10, "draft_sample_gumbel": 11}
 
 _lib = None
 

@@ -760,7 +760,7 @@ extern "C" int mtp_tv_loss_fwd_bwd(const void *target_logits, const void *draft_
 extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size,
                               int *clusters, int *smem_bytes, int *resident_drafts) {
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
-    if (op < 0 || op > 10 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
+    if (op < 0 || op > 11 || units < 1 || gamma < 1 || gamma > MTP_MAX_GAMMA || V < 1) return MTP_ERR_INVALID_ARG;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
@@ -770,9 +770,9 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
     if (op == 3 && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
     if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
-    if (op == 10) {  // draft sampling (inverse CDF): one-row sequences of the streaming kernel
+    if (op == 10 || op == 11) {  // draft sampling (inverse CDF, Gumbel-max): one-row sequences of the streaming kernel
         if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
-        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, 0, true);
+        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, op == 10 ? 0 : 2, true);
         if (!ok) return MTP_ERR_NO_DEVICE;
     }
     if (op == 8 || op == 9) {  // target-only verify, Gumbel-max verify: streaming kernel only

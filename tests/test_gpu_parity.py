@@ -125,6 +125,18 @@ def test_verify_plan_kernels():
         assert mtp.mtp_query_plan("verify", "bf16", 64, 3, 151936)["resident_drafts"] == 0
 
 
+def test_draft_sample_plans():
+    """Both draft-sampling plans count rows as units: at most one cluster per
+    row, streaming-kernel ring slots, and the Gumbel-max plan is its own."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    for op in ("draft_sample", "draft_sample_gumbel"):
+        p = mtp.mtp_query_plan(op, "bf16", 192, 3, 151936)
+        assert 1 <= p["clusters"] <= 192 and p["cluster_size"] >= 1 and p["smem_bytes"] > 0, (op, p)
+        assert p["resident_drafts"] >= 2, (op, p)
+    small = mtp.mtp_query_plan("draft_sample_gumbel", "bf16", 3, 3, 151936)
+    assert small["clusters"] <= 3
+
+
 @pytest.mark.parametrize("name,kernel", [("verify64", None), ("rl512", None), ("deep256", None),
                                          ("verify64", "resident"), ("rl512", "resident")])
 def test_verify_full_configs(name, kernel):
