@@ -73,6 +73,20 @@ def test_host_validation_without_gpu(lib):
     assert lib.mtp_tv_loss_fwd_bwd(fake, fake, 5, 1.0, 4, 3, 10, 1.0, fake, None, fake, None, None) == 2
 
 
+def test_query_plan_validation_without_gpu(lib):
+    """Arguments are checked before any device call: ops 0-11 exist, the
+    dtype must be f32 or bf16, units, gamma and V must be in range."""
+    c = ctypes.c_int(0)
+    r = ctypes.byref(c)
+    for op in (-1, 12, 99):
+        assert lib.mtp_query_plan(op, 1, 64, 3, 151936, r, r, r, r) == 1, op
+    assert lib.mtp_query_plan(0, 7, 64, 3, 151936, r, r, r, r) == 2
+    assert lib.mtp_query_plan(11, 1, 0, 3, 151936, r, r, r, r) == 1
+    assert lib.mtp_query_plan(11, 1, 192, 0, 151936, r, r, r, r) == 1
+    assert lib.mtp_query_plan(10, 1, 192, 3, 0, r, r, r, r) == 1
+    assert lib.mtp_query_plan(9, 1, 64, 33, 151936, r, r, r, r) == 1
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         mtp.load_library(str(tmp_path / "missing.so"))
