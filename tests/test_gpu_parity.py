@@ -515,6 +515,38 @@ def test_draft_sample_gumbel_cold(C):
     assert np.all(ids >= 0)
 
 
+def test_draft_sample_in_cuda_graph():
+    """mtp_draft_sample, both draws, captured once in a CUDA graph on a side
+    stream and replayed on two sets of rows copied into the captured buffers:
+    each replay matches the oracle (the noise key and counter word are part
+    of the captured launch)."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    sets = [_draft_rows(30000, "bf16", 2, 6400 + i, B=24) for i in range(2)]
+    for method in ("multinomial", "gumbel"):
+        bufs = [to_dev(a) for a in sets[0]]
+        out = mtp.mtp_draft_sample(*bufs, method=method, seed=77, offset=5)  # plan caches before capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                mtp.mtp_draft_sample(*bufs, method=method, seed=77, offset=5, out=out, stream=s)
+        torch.cuda.synchronize()
+        for z, T, u in reversed(sets):
+            for dst, src in zip(bufs, (z, T, u)):
+                dst.copy_(to_dev(src))
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            ids, flags = out.ids.cpu().numpy(), out.row_flags.cpu().numpy()
+            o = oracle.draft_sample(z, T, u, method=method, seed=77, offset=5)
+            np.testing.assert_array_equal(flags, o["flags"], err_msg=method)
+            lim = compare.GUMBEL_MARGIN if method == "gumbel" else compare.MARGIN
+            bad = (ids != o["ids"]) & ~(o["margin"] < lim)
+            assert not bad.any(), (method, np.nonzero(bad)[0][:8])
+
+
 def test_draft_sample_gumbel_extreme_noise():
     """Noise at the top of the uniform's range.  With seed 4696 (offset 0),
     row 0, index 376 draws U = 1 - 2^-25, the largest Gumbel noise the
