@@ -708,6 +708,39 @@ def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres):
     compare.assert_ok(rep, f"tv N={N} V={V}")
 
 
+def test_tv_loss_in_cuda_graph():
+    """mtp_tv_loss_fwd_bwd captured once in a CUDA graph on a side stream and
+    replayed on two input sets copied into the captured buffers: loss, alpha
+    and gradient match the oracle for each set."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    T, scale = 0.9, 0.5
+    xs = [W.tvloss_inputs(f"tvg{i}", 6, 3, 40000, "bf16", 640 + i, delta=0.5, sigmas=np.linspace(1.0, 8.0, 6))
+          for i in range(2)]
+    bufs = [to_dev(xs[0].target), to_dev(xs[0].draft)]
+    out = mtp.mtp_tv_loss_fwd_bwd(*bufs, T, scale)  # plan caches and outputs before capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            mtp.mtp_tv_loss_fwd_bwd(*bufs, T, scale, out=out, stream=s)
+    torch.cuda.synchronize()
+    for x in reversed(xs):
+        bufs[0].copy_(to_dev(x.target))
+        bufs[1].copy_(to_dev(x.draft))
+        out.grad.fill_(float("nan"))  # every entry must be rewritten by the replay
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        o = oracle.tv_loss(x.target, x.draft, T, scale)
+        tf = W.bf16_bits_to_f32(x.target).astype(np.float64)
+        df = W.bf16_bits_to_f32(x.draft).astype(np.float64)
+        rep = compare.tv_report(out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy(),
+                                out.row_flags.cpu().numpy(), o, "bf16", tf, df, T)
+        compare.assert_ok(rep, "tv graph replay")
+
+
 @pytest.mark.parametrize("N,gamma,V,dtype,C,clusters,ring,kernel", [
     (9, 3, 40000, "bf16", 16, 2, None, None),     # several positions per cluster: both exchange banks
     (7, 2, 20000, "f32", 4, 3, 3, None),
