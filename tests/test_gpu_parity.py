@@ -515,6 +515,43 @@ def test_draft_sample_gumbel_cold(C):
     assert np.all(ids >= 0)
 
 
+def test_concurrent_calls_on_streams():
+    """Verify, row statistics and Gumbel-max draft sampling launched back to
+    back on three streams with no synchronisation between them (the library
+    keeps no state between calls, so concurrent calls cannot interfere): each
+    result matches the oracle."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    x = W.verify_inputs("conc", 16, 3, 40000, "bf16", 5300, family="sigma", sigmas=np.linspace(1.0, 6.0, 16),
+                        delta=0.4, temperature=np.linspace(0.7, 1.2, 16))
+    z, T, u = _draft_rows(30000, "bf16", 2, 6500, B=24)
+    dv = [to_dev(a) for a in (x.target, x.draft, x.draft_ids, x.temperature, x.uniforms)]
+    dz = [to_dev(a) for a in (z, T, u)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):  # several rounds in flight at once
+        with torch.cuda.stream(streams[0]):
+            v = mtp.mtp_rs_verify(*dv, stream=streams[0])
+        with torch.cuda.stream(streams[1]):
+            st = mtp.mtp_row_stats(dv[0], dv[1], dv[3], stream=streams[1])
+        with torch.cuda.stream(streams[2]):
+            ds = mtp.mtp_draft_sample(*dz, method="gumbel", seed=3, offset=1, stream=streams[2])
+    torch.cuda.synchronize()
+    g = {k: (t.cpu().numpy() if t is not None else None) for k, t in v._asdict().items()}
+    o = oracle.verify(x.target, x.draft, x.draft_ids, x.temperature, x.uniforms, want_stats=False)
+    compare.assert_ok(compare.verify_report(g["tokens"], g["accept_len"], g["row_flags"], o, x.draft_ids, x.gamma,
+                                            x.V, x.dtype), "concurrent verify")
+    gs = {k: t.cpu().numpy() for k, t in st._asdict().items()}
+    os_ = oracle.row_stats(x.target, x.draft, x.temperature)
+    compare.assert_ok(compare.stats_report(gs["alpha"], gs["entropy"], os_, x.dtype, gs["row_flags"]),
+                      "concurrent stats")
+    od = oracle.draft_sample(z, T, u, method="gumbel", seed=3, offset=1)
+    ids = ds.ids.cpu().numpy()
+    np.testing.assert_array_equal(ds.row_flags.cpu().numpy(), od["flags"])
+    assert not ((ids != od["ids"]) & ~(od["margin"] < compare.GUMBEL_MARGIN)).any()
+
+
 def test_draft_sample_in_cuda_graph():
     """mtp_draft_sample, both draws, captured once in a CUDA graph on a side
     stream and replayed on two sets of rows copied into the captured buffers:
