@@ -115,6 +115,45 @@ def test_verify_long_draft(gamma):
     assert rep["exact"] + rep["near_margin"] == x.B
 
 
+def _random_configs(n, seed=2026):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        dtype = "bf16" if rng.random() < 0.6 else "f32"
+        V = int(rng.choice([int(rng.integers(1, 64)), int(rng.integers(64, 5000)), int(rng.integers(5000, 70000))]))
+        out.append((i, dtype, V, int(rng.integers(1, 21)), int(rng.integers(1, 9))))
+    return out
+
+
+@pytest.mark.parametrize("i,dtype,V,B,gamma", _random_configs(24))
+def test_randomized_shapes(i, dtype, V, B, gamma):
+    """Seeded random shapes (V from 1 to 70,000, odd sizes that leave rows
+    unaligned included; B up to 20; gamma up to 8; per-sequence temperatures
+    with greedy rows; logit scales and draft offsets spread wide): verify
+    without and with statistics (a greedy row with statistics is flagged, as
+    documented) and row statistics against the oracle, and draft sampling by
+    both draws where the rows are whole 16-byte vectors."""
+    rng = np.random.default_rng(9000 + i)
+    T = rng.uniform(0.3, 2.0, B).astype(np.float32)
+    T[rng.random(B) < 0.15] = 0.0
+    x = W.verify_inputs(f"rand{i}", B, gamma, V, dtype, 9100 + i, family="sigma",
+                        sigmas=rng.uniform(0.2, 12.0, B), delta=rng.uniform(0.0, 1.5, B), temperature=T)
+    what = f"random {i}: {dtype} V={V} B={B} gamma={gamma}"
+    rep, g, o = _check_verify(x, False, what)  # T = 0 rows are greedy sequences
+    assert rep["exact"] + rep["near_margin"] == x.B
+    rep, g, o = _check_verify(x, True, what + " with stats")  # greedy rows with statistics are flagged
+    assert rep["exact"] + rep["near_margin"] + int((o["accept_len"] < 0).sum()) == x.B
+    gs = run_stats(x)
+    os_ = oracle.row_stats(x.target, x.draft, x.temperature)
+    compare.assert_ok(compare.stats_report(gs["alpha"], gs["entropy"], os_, dtype, gs["row_flags"]), f"random {i} stats")
+    if V % (16 // (2 if dtype == "bf16" else 4)) == 0:
+        z = x.draft.reshape(B * gamma, V)
+        Tz = np.repeat(x.temperature, gamma).astype(np.float32)
+        u = x.uniforms[:, :gamma].reshape(-1).copy()
+        for method in ("multinomial", "gumbel"):
+            _check_draft(z, Tz, u, method, 40 + i, i, dtype, f"random {i} draft {method}")
+
+
 def test_verify_plan_kernels():
     import mtp_speculative_decoding_row_gb300 as mtp
     p = mtp.mtp_query_plan("verify", "bf16", 64, 3, 151936)
