@@ -784,6 +784,36 @@ def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres):
     compare.assert_ok(rep, f"tv N={N} V={V}")
 
 
+def _random_tv_configs(n, seed=2027):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        dtype = "bf16" if rng.random() < 0.6 else "f32"
+        V = int(rng.choice([int(rng.integers(2, 64)), int(rng.integers(64, 5000)), int(rng.integers(5000, 50000))]))
+        out.append((i, dtype, V, int(rng.integers(1, 10)), int(rng.integers(1, 13))))
+    return out
+
+
+@pytest.mark.parametrize("i,dtype,V,N,gamma", _random_tv_configs(12))
+def test_tv_loss_randomized_shapes(i, dtype, V, N, gamma):
+    """Seeded random shapes for the TV loss forward and backward (V from 2 to
+    50,000 with unaligned sizes, N up to 9, gamma up to 12: past the
+    streaming limit of 8 the cluster-resident kernel runs), random
+    temperature and gradient scale: loss, alpha and gradient against the
+    oracle."""
+    rng = np.random.default_rng(9500 + i)
+    T, scale = float(rng.uniform(0.5, 1.5)), float(rng.uniform(0.1, 2.0))
+    x = W.tvloss_inputs(f"tvr{i}", N, gamma, V, dtype, 9600 + i, delta=float(rng.uniform(0.1, 1.0)),
+                        sigmas=rng.uniform(0.3, 9.0, N))
+    out = run_tv(to_dev(x.target), to_dev(x.draft), T, scale)
+    o = oracle.tv_loss(x.target, x.draft, T, scale)
+    tf = W.bf16_bits_to_f32(x.target).astype(np.float64) if dtype == "bf16" else x.target.astype(np.float64)
+    df = W.bf16_bits_to_f32(x.draft).astype(np.float64) if dtype == "bf16" else x.draft.astype(np.float64)
+    rep = compare.tv_report(out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy(),
+                            out.row_flags.cpu().numpy(), o, dtype, tf, df, T)
+    compare.assert_ok(rep, f"random tv {i}: {dtype} V={V} N={N} gamma={gamma}")
+
+
 def test_tv_loss_in_cuda_graph():
     """mtp_tv_loss_fwd_bwd captured once in a CUDA graph on a side stream and
     replayed on two input sets copied into the captured buffers: loss, alpha
