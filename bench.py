@@ -2,12 +2,14 @@
 the measured HBM roofline) at V = 151,936 on one GB300.
 
 Step = one call of the hot path over one batch of synthetic input.  The
-headline workload is the verify batch (B = 64 sequences, gamma = 3,
-V = 151,936, bf16 logits, entropy-spanning target rows, draft = target +
-N(0, 0.3), T = 1): one mtp_rs_verify call per step.  The same JSON line also
-reports the other workloads measured in the same run: RL-rollout verify
-(B = 512), deep speculation with per-position alpha and entropy (B = 256,
-gamma = 7, fp32) and the e2e TV-loss forward+backward (N = 16,384).
+headline workload is the RL-rollout verify batch (B = 512 sequences,
+gamma = 3, V = 151,936, bf16 logits; peaked Zipf(1.1)+8 rows with 30 %
+N(0, 1) rows, delta in {0.1, 0.5}, T in {0.6, 1.0}): one mtp_rs_verify call
+per step.  The same JSON line also reports the other workloads measured in
+the same run: the B = 64 verify batch, deep speculation with per-position
+alpha and entropy (B = 256, gamma = 7, fp32), row statistics, diagnostics,
+the acceptance-method variants, draft sampling and the e2e TV-loss
+forward+backward (N = 16,384) with its variants.
 
 Timing: inputs resident in HBM; several copies of each input are rotated so
 successive steps never hit L2 (each copy is > L2 or the rotation exceeds 4x
@@ -17,8 +19,8 @@ metric through the public API with pinned host buffers: host-to-device copy
 of the step's inputs, the call, and the device-to-host copy of its outputs.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {cuda,reference}]
-       [--workloads verify64,rl512,deep256,stats256,diag256,to64,gumbel64,sample192,gsample192,tvloss,
-                    tvshared,tvtopk]
+       [--workloads rl512,verify64,deep256,stats256,diag256,to64,gumbel64,sample192,gsample192,tvloss,
+                    tvshared,tvtopk] [--cpu-baselines {all,headline,none}]
 Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
 one JSON line.
 """
@@ -30,6 +32,7 @@ import glob
 import json
 import math
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -47,10 +50,7 @@ L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
 # ncu captures (profiles/), keyed by workload, valid only for the kernel
 # sources they were taken on (hash of csrc/).
-TRAFFIC = {
-    # stream_kernel_impl<bf16_t,160,0>, B=64 gamma=3 V=151936: 132,281,600 read + 3,959,296 written
-    "verify64": {"bytes": 135653376, "csrc": "c6a530b9c1f3a6cb"},
-}
+TRAFFIC = {}
 
 
 def csrc_hash() -> str:
@@ -423,38 +423,119 @@ def time_e2e(wl: VerifyWorkload, steps: int, warmup: int, device) -> dict:
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def oracle_verify_rate(name: str, budget_s: float, sample_b: int) -> dict:
-    """Positions/s of the float64 oracle on a bounded sample of the workload."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip() + f" ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _oracle_pass(kind: str, x, n: int):
+    """One oracle evaluation of the first n sequences (positions) of inputs x:
+    verify (with statistics where the config asks), row statistics or the TV
+    loss with its gradient."""
+    import oracle
+
+    if kind == "tv":
+        oracle.tv_loss(x.target[:n], x.draft[:n], x.temperature, x.grad_scale)
+    elif kind == "stats":
+        oracle.row_stats(x.target[:n], x.draft[:n], x.temperature[:n])
+    else:
+        oracle.verify(x.target[:n], x.draft[:n], x.draft_ids[:n], x.temperature[:n], x.uniforms[:n],
+                      want_stats=x.want_stats)
+
+
+def oracle_rate(name: str, threads: int, n=None, min_s: float = 0.0, x=None, kind: str = None) -> dict:
+    """Positions/s of the float64 oracle (as it stands) on `threads` host
+    threads over the first n sequences (positions) of the named config, whole
+    passes repeated until min_s seconds have passed (at least one pass)."""
     import oracle
     import workloads as W
 
-    x = W.config(name)
-    sl = slice(0, min(sample_b, x.B))
-    args = (x.target[sl], x.draft[sl], x.draft_ids[sl], x.temperature[sl], x.uniforms[sl])
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.verify(*args, want_stats=x.want_stats)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    pos = reps * (sl.stop - sl.start) * x.gamma
-    return {"value": pos / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{sl.stop - sl.start} sequences of {name} x {reps} repeats ({el:.1f} s, float64 C, OpenMP)"}
+    if x is None:
+        x = W.config(name, N_override=512) if name == "tvloss" else W.config(name)
+    kind = kind or ("tv" if name == "tvloss" else "verify")
+    units = x.N if name == "tvloss" else x.B
+    n = units if n is None else min(n, units)
+    full = oracle.num_threads()
+    oracle.set_threads(threads)
+    try:
+        _oracle_pass(kind, x, min(n, 2))  # page in the code and the first rows
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            _oracle_pass(kind, x, n)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                break
+        used = oracle.num_threads()
+    finally:
+        oracle.set_threads(full)
+    what = "positions" if name == "tvloss" else "sequences"
+    if name == "tvloss":
+        scope = f"subset: {n} positions drawn by the tvloss recipe on the host (the full config has 16384)"
+    else:
+        scope = "full config" if n == units else f"subset: the first {n} of {units} sequences"
+    return {"value": reps * n * x.gamma / el, "unit": UNIT, "cores": used, "kind": "oracle", "seconds": el,
+            "passes": reps, "sample": f"{scope}; {reps} pass(es) of {n} {what} in {el:.2f} s, float64 C, OpenMP"}
+
+
+# timed workload -> (input config, oracle call, sequences or positions timed on
+# all cores, on one core); None = the whole config
+CPU_PLAN = {"tiny": ("tiny", "verify", None, None), "verify64": ("verify64", "verify", None, 8),
+            "rl512": ("rl512", "verify", None, 32), "deep256": ("deep256", "verify", None, 8),
+            "stats256": ("deep256", "stats", None, 8), "tvloss": ("tvloss", "tv", 512, 16)}
+
+
+def cpu_baselines(headline: str, min_s: float, which: str) -> tuple:
+    """The oracle timed on the host cores: the headline config in full,
+    repeated for at least min_s seconds (the line's cpu_baseline), and with
+    which == "all" every config of the plan on all cores and on one core."""
+    import oracle
+    import workloads as W
+
+    allc = oracle.num_threads()
+    model = cpu_model()
+    head = oracle_rate(headline, allc, None, min_s)
+    head["cpu_model"] = model
+    table = None
+    if which == "all":
+        table = {"cpu_model": model, "cores_all": allc}
+        inputs = {}
+        for name, (cfg, kind, n_all, n_one) in CPU_PLAN.items():
+            if cfg not in inputs:
+                inputs[cfg] = W.config(cfg, N_override=n_all) if cfg == "tvloss" else W.config(cfg)
+            x = inputs[cfg]
+            table[name] = {"all_cores": oracle_rate(cfg, allc, n_all, 0.0, x=x, kind=kind),
+                           "one_core": oracle_rate(cfg, 1, n_one, 0.0, x=x, kind=kind)}
+        del inputs
+    return head, table
 
 
 # ------------------------------------------------------------------- main --
 
 def run_reference(args, world, rank):
-    """Reference arm: the float64 oracle timed on the host cores."""
+    """Reference arm: the float64 oracle timed on the host cores, on the
+    headline workload (rl512), each step a bounded sample of its sequences."""
     if rank != 0:
         return
     import oracle
     import workloads as W
 
-    x = W.config("verify64")
-    sample = 8
+    x = W.config("rl512")
+    sample = 32
     sl = slice(0, sample)
     a = (x.target[sl], x.draft[sl], x.draft_ids[sl], x.temperature[sl], x.uniforms[sl])
     for _ in range(args.warmup):
@@ -468,10 +549,10 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "verify64 (bounded sample: 8 of 64 sequences per step)", "B": 64, "gamma": 3,
-                   "V": 151936, "input_dtype": "bf16"},
+        "config": {"workload": f"rl512 (bounded sample: the first {sample} of 512 sequences per step)", "B": 512,
+                   "gamma": 3, "V": 151936, "input_dtype": "bf16"},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{sample} sequences of verify64 per step"},
+                         "sample": f"the first {sample} sequences of rl512 per step", "cpu_model": cpu_model()},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -535,6 +616,8 @@ def run_cuda(args, world, rank, local, pg):
             "steps": steps,
             "input_copies": wl.copies,
         }
+        tr = TRAFFIC.get(name)
+        r["traffic"] = tr["bytes"] if tr and tr.get("csrc") == csrc_hash() else None
         results[name] = r
         if head is None:
             head = (name, wl, t, t_ms, steps, clocks, alg, achieved)
@@ -551,16 +634,21 @@ def run_cuda(args, world, rank, local, pg):
     h = csrc_hash()
     traffic = TRAFFIC.get(name)
     traffic_val = traffic["bytes"] if traffic and traffic.get("csrc") == h else None
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and name not in TV_WORKLOADS:
-        cpu = oracle_verify_rate(name, args.cpu_seconds, 16)
+    cpu, cpu_table = None, None
+    if rank == 0 and world == 1 and args.cpu_baselines != "none" and name not in TV_WORKLOADS:
+        cpu, cpu_table = cpu_baselines(name, args.cpu_seconds, args.cpu_baselines)
 
+    if cpu_table:
+        for wname, r in results.items():
+            if wname in CPU_PLAN:
+                r["cpu_baseline"] = cpu_table[wname]
     if rank == 0:
         hr = results[name]
         line = {
             "metric": METRIC, "value": hr["positions_per_s"], "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": hr["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f32", "input_dtype": "bf16" if wl0.es == 2 else "f32",
+            "dtype_note": "dtype is the arithmetic type; input_dtype is the logits' storage", "data": "synthetic",
             "config": {"workload": hr["workload"], "B": wl0.B if hasattr(wl0, "B") else wl0.N, "gamma": wl0.gamma,
                        "V": wl0.V, "input_dtype": "bf16" if wl0.es == 2 else "f32",
                        "l2": f"{hr['input_copies']} rotated input copies of {hr['full_bytes_per_step'] / 1e6:.0f} MB "
@@ -574,6 +662,7 @@ def run_cuda(args, world, rank, local, pg):
                          "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)",
                          "algorithmic_bytes_per_launch": alg},
             "cpu_baseline": cpu,
+            "cpu_baselines": cpu_table,
             "e2e": e2e,
             "gpu_launches": t["launches"],
             "clocks": clocks,
@@ -595,10 +684,12 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workloads", default="verify64,rl512,deep256,stats256,diag256,to64,gumbel64,sample192,"
+    ap.add_argument("--workloads", default="rl512,verify64,deep256,stats256,diag256,to64,gumbel64,sample192,"
                                            "gsample192,tvloss,tvshared,tvtopk")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum seconds of oracle time for the headline cpu_baseline")
+    ap.add_argument("--cpu-baselines", choices=["all", "headline", "none"], default="all",
+                    help="oracle timings: every config on all cores and one core, the headline only, or none")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")
     ap.add_argument("--deep-b", type=int, default=None,
                     help="sequences of the deep256-based workloads (default 256; smaller for profiling)")

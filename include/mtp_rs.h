@@ -53,7 +53,11 @@ typedef enum {
     MTP_ERR_UNSUPPORTED_DTYPE = 2,
     MTP_ERR_MISALIGNED = 3,       /* logit base pointer not 16-byte aligned */
     MTP_ERR_CUDA = 4,             /* CUDA launch / earlier asynchronous error */
-    MTP_ERR_NO_DEVICE = 5         /* no usable cluster launch configuration */
+    MTP_ERR_TIMEOUT = 5,          /* an on-chip wait gave up.  Calls are asynchronous, so no
+                                     call returns it: the device reports the affected rows
+                                     with MTP_ROW_TIMEOUT, and the Python binding's
+                                     check_row_flags() raises this status for them. */
+    MTP_ERR_NO_DEVICE = 6         /* no usable cluster launch configuration */
 } mtp_status;
 
 typedef enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 } mtp_dtype;
@@ -333,6 +337,50 @@ int mtp_tv_loss_topk(const void *target_values, const int32_t *target_idx, const
  */
 int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size, int *clusters,
                    int *smem_bytes, int *resident_drafts);
+
+/*
+ * Kernel choices for mtp_tuning (0 = the planner's choice everywhere).
+ */
+enum {
+    MTP_KERNEL_AUTO = 0,
+    MTP_KERNEL_STREAM = 1,      /* per-warp streaming kernels (rows re-read from L2) */
+    MTP_KERNEL_RESIDENT = 2,    /* cluster-resident kernels (row slices in shared memory) */
+    MTP_KERNEL_TMEM = 3         /* tensor-memory-resident kernels (row slices parked in TMEM) */
+};
+
+/*
+ * mtp_tuning -- explicit, process-wide overrides of the launch planners, for
+ * tests and tuning sweeps.  The library reads no environment variable: the
+ * kernel a call runs depends only on its arguments, the device and the last
+ * mtp_set_tuning() of the process.  Every field 0 (or a zero-initialised
+ * struct, or mtp_set_tuning(NULL)) restores the planners' own choices.  An
+ * override that does not fit a call (a cluster size whose shared memory does
+ * not fit, say) is ignored for that call or makes the call return
+ * MTP_ERR_NO_DEVICE; outputs never depend on it beyond the documented
+ * tie-breaking of equal results.
+ */
+typedef struct mtp_tuning {
+    int cluster_size;        /* CTAs per cluster, 1..16 (streaming kernels: a power of two); 0 = planner */
+    int ring_slots;          /* streaming kernels: chunk slots per warp, 2..8; 0 = 2 */
+    int lookahead;           /* streaming verify: 0 = gamma positions streamed ahead of the last
+                                decision; d + 1 = d positions */
+    int chunk_vectors;       /* streaming kernels: 16-byte vectors per chunk, 128, 160 or 192; 0 = planner */
+    int max_clusters;        /* cap on the persistent clusters launched; 0 = every co-resident one */
+    int verify_kernel;       /* mtp_rs_verify without statistics: MTP_KERNEL_AUTO / _STREAM / _RESIDENT */
+    int tv_kernel;           /* TV loss: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM */
+    int stats_kernel;        /* mtp_row_stats: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM */
+    int tv_resident_drafts;  /* cluster-resident TV kernel: cap on draft slices kept on chip; 0 = none */
+    int tv_l2_mb;            /* streaming TV kernel: cap positions in flight so the rows they re-read
+                                fit this many MB; 0 = no cap */
+    int pair_l2_mb;          /* streaming row-pair kernel: the same cap for sequences; 0 = no cap */
+    int row_streams;         /* cluster-resident row kernel: sequences in flight per CTA, 1 or 2; 0 = planner */
+} mtp_tuning;
+
+/* Set (t != NULL) or clear (t == NULL) the overrides; affects calls made
+ * after it returns, from any thread.  Returns MTP_OK. */
+int mtp_set_tuning(const mtp_tuning *t);
+/* Copy the current overrides into *t.  MTP_ERR_INVALID_ARG if t is NULL. */
+int mtp_get_tuning(mtp_tuning *t);
 
 /* Static description of a status code. */
 const char *mtp_status_string(int status);

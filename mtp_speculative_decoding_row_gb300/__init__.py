@@ -1,7 +1,8 @@
 """Python binding of the C-ABI library ``libmtprs.so`` (see ``include/mtp_rs.h``).
 
-Argument marshalling only: each function checks tensor devices, dtypes,
-shapes and contiguity, allocates outputs with PyTorch on the inputs' device,
+Argument marshalling only: each function checks the devices, dtypes,
+shapes and contiguity of its input tensors and of any caller-supplied
+``out`` tensors, allocates missing outputs with PyTorch on the inputs' device,
 and calls the C function of the same name on the current CUDA stream.  Every
 step of the computation runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback, and importing a missing library raises.
@@ -21,7 +22,8 @@ from . import build as _build
 __all__ = [
     "mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_draft_sample", "mtp_row_stats",
     "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_tv_loss_topk",
-    "mtp_query_plan", "mtp_status_string", "MTPError", "load_library",
+    "mtp_query_plan", "mtp_status_string", "mtp_set_tuning", "mtp_get_tuning", "tuning", "check_row_flags",
+    "MTPError", "load_library", "MTP_ERR_TIMEOUT", "KERNEL_AUTO", "KERNEL_STREAM", "KERNEL_RESIDENT", "KERNEL_TMEM",
     "VerifyResult", "TOVerifyResult", "StatsResult", "DiagResult", "TVLossResult", "SampleResult", "ROW_NONFINITE",
     "ROW_BAD_ID", "ROW_BAD_TEMP", "ROW_ZERO_MASS", "ROW_BAD_UNIFORM", "ROW_TIMEOUT", "ERROR_BITS", "MAX_GAMMA", "EXPORTED_SYMBOLS",
 ]
@@ -32,7 +34,18 @@ MAX_GAMMA = 32
 DTYPE_F32, DTYPE_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("mtp_rs_verify", "mtp_to_verify", "mtp_gumbel_verify", "mtp_draft_sample", "mtp_row_stats",
                     "mtp_rs_diagnostics", "mtp_tv_loss_fwd_bwd", "mtp_tv_loss_ex", "mtp_tv_loss_topk",
-                    "mtp_query_plan", "mtp_status_string")
+                    "mtp_query_plan", "mtp_set_tuning", "mtp_get_tuning", "mtp_status_string")
+MTP_OK, MTP_ERR_INVALID_ARG, MTP_ERR_UNSUPPORTED_DTYPE, MTP_ERR_MISALIGNED, MTP_ERR_CUDA, MTP_ERR_TIMEOUT, \
+    MTP_ERR_NO_DEVICE = range(7)
+KERNEL_AUTO, KERNEL_STREAM, KERNEL_RESIDENT, KERNEL_TMEM = range(4)
+TUNING_FIELDS = ("cluster_size", "ring_slots", "lookahead", "chunk_vectors", "max_clusters", "verify_kernel",
+                 "tv_kernel", "stats_kernel", "tv_resident_drafts", "tv_l2_mb", "pair_l2_mb", "row_streams")
+
+
+class _Tuning(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in TUNING_FIELDS]
+
+
 PLAN_OPS = {"verify": 0, "verify_stats": 1, "row_stats": 2, "tv_loss": 3, "verify_resident": 4,
             "tv_loss_resident": 5, "diagnostics": 6, "row_stats_resident": 7, "to_verify": 8, "gumbel_verify": 9,
             "draft_sample": 10, "draft_sample_gumbel": 11}
@@ -82,6 +95,10 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False):
     lib.mtp_tv_loss_fwd_bwd.restype = I
     lib.mtp_query_plan.argtypes = [I, I, I, I, I, P, P, P, P]
     lib.mtp_query_plan.restype = I
+    lib.mtp_set_tuning.argtypes = [P]
+    lib.mtp_set_tuning.restype = I
+    lib.mtp_get_tuning.argtypes = [P]
+    lib.mtp_get_tuning.restype = I
     lib.mtp_status_string.argtypes = [I]
     lib.mtp_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -106,6 +123,56 @@ def mtp_status_string(status: int) -> str:
     return load_library().mtp_status_string(int(status)).decode()
 
 
+def mtp_set_tuning(**fields) -> None:
+    """Set the process-wide planner overrides (see mtp_tuning in
+    include/mtp_rs.h); no argument clears them.  Field names: TUNING_FIELDS;
+    a value of 0 or None keeps the planner's choice for that field."""
+    unknown = set(fields) - set(TUNING_FIELDS)
+    if unknown:
+        raise ValueError(f"unknown tuning fields {sorted(unknown)}")
+    t = _Tuning(*(int(fields.get(name) or 0) for name in TUNING_FIELDS))
+    rc = load_library().mtp_set_tuning(ctypes.byref(t))
+    if rc:
+        raise MTPError("mtp_set_tuning", rc)
+
+
+def mtp_get_tuning() -> dict:
+    t = _Tuning()
+    rc = load_library().mtp_get_tuning(ctypes.byref(t))
+    if rc:
+        raise MTPError("mtp_get_tuning", rc)
+    return {name: getattr(t, name) for name in TUNING_FIELDS}
+
+
+class tuning:
+    """Context manager: planner overrides for the calls made inside it, the
+    previous overrides restored on exit (``with tuning(cluster_size=8): ...``).
+    Fields given as None keep the planner's choice."""
+
+    def __init__(self, **fields):
+        self.fields = fields
+
+    def __enter__(self):
+        self.old = mtp_get_tuning()
+        new = dict(self.old)
+        new.update({k: (v or 0) for k, v in self.fields.items()})
+        mtp_set_tuning(**new)
+        return self
+
+    def __exit__(self, *exc):
+        mtp_set_tuning(**self.old)
+        return False
+
+
+def check_row_flags(row_flags) -> None:
+    """Raise MTPError(MTP_ERR_TIMEOUT) if any row of a finished call carries
+    ROW_TIMEOUT (an on-chip wait gave up).  Synchronises with the tensor's
+    stream by reading it back."""
+    flags = row_flags.cpu() if hasattr(row_flags, "cpu") else row_flags
+    if bool(((flags & ROW_TIMEOUT) != 0).any()):
+        raise MTPError("device", MTP_ERR_TIMEOUT)
+
+
 # ------------------------------------------------------------ marshalling --
 
 def _torch():
@@ -126,14 +193,31 @@ def _dtype_code(t) -> int:
 def _check(t, name, device, dtype=None, shape=None):
     if t is None:
         raise ValueError(f"{name} is required")
-    if not t.is_cuda or t.device != device:
-        raise ValueError(f"{name} must be a CUDA tensor on {device}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and (not t.is_cuda or t.device != device):
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+
+
+def _check_out(out, specs, device, fn: str):
+    """Check every field of a caller-supplied result tuple: (name, dtype,
+    shape, required).  A missing required field, or a field of another
+    device, dtype or shape, or non-contiguous, raises before any launch."""
+    given = []
+    for name, dtype, shape, required in specs:
+        t = getattr(out, name)
+        if t is None:
+            if required:
+                raise ValueError(f"{fn}: out.{name} is required")
+            continue
+        _check(t, f"out.{name}", None, dtype, shape)
+        given.append((t, name))
+    for t, name in given:
+        _check(t, f"out.{name}", device)
 
 
 def _ptr(t):
@@ -195,6 +279,12 @@ def mtp_rs_verify(target_logits, draft_logits, draft_ids, temperature, uniforms,
     dev = target_logits.device
     B, g1, V = target_logits.shape
     gamma = g1 - 1
+    if out is not None:
+        if (out.alpha is None) != (out.entropy is None) or (out.alpha is not None) != bool(with_stats):
+            raise ValueError("mtp_rs_verify: out.alpha and out.entropy must both be given iff with_stats")
+        _check_out(out, [("tokens", torch.int32, (B, gamma + 1), True), ("accept_len", torch.int32, (B,), True),
+                         ("alpha", torch.float32, (B, gamma), False), ("entropy", torch.float32, (B, gamma + 1), False),
+                         ("row_flags", torch.int32, (B,), False)], dev, "mtp_rs_verify")
     _check(target_logits, "target_logits", dev)
     _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
     _check(draft_ids, "draft_ids", dev, torch.int32, (B, gamma))
@@ -226,6 +316,10 @@ def mtp_to_verify(target_logits, draft_logits, temperature, uniforms, *, out: Op
     dev = target_logits.device
     B, g1, V = target_logits.shape
     gamma = g1 - 1
+    if out is not None:
+        _check_out(out, [("tokens", torch.int32, (B, gamma + 1), True), ("accept_len", torch.int32, (B,), True),
+                         ("draft_tokens", torch.int32, (B, gamma), False), ("row_flags", torch.int32, (B,), False)],
+                   dev, "mtp_to_verify")
     _check(target_logits, "target_logits", dev)
     _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
     _check(temperature, "temperature", dev, torch.float32, (B,))
@@ -255,6 +349,11 @@ def mtp_gumbel_verify(target_logits, draft_logits, draft_ids, temperature, unifo
     dev = target_logits.device
     B, g1, V = target_logits.shape
     gamma = g1 - 1
+    if out is not None:
+        if out.alpha is not None or out.entropy is not None:
+            raise ValueError("mtp_gumbel_verify: out.alpha and out.entropy must be None")
+        _check_out(out, [("tokens", torch.int32, (B, g1), True), ("accept_len", torch.int32, (B,), True),
+                         ("row_flags", torch.int32, (B,), False)], dev, "mtp_gumbel_verify")
     _check(target_logits, "target_logits", dev)
     _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
     _check(draft_ids, "draft_ids", dev, torch.int32, (B, gamma))
@@ -287,6 +386,9 @@ def mtp_draft_sample(draft_logits, temperature, uniforms=None, *, method: str = 
     dev = draft_logits.device
     V = draft_logits.shape[-1]
     R = draft_logits.numel() // V if V else 0
+    if out is not None:
+        _check_out(out, [("ids", torch.int32, (R,), True), ("row_flags", torch.int32, (R,), False)], dev,
+                   "mtp_draft_sample")
     _check(draft_logits, "draft_logits", dev)
     _check(temperature, "temperature", dev, torch.float32)
     if temperature.numel() != R:
@@ -317,6 +419,9 @@ def mtp_row_stats(target_logits, draft_logits, temperature, *, out: Optional[Sta
     dev = target_logits.device
     B, g1, V = target_logits.shape
     gamma = g1 - 1
+    if out is not None:
+        _check_out(out, [("alpha", torch.float32, (B, gamma), True), ("entropy", torch.float32, (B, g1), True),
+                         ("row_flags", torch.int32, (B,), False)], dev, "mtp_row_stats")
     _check(target_logits, "target_logits", dev)
     _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
     _check(temperature, "temperature", dev, torch.float32, (B,))
@@ -341,6 +446,13 @@ def mtp_rs_diagnostics(target_logits, draft_logits, temperature, *, out: Optiona
     dev = target_logits.device
     B, g1, V = target_logits.shape
     gamma = g1 - 1
+    if out is not None:
+        f32, i32 = torch.float32, torch.int32
+        _check_out(out, [("alpha", f32, (B, gamma), False), ("ent_p", f32, (B, g1), False),
+                         ("ent_q", f32, (B, gamma), False), ("kl", f32, (B, gamma), False),
+                         ("yhat", i32, (B, gamma), False), ("p_yhat", f32, (B, gamma), False),
+                         ("rs_better", i32, (B, gamma), False), ("row_flags", i32, (B,), False)], dev,
+                   "mtp_rs_diagnostics")
     _check(target_logits, "target_logits", dev)
     _check(draft_logits, "draft_logits", dev, target_logits.dtype, (B, gamma, V))
     _check(temperature, "temperature", dev, torch.float32, (B,))
@@ -368,6 +480,10 @@ def mtp_tv_loss_topk(target_values, target_idx, draft_logits, temperature: float
     dev = draft_logits.device
     N, gamma, V = draft_logits.shape
     K = target_values.shape[-1]
+    if out is not None:
+        _check_out(out, [("loss", torch.float32, (N,), True), ("alpha", torch.float32, (N, gamma), False),
+                         ("grad", torch.float32, (N, gamma, V), True), ("row_flags", torch.int32, (N,), False)], dev,
+                   "mtp_tv_loss_topk")
     _check(draft_logits, "draft_logits", dev)
     _check(target_values, "target_values", dev, draft_logits.dtype, (N, gamma, K))
     _check(target_idx, "target_idx", dev, torch.int32, (N, gamma, K))
@@ -397,6 +513,10 @@ def mtp_tv_loss_fwd_bwd(target_logits, draft_logits, temperature: float = 1.0, g
     torch = _torch()
     dev = draft_logits.device
     N, gamma, V = draft_logits.shape
+    if out is not None:
+        _check_out(out, [("loss", torch.float32, (N,), True), ("alpha", torch.float32, (N, gamma), False),
+                         ("grad", torch.float32, (N, gamma, V), True), ("row_flags", torch.int32, (N,), False)], dev,
+                   "mtp_tv_loss_fwd_bwd")
     _check(draft_logits, "draft_logits", dev)
     if shared_target:
         if target_logits.dim() != 2 or target_logits.shape[0] < N + gamma - 1 or target_logits.shape[1] != V:

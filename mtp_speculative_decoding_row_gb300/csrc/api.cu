@@ -3,7 +3,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -44,16 +43,18 @@ std::mutex g_mu;
 std::vector<CacheEntry> g_cache;
 std::vector<std::pair<int, const void *>> g_attr_done;
 
-int env_cluster() {
-    const char *e = std::getenv("MTP_RS_CLUSTER");
-    if (!e) return 0;
-    const int c = std::atoi(e);
-    return (c == 1 || c == 2 || c == 4 || c == 8 || c == 16) ? c : 0;
+// Process-wide tuning overrides (mtp_set_tuning); all zero = the planners'
+// own choices.  Read under the lock, once per call.
+mtp_tuning g_tune = {};
+
+mtp_tuning tuning() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_tune;
 }
 
-int env_int(const char *name) {
-    const char *e = std::getenv(name);
-    return e ? std::atoi(e) : 0;
+int tuned_cluster(const mtp_tuning &t) {
+    const int c = t.cluster_size;
+    return (c == 1 || c == 2 || c == 4 || c == 8 || c == 16) ? c : 0;
 }
 
 // Set the function attributes once per device and kernel.
@@ -117,8 +118,9 @@ uint32_t smem_optin(int dev) {
 // keep the most sequence slices in flight for `units` sequences; the grid is
 // the co-resident cluster count.
 bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
-    const int forced = env_cluster();
-    const int forced_ns = env_int("MTP_RS_STREAMS");
+    const mtp_tuning tu = tuning();
+    const int forced = tu.cluster_size;
+    const int forced_ns = tu.row_streams;
     const uint32_t cap = smem_optin(dev);
     long best = -1;
     for (int ns = 1; ns <= 2; ++ns) {
@@ -131,8 +133,7 @@ bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
             const int nc = max_clusters(dev, func, C, smem, row_threads());
             if (nc <= 0) continue;
             int used = nc < units ? nc : units;
-            const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
-            if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+            if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
             const long inflight = static_cast<long>(nc) * ns < units ? static_cast<long>(nc) * ns : units;
             const long score = inflight * C * 4 + used;  // slices in flight, then clusters used
             if (score > best) {
@@ -151,8 +152,7 @@ bool plan_row(int dev, const void *func, int V, int es, int units, Plan &p) {
 // hold at least 64 vectors (or C = 1) and at most the chunk-list limit; ties
 // go to more busy CTAs.
 bool stream_usable(int V, int es, int gamma) {
-    const char *e = std::getenv("MTP_RS_VERIFY_KERNEL");
-    if (e && e[0] == 'r') return false;  // "resident"
+    if (tuning().verify_kernel == MTP_KERNEL_RESIDENT) return false;
     return gamma <= stream_max_gamma() && V % (16 / es) == 0;
 }
 
@@ -166,7 +166,7 @@ bool stream_usable(int V, int es, int gamma) {
 // diagnostics (fewer chunks than 2 KB, four CTAs per SM still fit, unlike
 // 3 KB).
 int stream_chunk_for(int nvs, int mode = -1) {
-    const int forced = env_int("MTP_RS_CHUNK");
+    const int forced = tuning().chunk_vectors;
     if (forced == 128 || forced == 192) return forced;
     if (forced == 160 && (mode == 0 || mode == 3 || mode == 4)) return forced;
     if (mode == 0 || mode == 3 || mode == 4) return 160;
@@ -175,12 +175,12 @@ int stream_chunk_for(int nvs, int mode = -1) {
 
 bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, int mode = 0,
                  bool dbl = false) {
-    const int forced = env_cluster();
-    int R = env_int("MTP_RS_RING");
+    const mtp_tuning tu = tuning();
+    const int forced = tuned_cluster(tu);
+    int R = tu.ring_slots;
     if (R < 2 || R > stream_max_ring()) R = 2;
     int depth = gamma;  // stream every position without waiting for decisions
-    const char *de = std::getenv("MTP_RS_DEPTH");
-    if (de) depth = std::atoi(de);
+    if (tu.lookahead > 0) depth = tu.lookahead - 1;
     if (depth < 0) depth = 0;
     if (depth > gamma) depth = gamma;
     const uint32_t cap = smem_optin(dev);
@@ -205,8 +205,7 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
         const int nc = max_clusters(dev, func, C, smem, stream_threads());
         if (nc <= 0) continue;
         int used = nc < units ? nc : units;
-        const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
-        if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+        if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
         // per wave: the sequence's share of the row (1 / C) plus a fixed
         // latency term (exchanges, decision, sampling)
         const double est = static_cast<double>((units + used - 1) / used) * (1.0 / C + 0.03);
@@ -238,16 +237,16 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
 // the positions in flight are capped only when MTP_RS_TV_L2MB sets an L2
 // budget for the 2 gamma rows a position re-reads.
 bool tvs_usable(int V, int es, int gamma) {
-    const char *e = std::getenv("MTP_RS_TV_KERNEL");
-    if (e && e[0] == 'r') return false;  // "resident"
+    if (tuning().tv_kernel == MTP_KERNEL_RESIDENT) return false;
     return gamma <= tvs_max_gamma() && V % (16 / es) == 0;
 }
 
 bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, bool topk = false) {
-    const int forced = env_cluster();
-    int R = env_int("MTP_RS_RING");
+    const mtp_tuning tu = tuning();
+    const int forced = tuned_cluster(tu);
+    int R = tu.ring_slots;
     if (R < 2 || R > stream_max_ring()) R = 2;
-    const int l2mb = env_int("MTP_RS_TV_L2MB");
+    const int l2mb = tu.tv_l2_mb;
     const double pos_bytes = 2.0 * gamma * static_cast<double>(V) * es;
     int cap_l2 = l2mb > 0 ? static_cast<int>((static_cast<double>(l2mb) * 1048576.0) / pos_bytes) : 1 << 30;
     if (cap_l2 < 1) cap_l2 = 1;
@@ -271,8 +270,7 @@ bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, 
         if (nc <= 0) continue;
         int used = nc < units ? nc : units;
         if (used > cap_l2) used = cap_l2;
-        const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
-        if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+        if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
         const long warps = static_cast<long>(used) * C * nw;
         // the most warps in flight; within 5 % the larger cluster
         if (!found || warps * 20 > best * 21 || (warps * 21 >= best * 20 && C > p.C)) {
@@ -295,8 +293,9 @@ bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, 
 // Persistent TV kernel: two target slots, nres (>= 2, ideally gamma) draft
 // slots and gamma rows of indicator bits per CTA.
 bool plan_tv(int dev, const void *func, int V, int es, int gamma, int units, Plan &p) {
-    const int forced = env_cluster();
-    const int cap_nres = env_int("MTP_RS_TV_NRES");
+    const mtp_tuning tu = tuning();
+    const int forced = tu.cluster_size;
+    const int cap_nres = tu.tv_resident_drafts;
     const uint32_t cap = smem_optin(dev);
     long best = -1;
     for (int C = 1; C <= MAX_C; ++C) {
@@ -413,16 +412,14 @@ bool pairs_usable(int V, int es, int gamma) {
     return gamma <= pair_max_gamma() && V % (16 / es) == 0;
 }
 
-bool stats_streamed() {
-    const char *e = std::getenv("MTP_RS_STATS_KERNEL");
-    return e && e[0] == 's';  // "stream"
-}
+bool stats_streamed() { return tuning().stats_kernel == MTP_KERNEL_STREAM; }
 
 bool plan_pairs(int dev, int dtype, int V, int es, int gamma, int units, int mode, Plan &p) {
-    const int forced = env_cluster();
-    int R = env_int("MTP_RS_RING");
+    const mtp_tuning tu = tuning();
+    const int forced = tuned_cluster(tu);
+    int R = tu.ring_slots;
     if (R < 2 || R > pair_max_ring()) R = 2;
-    const int l2mb = env_int("MTP_RS_PAIR_L2MB");
+    const int l2mb = tu.pair_l2_mb;
     const double seq_bytes = 2.0 * static_cast<double>(V) * es;  // the row pair a sequence re-reads next
     int cap_l2 = l2mb > 0 ? static_cast<int>((static_cast<double>(l2mb) * 1048576.0) / seq_bytes) : 1 << 30;
     if (cap_l2 < 1) cap_l2 = 1;
@@ -447,8 +444,7 @@ bool plan_pairs(int dev, int dtype, int V, int es, int gamma, int units, int mod
         if (nc <= 0) continue;
         int used = nc < units ? nc : units;
         if (used > cap_l2) used = cap_l2;
-        const int cap_nc = env_int("MTP_RS_MAX_CLUSTERS");
-        if (cap_nc > 0 && used > cap_nc) used = cap_nc;
+        if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
         const long warps = static_cast<long>(used) * C * nw;
         if (!found || warps * 20 > best * 21 || (warps * 21 >= best * 20 && C > p.C)) {
             if (warps > best) best = warps;
@@ -801,6 +797,20 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     return MTP_OK;
 }
 
+extern "C" int mtp_set_tuning(const mtp_tuning *t) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (t) g_tune = *t;
+    else g_tune = mtp_tuning{};
+    return MTP_OK;
+}
+
+extern "C" int mtp_get_tuning(mtp_tuning *t) {
+    if (!t) return MTP_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    *t = g_tune;
+    return MTP_OK;
+}
+
 extern "C" const char *mtp_status_string(int status) {
     switch (status) {
         case MTP_OK: return "ok";
@@ -808,6 +818,7 @@ extern "C" const char *mtp_status_string(int status) {
         case MTP_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
         case MTP_ERR_MISALIGNED: return "logit or gradient base pointer not 16-byte aligned";
         case MTP_ERR_CUDA: return "CUDA error";
+        case MTP_ERR_TIMEOUT: return "an on-chip wait gave up (rows flagged MTP_ROW_TIMEOUT)";
         case MTP_ERR_NO_DEVICE: return "no usable cluster launch configuration on this device";
         default: return "unknown status";
     }

@@ -251,23 +251,22 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
     bool dead = false;
     int pc = 0;  // pairs consumed by this CTA (target slot = pc & 1)
 
+    // A slot's phase advances only when its copy has landed: after a wait
+    // that gave up the slot stays armed (the CTA is then dead and issues no
+    // further copy), and the drain before exit waits for it once more.
     auto wait_t = [&](int sl) -> bool {
-        bool ok = true;
-        if (tarm & (1u << sl)) {
-            ok = mbar_wait_bounded(smem_addr(&sh.tbar[sl]), (tph >> sl) & 1u);
-            tph ^= 1u << sl;
-            tarm &= ~(1u << sl);
-        }
-        return ok;
+        if (!(tarm & (1u << sl))) return true;
+        if (!mbar_wait_bounded(smem_addr(&sh.tbar[sl]), (tph >> sl) & 1u)) return false;
+        tph ^= 1u << sl;
+        tarm &= ~(1u << sl);
+        return true;
     };
     auto wait_d = [&](int sl) -> bool {
-        bool ok = true;
-        if (darm & (1u << sl)) {
-            ok = mbar_wait_bounded(smem_addr(&sh.dbar[sl]), (dph >> sl) & 1u);
-            dph ^= 1u << sl;
-            darm &= ~(1u << sl);
-        }
-        return ok;
+        if (!(darm & (1u << sl))) return true;
+        if (!mbar_wait_bounded(smem_addr(&sh.dbar[sl]), (dph >> sl) & 1u)) return false;
+        dph ^= 1u << sl;
+        darm &= ~(1u << sl);
+        return true;
     };
     auto load_t = [&](int t, int kk, int sl) {
         if (aligned && s.nvec > 0) {
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
             unsigned char *db = dres + static_cast<size_t>(ds) * A.slice_bytes;
             int tmo = 0;
             if (!bad_temp && !dead && !d_issued) load_d(t, kk, ds);
-            if (!bad_temp) {
+            if (!bad_temp && !dead) {
                 if (!wait_t(ts)) tmo = 1;
                 if (!wait_d(ds)) tmo = 1;
                 if (!aligned) {
@@ -313,7 +312,11 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
                     load_slice<Tin, NT>(s, tv_row<Tin>(A.draft, t, kk, g, V), db, 0, false);
                 }
             }
-            __syncthreads();
+            // one verdict for the CTA: a slice that did not arrive ends its work
+            if (__syncthreads_or(tmo)) {
+                tmo = 1;
+                dead = true;
+            }
             // prefetch the next pair: (t, kk+1), or the next position's first target
             if (!bad_temp && !dead) {
                 d_issued = false;
@@ -440,16 +443,21 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
                 } else {  // re-read a draft slice that did not stay on chip
                     const int sl = (pc - 1) & 1;  // the last pair's target slot is free
                     const unsigned char *drow = tv_row<Tin>(A.draft, t, kk, g, V);
+                    bool arrived = true;
                     if (aligned) {
                         if (s.nvec > 0) {
                             issue_row<Tin>(s, drow, tslot[sl], smem_addr(&sh.tbar[sl]));
                             tarm |= 1u << sl;
                         }
-                        wait_t(sl);
+                        arrived = wait_t(sl);
                     } else {
                         load_slice<Tin, NT>(s, drow, tslot[sl], 0, false);
                     }
-                    __syncthreads();
+                    if (!__syncthreads_and(arrived ? 1 : 0)) {  // the re-read slice did not arrive
+                        dead = true;
+                        flags |= F_TIMEOUT;
+                        break;
+                    }
                     db = tslot[sl];
                 }
                 const float coef = A.grad_scale * sh.gk[kk] / T;
@@ -492,7 +500,8 @@ __global__ void __launch_bounds__(NT, 2) tv_kernel_impl(const TVArgs A) {
                     d_issued = true;
                 }
             }
-        } else {
+        }
+        if (flags) {  // a flagged position (also one that timed out above) gets a zero gradient
             for (int kk = 0; kk < g; ++kk) {
                 float *out = gbase + static_cast<size_t>(kk) * V;
                 for (int v = s.lo + tid; v < s.hi; v += NT) out[v] = 0.f;

@@ -60,6 +60,8 @@ def _load():
             lib.oracle_tv_loss_topk.argtypes = [P, P, P, I, D, I, I, I, I, D, I, I, D, P, P, P, P, P, P]
             lib.oracle_draft_sample.argtypes = [P, I, P, P, I, U32, U32, U32, I, I, P, P, P]
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_set_threads.argtypes = [I]
+            lib.oracle_set_threads.restype = None
             for f in (lib.oracle_softmax, lib.oracle_verify, lib.oracle_row_stats, lib.oracle_tv_loss,
                       lib.oracle_num_threads):
                 f.restype = I
@@ -85,6 +87,12 @@ def _ptr(a):
 def num_threads() -> int:
     """Threads the oracle's parallel loops use (OMP_NUM_THREADS respected)."""
     return _load().oracle_num_threads()
+
+
+def set_threads(n: int) -> None:
+    """Thread count of the oracle's later parallel loops (benchmark timing on a
+    stated number of cores).  Results do not depend on it."""
+    _load().oracle_set_threads(int(n))
 
 
 def softmax(z, T: float = 1.0) -> np.ndarray:

@@ -1048,6 +1048,17 @@ int oracle_tv_loss_topk(const void *values, const int32_t *idx, const void *draf
     return fail ? 2 : 0;
 }
 
+/* Thread count of later parallel regions (timing runs on a stated number
+ * of cores; n <= 0 leaves it unchanged).  No arithmetic depends on it. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_num_threads(void)
 {

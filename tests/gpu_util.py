@@ -1,8 +1,5 @@
 """Helpers shared by the GPU tests: upload host inputs, run the library,
 bring outputs back as NumPy arrays."""
-import os
-from contextlib import contextmanager
-
 import numpy as np
 import torch
 
@@ -31,22 +28,18 @@ def to_host_bits(t) -> np.ndarray:
     return t.cpu().numpy()
 
 
-@contextmanager
-def env(**kv):
-    old = {k: os.environ.get(k) for k in kv}
-    for k, v in kv.items():
-        if v is None:
-            os.environ.pop(k, None)
-        else:
-            os.environ[k] = str(v)
-    try:
-        yield
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
+KERNELS = {None: mtp.KERNEL_AUTO, "stream": mtp.KERNEL_STREAM, "resident": mtp.KERNEL_RESIDENT,
+           "tmem": mtp.KERNEL_TMEM}
+
+
+def kcode(name):
+    """Kernel choice name (None, "stream", "resident", "tmem") -> mtp_tuning code."""
+    return KERNELS[name]
+
+
+def tune(**fields):
+    """Planner overrides through the library's tuning API for a with-block."""
+    return mtp.tuning(**fields)
 
 
 def run_verify(x, with_stats=False):
