@@ -572,6 +572,9 @@ def run_cuda(args, world, rank, local, pg):
         mtp_build.build()
     barrier(pg, device)
     mtp.load_library()
+    if args.tv_kernel != "auto":
+        mtp.mtp_set_tuning(tv_kernel={"tmem": mtp.KERNEL_TMEM, "stream": mtp.KERNEL_STREAM,
+                                      "resident": mtp.KERNEL_RESIDENT}[args.tv_kernel])
     peaks = load_peaks()
     peak = peaks["hbm_gbs"]
     uuid = str(torch.cuda.get_device_properties(device).uuid)
@@ -691,6 +694,8 @@ def main():
     ap.add_argument("--cpu-baselines", choices=["all", "headline", "none"], default="all",
                     help="oracle timings: every config on all cores and one core, the headline only, or none")
     ap.add_argument("--tv-n", type=int, default=None, help="TV-loss positions (default 16384; smaller for profiling)")
+    ap.add_argument("--tv-kernel", choices=["auto", "tmem", "stream", "resident"], default="auto",
+                    help="TV-loss kernel (the library's tuning API; auto = the planner's choice)")
     ap.add_argument("--deep-b", type=int, default=None,
                     help="sequences of the deep256-based workloads (default 256; smaller for profiling)")
     args = ap.parse_args()

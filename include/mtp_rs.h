@@ -367,7 +367,8 @@ typedef struct mtp_tuning {
     int chunk_vectors;       /* streaming kernels: 16-byte vectors per chunk, 128, 160 or 192; 0 = planner */
     int max_clusters;        /* cap on the persistent clusters launched; 0 = every co-resident one */
     int verify_kernel;       /* mtp_rs_verify without statistics: MTP_KERNEL_AUTO / _STREAM / _RESIDENT */
-    int tv_kernel;           /* TV loss: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM */
+    int tv_kernel;           /* TV loss: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM (_TMEM where a
+                                position's draft rows fit in tensor memory, else as _AUTO) */
     int stats_kernel;        /* mtp_row_stats: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM */
     int tv_resident_drafts;  /* cluster-resident TV kernel: cap on draft slices kept on chip; 0 = none */
     int tv_l2_mb;            /* streaming TV kernel: cap positions in flight so the rows they re-read

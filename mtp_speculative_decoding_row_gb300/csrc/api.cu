@@ -237,7 +237,7 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
 // the positions in flight are capped only when MTP_RS_TV_L2MB sets an L2
 // budget for the 2 gamma rows a position re-reads.
 bool tvs_usable(int V, int es, int gamma) {
-    if (tuning().tv_kernel == MTP_KERNEL_RESIDENT) return false;
+    if (tuning().tv_kernel == MTP_KERNEL_RESIDENT) return false;  // a TMEM request that does not fit streams
     return gamma <= tvs_max_gamma() && V % (16 / es) == 0;
 }
 
@@ -288,6 +288,74 @@ bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, 
         }
     }
     return found;
+}
+
+// TMEM-resident TV kernel: clusters of C CTAs x 16 warps, one CTA per SM
+// holding all 512 TMEM columns, in which its warps park their segments of
+// the position's gamma draft rows (NS 16-byte vectors per lane and row, 4
+// columns each, 128 columns per warp).  The warps of a CTA form teams that
+// work on different positions; a segment is 1 / (C x team warps) of a row.  The smallest power-of-two C whose
+// segments fit wins (the most positions in flight).  TMEM allocation blocks
+// until columns are free, so the shared memory asked for keeps a second CTA
+// off the SM: more than half of the SM's shared memory.
+bool tvm_usable(int V, int es, int gamma) {
+    if (tuning().tv_kernel != MTP_KERNEL_TMEM) return false;  // measured slower than streaming: on request only
+    return gamma <= tvm_max_gamma() && V % (16 / es) == 0;
+}
+
+bool plan_tvm(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) {
+    const mtp_tuning tu = tuning();
+    const int forced = tuned_cluster(tu);
+    int per_sm = 0, reserved = 0;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    const uint32_t hi = smem_optin(dev);
+    const uint32_t lo = static_cast<uint32_t>(per_sm / 2 - reserved + 128) & ~127u;  // 2 CTAs do not fit
+    const int nv = V / (16 / es);
+    const int ns_set[] = {2, 4, 5, 8, 10};
+    for (int C = 1; C <= tvm_max_cluster(); C *= 2) {
+        if (forced && C != forced) continue;
+        const int S = C * tvm_team_warps();
+        const int nvs = (nv + S - 1) / S;
+        const int need = (nvs + 31) / 32;
+        int ns = 0;
+        for (int c : ns_set)
+            if (c >= need) {
+                ns = c;
+                break;
+            }
+        if (!ns || gamma * ns * 4 > tvm_warp_cols()) continue;
+        int R = tu.ring_slots;
+        if (R < 2 || R > tvm_max_ring()) R = tvm_max_ring();
+        while (R >= 2 && tvm_smem_bytes(gamma, C, ns, R) > hi) --R;
+        if (R < 2) continue;
+        uint32_t smem = tvm_smem_bytes(gamma, C, ns, R);
+        if (smem < lo) smem = lo;  // padding: keeps a second CTA (and its TMEM allocation) off the SM
+        if (smem > hi || lo > hi) continue;
+        const void *func = tvm_kernel(dtype, ns);
+        if (!func) continue;
+        if (prepare_func(dev, func) != cudaSuccess) return false;
+        const int nc = max_clusters(dev, func, C, smem, tvm_threads());
+        if (nc <= 0) continue;
+        // every cluster takes tvm_teams() positions at a time
+        const int want = (units + tvm_teams() - 1) / tvm_teams();
+        int used = nc < want ? nc : want;
+        if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
+        p = Plan{};
+        p.C = C;
+        p.smem = smem;
+        p.clusters = used;
+        p.threads = tvm_threads();
+        p.ring = R;
+        p.seg_vectors = nvs;
+        p.nres = gamma;  // every draft row of a position stays on chip
+        p.func = func;
+        return true;
+    }
+    return false;
 }
 
 // Persistent TV kernel: two target slots, nres (>= 2, ideally gamma) draft
@@ -673,7 +741,8 @@ extern "C" int mtp_tv_loss_ex(const void *target_logits, const void *draft_logit
     const int d = dtype == MTP_DTYPE_F32 ? 0 : 1;
     const void *func = nullptr;
     Plan p;
-    if (tvs_usable(V, es, gamma) && plan_tvs(dev, d, V, es, gamma, N, p)) func = p.func;
+    if (tvm_usable(V, es, gamma) && plan_tvm(dev, d, V, es, gamma, N, p)) func = p.func;
+    if (!func && tvs_usable(V, es, gamma) && plan_tvs(dev, d, V, es, gamma, N, p)) func = p.func;
     if (!func) {
         func = tv_kernel(d);
         if (prepare_func(dev, func) != cudaSuccess) return MTP_ERR_CUDA;
@@ -764,7 +833,8 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     Plan p;
     bool ok = false, streamed = false;
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
-    if (op == 3 && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
+    if (op == 3 && tvm_usable(V, es, gamma)) ok = plan_tvm(dev, d, V, es, gamma, units, p);
+    if (op == 3 && !ok && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
     if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
     if (op == 10 || op == 11) {  // draft sampling (inverse CDF, Gumbel-max): one-row sequences of the streaming kernel
         if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;

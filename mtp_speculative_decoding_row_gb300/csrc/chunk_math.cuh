@@ -187,4 +187,96 @@ __device__ __forceinline__ void argmax_merge(float &v, int &i, float &x, float o
     }
 }
 
+// ------------------------------------------- TV loss: overlap and gradient --
+
+// Fold every word of the lane's chunk registers into one value.  Consuming
+// the registers completes the shared-memory loads that filled them, so the
+// slot can be handed back to the producer before the chunk is processed.
+template <int QV>
+__device__ __forceinline__ uint32_t consume_regs(const uint4 (&r)[QV]) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int q = 0; q < QV; ++q) x ^= r[q].x ^ r[q].y ^ r[q].z ^ r[q].w;
+    return x;
+}
+
+// Merge two softmax partials (m, s); a NaN sum propagates.
+__device__ __forceinline__ Soft soft_pair_merge(const Soft &a, const Soft &b, float k) {
+    Soft r;
+    r.m = fmaxf(a.m, b.m);
+    r.s = 0.f;
+    r.s1 = 0.f;
+    if (a.s != 0.f) r.s += a.s * ex2((a.m - r.m) * k);
+    if (b.s != 0.f) r.s += b.s * ex2((b.m - r.m) * k);
+    return r;
+}
+
+// One lane's partial overlap sums over one chunk (registers): alpha =
+// sum 2^{min(lp, lq)}, S = sum over lq <= lp of the same, and the indicator
+// byte of each vector (bit e: q <= p for element e).
+template <typename Tin, int QV>
+__device__ __forceinline__ void ovl_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], float k, float ct, float cd,
+                                         float &acc_a, float &acc_s, uint32_t (&m)[QV]) {
+    const uint64_t K2 = f2pack(k, k), NCT = f2pack(-ct, -ct), NCD = f2pack(-cd, -cd);
+    uint64_t aa = f2pack(0.f, 0.f), as = f2pack(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        const uint32_t wt[4] = {rt[q].x, rt[q].y, rt[q].z, rt[q].w}, wd[4] = {rd[q].x, rd[q].y, rd[q].z, rd[q].w};
+        uint32_t bb = 0;
+#pragma unroll
+        for (int h = 0; h < (Store<Tin>::ES == 2 ? 4 : 2); ++h) {
+            uint64_t zt2, zd2;
+            if (Store<Tin>::ES == 2) {
+                zt2 = bf16pair_f2(wt[h]);
+                zd2 = bf16pair_f2(wd[h]);
+            } else {
+                zt2 = f2pack(__uint_as_float(wt[2 * h]), __uint_as_float(wt[2 * h + 1]));
+                zd2 = f2pack(__uint_as_float(wd[2 * h]), __uint_as_float(wd[2 * h + 1]));
+            }
+            float lp0, lp1, lq0, lq1;
+            f2unpack(f2fma(zt2, K2, NCT), lp0, lp1);
+            f2unpack(f2fma(zd2, K2, NCD), lq0, lq1);
+            const float x0 = ex2(fminf(lp0, lq0)), x1 = ex2(fminf(lp1, lq1));
+            const bool b0 = lq0 <= lp0, b1 = lq1 <= lp1;
+            aa = f2add(aa, f2pack(x0, x1));
+            as = f2add(as, f2pack(b0 ? x0 : 0.f, b1 ? x1 : 0.f));
+            bb |= (b0 ? 1u : 0u) << (2 * h);
+            bb |= (b1 ? 1u : 0u) << (2 * h + 1);
+        }
+        m[q] = bb;
+    }
+    float a0, a1, s0, s1;
+    f2unpack(aa, a0, a1);
+    f2unpack(as, s0, s1);
+    acc_a += a0 + a1;
+    acc_s += s0 + s1;
+}
+
+// Gradient of one 16-byte draft vector: out[e] = 2^{z_e k - cd} (bit e ? on : off).
+template <typename Tin>
+__device__ __forceinline__ void grad_vec(const uint4 &r, uint32_t m, float k, float cd, float on, float off,
+                                         float *out) {
+    const uint64_t K2 = f2pack(k, k), NCD = f2pack(-cd, -cd);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    if (Store<Tin>::ES == 2) {
+        float g[8];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float d0, d1;
+            f2unpack(f2fma(bf16pair_f2(w[h]), K2, NCD), d0, d1);
+            g[2 * h] = ex2(d0) * ((m >> (2 * h)) & 1u ? on : off);
+            g[2 * h + 1] = ex2(d1) * ((m >> (2 * h + 1)) & 1u ? on : off);
+        }
+        __stcs(reinterpret_cast<float4 *>(out), make_float4(g[0], g[1], g[2], g[3]));
+        __stcs(reinterpret_cast<float4 *>(out) + 1, make_float4(g[4], g[5], g[6], g[7]));
+    } else {
+        float d0, d1, d2, d3;
+        f2unpack(f2fma(f2pack(__uint_as_float(w[0]), __uint_as_float(w[1])), K2, NCD), d0, d1);
+        f2unpack(f2fma(f2pack(__uint_as_float(w[2]), __uint_as_float(w[3])), K2, NCD), d2, d3);
+        __stcs(reinterpret_cast<float4 *>(out),
+               make_float4(ex2(d0) * (m & 1u ? on : off), ex2(d1) * (m & 2u ? on : off),
+                           ex2(d2) * (m & 4u ? on : off), ex2(d3) * (m & 8u ? on : off)));
+    }
+}
+
 }  // namespace mtp

@@ -93,6 +93,33 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity) {
     }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in the instruction (woken when the phase completes, or after about
+// `ns` nanoseconds) instead of re-issuing polls that take issue slots from
+// the warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for an mbarrier phase, sleeping in try_wait between checks of the
+// clock; gives up after 2 s (false).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
 // Wait for an mbarrier phase with a 2 s limit; false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     return mbar_wait_spin(bar, parity);

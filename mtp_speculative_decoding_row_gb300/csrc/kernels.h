@@ -109,6 +109,19 @@ int pair_max_gamma();
 int pair_max_segments();
 int pair_max_ring();
 
+// TMEM-resident TV kernel: the draft rows of a position parked in tensor
+// memory.  ns: 16-byte vectors per lane and row (2, 4, 5, 8 or 10); null for
+// another.
+const void *tvm_kernel(int dtype, int ns);
+uint32_t tvm_smem_bytes(int gamma, int C, int ns, int ring);
+int tvm_threads();
+int tvm_max_gamma();
+int tvm_max_ring();
+int tvm_warp_cols();
+int tvm_max_cluster();
+int tvm_team_warps();  // warps of one team per CTA (segments per CTA of a position)
+int tvm_teams();       // independent teams per CTA
+
 // Streaming TV kernel geometry.
 uint32_t tvs_hdr_bytes();
 uint32_t tvs_rec_bytes(int gamma, int S);

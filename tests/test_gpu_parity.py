@@ -778,10 +778,14 @@ TV_SWEEP = [
 ]
 
 
+@pytest.mark.parametrize("kernel", [None, "tmem"])
 @pytest.mark.parametrize("N,gamma,V,dtype,T,scale,C,nres", TV_SWEEP)
-def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres):
+def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres, kernel):
+    """The sweep on the planner's kernel (streaming where rows are whole
+    vectors and gamma <= 8, else cluster-resident) and on the TMEM-resident
+    kernel where a position's draft rows fit in tensor memory."""
     x = W.tvloss_inputs("tv", N, gamma, V, dtype, 500 + V + gamma, delta=0.5, sigmas=np.linspace(1.0, 8.0, N))
-    with tune(cluster_size=C, tv_resident_drafts=nres):
+    with tune(cluster_size=C, tv_resident_drafts=nres, tv_kernel=kcode(kernel)):
         out = run_tv(to_dev(x.target), to_dev(x.draft), T, scale)
     o = oracle.tv_loss(x.target, x.draft, T, scale)
     tf = W.bf16_bits_to_f32(x.target).astype(np.float64) if dtype == "bf16" else x.target.astype(np.float64)
@@ -862,10 +866,23 @@ def test_tv_loss_in_cuda_graph():
     (4, 5, 12000, "f32", 8, None, None, "resident"),
     (3, 8, 30000, "bf16", None, 2, None, None),   # gamma = 8, the streaming limit
     (3, 9, 30000, "bf16", None, None, None, None),  # gamma = 9 takes the resident kernel
+    (9, 3, 40000, "bf16", 16, 2, None, "stream"),
+    (7, 2, 20000, "f32", 4, 3, 3, "stream"),
+    (3, 8, 30000, "bf16", None, 2, None, "stream"),
+    # TMEM-resident kernel: cluster sizes, rings, several positions per cluster, the largest row per lane
+    (11, 3, 151936, "bf16", 8, 3, 2, "tmem"),
+    (9, 3, 151936, "bf16", None, None, 3, "tmem"),
+    (8, 1, 50000, "f32", 8, 2, None, "tmem"),
+    (10, 2, 60000, "f32", 8, 3, 4, "tmem"),
+    (7, 4, 30000, "bf16", 4, 2, None, "tmem"),
+    (6, 8, 16384, "f32", 8, 2, None, "tmem"),
+    (13, 3, 4096, "bf16", 1, 4, 2, "tmem"),
+    (5, 2, 8, "bf16", 2, None, None, "tmem"),     # V = 8: most warps hold no vector
 ])
 def test_tv_loss_kernels(N, gamma, V, dtype, C, clusters, ring, kernel):
-    """Streaming and cluster-resident TV kernels, several positions per
-    cluster, ring depths and the gamma limit."""
+    """TMEM-resident, streaming and cluster-resident TV kernels, several
+    positions per cluster (both exchange banks), ring depths, cluster sizes
+    and the gamma limit."""
     x = W.tvloss_inputs("tvk", N, gamma, V, dtype, 600 + V + gamma, delta=0.5, sigmas=np.linspace(0.7, 9.0, N))
     with tune(cluster_size=C, max_clusters=clusters, ring_slots=ring, tv_kernel=kcode(kernel)):
         out = run_tv(to_dev(x.target), to_dev(x.draft), 0.8, 1.5)
@@ -887,6 +904,9 @@ TV_VARIANTS = [
     (5, 3, 4097, "bf16", True, 0.4, None, None),      # unaligned rows: the resident kernel
     (6, 3, 20000, "f32", True, 0.3, 4, "resident"),
     (4, 9, 8192, "bf16", True, None, None, None),     # gamma = 9: the resident kernel
+    (9, 3, 40000, "bf16", True, None, 8, "tmem"),
+    (6, 3, 30000, "f32", False, 0.3, None, "tmem"),
+    (9, 3, 151936, "bf16", True, 0.4, 8, "tmem"),
 ]
 
 
@@ -974,11 +994,26 @@ def test_tv_loss_topk_bad_index_and_nan():
 
 
 def test_tv_plan_kernels():
+    """At the tvloss size the TMEM-resident kernel runs 8-CTA clusters whose
+    gamma draft rows per position fit the CTAs' tensor memory, with shared
+    memory above half of the SM's, so that a second CTA and its TMEM
+    allocation never land on an SM; the planner's default is the streaming
+    kernel."""
     import mtp_speculative_decoding_row_gb300 as mtp
-    p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
+    with tune(tv_kernel=kcode("tmem")):
+        p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
+    assert p["cluster_size"] == 8 and p["resident_drafts"] == 3, p
+    props = torch.cuda.get_device_properties(0)
+    per_sm = props.shared_memory_per_multiprocessor
+    assert per_sm // 2 < p["smem_bytes"] + 1024, p
+    s = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
     q = mtp.mtp_query_plan("tv_loss_resident", "bf16", 16384, 3, 151936)
-    assert p["resident_drafts"] == 0 and q["resident_drafts"] >= 1
-    assert p["clusters"] * p["cluster_size"] > q["clusters"] * q["cluster_size"]
+    assert s["resident_drafts"] == 0 and q["resident_drafts"] >= 1
+    assert s["clusters"] * s["cluster_size"] > q["clusters"] * q["cluster_size"]
+    # gamma = 7 draft rows of a position do not fit in tensor memory: the request falls back to streaming
+    with tune(tv_kernel=kcode("tmem")):
+        f = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 7, 151936)
+    assert f["resident_drafts"] == 0, f
 
 
 def test_tv_loss_full_config_sampled():
@@ -1007,11 +1042,11 @@ def test_tv_loss_full_config_sampled():
     print("tvloss sampled", {k: v for k, v in rep.items() if not isinstance(v, list)})
 
 
-@pytest.mark.parametrize("kernel", [None, "resident"])
+@pytest.mark.parametrize("kernel", [None, "stream", "resident"])
 def test_tv_loss_bad_temperature_and_nan(kernel):
     x = W.tvloss_inputs("tvbad", 3, 2, 2000, "f32", 9, sigmas=2.0)
     x.target[1, 1, 3] = np.nan
-    with tune(tv_kernel=kcode(kernel), max_clusters=1 if kernel is None else None):
+    with tune(tv_kernel=kcode(kernel), max_clusters=1 if kernel != "resident" else None):
         out = run_tv(to_dev(x.target), to_dev(x.draft), 1.0, 1.0)
     f = out.row_flags.cpu().numpy()
     assert list(f) == [0, oracle.ROW_NONFINITE, 0]
