@@ -299,7 +299,8 @@ bool plan_tvs(int dev, int dtype, int V, int es, int gamma, int units, Plan &p, 
 // until columns are free, so the shared memory asked for keeps a second CTA
 // off the SM: more than half of the SM's shared memory.
 bool tvm_usable(int V, int es, int gamma) {
-    if (tuning().tv_kernel != MTP_KERNEL_TMEM) return false;  // measured slower than streaming: on request only
+    const int k = tuning().tv_kernel;
+    if (k == MTP_KERNEL_STREAM || k == MTP_KERNEL_RESIDENT) return false;
     return gamma <= tvm_max_gamma() && V % (16 / es) == 0;
 }
 
@@ -770,6 +771,7 @@ extern "C" int mtp_tv_loss_ex(const void *target_logits, const void *draft_logit
     A.tau_max = loss_kind == 1 ? tau_max : 0.f;
     A.topk_idx = nullptr;
     A.K = 0;
+    A.grad32 = (reinterpret_cast<uintptr_t>(grad_draft_logits) & 31u) == 0 ? 1 : 0;
     return launch(func, p, &A, stream);
 }
 
@@ -811,6 +813,7 @@ extern "C" int mtp_tv_loss_topk(const void *target_values, const int32_t *target
     A.tau_max = loss_kind == 1 ? tau_max : 0.f;
     A.topk_idx = target_idx;
     A.K = K;
+    A.grad32 = (reinterpret_cast<uintptr_t>(grad_draft_logits) & 31u) == 0 ? 1 : 0;
     return launch(p.func, p, &A, stream);
 }
 

@@ -252,8 +252,18 @@ __device__ __forceinline__ void ovl_regs(const uint4 (&rt)[QV], const uint4 (&rd
     acc_s += s0 + s1;
 }
 
+// 32-byte streaming store of eight floats (one 256-bit store instruction:
+// a warp writes 1 KB contiguous, half the store instructions of two 16-byte
+// stores).  `out` must be 32-byte aligned.
+__device__ __forceinline__ void stcs_v8(float *out, const float (&g)[8]) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(out), "f"(g[0]), "f"(g[1]),
+                 "f"(g[2]), "f"(g[3]), "f"(g[4]), "f"(g[5]), "f"(g[6]), "f"(g[7])
+                 : "memory");
+}
+
 // Gradient of one 16-byte draft vector: out[e] = 2^{z_e k - cd} (bit e ? on : off).
-template <typename Tin>
+// W32: `out` is 32-byte aligned (bf16 rows then take one 256-bit store).
+template <typename Tin, bool W32 = false>
 __device__ __forceinline__ void grad_vec(const uint4 &r, uint32_t m, float k, float cd, float on, float off,
                                          float *out) {
     const uint64_t K2 = f2pack(k, k), NCD = f2pack(-cd, -cd);
@@ -267,8 +277,12 @@ __device__ __forceinline__ void grad_vec(const uint4 &r, uint32_t m, float k, fl
             g[2 * h] = ex2(d0) * ((m >> (2 * h)) & 1u ? on : off);
             g[2 * h + 1] = ex2(d1) * ((m >> (2 * h + 1)) & 1u ? on : off);
         }
-        __stcs(reinterpret_cast<float4 *>(out), make_float4(g[0], g[1], g[2], g[3]));
-        __stcs(reinterpret_cast<float4 *>(out) + 1, make_float4(g[4], g[5], g[6], g[7]));
+        if (W32) {
+            stcs_v8(out, g);
+        } else {
+            __stcs(reinterpret_cast<float4 *>(out), make_float4(g[0], g[1], g[2], g[3]));
+            __stcs(reinterpret_cast<float4 *>(out) + 1, make_float4(g[4], g[5], g[6], g[7]));
+        }
     } else {
         float d0, d1, d2, d3;
         f2unpack(f2fma(f2pack(__uint_as_float(w[0]), __uint_as_float(w[1])), K2, NCD), d0, d1);

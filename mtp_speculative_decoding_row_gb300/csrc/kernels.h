@@ -51,6 +51,7 @@ struct TVArgs {
     float tau_max;
     const int32_t *topk_idx;  // top-K mode: [N, gamma, K] vocabulary indices (target = [N, gamma, K] values)
     int K;
+    int grad32;             // the gradient base is 32-byte aligned: bf16 rows store 32 bytes at once
 };
 
 // Modes of the streaming row-pair statistics kernel.

@@ -544,7 +544,8 @@ __global__ void __launch_bounds__(NT, 4) tvs_kernel_impl(const TVArgs A) {
                                 __stcs(reinterpret_cast<float4 *>(out), make_float4(0.f, 0.f, 0.f, 0.f));
                                 if (VEC == 8) __stcs(reinterpret_cast<float4 *>(out) + 1, make_float4(0.f, 0.f, 0.f, 0.f));
                             } else {
-                                grad_vec<Tin>(rd[q], TOPK ? 0u : bk[ch * CV + j], k, cd, on, off, out);
+                                // two 16-byte stores: measured slightly faster here than one 32-byte store
+                                grad_vec<Tin, false>(rd[q], TOPK ? 0u : bk[ch * CV + j], k, cd, on, off, out);
                             }
                         }
                     }

@@ -47,7 +47,7 @@ namespace {
 
 constexpr int NT = 512;          // threads per CTA (one CTA per SM: it holds all TMEM columns)
 constexpr int NW = NT / 32;      // warps per CTA; four per TMEM lane quarter
-constexpr int TEAMS = 2;         // independent warp teams per CTA, each on its own position
+constexpr int TEAMS = 1;         // independent warp teams per CTA, each on its own position
 constexpr int TW = NW / TEAMS;   // warps (segments) per team and CTA
 constexpr int MAXC = 8;          // largest cluster
 constexpr int MAXS = MAXC * TW;  // segments per team and cluster
@@ -272,8 +272,8 @@ __device__ __forceinline__ void mnorm_row(const TVArgs &A, MC &c, int k, float k
             for (int q = 0; q < GS; ++q) tmem_st_v4(c.tbase + mcol<NS>(k, gi * GS + q), v[q]);
         }
         fold_regs<Tin, GS>(v, cmx, kk2, m, s, bad);
-        if (PARK) tmem_wait_st();
     }
+    if (PARK) tmem_wait_st();
 }
 
 // Zero this warp's segment of one gradient row (flagged positions).
@@ -283,6 +283,40 @@ __device__ __forceinline__ void mzero_segment(const MC &c, float *row) {
     float4 *o = reinterpret_cast<float4 *>(row + static_cast<size_t>(c.seg_lo) * VEC);
     const int n4 = c.seg_n * VEC / 4;
     for (int i = c.lane; i < n4; i += 32) __stcs(o + i, make_float4(0.f, 0.f, 0.f, 0.f));
+}
+
+// G(k) of position t: the gradient row k of this warp's segment from the
+// parked draft row k and the indicator bytes (a flagged position: zeros).
+// The warp's cd, on and off of step k and the bytes belong to position t.
+template <typename Tin, int NS>
+__device__ __forceinline__ void mgrad_row(const TVArgs &A, const MC &c, int t, int kk, int pflags, float k) {
+    constexpr int VEC = Store<Tin>::VEC;
+    constexpr int GS = Group<NS>::GS, NG = Group<NS>::NG;
+    float *orow = A.grad + (static_cast<size_t>(t) * c.g + kk) * static_cast<size_t>(A.V);
+    if (pflags) {
+        mzero_segment<Tin>(c, orow);
+        return;
+    }
+    const float cd = c.ws->cd[kk], on = c.ws->on[kk], off = c.ws->off[kk];
+    const unsigned char *bk = c.bits + static_cast<size_t>(kk) * NS * 32;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+        uint4 rd[GS];
+#pragma unroll
+        for (int q = 0; q < GS; ++q) tmem_ld_v4(c.tbase + mcol<NS>(kk, gi * GS + q), rd[q]);
+        tmem_wait_ld_regs<GS>(rd);
+#pragma unroll
+        for (int q = 0; q < GS; ++q) {
+            const int j = (gi * GS + q) * 32 + c.lane;
+            if (j < c.seg_n) {
+                float *out = orow + (static_cast<size_t>(c.seg_lo) + j) * VEC;
+                if (A.grad32)
+                    grad_vec<Tin, true>(rd[q], bk[j], k, cd, on, off, out);
+                else
+                    grad_vec<Tin, false>(rd[q], bk[j], k, cd, on, off, out);
+            }
+        }
+    }
 }
 
 template <typename Tin, int NS>
@@ -351,18 +385,30 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
     cluster_sync();  // every barrier of the cluster is initialised and armed before any push
     mproduce<Tin, NS>(A, c);
 
+    // The gradient pass of a position runs interleaved with the next
+    // position's first passes: G(k) of the previous position right before
+    // N(k) of this one, which parks its draft row k in the columns G(k) has
+    // just read.  So the stores of one position overlap the loads and
+    // arithmetic of the next instead of every warp storing at once.
+    int prev_t = -1, prev_flags = 0, prev_done = 0;  // pending G: position, its flags, rows done
     for (int t = c.vc; t < A.N; t += c.NT_) {
         float *grow = A.grad + static_cast<size_t>(t) * g * static_cast<size_t>(A.V);
         int flags = 0;
         float loss = NAN;
         float alpha_l = NAN;  // lane kk < g: alpha_kk
         if (bad_temp || c.dead) {
+            for (; prev_t >= 0 && prev_done < g; ++prev_done) mgrad_row<Tin, NS>(A, c, prev_t, prev_done, prev_flags, k);
+            prev_t = -1;
             flags = bad_temp ? F_BAD_TEMP : F_TIMEOUT;
             for (int kk = 0; kk < g; ++kk) mzero_segment<Tin>(c, grow + static_cast<size_t>(kk) * A.V);
         } else {
             // ---- N(k), and O(k - 1) right after it: the all-gather of N(k - 1)
             // had the streaming of N(k) to complete
             for (int u = 0; u <= g && !c.dead; ++u) {
+                if (u < g && prev_t >= 0) {
+                    mgrad_row<Tin, NS>(A, c, prev_t, u, prev_flags, k);
+                    prev_done = u + 1;
+                }
                 if (u < g) {
                     float mt, st, md, sd;
                     int bad = 0;
@@ -433,6 +479,9 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
                 }
                 mpush(sh, c, g + kk, make_float4(warp_allsum(acc_a), warp_allsum(acc_s), 0.f, 0.f));
             }
+            // rows of the previous position still pending (the loop above
+            // stopped early): before the chain overwrites their coefficients
+            for (; prev_t >= 0 && prev_done < g; ++prev_done) mgrad_row<Tin, NS>(A, c, prev_t, prev_done, prev_flags, k);
             // ---- the chain: every warp from the gathered records
             if (!c.dead) {
                 float av[MAXG], sv[MAXG];
@@ -492,31 +541,10 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
             }
             if (c.dead) flags |= F_TIMEOUT;
             __syncwarp();
-            // ---- G(k): the gradient from the parked draft rows
-            for (int kk = 0; kk < g; ++kk) {
-                float *orow = grow + static_cast<size_t>(kk) * A.V;
-                if (flags) {
-                    mzero_segment<Tin>(c, orow);
-                    continue;
-                }
-                const float cd = c.ws->cd[kk], on = c.ws->on[kk], off = c.ws->off[kk];
-                const unsigned char *bk = c.bits + static_cast<size_t>(kk) * NS * 32;
-                constexpr int GS = Group<NS>::GS, NG = Group<NS>::NG;
-#pragma unroll
-                for (int gi = 0; gi < NG; ++gi) {
-                    uint4 rd[GS];
-#pragma unroll
-                    for (int q = 0; q < GS; ++q) tmem_ld_v4(c.tbase + mcol<NS>(kk, gi * GS + q), rd[q]);
-                    tmem_wait_ld_regs<GS>(rd);
-#pragma unroll
-                    for (int q = 0; q < GS; ++q) {
-                        const int j = (gi * GS + q) * 32 + c.lane;
-                        if (j < c.seg_n)
-                            grad_vec<Tin>(rd[q], bk[j], k, cd, on, off,
-                                          orow + (static_cast<size_t>(c.seg_lo) + j) * VEC);
-                    }
-                }
-            }
+            // ---- G(k) of this position: with the next position's N passes
+            prev_t = t;
+            prev_flags = flags;
+            prev_done = 0;
             // the team's warp 0 closes the bank: every round of this position
             // complete, re-armed
             if (c.tw == 0 && !c.dead) {
@@ -541,6 +569,7 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
         }
     }
 
+    for (; prev_t >= 0 && prev_done < g; ++prev_done) mgrad_row<Tin, NS>(A, c, prev_t, prev_done, prev_flags, k);
     // copies still in flight (after a bounded wait gave up, or issued ahead
     // past a dead position) land before the CTA leaves
     while (c.ccount != c.pcount) {

@@ -778,12 +778,13 @@ TV_SWEEP = [
 ]
 
 
-@pytest.mark.parametrize("kernel", [None, "tmem"])
+@pytest.mark.parametrize("kernel", [None, "stream"])
 @pytest.mark.parametrize("N,gamma,V,dtype,T,scale,C,nres", TV_SWEEP)
 def test_tv_loss(N, gamma, V, dtype, T, scale, C, nres, kernel):
-    """The sweep on the planner's kernel (streaming where rows are whole
-    vectors and gamma <= 8, else cluster-resident) and on the TMEM-resident
-    kernel where a position's draft rows fit in tensor memory."""
+    """The sweep on the planner's kernel (TMEM-resident where a position's
+    draft rows fit in tensor memory, else streaming where rows are whole
+    vectors and gamma <= 8, else cluster-resident) and on the streaming
+    kernel."""
     x = W.tvloss_inputs("tv", N, gamma, V, dtype, 500 + V + gamma, delta=0.5, sigmas=np.linspace(1.0, 8.0, N))
     with tune(cluster_size=C, tv_resident_drafts=nres, tv_kernel=kcode(kernel)):
         out = run_tv(to_dev(x.target), to_dev(x.draft), T, scale)
@@ -994,19 +995,18 @@ def test_tv_loss_topk_bad_index_and_nan():
 
 
 def test_tv_plan_kernels():
-    """At the tvloss size the TMEM-resident kernel runs 8-CTA clusters whose
-    gamma draft rows per position fit the CTAs' tensor memory, with shared
-    memory above half of the SM's, so that a second CTA and its TMEM
-    allocation never land on an SM; the planner's default is the streaming
-    kernel."""
+    """At the tvloss size the planner takes the TMEM-resident kernel: 4-CTA
+    clusters whose gamma draft rows per position fit the CTAs' tensor
+    memory, with shared memory above half of the SM's, so that a second CTA
+    and its TMEM allocation never land on an SM."""
     import mtp_speculative_decoding_row_gb300 as mtp
-    with tune(tv_kernel=kcode("tmem")):
-        p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
-    assert p["cluster_size"] == 8 and p["resident_drafts"] == 3, p
+    p = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
+    assert p["cluster_size"] == 4 and p["resident_drafts"] == 3, p
     props = torch.cuda.get_device_properties(0)
     per_sm = props.shared_memory_per_multiprocessor
     assert per_sm // 2 < p["smem_bytes"] + 1024, p
-    s = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
+    with tune(tv_kernel=kcode("stream")):
+        s = mtp.mtp_query_plan("tv_loss", "bf16", 16384, 3, 151936)
     q = mtp.mtp_query_plan("tv_loss_resident", "bf16", 16384, 3, 151936)
     assert s["resident_drafts"] == 0 and q["resident_drafts"] >= 1
     assert s["clusters"] * s["cluster_size"] > q["clusters"] * q["cluster_size"]
