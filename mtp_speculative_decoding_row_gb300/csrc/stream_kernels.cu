@@ -649,6 +649,71 @@ __device__ __forceinline__ float psum_regs(const uint4 (&rt)[QV], float k, float
 // -4.64, widened for the approximate logarithms.
 constexpr float GUMBEL2_MAX = 25.5f;
 constexpr float GUMBEL2_MIN = -6.f;
+// Keys (log2 units) within this gap of the best are near-ties: the single
+// precision keys (approximate logarithms, noise within 4e-5) may order them
+// wrongly, so the two best candidates of a draw are re-keyed in double
+// precision whenever their gap is below it.  The filters below keep every
+// index that can come within the gap of the best key.
+constexpr float GUMBEL_TIE = 1e-3f;
+
+// Running top two (key, index) of a lane: a key enters when it beats the
+// second; ties keep the earlier (smaller) index.
+__device__ __forceinline__ void top2_push(float &k1, int &i1, float &k2, int &i2, float key, int idx) {
+    if (key > k1) {
+        k2 = k1;
+        i2 = i1;
+        k1 = key;
+        i1 = idx;
+    } else if (key > k2) {
+        k2 = key;
+        i2 = idx;
+    }
+}
+
+// Merge another top two into this one (disjoint index sets); the larger key
+// first, ties to the smaller index.  Index -1: no candidate.
+__device__ __forceinline__ void top2_merge(float &k1, int &i1, float &k2, int &i2, float o1, int j1, float o2, int j2) {
+    auto before = [](float a, int ia, float b, int ib) {  // (a, ia) ranks above (b, ib)
+        return ia >= 0 && (ib < 0 || a > b || (a == b && ia < ib));
+    };
+    float c[4] = {k1, k2, o1, o2};
+    int ci[4] = {i1, i2, j1, j2};
+    int b1 = 0;
+#pragma unroll
+    for (int q = 1; q < 4; ++q)
+        if (before(c[q], ci[q], c[b1], ci[b1])) b1 = q;
+    int b2 = -1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (q != b1 && (b2 < 0 || before(c[q], ci[q], c[b2], ci[b2]))) b2 = q;
+    k1 = c[b1];
+    i1 = ci[b1];
+    k2 = c[b2];
+    i2 = ci[b2];
+}
+
+// Top two across the warp (butterfly over disjoint lane groups); the same
+// result in every lane.
+__device__ __forceinline__ void top2_allreduce(float &k1, int &i1, float &k2, int &i2) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float o1 = __shfl_xor_sync(FULL, k1, o), o2 = __shfl_xor_sync(FULL, k2, o);
+        const int j1 = __shfl_xor_sync(FULL, i1, o), j2 = __shfl_xor_sync(FULL, i2, o);
+        top2_merge(k1, i1, k2, i2, o1, j1, o2, j2);
+    }
+}
+
+// Gumbel noise of index v in row j of sequence b in double precision,
+// G = -ln(-ln U), U = (floor(x / 2^8) + 1/2) 2^-24 from word v mod 4 of
+// Philox4x32-10 at counter (v / 4, j, b, offset).
+__device__ __forceinline__ double gumbel_noise_d(int v, int j, uint32_t b, uint32_t offset, uint32_t seed_lo,
+                                                 uint32_t seed_hi) {
+    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(v / 4), static_cast<uint32_t>(j), b, offset), seed_lo,
+                                  seed_hi);
+    const uint32_t w = (v & 3) == 0 ? x.x : (v & 3) == 1 ? x.y : (v & 3) == 2 ? x.z : x.w;
+    const double u = (static_cast<double>(w >> 8) + 0.5) * 5.9604644775390625e-8;
+    return -log(-log(u));
+}
 
 // Gumbel-max keys of one chunk (registers; vbase: vector index of the lane's
 // first vector) into the lane's running arg maxes, first index among equals:
@@ -672,7 +737,7 @@ template <typename Tin, int QV, bool RESID>
 __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], int cnt, int lane, float k,
                                             float ct, float cd, int vbase, uint32_t seed_lo, uint32_t seed_hi, int j,
                                             uint32_t b, uint32_t offset, float bp, float br, float &kr, int &ir,
-                                            float &kp, int &ip) {
+                                            float &kr2, int &ir2, float &kp, int &ip, float &kp2, int &ip2) {
     constexpr int VEC = Store<Tin>::VEC;
 #pragma unroll
     for (int q = 0; q < QV; ++q) {
@@ -690,7 +755,8 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
                 zk[e4] = zt[h * 4 + e4] * k;
                 mx = fmaxf(mx, zk[e4]);
             }
-            const float bpv = fmaxf(kp, bp), brv = fmaxf(kr, br);
+            // a key must come within GUMBEL_TIE of the best to matter
+            const float bpv = fmaxf(kp, bp) - GUMBEL_TIE, brv = fmaxf(kr, br) - GUMBEL_TIE;
             const bool want_p = mx + GUMBEL2_MAX >= bpv;
             const bool want_r = RESID && mx - ct + GUMBEL2_MAX >= brv;
             if (!want_p && !want_r) continue;  // no index of the group can win either draw
@@ -712,18 +778,12 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
                 const int e = h * 4 + e4;
                 const float gv = gumbel2(xs[e4]);
                 const float key_p = zk[e4] + gv;
-                if (key_p > kp) {
-                    kp = key_p;
-                    ip = vv * VEC + e;
-                }
+                if (key_p > kp2) top2_push(kp, ip, kp2, ip2, key_p, vv * VEC + e);
                 if (RESID && want_r) {
                     const float w = ex2(zk[e4] - ct) - ex2(fmaf(zd[e], k, -cd));
                     if (w > 0.f) {
                         const float key_r = __log2f(w) + gv;
-                        if (key_r > kr) {
-                            kr = key_r;
-                            ir = vv * VEC + e;
-                        }
+                        if (key_r > kr2) top2_push(kr, ir, kr2, ir2, key_r, vv * VEC + e);
                     }
                 }
             }
@@ -734,20 +794,25 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
 // The Gumbel-max pass of one warp over its segment [seg_lo, seg_lo + seg_n)
 // of row j (target row trow, draft row drow), read directly from global
 // memory (the rows were streamed moments ago and mostly sit in L2): the
-// warp's best residual and p keys with their indices {key_r, idx_r, key_p,
-// idx_p} (index -1: no candidate; the p keys start at the bound lb).  Out of
+// warp's two best residual and p keys with their indices (index -1: no
+// candidate; the p keys start at the bound lb).  Out of
 // line and by value: it runs once per sequence, and neither its generator
 // state nor the warp's streaming state should crowd the other's registers.
+struct Top2x2 {
+    float4 best;    // {key_r, idx_r, key_p, idx_p}
+    float4 second;  // the runners-up, same layout
+};
+
 template <typename Tin, bool RESID>
-__device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsigned char *drow, int seg_lo,
+__device__ __noinline__ Top2x2 gumbel_pass(const unsigned char *trow, const unsigned char *drow, int seg_lo,
                                            int seg_n, int j, uint32_t b, float k, float ct, float cd, float lb,
                                            uint32_t seed_lo, uint32_t seed_hi, uint32_t offset) {
     constexpr int QV = 2;  // vectors per lane per tile
     const int lane = threadIdx.x & 31;
     const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + seg_lo;
     const uint4 *gd = reinterpret_cast<const uint4 *>(drow) + seg_lo;
-    float kr = -INFINITY, kp = lb, bp = lb, br = -INFINITY;
-    int ir = -1, ip = -1;
+    float kr = -INFINITY, kp = lb, bp = lb, br = -INFINITY, kr2 = -INFINITY, kp2 = -INFINITY;
+    int ir = -1, ip = -1, ir2 = -1, ip2 = -1;
     // The pass is bound by load latency, not arithmetic: the next tile's
     // loads are in flight while a tile is keyed.
     uint4 rt[QV], rd[QV], nt[QV], nd[QV];
@@ -765,7 +830,7 @@ __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsi
     for (int base = 0; base < seg_n; base += QV * 32) {
         if (base + QV * 32 < seg_n) load_tile(base + QV * 32, nt, nd);
         gumbel_regs<Tin, QV, RESID>(rt, rd, min(QV * 32, seg_n - base), lane, k, ct, cd, seg_lo + base + lane,
-                                    seed_lo, seed_hi, j, b, offset, bp, br, kr, ir, kp, ip);
+                                    seed_lo, seed_hi, j, b, offset, bp, br, kr, ir, kr2, ir2, kp, ip, kp2, ip2);
         // the warp's best p key so far bounds every lane's filters
         if (!RESID) bp = warp_allmax(kp);
 #pragma unroll
@@ -774,31 +839,32 @@ __device__ __noinline__ float4 gumbel_pass(const unsigned char *trow, const unsi
             if (RESID) rd[q] = nd[q];
         }
     }
-    float d0 = 0.f;
-    argmax_allreduce(kr, ir, d0);
-    argmax_allreduce(kp, ip, d0);
-    return make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
+    top2_allreduce(kr, ir, kr2, ir2);
+    top2_allreduce(kp, ip, kp2, ip2);
+    Top2x2 r;
+    r.best = make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
+    r.second = make_float4(kr2, __int_as_float(ir2), kp2, __int_as_float(ip2));
+    return r;
 }
 
 // Gumbel-max p keys of one chunk of row j held in a ring slot (target
 // vectors at tb; cnt vectors; chunk_v0: the chunk's first vector in the row)
-// into the lane's running arg max, passed and returned by value as {kp,
-// ip}; bp is the warp's best p key so far.  Out of line: it runs once per
+// into the lane's running top two, passed and returned by value as {kp, ip,
+// kp2, ip2}; bp is the warp's best p key so far.  Out of line: it runs once per
 // chunk of the bonus draw, and neither its generator state nor the warp's
 // streaming state should crowd the other's registers.
 template <typename Tin, int CV>
-__device__ __noinline__ float2 gumbel_slot(const unsigned char *tb, int cnt, int chunk_v0, float k, int j, uint32_t b,
-                                           uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, float bp, float kp,
-                                           int ip) {
+__device__ __noinline__ float4 gumbel_slot(const unsigned char *tb, int cnt, int chunk_v0, float k, int j, uint32_t b,
+                                           uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, float bp, float4 top) {
     const int lane = threadIdx.x & 31;
-    float kr = -INFINITY;
-    int ir = -1;
+    float kr = -INFINITY, kr2 = -INFINITY, kp = top.x, kp2 = top.z;
+    int ir = -1, ir2 = -1, ip = __float_as_int(top.y), ip2 = __float_as_int(top.w);
     for (int q = 0; q < CV / 32 && q * 32 + lane < cnt; ++q) {
         const uint4 v[1] = {vec_at(tb, q * 32 + lane)};
         gumbel_regs<Tin, 1, false>(v, v, 32, lane, k, 0.f, 0.f, chunk_v0 + q * 32 + lane, seed_lo, seed_hi, j, b,
-                                   offset, bp, -INFINITY, kr, ir, kp, ip);
+                                   offset, bp, -INFINITY, kr, ir, kr2, ir2, kp, ip, kp2, ip2);
     }
-    return make_float2(kp, __int_as_float(ip));
+    return make_float4(kp, __int_as_float(ip), kp2, __int_as_float(ip2));
 }
 
 template <typename Tin, int CV, int MODE, bool DBL>
@@ -1142,10 +1208,13 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 // draw is the bonus, or the residual's fallback when every
                 // residual weight rounded to zero (ZERO_MASS)
                 float4 best = make_float4(-INFINITY, __int_as_float(-1), -INFINITY, __int_as_float(-1));
+                float4 second = best;
                 if (!(flags & ERR_BITS)) {
                     const uint32_t bb = static_cast<uint32_t>(b);
                     float kr = -INFINITY, kp = fmaf(r.Mt, k, GUMBEL2_MIN);  // the best p key is at least max z k + min g
                     int ir = -1, ip = -1;
+                    float kr2 = -INFINITY, kp2 = -INFINITY;
+                    int ir2 = -1, ip2 = -1;
                     if (resid) {
                         // drop the look-ahead rows past the rejection (the producer
                         // moves on to the next sequence's first row) and read row j
@@ -1154,13 +1223,11 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         redirect_next(c, ord, A.B);
                         c.c_conf = g;  // the path is fixed
                         produce<Tin, MODE, DBL>(A, c);
-                        const float4 kk = gumbel_pass<Tin, true>(row_base<Tin>(A, true, b, j), row_base<Tin>(A, false, b, j),
-                                                                 c.seg_lo, c.seg_n, j, bb, k, r.ct, r.cd, kp, A.seed_lo,
-                                                                 A.seed_hi, A.offset);
-                        kr = kk.x;
-                        ir = __float_as_int(kk.y);
-                        kp = kk.z;
-                        ip = __float_as_int(kk.w);
+                        const Top2x2 kk = gumbel_pass<Tin, true>(row_base<Tin>(A, true, b, j),
+                                                                 row_base<Tin>(A, false, b, j), c.seg_lo, c.seg_n, j,
+                                                                 bb, k, r.ct, r.cd, kp, A.seed_lo, A.seed_hi, A.offset);
+                        best = kk.best;
+                        second = kk.second;
                     } else {
                         // the bonus: row gamma streams through the ring once more
                         // (mostly from L2) as a residual unit of the target row
@@ -1174,49 +1241,78 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         c.p_done = (c.nch == 0);
                         c.c_conf = g;  // the path is fixed
                         float bp = kp;
+                        float4 top = make_float4(kp, __int_as_float(ip), kp2, __int_as_float(ip2));
                         for (int ch = 0; ch < c.nch; ++ch) {
                             produce<Tin, MODE, DBL>(A, c);
                             if (c.pcount == c.ccount) c.dead = true;
                             if (c.dead || !slot_wait(c)) break;
                             const unsigned char *tb = c.ring + c.cslot * SLOT_BYTES;
-                            const float2 kk = gumbel_slot<Tin, CV>(tb, chunk_count(c, ch), c.seg_lo + ch * CV, k, j, bb,
-                                                                   A.seed_lo, A.seed_hi, A.offset, bp, kp, ip);
-                            kp = kk.x;
-                            ip = __float_as_int(kk.y);
+                            top = gumbel_slot<Tin, CV>(tb, chunk_count(c, ch), c.seg_lo + ch * CV, k, j, bb, A.seed_lo,
+                                                       A.seed_hi, A.offset, bp, top);
                             __syncwarp();
                             consumed(c);
                             produce<Tin, MODE, DBL>(A, c);
-                            bp = warp_allmax(kp);  // the warp's best p key so far bounds every lane's filters
+                            bp = warp_allmax(top.x);  // the warp's best p key so far bounds every lane's filters
                         }
+                        kp = top.x;
+                        ip = __float_as_int(top.y);
+                        kp2 = top.z;
+                        ip2 = __float_as_int(top.w);
+                        top2_allreduce(kr, ir, kr2, ir2);
+                        top2_allreduce(kp, ip, kp2, ip2);
+                        best = make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
+                        second = make_float4(kr2, __int_as_float(ir2), kp2, __int_as_float(ip2));
                     }
-                    float d0 = 0.f;
-                    argmax_allreduce(kr, ir, d0);
-                    argmax_allreduce(kp, ip, d0);
-                    best = make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
                 }
-                // every warp fills round gamma + 1 (no candidate when the row is flagged)
+                // every warp fills round gamma + 1 with its two best candidates
+                // of each draw (none when the row is flagged)
                 if (!c.dead) {
-                    xpush(sh, c, g + 1, best, ZERO4);
+                    xpush(sh, c, g + 1, best, second);
                     xwait(sh, c, g + 1);
                 }
                 if (c.dead) {
                     flags |= F_TIMEOUT;
                 } else if (!(flags & ERR_BITS)) {
-                    float vr = -INFINITY, vp = -INFINITY, d0 = 0.f;
-                    int jr = -1, jp = -1;
+                    float vr = -INFINITY, vp = -INFINITY, vr2 = -INFINITY, vp2 = -INFINITY;
+                    int jr = -1, jp = -1, jr2 = -1, jp2 = -1;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int q = 2 * c.lane + h;
                         if (q < c.S) {
                             const float4 v = *rec_at(c, c.bank, g + 1, q);
-                            argmax_merge(vr, jr, d0, v.x, __float_as_int(v.y), 0.f);
-                            argmax_merge(vp, jp, d0, v.z, __float_as_int(v.w), 0.f);
+                            const float4 w = *rec_at(c, c.bank, g + 1, c.S + q);
+                            top2_merge(vr, jr, vr2, jr2, v.x, __float_as_int(v.y), w.x, __float_as_int(w.y));
+                            top2_merge(vp, jp, vp2, jp2, v.z, __float_as_int(v.w), w.z, __float_as_int(w.w));
                         }
                     }
-                    argmax_allreduce(vr, jr, d0);
-                    argmax_allreduce(vp, jp, d0);
+                    top2_allreduce(vr, jr, vr2, jr2);
+                    top2_allreduce(vp, jp, vp2, jp2);
                     if (resid && jr < 0) flags |= F_ZERO_MASS;  // every residual weight rounded to zero
-                    tok = (resid && jr >= 0) ? jr : jp;
+                    const bool use_r = resid && jr >= 0;
+                    tok = use_r ? jr : jp;
+                    const int tok2 = use_r ? jr2 : jp2;
+                    const float gap = use_r ? vr - vr2 : vp - vp2;
+                    if (tok >= 0 && tok2 >= 0 && gap < GUMBEL_TIE) {
+                        // a near-tie: both keys once more in double precision
+                        // (the same inputs and order in every warp, so every
+                        // warp takes the same token)
+                        const unsigned char *trow = row_base<Tin>(A, true, b, j);
+                        const unsigned char *drow = row_base<Tin>(A, false, b, j);
+                        const uint32_t bb = static_cast<uint32_t>(b);
+                        auto key_d = [&](int v) {
+                            const double zt = static_cast<double>(St::scalar_g(trow, static_cast<size_t>(v)));
+                            const double lp = zt * static_cast<double>(k) - static_cast<double>(r.ct);
+                            double w = exp2(lp);
+                            if (use_r) {
+                                const double zd = static_cast<double>(St::scalar_g(drow, static_cast<size_t>(v)));
+                                w -= exp2(zd * static_cast<double>(k) - static_cast<double>(r.cd));
+                            }
+                            return (w > 0.0 ? log(w) : -static_cast<double>(INFINITY)) +
+                                   gumbel_noise_d(v, j, bb, A.offset, A.seed_lo, A.seed_hi);
+                        };
+                        const double a1 = key_d(tok), a2 = key_d(tok2);
+                        if (a2 > a1 || (a2 == a1 && tok2 < tok)) tok = tok2;
+                    }
                     if (tok < 0) flags |= F_NONFINITE;
                 }
                 owner = 0;

@@ -501,6 +501,62 @@ def test_draft_sample(V, dtype, C, method):
     assert len(np.unique(ids)) > len(ids) // 4  # rows differ: the draws are not all one token
 
 
+def _near_tie_rows(R, V, seed, offset, lo=1.5e-5, hi=5e-4, row=0):
+    """Rows whose two largest logits are equal (5.0, exact in bf16 too), at
+    the two indices whose Gumbel noise (the draws' counter-based noise of
+    sequence r, row `row`) is closest within [lo, hi): their keys ln w + G
+    differ by that gap, far above every other key (the rest is -30)."""
+    z = np.full((R, V), -30.0, np.float32)
+    gaps = np.empty(R)
+    for r in range(R):
+        G = oracle.gumbel_noise(seed, offset, r, row, 0, V)
+        order = np.argsort(G)
+        d = np.diff(G[order])
+        ok = np.nonzero((d >= lo) & (d < hi))[0]
+        i = ok[np.argmin(d[ok])] if r % 2 == 0 else ok[-1]
+        z[r, order[i]] = z[r, order[i + 1]] = 5.0
+        gaps[r] = d[i]
+    return z, gaps
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gumbel_near_ties_resolved(dtype):
+    """Two candidates whose Gumbel keys differ by 1.5e-5 to 5e-4 (natural-log
+    units): the fp32 keys cannot order them reliably, the kernel's
+    double-precision re-keying of its two best candidates must, so the
+    draws equal the oracle's exactly (every gap is above GUMBEL_MARGIN)."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    R, V, seed, offset = 48, 512, 31337, 5
+    z, gaps = _near_tie_rows(R, V, seed, offset)
+    zs = W.to_bf16_bits(z) if dtype == "bf16" else z
+    o = oracle.draft_sample(zs, np.ones(R, np.float32), None, method="gumbel", seed=seed, offset=offset)
+    assert (o["margin"] >= compare.GUMBEL_MARGIN).all() and (o["margin"] < 1e-3).all()
+    np.testing.assert_allclose(o["margin"], gaps, rtol=1e-6)
+    out = mtp.mtp_draft_sample(to_dev(zs), torch.ones(R, device="cuda"), None, method="gumbel", seed=seed,
+                               offset=offset)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.ids.cpu().numpy(), o["ids"])
+
+
+def test_gumbel_verify_bonus_near_ties_resolved():
+    """The same near-ties as the bonus draw of Gumbel-max verification: every
+    draft accepted (draft row = target row 0), row gamma = 1 holds the tie."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    B, V, seed, offset = 32, 512, 4242, 9
+    z1, gaps = _near_tie_rows(B, V, seed, offset, row=1)
+    rng = np.random.default_rng(5)
+    t = np.stack([rng.standard_normal((B, V)).astype(np.float32), z1], axis=1)
+    d = t[:, :1].copy()
+    ids = rng.integers(0, V, (B, 1)).astype(np.int32)
+    T = np.ones(B, np.float32)
+    u = rng.random((B, 2), dtype=np.float32)
+    o = oracle.gumbel_verify(t, d, ids, T, u, seed, offset)
+    assert (o["accept_len"] == 1).all() and (o["gumbel_margin"] >= compare.GUMBEL_MARGIN).all()
+    out = mtp.mtp_gumbel_verify(to_dev(t), to_dev(d), to_dev(ids), to_dev(T), to_dev(u), seed, offset)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.tokens.cpu().numpy(), o["tokens"])
+
+
 def test_draft_sample_bad_rows_and_full_size():
     """Bad temperature / uniform / NaN rows in between good ones, and the
     verify64 draft rows (192 rows of V = 151,936 bf16) against the oracle."""
