@@ -207,8 +207,9 @@ int mtp_draft_sample(const void *draft_logits, mtp_dtype dtype, const float *tem
  *   target_logits [B, gamma+1, V], draft_logits [B, gamma, V], temperature [B]
  *   alpha [B, gamma] float32 (required), entropy [B, gamma+1] float32
  *   (required), row_flags [B] int32 or NULL.
- * Runs on the cluster-resident kernel; with MTP_RS_STATS_KERNEL=stream (and
- * aligned rows, gamma <= 8) on the streaming kernel of mtp_rs_diagnostics.
+ * Runs on the cluster-resident kernel; mtp_tuning.stats_kernel selects the
+ * streaming kernel of mtp_rs_diagnostics or the TMEM-resident kernel
+ * (aligned rows, gamma <= 8) instead.
  */
 int mtp_row_stats(const void *target_logits, const void *draft_logits, mtp_dtype dtype,
                   const float *temperature, int B, int gamma, int V,
@@ -369,7 +370,8 @@ typedef struct mtp_tuning {
     int verify_kernel;       /* mtp_rs_verify without statistics: MTP_KERNEL_AUTO / _STREAM / _RESIDENT */
     int tv_kernel;           /* TV loss: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM (_TMEM where a
                                 position's draft rows fit in tensor memory, else as _AUTO) */
-    int stats_kernel;        /* mtp_row_stats: MTP_KERNEL_AUTO / _STREAM / _RESIDENT / _TMEM */
+    int stats_kernel;        /* mtp_row_stats: MTP_KERNEL_AUTO (= _RESIDENT) / _STREAM / _RESIDENT /
+                                _TMEM (where two draft row segments fit a warp's tensor memory) */
     int tv_resident_drafts;  /* cluster-resident TV kernel: cap on draft slices kept on chip; 0 = none */
     int tv_l2_mb;            /* streaming TV kernel: cap positions in flight so the rows they re-read
                                 fit this many MB; 0 = no cap */

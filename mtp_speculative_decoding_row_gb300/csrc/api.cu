@@ -234,7 +234,7 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
 // (powers of two) whose shared memory fits, the one with the most warps in
 // flight wins; within 5 % the larger cluster (shorter per-position chain).  Measured on
 // GB300, concurrency matters more than keeping every re-read row in L2, so
-// the positions in flight are capped only when MTP_RS_TV_L2MB sets an L2
+// the positions in flight are capped only when mtp_tuning.tv_l2_mb sets an L2
 // budget for the 2 gamma rows a position re-reads.
 bool tvs_usable(int V, int es, int gamma) {
     if (tuning().tv_kernel == MTP_KERNEL_RESIDENT) return false;  // a TMEM request that does not fit streams
@@ -359,6 +359,72 @@ bool plan_tvm(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) 
     return false;
 }
 
+// TMEM-resident row-statistics kernel: clusters of C CTAs x 16 warps, one
+// CTA per SM holding all 512 TMEM columns; a warp parks two draft row
+// segments at a time (NS vectors per lane each).  The smallest C whose
+// segments fit wins; shared memory above half the SM's keeps a second CTA
+// (and its TMEM allocation) off the SM.
+bool stm_usable(int V, int es, int gamma) {
+    // measured slower than the cluster-resident kernel on the B = 256, gamma
+    // = 7 fp32 rows (each warp's chain of exchanges per sequence is latency
+    // bound with one CTA per SM): on request only
+    if (tuning().stats_kernel != MTP_KERNEL_TMEM) return false;
+    return gamma <= stm_max_gamma() && V % (16 / es) == 0;
+}
+
+bool plan_stm(int dev, int dtype, int V, int es, int gamma, int units, Plan &p) {
+    const mtp_tuning tu = tuning();
+    const int forced = tuned_cluster(tu);
+    int per_sm = 0, reserved = 0;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    const uint32_t hi = smem_optin(dev);
+    const uint32_t lo = static_cast<uint32_t>(per_sm / 2 - reserved + 128) & ~127u;  // 2 CTAs do not fit
+    const int nv = V / (16 / es);
+    const int ns_set[] = {2, 4, 5, 8, 10, 15};
+    for (int C = 1; C <= stm_max_cluster(); C *= 2) {
+        if (forced && C != forced) continue;
+        const int S = C * (stm_threads() / 32);
+        const int nvs = (nv + S - 1) / S;
+        const int need = (nvs + 31) / 32;
+        int ns = 0;
+        for (int c : ns_set)
+            if (c >= need) {
+                ns = c;
+                break;
+            }
+        if (!ns || stm_parked() * ns * 4 > stm_warp_cols()) continue;
+        int R = tu.ring_slots;
+        if (R < 2 || R > stm_max_ring()) R = stm_max_ring();
+        while (R >= 2 && stm_smem_bytes(gamma, C, ns, R) > hi) --R;
+        if (R < 2) continue;
+        uint32_t smem = stm_smem_bytes(gamma, C, ns, R);
+        if (smem < lo) smem = lo;  // padding: keeps a second CTA (and its TMEM allocation) off the SM
+        if (smem > hi) continue;
+        const void *func = stm_kernel(dtype, ns);
+        if (!func) continue;
+        if (prepare_func(dev, func) != cudaSuccess) return false;
+        const int nc = max_clusters(dev, func, C, smem, stm_threads());
+        if (nc <= 0) continue;
+        int used = nc < units ? nc : units;
+        if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
+        p = Plan{};
+        p.C = C;
+        p.smem = smem;
+        p.clusters = used;
+        p.threads = stm_threads();
+        p.ring = R;
+        p.seg_vectors = nvs;
+        p.nres = stm_parked();
+        p.func = func;
+        return true;
+    }
+    return false;
+}
+
 // Persistent TV kernel: two target slots, nres (>= 2, ideally gamma) draft
 // slots and gamma rows of indicator bits per CTA.
 bool plan_tv(int dev, const void *func, int V, int es, int gamma, int units, Plan &p) {
@@ -471,12 +537,12 @@ int row_call(int mode, const void *target, const void *draft, mtp_dtype dtype, c
 // request): clusters of C CTAs x NT/32 warps, one vocabulary segment per
 // warp, one sequence per cluster at a time.  Same rule as the streaming TV
 // kernel: the most warps in flight, within 5 % the larger cluster;
-// MTP_RS_PAIR_L2MB caps the sequences in flight by the bytes of the row
+// mtp_tuning.pair_l2_mb caps the sequences in flight by the bytes of the row
 // pairs they re-read.  Measured on GB300 at B = 256, gamma = 7, V = 151,936
 // fp32, the cluster-resident kernel (one load per row, the second pass from
 // shared memory) computes the row statistics faster than this kernel, whose
 // second pass re-reads rows that L2 no longer holds; mtp_row_stats therefore
-// uses it only when MTP_RS_STATS_KERNEL=stream.
+// uses it only when mtp_tuning.stats_kernel asks for it.
 bool pairs_usable(int V, int es, int gamma) {
     return gamma <= pair_max_gamma() && V % (16 / es) == 0;
 }
@@ -702,6 +768,28 @@ extern "C" int mtp_row_stats(const void *target_logits, const void *draft_logits
                              int32_t *row_flags, mtp_stream_t stream) {
     if (B > 0 && (!alpha || !entropy)) return MTP_ERR_INVALID_ARG;
     if (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED_DTYPE;
+    if (B > 0 && gamma >= 1 && gamma <= MTP_MAX_GAMMA && V >= 1 && target_logits && draft_logits && temperature &&
+        aligned16(target_logits) && aligned16(draft_logits) && stm_usable(V, esize(dtype), gamma)) {
+        int dev;
+        if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+        Plan p;
+        if (plan_stm(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, esize(dtype), gamma, B, p)) {
+            VerifyArgs A = {};
+            A.target = target_logits;
+            A.draft = draft_logits;
+            A.temp = temperature;
+            A.B = B;
+            A.gamma = gamma;
+            A.V = V;
+            A.aligned = 1;
+            A.ring = p.ring;
+            A.seg_vectors = p.seg_vectors;
+            A.alpha = alpha;
+            A.entropy = entropy;
+            A.flags = row_flags;
+            return launch(p.func, p, &A, stream);
+        }
+    }
     if (B > 0 && gamma >= 1 && V >= 1 && target_logits && draft_logits && temperature && aligned16(target_logits) &&
         aligned16(draft_logits) && stats_streamed() && pairs_usable(V, esize(dtype), gamma))
         return pair_call(PAIR_STATS, target_logits, draft_logits, dtype, temperature, B, gamma, V, alpha, entropy,
@@ -838,7 +926,8 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     if (op == 0 && stream_usable(V, es, gamma)) ok = streamed = plan_stream(dev, d, V, es, gamma, units, p);
     if (op == 3 && tvm_usable(V, es, gamma)) ok = plan_tvm(dev, d, V, es, gamma, units, p);
     if (op == 3 && !ok && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
-    if (op == 2 && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
+    if (op == 2 && stm_usable(V, es, gamma)) ok = plan_stm(dev, d, V, es, gamma, units, p);
+    if (op == 2 && !ok && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
     if (op == 10 || op == 11) {  // draft sampling (inverse CDF, Gumbel-max): one-row sequences of the streaming kernel
         if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
         ok = streamed = plan_stream(dev, d, V, es, 0, units, p, op == 10 ? 0 : 2, true);

@@ -118,6 +118,48 @@ __device__ __forceinline__ float fold_regs(const uint4 (&r)[QV], float cmx, floa
     return cs;
 }
 
+// Fold one chunk row into the lane's running partial with the entropy sum:
+// exact running maximum m (NaN or +inf sets `bad`), s = sum 2^{d},
+// s1 = sum 2^{d} d with d = z k - m k (clamped at -256 so that -inf logits
+// add exactly zero).
+template <typename Tin, int QV>
+__device__ __forceinline__ void fold_ent(const uint4 (&r)[QV], float cmx, float k, float &m, float &s, float &s1,
+                                         int &bad) {
+    using St = Store<Tin>;
+    bad |= !(cmx < INFINITY);
+    const float nm = fmaxf(m, cmx);
+    const float mr = nm > -INFINITY ? nm : 0.f;
+    const float dl = (mr - m) * k;  // +inf while nothing finite was seen (s == 0)
+    const float sc = ex2(-dl);
+    s1 = (s != 0.f) ? sc * fmaf(-dl, s, s1) : 0.f;
+    s *= sc;
+    m = nm;
+    const float mk = mr * k;
+    const uint64_t K2 = f2pack(k, k), NMK2 = f2pack(-mk, -mk);
+    uint64_t as = f2pack(0.f, 0.f), a1 = f2pack(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < QV; ++q) {
+        const uint32_t w[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+#pragma unroll
+        for (int h = 0; h < (St::ES == 2 ? 4 : 2); ++h) {
+            const uint64_t z2 = St::ES == 2 ? bf16pair_f2(w[h])
+                                            : f2pack(__uint_as_float(w[2 * h]), __uint_as_float(w[2 * h + 1]));
+            float d0, d1;
+            f2unpack(f2fma(z2, K2, NMK2), d0, d1);
+            d0 = fmaxf(d0, -256.f);
+            d1 = fmaxf(d1, -256.f);
+            const uint64_t e2 = f2pack(ex2(d0), ex2(d1));
+            as = f2add(as, e2);
+            a1 = f2fma(e2, f2pack(d0, d1), a1);
+        }
+    }
+    float x0, x1, y0, y1;
+    f2unpack(as, x0, x1);
+    f2unpack(a1, y0, y1);
+    s += x0 + x1;
+    s1 += y0 + y1;
+}
+
 // Running arg max of one chunk row kept warp-uniform: the warp maximum of
 // the lanes' chunk maxima (cmx from chunk_max; a NaN or +inf lane takes no
 // part, it is flagged elsewhere) replaces (m, idx, x) only when it exceeds

@@ -123,6 +123,18 @@ int tvm_max_cluster();
 int tvm_team_warps();  // warps of one team per CTA (segments per CTA of a position)
 int tvm_teams();       // independent teams per CTA
 
+// TMEM-resident row-statistics kernel: draft rows parked in tensor memory
+// for the overlap pass.  ns: 16-byte vectors per lane and row (2, 4, 5, 8,
+// 10 or 15); null for another.
+const void *stm_kernel(int dtype, int ns);
+uint32_t stm_smem_bytes(int gamma, int C, int ns, int ring);
+int stm_threads();
+int stm_max_gamma();
+int stm_max_ring();
+int stm_warp_cols();
+int stm_max_cluster();
+int stm_parked();  // draft rows parked at a time
+
 // Streaming TV kernel geometry.
 uint32_t tvs_hdr_bytes();
 uint32_t tvs_rec_bytes(int gamma, int S);

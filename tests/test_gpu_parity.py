@@ -313,12 +313,16 @@ def test_greedy_rs_verify(V, dtype, gamma, kernel, clusters):
                                                     (1024, "f32", 3, None, "stream"), (40000, "f32", 7, 4, "stream"),
                                                     (40000, "bf16", 8, 16, "stream"), (64, "f32", 3, 16, "stream"),
                                                     (151936, "bf16", 3, None, "stream"),
-                                                    (4097, "bf16", 5, 8, "stream")])
+                                                    (4097, "bf16", 5, 8, "stream"),
+                                                    (1024, "f32", 3, None, "resident"),
+                                                    (151936, "bf16", 3, None, "resident"),
+                                                    (1024, "f32", 3, 2, "tmem"), (151936, "f32", 7, 8, "tmem"),
+                                                    (40000, "bf16", 8, 4, "tmem"), (64, "f32", 3, 8, "tmem"),
+                                                    (151936, "bf16", 1, None, "tmem")])
 def test_row_stats(V, dtype, gamma, C, kernel):
-    """Row statistics on the cluster-resident kernel (the default) and on the
-    streaming row-pair kernel when asked for (aligned rows, gamma <= 8, else
-    the resident kernel; V = 64 over 64 segments leaves most warps without
-    vocabulary)."""
+    """Row statistics on the planner's kernel (cluster-resident), and on the
+    streaming row-pair and TMEM-resident kernels when asked for (V = 64 over
+    64 or 128 segments leaves most warps without vocabulary)."""
     x = W.verify_inputs("stats", 12, gamma, V, dtype, 2000 + V, family="sigma", sigmas=np.linspace(0.3, 9, 12),
                         delta=np.linspace(0, 1.5, 12), temperature=np.linspace(0.6, 1.4, 12))
     with tune(cluster_size=C, stats_kernel=kcode(kernel)):
@@ -326,6 +330,27 @@ def test_row_stats(V, dtype, gamma, C, kernel):
     o = oracle.row_stats(x.target, x.draft, x.temperature)
     rep = compare.stats_report(g["alpha"], g["entropy"], o, dtype, g["row_flags"])
     compare.assert_ok(rep, f"stats V={V}")
+
+
+@pytest.mark.parametrize("clusters,C", [(1, None), (3, 8), (2, 4)])
+def test_row_stats_tmem_sequences_and_flags(clusters, C):
+    """The TMEM-resident statistics kernel with several sequences per
+    cluster (the exchange barriers reused sequence after sequence), bad
+    temperatures (T = 0 included) skipped between good sequences, and NaN
+    and +inf logits flagged."""
+    B, gamma, V = 11, 4, 40000
+    x = W.verify_inputs("stm", B, gamma, V, "f32", 2150 + clusters, family="sigma", sigmas=np.linspace(0.5, 7, B),
+                        delta=np.linspace(0, 1.2, B), temperature=np.linspace(0.6, 1.4, B))
+    x.temperature[[2, 7]] = [0.0, -1.0]
+    x.target[4, 1, 123] = np.nan
+    x.draft[9, 3, 39999] = np.inf
+    with tune(stats_kernel=kcode("tmem"), max_clusters=clusters, cluster_size=C):
+        g = run_stats(x)
+    o = oracle.row_stats(x.target, x.draft, x.temperature)
+    np.testing.assert_array_equal(g["row_flags"], o["flags"])
+    assert list(np.nonzero(o["flags"])[0]) == [2, 4, 7, 9]
+    rep = compare.stats_report(g["alpha"], g["entropy"], o, "f32", g["row_flags"])
+    compare.assert_ok(rep, f"tmem stats clusters={clusters}")
 
 
 def test_row_stats_deep_config():
