@@ -377,6 +377,12 @@ typedef struct mtp_tuning {
                                 fit this many MB; 0 = no cap */
     int pair_l2_mb;          /* streaming row-pair kernel: the same cap for sequences; 0 = no cap */
     int row_streams;         /* cluster-resident row kernel: sequences in flight per CTA, 1 or 2; 0 = planner */
+    /* Fault injection for tests of the bounded waits (both 0 in normal use).
+     * They act on the TMEM-resident TV kernel only. */
+    int fault_wait_us;       /* limit of every on-chip wait in microseconds; 0 = 2 s */
+    int fault_skip_position; /* 1 + the position whose first exchange push the cluster's first warp
+                                skips: every wait on it gives up, and that position and the later ones
+                                of its cluster come back flagged MTP_ROW_TIMEOUT; 0 = none */
 } mtp_tuning;
 
 /* Set (t != NULL) or clear (t == NULL) the overrides; affects calls made

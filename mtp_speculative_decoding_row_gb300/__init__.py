@@ -39,7 +39,8 @@ MTP_OK, MTP_ERR_INVALID_ARG, MTP_ERR_UNSUPPORTED_DTYPE, MTP_ERR_MISALIGNED, MTP_
     MTP_ERR_NO_DEVICE = range(7)
 KERNEL_AUTO, KERNEL_STREAM, KERNEL_RESIDENT, KERNEL_TMEM = range(4)
 TUNING_FIELDS = ("cluster_size", "ring_slots", "lookahead", "chunk_vectors", "max_clusters", "verify_kernel",
-                 "tv_kernel", "stats_kernel", "tv_resident_drafts", "tv_l2_mb", "pair_l2_mb", "row_streams")
+                 "tv_kernel", "stats_kernel", "tv_resident_drafts", "tv_l2_mb", "pair_l2_mb", "row_streams",
+                 "fault_wait_us", "fault_skip_position")
 
 
 class _Tuning(ctypes.Structure):

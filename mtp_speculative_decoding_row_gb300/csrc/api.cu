@@ -860,6 +860,9 @@ extern "C" int mtp_tv_loss_ex(const void *target_logits, const void *draft_logit
     A.topk_idx = nullptr;
     A.K = 0;
     A.grad32 = (reinterpret_cast<uintptr_t>(grad_draft_logits) & 31u) == 0 ? 1 : 0;
+    const mtp_tuning tu = tuning();
+    A.wait_ns = tu.fault_wait_us > 0 ? static_cast<uint32_t>(tu.fault_wait_us) * 1000u : 0u;
+    A.skip_t = tu.fault_skip_position > 0 ? tu.fault_skip_position - 1 : -1;
     return launch(func, p, &A, stream);
 }
 
@@ -902,6 +905,8 @@ extern "C" int mtp_tv_loss_topk(const void *target_values, const int32_t *target
     A.topk_idx = target_idx;
     A.K = K;
     A.grad32 = (reinterpret_cast<uintptr_t>(grad_draft_logits) & 31u) == 0 ? 1 : 0;
+    A.wait_ns = 0;
+    A.skip_t = -1;
     return launch(p.func, p, &A, stream);
 }
 

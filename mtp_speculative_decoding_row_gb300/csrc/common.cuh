@@ -110,13 +110,13 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 }
 
 // Wait for an mbarrier phase, sleeping in try_wait between checks of the
-// clock; gives up after 2 s (false).
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+// clock; gives up after limit_ns (default 2 s) and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
-        if (globaltimer_ns() - t0 > 2000000000ull) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -52,6 +52,9 @@ struct TVArgs {
     const int32_t *topk_idx;  // top-K mode: [N, gamma, K] vocabulary indices (target = [N, gamma, K] values)
     int K;
     int grad32;             // the gradient base is 32-byte aligned: bf16 rows store 32 bytes at once
+    // fault injection (TMEM-resident TV kernel; tests of the bounded waits)
+    uint32_t wait_ns;       // limit of every on-chip wait; 0 = 2 s
+    int skip_t;             // the position whose first exchange push warp 0 of CTA 0 skips; -1 = none
 };
 
 // Modes of the streaming row-pair statistics kernel.

@@ -1097,6 +1097,45 @@ def test_tv_plan_kernels():
     assert f["resident_drafts"] == 0, f
 
 
+def test_tv_loss_tmem_wait_timeout():
+    """Failure detection of the bounded waits, with no GPU fault: the
+    cluster's first warp leaves out its first exchange record at position 4
+    (test-only tuning fields), so every wait on that round gives up after
+    20 ms.  The call returns; position 4 and the later positions of its
+    cluster (positions 1, 4, 7, 10 belong to cluster 1 of 3) come back
+    flagged MTP_ROW_TIMEOUT with a NaN loss and alpha and a zero gradient;
+    every other position matches the oracle; and the next call, without the
+    fault, is correct again."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    N, gamma, V = 12, 3, 40000
+    x = W.tvloss_inputs("tvto", N, gamma, V, "bf16", 990, delta=0.5, sigmas=np.linspace(0.7, 6.0, N))
+    T, scale = 0.9, 1.3
+    with tune(tv_kernel=kcode("tmem"), max_clusters=3):
+        assert mtp.mtp_query_plan("tv_loss", "bf16", N, gamma, V)["clusters"] == 3
+        with tune(fault_wait_us=20000, fault_skip_position=4 + 1):
+            out = run_tv(to_dev(x.target), to_dev(x.draft), T, scale)
+        flags = out.row_flags.cpu().numpy()
+        with pytest.raises(mtp.MTPError) as e:
+            mtp.check_row_flags(out.row_flags)
+        assert e.value.status == mtp.MTP_ERR_TIMEOUT
+        again = run_tv(to_dev(x.target), to_dev(x.draft), T, scale)
+    timed_out = np.array([4, 7, 10])
+    assert list(np.nonzero(flags)[0]) == list(timed_out) and np.all(flags[timed_out] == mtp.ROW_TIMEOUT)
+    loss, alpha, grad = out.loss.cpu().numpy(), out.alpha.cpu().numpy(), out.grad.cpu().numpy()
+    assert np.all(np.isnan(loss[timed_out])) and np.all(np.isnan(alpha[timed_out]))
+    assert np.all(grad[timed_out] == 0)
+    o = oracle.tv_loss(x.target, x.draft, T, scale)
+    ok = np.setdiff1d(np.arange(N), timed_out)
+    tf = W.bf16_bits_to_f32(x.target).astype(np.float64)
+    df = W.bf16_bits_to_f32(x.draft).astype(np.float64)
+    sub = {k: (v[ok] if isinstance(v, np.ndarray) and v.shape[:1] == (N,) else v) for k, v in o.items()}
+    rep = compare.tv_report(loss[ok], alpha[ok], grad[ok], flags[ok], sub, "bf16", tf[ok], df[ok], T)
+    compare.assert_ok(rep, "positions outside the timed-out cluster")
+    rep = compare.tv_report(again.loss.cpu().numpy(), again.alpha.cpu().numpy(), again.grad.cpu().numpy(),
+                            again.row_flags.cpu().numpy(), o, "bf16", tf, df, T)
+    compare.assert_ok(rep, "the call after the timeout")
+
+
 def test_tv_loss_full_config_sampled():
     """N = 16,384, gamma = 3, V = 151,936 bf16 on device: sampled positions
     against the oracle, sum_j grad = 0 on every row, loss in [-gamma, 0]."""
