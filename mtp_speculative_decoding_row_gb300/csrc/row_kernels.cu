@@ -26,7 +26,7 @@
 
 namespace mtp {
 
-constexpr int NT = 128;      // threads per CTA
+constexpr int NT = 256;      // threads per CTA
 constexpr int NW = NT / 32;  // warps per CTA
 
 struct StreamSt {
@@ -434,7 +434,7 @@ __device__ __forceinline__ StreamSt start_seq(const VerifyArgs &A, RowShared &sh
 // ---------------------------------------------------------------- kernel ---
 
 template <typename Tin, int MODE>
-__global__ void __launch_bounds__(NT, 4) row_kernel_impl(const VerifyArgs A) {
+__global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
     using S = Store<Tin>;
     constexpr int VEC = S::VEC;
     constexpr bool STATS = (MODE != MODE_VERIFY);
