@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
             const uint32_t lbar = smem_addr(&sh.lbar[si]);
             const int b = st.b, i = st.i;
             bool finish = false;
+            bool issued_early = false;  // the stream's next unit is already in flight
             if (i == 0) st.flags |= validate_seq(sh, si, g, A.V, DECIDE, MODE == MODE_VERIFY);
 
             if ((st.flags & ERR_BITS) || dead) {
@@ -629,7 +630,17 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                                 for (int e = 0; e < VEC; ++e)
                                     acc += ex2(fminf(fmaf(zt[e], k, -ct), fmaf(zd[e], k, -cd)));
                             }
-                            float r4[4] = {block_sum(sh.tpart, acc), 0.f, 0.f, 0.f};
+                            const float part = block_sum(sh.tpart, acc);  // every read of the slices is done
+                            if (MODE == MODE_STATS && !dead) {
+                                // no decision waits on the overlap: the next position's
+                                // slices load while its exchange completes
+                                StreamSt nx = st;
+                                nx.i = i + 1;
+                                issue_unit<Tin>(A, nx, s, tb, db, lbar);
+                                st.armed = nx.armed;
+                                issued_early = true;
+                            }
+                            float r4[4] = {part, 0.f, 0.f, 0.f};
                             const int sl2 = xchg_round<4>(sh.x, round, r4, C, rank, ok);
                             const float a = gather_sum(sh.x, sl2, C);
                             if (tid == 0) sh.alpha[si][i] = a;
@@ -637,6 +648,12 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                                 dead = true;
                                 st.flags |= F_TIMEOUT;
                                 finish = true;
+                                if (issued_early && st.armed) {  // the early copy lands before the buffers change hands
+                                    mbar_wait_bounded(lbar, st.ph);
+                                    st.ph ^= 1u;
+                                    st.armed = 0;
+                                }
+                                issued_early = false;
                             }
                         }
                     }
@@ -702,7 +719,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
             } else {
                 st.i = i + 1;
             }
-            if (st.active && !dead) issue_unit<Tin>(A, st, s, tb, db, lbar);
+            if (st.active && !dead && !issued_early) issue_unit<Tin>(A, st, s, tb, db, lbar);
             if (tid == 0) sh.st[si] = st;
         }
         __syncthreads();
