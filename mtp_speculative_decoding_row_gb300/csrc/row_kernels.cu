@@ -631,9 +631,15 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                                     acc += ex2(fminf(fmaf(zt[e], k, -ct), fmaf(zd[e], k, -cd)));
                             }
                             const float part = block_sum(sh.tpart, acc);  // every read of the slices is done
-                            if (MODE == MODE_STATS && !dead) {
-                                // no decision waits on the overlap: the next position's
-                                // slices load while its exchange completes
+                            // the slices are not needed again unless this position draws
+                            // the final token (a rejection here): otherwise the next
+                            // position's slices load while the overlap exchange completes
+                            bool no_draw = MODE == MODE_STATS || st.stopped;
+                            if (DECIDE && !st.stopped) {
+                                const float lp = fmaf(Zty, k, -ct), lq = fmaf(Zdy, k, -cd);
+                                no_draw = log2f(sh.u[si][i]) + lq < lp;  // the accept test taken below
+                            }
+                            if (no_draw && !dead) {
                                 StreamSt nx = st;
                                 nx.i = i + 1;
                                 issue_unit<Tin>(A, nx, s, tb, db, lbar);
