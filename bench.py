@@ -47,17 +47,50 @@ METRIC = "verified draft positions/sec and logit GB/s (% of HBM roofline) at V=1
 UNIT = "positions/s"
 L2_BYTES = 129 * 1024 * 1024
 
+# Source files of each kernel family (the kernel and the headers it uses).
+KERNEL_FILES = {
+    "stream": ["stream_kernels.cu", "chunk_math.cuh", "common.cuh", "philox.cuh", "kernels.h"],
+    "tv_tmem": ["tv_tmem_kernels.cu", "chunk_math.cuh", "common.cuh", "tmem.cuh", "kernels.h"],
+    "row": ["row_kernels.cu", "common.cuh", "kernels.h"],
+}
+
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
-# ncu captures (profiles/), keyed by workload, valid only for the kernel
-# sources they were taken on (hash of csrc/).
-TRAFFIC = {}
+# ncu captures (profiles/), keyed by workload: valid only while the kernel's
+# source files hash to the value they were captured on (null otherwise).
+# Captures on a reduced case are scaled to the workload by the units
+# processed (traffic grows in proportion; profiles/ says which).
+TRAFFIC = {
+    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,089,216 read + 3,650,560 written
+    # (profiles/stream_kernel_rl512.md)
+    "rl512": {"bytes": 1069739776, "family": "stream", "csrc": "a85b25773c784224"},
+    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,093,342,464 read + 873,745,152 written) x 32
+    # for N = 16,384 (profiles/tv_tmem_kernel_tvloss_n512.md)
+    "tvloss": {"bytes": 62946803712, "family": "tv_tmem", "csrc": "eb1bfaa10f8406a2"},
+    # row_kernel_impl<float,2> (statistics) and <float,1> (verify with statistics) on the first 64
+    # sequences of deep256 (583,623,936 + 3,812,352 and 583,899,136 + 3,688,448 bytes) x 4 for
+    # B = 256 (profiles/row_kernel_deep256_b64.md)
+    "stats256": {"bytes": 2349745152, "family": "row", "csrc": "7d67229aa8896636"},
+    "deep256": {"bytes": 2350350336, "family": "row", "csrc": "7d67229aa8896636"},
+}
 
 
-def csrc_hash() -> str:
+def csrc_hash(family: str = None) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "mtp_speculative_decoding_row_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "mtp_speculative_decoding_row_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*"))) if family is None else \
+        [os.path.join(csrc, f) for f in KERNEL_FILES[family]]
+    for p in files:
         h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
+
+
+def traffic_for(name: str):
+    """ncu DRAM bytes per launch of the workload, or None when the capture is
+    missing or its kernel sources have changed since."""
+    tr = TRAFFIC.get(name)
+    if not tr or tr.get("csrc") != csrc_hash(tr["family"]):
+        return None
+    return tr["bytes"]
 
 
 def load_peaks() -> dict:
@@ -605,8 +638,12 @@ def run_cuda(args, world, rank, local, pg):
         achieved = alg / per_launch_s / 1e9
         tv = name in TV_WORKLOADS
         units = wl.N if tv else (wl.B * wl.gamma if wl.kind in ("sample", "gsample") else wl.B)  # draft sampling: rows
-        plan = mtp.mtp_query_plan("tv_loss" if tv else wl.plan_op(), "bf16" if wl.es == 2 else "f32", units,
-                                  wl.gamma, wl.V)
+        if tv and name == "tvtopk":  # the top-K path runs on the streaming TV kernel
+            with mtp.tuning(tv_kernel=mtp.KERNEL_STREAM):
+                plan = mtp.mtp_query_plan("tv_loss", "bf16", units, wl.gamma, wl.V)
+        else:
+            plan = mtp.mtp_query_plan("tv_loss" if tv else wl.plan_op(), "bf16" if wl.es == 2 else "f32", units,
+                                      wl.gamma, wl.V)
         r = {
             "workload": wl.describe(),
             "launch_plan": plan,
@@ -619,8 +656,7 @@ def run_cuda(args, world, rank, local, pg):
             "steps": steps,
             "input_copies": wl.copies,
         }
-        tr = TRAFFIC.get(name)
-        r["traffic"] = tr["bytes"] if tr and tr.get("csrc") == csrc_hash() else None
+        r["traffic"] = traffic_for(name)
         results[name] = r
         if head is None:
             head = (name, wl, t, t_ms, steps, clocks, alg, achieved)
@@ -635,8 +671,7 @@ def run_cuda(args, world, rank, local, pg):
         e2e = time_e2e(wl, max(3, min(args.steps, 50)), max(3, args.warmup), device)
         e2e["value"] = max_over_ranks(pg, -e2e["value"], device) * -1 * world
     h = csrc_hash()
-    traffic = TRAFFIC.get(name)
-    traffic_val = traffic["bytes"] if traffic and traffic.get("csrc") == h else None
+    traffic_val = traffic_for(name)
     cpu, cpu_table = None, None
     if rank == 0 and world == 1 and args.cpu_baselines != "none" and name not in TV_WORKLOADS:
         cpu, cpu_table = cpu_baselines(name, args.cpu_seconds, args.cpu_baselines)
