@@ -656,53 +656,6 @@ constexpr float GUMBEL2_MIN = -6.f;
 // index that can come within the gap of the best key.
 constexpr float GUMBEL_TIE = 1e-3f;
 
-// Running top two (key, index) of a lane: a key enters when it beats the
-// second; ties keep the earlier (smaller) index.
-__device__ __forceinline__ void top2_push(float &k1, int &i1, float &k2, int &i2, float key, int idx) {
-    if (key > k1) {
-        k2 = k1;
-        i2 = i1;
-        k1 = key;
-        i1 = idx;
-    } else if (key > k2) {
-        k2 = key;
-        i2 = idx;
-    }
-}
-
-// Merge another top two into this one (disjoint index sets); the larger key
-// first, ties to the smaller index.  Index -1: no candidate.
-__device__ __forceinline__ void top2_merge(float &k1, int &i1, float &k2, int &i2, float o1, int j1, float o2, int j2) {
-    auto before = [](float a, int ia, float b, int ib) {  // (a, ia) ranks above (b, ib)
-        return ia >= 0 && (ib < 0 || a > b || (a == b && ia < ib));
-    };
-    float c[4] = {k1, k2, o1, o2};
-    int ci[4] = {i1, i2, j1, j2};
-    int b1 = 0;
-#pragma unroll
-    for (int q = 1; q < 4; ++q)
-        if (before(c[q], ci[q], c[b1], ci[b1])) b1 = q;
-    int b2 = -1;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        if (q != b1 && (b2 < 0 || before(c[q], ci[q], c[b2], ci[b2]))) b2 = q;
-    k1 = c[b1];
-    i1 = ci[b1];
-    k2 = c[b2];
-    i2 = ci[b2];
-}
-
-// Top two across the warp (butterfly over disjoint lane groups); the same
-// result in every lane.
-__device__ __forceinline__ void top2_allreduce(float &k1, int &i1, float &k2, int &i2) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float o1 = __shfl_xor_sync(FULL, k1, o), o2 = __shfl_xor_sync(FULL, k2, o);
-        const int j1 = __shfl_xor_sync(FULL, i1, o), j2 = __shfl_xor_sync(FULL, i2, o);
-        top2_merge(k1, i1, k2, i2, o1, j1, o2, j2);
-    }
-}
-
 // Gumbel noise of index v in row j of sequence b in double precision,
 // G = -ln(-ln U), U = (floor(x / 2^8) + 1/2) 2^-24 from word v mod 4 of
 // Philox4x32-10 at counter (v / 4, j, b, offset).
@@ -716,7 +669,9 @@ __device__ __forceinline__ double gumbel_noise_d(int v, int j, uint32_t b, uint3
 }
 
 // Gumbel-max keys of one chunk (registers; vbase: vector index of the lane's
-// first vector) into the lane's running arg maxes, first index among equals:
+// first vector) into the lane's running arg maxes, first index among equals,
+// and the lane's runner-up keys kp2 and kr2 (the best key other than the
+// arg max's; its index is recovered by warp_top2 only on a near-tie):
 // p keys z_v k + g_v into (kp, ip) and, with RESID, residual keys
 // log2(p_v - q_v) + g_v over the v with p_v > q_v into (kr, ir) (p =
 // 2^{z_t k - ct}, q = 2^{z_d k - cd}; g_v the noise of index v in row j of
@@ -737,7 +692,7 @@ template <typename Tin, int QV, bool RESID>
 __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (&rd)[QV], int cnt, int lane, float k,
                                             float ct, float cd, int vbase, uint32_t seed_lo, uint32_t seed_hi, int j,
                                             uint32_t b, uint32_t offset, float bp, float br, float &kr, int &ir,
-                                            float &kr2, int &ir2, float &kp, int &ip, float &kp2, int &ip2) {
+                                            float &kr2, float &kp, int &ip, float &kp2) {
     constexpr int VEC = Store<Tin>::VEC;
 #pragma unroll
     for (int q = 0; q < QV; ++q) {
@@ -778,12 +733,20 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
                 const int e = h * 4 + e4;
                 const float gv = gumbel2(xs[e4]);
                 const float key_p = zk[e4] + gv;
-                if (key_p > kp2) top2_push(kp, ip, kp2, ip2, key_p, vv * VEC + e);
+                kp2 = fmaxf(kp2, fminf(key_p, kp));  // the runner-up key (its index is found only if needed)
+                if (key_p > kp) {
+                    kp = key_p;
+                    ip = vv * VEC + e;
+                }
                 if (RESID && want_r) {
                     const float w = ex2(zk[e4] - ct) - ex2(fmaf(zd[e], k, -cd));
                     if (w > 0.f) {
                         const float key_r = __log2f(w) + gv;
-                        if (key_r > kr2) top2_push(kr, ir, kr2, ir2, key_r, vv * VEC + e);
+                        kr2 = fmaxf(kr2, fminf(key_r, kr));
+                        if (key_r > kr) {
+                            kr = key_r;
+                            ir = vv * VEC + e;
+                        }
                     }
                 }
             }
@@ -791,13 +754,95 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
     }
 }
 
+// The warp's best two Gumbel-max keys of one draw, {K1, I1, K2, I2}, from
+// every lane's arg max (k1, i1) and runner-up key k2 (index -1: no
+// candidate).  The runner-up is another lane's arg max or, when it is the
+// best lane's own runner-up, a key whose index no lane kept; that index is
+// found only when it matters, a near-tie (K1 - K2 < GUMBEL_TIE): the warp
+// keys the best lane's vectors of the segment once more (vector seg_lo + L +
+// 32 t for lane L, with the pass's own arithmetic) and takes their arg max
+// other than I1.  Indices the pass skipped have keys below K1 - GUMBEL_TIE,
+// so they cannot be that runner-up.  Otherwise the runner-up's index is
+// left at -1: it is never needed.  RKEY: residual keys log2(p - q) + g
+// (target row trow, draft row drow); else p keys z k + g of trow.  Out of
+// line: it runs once per draw, off the streaming path.
+constexpr int TOP2_NONE = 0x7fffffff;      // no candidate
+constexpr int TOP2_HIDDEN = 0x7ffffffe;    // the best lane's runner-up
+
+template <typename Tin, bool RKEY>
+__device__ __noinline__ float4 warp_top2(float k1, int i1, float k2, const unsigned char *trow,
+                                         const unsigned char *drow, int seg_lo, int seg_n, int j, uint32_t b, float k,
+                                         float ct, float cd, uint32_t seed_lo, uint32_t seed_hi, uint32_t offset) {
+    constexpr int VEC = Store<Tin>::VEC;
+    const int lane = threadIdx.x & 31;
+    // larger key first; at equal keys the smaller index (TOP2_HIDDEN after
+    // every index, TOP2_NONE last)
+    auto reduce = [](float &key, int &idx) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ok = __shfl_xor_sync(FULL, key, o);
+            const int oi = __shfl_xor_sync(FULL, idx, o);
+            if (ok > key || (ok == key && oi < idx)) {
+                key = ok;
+                idx = oi;
+            }
+        }
+    };
+    float K1 = k1;
+    int I1 = i1 >= 0 ? i1 : TOP2_NONE;
+    reduce(K1, I1);
+    const unsigned holder = __ballot_sync(FULL, I1 != TOP2_NONE && i1 == I1);
+    const int L1 = holder ? __ffs(holder) - 1 : -1;
+    float K2 = lane == L1 ? k2 : k1;
+    int I2 = lane == L1 ? TOP2_HIDDEN : (i1 >= 0 ? i1 : TOP2_NONE);
+    reduce(K2, I2);
+    if (I2 == TOP2_HIDDEN && K1 - K2 < GUMBEL_TIE) {  // warp-uniform
+        float bk = -INFINITY;
+        int bi = TOP2_NONE;
+        const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + seg_lo;
+        const uint4 *gd = reinterpret_cast<const uint4 *>(drow) + seg_lo;
+        for (int t = lane; L1 + 32 * t < seg_n; t += 32) {
+            const int jv = L1 + 32 * t, vv = seg_lo + jv;
+            float zt[VEC], zd[VEC];
+            Store<Tin>::unpack(__ldg(gt + jv), zt);
+            if (RKEY) Store<Tin>::unpack(__ldg(gd + jv), zd);
+#pragma unroll
+            for (int h = 0; h < VEC / 4; ++h) {
+                const uint4 x = philox4x32_10(
+                    make_uint4(static_cast<uint32_t>(vv * (VEC / 4) + h), static_cast<uint32_t>(j), b, offset),
+                    seed_lo, seed_hi);
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int e = h * 4 + e4, idx = vv * VEC + e;
+                    const float zk = zt[e] * k, gv = gumbel2(xs[e4]);
+                    float key = zk + gv;
+                    if (RKEY) {
+                        const float w = ex2(zk - ct) - ex2(fmaf(zd[e], k, -cd));
+                        key = w > 0.f ? __log2f(w) + gv : -INFINITY;
+                    }
+                    if (idx != I1 && key > -INFINITY && (key > bk || (key == bk && idx < bi))) {
+                        bk = key;
+                        bi = idx;
+                    }
+                }
+            }
+        }
+        reduce(bk, bi);
+        I2 = bi;
+    }
+    return make_float4(K1, __int_as_float(I1 == TOP2_NONE ? -1 : I1), K2,
+                       __int_as_float(I2 >= TOP2_HIDDEN ? -1 : I2));
+}
+
 // The Gumbel-max pass of one warp over its segment [seg_lo, seg_lo + seg_n)
 // of row j (target row trow, draft row drow), read directly from global
 // memory (the rows were streamed moments ago and mostly sit in L2): the
 // warp's two best residual and p keys with their indices (index -1: no
-// candidate; the p keys start at the bound lb).  Out of
-// line and by value: it runs once per sequence, and neither its generator
-// state nor the warp's streaming state should crowd the other's registers.
+// candidate, or a runner-up far from the best; the p keys start at the
+// bound lb).  Out of line and by value: it runs once per sequence, and
+// neither its generator state nor the warp's streaming state should crowd
+// the other's registers.
 struct Top2x2 {
     float4 best;    // {key_r, idx_r, key_p, idx_p}
     float4 second;  // the runners-up, same layout
@@ -812,7 +857,7 @@ __device__ __noinline__ Top2x2 gumbel_pass(const unsigned char *trow, const unsi
     const uint4 *gt = reinterpret_cast<const uint4 *>(trow) + seg_lo;
     const uint4 *gd = reinterpret_cast<const uint4 *>(drow) + seg_lo;
     float kr = -INFINITY, kp = lb, bp = lb, br = -INFINITY, kr2 = -INFINITY, kp2 = -INFINITY;
-    int ir = -1, ip = -1, ir2 = -1, ip2 = -1;
+    int ir = -1, ip = -1;
     // The pass is bound by load latency, not arithmetic: the next tile's
     // loads are in flight while a tile is keyed.
     uint4 rt[QV], rd[QV], nt[QV], nd[QV];
@@ -830,7 +875,7 @@ __device__ __noinline__ Top2x2 gumbel_pass(const unsigned char *trow, const unsi
     for (int base = 0; base < seg_n; base += QV * 32) {
         if (base + QV * 32 < seg_n) load_tile(base + QV * 32, nt, nd);
         gumbel_regs<Tin, QV, RESID>(rt, rd, min(QV * 32, seg_n - base), lane, k, ct, cd, seg_lo + base + lane,
-                                    seed_lo, seed_hi, j, b, offset, bp, br, kr, ir, kr2, ir2, kp, ip, kp2, ip2);
+                                    seed_lo, seed_hi, j, b, offset, bp, br, kr, ir, kr2, kp, ip, kp2);
         // the warp's best p key so far bounds every lane's filters
         if (!RESID) bp = warp_allmax(kp);
 #pragma unroll
@@ -839,32 +884,130 @@ __device__ __noinline__ Top2x2 gumbel_pass(const unsigned char *trow, const unsi
             if (RESID) rd[q] = nd[q];
         }
     }
-    top2_allreduce(kr, ir, kr2, ir2);
-    top2_allreduce(kp, ip, kp2, ip2);
+    const float4 r2 = RESID ? warp_top2<Tin, true>(kr, ir, kr2, trow, drow, seg_lo, seg_n, j, b, k, ct, cd, seed_lo,
+                                                   seed_hi, offset)
+                            : make_float4(-INFINITY, __int_as_float(-1), -INFINITY, __int_as_float(-1));
+    const float4 p2 =
+        warp_top2<Tin, false>(kp, ip, kp2, trow, drow, seg_lo, seg_n, j, b, k, ct, cd, seed_lo, seed_hi, offset);
     Top2x2 r;
-    r.best = make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
-    r.second = make_float4(kr2, __int_as_float(ir2), kp2, __int_as_float(ip2));
+    r.best = make_float4(r2.x, r2.y, p2.x, p2.y);
+    r.second = make_float4(r2.z, r2.w, p2.z, p2.w);
     return r;
 }
 
 // Gumbel-max p keys of one chunk of row j held in a ring slot (target
 // vectors at tb; cnt vectors; chunk_v0: the chunk's first vector in the row)
-// into the lane's running top two, passed and returned by value as {kp, ip,
-// kp2, ip2}; bp is the warp's best p key so far.  Out of line: it runs once per
-// chunk of the bonus draw, and neither its generator state nor the warp's
-// streaming state should crowd the other's registers.
+// into the lane's running arg max and runner-up key, passed and returned by
+// value as {kp, ip, kp2, -}; bp is the warp's best p key so far.  Out of
+// line: it runs once per chunk of the bonus draw, and neither its generator
+// state nor the warp's streaming state should crowd the other's registers.
 template <typename Tin, int CV>
 __device__ __noinline__ float4 gumbel_slot(const unsigned char *tb, int cnt, int chunk_v0, float k, int j, uint32_t b,
                                            uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, float bp, float4 top) {
     const int lane = threadIdx.x & 31;
     float kr = -INFINITY, kr2 = -INFINITY, kp = top.x, kp2 = top.z;
-    int ir = -1, ir2 = -1, ip = __float_as_int(top.y), ip2 = __float_as_int(top.w);
+    int ir = -1, ip = __float_as_int(top.y);
     for (int q = 0; q < CV / 32 && q * 32 + lane < cnt; ++q) {
         const uint4 v[1] = {vec_at(tb, q * 32 + lane)};
         gumbel_regs<Tin, 1, false>(v, v, 32, lane, k, 0.f, 0.f, chunk_v0 + q * 32 + lane, seed_lo, seed_hi, j, b,
-                                   offset, bp, -INFINITY, kr, ir, kr2, ir2, kp, ip, kp2, ip2);
+                                   offset, bp, -INFINITY, kr, ir, kr2, kp, ip, kp2);
     }
-    return make_float4(kp, __int_as_float(ip), kp2, __int_as_float(ip2));
+    return make_float4(kp, __int_as_float(ip), kp2, 0.f);
+}
+
+// A near-tie of a Gumbel-max draw: the two best candidates t1 and t2 (fp32
+// keys within GUMBEL_TIE) keyed once more in double precision, ln w_v + G_v
+// with w the residual weight max(0, p - q) (resid) or p; the larger key wins,
+// ties to the smaller index.  Every warp passes the same inputs in the same
+// order and so takes the same token.  Out of line: it runs for about one
+// draw in a thousand, and its double-precision code should not weigh on the
+// kernel's registers.
+template <typename Tin>
+__device__ __noinline__ int gumbel_retie(const unsigned char *trow, const unsigned char *drow, bool resid, int t1,
+                                         int t2, int j, uint32_t b, float k, float ct, float cd, uint32_t seed_lo,
+                                         uint32_t seed_hi, uint32_t offset) {
+    auto key_d = [&](int v) {
+        const double zt = static_cast<double>(Store<Tin>::scalar_g(trow, static_cast<size_t>(v)));
+        double w = exp2(zt * static_cast<double>(k) - static_cast<double>(ct));
+        if (resid) {
+            const double zd = static_cast<double>(Store<Tin>::scalar_g(drow, static_cast<size_t>(v)));
+            w -= exp2(zd * static_cast<double>(k) - static_cast<double>(cd));
+        }
+        return (w > 0.0 ? log(w) : -static_cast<double>(INFINITY)) + gumbel_noise_d(v, j, b, offset, seed_lo, seed_hi);
+    };
+    const double a1 = key_d(t1), a2 = key_d(t2);
+    return (a2 > a1 || (a2 == a1 && t2 < t1)) ? t2 : t1;
+}
+
+// The final token of a Gumbel-max draw from the S warps' records of the
+// draw's round (rec: S best records, then S runner-up records, each {key_r,
+// idx_r, key_p, idx_p}): the best residual key (at a rejection, resid) or
+// the best p key, the two best candidates re-keyed by gumbel_retie on a
+// near-tie.  Returns {token, flags}: F_ZERO_MASS when every residual weight
+// rounded to zero (the p draw stands in).  Every warp reads the same records
+// in the same order and so takes the same token.  Out of line: it runs once
+// per sequence, after the streaming.
+template <typename Tin>
+__device__ __noinline__ int2 gumbel_select(const float4 *rec, int S, int lane, bool resid, const unsigned char *trow,
+                                           const unsigned char *drow, int j, uint32_t b, float k, float ct, float cd,
+                                           uint32_t seed_lo, uint32_t seed_hi, uint32_t offset) {
+    float vr = -INFINITY, vp = -INFINITY, d0 = 0.f;
+    int jr = -1, jp = -1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int q = 2 * lane + h;
+        if (q < S) {
+            const float4 v = rec[q];
+            argmax_merge(vr, jr, d0, v.x, __float_as_int(v.y), 0.f);
+            argmax_merge(vp, jp, d0, v.z, __float_as_int(v.w), 0.f);
+        }
+    }
+    argmax_allreduce(vr, jr, d0);
+    argmax_allreduce(vp, jp, d0);
+    int flags = 0;
+    if (resid && jr < 0) flags |= F_ZERO_MASS;  // every residual weight rounded to zero
+    const bool use_r = resid && jr >= 0;
+    int tok = use_r ? jr : jp;
+    if (tok < 0) return make_int2(tok, flags);
+    // the runner-up: every warp's best other than the winner, and the
+    // winning warp's own runner-up; its key first, its index only on a
+    // near-tie
+    auto cand = [&](int q, float &key, int &idx) {
+        const float4 v = rec[q], w = rec[S + q];
+        const float kb = use_r ? v.x : v.z, kw = use_r ? w.x : w.z;
+        const int ib = __float_as_int(use_r ? v.y : v.w), iw = __float_as_int(use_r ? w.y : w.w);
+        key = ib == tok ? kw : kb;
+        idx = ib == tok ? iw : ib;
+    };
+    float k2 = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int q = 2 * lane + h;
+        if (q < S) {
+            float key;
+            int idx;
+            cand(q, key, idx);
+            if (idx >= 0) k2 = fmaxf(k2, key);
+        }
+    }
+    k2 = warp_allmax(k2);
+    if ((use_r ? vr : vp) - k2 < GUMBEL_TIE) {  // warp-uniform
+        float v2 = -INFINITY;
+        int t2 = -1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int q = 2 * lane + h;
+            if (q < S) {
+                float key;
+                int idx;
+                cand(q, key, idx);
+                argmax_merge(v2, t2, d0, key, idx, 0.f);
+            }
+        }
+        argmax_allreduce(v2, t2, d0);
+        if (t2 >= 0) tok = gumbel_retie<Tin>(trow, drow, use_r, tok, t2, j, b, k, ct, cd, seed_lo, seed_hi, offset);
+    }
+    return make_int2(tok, flags);
 }
 
 template <typename Tin, int CV, int MODE, bool DBL>
@@ -1211,10 +1354,9 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 float4 second = best;
                 if (!(flags & ERR_BITS)) {
                     const uint32_t bb = static_cast<uint32_t>(b);
-                    float kr = -INFINITY, kp = fmaf(r.Mt, k, GUMBEL2_MIN);  // the best p key is at least max z k + min g
-                    int ir = -1, ip = -1;
-                    float kr2 = -INFINITY, kp2 = -INFINITY;
-                    int ir2 = -1, ip2 = -1;
+                    const float kp = fmaf(r.Mt, k, GUMBEL2_MIN);  // the best p key is at least max z k + min g
+                    const int ip = -1;
+                    const float kp2 = -INFINITY;
                     if (resid) {
                         // drop the look-ahead rows past the rejection (the producer
                         // moves on to the next sequence's first row) and read row j
@@ -1241,7 +1383,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                         c.p_done = (c.nch == 0);
                         c.c_conf = g;  // the path is fixed
                         float bp = kp;
-                        float4 top = make_float4(kp, __int_as_float(ip), kp2, __int_as_float(ip2));
+                        float4 top = make_float4(kp, __int_as_float(ip), kp2, 0.f);
                         for (int ch = 0; ch < c.nch; ++ch) {
                             produce<Tin, MODE, DBL>(A, c);
                             if (c.pcount == c.ccount) c.dead = true;
@@ -1254,14 +1396,12 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                             produce<Tin, MODE, DBL>(A, c);
                             bp = warp_allmax(top.x);  // the warp's best p key so far bounds every lane's filters
                         }
-                        kp = top.x;
-                        ip = __float_as_int(top.y);
-                        kp2 = top.z;
-                        ip2 = __float_as_int(top.w);
-                        top2_allreduce(kr, ir, kr2, ir2);
-                        top2_allreduce(kp, ip, kp2, ip2);
-                        best = make_float4(kr, __int_as_float(ir), kp, __int_as_float(ip));
-                        second = make_float4(kr2, __int_as_float(ir2), kp2, __int_as_float(ip2));
+                        const float4 p2 = warp_top2<Tin, false>(top.x, __float_as_int(top.y), top.z,
+                                                                row_base<Tin>(A, true, b, j), nullptr, c.seg_lo,
+                                                                c.seg_n, j, bb, k, 0.f, 0.f, A.seed_lo, A.seed_hi,
+                                                                A.offset);
+                        best = make_float4(-INFINITY, __int_as_float(-1), p2.x, p2.y);
+                        second = make_float4(-INFINITY, __int_as_float(-1), p2.z, p2.w);
                     }
                 }
                 // every warp fills round gamma + 1 with its two best candidates
@@ -1273,46 +1413,12 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
                 if (c.dead) {
                     flags |= F_TIMEOUT;
                 } else if (!(flags & ERR_BITS)) {
-                    float vr = -INFINITY, vp = -INFINITY, vr2 = -INFINITY, vp2 = -INFINITY;
-                    int jr = -1, jp = -1, jr2 = -1, jp2 = -1;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int q = 2 * c.lane + h;
-                        if (q < c.S) {
-                            const float4 v = *rec_at(c, c.bank, g + 1, q);
-                            const float4 w = *rec_at(c, c.bank, g + 1, c.S + q);
-                            top2_merge(vr, jr, vr2, jr2, v.x, __float_as_int(v.y), w.x, __float_as_int(w.y));
-                            top2_merge(vp, jp, vp2, jp2, v.z, __float_as_int(v.w), w.z, __float_as_int(w.w));
-                        }
-                    }
-                    top2_allreduce(vr, jr, vr2, jr2);
-                    top2_allreduce(vp, jp, vp2, jp2);
-                    if (resid && jr < 0) flags |= F_ZERO_MASS;  // every residual weight rounded to zero
-                    const bool use_r = resid && jr >= 0;
-                    tok = use_r ? jr : jp;
-                    const int tok2 = use_r ? jr2 : jp2;
-                    const float gap = use_r ? vr - vr2 : vp - vp2;
-                    if (tok >= 0 && tok2 >= 0 && gap < GUMBEL_TIE) {
-                        // a near-tie: both keys once more in double precision
-                        // (the same inputs and order in every warp, so every
-                        // warp takes the same token)
-                        const unsigned char *trow = row_base<Tin>(A, true, b, j);
-                        const unsigned char *drow = row_base<Tin>(A, false, b, j);
-                        const uint32_t bb = static_cast<uint32_t>(b);
-                        auto key_d = [&](int v) {
-                            const double zt = static_cast<double>(St::scalar_g(trow, static_cast<size_t>(v)));
-                            const double lp = zt * static_cast<double>(k) - static_cast<double>(r.ct);
-                            double w = exp2(lp);
-                            if (use_r) {
-                                const double zd = static_cast<double>(St::scalar_g(drow, static_cast<size_t>(v)));
-                                w -= exp2(zd * static_cast<double>(k) - static_cast<double>(r.cd));
-                            }
-                            return (w > 0.0 ? log(w) : -static_cast<double>(INFINITY)) +
-                                   gumbel_noise_d(v, j, bb, A.offset, A.seed_lo, A.seed_hi);
-                        };
-                        const double a1 = key_d(tok), a2 = key_d(tok2);
-                        if (a2 > a1 || (a2 == a1 && tok2 < tok)) tok = tok2;
-                    }
+                    const int2 sel = gumbel_select<Tin>(rec_at(c, c.bank, g + 1, 0), c.S, c.lane, resid,
+                                                        row_base<Tin>(A, true, b, j), row_base<Tin>(A, false, b, j), j,
+                                                        static_cast<uint32_t>(b), k, r.ct, r.cd, A.seed_lo, A.seed_hi,
+                                                        A.offset);
+                    tok = sel.x;
+                    flags |= sel.y;
                     if (tok < 0) flags |= F_NONFINITE;
                 }
                 owner = 0;
