@@ -229,18 +229,29 @@ __device__ __forceinline__ bool mslot_ready(const TVArgs &A, MC &c) {
     return true;
 }
 
-// Group gi of this lane's vectors, from the current ring slot (-inf beyond
-// the segment), or all -inf for a warp without vectors.
+// Group gi of this lane's vectors, from the current ring slot.  A slot's
+// vectors past the segment (all of them for a warp without vectors) hold
+// -inf logits: mfill_tails writes them once, and the copies never reach
+// them.
 template <typename Tin, int NS>
 __device__ __forceinline__ void mload_group(const MC &c, int gi, uint4 (&v)[Group<NS>::GS]) {
     constexpr int GS = Group<NS>::GS;
-    const uint4 NEG = make_uint4(NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w);
     const unsigned char *buf = c.ring + c.cslot * mslot_bytes(NS);
 #pragma unroll
-    for (int q = 0; q < GS; ++q) {
-        const int j = (gi * GS + q) * 32 + c.lane;
-        v[q] = j < c.seg_n ? vec_at(buf, j) : NEG;
+    for (int q = 0; q < GS; ++q) v[q] = vec_at(buf, (gi * GS + q) * 32 + c.lane);
+}
+
+// Fill every ring slot's vectors past this warp's segment with -inf logits
+// (probability 0 in every pass), so that loading a group needs no bound
+// test.  Generic-proxy stores to bytes no bulk copy writes.
+template <typename Tin, int NS>
+__device__ __forceinline__ void mfill_tails(const MC &c) {
+    const uint4 NEG = make_uint4(NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w, NegInf<Tin>::w);
+    for (int s = 0; s < c.R; ++s) {
+        uint4 *slot = reinterpret_cast<uint4 *>(c.ring + s * mslot_bytes(NS));
+        for (int j = max(c.seg_n, 0) + c.lane; j < NS * 32; j += 32) slot[j] = NEG;
     }
+    __syncwarp();
 }
 
 // Hand the current ring slot back (every value read from it is consumed).
@@ -365,6 +376,7 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
     c.wait_ns = A.wait_ns ? A.wait_ns : 2000000000ull;
 
     if (c.warp == 0) tmem_alloc(&sh.tmem_base, TMEM_COLS);
+    mfill_tails<Tin, NS>(c);
     if (c.lane == 0)
         for (int s = 0; s < c.R; ++s) mbar_init(smem_addr(&c.ws->full[s]), 1);
     if (threadIdx.x == 0) {
