@@ -57,7 +57,7 @@ struct RowShared {
     float T[2];
     int ids[2][MAX_GAMMA];
     float u[2][MAX_GAMMA + 1];
-    unsigned long long lbar[2];  // load barriers, one per stream
+    unsigned long long lbar[2][2];  // load barriers: [stream][target slice, draft slice]
 };
 constexpr uint32_t HDR_BYTES = (sizeof(RowShared) + 127u) & ~127u;
 uint32_t row_hdr_bytes() { return HDR_BYTES; }
@@ -384,14 +384,26 @@ __device__ __forceinline__ void issue_unit(const VerifyArgs &A, StreamSt &st, co
     const bool has_d = st.i < g;
     if (threadIdx.x == 0) {
         fence_proxy_async();
-        mbar_arrive_expect_tx(bar, has_d ? 2 * bytes : bytes);
         const size_t lo = static_cast<size_t>(s.lo) * Store<Tin>::ES;
+        mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(smem_addr(tb), row_ptr<Tin>(A.target, static_cast<size_t>(st.b) * (g + 1) + st.i, A.V) + lo, bytes,
                  bar);
+        // the draft slice on its own barrier (completed at once without a draft
+        // row), so that the target's first pass overlaps the draft's arrival
+        mbar_arrive_expect_tx(bar + 8u, has_d ? bytes : 0u);
         if (has_d)
-            bulk_g2s(smem_addr(db), row_ptr<Tin>(A.draft, static_cast<size_t>(st.b) * g + st.i, A.V) + lo, bytes, bar);
+            bulk_g2s(smem_addr(db), row_ptr<Tin>(A.draft, static_cast<size_t>(st.b) * g + st.i, A.V) + lo, bytes,
+                     bar + 8u);
     }
     st.armed = 1;
+}
+
+// Wait for both slices of a unit (target barrier `bar`, draft barrier next
+// to it); false when a bounded wait gave up.
+__device__ __forceinline__ bool wait_unit(uint32_t bar, uint32_t ph) {
+    const bool a = mbar_wait_bounded(bar, ph);
+    const bool b = mbar_wait_bounded(bar + 8u, ph);
+    return a && b;
 }
 
 // Argument checks of stream si's sequence, from its prefetched parameters
@@ -455,8 +467,10 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
 
     if (tid == 0) {
         xchg_init(sh.x);
-        mbar_init(smem_addr(&sh.lbar[0]), 1);
-        mbar_init(smem_addr(&sh.lbar[1]), 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(smem_addr(&sh.lbar[q][0]), 1);
+            mbar_init(smem_addr(&sh.lbar[q][1]), 1);
+        }
         fence_mbar_init();
     }
     const int NS = A.streams;  // sequences in flight per CTA
@@ -465,8 +479,8 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
     StreamSt st1 = NS > 1 ? start_seq(A, sh, 1, cid + NC, DECIDE, 0) : StreamSt{};
     __syncthreads();
     cluster_sync();  // peers' barriers are initialised before any push
-    if (st0.active) issue_unit<Tin>(A, st0, s, tbuf(0), tbuf(0) + A.slice_bytes, smem_addr(&sh.lbar[0]));
-    if (st1.active) issue_unit<Tin>(A, st1, s, tbuf(1), tbuf(1) + A.slice_bytes, smem_addr(&sh.lbar[1]));
+    if (st0.active) issue_unit<Tin>(A, st0, s, tbuf(0), tbuf(0) + A.slice_bytes, smem_addr(&sh.lbar[0][0]));
+    if (st1.active) issue_unit<Tin>(A, st1, s, tbuf(1), tbuf(1) + A.slice_bytes, smem_addr(&sh.lbar[1][0]));
     if (tid == 0) {
         sh.st[0] = st0;
         sh.st[1] = st1;
@@ -484,7 +498,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
             if (!st.active) continue;
             any = true;
             unsigned char *tb = tbuf(si), *db = tb + A.slice_bytes;
-            const uint32_t lbar = smem_addr(&sh.lbar[si]);
+            const uint32_t lbar = smem_addr(&sh.lbar[si][0]);
             const int b = st.b, i = st.i;
             bool finish = false;
             bool issued_early = false;  // the stream's next unit is already in flight
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                 finish = true;
                 if (dead) st.flags |= F_TIMEOUT;
                 if (st.armed) {  // drain the copy before the buffers change hands
-                    mbar_wait_bounded(lbar, st.ph);
+                    wait_unit(lbar, st.ph);
                     st.ph ^= 1u;
                     st.armed = 0;
                 }
@@ -502,7 +516,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                 // ---- greedy (T = 0): the target's arg max decides
                 int tmo = 0;
                 if (st.armed) {
-                    if (!mbar_wait_bounded(lbar, st.ph)) tmo = 1;
+                    if (!wait_unit(lbar, st.ph)) tmo = 1;
                     st.ph ^= 1u;
                     st.armed = 0;
                 } else if (!A.aligned) {
@@ -566,19 +580,23 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                 const float k = LOG2E / T;
                 const bool has_d = i < g;
                 int tmo = 0;
+                const bool split = st.armed;  // the draft slice is waited for after the target's pass
                 if (st.armed) {
                     if (!mbar_wait_bounded(lbar, st.ph)) tmo = 1;
-                    st.ph ^= 1u;
-                    st.armed = 0;
                 } else if (!A.aligned) {
                     load_slice<Tin, NT>(s, row_ptr<Tin>(A.target, static_cast<size_t>(b) * (g + 1) + i, A.V), tb, 0, false);
                     if (has_d) load_slice<Tin, NT>(s, row_ptr<Tin>(A.draft, static_cast<size_t>(b) * g + i, A.V), db, 0, false);
+                    __syncthreads();
                 }
-                __syncthreads();
 
                 // pass A: online max / normaliser (and entropy sum) per row
                 bool nonfin = false;
                 Soft at = thread_soft<Tin, STATS, NT>(tb, s.nvec, k, nonfin);
+                if (split) {
+                    if (!mbar_wait_bounded(lbar + 8u, st.ph)) tmo = 1;
+                    st.ph ^= 1u;
+                    st.armed = 0;
+                }
                 Soft ad = has_d ? thread_soft<Tin, false, NT>(db, s.nvec, k, nonfin) : soft_empty();
                 const bool want_y = DECIDE && has_d && !st.stopped;
                 const int y = want_y ? sh.ids[si][i] : -1;
@@ -655,7 +673,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                                 st.flags |= F_TIMEOUT;
                                 finish = true;
                                 if (issued_early && st.armed) {  // the early copy lands before the buffers change hands
-                                    mbar_wait_bounded(lbar, st.ph);
+                                    wait_unit(lbar, st.ph);
                                     st.ph ^= 1u;
                                     st.armed = 0;
                                 }
@@ -735,7 +753,7 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
     // Copies that outlived a bounded wait must land before the CTA exits.
     for (int si = 0; si < NS; ++si) {
         const StreamSt st = sh.st[si];
-        if (st.armed) mbar_wait_bounded(smem_addr(&sh.lbar[si]), st.ph);
+        if (st.armed) wait_unit(smem_addr(&sh.lbar[si][0]), st.ph);
     }
     cluster_sync();  // no CTA leaves while a peer may still push into it
 }
