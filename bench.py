@@ -60,17 +60,17 @@ KERNEL_FILES = {
 # Captures on a reduced case are scaled to the workload by the units
 # processed (traffic grows in proportion; profiles/ says which).
 TRAFFIC = {
-    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,089,216 read + 3,650,560 written
+    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,216,192 read + 4,020,736 written
     # (profiles/stream_kernel_rl512.md)
-    "rl512": {"bytes": 1069739776, "family": "stream", "csrc": "a85b25773c784224"},
-    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,093,342,464 read + 873,745,152 written) x 32
+    "rl512": {"bytes": 1070236928, "family": "stream", "csrc": "a5f4926d5313d90d"},
+    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,098,446,080 read + 872,957,440 written) x 32
     # for N = 16,384 (profiles/tv_tmem_kernel_tvloss_n512.md)
-    "tvloss": {"bytes": 62946803712, "family": "tv_tmem", "csrc": "eb1bfaa10f8406a2"},
+    "tvloss": {"bytes": 63084912640, "family": "tv_tmem", "csrc": "ed090e01c35f1886"},
     # row_kernel_impl<float,2> (statistics) and <float,1> (verify with statistics) on the first 64
-    # sequences of deep256 (583,623,936 + 3,812,352 and 583,899,136 + 3,688,448 bytes) x 4 for
+    # sequences of deep256 (583,620,352 + 3,546,624 and 583,904,768 + 3,700,736 bytes) x 4 for
     # B = 256 (profiles/row_kernel_deep256_b64.md)
-    "stats256": {"bytes": 2349745152, "family": "row", "csrc": "7d67229aa8896636"},
-    "deep256": {"bytes": 2350350336, "family": "row", "csrc": "7d67229aa8896636"},
+    "stats256": {"bytes": 2348667904, "family": "row", "csrc": "95116e72a8f1fa14"},
+    "deep256": {"bytes": 2350422016, "family": "row", "csrc": "95116e72a8f1fa14"},
 }
 
 
