@@ -52,6 +52,8 @@ KERNEL_FILES = {
     "stream": ["stream_kernels.cu", "chunk_math.cuh", "common.cuh", "philox.cuh", "kernels.h"],
     "tv_tmem": ["tv_tmem_kernels.cu", "chunk_math.cuh", "common.cuh", "tmem.cuh", "kernels.h"],
     "row": ["row_kernels.cu", "common.cuh", "kernels.h"],
+    "pair": ["pair_stream_kernels.cu", "chunk_math.cuh", "common.cuh", "kernels.h"],
+    "tv_stream": ["tv_stream_kernels.cu", "chunk_math.cuh", "common.cuh", "kernels.h"],
 }
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
