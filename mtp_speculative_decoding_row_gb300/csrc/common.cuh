@@ -28,6 +28,52 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------- debug-build checks --
+//
+// Built with MTP_DEBUG (build.build(debug=True) -> libmtprs_debug.so), the
+// primitives below check every access they make against the launch: a shared
+// 16-byte vector load, a bulk copy's shared destination (and the 16-byte
+// alignment of both ends and of its size), a DSMEM address before it is
+// mapped to a peer, and a TMEM column.  A failed check prints one line
+// starting with "MTP_DEBUG" and the access is skipped (a load returns zeros):
+// nothing traps, and the results go wrong so that the oracle comparison
+// fails too.  Stores to global memory are not checked.  In the normal build
+// every check compiles to nothing.
+#ifdef MTP_DEBUG
+}  // namespace mtp
+#include <cstdio>
+namespace mtp {
+__device__ __forceinline__ uint32_t dbg_smem_base() {
+    extern __shared__ __align__(16) unsigned char mtp_dbg_dyn_smem[];
+    return smem_addr(mtp_dbg_dyn_smem);
+}
+__device__ __forceinline__ uint32_t dbg_smem_size() {
+    uint32_t r;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+// True when [addr, addr + bytes) lies in this CTA's dynamic shared memory.
+__device__ __forceinline__ bool dbg_smem_ok(uint32_t addr, uint32_t bytes) {
+    const uint32_t base = dbg_smem_base();
+    return addr >= base && addr - base + bytes <= dbg_smem_size();
+}
+static __device__ __noinline__ void dbg_report(const char *what, uint64_t a, uint64_t b) {
+    printf("MTP_DEBUG %s block %d thread %d a=%llu b=%llu\n", what, static_cast<int>(blockIdx.x),
+           static_cast<int>(threadIdx.x), static_cast<unsigned long long>(a), static_cast<unsigned long long>(b));
+}
+#define MTP_DBG_CHECK(cond, what, a, b, onfail) \
+    do {                                        \
+        if (!(cond)) {                          \
+            dbg_report(what, a, b);             \
+            onfail;                             \
+        }                                       \
+    } while (0)
+#else
+#define MTP_DBG_CHECK(cond, what, a, b, onfail) \
+    do {                                        \
+    } while (0)
+#endif
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -127,6 +173,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 
 // Bulk copy global -> own shared memory; completion counted on `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    MTP_DBG_CHECK(dbg_smem_ok(dst, bytes) && dbg_smem_ok(bar, 8) && dst % 16 == 0 && bytes % 16 == 0 &&
+                      reinterpret_cast<uintptr_t>(src) % 16 == 0 && bar % 8 == 0,
+                  "bulk_g2s", dst, bytes, return);
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
@@ -165,6 +214,7 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+    MTP_DBG_CHECK(dbg_smem_ok(addr, 4), "map_rank", addr, rank, (void)0);
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
@@ -350,6 +400,10 @@ __device__ __forceinline__ bool load_slice(const Slice &s, const void *row, unsi
 }
 
 __device__ __forceinline__ uint4 vec_at(const unsigned char *buf, int j) {
+    MTP_DBG_CHECK(!__isShared(buf + 16 * static_cast<ptrdiff_t>(j)) ||
+                      (dbg_smem_ok(smem_addr(buf + 16 * static_cast<ptrdiff_t>(j)), 16) &&
+                       smem_addr(buf + 16 * static_cast<ptrdiff_t>(j)) % 16 == 0),
+                  "vec_at", smem_addr(buf), static_cast<uint32_t>(j), return make_uint4(0u, 0u, 0u, 0u));
     return reinterpret_cast<const uint4 *>(buf)[j];
 }
 

@@ -18,6 +18,8 @@
 
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace mtp {
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -55,6 +57,7 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane0, uin
 // Warp-wide: each thread stores one 16-byte vector into columns col .. col+3
 // of its own lane.
 __device__ __forceinline__ void tmem_st_v4(uint32_t taddr, const uint4 &v) {
+    MTP_DBG_CHECK((taddr & 0xffffu) + 4u <= TMEM_COLS && (taddr >> 16) < 128u, "tmem_st", taddr, 0, (void)0);
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
@@ -63,6 +66,7 @@ __device__ __forceinline__ void tmem_st_v4(uint32_t taddr, const uint4 &v) {
 // Warp-wide: each thread loads one 16-byte vector from columns col .. col+3
 // of its own lane.  The registers are valid after tmem_wait_ld().
 __device__ __forceinline__ void tmem_ld_v4(uint32_t taddr, uint4 &v) {
+    MTP_DBG_CHECK((taddr & 0xffffu) + 4u <= TMEM_COLS && (taddr >> 16) < 128u, "tmem_ld", taddr, 0, (void)0);
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(taddr)

@@ -10,6 +10,10 @@ DEV = torch.device("cuda:0")
 
 
 def ensure_library():
+    from tests import gpu_util_paths
+
+    if gpu_util_paths.LIBRARY:
+        return mtp.load_library(gpu_util_paths.LIBRARY)
     mtp_build.build()
     return mtp.load_library()
 
