@@ -62,17 +62,24 @@ KERNEL_FILES = {
 # Captures on a reduced case are scaled to the workload by the units
 # processed (traffic grows in proportion; profiles/ says which).
 TRAFFIC = {
-    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,216,192 read + 4,020,736 written
+    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,557,184 read + 3,804,672 written
     # (profiles/stream_kernel_rl512.md)
-    "rl512": {"bytes": 1070236928, "family": "stream", "csrc": "a5f4926d5313d90d"},
-    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,098,446,080 read + 872,957,440 written) x 32
+    "rl512": {"bytes": 1070361856, "family": "stream", "csrc": "4e8673afdd0af569"},
+    # stream_kernel_impl<bf16_t,128,2> and <bf16_t,192,2> (Gumbel-max verify and draft sampling) in
+    # full: 132,863,744 + 5,873,152 and 58,887,936 + 493,312 bytes (profiles/stream_kernel_gumbel.md)
+    "gumbel64": {"bytes": 138736896, "family": "stream", "csrc": "4e8673afdd0af569"},
+    "gsample192": {"bytes": 59381248, "family": "stream", "csrc": "4e8673afdd0af569"},
+    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,089,974,272 read + 872,883,200 written) x 32
     # for N = 16,384 (profiles/tv_tmem_kernel_tvloss_n512.md)
-    "tvloss": {"bytes": 63084912640, "family": "tv_tmem", "csrc": "ed090e01c35f1886"},
+    "tvloss": {"bytes": 62811439104, "family": "tv_tmem", "csrc": "5078ba172ada3c2a"},
+    # tvs_kernel_impl<bf16_t,160,1> (top-K targets) at N = 512 (691,457,280 read + 873,746,176
+    # written) x 32 for N = 16,384, the same launch plan (profiles/tv_stream_kernel_tvtopk_n512.md)
+    "tvtopk": {"bytes": 50086510592, "family": "tv_stream", "csrc": "f7118740f92f9310"},
     # row_kernel_impl<float,2> (statistics) and <float,1> (verify with statistics) on the first 64
-    # sequences of deep256 (583,620,352 + 3,546,624 and 583,904,768 + 3,700,736 bytes) x 4 for
+    # sequences of deep256 (583,617,024 + 4,086,272 and 583,896,832 + 4,410,368 bytes) x 4 for
     # B = 256 (profiles/row_kernel_deep256_b64.md)
-    "stats256": {"bytes": 2348667904, "family": "row", "csrc": "95116e72a8f1fa14"},
-    "deep256": {"bytes": 2350422016, "family": "row", "csrc": "95116e72a8f1fa14"},
+    "stats256": {"bytes": 2350813184, "family": "row", "csrc": "0dda1edb6e04823d"},
+    "deep256": {"bytes": 2353228800, "family": "row", "csrc": "0dda1edb6e04823d"},
 }
 
 
