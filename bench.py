@@ -371,6 +371,41 @@ class TVWorkload:
                 "draft = target + N(0,0.5)), fp32 gradient, T=1")
 
 
+def method_stats(out) -> dict:
+    """What the method computed in the last timed call, read back after the
+    timed region: acceptance (mean accepted drafts per sequence, acceptance
+    rate per draft position), the mean overlap alpha and target entropy, the
+    TV loss, and how many rows came back flagged."""
+    import numpy as np
+
+    if out is None:
+        return {}
+    f = out._asdict()
+    r = {}
+    flags = f["row_flags"].cpu().numpy()
+    good = flags == 0
+    r["flagged_rows"] = int((~good).sum())
+    if "accept_len" in f:
+        n = f["accept_len"].cpu().numpy()[good]
+        gamma = f["tokens"].shape[1] - 1
+        r["mean_accept_len"] = float(n.mean()) if n.size else None
+        r["acceptance_rate"] = float(n.mean() / gamma) if n.size else None
+    if f.get("alpha") is not None:
+        a = f["alpha"].cpu().numpy()[good]
+        r["mean_alpha"] = float(np.nanmean(a)) if a.size else None
+    ent = f.get("entropy", f.get("ent_p"))
+    if ent is not None:
+        e = ent.cpu().numpy()[good]
+        r["mean_entropy_nats"] = float(np.nanmean(e)) if e.size else None
+    if "rs_better" in f:
+        rb = f["rs_better"].cpu().numpy()[good]
+        r["rs_better_fraction"] = float(rb.mean()) if rb.size else None
+    if "loss" in f:
+        lo = f["loss"].cpu().numpy()[good]
+        r["mean_loss"] = float(lo.mean()) if lo.size else None
+    return r
+
+
 def time_graph(wl, steps: int, warmup: int, device) -> dict:
     """Capture `copies` consecutive calls in a CUDA graph; replay; time K calls."""
     import torch
@@ -639,7 +674,9 @@ def run_cuda(args, world, rank, local, pg):
         torch.cuda.synchronize(device)
         if sampler:
             sampler.start()
+        torch.cuda.nvtx.range_push(f"mtp {name}")  # a range per workload for timeline tools
         t = time_graph(wl, steps, args.warmup, device)
+        torch.cuda.nvtx.range_pop()
         clocks = sampler.stop() if sampler else None
         t_ms = max_over_ranks(pg, t["ms_total"], device)
         alg = wl.alg_bytes()
@@ -666,6 +703,7 @@ def run_cuda(args, world, rank, local, pg):
             "input_copies": wl.copies,
         }
         r["traffic"] = traffic_for(name)
+        r["method"] = method_stats(wl.out if tv else wl.outs[0])
         results[name] = r
         if head is None:
             head = (name, wl, t, t_ms, steps, clocks, alg, achieved)
