@@ -405,6 +405,12 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
     // just read.  So the stores of one position overlap the loads and
     // arithmetic of the next instead of every warp storing at once.
     int prev_t = -1, prev_flags = 0, prev_done = 0;  // pending G: position, its flags, rows done
+    // The next position's target row 0 is folded before this position's
+    // chain waits for the overlap records, so that its streaming covers the
+    // wait for the cluster's slowest warp (the ring's copy order is the same).
+    bool pre_nt = false;  // the fold below already holds target row 0 of position t
+    float pre_mt = -INFINITY, pre_st = 0.f;
+    int pre_bad = 0;
     for (int t = c.vc; t < A.N; t += c.NT_) {
         float *grow = A.grad + static_cast<size_t>(t) * g * static_cast<size_t>(A.V);
         int flags = 0;
@@ -426,7 +432,14 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
                 if (u < g) {
                     float mt, st, md, sd;
                     int bad = 0;
-                    mnorm_row<Tin, NS, false>(A, c, u, k, mt, st, bad);
+                    if (u == 0 && pre_nt) {
+                        mt = pre_mt;
+                        st = pre_st;
+                        bad = pre_bad;
+                    } else {
+                        mnorm_row<Tin, NS, false>(A, c, u, k, mt, st, bad);
+                    }
+                    pre_nt = false;
                     if (c.dead) break;
                     mnorm_row<Tin, NS, true>(A, c, u, k, md, sd, bad);
                     if (c.dead) break;
@@ -498,6 +511,12 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
             // rows of the previous position still pending (the loop above
             // stopped early): before the chain overwrites their coefficients
             for (; prev_t >= 0 && prev_done < g; ++prev_done) mgrad_row<Tin, NS>(A, c, prev_t, prev_done, prev_flags, k);
+            // the next position's target row 0, while the overlap records arrive
+            if (!c.dead && t + c.NT_ < A.N) {
+                pre_bad = 0;
+                mnorm_row<Tin, NS, false>(A, c, 0, k, pre_mt, pre_st, pre_bad);
+                pre_nt = !c.dead;
+            }
             // ---- the chain: every warp from the gathered records
             if (!c.dead) {
                 float av[MAXG], sv[MAXG];
