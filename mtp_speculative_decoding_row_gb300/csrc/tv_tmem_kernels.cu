@@ -460,23 +460,30 @@ __global__ void __launch_bounds__(NT, 1) tvm_kernel_impl(const TVArgs A) {
                 // ---- O(kk): the final normalisers, then the parked pair
                 const int kk = u - 1;
                 if (!mwait_round(sh, c, kk)) break;
-                Soft lt = soft_empty(), ld = soft_empty();
+                // the cluster's normalisers from the S warp records: the maxima
+                // first, then every record's sum rescaled once (a NaN sum, a
+                // flagged row, propagates; an empty record adds nothing)
+                float4 rv[MAXS / 32];
+                float mtl = -INFINITY, mdl = -INFINITY;
 #pragma unroll
                 for (int h = 0; h < MAXS / 32; ++h) {
                     const int q = (MAXS / 32) * c.lane + h;
-                    if (q < c.S) {
-                        const float4 v = *mrec(c, kk, q);
-                        Soft r;
-                        r.m = v.x;
-                        r.s = v.y;
-                        r.s1 = 0.f;
-                        lt = soft_pair_merge(lt, r, k);
-                        r.m = v.z;
-                        r.s = v.w;
-                        ld = soft_pair_merge(ld, r, k);
-                    }
+                    rv[h] = q < c.S ? *mrec(c, kk, q) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+                    mtl = fmaxf(mtl, rv[h].x);
+                    mdl = fmaxf(mdl, rv[h].z);
                 }
-                const Soft Ct = soft_warp_allreduce<false>(lt, k), Cd = soft_warp_allreduce<false>(ld, k);
+                Soft Ct, Cd;
+                Ct.m = warp_allmax(mtl);
+                Cd.m = warp_allmax(mdl);
+                float stl = 0.f, sdl = 0.f;
+#pragma unroll
+                for (int h = 0; h < MAXS / 32; ++h) {
+                    if (rv[h].y != 0.f) stl = fmaf(rv[h].y, ex2((rv[h].x - Ct.m) * k), stl);
+                    if (rv[h].w != 0.f) sdl = fmaf(rv[h].w, ex2((rv[h].z - Cd.m) * k), sdl);
+                }
+                Ct.s = warp_allsum(stl);
+                Cd.s = warp_allsum(sdl);
+                Ct.s1 = Cd.s1 = 0.f;
                 if (!(Ct.m > -INFINITY) || !(Ct.s > 0.f) || !(Ct.s < INFINITY) || !(Cd.m > -INFINITY) ||
                     !(Cd.s > 0.f) || !(Cd.s < INFINITY))
                     flags |= F_NONFINITE;
