@@ -69,9 +69,9 @@ TRAFFIC = {
     # full: 132,863,744 + 5,873,152 and 58,887,936 + 493,312 bytes (profiles/stream_kernel_gumbel.md)
     "gumbel64": {"bytes": 138736896, "family": "stream", "csrc": "4e8673afdd0af569"},
     "gsample192": {"bytes": 59381248, "family": "stream", "csrc": "4e8673afdd0af569"},
-    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,124,569,344 read + 873,304,576 written) x 32
+    # tvm_kernel_impl<bf16_t,10> at N = 512 (1,123,948,800 read + 872,851,968 written) x 32
     # for N = 16,384 (profiles/tv_tmem_kernel_tvloss_n512.md)
-    "tvloss": {"bytes": 63931965440, "family": "tv_tmem", "csrc": "2b5d0e4fa84f79e0"},
+    "tvloss": {"bytes": 63897624576, "family": "tv_tmem", "csrc": "04c6799a1030e40f"},
     # tvs_kernel_impl<bf16_t,160,1> (top-K targets) at N = 512 (691,457,280 read + 873,746,176
     # written) x 32 for N = 16,384, the same launch plan (profiles/tv_stream_kernel_tvtopk_n512.md)
     "tvtopk": {"bytes": 50086510592, "family": "tv_stream", "csrc": "f7118740f92f9310"},
