@@ -191,9 +191,10 @@ int mtp_gumbel_verify(const void *target_logits, const void *draft_logits, mtp_d
  *   out_ids [R] int32 (-1 for a flagged row), row_flags [R] or NULL
  *   (BAD_TEMP, BAD_UNIFORM, NONFINITE).
  * Requirements: 16-byte aligned base and V a multiple of 16 / esize (else
- * MTP_ERR_MISALIGNED).  Each row is read once from HBM plus, for the draw, a
- * second time shortly after (inverse CDF: one chunk of the row; Gumbel-max:
- * the row, mostly from L2).
+ * MTP_ERR_MISALIGNED).  Inverse CDF: each row is read once from HBM and one
+ * chunk of it a second time for the draw.  Gumbel-max: each row is read once
+ * (its arg max needs no normaliser); a near-tie of the two best keys
+ * re-reads those two logits.
  */
 int mtp_draft_sample(const void *draft_logits, mtp_dtype dtype, const float *temperature, const float *uniforms,
                      int method, uint64_t seed, uint32_t offset, int R, int V, int32_t *out_ids,
@@ -332,8 +333,9 @@ int mtp_tv_loss_topk(const void *target_values, const int32_t *target_idx, const
  * CTAs per thread-block cluster; the vocabulary is split across them),
  * clusters (persistent clusters launched), smem_bytes (dynamic shared memory
  * per CTA), resident_drafts (cluster-resident TV kernel: draft slices kept on
- * chip; ops 0, 8-11: chunk slots per warp of the streaming kernel, 0 when the call
- * would use the cluster-resident kernel; else 0).
+ * chip; ops 0 and 8-11: chunk slots per warp of the streaming kernel, 0 when the call
+ * would use the cluster-resident kernel or, op 11, the one-pass Gumbel-max
+ * kernel; else 0).
  * Returns the status the call's planning step would return.
  */
 int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int V, int *cluster_size, int *clusters,

@@ -229,6 +229,42 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
     return found;
 }
 
+// Gumbel-max draft sampling (one pass per row): clusters of C CTAs, one row
+// per cluster at a time.  Same estimate as plan_stream: waves of rows times
+// each row's share (1 / C) plus a fixed term for the cluster barrier and the
+// selection; rows too short for a cluster stay on one CTA.
+bool plan_gsample(int dev, int dtype, int V, int es, int units, Plan &p) {
+    const mtp_tuning tu = tuning();
+    const int forced = tuned_cluster(tu);
+    const void *func = gsample_kernel(dtype);
+    if (prepare_func(dev, func) != cudaSuccess) return false;
+    const int nw = gsample_threads() / 32;
+    const int nv = V / (16 / es);
+    const uint32_t smem = gsample_smem_bytes();
+    double best = 1e30;
+    bool found = false;
+    for (int C = 1; C <= gsample_max_cluster(); ++C) {
+        if (forced && C != forced) continue;
+        if (!forced && C > 1 && (nv + C * nw - 1) / (C * nw) < 64) continue;
+        const int nc = max_clusters(dev, func, C, smem, gsample_threads());
+        if (nc <= 0) continue;
+        int used = nc < units ? nc : units;
+        if (tu.max_clusters > 0 && used > tu.max_clusters) used = tu.max_clusters;
+        const double est = static_cast<double>((units + used - 1) / used) * (1.0 / C + 0.03);
+        if (est < best - 1e-12) {
+            best = est;
+            p = Plan{};
+            p.C = C;
+            p.smem = smem;
+            p.clusters = used;
+            p.threads = gsample_threads();
+            p.func = func;
+            found = true;
+        }
+    }
+    return found;
+}
+
 // Streaming TV kernel: clusters of C CTAs x NT/32 warps, one vocabulary
 // segment per warp, one position per cluster at a time.  Among cluster sizes
 // (powers of two) whose shared memory fits, the one with the most warps in
@@ -734,10 +770,26 @@ extern "C" int mtp_draft_sample(const void *draft_logits, mtp_dtype dtype, const
     if (V % (16 / es) != 0) return MTP_ERR_MISALIGNED;
     int dev;
     if (current_device(dev) != MTP_OK) return MTP_ERR_CUDA;
+    Plan p;
+    // Gumbel-max: one pass per row (no normaliser needed), clusters of at
+    // most 8; a forced larger cluster takes the streaming kernel below
+    if (method == 1 && plan_gsample(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, R, p)) {
+        VerifyArgs A = {};
+        A.target = draft_logits;
+        A.temp = temperature;
+        A.B = R;
+        A.V = V;
+        A.aligned = 1;
+        A.tokens = out_ids;
+        A.flags = row_flags;
+        A.seed_lo = static_cast<uint32_t>(seed);
+        A.seed_hi = static_cast<uint32_t>(seed >> 32);
+        A.offset = offset;
+        return launch(p.func, p, &A, stream);
+    }
     // each row is a one-row sequence of the streaming verify kernel: no draft
     // step, and its final draw (the bonus) samples the row
     const int mode = method == 0 ? 0 : 2;
-    Plan p;
     if (!plan_stream(dev, dtype == MTP_DTYPE_F32 ? 0 : 1, V, es, 0, R, p, mode, true)) return MTP_ERR_NO_DEVICE;
     VerifyArgs A = {};
     A.target = draft_logits;
@@ -933,9 +985,15 @@ extern "C" int mtp_query_plan(int op, mtp_dtype dtype, int units, int gamma, int
     if (op == 3 && !ok && tvs_usable(V, es, gamma)) ok = streamed = plan_tvs(dev, d, V, es, gamma, units, p);
     if (op == 2 && stm_usable(V, es, gamma)) ok = plan_stm(dev, d, V, es, gamma, units, p);
     if (op == 2 && !ok && stats_streamed() && pairs_usable(V, es, gamma)) ok = streamed = plan_pairs(dev, d, V, es, gamma, units, PAIR_STATS, p);
-    if (op == 10 || op == 11) {  // draft sampling (inverse CDF, Gumbel-max): one-row sequences of the streaming kernel
+    if (op == 10) {  // draft sampling by inverse CDF: one-row sequences of the streaming kernel
         if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
-        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, op == 10 ? 0 : 2, true);
+        ok = streamed = plan_stream(dev, d, V, es, 0, units, p, 0, true);
+        if (!ok) return MTP_ERR_NO_DEVICE;
+    }
+    if (op == 11) {  // draft sampling by Gumbel-max: the one-pass kernel, else the streaming kernel
+        if (V % (16 / es) != 0) return MTP_ERR_INVALID_ARG;
+        ok = plan_gsample(dev, d, V, es, units, p);
+        if (!ok) ok = streamed = plan_stream(dev, d, V, es, 0, units, p, 2, true);
         if (!ok) return MTP_ERR_NO_DEVICE;
     }
     if (op == 8 || op == 9) {  // target-only verify, Gumbel-max verify: streaming kernel only

@@ -721,15 +721,19 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
             const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
             // largest W = 1 - U (in units of 2^-24) that can still reach the p
             // bound (the bonus draw; a residual pass keeps every index of the
-            // group: its bound rises late, and the filter would only cost)
+            // group: its bound rises late, and the filter would only cost).
+            // W 2^24 >= 2^24 - 1 - floor(x / 2^8), so an index with W 2^24 <=
+            // wlim has floor(x / 2^8) >= 2^24 - 1 - wlim: the test is one
+            // integer comparison of x against the group's threshold, taken
+            // from 2^24 - 2 - wlim rounded down (at most that plus 1/2, a
+            // larger kept set: the filter stays exact).  2 <= wlim < 2^54
+            // keeps the clamped threshold in [0, 2^24 - 4].
             const float wlim =
                 RESID ? INFINITY : fmaf(ex2(fminf(mx - bpv, 30.f)), 0.69314724f * 16777216.f * 1.000002f, 2.f);
+            const uint32_t xmin = RESID ? 0u : static_cast<uint32_t>(fmaxf(16777214.f - wlim, 0.f)) << 8;
 #pragma unroll
             for (int e4 = 0; e4 < 4; ++e4) {
-                if (!RESID) {
-                    const float w24 = __uint2float_rn((1u << 24) - 1u - (xs[e4] >> 8)) + 0.5f;  // W 2^24
-                    if (!(w24 <= wlim)) continue;  // too little noise to reach the bound
-                }
+                if (!RESID && xs[e4] < xmin) continue;  // too little noise to reach the bound
                 const int e = h * 4 + e4;
                 const float gv = gumbel2(xs[e4]);
                 const float key_p = zk[e4] + gv;
@@ -1008,6 +1012,179 @@ __device__ __noinline__ int2 gumbel_select(const float4 *rec, int S, int lane, b
         if (t2 >= 0) tok = gumbel_retie<Tin>(trow, drow, use_r, tok, t2, j, b, k, ct, cd, seed_lo, seed_hi, offset);
     }
     return make_int2(tok, flags);
+}
+
+// ------------------------------------------ Gumbel-max draft sampling ----
+//
+// mtp_draft_sample with the Gumbel-max method.  Row r's token is arg max_v
+// [z_v k + g_v] (k = log2(e) / T_r; g_v the noise of index v in row 0 of
+// sequence r), which needs no normaliser, so every row is read once, with
+// no ring and no shared-memory staging: a cluster of C CTAs x GS_NW warps
+// cuts the row into warp segments read straight from global memory.  Each
+// warp keys its segment with the exact filters of gumbel_regs (bounded by
+// the warp's best key so far) and also takes the segment's exact maximum
+// with its first index (greedy rows, the all -inf check) and whether it holds
+// a NaN or +inf.  The warps' records are all-gathered through distributed
+// shared memory behind one cluster barrier, and warp 0 of CTA 0 takes the
+// token (gumbel_select: the two best candidates re-keyed in double precision
+// on a near-tie) and writes the outputs.  Persistent clusters take rows cid,
+// cid + NC, ...; the records alternate between two buffers by row, so a
+// row's records are overwritten only after the barrier of the row after it,
+// which CTA 0 passes once it has read them.
+constexpr int GS_NT = 256;
+constexpr int GS_NW = GS_NT / 32;
+constexpr int GS_MAXC = 8;                 // largest cluster
+constexpr int GS_MAXS = GS_MAXC * GS_NW;   // segments per row (gumbel_select: two per lane)
+
+// [row parity][best records (S), runner-up records (S), {max z, its index,
+// NaN or +inf seen, -} (S)], S = C * GS_NW used of each GS_MAXS.
+struct GsShared {
+    float4 rec[2][3 * GS_MAXS];
+};
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t raddr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+// One warp's pass over its segment [seg_lo, seg_lo + seg_n) of row r (vector
+// seg_lo + L + 32 t for lane L, as warp_top2 expects): the p-key arg max and
+// runner-up when sampling, the exact maximum with its first index, and the
+// NaN / +inf test.  Tiles of two vectors per lane; the next tile's loads are
+// in flight while a tile is keyed.
+template <typename Tin>
+__device__ __forceinline__ void gsample_pass(const unsigned char *row, int seg_lo, int seg_n, bool sample, float k,
+                                             uint32_t r, uint32_t seed_lo, uint32_t seed_hi, uint32_t offset,
+                                             float4 &best, float4 &second, float4 &mrec) {
+    constexpr int QV = 2;
+    constexpr int VEC = Store<Tin>::VEC;
+    const int lane = threadIdx.x & 31;
+    const uint4 *g = reinterpret_cast<const uint4 *>(row) + seg_lo;
+    float kr = -INFINITY, kr2 = -INFINITY, kp = -INFINITY, kp2 = -INFINITY, bp = -INFINITY;
+    int ir = -1, ip = -1;
+    float mz = -INFINITY;
+    int mi = -1, bad = 0;
+    uint4 rt[QV], nt[QV];
+    auto load_tile = [&](int base, uint4 (&t)[QV]) {
+#pragma unroll
+        for (int q = 0; q < QV; ++q) {
+            const int jv = base + q * 32 + lane;
+            if (jv < seg_n) t[q] = __ldg(g + jv);
+        }
+    };
+    load_tile(0, rt);
+    for (int base = 0; base < seg_n; base += QV * 32) {
+        if (base + QV * 32 < seg_n) load_tile(base + QV * 32, nt);
+#pragma unroll
+        for (int q = 0; q < QV; ++q) {
+            const int jv = base + q * 32 + lane;
+            if (jv < seg_n) {
+                const float vm = Store<Tin>::vmax(rt[q]);  // NaN if the vector holds one
+                if (!(vm < INFINITY)) {
+                    bad = 1;
+                } else if (vm > mz) {  // first index of the lane's maximum (its vectors ascend)
+                    float z[VEC];
+                    Store<Tin>::unpack(rt[q], z);
+                    int e0 = VEC - 1;
+#pragma unroll
+                    for (int e = VEC - 1; e >= 0; --e)
+                        if (z[e] == vm) e0 = e;
+                    mz = vm;
+                    mi = (seg_lo + jv) * VEC + e0;
+                }
+            }
+        }
+        if (sample) {
+            gumbel_regs<Tin, QV, false>(rt, rt, min(QV * 32, seg_n - base), lane, k, 0.f, 0.f, seg_lo + base + lane,
+                                        seed_lo, seed_hi, 0, r, offset, bp, -INFINITY, kr, ir, kr2, kp, ip, kp2);
+            bp = warp_allmax(kp);  // the warp's best key so far bounds every lane's filters
+        }
+#pragma unroll
+        for (int q = 0; q < QV; ++q) rt[q] = nt[q];
+    }
+    const float4 t2 = sample ? warp_top2<Tin, false>(kp, ip, kp2, row, nullptr, seg_lo, seg_n, 0, r, k, 0.f, 0.f,
+                                                     seed_lo, seed_hi, offset)
+                             : make_float4(-INFINITY, __int_as_float(-1), -INFINITY, __int_as_float(-1));
+    float dummy = 0.f;
+    argmax_allreduce(mz, mi, dummy);
+    bad = warp_allor(bad);
+    best = make_float4(-INFINITY, __int_as_float(-1), t2.x, t2.y);
+    second = make_float4(-INFINITY, __int_as_float(-1), t2.z, t2.w);
+    mrec = make_float4(mz, __int_as_float(mi), __int_as_float(bad), 0.f);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(GS_NT, 4) gsample_kernel_impl(const VerifyArgs A) {
+    constexpr int VEC = Store<Tin>::VEC;
+    extern __shared__ __align__(128) unsigned char smem[];
+    GsShared &sh = *reinterpret_cast<GsShared *>(smem);
+    const int C = static_cast<int>(cluster_size());
+    const int rank = static_cast<int>(cluster_rank());
+    const int cid = static_cast<int>(cluster_id_x());
+    const int NC = static_cast<int>(gridDim.x) / C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = C * GS_NW, sg = rank * GS_NW + warp;
+    const int nv = A.V / VEC;
+    const int nvs = (nv + S - 1) / S;
+    const int seg_lo = min(nv, sg * nvs), seg_n = min(nv, seg_lo + nvs) - seg_lo;
+    int par = 0;
+    for (int r = cid; r < A.B; r += NC) {
+        const float T = __ldg(A.temp + r);
+        const bool bad_t = !(T >= 0.f) || !(T < INFINITY);
+        const bool sample = !bad_t && T != 0.f;
+        const float k = sample ? LOG2E / T : 0.f;
+        const unsigned char *row =
+            reinterpret_cast<const unsigned char *>(A.target) + static_cast<size_t>(r) * A.V * Store<Tin>::ES;
+        float4 best = make_float4(-INFINITY, __int_as_float(-1), -INFINITY, __int_as_float(-1)), second = best;
+        float4 mrec = make_float4(-INFINITY, __int_as_float(-1), __int_as_float(0), 0.f);
+        if (!bad_t)
+            gsample_pass<Tin>(row, seg_lo, seg_n, sample, k, static_cast<uint32_t>(r), A.seed_lo, A.seed_hi,
+                              A.offset, best, second, mrec);
+        // lane q < C stores this warp's three records into CTA q
+        if (lane < C) {
+            float4 *base = sh.rec[par];
+            st_cluster_v4(map_rank(smem_addr(base + sg), lane), best);
+            st_cluster_v4(map_rank(smem_addr(base + S + sg), lane), second);
+            st_cluster_v4(map_rank(smem_addr(base + 2 * S + sg), lane), mrec);
+        }
+        cluster_sync();  // every record of the row is in every CTA
+        if (rank == 0 && warp == 0) {
+            const float4 *rec = sh.rec[par];
+            float mz = -INFINITY, dummy = 0.f;
+            int mi = -1, bad = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = 2 * lane + h;
+                if (q < S) {
+                    const float4 v = rec[2 * S + q];
+                    argmax_merge(mz, mi, dummy, v.x, __float_as_int(v.y), 0.f);
+                    bad |= __float_as_int(v.z);
+                }
+            }
+            argmax_allreduce(mz, mi, dummy);
+            bad = warp_allor(bad);
+            int flags = 0, tok = -1;
+            if (bad_t) {
+                flags |= F_BAD_TEMP;
+            } else if (bad || mi < 0) {
+                flags |= F_NONFINITE;  // a NaN or +inf logit, or nothing but -inf
+            } else if (!sample) {
+                tok = mi;  // greedy: the arg max, ties to the smallest index
+            } else {
+                const int2 sel = gumbel_select<Tin>(rec, S, lane, false, row, nullptr, 0, static_cast<uint32_t>(r), k,
+                                                    mz * k, 0.f, A.seed_lo, A.seed_hi, A.offset);
+                tok = sel.x;
+                flags |= sel.y;
+                if (tok < 0) flags |= F_NONFINITE;
+            }
+            if (lane == 0) {
+                A.tokens[r] = flags ? -1 : tok;
+                if (A.flags) A.flags[r] = flags;
+            }
+        }
+        par ^= 1;
+    }
 }
 
 template <typename Tin, int CV, int MODE, bool DBL>
@@ -1581,6 +1758,14 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
 }
 
 }  // namespace
+
+const void *gsample_kernel(int dtype) {
+    return dtype == 0 ? reinterpret_cast<const void *>(&gsample_kernel_impl<float>)
+                      : reinterpret_cast<const void *>(&gsample_kernel_impl<bf16_t>);
+}
+int gsample_threads() { return GS_NT; }
+int gsample_max_cluster() { return GS_MAXC; }
+uint32_t gsample_smem_bytes() { return static_cast<uint32_t>(sizeof(GsShared)); }
 
 uint32_t stream_hdr_bytes() { return HDR_BYTES; }
 uint32_t stream_rec_bytes(int gamma, int S) { return rec_bytes(gamma, S); }

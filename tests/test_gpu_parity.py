@@ -166,12 +166,15 @@ def test_verify_plan_kernels():
 
 def test_draft_sample_plans():
     """Both draft-sampling plans count rows as units: at most one cluster per
-    row, streaming-kernel ring slots, and the Gumbel-max plan is its own."""
+    row.  Inverse CDF runs on the streaming kernel (ring slots per warp); the
+    Gumbel-max plan is the one-pass kernel's (no ring, clusters of at most 8)."""
     import mtp_speculative_decoding_row_gb300 as mtp
     for op in ("draft_sample", "draft_sample_gumbel"):
         p = mtp.mtp_query_plan(op, "bf16", 192, 3, 151936)
         assert 1 <= p["clusters"] <= 192 and p["cluster_size"] >= 1 and p["smem_bytes"] > 0, (op, p)
-        assert p["resident_drafts"] >= 2, (op, p)
+    assert mtp.mtp_query_plan("draft_sample", "bf16", 192, 3, 151936)["resident_drafts"] >= 2
+    g = mtp.mtp_query_plan("draft_sample_gumbel", "bf16", 192, 3, 151936)
+    assert g["resident_drafts"] == 0 and g["cluster_size"] <= 8, g
     small = mtp.mtp_query_plan("draft_sample_gumbel", "bf16", 3, 3, 151936)
     assert small["clusters"] <= 3
 
