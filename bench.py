@@ -49,7 +49,7 @@ L2_BYTES = 129 * 1024 * 1024
 
 # Source files of each kernel family (the kernel and the headers it uses).
 KERNEL_FILES = {
-    "stream": ["stream_kernels.cu", "chunk_math.cuh", "common.cuh", "philox.cuh", "kernels.h"],
+    "stream": ["stream_kernels.cu", "chunk_math.cuh", "common.cuh", "philox.cuh", "kernels.h", "gsample.h"],
     "tv_tmem": ["tv_tmem_kernels.cu", "chunk_math.cuh", "common.cuh", "tmem.cuh", "kernels.h"],
     "row": ["row_kernels.cu", "common.cuh", "kernels.h"],
     "pair": ["pair_stream_kernels.cu", "chunk_math.cuh", "common.cuh", "kernels.h"],

@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "gsample.h"
 #include "mtp_rs.h"
 
 namespace {

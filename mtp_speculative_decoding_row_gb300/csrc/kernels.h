@@ -85,11 +85,6 @@ int row_threads();
 int tv_threads();
 
 // Streaming verify kernel geometry.
-// Gumbel-max draft sampling: one pass per row, no ring (stream_kernels.cu).
-const void *gsample_kernel(int dtype);
-int gsample_threads();
-int gsample_max_cluster();
-uint32_t gsample_smem_bytes();
 uint32_t stream_hdr_bytes();
 uint32_t stream_rec_bytes(int gamma, int S);
 int stream_max_gamma();

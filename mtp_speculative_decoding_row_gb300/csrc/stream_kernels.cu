@@ -48,6 +48,7 @@
 #include "common.cuh"
 #include "philox.cuh"
 #include "kernels.h"
+#include "gsample.h"
 
 namespace mtp {
 namespace {

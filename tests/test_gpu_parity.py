@@ -529,6 +529,22 @@ def test_draft_sample(V, dtype, C, method):
     assert len(np.unique(ids)) > len(ids) // 4  # rows differ: the draws are not all one token
 
 
+@pytest.mark.parametrize("C,clusters", [(1, 7), (2, 5), (8, 3), (None, None)])
+def test_draft_sample_gumbel_rows_per_cluster(C, clusters):
+    """The one-pass Gumbel-max kernel with several rows per persistent
+    cluster (its records alternate between two buffers by row), across
+    cluster sizes 1-8, with greedy rows, a NaN row and a bad temperature in
+    between: draws and flags against the oracle."""
+    z, T, u = _draft_rows(3000, "bf16", 3, 777, B=30)
+    z = z.copy()
+    z[17, 123] = 0x7FC0  # NaN (bf16 bits)
+    T[40] = -1.0
+    with tune(cluster_size=C, max_clusters=clusters):
+        ids, o = _check_draft(z, T, u, "gumbel", 5, 2, "bf16", f"gumbel rows per cluster C={C} clusters={clusters}")
+    assert o["flags"][17] != 0 and o["flags"][40] != 0
+    assert np.count_nonzero(ids >= 0) >= len(ids) - 2
+
+
 def _near_tie_rows(R, V, seed, offset, lo=1.5e-5, hi=5e-4, row=0):
     """Rows whose two largest logits are equal (5.0, exact in bf16 too), at
     the two indices whose Gumbel noise (the draws' counter-based noise of
