@@ -30,6 +30,7 @@ struct Plan {
     int cv = 0;        // streaming kernel: vectors of each row per chunk
     const void *func = nullptr;
     int seg_vectors = 0;
+    bool pdl = false;  // the kernel waits for earlier launches itself (griddepcontrol): launch it programmatically
 };
 
 struct CacheEntry {
@@ -224,6 +225,7 @@ bool plan_stream(int dev, int dtype, int V, int es, int gamma, int units, Plan &
             p.seg_vectors = nvs;
             p.cv = cv;
             p.func = func;
+            p.pdl = true;
             found = true;
         }
     }
@@ -501,13 +503,18 @@ int launch(const void *func, const Plan &p, void *args, mtp_stream_t stream) {
     cfg.blockDim = dim3(p.threads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic stream serialization: the kernel may start while the
+    // previous launch on the stream finishes; it waits for it in-kernel
+    // (griddepcontrol.wait) before touching global memory
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     void *kargs[] = {args};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, func, kargs);
     return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;

@@ -1015,6 +1015,19 @@ __device__ __noinline__ int2 gumbel_select(const float4 *rec, int S, int lane, b
     return make_int2(tok, flags);
 }
 
+// Programmatic dependent launch.  The streaming kernel is launched with
+// programmatic stream serialization: the next launch on the stream may start
+// once every CTA of the running one has signalled (each signals as it
+// starts), so its CTAs take SMs as the running grid's CTAs retire and set up
+// their shared memory meanwhile.  Before its first global-memory access the
+// kernel waits until every prerequisite grid has completed and its writes
+// are visible, so the results are those of plain stream order.  (The
+// one-pass Gumbel-max kernel below is launched plainly: it is bound by
+// arithmetic in a single wave, and CTAs of the next launch placed early on
+// whichever SMs free up first made it slower.)
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------ Gumbel-max draft sampling ----
 //
 // mtp_draft_sample with the Gumbel-max method.  Row r's token is arg max_v
@@ -1197,6 +1210,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
     constexpr uint32_t SLOT_BYTES = 2u * CV * 16u;
     extern __shared__ __align__(128) unsigned char smem[];
     StreamShared &sh = *reinterpret_cast<StreamShared *>(smem);
+    pdl_allow_next();
 
     Ctx c;
     c.C = static_cast<int>(cluster_size());
@@ -1247,6 +1261,7 @@ __global__ void __launch_bounds__(NT, 4) stream_kernel_impl(const VerifyArgs A) 
     fence_mbar_init();
     __syncthreads();
     cluster_sync();  // every barrier of the cluster is initialised and armed before any push
+    pdl_wait_prior();  // inputs and outputs of earlier launches on the stream: settled from here on
 
     // sequence parameters, prefetched one sequence ahead (lane l: u_l, y_l)
     auto load_params = [&](int b, float &u, int &y, float &T) {
