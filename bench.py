@@ -62,15 +62,15 @@ KERNEL_FILES = {
 # Captures on a reduced case are scaled to the workload by the units
 # processed (traffic grows in proportion; profiles/ says which).
 TRAFFIC = {
-    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,213,632 read + 3,808,256 written
+    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,165,504 read + 3,677,184 written
     # (profiles/stream_kernel_rl512.md)
-    "rl512": {"bytes": 1070021888, "family": "stream", "csrc": "114514afd3423d2e"},
-    # stream_kernel_impl<bf16_t,128,2> (Gumbel-max verify) in full: 132,515,328 + 5,972,224 bytes
+    "rl512": {"bytes": 1069842688, "family": "stream", "csrc": "8558c7635531528d"},
+    # stream_kernel_impl<bf16_t,128,2> (Gumbel-max verify) in full: 132,717,056 + 6,317,056 bytes
     # (profiles/stream_kernel_gumbel64.md)
-    "gumbel64": {"bytes": 138487552, "family": "stream", "csrc": "114514afd3423d2e"},
-    # gsample_kernel_impl<bf16_t> (Gumbel-max draft sampling, one pass) in full: 63,137,536 +
-    # 525,568 bytes (profiles/gsample_kernel_gsample192.md)
-    "gsample192": {"bytes": 63663104, "family": "stream", "csrc": "114514afd3423d2e"},
+    "gumbel64": {"bytes": 139034112, "family": "stream", "csrc": "8558c7635531528d"},
+    # gsample_kernel_impl<bf16_t> (Gumbel-max draft sampling, one pass) in full: 63,136,512 +
+    # 488,192 bytes (profiles/gsample_kernel_gsample192.md)
+    "gsample192": {"bytes": 63624704, "family": "stream", "csrc": "8558c7635531528d"},
     # tvm_kernel_impl<bf16_t,10> at N = 512 (1,123,948,800 read + 872,851,968 written) x 32
     # for N = 16,384 (profiles/tv_tmem_kernel_tvloss_n512.md)
     "tvloss": {"bytes": 63897624576, "family": "tv_tmem", "csrc": "04c6799a1030e40f"},
