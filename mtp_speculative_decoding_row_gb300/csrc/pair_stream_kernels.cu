@@ -410,7 +410,7 @@ __device__ __forceinline__ bool norm_ok(const SoftX &a) {
 }
 
 template <typename Tin, int CV, int MODE>
-__global__ void __launch_bounds__(NT, MODE == PAIR_DIAG ? 3 : 4) pair_kernel_impl(const PairArgs A) {
+__global__ void __launch_bounds__(NT, 4) pair_kernel_impl(const PairArgs A) {
     using St = Store<Tin>;
     constexpr int QV = CV / 32;
     static_assert(CV % 32 == 0, "chunk layout: whole vectors per lane");
