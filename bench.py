@@ -62,15 +62,15 @@ KERNEL_FILES = {
 # Captures on a reduced case are scaled to the workload by the units
 # processed (traffic grows in proportion; profiles/ says which).
 TRAFFIC = {
-    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,165,504 read + 3,677,184 written
+    # stream_kernel_impl<bf16_t,160,0>, rl512 in full: 1,066,138,368 read + 3,778,560 written
     # (profiles/stream_kernel_rl512.md)
-    "rl512": {"bytes": 1069842688, "family": "stream", "csrc": "8558c7635531528d"},
-    # stream_kernel_impl<bf16_t,128,2> (Gumbel-max verify) in full: 132,717,056 + 6,317,056 bytes
+    "rl512": {"bytes": 1069916928, "family": "stream", "csrc": "5e20b20ae3cf8a29"},
+    # stream_kernel_impl<bf16_t,128,2> (Gumbel-max verify) in full: 132,694,016 + 6,277,376 bytes
     # (profiles/stream_kernel_gumbel64.md)
-    "gumbel64": {"bytes": 139034112, "family": "stream", "csrc": "8558c7635531528d"},
-    # gsample_kernel_impl<bf16_t> (Gumbel-max draft sampling, one pass) in full: 63,136,512 +
-    # 488,192 bytes (profiles/gsample_kernel_gsample192.md)
-    "gsample192": {"bytes": 63624704, "family": "stream", "csrc": "8558c7635531528d"},
+    "gumbel64": {"bytes": 138971392, "family": "stream", "csrc": "5e20b20ae3cf8a29"},
+    # gsample_kernel_impl<bf16_t> (Gumbel-max draft sampling, one pass) in full: 63,138,816 +
+    # 500,480 bytes (profiles/gsample_kernel_gsample192.md)
+    "gsample192": {"bytes": 63639296, "family": "stream", "csrc": "5e20b20ae3cf8a29"},
     # tvm_kernel_impl<bf16_t,10> at N = 512 (1,123,948,800 read + 872,851,968 written) x 32
     # for N = 16,384 (profiles/tv_tmem_kernel_tvloss_n512.md)
     "tvloss": {"bytes": 63897624576, "family": "tv_tmem", "csrc": "04c6799a1030e40f"},
@@ -78,10 +78,10 @@ TRAFFIC = {
     # written) x 32 for N = 16,384, the same launch plan (profiles/tv_stream_kernel_tvtopk_n512.md)
     "tvtopk": {"bytes": 50086510592, "family": "tv_stream", "csrc": "f7118740f92f9310"},
     # row_kernel_impl<float,2> (statistics) and <float,1> (verify with statistics) on the first 64
-    # sequences of deep256 (583,617,024 + 4,086,272 and 583,896,832 + 4,410,368 bytes) x 4 for
+    # sequences of deep256 (583,515,392 + 3,678,976 and 583,566,080 + 3,705,088 bytes) x 4 for
     # B = 256 (profiles/row_kernel_deep256_b64.md)
-    "stats256": {"bytes": 2350813184, "family": "row", "csrc": "0dda1edb6e04823d"},
-    "deep256": {"bytes": 2353228800, "family": "row", "csrc": "0dda1edb6e04823d"},
+    "stats256": {"bytes": 2348777472, "family": "row", "csrc": "903c4eee388664e8"},
+    "deep256": {"bytes": 2349084672, "family": "row", "csrc": "903c4eee388664e8"},
 }
 
 

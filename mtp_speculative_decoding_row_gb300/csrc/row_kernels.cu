@@ -177,6 +177,56 @@ __device__ __forceinline__ float gather_sum(const Xchg &x, int slot, int C) {
     return warp_allsum(lane < C ? x.rec[slot][lane][0] : 0.f);
 }
 
+// Draft partial of the statistics modes: the sum pass of thread_soft_exact
+// (same loop, same accumulation order) against the reference m, the target's
+// exact maximum over the same vectors, instead of a maximum of the draft's
+// own.  Where the draft row equals the target row away from elements whose
+// weight underflows, the two partials, and so the cluster's normalisers, come
+// out bit for bit the same; a rejection's residual max(0, p - q) is then
+// exactly zero there, as it is in exact arithmetic (up to the underflowing
+// terms), and the draw falls back to p with the row flagged ZERO_MASS,
+// instead of drawing from rounding noise.  Falls back to thread_soft_exact
+// when m is not finite or the sum leaves the safe range (a NaN or +inf logit
+// included, which that path flags).
+template <typename Tin, int NT>
+__device__ __forceinline__ Soft draft_soft_at(const unsigned char *buf, int nvec, float k, float m, bool &bad) {
+    if (m > -INFINITY && m < INFINITY) {
+        const float mk = m * k;
+        const uint64_t K2 = f2pack(k, k), NMK2 = f2pack(-mk, -mk);
+        uint64_t acc = f2pack(0.f, 0.f);
+        for (int j = threadIdx.x; j < nvec; j += NT) {
+            const uint4 r = vec_at(buf, j);
+            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+            if (Store<Tin>::ES == 2) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float d0, d1;
+                    f2unpack(f2fma(bf16pair_f2(w[q]), K2, NMK2), d0, d1);
+                    acc = f2add(acc, f2pack(ex2(d0), ex2(d1)));
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float d0, d1;
+                    f2unpack(f2fma(f2pack(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), K2, NMK2), d0, d1);
+                    acc = f2add(acc, f2pack(ex2(d0), ex2(d1)));
+                }
+            }
+        }
+        float s0, s1;
+        f2unpack(acc, s0, s1);
+        const float sum = s0 + s1;
+        if (sum < 1.8e19f) {  // finite, no NaN, far from overflow after merging
+            Soft a;
+            a.m = m;
+            a.s = sum;
+            a.s1 = 0.f;
+            return a;
+        }
+    }
+    return thread_soft_exact<Tin, false, NT>(buf, nvec, k, bad);
+}
+
 // ------------------------------------------------------------- sampling ----
 
 // Sampling weights of one image vector: WMODE 0 = residual max(0, p - q),
@@ -597,7 +647,9 @@ __global__ void __launch_bounds__(NT, 2) row_kernel_impl(const VerifyArgs A) {
                     st.ph ^= 1u;
                     st.armed = 0;
                 }
-                Soft ad = has_d ? thread_soft<Tin, false, NT>(db, s.nvec, k, nonfin) : soft_empty();
+                Soft ad = !has_d ? soft_empty()
+                          : STATS ? draft_soft_at<Tin, NT>(db, s.nvec, k, at.m, nonfin)
+                                  : thread_soft<Tin, false, NT>(db, s.nvec, k, nonfin);
                 const bool want_y = DECIDE && has_d && !st.stopped;
                 const int y = want_y ? sh.ids[si][i] : -1;
                 int bad = (nonfin ? F_NONFINITE : 0) | (tmo ? F_TIMEOUT : 0);

@@ -744,7 +744,8 @@ __device__ __forceinline__ void gumbel_regs(const uint4 (&rt)[QV], const uint4 (
                     ip = vv * VEC + e;
                 }
                 if (RESID && want_r) {
-                    const float w = ex2(zk[e4] - ct) - ex2(fmaf(zd[e], k, -cd));
+                    // both terms in the same form, so equal logits give exactly 0
+                    const float w = ex2(fmaf(zt[e], k, -ct)) - ex2(fmaf(zd[e], k, -cd));
                     if (w > 0.f) {
                         const float key_r = __log2f(w) + gv;
                         kr2 = fmaxf(kr2, fminf(key_r, kr));
@@ -823,7 +824,7 @@ __device__ __noinline__ float4 warp_top2(float k1, int i1, float k2, const unsig
                     const float zk = zt[e] * k, gv = gumbel2(xs[e4]);
                     float key = zk + gv;
                     if (RKEY) {
-                        const float w = ex2(zk - ct) - ex2(fmaf(zd[e], k, -cd));
+                        const float w = ex2(fmaf(zt[e], k, -ct)) - ex2(fmaf(zd[e], k, -cd));
                         key = w > 0.f ? __log2f(w) + gv : -INFINITY;
                     }
                     if (idx != I1 && key > -INFINITY && (key > bk || (key == bk && idx < bi))) {

@@ -202,6 +202,47 @@ def test_verify_equal_rows_accept_all():
     np.testing.assert_allclose(g["alpha"], 1.0, atol=2e-6)
 
 
+def _zero_mass_inputs(B=8, V=1024):
+    """Verify inputs (gamma = 1, fp32) whose every sequence rejects its draft
+    token y with a residual max(0, p - q) that is exactly zero: the draft row
+    equals the target row except at y, where the logits are -300 (target) and
+    -299 (draft).  At T = 1 that index's weight underflows next to the others
+    in single and in double precision, so both normalisers, and with them p
+    and q away from y, agree bit for bit; at y itself q > p, and u = 0.9
+    rejects (u q(y) >= p(y)).  The rounding case the pages' two-pass CDF
+    leaves open: the draw falls back to p and the row is flagged ZERO_MASS."""
+    rng = np.random.default_rng(4321)
+    g = 1
+    t = (rng.standard_normal((B, g + 1, V)) * 2.0).astype(np.float32)
+    y = rng.integers(0, V, size=(B, g)).astype(np.int32)
+    d = t[:, :g].copy()
+    for b in range(B):
+        t[b, 0, y[b, 0]] = -300.0
+        d[b, 0, y[b, 0]] = -299.0
+    u = np.full((B, g + 1), 0.9, np.float32)
+    u[:, g] = rng.random(B).astype(np.float32)
+    return W.VerifyInputs("zeromass", B, g, V, "f32", t, d, y, np.ones(B, np.float32), u)
+
+
+@pytest.mark.parametrize("kernel", ["stream", "resident", "stats", "gumbel"])
+def test_zero_mass_residual_fallback(kernel):
+    """A rejection whose residual mass is exactly zero (see
+    _zero_mass_inputs): every kernel path that takes the residual draw (the
+    streaming and the cluster-resident verify, verify with statistics, the
+    Gumbel-max draw) rejects, flags MTP_ROW_ZERO_MASS, draws from p instead,
+    and matches the oracle, which takes the same fallback."""
+    import mtp_speculative_decoding_row_gb300 as mtp
+    x = _zero_mass_inputs()
+    if kernel == "gumbel":
+        _, g, o = _check_gumbel(x, 77, 3, "zero-mass gumbel")
+    else:
+        with tune(verify_kernel=kcode("resident") if kernel == "resident" else 0):
+            _, g, o = _check_verify(x, with_stats=kernel == "stats", what=f"zero-mass {kernel}")
+    assert np.all(o["flags"] == mtp.ROW_ZERO_MASS) and np.all(g["row_flags"] == mtp.ROW_ZERO_MASS)
+    assert np.all(g["accept_len"] == 0)
+    assert np.all((g["tokens"][:, 0] >= 0) & (g["tokens"][:, 0] != x.draft_ids[:, 0]))
+
+
 def test_verify_deterministic():
     x = W.verify_inputs("det", 32, 3, 30000, "bf16", 8, family="sigma", sigmas=np.linspace(1, 6, 32), delta=0.4)
     a = run_verify(x, True)
